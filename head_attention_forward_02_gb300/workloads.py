@@ -1,0 +1,144 @@
+"""Seeded synthetic inputs for the attention forward pass.
+
+This module only draws and packs random numbers; it holds none of the
+attention arithmetic.  Both the CUDA path and the CPU oracle take their inputs
+from here, so that they see the same stored values.
+
+Every tensor is drawn on the CPU from ``torch.Generator().manual_seed(seed)``
+as N(0, 1) in float32 and then cast to the storage type (fp8 e4m3 inputs are
+clamped to +-448 first, the largest finite e4m3 value).  Variable-length
+workloads are packed back to back after one leading padding batch of
+``max_len`` rows, the layout the CUTLASS Blackwell FMHA walkthrough asks for
+(§变长序列: "valid but never used" padding ahead of the first batch).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+from typing import List, Optional
+
+import torch
+
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
+# codes shared with the C ABI (include/fmha.h) -- plain enum values, no arithmetic
+DTYPE_CODE = {"f16": 0, "bf16": 1, "e4m3": 2}
+MASK_CODE = {"none": 0, "residual": 1, "causal": 2}
+CAUSAL_CODE = {"qbegin": 0, "qend": 1}
+E4M3_MAX = 448.0
+
+
+@dataclass
+class Workload:
+    name: str
+    dtype: str = "bf16"
+    B: int = 1
+    H: int = 1
+    H_k: int = 1
+    Sq: int = 128
+    Sk: int = 128
+    D: int = 128
+    mask: str = "none"
+    causal_type: str = "qbegin"
+    scale: Optional[float] = None          # None -> 1/sqrt(D)
+    out_scale: float = 1.0
+    seqlens_q: Optional[List[int]] = None  # varlen when both are given
+    seqlens_k: Optional[List[int]] = None
+    seed: int = 0
+    # varlen: draw this many lengths uniform in [lo, hi] (inclusive) from the seed
+    varlen_draw: Optional[tuple] = None
+
+    @property
+    def varlen(self) -> bool:
+        return self.seqlens_q is not None or self.varlen_draw is not None
+
+    @property
+    def softmax_scale(self) -> float:
+        return self.scale if self.scale is not None else 1.0 / math.sqrt(self.D)
+
+
+@dataclass
+class Inputs:
+    """Host tensors for one call.  For varlen the real data of each packed tensor
+    starts after ``pad_rows`` padding rows: ``q_full[pad_rows:]`` is what the
+    kernel sees."""
+    w: Workload
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    q_full: Optional[torch.Tensor] = None
+    k_full: Optional[torch.Tensor] = None
+    v_full: Optional[torch.Tensor] = None
+    cu_seqlens_q: Optional[torch.Tensor] = None
+    cu_seqlens_k: Optional[torch.Tensor] = None
+    seqlens_q: Optional[List[int]] = None
+    seqlens_k: Optional[List[int]] = None
+    total_length: int = 0
+    max_len: int = 0
+    pad_rows: int = 0
+
+
+def _randn(shape, gen, dtype: str) -> torch.Tensor:
+    x = torch.randn(shape, generator=gen, dtype=torch.float32)
+    if dtype == "e4m3":
+        x = x.clamp_(-E4M3_MAX, E4M3_MAX)
+    return x.to(DTYPES[dtype])
+
+
+def _cumsum(lens: List[int]) -> torch.Tensor:
+    out = [0]
+    for n in lens:
+        out.append(out[-1] + int(n))
+    return torch.tensor(out, dtype=torch.int32)
+
+
+def generate(w: Workload, seed: Optional[int] = None) -> Inputs:
+    gen = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    if not w.varlen:
+        q = _randn((w.B, w.Sq, w.H, w.D), gen, w.dtype)
+        k = _randn((w.B, w.Sk, w.H_k, w.D), gen, w.dtype)
+        v = _randn((w.B, w.Sk, w.H_k, w.D), gen, w.dtype)
+        return Inputs(w, q, k, v)
+    if w.varlen_draw is not None:
+        n, lo, hi = w.varlen_draw
+        lens = torch.randint(lo, hi + 1, (n,), generator=gen).tolist()
+        lq, lk = list(lens), list(lens)
+    else:
+        lq, lk = list(w.seqlens_q), list(w.seqlens_k)
+    assert len(lq) == len(lk)
+    cq, ck = _cumsum(lq), _cumsum(lk)
+    total = max(int(cq[-1]), int(ck[-1]), 1)
+    max_len = max([1] + lq + lk)
+    pad = max_len
+    q_full = _randn((pad + total, w.H, w.D), gen, w.dtype)
+    k_full = _randn((pad + total, w.H_k, w.D), gen, w.dtype)
+    v_full = _randn((pad + total, w.H_k, w.D), gen, w.dtype)
+    return Inputs(w, q_full[pad:], k_full[pad:], v_full[pad:], q_full, k_full, v_full,
+                  cq, ck, lq, lk, total, max_len, pad)
+
+
+def bits(t: torch.Tensor):
+    """Raw storage bits of a tensor as a numpy array (uint16, or uint8 for fp8)."""
+    t = t.contiguous()
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).numpy()
+    return t.view(torch.int16).numpy().view("uint16")
+
+
+# The five workloads the benchmark and the parity tests are built around.
+CONFIGS = {
+    "fp16_b1_h2_s128_d64_nomask": Workload(
+        "fp16_b1_h2_s128_d64_nomask", dtype="f16", B=1, H=2, H_k=2, Sq=128, Sk=128, D=64,
+        mask="none", seed=1),
+    "bf16_causal_b4_h16_s2048_d128": Workload(
+        "bf16_causal_b4_h16_s2048_d128", dtype="bf16", B=4, H=16, H_k=16, Sq=2048, Sk=2048,
+        D=128, mask="causal", causal_type="qbegin", seed=2),
+    "bf16_causal_gqa_b2_h32_hk8_s8192_d128": Workload(
+        "bf16_causal_gqa_b2_h32_hk8_s8192_d128", dtype="bf16", B=2, H=32, H_k=8, Sq=8192,
+        Sk=8192, D=128, mask="causal", causal_type="qbegin", seed=3),
+    "bf16_varlen_causal_8x_u256_4096_h16_d128": Workload(
+        "bf16_varlen_causal_8x_u256_4096_h16_d128", dtype="bf16", B=8, H=16, H_k=16, D=128,
+        mask="causal", causal_type="qbegin", varlen_draw=(8, 256, 4096), seed=4),
+    "e4m3_nomask_b1_h16_s16384_d128": Workload(
+        "e4m3_nomask_b1_h16_s16384_d128", dtype="e4m3", B=1, H=16, H_k=16, Sq=16384,
+        Sk=16384, D=128, mask="none", out_scale=1.0, seed=5),
+}

@@ -1,0 +1,324 @@
+/*
+ * fmha_oracle.c -- CPU oracle for the fused multi-head attention forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link,
+ * load or call this file: only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline / reference arm use it.  It shares no code, header
+ * or table with the CUDA library; it reads the raw bits of the stored inputs
+ * and decodes them with its own decoders.
+ *
+ * What it computes is the plain definition, written out in double precision:
+ *
+ *   for every batch b (or packed sequence b), query head h, key/value head
+ *   g = floor(h / (H / H_k)), and query row i of that sequence:
+ *     s_j   = scale * sum_d Q[b,i,h,d] * K[b,j,g,d]          for allowed keys j
+ *     m     = max_j s_j
+ *     l     = sum_j exp(s_j - m)
+ *     O_d   = out_scale * sum_j exp(s_j - m) * V[b,j,g,d] / l
+ *     LSE   = m + ln(l)
+ *
+ * Sources (page title, section):
+ *  - "fmha sm120 : 超越 torch.sdpa(flash-attention-2)", §1 flash attention:
+ *    MHA = softmax(q @ k^T * scale) @ v, layout [batch, seq, heads, head_dim],
+ *    O has Q's shape; §2 fmha 实现: GQA maps query head h to kv head
+ *    h / (q_heads / kv_heads).
+ *  - "CUTLASS Blackwell FMHA 示例完全解析", §融合扩展点 (fmha_fusion.hpp):
+ *    masked scores become -infinity before the softmax; causal q-begin keeps
+ *    key <= query, causal q-end shifts the diagonal by seqlen_k - seqlen_q;
+ *    the residual mask only removes keys at or beyond seqlen_k.
+ *  - same page, §变长序列 (Variable Sequence Length): packed sequences are
+ *    addressed through cumulative lengths; sequence b owns rows
+ *    [cum[b], cum[b+1]).
+ *  - same page, §验证机制: both O and the log-sum-exp (LSE) are checked.
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *  - a row with no allowed key (causal q-end with seqlen_q > seqlen_k, or a
+ *    zero-length key sequence) yields O = 0 and LSE = -infinity;
+ *  - LSE is the natural-log log-sum-exp of the scaled scores; out_scale does
+ *    not enter it;
+ *  - mask NONE and mask RESIDUAL define the same result.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { OR_F16 = 0, OR_BF16 = 1, OR_E4M3 = 2 };
+enum { OR_MASK_NONE = 0, OR_MASK_RESIDUAL = 1, OR_MASK_CAUSAL = 2 };
+enum { OR_QBEGIN = 0, OR_QEND = 1 };
+
+/* ------------------------------------------------------------------------- */
+/* Bit decoders.  Each storage format is sign | exponent | mantissa.          */
+/* ------------------------------------------------------------------------- */
+
+/* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 mantissa bits. */
+static double decode_f16(uint32_t bits) {
+    int s = (bits >> 15) & 1, e = (bits >> 10) & 31, m = bits & 1023;
+    double mag;
+    if (e == 0)       mag = ldexp((double)m, -24);                 /* subnormal */
+    else if (e == 31) mag = m ? NAN : INFINITY;
+    else              mag = ldexp(1024.0 + m, e - 25);
+    return s ? -mag : mag;
+}
+
+/* bfloat16: 1 sign, 8 exponent (bias 127), 7 mantissa bits. */
+static double decode_bf16(uint32_t bits) {
+    int s = (bits >> 15) & 1, e = (bits >> 7) & 255, m = bits & 127;
+    double mag;
+    if (e == 0)        mag = ldexp((double)m, -133);               /* 2^-126 * m/128 */
+    else if (e == 255) mag = m ? NAN : INFINITY;
+    else               mag = ldexp(128.0 + m, e - 134);
+    return s ? -mag : mag;
+}
+
+/* OCP fp8 E4M3 ("fn" variant): 1 sign, 4 exponent (bias 7), 3 mantissa bits;
+ * no infinities, exponent 15 with mantissa 7 is NaN, largest finite 448. */
+static double decode_e4m3(uint32_t bits) {
+    int s = (bits >> 7) & 1, e = (bits >> 3) & 15, m = bits & 7;
+    double mag;
+    if (e == 0)                 mag = ldexp((double)m, -9);        /* 2^-6 * m/8 */
+    else if (e == 15 && m == 7) mag = NAN;
+    else                        mag = ldexp(8.0 + m, e - 10);
+    return s ? -mag : mag;
+}
+
+double oracle_decode(int dtype, uint32_t bits) {
+    switch (dtype) {
+    case OR_F16:  return decode_f16(bits & 0xFFFF);
+    case OR_BF16: return decode_bf16(bits & 0xFFFF);
+    case OR_E4M3: return decode_e4m3(bits & 0xFF);
+    default:      return NAN;
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Round-to-nearest-even encoders (used to report O rounded to the output     */
+/* type).  e4m3 saturates to +-448 (satfinite); fp16/bf16 overflow to inf.    */
+/* ------------------------------------------------------------------------- */
+
+typedef struct { int ebits, mbits, bias, has_inf; double maxfinite; } fmt_t;
+
+static const fmt_t FMT_F16  = {5, 10, 15, 1, 65504.0};
+static const fmt_t FMT_BF16 = {8, 7, 127, 1, 3.3895313892515355e38};
+static const fmt_t FMT_E4M3 = {4, 3, 7, 0, 448.0};
+
+/* Round |x| to the format's grid, ties to even.  Returns the rounded magnitude. */
+static double round_to_grid(double a, const fmt_t *f) {
+    int e2;
+    if (a == 0.0) return 0.0;
+    frexp(a, &e2);                       /* a = frac * 2^e2, frac in [0.5, 1) */
+    int E = e2 - 1;                      /* a in [2^E, 2^(E+1)) */
+    int emin = 1 - f->bias;              /* smallest normal exponent */
+    if (E < emin) E = emin;              /* subnormals share the smallest quantum */
+    double quantum = ldexp(1.0, E - f->mbits);
+    double q = a / quantum;              /* exact: power-of-two scaling */
+    double n = floor(q);
+    double rem = q - n;
+    if (rem > 0.5 || (rem == 0.5 && fmod(n, 2.0) != 0.0)) n += 1.0;
+    return n * quantum;
+}
+
+static uint32_t encode_fmt(double x, const fmt_t *f) {
+    uint32_t sign_bit = 1u << (f->ebits + f->mbits);
+    uint32_t exp_all = (1u << f->ebits) - 1;
+    if (isnan(x)) {
+        /* canonical quiet NaN: all exponent bits and all mantissa bits set */
+        return (exp_all << f->mbits) | ((1u << f->mbits) - 1);
+    }
+    uint32_t s = signbit(x) ? sign_bit : 0;
+    double a = fabs(x);
+    double r = isinf(a) ? a : round_to_grid(a, f);
+    if (r > f->maxfinite) {
+        if (f->has_inf) return s | (exp_all << f->mbits);           /* +-inf */
+        r = f->maxfinite;                                            /* satfinite */
+    }
+    if (r == 0.0) return s;
+    int e2;
+    frexp(r, &e2);
+    int E = e2 - 1;
+    int emin = 1 - f->bias;
+    if (E < emin) {                                                  /* subnormal */
+        uint32_t m = (uint32_t)(r / ldexp(1.0, emin - f->mbits));
+        return s | m;
+    }
+    uint32_t m = (uint32_t)(r / ldexp(1.0, E - f->mbits)) - (1u << f->mbits);
+    return s | ((uint32_t)(E + f->bias) << f->mbits) | m;
+}
+
+uint32_t oracle_encode(int dtype, double x) {
+    switch (dtype) {
+    case OR_F16:  return encode_fmt(x, &FMT_F16);
+    case OR_BF16: return encode_fmt(x, &FMT_BF16);
+    case OR_E4M3: return encode_fmt(x, &FMT_E4M3);
+    default:      return 0;
+    }
+}
+
+void oracle_decode_array(int dtype, const void *bits, int64_t n, double *out) {
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t b = dtype == OR_E4M3 ? ((const uint8_t *)bits)[i]
+                                      : ((const uint16_t *)bits)[i];
+        out[i] = oracle_decode(dtype, b);
+    }
+}
+
+void oracle_encode_array(int dtype, const double *x, int64_t n, void *bits) {
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t b = oracle_encode(dtype, x[i]);
+        if (dtype == OR_E4M3) ((uint8_t *)bits)[i] = (uint8_t)b;
+        else                  ((uint16_t *)bits)[i] = (uint16_t)b;
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Attention forward, one output row at a time.                               */
+/* ------------------------------------------------------------------------- */
+
+static inline uint32_t load_bits(const void *p, int dtype, int64_t idx) {
+    return dtype == OR_E4M3 ? ((const uint8_t *)p)[idx] : ((const uint16_t *)p)[idx];
+}
+
+/* Is key j visible to query i of a sequence with sq query and sk key rows?
+ * ("CUTLASS Blackwell FMHA 示例完全解析", §融合扩展点: CausalMask q-begin keeps
+ * key <= query; q-end adds the offset seqlen_k - seqlen_q; the residual mask
+ * drops keys at or past seqlen_k, which the loop bound below already does.) */
+static inline int key_allowed(int mask, int causal_type, int64_t i, int64_t j,
+                              int64_t sq, int64_t sk) {
+    if (j >= sk) return 0;
+    if (mask == OR_MASK_CAUSAL) {
+        int64_t off = causal_type == OR_QEND ? sk - sq : 0;
+        return j <= i + off;
+    }
+    return 1;
+}
+
+/*
+ * Compute O and LSE for selected output rows.
+ *
+ * Inputs are raw storage bits (uint16 for fp16/bf16, uint8 for e4m3):
+ *   fixed length: q [B, Sq, H, D], k/v [B, Sk, H_k, D]
+ *   varlen (cu_q and cu_k both non-NULL, B+1 entries each):
+ *                 q [total, H, D], k/v [total, H_k, D]; sequence b owns
+ *                 q rows [cu_q[b], cu_q[b+1]) and k rows [cu_k[b], cu_k[b+1]).
+ * A row index r follows the LSE layout:
+ *   fixed length: r = (b*H + h)*Sq + i   (LSE [B, H, Sq])
+ *   varlen:       r = h*total + t        (LSE [H, total]), t a packed q row.
+ * rows == NULL selects every row 0..n_rows-1.
+ * Outputs: o_out [n_rows, D] (before rounding to the output type) and
+ * lse_out [n_rows].  A varlen row t >= cu_q[B] belongs to no sequence and is
+ * reported as NaN.  Returns 0, or -1 on inconsistent arguments.
+ */
+int oracle_fmha_fwd(const void *q, const void *k, const void *v, int dtype,
+                    int B, int H, int H_k, int Sq, int Sk, int D,
+                    double scale, double out_scale, int mask, int causal_type,
+                    const int *cu_q, const int *cu_k, int64_t total_length,
+                    const int64_t *rows, int64_t n_rows,
+                    double *o_out, double *lse_out, int n_threads) {
+    int varlen = cu_q != NULL && cu_k != NULL;
+    if (B < 0 || H <= 0 || H_k <= 0 || H % H_k != 0 || D <= 0) return -1;
+    if ((cu_q == NULL) != (cu_k == NULL)) return -1;
+    if (!varlen && (Sq < 0 || Sk < 0)) return -1;
+    int64_t max_sk = varlen ? 0 : Sk;
+    if (varlen) {
+        for (int b = 0; b < B; ++b) {
+            int64_t lk = (int64_t)cu_k[b + 1] - cu_k[b];
+            if (lk < 0 || cu_q[b + 1] < cu_q[b]) return -1;
+            if (lk > max_sk) max_sk = lk;
+        }
+        if (cu_q[B] > total_length || cu_k[B] > total_length) return -1;
+    }
+    const int group = H / H_k;
+
+    double dtab[256];
+    double *table = NULL;               /* lookup for 16-bit codes */
+    if (dtype == OR_E4M3) {
+        for (int c = 0; c < 256; ++c) dtab[c] = decode_e4m3((uint32_t)c);
+    } else {
+        table = (double *)malloc(65536 * sizeof(double));
+        if (!table) return -1;
+        for (int c = 0; c < 65536; ++c) table[c] = oracle_decode(dtype, (uint32_t)c);
+    }
+    const double *lut = dtype == OR_E4M3 ? dtab : table;
+
+#ifdef _OPENMP
+    if (n_threads <= 0) n_threads = omp_get_max_threads();
+#pragma omp parallel num_threads(n_threads)
+#endif
+    {
+        double *s = (double *)malloc((size_t)(max_sk > 0 ? max_sk : 1) * sizeof(double));
+        double *qrow = (double *)malloc((size_t)D * sizeof(double));
+        double *acc = (double *)malloc((size_t)D * sizeof(double));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t n = 0; n < n_rows; ++n) {
+            int64_t r = rows ? rows[n] : n;
+            double *orow = o_out + n * D;
+            int64_t b, h, i, sq, sk, q_base_row, k_base_row;
+            if (!varlen) {
+                b = r / ((int64_t)H * Sq);
+                h = (r / Sq) % H;
+                i = r % Sq;
+                sq = Sq; sk = Sk;
+                q_base_row = b * Sq;          /* row index into [B*S] */
+                k_base_row = b * Sk;
+            } else {
+                h = r / total_length;
+                int64_t t = r % total_length;
+                /* find the sequence that owns packed row t */
+                b = -1;
+                for (int bb = 0; bb < B; ++bb)
+                    if (t >= cu_q[bb] && t < cu_q[bb + 1]) { b = bb; break; }
+                if (b < 0) {
+                    for (int d = 0; d < D; ++d) orow[d] = NAN;
+                    lse_out[n] = NAN;
+                    continue;
+                }
+                i = t - cu_q[b];
+                sq = (int64_t)cu_q[b + 1] - cu_q[b];
+                sk = (int64_t)cu_k[b + 1] - cu_k[b];
+                q_base_row = cu_q[b];
+                k_base_row = cu_k[b];
+            }
+            int64_t g = h / group;
+            const int64_t qoff = ((q_base_row + i) * H + h) * D;
+            for (int d = 0; d < D; ++d) qrow[d] = lut[load_bits(q, dtype, qoff + d)];
+
+            /* step 1: scaled scores of the allowed keys, and their maximum */
+            double m = -INFINITY;
+            int64_t n_allowed = 0;
+            for (int64_t j = 0; j < sk; ++j) {
+                if (!key_allowed(mask, causal_type, i, j, sq, sk)) { s[j] = -INFINITY; continue; }
+                const int64_t koff = ((k_base_row + j) * H_k + g) * D;
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d) dot += qrow[d] * lut[load_bits(k, dtype, koff + d)];
+                s[j] = scale * dot;
+                if (s[j] > m) m = s[j];
+                ++n_allowed;
+            }
+            if (n_allowed == 0) {             /* no visible key */
+                for (int d = 0; d < D; ++d) orow[d] = 0.0;
+                lse_out[n] = -INFINITY;
+                continue;
+            }
+            /* step 2: softmax numerators, their sum, and P.V */
+            double l = 0.0;
+            for (int d = 0; d < D; ++d) acc[d] = 0.0;
+            for (int64_t j = 0; j < sk; ++j) {
+                if (s[j] == -INFINITY) continue;
+                double p = exp(s[j] - m);
+                l += p;
+                const int64_t voff = ((k_base_row + j) * H_k + g) * D;
+                for (int d = 0; d < D; ++d) acc[d] += p * lut[load_bits(v, dtype, voff + d)];
+            }
+            for (int d = 0; d < D; ++d) orow[d] = out_scale * acc[d] / l;
+            lse_out[n] = m + log(l);
+        }
+        free(s); free(qrow); free(acc);
+    }
+    free(table);
+    return 0;
+}
