@@ -1,0 +1,499 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused attention forward on one or more GB300s.
+
+A step is one fmha_fwd call (one kernel launch) over one batch of seeded
+synthetic input.  The default workload is causal bf16 grouped-query attention,
+B=2, H=32, H_k=8, Sq=Sk=8192, D=128 (the size the 60%-of-peak target is set
+at).  Metric: TFLOP/s counting 4*B*H*Sq*Sk*D, halved for causal.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Under torchrun every rank runs the same per-GPU workload on its own GPU
+(independent problems, no data exchange: weak scaling); rank 0 prints one
+JSON line.  ``--impl reference`` times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from head_attention_forward_02_gb300 import workloads as wl  # noqa: E402
+from head_attention_forward_02_gb300.metrics import algorithmic_bytes, attention_flops  # noqa: E402
+
+DEFAULT_CONFIG = "bf16_causal_gqa_b2_h32_hk8_s8192_d128"
+L2_BYTES = 129 * 2 ** 20
+KERNEL_SOURCES = ["head_attention_forward_02_gb300/csrc/fmha_sm103.cu",
+                  "head_attention_forward_02_gb300/csrc/fmha_common.h"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(wl.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--kernel", default="tc", choices=["tc", "simt"],
+                    help="tc: tcgen05 kernel (fmha_fwd); simt: CUDA-core cross-check kernel")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (timing only: barrier and max over ranks)
+# ----------------------------------------------------------------------------
+
+def dist_setup(n):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.rows = []
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        inside = [r for t, r in self.rows if t0 <= t <= t1]
+        window = "timed"
+        if not inside:   # timed region shorter than the sampling period
+            inside = [r for t, r in self.rows if t <= t1 + 0.2]
+            window = "warmup+timed"
+        sm = sorted(v for v in (num(r[1]) for r in inside if len(r) > 1) if v is not None)
+        mx = [num(r[2]) for r in inside if len(r) > 2 and num(r[2])]
+        reasons = set()
+        for r in inside:
+            for name, val in zip(self.NAMES, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+def gpu_uuid(dev: int) -> str:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else f"GPU-{u}"
+    except Exception:
+        return "0"
+
+
+# ----------------------------------------------------------------------------
+# roofline inputs
+# ----------------------------------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for s in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, s), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary of this kernel source
+    and workload (profiles/*.md lines 'workload:', 'source_sha256:',
+    'traffic_bytes_per_launch:'); None if absent or the kernel changed since."""
+    want = kernel_source_hash()
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        text = open(path).read()
+        kv = dict(re.findall(r"^- ?(workload|source_sha256|traffic_bytes_per_launch): *(\S+)",
+                             text, flags=re.M))
+        if kv.get("workload") == workload and kv.get("source_sha256") == want:
+            try:
+                return float(kv["traffic_bytes_per_launch"])
+            except (KeyError, ValueError):
+                return None
+    return None
+
+
+# ----------------------------------------------------------------------------
+# the CPU oracle (baseline / reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_rows_flops(inp, rows):
+    """Algorithmic FLOPs of the selected oracle rows: 4*D per visible key, with
+    the causal half counted as the accounting of the whole call does (x 1/2
+    of the dense count), so that rows sum to attention_flops."""
+    w = inp.w
+    import numpy as np
+    rows = np.asarray(rows)
+    if inp.cu_seqlens_q is not None:
+        cq = inp.cu_seqlens_q.numpy()
+        ck = inp.cu_seqlens_k.numpy()
+        t = rows % inp.total_length
+        b = np.searchsorted(cq, t, side="right") - 1
+        sk = (ck[b + 1] - ck[b]).astype(np.float64)
+    else:
+        sk = np.full(rows.shape, float(w.Sk))
+    f = 0.5 if w.mask == "causal" else 1.0
+    return float((4.0 * w.D * sk * f).sum())
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(inp, target_s: float, seed: int = 0):
+    """Run the oracle on growing seeded row samples until ~target_s of CPU work."""
+    import numpy as np
+    import oracle
+    from tests.helpers import oracle_on
+    oracle.build()
+    w = inp.w
+    rng = np.random.default_rng(seed)
+    if inp.cu_seqlens_q is None:
+        pool = np.arange(w.B * w.H * w.Sq)
+    else:
+        T, end = inp.total_length, int(inp.cu_seqlens_q[-1])
+        pool = np.array([h * T + t for h in range(w.H) for t in range(end)])
+    n, done_t, done_f, done_rows = 512, 0.0, 0.0, 0
+    threads = cpu_threads()
+    while done_t < target_s:
+        rows = rng.choice(pool, size=n)
+        t = time.perf_counter()
+        oracle_on(oracle, inp, rows=rows, threads=threads)
+        dt = time.perf_counter() - t
+        done_t += dt
+        done_f += oracle_rows_flops(inp, rows)
+        done_rows += n
+        if dt < target_s / 4:
+            n *= 2
+    return done_f, done_t, done_rows, threads
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def make_device_set(inp, dev):
+    w = inp.w
+    s = {"q": inp.q.to(dev), "k": inp.k.to(dev), "v": inp.v.to(dev)}
+    if inp.cu_seqlens_q is not None:
+        s["cu_q"] = inp.cu_seqlens_q.to(dev)
+        s["cu_k"] = inp.cu_seqlens_k.to(dev)
+        s["lse"] = torch.empty((w.H, inp.total_length), dtype=torch.float32, device=dev)
+    else:
+        s["lse"] = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
+    s["o"] = torch.empty_like(s["q"])
+    return s
+
+
+def call(fm, inp, s, kernel, stream):
+    w = inp.w
+    f = fm.fmha_fwd if kernel == "tc" else fm.fmha_fwd_simt
+    if inp.cu_seqlens_q is not None:
+        rc = f(s["q"], s["k"], s["v"], s["o"], s["lse"], len(inp.seqlens_q), w.H, w.H_k, 0, 0, w.D,
+               w.softmax_scale, w.out_scale, wl.MASK_CODE[w.mask], wl.CAUSAL_CODE[w.causal_type],
+               s["cu_q"], s["cu_k"], inp.max_len, inp.total_length, stream)
+    else:
+        rc = f(s["q"], s["k"], s["v"], s["o"], s["lse"], w.B, w.H, w.H_k, w.Sq, w.Sk, w.D,
+               w.softmax_scale, w.out_scale, wl.MASK_CODE[w.mask], wl.CAUSAL_CODE[w.causal_type],
+               None, None, 0, 0, stream)
+    if rc != 0:
+        raise RuntimeError(f"fmha call failed: {fm.status_string(rc)}")
+
+
+def run_ours(args, rank, world, local):
+    from head_attention_forward_02_gb300 import build, fmha as fm
+    build.build()
+    fm.lib()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    w = wl.CONFIGS[args.config]
+    stream = torch.cuda.current_stream(dev)
+
+    inp0 = wl.generate(w)
+    set_bytes = sum(inp0.q.numel() * inp0.q.element_size() * 2 + t.numel() * t.element_size()
+                    for t in (inp0.k, inp0.v))
+    # inputs larger than L2: alternate two input sets so that no step finds the
+    # previous step's K/V in L2; smaller inputs: flush L2 before every launch
+    n_sets = 2 if set_bytes >= L2_BYTES else 1
+    inputs = [inp0] + [wl.generate(w, seed=w.seed + 1000 * i) for i in range(1, n_sets)]
+    sets = [make_device_set(x, dev) for x in inputs]
+    if n_sets == 1:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    if inp0.cu_seqlens_q is not None:
+        flops = attention_flops(0, w.H, 0, 0, w.D, w.mask == "causal",
+                                inp0.seqlens_q, inp0.seqlens_k)
+        nbytes = algorithmic_bytes(0, w.H, w.H_k, 0, 0, w.D, inp0.q.element_size(),
+                                   inp0.q.element_size(), True, inp0.seqlens_q, inp0.seqlens_k)
+    else:
+        flops = attention_flops(w.B, w.H, w.Sq, w.Sk, w.D, w.mask == "causal")
+        nbytes = algorithmic_bytes(w.B, w.H, w.H_k, w.Sq, w.Sk, w.D, inp0.q.element_size(),
+                                   inp0.q.element_size())
+
+    sampler = ClockSampler(gpu_uuid(dev.index or 0))
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    for i in range(args.warmup):
+        if n_sets == 1:
+            flush.zero_()
+        call(fm, inputs[i % n_sets], sets[i % n_sets], args.kernel, stream)
+    torch.cuda.synchronize(dev)
+    if fm.device_status(reset=True) != 0:
+        raise RuntimeError("device status reports a timeout")
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(K):
+        j = i % n_sets
+        if n_sets == 1:
+            flush.zero_()
+        starts[i].record(stream)
+        call(fm, inputs[j], sets[j], args.kernel, stream)
+        ends[i].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t_host1 = time.time()
+    total_ms = ev0.elapsed_time(ev1)
+    launch_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / K
+    if rank == 0:
+        sampler.stop()
+    if fm.device_status(reset=True) != 0:
+        raise RuntimeError("device status reports a timeout")
+    total_ms = max_over_ranks(total_ms, world)
+    launch_ms = max_over_ranks(launch_ms, world)
+    ms_per_step = total_ms / K
+    # with a flush buffer the step time includes the flush; report the launch time
+    step_ms = launch_ms if n_sets == 1 else ms_per_step
+    value = world * flops / (step_ms * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, O and LSE out
+    e2e_steps = args.e2e_steps or max(3, min(K, 20))
+    h = {"q": inputs[0].q.pin_memory(), "k": inputs[0].k.pin_memory(), "v": inputs[0].v.pin_memory()}
+    ho = torch.empty(sets[0]["o"].shape, dtype=sets[0]["o"].dtype).pin_memory()
+    hl = torch.empty(sets[0]["lse"].shape, dtype=torch.float32).pin_memory()
+    s = sets[0]
+
+    def e2e_step():
+        for key in ("q", "k", "v"):
+            s[key].copy_(h[key], non_blocking=True)
+        call(fm, inputs[0], s, args.kernel, stream)
+        ho.copy_(s["o"], non_blocking=True)
+        hl.copy_(s["lse"], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = ho.numel() * ho.element_size() + hl.numel() * 4
+
+    if rank != 0:
+        return
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    dtype_name = {"bf16": "bf16", "f16": "f16", "e4m3": "e4m3"}[w.dtype]
+    if w.dtype == "e4m3":
+        peak *= 2.0          # fp8 dense rate is twice bf16 (4.5 vs 2.25 PFLOP/s nominal)
+    achieved = flops / (launch_ms * 1e-3) / 1e12
+    traffic = profiled_traffic(args.config)
+    line = {
+        "metric": "FMHA forward TFLOP/s and % of GB300 dense tensor peak (bf16/fp8)",
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": dtype_name,
+        "data": "synthetic (seeded N(0,1); varlen lengths seeded uniform)",
+        "config": {"workload": args.config, "B": w.B, "H": w.H, "H_k": w.H_k, "Sq": w.Sq,
+                   "Sk": w.Sk, "D": w.D, "mask": w.mask, "causal_type": w.causal_type,
+                   "kernel": "fmha_fwd" if args.kernel == "tc" else "fmha_fwd_simt",
+                   "l2": (f"ring of {n_sets} input sets of {set_bytes / 2**20:.0f} MiB"
+                          if n_sets > 1 else "L2 flushed (256 MiB write) before every launch"),
+                   "parallelism": f"replicas x{world} (independent problems)"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{'bf16_tflops' if w.dtype != 'e4m3' else '2 x bf16_tflops'} "
+                                    f"of {peak_src}",
+                     "traffic": traffic, "algorithmic_bytes": nbytes,
+                     "launch_ms": round(launch_ms, 5)},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": K,
+        "clocks": sampler.summary(t_host0, t_host1),
+    }
+    if not args.no_cpu_baseline:
+        f, t, nrows, threads = time_oracle(inputs[0], target_s=10.0)
+        line["cpu_baseline"] = {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s",
+                                "cores": threads, "kind": "oracle",
+                                "sample": f"{nrows} seeded random query rows of {args.config} "
+                                          f"({f / 1e9:.1f} GFLOP, {t:.1f} s)"}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step is a bounded seeded sample
+    of query rows of the same workload."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from tests.helpers import oracle_on
+    oracle.build()
+    w = wl.CONFIGS[args.config]
+    inp = wl.generate(w)
+    threads = cpu_threads()
+    rng = np.random.default_rng(1)
+    if inp.cu_seqlens_q is None:
+        pool = np.arange(w.B * w.H * w.Sq)
+    else:
+        T, end = inp.total_length, int(inp.cu_seqlens_q[-1])
+        pool = np.array([h * T + t for h in range(w.H) for t in range(end)])
+    rows_per_step = 64
+    samples = [rng.choice(pool, size=rows_per_step) for _ in range(args.steps + args.warmup)]
+    for i in range(args.warmup):
+        oracle_on(oracle, inp, rows=samples[i], threads=threads)
+    t = time.perf_counter()
+    fl = 0.0
+    for i in range(args.steps):
+        r = samples[args.warmup + i]
+        oracle_on(oracle, inp, rows=r, threads=threads)
+        fl += oracle_rows_flops(inp, r)
+    dt = time.perf_counter() - t
+    value = fl / dt / 1e12
+    line = {"metric": "FMHA forward TFLOP/s and % of GB300 dense tensor peak (bf16/fp8)",
+            "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded N(0,1))",
+            "config": {"workload": args.config}, "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle",
+                             "sample": f"{rows_per_step} seeded random query rows per step"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    rank, world, local = dist_setup(args.gpus)
+    try:
+        run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,179 @@
+"""Python binding of the C ABI in include/fmha.h (argument marshalling only).
+
+Every step of the computation runs in libfmha.so's CUDA kernels; this module
+only turns torch tensors into pointers and the current torch stream into a
+cudaStream_t.  If the library has not been built it raises: there is no
+fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfmha.so")
+
+F16, BF16, E4M3 = 0, 1, 2
+MASK_NONE, MASK_RESIDUAL, MASK_CAUSAL = 0, 1, 2
+CAUSAL_QBEGIN, CAUSAL_QEND = 0, 1
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4
+
+_TORCH_DTYPE = {torch.float16: F16, torch.bfloat16: BF16, torch.float8_e4m3fn: E4M3}
+_MASKS = {"none": MASK_NONE, "residual": MASK_RESIDUAL, "causal": MASK_CAUSAL}
+_CAUSAL = {"qbegin": CAUSAL_QBEGIN, "qend": CAUSAL_QEND}
+
+EXPORTED = ("fmha_fwd", "fmha_fwd_simt", "fmha_status_string", "fmha_device_status",
+            "fmha_kv_tile_range")
+
+
+class fmha_tensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int)]
+
+
+class FmhaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """Load libfmha.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(_LIB_PATH)
+        fwd_args = [fmha_tensor, fmha_tensor, fmha_tensor, fmha_tensor, ctypes.c_void_p,
+                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                    ctypes.c_int, ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                    ctypes.c_void_p]
+        for name in ("fmha_fwd", "fmha_fwd_simt"):
+            f = getattr(L, name)
+            f.restype = ctypes.c_int
+            f.argtypes = fwd_args
+        L.fmha_status_string.restype = ctypes.c_char_p
+        L.fmha_status_string.argtypes = [ctypes.c_int]
+        L.fmha_device_status.restype = ctypes.c_int
+        L.fmha_device_status.argtypes = [ctypes.c_int]
+        L.fmha_kv_tile_range.restype = ctypes.c_int
+        L.fmha_kv_tile_range.argtypes = [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_int)] * 2
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().fmha_status_string(int(status)).decode()
+
+
+def device_status(reset: bool = False) -> int:
+    return lib().fmha_device_status(1 if reset else 0)
+
+
+def kv_tile_range(q_row0: int, q_rows: int, Sq: int, Sk: int, mask: int, causal_type: int,
+                  tile_n: int) -> Tuple[int, int]:
+    a, b = ctypes.c_int(), ctypes.c_int()
+    rc = lib().fmha_kv_tile_range(q_row0, q_rows, Sq, Sk, mask, causal_type, tile_n,
+                                  ctypes.byref(a), ctypes.byref(b))
+    if rc != OK:
+        raise FmhaError(rc, status_string(rc))
+    return a.value, b.value
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _tensor(t, dtype: Optional[int] = None) -> fmha_tensor:
+    if t is None:
+        return fmha_tensor(None, BF16 if dtype is None else dtype)
+    if isinstance(t, torch.Tensor):
+        return fmha_tensor(t.data_ptr(), _TORCH_DTYPE[t.dtype] if dtype is None else dtype)
+    return fmha_tensor(int(t), dtype)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _call(name, q, k, v, o, lse, B, H, H_k, Sq, Sk, D, scale, out_scale, mask, causal_type,
+          cu_seqlens_q, cu_seqlens_k, max_len, total_length, stream) -> int:
+    f = getattr(lib(), name)
+    return f(_tensor(q), _tensor(k), _tensor(v), _tensor(o), _ptr(lse), int(B), int(H), int(H_k),
+             int(Sq), int(Sk), int(D), float(scale), float(out_scale), int(mask), int(causal_type),
+             _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(max_len), int(total_length),
+             _stream(stream))
+
+
+def fmha_fwd(q, k, v, o, lse, B, H, H_k, Sq, Sk, D, scale, out_scale, mask, causal_type,
+             cu_seqlens_q=None, cu_seqlens_k=None, max_len=0, total_length=0, stream=None) -> int:
+    """Same arguments, order and status codes as the C function fmha_fwd.
+
+    Tensors are passed as torch tensors (or raw device addresses); ``stream``
+    defaults to torch's current stream.  Returns the C status code."""
+    return _call("fmha_fwd", q, k, v, o, lse, B, H, H_k, Sq, Sk, D, scale, out_scale, mask,
+                 causal_type, cu_seqlens_q, cu_seqlens_k, max_len, total_length, stream)
+
+
+def fmha_fwd_simt(q, k, v, o, lse, B, H, H_k, Sq, Sk, D, scale, out_scale, mask, causal_type,
+                  cu_seqlens_q=None, cu_seqlens_k=None, max_len=0, total_length=0,
+                  stream=None) -> int:
+    """The CUDA-core cross-check kernel; same contract as fmha_fwd."""
+    return _call("fmha_fwd_simt", q, k, v, o, lse, B, H, H_k, Sq, Sk, D, scale, out_scale, mask,
+                 causal_type, cu_seqlens_q, cu_seqlens_k, max_len, total_length, stream)
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Optional[float] = None,
+        out_scale: float = 1.0, mask: str = "none", causal_type: str = "qbegin",
+        cu_seqlens_q: Optional[torch.Tensor] = None, cu_seqlens_k: Optional[torch.Tensor] = None,
+        max_len: Optional[int] = None, total_length: Optional[int] = None,
+        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+        return_lse: bool = True, impl: str = "tc", stream=None):
+    """Attention forward on device tensors; allocates O (and LSE) if not given.
+
+    Fixed length: q [B,Sq,H,D], k/v [B,Sk,H_k,D].  Varlen: q [T,H,D], k/v
+    [T,H_k,D] with int32 device cumulative lengths.  Returns (O, LSE)."""
+    varlen = cu_seqlens_q is not None
+    D = q.shape[-1]
+    if varlen:
+        T = q.shape[0] if total_length is None else int(total_length)
+        B = cu_seqlens_q.numel() - 1
+        H, H_k = q.shape[1], k.shape[1]
+        Sq = Sk = 0
+        if max_len is None:
+            raise ValueError("varlen needs max_len")
+        lse_shape = (H, T)
+    else:
+        B, Sq, H = q.shape[0], q.shape[1], q.shape[2]
+        Sk, H_k = k.shape[1], k.shape[2]
+        T = 0
+        lse_shape = (B, H, Sq)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    sc = 1.0 / math.sqrt(D) if scale is None else scale
+    name = "fmha_fwd" if impl == "tc" else "fmha_fwd_simt"
+    rc = _call(name, q, k, v, out, lse, B, H, H_k, Sq, Sk, D, sc, out_scale, _MASKS[mask],
+               _CAUSAL[causal_type], cu_seqlens_q, cu_seqlens_k, max_len or 0, T, stream)
+    if rc != OK:
+        raise FmhaError(rc, status_string(rc))
+    return out, lse

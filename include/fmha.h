@@ -1,0 +1,164 @@
+/*
+ * fmha.h -- C ABI of the GB300 (sm_103a) fused multi-head attention forward.
+ *
+ *   O = softmax(scale * Q K^T + mask) V      (per batch, query head)
+ *   LSE = log(sum_j exp(scale * q.k_j))      (natural log, visible keys only)
+ *
+ * computed with an online (running max / running sum) softmax so that the
+ * score and probability matrices never leave the chip.
+ *
+ * Passages that define the operation (page title, section):
+ *  - "fmha sm120 : 超越 torch.sdpa(flash-attention-2)", §1 flash attention:
+ *    MHA = softmax(q @ k^T * scale) @ v on [batch, seq, heads, head_dim]
+ *    tensors, O shaped like Q, scale conventionally 1/sqrt(head_dim); §2:
+ *    grouped-query attention maps query head h to kv head h / (H / H_k).
+ *  - "FMHA for Blackwell: Forward" (CUTLASS example 77 README): head dims
+ *    32/64/128, fp8/fp16/bf16 inputs.
+ *  - "CUTLASS Blackwell FMHA 示例完全解析": §融合扩展点 (masks: none, residual,
+ *    causal with q-begin / q-end alignment, masked scores are -infinity);
+ *    §变长序列 (cumulative lengths, total_length, a padding batch ahead of the
+ *    packed data); §验证机制 (O and LSE are both outputs); §核心设计 (the
+ *    output scale is applied in fp32 before the cast to the output type).
+ *
+ * All functions are thread-safe.  Nothing here allocates device memory except
+ * one lazily created 4-byte device status word per library instance.
+ */
+#ifndef FMHA_H
+#define FMHA_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>   /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage types of Q, K, V and O. */
+enum fmha_dtype {
+    FMHA_F16 = 0,   /* IEEE binary16 */
+    FMHA_BF16 = 1,  /* bfloat16 */
+    FMHA_E4M3 = 2   /* OCP fp8 E4M3 ("fn": no inf, max 448) */
+};
+
+/* A device buffer and its storage type. */
+typedef struct fmha_tensor {
+    void *data;
+    int dtype;      /* enum fmha_dtype */
+} fmha_tensor;
+
+enum fmha_mask {
+    FMHA_MASK_NONE = 0,      /* every key of the sequence is visible */
+    FMHA_MASK_RESIDUAL = 1,  /* same result as NONE: keys >= Sk are dropped */
+    FMHA_MASK_CAUSAL = 2     /* key j visible to query i iff j <= i + offset */
+};
+
+enum fmha_causal_type {
+    FMHA_CAUSAL_QBEGIN = 0,  /* offset 0: queries aligned to the first key */
+    FMHA_CAUSAL_QEND = 1     /* offset Sk - Sq: last query sees every key */
+};
+
+enum fmha_status {
+    FMHA_OK = 0,
+    FMHA_ERR_INVALID_ARG = -1,   /* bad pointer, size, enum or varlen arguments */
+    FMHA_ERR_UNSUPPORTED = -2,   /* valid but not supported: dtype combination,
+                                    alignment, device not sm_103 */
+    FMHA_ERR_CUDA = -3,          /* a CUDA runtime / driver call failed */
+    FMHA_ERR_TIMEOUT = -4        /* a bounded on-device wait expired
+                                    (reported by fmha_device_status) */
+};
+
+/*
+ * fmha_fwd -- fused attention forward on the tcgen05 tensor cores.
+ *
+ * Arguments
+ *   q, k, v      inputs.  k and v have q's dtype.
+ *   o            output.  dtype == q's for fp16/bf16; FMHA_E4M3 (saturating
+ *                round-to-nearest-even) for e4m3 inputs.
+ *   lse          fp32 log-sum-exp output, or NULL to skip it.
+ *   B            batch size (number of sequences when varlen).
+ *   H, H_k       query heads and key/value heads; H % H_k == 0 (GQA, MQA
+ *                when H_k == 1).  Query head h reads kv head h / (H / H_k).
+ *   Sq, Sk       query and key lengths (fixed-length mode; ignored if varlen).
+ *   D            head dim: 32, 64 or 128.
+ *   scale        softmax scale applied to Q K^T (1/sqrt(D) is the usual).
+ *   out_scale    fp32 factor applied to O before the cast to o's dtype.
+ *                It does not enter LSE.
+ *   mask         enum fmha_mask.  causal_type: enum fmha_causal_type.
+ *   cu_seqlens_q, cu_seqlens_k
+ *                both NULL: fixed length.  Both non-NULL: variable length,
+ *                int32 device arrays of B+1 non-decreasing entries starting
+ *                at 0; sequence b owns packed q rows [cu_q[b], cu_q[b+1]) and
+ *                k/v rows [cu_k[b], cu_k[b+1]).  One NULL: INVALID_ARG.
+ *   max_len      varlen: >= every per-sequence q and k length.
+ *   total_length varlen: number of rows allocated in every packed tensor,
+ *                >= cu_q[B] and >= cu_k[B].  It bounds every load.
+ *   stream       CUDA stream; the call is asynchronous on it.
+ *
+ * Layouts (all contiguous, row-major):
+ *   fixed:  q, o [B, Sq, H, D];  k, v [B, Sk, H_k, D];  lse [B, H, Sq]
+ *   varlen: q, o [total_length, H, D];  k, v [total_length, H_k, D];
+ *           lse [H, total_length]; each pointer addresses the first packed row.
+ *   Varlen callers keep one batch of valid padding rows ahead of the packed
+ *   data (the layout of the CUTLASS example); this library never reads or
+ *   writes it, and never writes o or lse rows outside [0, cu_q[B]).
+ *   Input rows that share a load tile with a sequence but lie outside it are
+ *   read and then masked, so inputs must hold no NaN or Inf.
+ *
+ * Semantics: a query row with no visible key (causal q-end with Sq_b > Sk_b
+ * rows, or Sk_b == 0) gets O = 0 and LSE = -infinity.
+ *
+ * Ownership: the caller owns every buffer; the library keeps no pointer after
+ * the call returns.  Data pointers must be 16-byte aligned (TMA), otherwise
+ * FMHA_ERR_UNSUPPORTED.
+ *
+ * Errors: arguments are validated before anything is launched; on error
+ * nothing is launched and the status says why.  Returns FMHA_OK when the work
+ * was enqueued (or there was nothing to do).
+ */
+int fmha_fwd(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor o, float *lse,
+             int B, int H, int H_k, int Sq, int Sk, int D,
+             float scale, float out_scale, int mask, int causal_type,
+             const int *cu_seqlens_q, const int *cu_seqlens_k, int max_len,
+             int64_t total_length, cudaStream_t stream);
+
+/*
+ * fmha_fwd_simt -- the same operation on CUDA cores (fp32 FMA, no tensor
+ * cores).  Same arguments, layouts, semantics and errors as fmha_fwd.  It is
+ * a slow cross-check of the tensor-core kernel, not a fast path.
+ */
+int fmha_fwd_simt(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor o, float *lse,
+                  int B, int H, int H_k, int Sq, int Sk, int D,
+                  float scale, float out_scale, int mask, int causal_type,
+                  const int *cu_seqlens_q, const int *cu_seqlens_k, int max_len,
+                  int64_t total_length, cudaStream_t stream);
+
+/* Text for a status code (static storage, never NULL). */
+const char *fmha_status_string(int status);
+
+/*
+ * fmha_device_status -- read the device-side status word of the current
+ * device: FMHA_OK, or FMHA_ERR_TIMEOUT if a kernel gave up a bounded wait
+ * (it then skipped its remaining work and released its resources).
+ * Synchronises the device.  reset != 0 clears the word.  Returns
+ * FMHA_ERR_CUDA if the word cannot be read.
+ */
+int fmha_device_status(int reset);
+
+/*
+ * fmha_kv_tile_range -- host copy of the scheduler's key-tile bounds for one
+ * query tile (exposed for testing).  For query rows [q_row0, q_row0 + q_rows)
+ * of a sequence with Sq queries and Sk keys, key tiles of tile_n rows:
+ *   *n_tiles    = number of key tiles that hold at least one visible key,
+ *   *n_unmasked = leading key tiles in which every key is visible to every
+ *                 query row of the tile (no mask needs to be applied there).
+ * Rows at or past Sq are ignored.  Returns FMHA_OK or FMHA_ERR_INVALID_ARG.
+ * ("CUTLASS Blackwell FMHA 示例完全解析", §融合扩展点: get_trip_count,
+ * get_masked_trip_count, get_unmasked_trip_count.)
+ */
+int fmha_kv_tile_range(int q_row0, int q_rows, int Sq, int Sk, int mask, int causal_type,
+                       int tile_n, int *n_tiles, int *n_unmasked);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FMHA_H */

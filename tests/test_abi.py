@@ -1,0 +1,115 @@
+"""The C ABI without a GPU: symbols, argument validation, scheduler tile math."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fmha.h")
+
+
+@pytest.fixture(scope="module")
+def fm():
+    from head_attention_forward_02_gb300 import build, fmha
+    build.build()
+    fmha.lib()
+    return fmha
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \t\*]*?\b(fmha_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("fmha_fwd", "fmha_fwd_simt", "fmha_status_string", "fmha_device_status",
+              "fmha_kv_tile_range"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(fm):
+    L = fm.lib()
+    for n in declared_functions():
+        assert hasattr(L, n), n
+
+
+def test_status_strings(fm):
+    for code in (0, -1, -2, -3, -4):
+        assert fm.status_string(code)
+    assert fm.status_string(-99) == "unknown status"
+
+
+P = 0x10000  # a fake, 16-byte aligned address: validation never dereferences
+
+
+def call(fm, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=None, B=1, H=2, H_k=2, Sq=128, Sk=128, D=128,
+             scale=0.1, out_scale=1.0, mask=0, causal_type=0, cu_seqlens_q=None,
+             cu_seqlens_k=None, max_len=0, total_length=0, dtypes=(1, 1, 1, 1))
+    a.update(kw)
+    dq, dk, dv, do = a.pop("dtypes")
+    L = fm.lib()
+    return L.fmha_fwd(fm.fmha_tensor(a["q"], dq), fm.fmha_tensor(a["k"], dk),
+                      fm.fmha_tensor(a["v"], dv), fm.fmha_tensor(a["o"], do), a["lse"],
+                      a["B"], a["H"], a["H_k"], a["Sq"], a["Sk"], a["D"], a["scale"],
+                      a["out_scale"], a["mask"], a["causal_type"], a["cu_seqlens_q"],
+                      a["cu_seqlens_k"], a["max_len"], a["total_length"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=96), -1), (dict(D=256), -1), (dict(H=3, H_k=2), -1), (dict(H_k=0), -1),
+    (dict(B=-1), -1), (dict(Sq=-5), -1), (dict(mask=3), -1), (dict(causal_type=2), -1),
+    (dict(scale=float("nan")), -1), (dict(out_scale=float("inf")), -1),
+    (dict(cu_seqlens_q=P), -1),                                   # only one cu_seqlens
+    (dict(cu_seqlens_q=P, cu_seqlens_k=P, total_length=-1, max_len=4), -1),
+    (dict(cu_seqlens_q=P, cu_seqlens_k=P, total_length=10, max_len=0), -1),
+    (dict(q=0), -1), (dict(o=0), -1),
+    (dict(dtypes=(1, 0, 1, 1)), -2), (dict(dtypes=(2, 2, 2, 1)), -2), (dict(dtypes=(1, 1, 1, 7)), -1),
+    (dict(q=P + 8), -2), (dict(v=P + 2), -2), (dict(lse=P + 2), -1),
+])
+def test_validation_rejects_before_any_launch(fm, kw, code):
+    assert call(fm, **kw) == code
+
+
+def test_empty_problems_succeed_without_a_device(fm):
+    assert call(fm, B=0, q=0, k=0, v=0, o=0) == 0
+    assert call(fm, Sq=0, q=0, k=0, v=0, o=0) == 0
+    assert call(fm, cu_seqlens_q=P, cu_seqlens_k=P, total_length=0, max_len=0, B=3) == 0
+
+
+def _brute(row0, rows, sq, sk, mask, ct, tn):
+    last = min(row0 + rows, sq) - 1
+    if last < row0 or sk <= 0:
+        return 0, 0
+    off = sk - sq if (mask == 2 and ct == 1) else 0
+
+    def vis(i, j):
+        return j < sk and (mask != 2 or j <= i + off)
+
+    top = -1
+    for i in range(row0, last + 1):
+        for j in range(sk):
+            if vis(i, j):
+                top = max(top, j)
+    n_tiles = 0 if top < 0 else top // tn + 1
+    nu = 0
+    while nu < n_tiles and all(vis(i, j) for i in range(row0, last + 1)
+                               for j in range(nu * tn, (nu + 1) * tn)):
+        nu += 1
+    return n_tiles, nu
+
+
+def test_kv_tile_range_matches_brute_force(fm):
+    rng = np.random.default_rng(5)
+    cases = [(0, 8, 9, 13, 2, 0, 4), (4, 8, 9, 5, 2, 1, 4), (0, 4, 3, 0, 0, 0, 4), (8, 8, 9, 20, 2, 1, 8)]
+    for _ in range(400):
+        tn = int(rng.choice([2, 4, 8]))
+        sq, sk = int(rng.integers(0, 40)), int(rng.integers(0, 40))
+        row0 = int(rng.integers(0, 40)) // tn * tn
+        cases.append((row0, tn * int(rng.integers(1, 3)), sq, sk, int(rng.integers(0, 3)),
+                      int(rng.integers(0, 2)), tn))
+    for c in cases:
+        assert fm.kv_tile_range(*c) == _brute(*c), c
