@@ -1,12 +1,941 @@
-// fmha_sm103.cu -- tensor-core attention forward for sm_103a (placeholder:
-// routes to the CUDA-core kernel until the tcgen05 kernel lands).
+// fmha_sm103.cu -- fused attention forward on the sm_103a tensor cores.
+//
+// O = softmax(scale * Q K^T + mask) V with an online softmax; S and P live in
+// tensor memory (TMEM) and never reach HBM.
+//
+// Design (prior art: "FMHA for Blackwell: Forward" -- two Q tiles per CTA
+// ping-ponged between the GEMMs and the softmax, 256 x 128 blocking, fp32
+// accumulators; "fmha sm120 : 超越 torch.sdpa(flash-attention-2)" -- TMA
+// tiles in swizzled shared memory, a separate barrier for V so its load
+// overlaps Q K^T, exp2 with the scale folded into one FMA, lazy rescaling
+// of O at a 2^8 threshold, masking only on boundary tiles):
+//
+//  * persistent CTAs, one per SM; a work unit is (batch, query head, 256
+//    query rows) = two 128-row Q tiles; units are taken heaviest first;
+//  * warp 8 (one lane) loads Q tiles and a ring of K/V tiles by TMA;
+//  * warp 9 (one lane) issues tcgen05.mma: S_t = Q_t K^T into TMEM (fp32),
+//    then O_t += P_t V with P_t read from TMEM (aliasing S_t) and V from
+//    shared memory (MN-major); it owns the TMEM allocation;
+//  * warps 0-3 / 4-7 run the softmax of Q tile 0 / 1, one thread per query
+//    row (TMEM lane), and the epilogue of their tile;
+//  * the MMA order S0_j, S1_j, PV0_j, S0_{j+1}, PV1_j, S1_{j+1}, ... gives
+//    each softmax warpgroup the time of two GEMMs to produce P, and makes
+//    "S_t_j complete" imply "PV_t_{j-1} complete", so the softmax warps may
+//    rescale O_t in TMEM before publishing P_t_j without another barrier.
+//
+// Every wait is bounded: after kTimeoutNs the waiting thread records
+// FMHA_ERR_TIMEOUT in g_status, raises a CTA-wide abort flag, and all roles
+// stop issuing work, drain what they issued (bounded), free TMEM and return.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
+#include <math.h>
+#include <mutex>
 
 #include "fmha_common.h"
 
 namespace fmha {
 
 __device__ int g_status;   // FMHA_OK, or FMHA_ERR_TIMEOUT after a bounded wait expired
+
+namespace {
+
+constexpr int kTile = 128;                 // query rows per Q tile, keys per K/V tile
+constexpr int kUnitRows = 2 * kTile;       // query rows per work unit
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr unsigned long long kTimeoutNs = 4000000000ull;
+constexpr unsigned long long kDrainNs = 200000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;       // rescale O when the max grows by > 2^8
+
+enum Elem { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
+
+template <int D_, int ELEM_>
+struct Cfg {
+    static constexpr int D = D_;
+    static constexpr int ELEM = ELEM_;
+    static constexpr bool FP8 = ELEM == kE4M3;
+    static constexpr int E = FP8 ? 1 : 2;                 // bytes per element
+    static constexpr int ROW_BYTES = D * E;
+    static constexpr int SW = ROW_BYTES >= 128 ? 128 : ROW_BYTES;   // swizzle span (bytes)
+    static constexpr int PANELS = ROW_BYTES / SW;         // 128-byte column panels per row
+    static constexpr int BOX_D = SW / E;                  // elements per panel row
+    static constexpr int PANEL_BYTES = kTile * SW;
+    static constexpr int TILE_BYTES = kTile * ROW_BYTES;
+    static constexpr uint64_t SW_CODE = SW == 128 ? 2 : (SW == 64 ? 4 : 6);
+    static constexpr int SBO = 8 * SW;                    // one 8-row swizzle atom
+    static constexpr int MMA_K = FP8 ? 32 : 16;           // K of one tcgen05.mma
+    static constexpr int KSTEP_BYTES = MMA_K * E;         // 32 bytes
+    static constexpr int QK_STEPS = D / MMA_K;
+    static constexpr int PV_STEPS = kTile / MMA_K;
+    static constexpr int NS = TILE_BYTES <= 8192 ? 8 : (TILE_BYTES <= 16384 ? 6 : 4);
+    static constexpr int S_COL0 = 0, S_COL1 = kTile;
+    static constexpr int O_COL0 = 2 * kTile, O_COL1 = 2 * kTile + D;
+    static constexpr int BAR_BYTES = 512;
+    static constexpr int SMEM_USED = 2 * TILE_BYTES + NS * TILE_BYTES + BAR_BYTES;
+    // at least 120 KB so that a second CTA can never share the SM (TMEM is
+    // allocated whole), plus 1 KB to align the tiles for the 128-byte swizzle
+    static constexpr int SMEM_BYTES = (SMEM_USED < 120 * 1024 ? 120 * 1024 : SMEM_USED) + 1024;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(O_COL1 + D <= (int)kTmemCols, "TMEM budget");
+    // instruction descriptor fields (kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = e4m3)
+    static constexpr uint32_t AB_FMT = ELEM == kBF16 ? 1u : 0u;
+    static constexpr uint32_t idesc(int n, bool b_mn_major) {
+        return (1u << 4)                        // D: f32
+               | (AB_FMT << 7) | (AB_FMT << 10)  // A, B formats
+               | ((b_mn_major ? 1u : 0u) << 16)  // B major-ness
+               | ((uint32_t)(n >> 3) << 17)      // N >> 3
+               | ((uint32_t)(kTile >> 4) << 24); // M >> 4
+    }
+};
+
+struct Bars {
+    uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], drain;
+    uint64_t kv_full[8], kv_empty[8];
+    uint32_t tmem_base;
+    int abort;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers (mbarrier, TMA, tcgen05)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Slow path of a bounded wait: poll until the phase completes, the CTA aborts,
+// or kTimeoutNs pass (then record the timeout and raise the abort flag).
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kTimeoutNs) {
+                *abort_flag = 1;
+                atomicExch(&g_status, FMHA_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort_flag);
+}
+
+// Bounded wait that ignores the abort flag (used only while draining).
+__device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > kDrainNs) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Arrive on an mbarrier once every tcgen05 operation issued so far by this
+// thread has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor: start address, leading / stride byte
+// offsets (16-byte units), descriptor version 1, swizzle mode.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint64_t swz) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (swz << 61);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]
+template <bool FP8>
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    if constexpr (FP8) {
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(acc)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(acc)
+            : "memory");
+    }
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]
+template <bool FP8>
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    if constexpr (FP8) {
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+            "r"(a), "l"(b), "r"(idesc), "r"(acc)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+            "r"(a), "l"(b), "r"(idesc), "r"(acc)
+            : "memory");
+    }
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Load 32 consecutive TMEM columns of this thread's lane (32x32b shape).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+}
+
+// Wait for this thread's outstanding TMEM loads; the register operands tie the
+// loaded values to the wait so no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// Store 32 consecutive TMEM columns of this thread's lane (32x32b shape).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+                 :
+                 : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Element packing
+// ---------------------------------------------------------------------------
+
+template <int ELEM>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (ELEM == kBF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+}
+
+// four values to e4m3 (round to nearest even, saturating), first value in the low byte
+__device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+// ---------------------------------------------------------------------------
+// Work units: (batch, query head, 256 query rows), heaviest first for causal
+// ---------------------------------------------------------------------------
+
+struct Unit {
+    int b, h, g, q0;      // batch, query head, kv head, first query row of the unit
+    int sq, sk;           // sequence lengths
+    int q_row, k_row;     // row of the sequence's first token in the stored tensors
+    int n[2], nu[2];      // per Q tile: key tiles to visit / of which unmasked
+};
+
+struct Cursor {           // varlen: sequence holding the last decoded unit
+    int b = 0, base = 0;  // and the index of its first unit
+};
+
+__device__ __forceinline__ bool decode_unit(const Params &p, int u, Cursor &cur, Unit &U) {
+    int b, h, qb;
+    if (!p.varlen) {
+        const int nqb = (p.Sq + kUnitRows - 1) / kUnitRows;
+        const int per = p.B * p.H;
+        if (u >= per * nqb) return false;
+        const int r = u / per, rem = u - r * per;
+        b = rem / p.H;
+        h = rem - b * p.H;
+        qb = p.mask == FMHA_MASK_CAUSAL ? nqb - 1 - r : r;
+        U.sq = p.Sq;
+        U.sk = p.Sk;
+        U.q_row = b * p.Sq;
+        U.k_row = b * p.Sk;
+    } else {
+        int bb = cur.b, base = cur.base;
+        for (;;) {
+            if (bb >= p.B) {
+                cur.b = bb;
+                cur.base = base;
+                return false;
+            }
+            const int lq = p.cu_q[bb + 1] - p.cu_q[bb];
+            const int cnt = ((lq + kUnitRows - 1) / kUnitRows) * p.H;
+            if (u < base + cnt) break;
+            base += cnt;
+            ++bb;
+        }
+        cur.b = bb;
+        cur.base = base;
+        b = bb;
+        const int rem = u - base;
+        U.q_row = p.cu_q[b];
+        U.sq = p.cu_q[b + 1] - U.q_row;
+        U.k_row = p.cu_k[b];
+        U.sk = p.cu_k[b + 1] - U.k_row;
+        const int nqb = (U.sq + kUnitRows - 1) / kUnitRows;
+        qb = nqb - 1 - rem / p.H;
+        h = rem % p.H;
+    }
+    U.b = b;
+    U.h = h;
+    U.g = h / p.group;
+    U.q0 = qb * kUnitRows;
+    kv_tile_range(U.q0, kTile, U.sq, U.sk, p.mask, p.causal_type, kTile, &U.n[0], &U.nu[0]);
+    kv_tile_range(U.q0 + kTile, kTile, U.sq, U.sk, p.mask, p.causal_type, kTile, &U.n[1], &U.nu[1]);
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Producer: Q tiles and the K/V ring, by TMA (one lane)
+// ---------------------------------------------------------------------------
+
+template <class C>
+__device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensorMap *tmK,
+                         const CUtensorMap *tmV, uint8_t *sQ, uint8_t *sKV, Bars *bars) {
+    volatile int *abort_flag = &bars->abort;
+    prefetch_tmap(tmQ);
+    prefetch_tmap(tmK);
+    prefetch_tmap(tmV);
+    uint32_t fill = 0, qload[2] = {0, 0};
+    bool ok = true;
+    Cursor cur;
+    for (int u = blockIdx.x; ok; u += gridDim.x) {
+        Unit U;
+        if (!decode_unit(p, u, cur, U)) break;
+        const int nmax = imax(U.n[0], U.n[1]);
+        for (int t = 0; t < 2; ++t) {
+            if (U.n[t] == 0) continue;
+            if (qload[t] > 0 &&
+                !mbar_wait(smem_u32(&bars->q_empty[t]), (qload[t] - 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = smem_u32(&bars->q_full[t]);
+            mbar_expect_tx(fb, C::TILE_BYTES);
+            const uint32_t dst = smem_u32(sQ + t * C::TILE_BYTES);
+            const int row = U.q0 + t * kTile;
+#pragma unroll
+            for (int pn = 0; pn < C::PANELS; ++pn) {
+                if (p.varlen)
+                    tma_load_3d(dst + pn * C::PANEL_BYTES, tmQ, fb, pn * C::BOX_D, U.h, U.q_row + row);
+                else
+                    tma_load_4d(dst + pn * C::PANEL_BYTES, tmQ, fb, pn * C::BOX_D, U.h, row, U.b);
+            }
+            ++qload[t];
+        }
+        for (int j = 0; j < nmax && ok; ++j) {
+            for (int kv = 0; kv < 2; ++kv) {
+                const int st = fill % C::NS;
+                const uint32_t rnd = fill / C::NS;
+                if (rnd > 0 && !mbar_wait(smem_u32(&bars->kv_empty[st]), (rnd - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&bars->kv_full[st]);
+                mbar_expect_tx(fb, C::TILE_BYTES);
+                const uint32_t dst = smem_u32(sKV + st * C::TILE_BYTES);
+                const CUtensorMap *m = kv ? tmV : tmK;
+#pragma unroll
+                for (int pn = 0; pn < C::PANELS; ++pn) {
+                    if (p.varlen)
+                        tma_load_3d(dst + pn * C::PANEL_BYTES, m, fb, pn * C::BOX_D, U.g,
+                                    U.k_row + j * kTile);
+                    else
+                        tma_load_4d(dst + pn * C::PANEL_BYTES, m, fb, pn * C::BOX_D, U.g, j * kTile, U.b);
+                }
+                ++fill;
+            }
+        }
+    }
+    if (ok) {
+        // every stage's last release and every Q tile's last release must have
+        // arrived before the CTA may exit
+        for (int st = 0; st < C::NS; ++st) {
+            const uint32_t nf = fill > (uint32_t)st ? (fill - st + C::NS - 1) / C::NS : 0;
+            if (nf && !mbar_wait(smem_u32(&bars->kv_empty[st]), (nf - 1) & 1, abort_flag)) break;
+        }
+        for (int t = 0; t < 2; ++t)
+            if (qload[t] && !mbar_wait(smem_u32(&bars->q_empty[t]), (qload[t] - 1) & 1, abort_flag))
+                break;
+    } else {
+        // aborted: let the copies already issued land before the CTA exits
+        const uint32_t first = fill > (uint32_t)C::NS ? fill - C::NS : 0;
+        for (uint32_t f = first; f < fill; ++f)
+            mbar_wait_drain(smem_u32(&bars->kv_full[f % C::NS]), (f / C::NS) & 1);
+        for (int t = 0; t < 2; ++t)
+            if (qload[t]) mbar_wait_drain(smem_u32(&bars->q_full[t]), (qload[t] - 1) & 1);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (one lane)
+// ---------------------------------------------------------------------------
+
+template <class C>
+__device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bars, uint32_t tmem) {
+    volatile int *abort_flag = &bars->abort;
+    constexpr uint32_t kIdS = C::idesc(kTile, false);
+    constexpr uint32_t kIdPV = C::idesc(C::D, true);
+    const uint32_t sq_addr = smem_u32(sQ), skv_addr = smem_u32(sKV);
+    uint32_t cons = 0, qc[2] = {0, 0}, pc[2] = {0, 0};
+    bool ok = true;
+    Cursor cur;
+
+    // S_t = Q_t K^T: both operands K-major; each k-step advances 32 bytes
+    // within a 128-byte swizzled panel row, then moves to the next panel.
+    auto issue_s = [&](int t, int st) {
+        const uint32_t d = tmem + (t ? C::S_COL1 : C::S_COL0);
+        const uint32_t qa = sq_addr + t * C::TILE_BYTES, ka = skv_addr + st * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+            const uint32_t off =
+                (kk * C::KSTEP_BYTES / C::SW) * C::PANEL_BYTES + (kk * C::KSTEP_BYTES) % C::SW;
+            mma_ss<C::FP8>(d, smem_desc(qa + off, 16, C::SBO, C::SW_CODE),
+                           smem_desc(ka + off, 16, C::SBO, C::SW_CODE), kIdS, kk > 0 ? 1u : 0u);
+        }
+    };
+    // O_t (+)= P_t V: P from TMEM (aliasing S_t), V MN-major (keys are the K
+    // dimension, head dim the N dimension spread over PANELS panels).
+    auto issue_pv = [&](int t, int st, bool acc) {
+        const uint32_t d = tmem + (t ? C::O_COL1 : C::O_COL0);
+        const uint32_t a = tmem + (t ? C::S_COL1 : C::S_COL0);
+        const uint32_t va = skv_addr + st * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+            mma_ts<C::FP8>(d, a + kk * (C::MMA_K * C::E / 4),
+                           smem_desc(va + kk * C::MMA_K * C::SW, C::PANEL_BYTES, C::SBO, C::SW_CODE),
+                           kIdPV, (acc || kk > 0) ? 1u : 0u);
+        }
+    };
+    auto next_kv = [&](int &st) -> bool {
+        st = cons % C::NS;
+        const bool r = mbar_wait(smem_u32(&bars->kv_full[st]), (cons / C::NS) & 1, abort_flag);
+        ++cons;
+        if (r) tc_fence_after();
+        return r;
+    };
+    auto wait_p = [&](int t) -> bool {
+        const bool r = mbar_wait(smem_u32(&bars->p_full[t]), pc[t] & 1, abort_flag);
+        ++pc[t];
+        if (r) tc_fence_after();
+        return r;
+    };
+
+    for (int u = blockIdx.x; ok; u += gridDim.x) {
+        Unit U;
+        if (!decode_unit(p, u, cur, U)) break;
+        const int n0 = U.n[0], n1 = U.n[1];
+        const int nmax = imax(n0, n1);
+        if (nmax == 0) continue;
+        for (int t = 0; t < 2 && ok; ++t) {
+            if (U.n[t] == 0) continue;
+            ok = mbar_wait(smem_u32(&bars->q_full[t]), qc[t] & 1, abort_flag);
+            ++qc[t];
+        }
+        if (!ok) break;
+        tc_fence_after();
+        int kst;
+        if (!next_kv(kst)) { ok = false; break; }
+        for (int t = 0; t < 2; ++t) {
+            if (U.n[t] == 0) continue;
+            issue_s(t, kst);
+            tc_commit(smem_u32(&bars->s_full[t]));
+            if (U.n[t] == 1) tc_commit(smem_u32(&bars->q_empty[t]));
+        }
+        tc_commit(smem_u32(&bars->kv_empty[kst]));
+        for (int j = 0; j < nmax; ++j) {
+            int vst, nst = 0;
+            if (!next_kv(vst)) { ok = false; break; }
+            const bool has_next = j + 1 < nmax;
+            if (j < n0) {
+                if (!wait_p(0)) { ok = false; break; }
+                issue_pv(0, vst, j > 0);
+                if (j == n0 - 1) tc_commit(smem_u32(&bars->o_full[0]));
+            }
+            if (has_next && !next_kv(nst)) { ok = false; break; }
+            if (j + 1 < n0) {
+                issue_s(0, nst);
+                tc_commit(smem_u32(&bars->s_full[0]));
+                if (j + 2 == n0) tc_commit(smem_u32(&bars->q_empty[0]));
+            }
+            if (j < n1) {
+                if (!wait_p(1)) { ok = false; break; }
+                issue_pv(1, vst, j > 0);
+                if (j == n1 - 1) tc_commit(smem_u32(&bars->o_full[1]));
+            }
+            tc_commit(smem_u32(&bars->kv_empty[vst]));
+            if (j + 1 < n1) {
+                issue_s(1, nst);
+                tc_commit(smem_u32(&bars->s_full[1]));
+                if (j + 2 == n1) tc_commit(smem_u32(&bars->q_empty[1]));
+            }
+            if (has_next) tc_commit(smem_u32(&bars->kv_empty[nst]));
+        }
+    }
+    // no tensor-core operation may be in flight when TMEM is released
+    tc_commit(smem_u32(&bars->drain));
+    mbar_wait_drain(smem_u32(&bars->drain), 0);
+}
+
+// ---------------------------------------------------------------------------
+// Softmax warpgroups (one thread per query row) and the epilogue
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    const bool r = mbar_wait(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, r);
+}
+
+template <class C>
+__device__ __forceinline__ void rescale_o(uint32_t o_tm, float alpha) {
+#pragma unroll 1
+    for (int ch = 0; ch < C::D / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(o_tm + 32 * ch, r);
+        tmem_wait_ld(r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+        tmem_st32(o_tm + 32 * ch, r);
+    }
+    tmem_wait_st();
+}
+
+template <class C>
+__device__ __forceinline__ void store_chunk(uint8_t *dst, const uint32_t (&r)[32], float inv) {
+    if constexpr (C::FP8) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            w[i] = pack4_e4m3(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                              __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    } else {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            w[i] = pack2<C::ELEM>(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
+}
+
+template <class C>
+__device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp, int lane) {
+    volatile int *abort_flag = &bars->abort;
+    const int t = warp >> 2, wq = warp & 3;
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t s_tm = lane_base + (t ? C::S_COL1 : C::S_COL0);
+    const uint32_t o_tm = lane_base + (t ? C::O_COL1 : C::O_COL0);
+    const uint32_t s_bar = smem_u32(&bars->s_full[t]);
+    const uint32_t p_bar = smem_u32(&bars->p_full[t]);
+    const uint32_t o_bar = smem_u32(&bars->o_full[t]);
+    const float c = p.scale * kLog2e;          // scores in log2 units: s * scale * log2(e)
+    const bool causal = p.mask == FMHA_MASK_CAUSAL;
+    uint32_t s_ph = 0, o_ph = 0;
+    bool ok = true;
+    Cursor cur;
+    for (int u = blockIdx.x; ok; u += gridDim.x) {
+        Unit U;
+        if (!decode_unit(p, u, cur, U)) break;
+        const int n = U.n[t], nu = U.nu[t];
+        const int row = U.q0 + t * kTile + wq * 32 + lane;      // query row within the sequence
+        // keys [0, key_end) are visible to this row
+        int key_end = U.sk;
+        if (causal) key_end = imin(key_end, row + 1 + (p.causal_type == FMHA_CAUSAL_QEND ? U.sk - U.sq : 0));
+        float m_ref = -INFINITY;   // reference max (log2 units) that P and O are relative to
+        float l = 0.f;             // running sum of P
+        for (int j = 0; j < n; ++j) {
+            if (!warp_wait(s_bar, s_ph, abort_flag)) { ok = false; break; }
+            s_ph ^= 1;
+            tc_fence_after();
+            float s[kTile];
+            {
+                uint32_t r0[32], r1[32], r2[32], r3[32];
+                tmem_ld32(s_tm, r0);
+                tmem_ld32(s_tm + 32, r1);
+                tmem_ld32(s_tm + 64, r2);
+                tmem_ld32(s_tm + 96, r3);
+                tmem_wait_ld(r0);
+                tmem_wait_ld(r1);
+                tmem_wait_ld(r2);
+                tmem_wait_ld(r3);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    s[i] = __uint_as_float(r0[i]);
+                    s[32 + i] = __uint_as_float(r1[i]);
+                    s[64 + i] = __uint_as_float(r2[i]);
+                    s[96 + i] = __uint_as_float(r3[i]);
+                }
+            }
+            if (j >= nu) {                                   // boundary tile: apply the mask
+                const int lim = key_end - j * kTile;
+#pragma unroll
+                for (int i = 0; i < kTile; ++i)
+                    if (i >= lim) s[i] = -INFINITY;
+            }
+            float mx;
+            {
+                float m8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+                for (int i = 8; i < kTile; ++i) m8[i & 7] = fmaxf(m8[i & 7], s[i]);
+                mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            }
+            const float m_tile = mx * c;                    // scale > 0 keeps the argmax
+            const bool resc = m_tile > m_ref + kRescaleLog2;
+            float alpha = 1.f;
+            if (resc) {
+                alpha = ex2(m_ref - m_tile);                // 0 when m_ref = -inf
+                l *= alpha;
+                m_ref = m_tile;
+            }
+            const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (!C::FP8) {
+                uint32_t pk0[32], pk1[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float a = ex2(fmaf(s[2 * i], c, neg_m));
+                    const float b = ex2(fmaf(s[2 * i + 1], c, neg_m));
+                    ls[i & 3] += a + b;
+                    pk0[i] = pack2<C::ELEM>(a, b);
+                }
+                tmem_st32(s_tm, pk0);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float a = ex2(fmaf(s[64 + 2 * i], c, neg_m));
+                    const float b = ex2(fmaf(s[64 + 2 * i + 1], c, neg_m));
+                    ls[i & 3] += a + b;
+                    pk1[i] = pack2<C::ELEM>(a, b);
+                }
+                tmem_st32(s_tm + 32, pk1);
+            } else {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float a = ex2(fmaf(s[4 * i], c, neg_m));
+                    const float b = ex2(fmaf(s[4 * i + 1], c, neg_m));
+                    const float d = ex2(fmaf(s[4 * i + 2], c, neg_m));
+                    const float e = ex2(fmaf(s[4 * i + 3], c, neg_m));
+                    ls[i & 3] += (a + b) + (d + e);
+                    pk[i] = pack4_e4m3(a, b, d, e);
+                }
+                tmem_st32(s_tm, pk);
+            }
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            // O_t holds PV_t_{j-1}, complete since S_t_j was issued after it;
+            // it must be rescaled before P_t_j is published
+            if (j > 0 && __any_sync(0xffffffffu, resc)) rescale_o<C>(o_tm, alpha);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_bar);
+        }
+        if (!ok) break;
+
+        // epilogue: O = out_scale * O_acc / l, cast, store; LSE = ln(sum exp(scale s))
+        const bool have = n > 0;
+        if (have) {
+            if (!warp_wait(o_bar, o_ph, abort_flag)) { ok = false; break; }
+            o_ph ^= 1;
+            tc_fence_after();
+        }
+        const bool valid = row < U.sq;
+        const float inv = l > 0.f ? p.out_scale / l : 0.f;
+        uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) +
+                        (((int64_t)U.q_row + row) * p.H + U.h) * (int64_t)(C::D * C::E);
+#pragma unroll 1
+        for (int ch = 0; ch < C::D / 32; ++ch) {
+            uint32_t r[32];
+            if (have) {
+                tmem_ld32(o_tm + 32 * ch, r);
+                tmem_wait_ld(r);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = 0u;
+            }
+            if (valid) store_chunk<C>(orow + ch * 32 * C::E, r, inv);
+        }
+        if (valid && p.lse) {
+            const int64_t li = p.varlen ? (int64_t)U.h * p.total_length + U.q_row + row
+                                        : ((int64_t)U.b * p.H + U.h) * p.Sq + row;
+            p.lse[li] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+
+template <class C>
+__global__ void __launch_bounds__(kThreads, 1)
+    fmha_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *sQ = smem;                               // 2 Q tiles
+    uint8_t *sKV = smem + 2 * C::TILE_BYTES;          // NS K/V stages
+    Bars *bars = reinterpret_cast<Bars *>(sKV + C::NS * C::TILE_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_u32(&bars->q_full[t]), 1);
+            mbar_init(smem_u32(&bars->q_empty[t]), 1);
+            mbar_init(smem_u32(&bars->s_full[t]), 1);
+            mbar_init(smem_u32(&bars->p_full[t]), 4);   // one arrival per softmax warp
+            mbar_init(smem_u32(&bars->o_full[t]), 1);
+        }
+        mbar_init(smem_u32(&bars->drain), 1);
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(smem_u32(&bars->kv_full[s]), 1);
+            mbar_init(smem_u32(&bars->kv_empty[s]), 1);
+        }
+        bars->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp < kProducerWarp) {
+        softmax_wg<C>(p, bars, tmem, warp, lane);
+    } else if (warp == kProducerWarp) {
+        if (lane == 0) producer<C>(p, &tmQ, &tmK, &tmV, sQ, sKV, bars);
+    } else {
+        if (lane == 0) mma_issuer<C>(p, sQ, sKV, bars, tmem);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps and launch
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+int sm_count() {
+    static std::mutex mu;
+    static int cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// [rows, heads, D] (varlen, rank 3) or [batch, rows, heads, D] (rank 4) with
+// a 128-row box of one head and one swizzle panel of the head dim.
+template <class C>
+bool encode_map(CUtensorMap *m, const void *base, int heads, int rows, int batch, bool varlen) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const CUtensorMapDataType dt = C::ELEM == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : C::ELEM == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const CUtensorMapSwizzle sw = C::SW == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : C::SW == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                : CU_TENSOR_MAP_SWIZZLE_32B;
+    const cuuint64_t row_bytes = (cuuint64_t)C::D * C::E;
+    cuuint64_t dims[4] = {(cuuint64_t)C::D, (cuuint64_t)heads, (cuuint64_t)imax(rows, 1), (cuuint64_t)batch};
+    cuuint64_t strides[3] = {row_bytes, row_bytes * heads, row_bytes * heads * (cuuint64_t)imax(rows, 1)};
+    cuuint32_t box[4] = {(cuuint32_t)C::BOX_D, 1, (cuuint32_t)kTile, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = fn(m, dt, varlen ? 3 : 4, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <class C>
+int launch_cfg(const Params &p, cudaStream_t stream) {
+    CUtensorMap tq, tk, tv;
+    const int rq = p.varlen ? (int)p.total_length : p.Sq;
+    const int rk = p.varlen ? (int)p.total_length : p.Sk;
+    const int nb = p.varlen ? 1 : p.B;
+    if (!encode_map<C>(&tq, p.q, p.H, rq, nb, p.varlen) || !encode_map<C>(&tk, p.k, p.H_k, rk, nb, p.varlen) ||
+        !encode_map<C>(&tv, p.v, p.H_k, rk, nb, p.varlen))
+        return FMHA_ERR_CUDA;
+    const int nsm = sm_count();
+    if (nsm <= 0) return FMHA_ERR_CUDA;
+    int64_t units;
+    if (p.varlen)
+        units = (int64_t)p.H * (p.B + p.total_length / kUnitRows + 1);   // upper bound
+    else
+        units = (int64_t)p.B * p.H * ((p.Sq + kUnitRows - 1) / kUnitRows);
+    const int grid = (int)(units < nsm ? units : nsm);
+    if (grid <= 0) return FMHA_OK;
+    auto kern = fmha_fwd_sm103_kernel<C>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess) {
+        cudaGetLastError();
+        return FMHA_ERR_CUDA;
+    }
+    kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+    if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
+    return FMHA_OK;
+}
+
+template <int D>
+int launch_d(const Params &p, cudaStream_t stream) {
+    switch (p.dtype) {
+    case FMHA_BF16: return launch_cfg<Cfg<D, kBF16>>(p, stream);
+    case FMHA_F16: return launch_cfg<Cfg<D, kF16>>(p, stream);
+    case FMHA_E4M3: return launch_cfg<Cfg<D, kE4M3>>(p, stream);
+    default: return FMHA_ERR_INVALID_ARG;
+    }
+}
+
+}  // namespace
+
+int launch_sm103(const Params &p, cudaStream_t stream) {
+    switch (p.D) {
+    case 32: return launch_d<32>(p, stream);
+    case 64: return launch_d<64>(p, stream);
+    case 128: return launch_d<128>(p, stream);
+    default: return FMHA_ERR_INVALID_ARG;
+    }
+}
 
 int sm103_read_status(int reset) {
     int v = 0;
@@ -23,7 +952,5 @@ int sm103_read_status(int reset) {
     }
     return v;
 }
-
-int launch_sm103(const Params &p, cudaStream_t stream) { return launch_simt(p, stream); }
 
 }  // namespace fmha
