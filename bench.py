@@ -294,8 +294,8 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
 
     inp0 = wl.generate(w)
-    set_bytes = sum(inp0.q.numel() * inp0.q.element_size() * 2 + t.numel() * t.element_size()
-                    for t in (inp0.k, inp0.v))
+    set_bytes = 2 * inp0.q.numel() * inp0.q.element_size() + sum(
+        t.numel() * t.element_size() for t in (inp0.k, inp0.v))          # Q, O, K, V
     # inputs larger than L2: alternate two input sets so that no step finds the
     # previous step's K/V in L2; smaller inputs: flush L2 before every launch
     n_sets = 2 if set_bytes >= L2_BYTES else 1

@@ -47,7 +47,7 @@ constexpr int kTile = 128;                 // query rows per Q tile, keys per K/
 constexpr int kUnitRows = 2 * kTile;       // query rows per work unit
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kThreads = 320;              // softmax warps 0-7, producer warp 8, MMA warp 9
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;
 constexpr unsigned long long kDrainNs = 200000000ull;
@@ -274,6 +274,35 @@ __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Packed pairs of fp32 (one 64-bit register pair) for the f32x2 FMA / add.
+__device__ __forceinline__ uint64_t pack_f2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ void unpack_f2(uint64_t v, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -336,6 +365,13 @@ struct Unit {
     int q_row, k_row;     // row of the sequence's first token in the stored tensors
     int n[2], nu[2];      // per Q tile: key tiles to visit / of which unmasked
 };
+
+// Unit taken by this CTA in round r: CTAs sweep the (heaviest-first) unit
+// list in alternating directions, which balances causal work to within a
+// fraction of a unit without a shared work counter.
+__device__ __forceinline__ int unit_of_round(int r) {
+    return r * gridDim.x + ((r & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
+}
 
 struct Cursor {           // varlen: sequence holding the last decoded unit
     int b = 0, base = 0;  // and the index of its first unit
@@ -404,9 +440,9 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
     uint32_t fill = 0, qload[2] = {0, 0};
     bool ok = true;
     Cursor cur;
-    for (int u = blockIdx.x; ok; u += gridDim.x) {
+    for (int r = 0; ok; ++r) {
         Unit U;
-        if (!decode_unit(p, u, cur, U)) break;
+        if (!decode_unit(p, unit_of_round(r), cur, U)) break;
         const int nmax = imax(U.n[0], U.n[1]);
         for (int t = 0; t < 2; ++t) {
             if (U.n[t] == 0) continue;
@@ -526,9 +562,9 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
         return r;
     };
 
-    for (int u = blockIdx.x; ok; u += gridDim.x) {
+    for (int r = 0; ok; ++r) {
         Unit U;
-        if (!decode_unit(p, u, cur, U)) break;
+        if (!decode_unit(p, unit_of_round(r), cur, U)) break;
         const int n0 = U.n[0], n1 = U.n[1];
         const int nmax = imax(n0, n1);
         if (nmax == 0) continue;
@@ -642,9 +678,9 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
     uint32_t s_ph = 0, o_ph = 0;
     bool ok = true;
     Cursor cur;
-    for (int u = blockIdx.x; ok; u += gridDim.x) {
+    for (int r = 0; ok; ++r) {
         Unit U;
-        if (!decode_unit(p, u, cur, U)) break;
+        if (!decode_unit(p, unit_of_round(r), cur, U)) break;
         const int n = U.n[t], nu = U.nu[t];
         const int row = U.q0 + t * kTile + wq * 32 + lane;      // query row within the sequence
         // keys [0, key_end) are visible to this row
@@ -687,9 +723,11 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
 #pragma unroll
                 for (int i = 0; i < 8; ++i) m8[i] = s[i];
 #pragma unroll
-                for (int i = 8; i < kTile; ++i) m8[i & 7] = fmaxf(m8[i & 7], s[i]);
-                mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                for (int i = 8; i < kTile; i += 16) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) m8[k] = max3(m8[k], s[i + k], s[i + 8 + k]);
+                }
+                mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
             }
             const float m_tile = mx * c;                    // scale > 0 keeps the argmax
             const bool resc = m_tile > m_ref + kRescaleLog2;
@@ -700,39 +738,48 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
                 m_ref = m_tile;
             }
             const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            // p = exp2(s * c - m_ref) two at a time: one f32x2 FMA, two ex2,
+            // one f32x2 add into the row sum, one pack
+            const uint64_t c2 = pack_f2(c, c), nm2 = pack_f2(neg_m, neg_m);
+            uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};
             if constexpr (!C::FP8) {
-                uint32_t pk0[32], pk1[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float a = ex2(fmaf(s[2 * i], c, neg_m));
-                    const float b = ex2(fmaf(s[2 * i + 1], c, neg_m));
-                    ls[i & 3] += a + b;
-                    pk0[i] = pack2<C::ELEM>(a, b);
-                }
-                tmem_st32(s_tm, pk0);
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float a = ex2(fmaf(s[64 + 2 * i], c, neg_m));
-                    const float b = ex2(fmaf(s[64 + 2 * i + 1], c, neg_m));
-                    ls[i & 3] += a + b;
-                    pk1[i] = pack2<C::ELEM>(a, b);
+                    for (int i = 0; i < 32; ++i) {
+                        float a, b;
+                        unpack_f2(fma_f2(pack_f2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]), c2, nm2), a, b);
+                        a = ex2(a);
+                        b = ex2(b);
+                        ls[i & 3] = add_f2(ls[i & 3], pack_f2(a, b));
+                        pk[i] = pack2<C::ELEM>(a, b);
+                    }
+                    tmem_st32(s_tm + 32 * half, pk);
                 }
-                tmem_st32(s_tm + 32, pk1);
             } else {
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float a = ex2(fmaf(s[4 * i], c, neg_m));
-                    const float b = ex2(fmaf(s[4 * i + 1], c, neg_m));
-                    const float d = ex2(fmaf(s[4 * i + 2], c, neg_m));
-                    const float e = ex2(fmaf(s[4 * i + 3], c, neg_m));
-                    ls[i & 3] += (a + b) + (d + e);
+                    float a, b, d, e;
+                    unpack_f2(fma_f2(pack_f2(s[4 * i], s[4 * i + 1]), c2, nm2), a, b);
+                    unpack_f2(fma_f2(pack_f2(s[4 * i + 2], s[4 * i + 3]), c2, nm2), d, e);
+                    a = ex2(a);
+                    b = ex2(b);
+                    d = ex2(d);
+                    e = ex2(e);
+                    ls[(2 * i) & 3] = add_f2(ls[(2 * i) & 3], pack_f2(a, b));
+                    ls[(2 * i + 1) & 3] = add_f2(ls[(2 * i + 1) & 3], pack_f2(d, e));
                     pk[i] = pack4_e4m3(a, b, d, e);
                 }
                 tmem_st32(s_tm, pk);
             }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            {
+                const uint64_t t2 = add_f2(add_f2(ls[0], ls[1]), add_f2(ls[2], ls[3]));
+                float a, b;
+                unpack_f2(t2, a, b);
+                l += a + b;
+            }
             // O_t holds PV_t_{j-1}, complete since S_t_j was issued after it;
             // it must be rescaled before P_t_j is published
             if (j > 0 && __any_sync(0xffffffffu, resc)) rescale_o<C>(o_tm, alpha);
