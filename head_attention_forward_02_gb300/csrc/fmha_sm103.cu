@@ -22,6 +22,8 @@
 //    each softmax warpgroup the time of two GEMMs to produce P, and makes
 //    "S_t_j complete" imply "PV_t_{j-1} complete", so the softmax warps may
 //    rescale O_t in TMEM before publishing P_t_j without another barrier.
+//    (Two issuing lanes, one per tile, were measured slower: the tensor pipe
+//    then interleaves the tiles and S_t completes later.)
 //
 // Every wait is bounded: after kTimeoutNs the waiting thread records
 // FMHA_ERR_TIMEOUT in g_status, raises a CTA-wide abort flag, and all roles
@@ -232,6 +234,60 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint64_t swz) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (swz << 61);
+}
+
+// The same descriptor split in two 32-bit words.  The low word holds the
+// start address (16-byte units, 14 bits) and the leading byte offset; adding
+// (bytes >> 4) to it moves the start address without touching anything else
+// as long as the address stays in the 256 KB window, which shared memory does.
+__host__ __device__ constexpr uint32_t desc_hi(uint32_t sbo, uint32_t swz) {
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (swz << 29);
+}
+
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+
+// D[tmem] (+)= A[smem] * B[smem], descriptors given as (low word, shared high word)
+template <bool FP8>
+__device__ __forceinline__ void mma_ss_w(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc,
+                                         uint32_t acc) {
+    if constexpr (FP8) {
+        asm volatile(
+            "{\n.reg .pred p;\n.reg .b64 da, db;\nsetp.ne.b32 p, %4, 0;\n"
+            "mov.b64 da, {%1, %3};\nmov.b64 db, {%2, %3};\n"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n}\n" ::"r"(d),
+            "r"(a_lo), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n.reg .pred p;\n.reg .b64 da, db;\nsetp.ne.b32 p, %4, 0;\n"
+            "mov.b64 da, {%1, %3};\nmov.b64 db, {%2, %3};\n"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d),
+            "r"(a_lo), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
+            : "memory");
+    }
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], B's descriptor given as (low word, high word)
+template <bool FP8>
+__device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a, uint32_t b_lo, uint32_t hi, uint32_t idesc,
+                                         uint32_t acc) {
+    if constexpr (FP8) {
+        asm volatile(
+            "{\n.reg .pred p;\n.reg .b64 db;\nsetp.ne.b32 p, %4, 0;\n"
+            "mov.b64 db, {%2, %3};\n"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %5, p;\n}\n" ::"r"(d),
+            "r"(a), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n.reg .pred p;\n.reg .b64 db;\nsetp.ne.b32 p, %4, 0;\n"
+            "mov.b64 db, {%2, %3};\n"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %5, p;\n}\n" ::"r"(d),
+            "r"(a), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
+            : "memory");
+    }
 }
 
 // D[tmem] (+)= A[smem] * B[smem]
@@ -517,22 +573,30 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
     volatile int *abort_flag = &bars->abort;
     constexpr uint32_t kIdS = C::idesc(kTile, false);
     constexpr uint32_t kIdPV = C::idesc(C::D, true);
-    const uint32_t sq_addr = smem_u32(sQ), skv_addr = smem_u32(sKV);
-    uint32_t cons = 0, qc[2] = {0, 0}, pc[2] = {0, 0};
+    uint32_t cons = 0, qc0 = 0, qc1 = 0, pc0 = 0, pc1 = 0;
     bool ok = true;
     Cursor cur;
+
+    // Descriptor words are computed once; each MMA then only adds a
+    // compile-time byte offset to the low word.  The issuing lane shares its
+    // SMSP with two busy softmax warps and the tensor-core queue is shallow,
+    // so every instruction between two MMA groups is time the pipe may idle.
+    constexpr uint32_t kHi = desc_hi(C::SBO, (uint32_t)C::SW_CODE);
+    constexpr uint32_t kTileStep = C::TILE_BYTES >> 4;
+    const uint32_t q_lo = desc_lo(smem_u32(sQ), 16);                 // K-major: LBO unused
+    const uint32_t k_lo = desc_lo(smem_u32(sKV), 16);
+    const uint32_t v_lo = desc_lo(smem_u32(sKV), C::PANEL_BYTES);    // MN-major: LBO = panel stride
 
     // S_t = Q_t K^T: both operands K-major; each k-step advances 32 bytes
     // within a 128-byte swizzled panel row, then moves to the next panel.
     auto issue_s = [&](int t, int st) {
         const uint32_t d = tmem + (t ? C::S_COL1 : C::S_COL0);
-        const uint32_t qa = sq_addr + t * C::TILE_BYTES, ka = skv_addr + st * C::TILE_BYTES;
+        const uint32_t a = q_lo + t * kTileStep, b = k_lo + st * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < C::QK_STEPS; ++kk) {
             const uint32_t off =
-                (kk * C::KSTEP_BYTES / C::SW) * C::PANEL_BYTES + (kk * C::KSTEP_BYTES) % C::SW;
-            mma_ss<C::FP8>(d, smem_desc(qa + off, 16, C::SBO, C::SW_CODE),
-                           smem_desc(ka + off, 16, C::SBO, C::SW_CODE), kIdS, kk > 0 ? 1u : 0u);
+                ((kk * C::KSTEP_BYTES / C::SW) * C::PANEL_BYTES + (kk * C::KSTEP_BYTES) % C::SW) >> 4;
+            mma_ss_w<C::FP8>(d, a + off, b + off, kHi, kIdS, kk > 0 ? 1u : 0u);
         }
     };
     // O_t (+)= P_t V: P from TMEM (aliasing S_t), V MN-major (keys are the K
@@ -540,24 +604,27 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
     auto issue_pv = [&](int t, int st, bool acc) {
         const uint32_t d = tmem + (t ? C::O_COL1 : C::O_COL0);
         const uint32_t a = tmem + (t ? C::S_COL1 : C::S_COL0);
-        const uint32_t va = skv_addr + st * C::TILE_BYTES;
+        const uint32_t b = v_lo + st * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-            mma_ts<C::FP8>(d, a + kk * (C::MMA_K * C::E / 4),
-                           smem_desc(va + kk * C::MMA_K * C::SW, C::PANEL_BYTES, C::SBO, C::SW_CODE),
-                           kIdPV, (acc || kk > 0) ? 1u : 0u);
+            mma_ts_w<C::FP8>(d, a + kk * (C::MMA_K * C::E / 4), b + ((kk * C::MMA_K * C::SW) >> 4), kHi, kIdPV,
+                             (acc || kk > 0) ? 1u : 0u);
         }
     };
+    // TMA writes and tensor-core reads of shared memory are both async-proxy
+    // operations ordered by the mbarrier: no tcgen05 fence is needed here.
     auto next_kv = [&](int &st) -> bool {
         st = cons % C::NS;
         const bool r = mbar_wait(smem_u32(&bars->kv_full[st]), (cons / C::NS) & 1, abort_flag);
         ++cons;
-        if (r) tc_fence_after();
         return r;
     };
+    // P_t was written to TMEM by the softmax threads (tcgen05.st): order this
+    // thread's MMAs after their fence::before_thread_sync + arrive.
     auto wait_p = [&](int t) -> bool {
-        const bool r = mbar_wait(smem_u32(&bars->p_full[t]), pc[t] & 1, abort_flag);
-        ++pc[t];
+        uint32_t &pc = t ? pc1 : pc0;
+        const bool r = mbar_wait(smem_u32(&bars->p_full[t]), pc & 1, abort_flag);
+        ++pc;
         if (r) tc_fence_after();
         return r;
     };
@@ -568,20 +635,28 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
         const int n0 = U.n[0], n1 = U.n[1];
         const int nmax = imax(n0, n1);
         if (nmax == 0) continue;
-        for (int t = 0; t < 2 && ok; ++t) {
-            if (U.n[t] == 0) continue;
-            ok = mbar_wait(smem_u32(&bars->q_full[t]), qc[t] & 1, abort_flag);
-            ++qc[t];
+        if (n0 > 0) {
+            ok = mbar_wait(smem_u32(&bars->q_full[0]), qc0 & 1, abort_flag);
+            ++qc0;
+        }
+        if (ok && n1 > 0) {
+            ok = mbar_wait(smem_u32(&bars->q_full[1]), qc1 & 1, abort_flag);
+            ++qc1;
         }
         if (!ok) break;
-        tc_fence_after();
+        // the previous unit's epilogue read O_t from TMEM before its softmax
+        // warps published this unit's first P_t, so no wait is needed here
         int kst;
         if (!next_kv(kst)) { ok = false; break; }
-        for (int t = 0; t < 2; ++t) {
-            if (U.n[t] == 0) continue;
-            issue_s(t, kst);
-            tc_commit(smem_u32(&bars->s_full[t]));
-            if (U.n[t] == 1) tc_commit(smem_u32(&bars->q_empty[t]));
+        if (n0 > 0) {
+            issue_s(0, kst);
+            tc_commit(smem_u32(&bars->s_full[0]));
+            if (n0 == 1) tc_commit(smem_u32(&bars->q_empty[0]));
+        }
+        if (n1 > 0) {
+            issue_s(1, kst);
+            tc_commit(smem_u32(&bars->s_full[1]));
+            if (n1 == 1) tc_commit(smem_u32(&bars->q_empty[1]));
         }
         tc_commit(smem_u32(&bars->kv_empty[kst]));
         for (int j = 0; j < nmax; ++j) {
@@ -625,6 +700,102 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
     const bool r = mbar_wait(bar, parity, abort_flag);
     return __all_sync(0xffffffffu, r);
+}
+
+// This thread's row of S_t (128 fp32 columns of its TMEM lane).
+__device__ __forceinline__ void load_s(uint32_t s_tm, float (&s)[kTile]) {
+    uint32_t r0[32], r1[32], r2[32], r3[32];
+    tmem_ld32(s_tm, r0);
+    tmem_ld32(s_tm + 32, r1);
+    tmem_ld32(s_tm + 64, r2);
+    tmem_ld32(s_tm + 96, r3);
+    tmem_wait_ld(r0);
+    tmem_wait_ld(r1);
+    tmem_wait_ld(r2);
+    tmem_wait_ld(r3);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        s[i] = __uint_as_float(r0[i]);
+        s[32 + i] = __uint_as_float(r1[i]);
+        s[64 + i] = __uint_as_float(r2[i]);
+        s[96 + i] = __uint_as_float(r3[i]);
+    }
+}
+
+// Keys at local column >= lim are invisible to this row: score -inf.
+__device__ __forceinline__ void mask_s(float (&s)[kTile], int lim) {
+#pragma unroll
+    for (int i = 0; i < kTile; ++i)
+        if (i >= lim) s[i] = -INFINITY;
+}
+
+__device__ __forceinline__ float row_max(const float (&s)[kTile]) {
+    float m8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+    for (int i = 8; i < kTile; i += 16) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = max3(m8[k], s[i + k], s[i + 8 + k]);
+    }
+    return max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+}
+
+// exp2 of 64 scores (one half row) into packed P words: 32 words for 16-bit
+// types, 16 for e4m3.  Returns the fp32 sum.
+template <class C>
+__device__ __forceinline__ float exp_half(const float *x, uint64_t c2, uint64_t nm2, uint32_t *w) {
+    uint64_t ls[2] = {0ull, 0ull};
+    if constexpr (!C::FP8) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            float a, b;
+            unpack_f2(fma_f2(pack_f2(x[2 * i], x[2 * i + 1]), c2, nm2), a, b);
+            a = ex2(a);
+            b = ex2(b);
+            ls[i & 1] = add_f2(ls[i & 1], pack_f2(a, b));
+            w[i] = pack2<C::ELEM>(a, b);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float a, b, d, e;
+            unpack_f2(fma_f2(pack_f2(x[4 * i], x[4 * i + 1]), c2, nm2), a, b);
+            unpack_f2(fma_f2(pack_f2(x[4 * i + 2], x[4 * i + 3]), c2, nm2), d, e);
+            a = ex2(a);
+            b = ex2(b);
+            d = ex2(d);
+            e = ex2(e);
+            ls[0] = add_f2(ls[0], pack_f2(a, b));
+            ls[1] = add_f2(ls[1], pack_f2(d, e));
+            w[i] = pack4_e4m3(a, b, d, e);
+        }
+    }
+    float a, b;
+    unpack_f2(add_f2(ls[0], ls[1]), a, b);
+    return a + b;
+}
+
+// P from scores held in registers, stored half a row at a time (keeps the
+// register footprint low).  Returns the fp32 sum.
+template <class C>
+__device__ __forceinline__ float exp_store_regs(uint32_t s_tm, const float (&s)[kTile], float c, float neg_m) {
+    const uint64_t c2 = pack_f2(c, c), nm2 = pack_f2(neg_m, neg_m);
+    float sum = 0.f;
+    if constexpr (!C::FP8) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t w[32];
+            sum += exp_half<C>(s + 64 * h, c2, nm2, w);
+            tmem_st32(s_tm + 32 * h, w);
+        }
+    } else {
+        uint32_t w[32];
+        sum += exp_half<C>(s, c2, nm2, w);
+        sum += exp_half<C>(s + 64, c2, nm2, w + 16);
+        tmem_st32(s_tm, w);
+    }
+    return sum;
 }
 
 template <class C>
@@ -693,93 +864,17 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
             s_ph ^= 1;
             tc_fence_after();
             float s[kTile];
-            {
-                uint32_t r0[32], r1[32], r2[32], r3[32];
-                tmem_ld32(s_tm, r0);
-                tmem_ld32(s_tm + 32, r1);
-                tmem_ld32(s_tm + 64, r2);
-                tmem_ld32(s_tm + 96, r3);
-                tmem_wait_ld(r0);
-                tmem_wait_ld(r1);
-                tmem_wait_ld(r2);
-                tmem_wait_ld(r3);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    s[i] = __uint_as_float(r0[i]);
-                    s[32 + i] = __uint_as_float(r1[i]);
-                    s[64 + i] = __uint_as_float(r2[i]);
-                    s[96 + i] = __uint_as_float(r3[i]);
-                }
-            }
-            if (j >= nu) {                                   // boundary tile: apply the mask
-                const int lim = key_end - j * kTile;
-#pragma unroll
-                for (int i = 0; i < kTile; ++i)
-                    if (i >= lim) s[i] = -INFINITY;
-            }
-            float mx;
-            {
-                float m8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) m8[i] = s[i];
-#pragma unroll
-                for (int i = 8; i < kTile; i += 16) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) m8[k] = max3(m8[k], s[i + k], s[i + 8 + k]);
-                }
-                mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-            }
-            const float m_tile = mx * c;                    // scale > 0 keeps the argmax
+            load_s(s_tm, s);
+            if (j >= nu) mask_s(s, key_end - j * kTile);     // boundary tile
+            const float m_tile = row_max(s) * c;             // scale > 0 keeps the argmax
             const bool resc = m_tile > m_ref + kRescaleLog2;
             float alpha = 1.f;
             if (resc) {
-                alpha = ex2(m_ref - m_tile);                // 0 when m_ref = -inf
+                alpha = ex2(m_ref - m_tile);                 // 0 when m_ref = -inf
                 l *= alpha;
                 m_ref = m_tile;
             }
-            const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-            // p = exp2(s * c - m_ref) two at a time: one f32x2 FMA, two ex2,
-            // one f32x2 add into the row sum, one pack
-            const uint64_t c2 = pack_f2(c, c), nm2 = pack_f2(neg_m, neg_m);
-            uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};
-            if constexpr (!C::FP8) {
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float a, b;
-                        unpack_f2(fma_f2(pack_f2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]), c2, nm2), a, b);
-                        a = ex2(a);
-                        b = ex2(b);
-                        ls[i & 3] = add_f2(ls[i & 3], pack_f2(a, b));
-                        pk[i] = pack2<C::ELEM>(a, b);
-                    }
-                    tmem_st32(s_tm + 32 * half, pk);
-                }
-            } else {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float a, b, d, e;
-                    unpack_f2(fma_f2(pack_f2(s[4 * i], s[4 * i + 1]), c2, nm2), a, b);
-                    unpack_f2(fma_f2(pack_f2(s[4 * i + 2], s[4 * i + 3]), c2, nm2), d, e);
-                    a = ex2(a);
-                    b = ex2(b);
-                    d = ex2(d);
-                    e = ex2(e);
-                    ls[(2 * i) & 3] = add_f2(ls[(2 * i) & 3], pack_f2(a, b));
-                    ls[(2 * i + 1) & 3] = add_f2(ls[(2 * i + 1) & 3], pack_f2(d, e));
-                    pk[i] = pack4_e4m3(a, b, d, e);
-                }
-                tmem_st32(s_tm, pk);
-            }
-            {
-                const uint64_t t2 = add_f2(add_f2(ls[0], ls[1]), add_f2(ls[2], ls[3]));
-                float a, b;
-                unpack_f2(t2, a, b);
-                l += a + b;
-            }
+            l += exp_store_regs<C>(s_tm, s, c, m_ref == -INFINITY ? 0.f : -m_ref);
             // O_t holds PV_t_{j-1}, complete since S_t_j was issued after it;
             // it must be rescaled before P_t_j is published
             if (j > 0 && __any_sync(0xffffffffu, resc)) rescale_o<C>(o_tm, alpha);
