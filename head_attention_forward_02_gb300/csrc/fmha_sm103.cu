@@ -429,9 +429,22 @@ __device__ __forceinline__ int unit_of_round(int r) {
     return r * gridDim.x + ((r & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
 }
 
-struct Cursor {           // varlen: sequence holding the last decoded unit
-    int b = 0, base = 0;  // and the index of its first unit
+struct Cursor {                  // varlen decoding state (units are decoded in increasing order)
+    int b = 0, base = 0;         // sequence-major order: current sequence, index of its first unit
+    bool init = false;           // block-level order (causal):
+    int q = 0, qbase = 0, qcnt = 0;  // current 256-row block index, its first unit, sequences that have it
 };
+
+// 256-row query blocks of packed sequence b
+__device__ __forceinline__ int seq_blocks(const Params &p, int b) {
+    return (p.cu_q[b + 1] - p.cu_q[b] + kUnitRows - 1) / kUnitRows;
+}
+
+__device__ __forceinline__ int seqs_with_block(const Params &p, int q) {
+    int n = 0;
+    for (int b = 0; b < p.B; ++b) n += seq_blocks(p, b) > q;
+    return n;
+}
 
 __device__ __forceinline__ bool decode_unit(const Params &p, int u, Cursor &cur, Unit &U) {
     int b, h, qb;
@@ -447,6 +460,38 @@ __device__ __forceinline__ bool decode_unit(const Params &p, int u, Cursor &cur,
         U.sk = p.Sk;
         U.q_row = b * p.Sq;
         U.k_row = b * p.Sk;
+    } else if (p.mask == FMHA_MASK_CAUSAL) {
+        // Causal work grows with the block index, so units go block level by
+        // block level, deepest first, across all sequences (heaviest first).
+        if (!cur.init) {
+            int mx = 0;
+            for (int bb = 0; bb < p.B; ++bb) mx = imax(mx, seq_blocks(p, bb));
+            cur.init = true;
+            cur.q = mx - 1;
+            cur.qbase = 0;
+            cur.qcnt = cur.q >= 0 ? seqs_with_block(p, cur.q) : 0;
+        }
+        while (cur.q >= 0 && u >= cur.qbase + cur.qcnt * p.H) {
+            cur.qbase += cur.qcnt * p.H;
+            --cur.q;
+            cur.qcnt = cur.q >= 0 ? seqs_with_block(p, cur.q) : 0;
+        }
+        if (cur.q < 0) return false;
+        const int rem = u - cur.qbase;
+        int k = rem / p.H;
+        h = rem - k * p.H;
+        b = 0;
+        for (int bb = 0; bb < p.B; ++bb) {
+            if (seq_blocks(p, bb) > cur.q) {
+                if (k == 0) { b = bb; break; }
+                --k;
+            }
+        }
+        qb = cur.q;
+        U.q_row = p.cu_q[b];
+        U.sq = p.cu_q[b + 1] - U.q_row;
+        U.k_row = p.cu_k[b];
+        U.sk = p.cu_k[b + 1] - U.k_row;
     } else {
         int bb = cur.b, base = cur.base;
         for (;;) {
@@ -455,8 +500,7 @@ __device__ __forceinline__ bool decode_unit(const Params &p, int u, Cursor &cur,
                 cur.base = base;
                 return false;
             }
-            const int lq = p.cu_q[bb + 1] - p.cu_q[bb];
-            const int cnt = ((lq + kUnitRows - 1) / kUnitRows) * p.H;
+            const int cnt = seq_blocks(p, bb) * p.H;
             if (u < base + cnt) break;
             base += cnt;
             ++bb;
