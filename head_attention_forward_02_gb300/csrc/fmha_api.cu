@@ -13,6 +13,8 @@ namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+}  // namespace
+
 // Is the current device an sm_103 part?  Cached per device ordinal.
 int check_device() {
     static std::mutex mu;
@@ -43,7 +45,8 @@ int make_params(Params &p, fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_ten
     if (mask < FMHA_MASK_NONE || mask > FMHA_MASK_CAUSAL) return FMHA_ERR_INVALID_ARG;
     if (causal_type != FMHA_CAUSAL_QBEGIN && causal_type != FMHA_CAUSAL_QEND)
         return FMHA_ERR_INVALID_ARG;
-    if (!isfinite(scale) || !isfinite(out_scale)) return FMHA_ERR_INVALID_ARG;
+    // scale > 0: the kernels take the row max of raw scores before scaling
+    if (!isfinite(scale) || !(scale > 0.f) || !isfinite(out_scale)) return FMHA_ERR_INVALID_ARG;
     if ((cu_q == nullptr) != (cu_k == nullptr)) return FMHA_ERR_INVALID_ARG;
     const bool varlen = cu_q != nullptr;
     if (varlen) {
@@ -78,10 +81,11 @@ int make_params(Params &p, fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_ten
     p.total_length = varlen ? total_length : 0;
     p.varlen = varlen ? 1 : 0;
     p.dtype = q.dtype; p.odtype = o.dtype;
+    p.num_splits = 1;
+    p.part_o = nullptr; p.part_lse = nullptr; p.part_rows = 0;
     return FMHA_OK;
 }
 
-}  // namespace
 }  // namespace fmha
 
 extern "C" {

@@ -26,6 +26,13 @@ struct Params {
     int64_t total_length;
     int varlen;
     int dtype, odtype;
+    // split-KV mode (num_splits > 1 or part_o set): each work unit's key
+    // tiles are cut into num_splits contiguous ranges whose normalised fp32
+    // partial O [num_splits][part_rows][H][D] and LSE [num_splits][part_rows][H]
+    // go to part_o / part_lse instead of o / lse.
+    int num_splits;
+    float *part_o, *part_lse;
+    int64_t part_rows;
 };
 
 FMHA_HD int imin(int a, int b) { return a < b ? a : b; }
@@ -58,9 +65,17 @@ FMHA_HD void kv_tile_range(int row0, int rows, int sq, int sk, int mask, int cau
     *n_unmasked = nu;
 }
 
-// Launchers, one per translation unit.  They assume validated parameters.
+// Argument validation shared by the entry points (fmha_api.cu).  Returns
+// FMHA_OK, an error status, or 1 when there is nothing to compute.
+int make_params(Params &p, fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor o, float *lse,
+                int B, int H, int H_k, int Sq, int Sk, int D, float scale, float out_scale, int mask,
+                int causal_type, const int *cu_q, const int *cu_k, int max_len, int64_t total_length);
+int check_device();
+
+// Launchers.  They assume validated parameters.
 int launch_simt(const Params &p, cudaStream_t stream);
 int launch_sm103(const Params &p, cudaStream_t stream);
+int launch_combine(const Params &p, cudaStream_t stream);
 int sm103_read_status(int reset);
 
 }  // namespace fmha

@@ -419,7 +419,9 @@ struct Unit {
     int b, h, g, q0;      // batch, query head, kv head, first query row of the unit
     int sq, sk;           // sequence lengths
     int q_row, k_row;     // row of the sequence's first token in the stored tensors
-    int n[2], nu[2];      // per Q tile: key tiles to visit / of which unmasked
+    int n[2], nu[2];      // per Q tile: end of its key tiles in this work item / unmasked ones
+    int j0, j1;           // key tiles [j0, j1) of this work item (split-KV: one range of several)
+    int split;            // split index (0 without split-KV)
 };
 
 // Unit taken by this CTA in round r: CTAs sweep the (heaviest-first) unit
@@ -526,11 +528,28 @@ __device__ __forceinline__ bool decode_unit(const Params &p, int u, Cursor &cur,
     return true;
 }
 
+// Work item u = unit u / num_splits, key range number u % num_splits: the
+// unit's key tiles [0, max(n0, n1)) are cut into num_splits near-equal
+// contiguous ranges; tile t then covers [j0, min(n_t, j1)) and is active
+// when that range is not empty.  Without split-KV, j0 = 0 and j1 = max(n0, n1).
+template <bool SPLIT>
+__device__ __forceinline__ bool decode_work(const Params &p, int u, Cursor &cur, Unit &U) {
+    const int ns = SPLIT ? p.num_splits : 1;      // a constant 1 folds the split arithmetic away
+    if (!decode_unit(p, u / ns, cur, U)) return false;
+    const int nmax = imax(U.n[0], U.n[1]);
+    U.split = u % ns;
+    U.j0 = (int)((int64_t)nmax * U.split / ns);
+    U.j1 = (int)((int64_t)nmax * (U.split + 1) / ns);
+    U.n[0] = imin(U.n[0], U.j1);
+    U.n[1] = imin(U.n[1], U.j1);
+    return true;
+}
+
 // ---------------------------------------------------------------------------
 // Producer: Q tiles and the K/V ring, by TMA (one lane)
 // ---------------------------------------------------------------------------
 
-template <class C>
+template <class C, bool SPLIT>
 __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensorMap *tmK,
                          const CUtensorMap *tmV, uint8_t *sQ, uint8_t *sKV, Bars *bars) {
     volatile int *abort_flag = &bars->abort;
@@ -542,10 +561,9 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
     Cursor cur;
     for (int r = 0; ok; ++r) {
         Unit U;
-        if (!decode_unit(p, unit_of_round(r), cur, U)) break;
-        const int nmax = imax(U.n[0], U.n[1]);
+        if (!decode_work<SPLIT>(p, unit_of_round(r), cur, U)) break;
         for (int t = 0; t < 2; ++t) {
-            if (U.n[t] == 0) continue;
+            if (U.n[t] <= U.j0) continue;                 // tile inactive in this work item
             if (qload[t] > 0 &&
                 !mbar_wait(smem_u32(&bars->q_empty[t]), (qload[t] - 1) & 1, abort_flag)) {
                 ok = false;
@@ -564,7 +582,7 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
             }
             ++qload[t];
         }
-        for (int j = 0; j < nmax && ok; ++j) {
+        for (int j = U.j0; j < U.j1 && ok; ++j) {
             for (int kv = 0; kv < 2; ++kv) {
                 const int st = fill % C::NS;
                 const uint32_t rnd = fill / C::NS;
@@ -612,7 +630,7 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
 // MMA issuer (one lane)
 // ---------------------------------------------------------------------------
 
-template <class C>
+template <class C, bool SPLIT>
 __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bars, uint32_t tmem) {
     volatile int *abort_flag = &bars->abort;
     constexpr uint32_t kIdS = C::idesc(kTile, false);
@@ -675,15 +693,14 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
 
     for (int r = 0; ok; ++r) {
         Unit U;
-        if (!decode_unit(p, unit_of_round(r), cur, U)) break;
-        const int n0 = U.n[0], n1 = U.n[1];
-        const int nmax = imax(n0, n1);
-        if (nmax == 0) continue;
-        if (n0 > 0) {
+        if (!decode_work<SPLIT>(p, unit_of_round(r), cur, U)) break;
+        const int n0 = U.n[0], n1 = U.n[1], j0 = U.j0, jn = U.j1;
+        if (j0 >= jn) continue;
+        if (n0 > j0) {
             ok = mbar_wait(smem_u32(&bars->q_full[0]), qc0 & 1, abort_flag);
             ++qc0;
         }
-        if (ok && n1 > 0) {
+        if (ok && n1 > j0) {
             ok = mbar_wait(smem_u32(&bars->q_full[1]), qc1 & 1, abort_flag);
             ++qc1;
         }
@@ -692,24 +709,24 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
         // warps published this unit's first P_t, so no wait is needed here
         int kst;
         if (!next_kv(kst)) { ok = false; break; }
-        if (n0 > 0) {
+        if (n0 > j0) {
             issue_s(0, kst);
             tc_commit(smem_u32(&bars->s_full[0]));
-            if (n0 == 1) tc_commit(smem_u32(&bars->q_empty[0]));
+            if (n0 == j0 + 1) tc_commit(smem_u32(&bars->q_empty[0]));
         }
-        if (n1 > 0) {
+        if (n1 > j0) {
             issue_s(1, kst);
             tc_commit(smem_u32(&bars->s_full[1]));
-            if (n1 == 1) tc_commit(smem_u32(&bars->q_empty[1]));
+            if (n1 == j0 + 1) tc_commit(smem_u32(&bars->q_empty[1]));
         }
         tc_commit(smem_u32(&bars->kv_empty[kst]));
-        for (int j = 0; j < nmax; ++j) {
+        for (int j = j0; j < jn; ++j) {
             int vst, nst = 0;
             if (!next_kv(vst)) { ok = false; break; }
-            const bool has_next = j + 1 < nmax;
+            const bool has_next = j + 1 < jn;
             if (j < n0) {
                 if (!wait_p(0)) { ok = false; break; }
-                issue_pv(0, vst, j > 0);
+                issue_pv(0, vst, j > j0);
                 if (j == n0 - 1) tc_commit(smem_u32(&bars->o_full[0]));
             }
             if (has_next && !next_kv(nst)) { ok = false; break; }
@@ -720,7 +737,7 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
             }
             if (j < n1) {
                 if (!wait_p(1)) { ok = false; break; }
-                issue_pv(1, vst, j > 0);
+                issue_pv(1, vst, j > j0);
                 if (j == n1 - 1) tc_commit(smem_u32(&bars->o_full[1]));
             }
             tc_commit(smem_u32(&bars->kv_empty[vst]));
@@ -878,7 +895,7 @@ __device__ __forceinline__ void store_chunk(uint8_t *dst, const uint32_t (&r)[32
     }
 }
 
-template <class C>
+template <class C, bool SPLIT>
 __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp, int lane) {
     volatile int *abort_flag = &bars->abort;
     const int t = warp >> 2, wq = warp & 3;
@@ -895,15 +912,15 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
     Cursor cur;
     for (int r = 0; ok; ++r) {
         Unit U;
-        if (!decode_unit(p, unit_of_round(r), cur, U)) break;
-        const int n = U.n[t], nu = U.nu[t];
+        if (!decode_work<SPLIT>(p, unit_of_round(r), cur, U)) break;
+        const int n = U.n[t], nu = U.nu[t], j0 = U.j0;
         const int row = U.q0 + t * kTile + wq * 32 + lane;      // query row within the sequence
         // keys [0, key_end) are visible to this row
         int key_end = U.sk;
         if (causal) key_end = imin(key_end, row + 1 + (p.causal_type == FMHA_CAUSAL_QEND ? U.sk - U.sq : 0));
         float m_ref = -INFINITY;   // reference max (log2 units) that P and O are relative to
         float l = 0.f;             // running sum of P
-        for (int j = 0; j < n; ++j) {
+        for (int j = j0; j < n; ++j) {
             if (!warp_wait(s_bar, s_ph, abort_flag)) { ok = false; break; }
             s_ph ^= 1;
             tc_fence_after();
@@ -921,7 +938,7 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
             l += exp_store_regs<C>(s_tm, s, c, m_ref == -INFINITY ? 0.f : -m_ref);
             // O_t holds PV_t_{j-1}, complete since S_t_j was issued after it;
             // it must be rescaled before P_t_j is published
-            if (j > 0 && __any_sync(0xffffffffu, resc)) rescale_o<C>(o_tm, alpha);
+            if (j > j0 && __any_sync(0xffffffffu, resc)) rescale_o<C>(o_tm, alpha);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -930,13 +947,39 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
         if (!ok) break;
 
         // epilogue: O = out_scale * O_acc / l, cast, store; LSE = ln(sum exp(scale s))
-        const bool have = n > 0;
+        const bool have = n > j0;
         if (have) {
             if (!warp_wait(o_bar, o_ph, abort_flag)) { ok = false; break; }
             o_ph ^= 1;
             tc_fence_after();
         }
         const bool valid = row < U.sq;
+        if constexpr (SPLIT) {
+            // split-KV: normalised fp32 partial O and its LSE for the combine
+            const int64_t prow = ((int64_t)U.split * p.part_rows + U.q_row + row) * p.H + U.h;
+            float *po = p.part_o + prow * C::D;
+            const float pinv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+            for (int ch = 0; ch < C::D / 32; ++ch) {
+                uint32_t r[32];
+                if (have) {
+                    tmem_ld32(o_tm + 32 * ch, r);
+                    tmem_wait_ld(r);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = 0u;
+                }
+                if (valid) {
+                    float4 *d4 = reinterpret_cast<float4 *>(po + 32 * ch);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        d4[i] = make_float4(__uint_as_float(r[4 * i]) * pinv, __uint_as_float(r[4 * i + 1]) * pinv,
+                                            __uint_as_float(r[4 * i + 2]) * pinv, __uint_as_float(r[4 * i + 3]) * pinv);
+                }
+            }
+            if (valid) p.part_lse[prow] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+            continue;
+        }
         const float inv = l > 0.f ? p.out_scale / l : 0.f;
         uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) +
                         (((int64_t)U.q_row + row) * p.H + U.h) * (int64_t)(C::D * C::E);
@@ -964,7 +1007,7 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
 // The kernel
 // ---------------------------------------------------------------------------
 
-template <class C>
+template <class C, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -1001,11 +1044,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = bars->tmem_base;
 
     if (warp < kProducerWarp) {
-        softmax_wg<C>(p, bars, tmem, warp, lane);
+        softmax_wg<C, SPLIT>(p, bars, tmem, warp, lane);
     } else if (warp == kProducerWarp) {
-        if (lane == 0) producer<C>(p, &tmQ, &tmK, &tmV, sQ, sKV, bars);
+        if (lane == 0) producer<C, SPLIT>(p, &tmQ, &tmK, &tmV, sQ, sKV, bars);
     } else {
-        if (lane == 0) mma_issuer<C>(p, sQ, sKV, bars, tmem);
+        if (lane == 0) mma_issuer<C, SPLIT>(p, sQ, sKV, bars, tmem);
     }
 
     tc_fence_before();
@@ -1090,9 +1133,11 @@ int launch_cfg(const Params &p, cudaStream_t stream) {
         units = (int64_t)p.H * (p.B + p.total_length / kUnitRows + 1);   // upper bound
     else
         units = (int64_t)p.B * p.H * ((p.Sq + kUnitRows - 1) / kUnitRows);
+    units *= p.num_splits;
     const int grid = (int)(units < nsm ? units : nsm);
     if (grid <= 0) return FMHA_OK;
-    auto kern = fmha_fwd_sm103_kernel<C>;
+    // split-KV is a separate instantiation so the plain kernel keeps its code
+    auto kern = p.part_o ? fmha_fwd_sm103_kernel<C, true> : fmha_fwd_sm103_kernel<C, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
         return FMHA_ERR_CUDA;

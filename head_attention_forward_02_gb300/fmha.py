@@ -25,8 +25,8 @@ _TORCH_DTYPE = {torch.float16: F16, torch.bfloat16: BF16, torch.float8_e4m3fn: E
 _MASKS = {"none": MASK_NONE, "residual": MASK_RESIDUAL, "causal": MASK_CAUSAL}
 _CAUSAL = {"qbegin": CAUSAL_QBEGIN, "qend": CAUSAL_QEND}
 
-EXPORTED = ("fmha_fwd", "fmha_fwd_simt", "fmha_status_string", "fmha_device_status",
-            "fmha_kv_tile_range")
+EXPORTED = ("fmha_fwd", "fmha_fwd_simt", "fmha_fwd_splitkv", "fmha_fwd_splitkv_workspace_size",
+            "fmha_status_string", "fmha_device_status", "fmha_kv_tile_range")
 
 
 class fmha_tensor(ctypes.Structure):
@@ -62,6 +62,11 @@ def lib():
             f = getattr(L, name)
             f.restype = ctypes.c_int
             f.argtypes = fwd_args
+        L.fmha_fwd_splitkv.restype = ctypes.c_int
+        L.fmha_fwd_splitkv.argtypes = fwd_args[:-1] + [ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                                                       ctypes.c_void_p]
+        L.fmha_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
+        L.fmha_fwd_splitkv_workspace_size.argtypes = [ctypes.c_int] * 5 + [ctypes.c_int64]
         L.fmha_status_string.restype = ctypes.c_char_p
         L.fmha_status_string.argtypes = [ctypes.c_int]
         L.fmha_device_status.restype = ctypes.c_int
@@ -141,16 +146,36 @@ def fmha_fwd_simt(q, k, v, o, lse, B, H, H_k, Sq, Sk, D, scale, out_scale, mask,
                  causal_type, cu_seqlens_q, cu_seqlens_k, max_len, total_length, stream)
 
 
+def fmha_fwd_splitkv(q, k, v, o, lse, B, H, H_k, Sq, Sk, D, scale, out_scale, mask, causal_type,
+                     cu_seqlens_q=None, cu_seqlens_k=None, max_len=0, total_length=0,
+                     num_splits=1, workspace=None, workspace_bytes=None, stream=None) -> int:
+    """Same arguments, order and status codes as the C function fmha_fwd_splitkv."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return lib().fmha_fwd_splitkv(
+        _tensor(q), _tensor(k), _tensor(v), _tensor(o), _ptr(lse), int(B), int(H), int(H_k), int(Sq),
+        int(Sk), int(D), float(scale), float(out_scale), int(mask), int(causal_type),
+        _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(max_len), int(total_length), int(num_splits),
+        _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def fmha_fwd_splitkv_workspace_size(B, H, Sq, D, num_splits, total_length=0) -> int:
+    return int(lib().fmha_fwd_splitkv_workspace_size(int(B), int(H), int(Sq), int(D), int(num_splits),
+                                                     int(total_length)))
+
+
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Optional[float] = None,
         out_scale: float = 1.0, mask: str = "none", causal_type: str = "qbegin",
         cu_seqlens_q: Optional[torch.Tensor] = None, cu_seqlens_k: Optional[torch.Tensor] = None,
         max_len: Optional[int] = None, total_length: Optional[int] = None,
         out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-        return_lse: bool = True, impl: str = "tc", stream=None):
+        return_lse: bool = True, impl: str = "tc", num_splits: Optional[int] = None, stream=None):
     """Attention forward on device tensors; allocates O (and LSE) if not given.
 
     Fixed length: q [B,Sq,H,D], k/v [B,Sk,H_k,D].  Varlen: q [T,H,D], k/v
-    [T,H_k,D] with int32 device cumulative lengths.  Returns (O, LSE)."""
+    [T,H_k,D] with int32 device cumulative lengths.  ``num_splits`` selects
+    the split-KV entry point (a workspace is allocated with torch).
+    Returns (O, LSE)."""
     varlen = cu_seqlens_q is not None
     D = q.shape[-1]
     if varlen:
@@ -171,6 +196,15 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Optional[fl
     if lse is None and return_lse:
         lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
     sc = 1.0 / math.sqrt(D) if scale is None else scale
+    if num_splits is not None:
+        nbytes = fmha_fwd_splitkv_workspace_size(B, H, Sq, D, num_splits, T)
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+        rc = fmha_fwd_splitkv(q, k, v, out, lse, B, H, H_k, Sq, Sk, D, sc, out_scale, _MASKS[mask],
+                              _CAUSAL[causal_type], cu_seqlens_q, cu_seqlens_k, max_len or 0, T,
+                              num_splits, ws, nbytes, stream)
+        if rc != OK:
+            raise FmhaError(rc, status_string(rc))
+        return out, lse
     name = "fmha_fwd" if impl == "tc" else "fmha_fwd_simt"
     rc = _call(name, q, k, v, out, lse, B, H, H_k, Sq, Sk, D, sc, out_scale, _MASKS[mask],
                _CAUSAL[causal_type], cu_seqlens_q, cu_seqlens_k, max_len or 0, T, stream)

@@ -26,6 +26,7 @@
 #ifndef FMHA_H
 #define FMHA_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>   /* cudaStream_t */
 
@@ -80,7 +81,8 @@ enum fmha_status {
  *                when H_k == 1).  Query head h reads kv head h / (H / H_k).
  *   Sq, Sk       query and key lengths (fixed-length mode; ignored if varlen).
  *   D            head dim: 32, 64 or 128.
- *   scale        softmax scale applied to Q K^T (1/sqrt(D) is the usual).
+ *   scale        softmax scale applied to Q K^T (1/sqrt(D) is the usual);
+ *                finite and > 0, otherwise FMHA_ERR_INVALID_ARG.
  *   out_scale    fp32 factor applied to O before the cast to o's dtype.
  *                It does not enter LSE.
  *   mask         enum fmha_mask.  causal_type: enum fmha_causal_type.
@@ -131,6 +133,44 @@ int fmha_fwd_simt(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor o, fl
                   float scale, float out_scale, int mask, int causal_type,
                   const int *cu_seqlens_q, const int *cu_seqlens_k, int max_len,
                   int64_t total_length, cudaStream_t stream);
+
+/*
+ * fmha_fwd_splitkv -- fmha_fwd with every work unit's key range cut into
+ * num_splits contiguous pieces, for shapes with few (batch, head, 256-row
+ * query block) units and long key sequences, where fmha_fwd would leave most
+ * SMs idle.  Each piece writes a normalised fp32 partial O and its LSE into
+ * the workspace; a second kernel merges them exactly:
+ *   LSE = ln sum_s exp(LSE_s),   O = out_scale * sum_s exp(LSE_s - LSE) * O_s.
+ * ("CUTLASS Blackwell FMHA 示例完全解析", §MLA 与 split-KV、reduction 策略: the
+ * same split-KV reduction, there for MLA decoding.)
+ *
+ * Arguments as fmha_fwd, plus:
+ *   num_splits       1..256.  More splits than key tiles leave some pieces
+ *                    empty (they contribute nothing).
+ *   workspace        device scratch owned by the caller, 256-byte aligned,
+ *                    at least fmha_fwd_splitkv_workspace_size(...) bytes.  Its
+ *                    contents on entry do not matter; every byte the merge
+ *                    reads is written first in the same call.  Two calls that
+ *                    share a workspace must not overlap on the GPU.
+ *   workspace_bytes  its size.
+ * Errors: as fmha_fwd; FMHA_ERR_INVALID_ARG for num_splits out of range or a
+ * missing, misaligned or too small workspace.  Two kernels are enqueued on
+ * stream; o and lse are complete when the second one finishes.
+ */
+int fmha_fwd_splitkv(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor o, float *lse,
+                     int B, int H, int H_k, int Sq, int Sk, int D,
+                     float scale, float out_scale, int mask, int causal_type,
+                     const int *cu_seqlens_q, const int *cu_seqlens_k, int max_len,
+                     int64_t total_length, int num_splits, void *workspace,
+                     size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Workspace bytes fmha_fwd_splitkv needs.  Fixed length: pass total_length = 0
+ * (rows = B * Sq).  Variable length: pass the call's total_length (rows =
+ * total_length; B and Sq are then ignored).  Returns 0 for invalid arguments.
+ */
+size_t fmha_fwd_splitkv_workspace_size(int B, int H, int Sq, int D, int num_splits,
+                                       int64_t total_length);
 
 /* Text for a status code (static storage, never NULL). */
 const char *fmha_status_string(int status);

@@ -29,7 +29,7 @@ def half_ulp(dtype: str, x: np.ndarray) -> np.ndarray:
 class Run:
     """One library call with guarded outputs; holds host copies of the results."""
 
-    def __init__(self, fm, inp: wl.Inputs, impl: str = "tc", lse: bool = True):
+    def __init__(self, fm, inp: wl.Inputs, impl: str = "tc", lse: bool = True, num_splits=None):
         w = inp.w
         dev = torch.device("cuda")
         self.inp = inp
@@ -63,7 +63,7 @@ class Run:
         lse_t = self.lse_buf[GUARD * 4: GUARD * 4 + n_lse * 4].view(torch.float32)
         fm.fwd(q, k, v, scale=w.softmax_scale, out_scale=w.out_scale, mask=w.mask,
                causal_type=w.causal_type, out=o, lse=lse_t if lse else None, return_lse=lse,
-               impl=impl, **kw)
+               impl=impl, num_splits=num_splits, **kw)
         torch.cuda.synchronize()
         self.status = fm.device_status(reset=True)
         self.esz = esz

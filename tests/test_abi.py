@@ -63,6 +63,7 @@ def call(fm, **kw):
     (dict(D=96), -1), (dict(D=256), -1), (dict(H=3, H_k=2), -1), (dict(H_k=0), -1),
     (dict(B=-1), -1), (dict(Sq=-5), -1), (dict(mask=3), -1), (dict(causal_type=2), -1),
     (dict(scale=float("nan")), -1), (dict(out_scale=float("inf")), -1),
+    (dict(scale=0.0), -1), (dict(scale=-0.1), -1),
     (dict(cu_seqlens_q=P), -1),                                   # only one cu_seqlens
     (dict(cu_seqlens_q=P, cu_seqlens_k=P, total_length=-1, max_len=4), -1),
     (dict(cu_seqlens_q=P, cu_seqlens_k=P, total_length=10, max_len=0), -1),
@@ -113,3 +114,35 @@ def test_kv_tile_range_matches_brute_force(fm):
                       int(rng.integers(0, 2)), tn))
     for c in cases:
         assert fm.kv_tile_range(*c) == _brute(*c), c
+
+
+def test_splitkv_workspace_size(fm):
+    # fixed length: rows = B*Sq; LSE block rounded up to 256 bytes, then fp32 O
+    n = fm.fmha_fwd_splitkv_workspace_size(2, 4, 100, 64, 3)
+    lse = 3 * 200 * 4 * 4
+    assert n == ((lse + 255) // 256) * 256 + 3 * 200 * 4 * 64 * 4
+    # varlen: rows = total_length
+    assert fm.fmha_fwd_splitkv_workspace_size(9, 2, 0, 128, 2, 77) == \
+        ((2 * 77 * 2 * 4 + 255) // 256) * 256 + 2 * 77 * 2 * 128 * 4
+    for bad in [(2, 4, 100, 96, 3), (2, 4, 100, 64, 0), (2, 4, 100, 64, 257), (2, 0, 100, 64, 1)]:
+        assert fm.fmha_fwd_splitkv_workspace_size(*bad) == 0
+
+
+def call_split(fm, ws=P, ws_bytes=1 << 30, splits=2, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=None, B=1, H=2, H_k=2, Sq=128, Sk=128, D=128, scale=0.1,
+             out_scale=1.0, mask=0, causal_type=0)
+    a.update(kw)
+    t = [fm.fmha_tensor(a[x], 1) for x in "qkvo"]
+    return fm.lib().fmha_fwd_splitkv(*t, a["lse"], a["B"], a["H"], a["H_k"], a["Sq"], a["Sk"], a["D"],
+                                      a["scale"], a["out_scale"], a["mask"], a["causal_type"], None, None,
+                                      0, 0, splits, ws, ws_bytes, None)
+
+
+def test_splitkv_validation(fm):
+    assert call_split(fm, splits=0) == -1
+    assert call_split(fm, splits=257) == -1
+    assert call_split(fm, ws=None) == -1
+    assert call_split(fm, ws_bytes=100) == -1                  # too small
+    assert call_split(fm, ws=P + 16) == -1                     # not 256-byte aligned
+    assert call_split(fm, D=48) == -1
+    assert call_split(fm, B=0, splits=3) == 0                  # nothing to do
