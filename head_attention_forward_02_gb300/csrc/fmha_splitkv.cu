@@ -15,6 +15,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <math.h>
+#include <mutex>
 
 #include "fmha_common.h"
 
@@ -172,3 +173,66 @@ int fmha_fwd_splitkv(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor o,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Split-KV without any allocation
+// ---------------------------------------------------------------------------
+//
+// Some callers cannot allocate device memory at the time they run attention:
+// a serving process that reserves all of its HBM once at start-up and treats
+// any later cudaMalloc as an error (it can fail, fragment the reservation, or
+// stall the device while it synchronises), or a plug-in hosted by a framework
+// that owns every device allocation.  For them the scratch of the split-KV
+// path lives in this file-scope array instead of a caller workspace.  Every
+// GPU that loads the library keeps these bytes reserved until the process
+// exits.
+
+namespace fmha {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = FMHA_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name stands for a host-side shadow, not for device memory, so
+// the address must come from cudaGetSymbolAddress -- once per device, with
+// that device current.
+int noalloc_scratch(void **out) {
+    static std::mutex mu;
+    static void *addr[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return FMHA_ERR_CUDA; }
+    if (dev < 0 || dev >= 64) return FMHA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return FMHA_ERR_CUDA;
+        }
+        addr[dev] = ptr;
+    }
+    *out = addr[dev];
+    return FMHA_OK;
+}
+
+}  // namespace
+}  // namespace fmha
+
+extern "C" int fmha_fwd_splitkv_noalloc(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor o,
+                                        float *lse, int B, int H, int H_k, int Sq, int Sk, int D,
+                                        float scale, float out_scale, int mask, int causal_type,
+                                        const int *cu_seqlens_q, const int *cu_seqlens_k, int max_len,
+                                        int64_t total_length, int num_splits, cudaStream_t stream) {
+    const bool varlen = cu_seqlens_q != nullptr && cu_seqlens_k != nullptr;
+    const size_t need = fmha_fwd_splitkv_workspace_size(B, H, varlen ? 0 : Sq, D, num_splits,
+                                                        varlen ? total_length : 0);
+    if (need == 0) return FMHA_ERR_INVALID_ARG;
+    if (need > fmha::kNoAllocScratchBytes) return FMHA_ERR_UNSUPPORTED;   // too big for the array
+    void *scratch = nullptr;
+    const int rc = fmha::noalloc_scratch(&scratch);
+    if (rc != FMHA_OK) return rc;
+    return fmha_fwd_splitkv(q, k, v, o, lse, B, H, H_k, Sq, Sk, D, scale, out_scale, mask, causal_type,
+                            cu_seqlens_q, cu_seqlens_k, max_len, total_length, num_splits, scratch,
+                            fmha::kNoAllocScratchBytes, stream);
+}

@@ -26,6 +26,7 @@ _MASKS = {"none": MASK_NONE, "residual": MASK_RESIDUAL, "causal": MASK_CAUSAL}
 _CAUSAL = {"qbegin": CAUSAL_QBEGIN, "qend": CAUSAL_QEND}
 
 EXPORTED = ("fmha_fwd", "fmha_fwd_simt", "fmha_fwd_splitkv", "fmha_fwd_splitkv_workspace_size",
+            "fmha_fwd_splitkv_noalloc",
             "fmha_status_string", "fmha_device_status", "fmha_kv_tile_range")
 
 
@@ -65,6 +66,8 @@ def lib():
         L.fmha_fwd_splitkv.restype = ctypes.c_int
         L.fmha_fwd_splitkv.argtypes = fwd_args[:-1] + [ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
                                                        ctypes.c_void_p]
+        L.fmha_fwd_splitkv_noalloc.restype = ctypes.c_int
+        L.fmha_fwd_splitkv_noalloc.argtypes = fwd_args[:-1] + [ctypes.c_int, ctypes.c_void_p]
         L.fmha_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
         L.fmha_fwd_splitkv_workspace_size.argtypes = [ctypes.c_int] * 5 + [ctypes.c_int64]
         L.fmha_status_string.restype = ctypes.c_char_p
@@ -157,6 +160,19 @@ def fmha_fwd_splitkv(q, k, v, o, lse, B, H, H_k, Sq, Sk, D, scale, out_scale, ma
         int(Sk), int(D), float(scale), float(out_scale), int(mask), int(causal_type),
         _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(max_len), int(total_length), int(num_splits),
         _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def fmha_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, H_k, Sq, Sk, D, scale, out_scale, mask,
+                             causal_type, cu_seqlens_q=None, cu_seqlens_k=None, max_len=0,
+                             total_length=0, num_splits=1, stream=None) -> int:
+    """Same arguments, order and status codes as the C function
+    fmha_fwd_splitkv_noalloc: split-KV with the library's built-in scratch,
+    for callers that must not allocate device memory while they run."""
+    return lib().fmha_fwd_splitkv_noalloc(
+        _tensor(q), _tensor(k), _tensor(v), _tensor(o), _ptr(lse), int(B), int(H), int(H_k), int(Sq),
+        int(Sk), int(D), float(scale), float(out_scale), int(mask), int(causal_type),
+        _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(max_len), int(total_length), int(num_splits),
+        _stream(stream))
 
 
 def fmha_fwd_splitkv_workspace_size(B, H, Sq, D, num_splits, total_length=0) -> int:

@@ -172,6 +172,39 @@ int fmha_fwd_splitkv(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor o,
 size_t fmha_fwd_splitkv_workspace_size(int B, int H, int Sq, int D, int num_splits,
                                        int64_t total_length);
 
+/*
+ * fmha_fwd_splitkv_noalloc -- fmha_fwd_splitkv for callers that must not
+ * allocate device memory while they run: processes that reserve their HBM
+ * once at start-up and treat a later cudaMalloc as a failure (it can fail,
+ * fragment the reservation or stall the device), or plug-ins whose host
+ * framework owns every device allocation.  The pages have no counterpart of
+ * this entry point.
+ *
+ * Same arguments as fmha_fwd_splitkv without workspace / workspace_bytes:
+ * the scratch is a library-owned device array of FMHA_NOALLOC_SCRATCH_BYTES
+ * (32 MiB), reserved on every GPU that loads the library until the process
+ * exits.  The caller still owns q, k, v, o and lse.  No device memory is
+ * allocated or freed by this call.
+ *
+ * - The first call on a device looks up the array's device address with the
+ *   device current (a host-side step, once per device); make that first call
+ *   before any stream capture.
+ * - Problems whose split-KV scratch (fmha_fwd_splitkv_workspace_size) exceeds
+ *   the array return FMHA_ERR_UNSUPPORTED without launching; use
+ *   fmha_fwd_splitkv with a workspace for those.
+ * - Every call uses the same array.  Nothing in it needs to start at zero
+ *   (each call writes every byte it later reads), but two calls whose kernels
+ *   overlap on the GPU -- on different streams, or different host threads --
+ *   race on it and corrupt each other's results.  Serialise them (one stream).
+ * Errors otherwise as fmha_fwd_splitkv.
+ */
+#define FMHA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int fmha_fwd_splitkv_noalloc(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor o, float *lse,
+                             int B, int H, int H_k, int Sq, int Sk, int D,
+                             float scale, float out_scale, int mask, int causal_type,
+                             const int *cu_seqlens_q, const int *cu_seqlens_k, int max_len,
+                             int64_t total_length, int num_splits, cudaStream_t stream);
+
 /* Text for a status code (static storage, never NULL). */
 const char *fmha_status_string(int status);
 
