@@ -78,6 +78,12 @@ struct Cfg {
     static constexpr int QK_STEPS = D / MMA_K;
     static constexpr int PV_STEPS = kTile / MMA_K;
     static constexpr int NS = TILE_BYTES <= 8192 ? 8 : (TILE_BYTES <= 16384 ? 6 : 4);
+    // 16-bit inputs pair the ring: stage i holds V_{j-1} and K_j behind one
+    // barrier, so the issuing lane waits and releases once per key step
+    // (measured +2% at D=128); e4m3 keeps one tile per stage, where V_j is
+    // not held back by K_{j+1} (pairing measured -3% there).
+    static constexpr bool PAIRED = !FP8;
+    static constexpr int NSTAGE = PAIRED ? NS / 2 : NS;   // ring stages (barrier pairs)
     static constexpr int S_COL0 = 0, S_COL1 = kTile;
     static constexpr int O_COL0 = 2 * kTile, O_COL1 = 2 * kTile + D;
     static constexpr int BAR_BYTES = 512;
@@ -582,35 +588,68 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
             }
             ++qload[t];
         }
-        for (int j = U.j0; j < U.j1 && ok; ++j) {
-            for (int kv = 0; kv < 2; ++kv) {
-                const int st = fill % C::NS;
-                const uint32_t rnd = fill / C::NS;
+        if constexpr (C::PAIRED) {
+            // fill i of a work item holds V_{j0+i-1} (none for i = 0) and
+            // K_{j0+i} (none for the last fill)
+            for (int i = 0; i <= U.j1 - U.j0 && U.j0 < U.j1 && ok; ++i) {
+                const int st = fill % C::NSTAGE;
+                const uint32_t rnd = fill / C::NSTAGE;
                 if (rnd > 0 && !mbar_wait(smem_u32(&bars->kv_empty[st]), (rnd - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
+                const int jk = U.j0 + i, jv = U.j0 + i - 1;
+                const bool has_k = jk < U.j1, has_v = i > 0;
                 const uint32_t fb = smem_u32(&bars->kv_full[st]);
-                mbar_expect_tx(fb, C::TILE_BYTES);
-                const uint32_t dst = smem_u32(sKV + st * C::TILE_BYTES);
-                const CUtensorMap *m = kv ? tmV : tmK;
+                mbar_expect_tx(fb, (has_k + has_v) * C::TILE_BYTES);
+                const uint32_t dst = smem_u32(sKV + st * 2 * C::TILE_BYTES);
 #pragma unroll
-                for (int pn = 0; pn < C::PANELS; ++pn) {
-                    if (p.varlen)
-                        tma_load_3d(dst + pn * C::PANEL_BYTES, m, fb, pn * C::BOX_D, U.g,
-                                    U.k_row + j * kTile);
-                    else
-                        tma_load_4d(dst + pn * C::PANEL_BYTES, m, fb, pn * C::BOX_D, U.g, j * kTile, U.b);
+                for (int kv = 0; kv < 2; ++kv) {
+                    if (kv ? !has_v : !has_k) continue;
+                    const CUtensorMap *m = kv ? tmV : tmK;
+                    const int j = kv ? jv : jk;
+                    const uint32_t d = dst + kv * C::TILE_BYTES;
+#pragma unroll
+                    for (int pn = 0; pn < C::PANELS; ++pn) {
+                        if (p.varlen)
+                            tma_load_3d(d + pn * C::PANEL_BYTES, m, fb, pn * C::BOX_D, U.g, U.k_row + j * kTile);
+                        else
+                            tma_load_4d(d + pn * C::PANEL_BYTES, m, fb, pn * C::BOX_D, U.g, j * kTile, U.b);
+                    }
                 }
                 ++fill;
+            }
+        } else {
+            for (int j = U.j0; j < U.j1 && ok; ++j) {
+                for (int kv = 0; kv < 2; ++kv) {
+                    const int st = fill % C::NSTAGE;
+                    const uint32_t rnd = fill / C::NSTAGE;
+                    if (rnd > 0 && !mbar_wait(smem_u32(&bars->kv_empty[st]), (rnd - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&bars->kv_full[st]);
+                    mbar_expect_tx(fb, C::TILE_BYTES);
+                    const uint32_t dst = smem_u32(sKV + st * C::TILE_BYTES);
+                    const CUtensorMap *m = kv ? tmV : tmK;
+#pragma unroll
+                    for (int pn = 0; pn < C::PANELS; ++pn) {
+                        if (p.varlen)
+                            tma_load_3d(dst + pn * C::PANEL_BYTES, m, fb, pn * C::BOX_D, U.g,
+                                        U.k_row + j * kTile);
+                        else
+                            tma_load_4d(dst + pn * C::PANEL_BYTES, m, fb, pn * C::BOX_D, U.g, j * kTile, U.b);
+                    }
+                    ++fill;
+                }
             }
         }
     }
     if (ok) {
         // every stage's last release and every Q tile's last release must have
         // arrived before the CTA may exit
-        for (int st = 0; st < C::NS; ++st) {
-            const uint32_t nf = fill > (uint32_t)st ? (fill - st + C::NS - 1) / C::NS : 0;
+        for (int st = 0; st < C::NSTAGE; ++st) {
+            const uint32_t nf = fill > (uint32_t)st ? (fill - st + C::NSTAGE - 1) / C::NSTAGE : 0;
             if (nf && !mbar_wait(smem_u32(&bars->kv_empty[st]), (nf - 1) & 1, abort_flag)) break;
         }
         for (int t = 0; t < 2; ++t)
@@ -618,9 +657,9 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
                 break;
     } else {
         // aborted: let the copies already issued land before the CTA exits
-        const uint32_t first = fill > (uint32_t)C::NS ? fill - C::NS : 0;
+        const uint32_t first = fill > (uint32_t)C::NSTAGE ? fill - C::NSTAGE : 0;
         for (uint32_t f = first; f < fill; ++f)
-            mbar_wait_drain(smem_u32(&bars->kv_full[f % C::NS]), (f / C::NS) & 1);
+            mbar_wait_drain(smem_u32(&bars->kv_full[f % C::NSTAGE]), (f / C::NSTAGE) & 1);
         for (int t = 0; t < 2; ++t)
             if (qload[t]) mbar_wait_drain(smem_u32(&bars->q_full[t]), (qload[t] - 1) & 1);
     }
@@ -653,7 +692,8 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
     // within a 128-byte swizzled panel row, then moves to the next panel.
     auto issue_s = [&](int t, int st) {
         const uint32_t d = tmem + (t ? C::S_COL1 : C::S_COL0);
-        const uint32_t a = q_lo + t * kTileStep, b = k_lo + st * kTileStep;
+        // K tile: whole stage, or the first half of a paired stage
+        const uint32_t a = q_lo + t * kTileStep, b = k_lo + st * (C::PAIRED ? 2 : 1) * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < C::QK_STEPS; ++kk) {
             const uint32_t off =
@@ -666,7 +706,8 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
     auto issue_pv = [&](int t, int st, bool acc) {
         const uint32_t d = tmem + (t ? C::O_COL1 : C::O_COL0);
         const uint32_t a = tmem + (t ? C::S_COL1 : C::S_COL0);
-        const uint32_t b = v_lo + st * kTileStep;
+        // V tile: whole stage, or the second half of a paired stage
+        const uint32_t b = v_lo + (C::PAIRED ? st * 2 + 1 : st) * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < C::PV_STEPS; ++kk) {
             mma_ts_w<C::FP8>(d, a + kk * (C::MMA_K * C::E / 4), b + ((kk * C::MMA_K * C::SW) >> 4), kHi, kIdPV,
@@ -676,8 +717,8 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
     // TMA writes and tensor-core reads of shared memory are both async-proxy
     // operations ordered by the mbarrier: no tcgen05 fence is needed here.
     auto next_kv = [&](int &st) -> bool {
-        st = cons % C::NS;
-        const bool r = mbar_wait(smem_u32(&bars->kv_full[st]), (cons / C::NS) & 1, abort_flag);
+        st = cons % C::NSTAGE;
+        const bool r = mbar_wait(smem_u32(&bars->kv_full[st]), (cons / C::NSTAGE) & 1, abort_flag);
         ++cons;
         return r;
     };
@@ -720,33 +761,61 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
             if (n1 == j0 + 1) tc_commit(smem_u32(&bars->q_empty[1]));
         }
         tc_commit(smem_u32(&bars->kv_empty[kst]));
-        for (int j = j0; j < jn; ++j) {
-            int vst, nst = 0;
-            if (!next_kv(vst)) { ok = false; break; }
-            const bool has_next = j + 1 < jn;
-            if (j < n0) {
-                if (!wait_p(0)) { ok = false; break; }
-                issue_pv(0, vst, j > j0);
-                if (j == n0 - 1) tc_commit(smem_u32(&bars->o_full[0]));
+        if constexpr (C::PAIRED) {
+            for (int j = j0; j < jn; ++j) {
+                int st;                                    // stage holding V_j and K_{j+1}
+                if (!next_kv(st)) { ok = false; break; }
+                if (j < n0) {
+                    if (!wait_p(0)) { ok = false; break; }
+                    issue_pv(0, st, j > j0);
+                    if (j == n0 - 1) tc_commit(smem_u32(&bars->o_full[0]));
+                }
+                if (j + 1 < n0) {
+                    issue_s(0, st);
+                    tc_commit(smem_u32(&bars->s_full[0]));
+                    if (j + 2 == n0) tc_commit(smem_u32(&bars->q_empty[0]));
+                }
+                if (j < n1) {
+                    if (!wait_p(1)) { ok = false; break; }
+                    issue_pv(1, st, j > j0);
+                    if (j == n1 - 1) tc_commit(smem_u32(&bars->o_full[1]));
+                }
+                if (j + 1 < n1) {
+                    issue_s(1, st);
+                    tc_commit(smem_u32(&bars->s_full[1]));
+                    if (j + 2 == n1) tc_commit(smem_u32(&bars->q_empty[1]));
+                }
+                tc_commit(smem_u32(&bars->kv_empty[st]));
             }
-            if (has_next && !next_kv(nst)) { ok = false; break; }
-            if (j + 1 < n0) {
-                issue_s(0, nst);
-                tc_commit(smem_u32(&bars->s_full[0]));
-                if (j + 2 == n0) tc_commit(smem_u32(&bars->q_empty[0]));
+        } else {
+            for (int j = j0; j < jn; ++j) {
+                int vst, nst = 0;
+                if (!next_kv(vst)) { ok = false; break; }
+                const bool has_next = j + 1 < jn;
+                if (j < n0) {
+                    if (!wait_p(0)) { ok = false; break; }
+                    issue_pv(0, vst, j > j0);
+                    if (j == n0 - 1) tc_commit(smem_u32(&bars->o_full[0]));
+                }
+                if (has_next && !next_kv(nst)) { ok = false; break; }
+                if (j + 1 < n0) {
+                    issue_s(0, nst);
+                    tc_commit(smem_u32(&bars->s_full[0]));
+                    if (j + 2 == n0) tc_commit(smem_u32(&bars->q_empty[0]));
+                }
+                if (j < n1) {
+                    if (!wait_p(1)) { ok = false; break; }
+                    issue_pv(1, vst, j > j0);
+                    if (j == n1 - 1) tc_commit(smem_u32(&bars->o_full[1]));
+                }
+                tc_commit(smem_u32(&bars->kv_empty[vst]));
+                if (j + 1 < n1) {
+                    issue_s(1, nst);
+                    tc_commit(smem_u32(&bars->s_full[1]));
+                    if (j + 2 == n1) tc_commit(smem_u32(&bars->q_empty[1]));
+                }
+                if (has_next) tc_commit(smem_u32(&bars->kv_empty[nst]));
             }
-            if (j < n1) {
-                if (!wait_p(1)) { ok = false; break; }
-                issue_pv(1, vst, j > j0);
-                if (j == n1 - 1) tc_commit(smem_u32(&bars->o_full[1]));
-            }
-            tc_commit(smem_u32(&bars->kv_empty[vst]));
-            if (j + 1 < n1) {
-                issue_s(1, nst);
-                tc_commit(smem_u32(&bars->s_full[1]));
-                if (j + 2 == n1) tc_commit(smem_u32(&bars->q_empty[1]));
-            }
-            if (has_next) tc_commit(smem_u32(&bars->kv_empty[nst]));
         }
     }
     // no tensor-core operation may be in flight when TMEM is released
@@ -1027,7 +1096,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bars->o_full[t]), 1);
         }
         mbar_init(smem_u32(&bars->drain), 1);
-        for (int s = 0; s < C::NS; ++s) {
+        for (int s = 0; s < C::NSTAGE; ++s) {
             mbar_init(smem_u32(&bars->kv_full[s]), 1);
             mbar_init(smem_u32(&bars->kv_empty[s]), 1);
         }
