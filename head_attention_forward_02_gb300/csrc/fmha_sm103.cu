@@ -48,8 +48,9 @@ namespace {
 constexpr int kTile = 128;                 // query rows per Q tile, keys per K/V tile
 constexpr int kUnitRows = 2 * kTile;       // query rows per work unit
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;              // softmax warps 0-7, producer warp 8, MMA warp 9
+constexpr int kMmaWarp = 9;                // issues Q tile 0's MMAs; owns the TMEM allocation
+constexpr int kMmaWarp1 = 10;              // issues Q tile 1's MMAs
+constexpr int kThreads = 352;              // softmax warps 0-7, producer warp 8, MMA warps 9-10
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;
 constexpr unsigned long long kDrainNs = 200000000ull;
@@ -105,7 +106,8 @@ struct Cfg {
 };
 
 struct Bars {
-    uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], drain;
+    uint64_t q_full[2], q_empty[2], s_full[2], p_half[2], p_full[2], o_full[2], drain;
+    uint64_t turn[2];          // issue turn of the MMA lane of Q tile t
     uint64_t kv_full[8], kv_empty[8];
     uint32_t tmem_base;
     int abort;
@@ -384,6 +386,30 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
                  :
+                 : "memory");
+}
+
+// Load 16 consecutive TMEM columns of this thread's lane (32x32b shape).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+}
+
+// Wait for this thread's TMEM loads, tying the 16 loaded registers to the wait.
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t *r) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+
+// Store 16 consecutive TMEM columns of this thread's lane (32x32b shape).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+                 :
+                 : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                   "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
                  : "memory");
 }
 
@@ -670,52 +696,65 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
 // ---------------------------------------------------------------------------
 
 template <class C, bool SPLIT>
-__device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bars, uint32_t tmem) {
+__device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bars, uint32_t tmem, int t) {
+    // Two lanes issue the MMAs, lane t for Q tile t, and take turns so that
+    // the tensor pipe sees the order S0_j0, S1_j0, then per key step
+    // PV0_j S0_j+1, PV1_j S1_j+1: each S_t lands right behind its PV_t and the
+    // other tile's work fills the pipe while tile t's softmax runs.  A
+    // tcgen05.mma holds its issuing thread for most of its 64 pipe cycles, so
+    // one lane alone cannot also do the commits and barrier waits between
+    // groups without starving the shallow tensor queue; with two lanes that
+    // bookkeeping runs while the other lane issues.
     volatile int *abort_flag = &bars->abort;
     constexpr uint32_t kIdS = C::idesc(kTile, false);
     constexpr uint32_t kIdPV = C::idesc(C::D, true);
-    uint32_t cons = 0, qc0 = 0, qc1 = 0, pc0 = 0, pc1 = 0;
+    uint32_t cons = 0, qc = 0, pc = 0, hc = 0, tc = 0;
     bool ok = true;
     Cursor cur;
 
     // Descriptor words are computed once; each MMA then only adds a
-    // compile-time byte offset to the low word.  The issuing lane shares its
-    // SMSP with two busy softmax warps and the tensor-core queue is shallow,
-    // so every instruction between two MMA groups is time the pipe may idle.
+    // compile-time byte offset to the low word.
     constexpr uint32_t kHi = desc_hi(C::SBO, (uint32_t)C::SW_CODE);
     constexpr uint32_t kTileStep = C::TILE_BYTES >> 4;
-    const uint32_t q_lo = desc_lo(smem_u32(sQ), 16);                 // K-major: LBO unused
+    const uint32_t q_lo = desc_lo(smem_u32(sQ), 16) + t * kTileStep;  // K-major: LBO unused
     const uint32_t k_lo = desc_lo(smem_u32(sKV), 16);
     const uint32_t v_lo = desc_lo(smem_u32(sKV), C::PANEL_BYTES);    // MN-major: LBO = panel stride
+    const uint32_t s_tm = tmem + (t ? C::S_COL1 : C::S_COL0);
+    const uint32_t o_tm = tmem + (t ? C::O_COL1 : C::O_COL0);
+    const uint32_t s_full = smem_u32(&bars->s_full[t]), q_empty = smem_u32(&bars->q_empty[t]);
+    const uint32_t o_full = smem_u32(&bars->o_full[t]);
+    const uint32_t p_half = smem_u32(&bars->p_half[t]), p_full = smem_u32(&bars->p_full[t]);
+    const uint32_t my_turn = smem_u32(&bars->turn[t]), next_turn = smem_u32(&bars->turn[t ^ 1]);
 
     // S_t = Q_t K^T: both operands K-major; each k-step advances 32 bytes
     // within a 128-byte swizzled panel row, then moves to the next panel.
-    auto issue_s = [&](int t, int st) {
-        const uint32_t d = tmem + (t ? C::S_COL1 : C::S_COL0);
+    auto issue_s = [&](int st) {
         // K tile: whole stage, or the first half of a paired stage
-        const uint32_t a = q_lo + t * kTileStep, b = k_lo + st * (C::PAIRED ? 2 : 1) * kTileStep;
+        const uint32_t b = k_lo + st * (C::PAIRED ? 2 : 1) * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < C::QK_STEPS; ++kk) {
             const uint32_t off =
                 ((kk * C::KSTEP_BYTES / C::SW) * C::PANEL_BYTES + (kk * C::KSTEP_BYTES) % C::SW) >> 4;
-            mma_ss_w<C::FP8>(d, a + off, b + off, kHi, kIdS, kk > 0 ? 1u : 0u);
+            mma_ss_w<C::FP8>(s_tm, q_lo + off, b + off, kHi, kIdS, kk > 0 ? 1u : 0u);
         }
     };
-    // O_t (+)= P_t V: P from TMEM (aliasing S_t), V MN-major (keys are the K
-    // dimension, head dim the N dimension spread over PANELS panels).
-    auto issue_pv = [&](int t, int st, bool acc) {
-        const uint32_t d = tmem + (t ? C::O_COL1 : C::O_COL0);
-        const uint32_t a = tmem + (t ? C::S_COL1 : C::S_COL0);
+    // O_t (+)= P_t V over one half of the keys (hf = 0: keys 0-63, 1: 64-127):
+    // P from TMEM (aliasing S_t), V MN-major (keys are the K dimension, head
+    // dim the N dimension spread over PANELS panels).
+    auto issue_pv_half = [&](int st, int hf, bool acc) {
         // V tile: whole stage, or the second half of a paired stage
         const uint32_t b = v_lo + (C::PAIRED ? st * 2 + 1 : st) * kTileStep;
+        constexpr int H = C::PV_STEPS / 2;
 #pragma unroll
-        for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-            mma_ts_w<C::FP8>(d, a + kk * (C::MMA_K * C::E / 4), b + ((kk * C::MMA_K * C::SW) >> 4), kHi, kIdPV,
-                             (acc || kk > 0) ? 1u : 0u);
+        for (int k = 0; k < H; ++k) {
+            const int kk = hf * H + k;
+            mma_ts_w<C::FP8>(o_tm, s_tm + kk * (C::MMA_K * C::E / 4), b + ((kk * C::MMA_K * C::SW) >> 4), kHi,
+                             kIdPV, (acc || kk > 0) ? 1u : 0u);
         }
     };
     // TMA writes and tensor-core reads of shared memory are both async-proxy
     // operations ordered by the mbarrier: no tcgen05 fence is needed here.
+    // Both lanes consume every ring stage and each releases it once.
     auto next_kv = [&](int &st) -> bool {
         st = cons % C::NSTAGE;
         const bool r = mbar_wait(smem_u32(&bars->kv_full[st]), (cons / C::NSTAGE) & 1, abort_flag);
@@ -724,98 +763,69 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
     };
     // P_t was written to TMEM by the softmax threads (tcgen05.st): order this
     // thread's MMAs after their fence::before_thread_sync + arrive.
-    auto wait_p = [&](int t) -> bool {
-        uint32_t &pc = t ? pc1 : pc0;
-        const bool r = mbar_wait(smem_u32(&bars->p_full[t]), pc & 1, abort_flag);
-        ++pc;
+    auto wait_p = [&](uint32_t bar, uint32_t &cnt) -> bool {
+        const bool r = mbar_wait(bar, cnt & 1, abort_flag);
+        ++cnt;
         if (r) tc_fence_after();
         return r;
     };
+    auto take_turn = [&]() -> bool {
+        const bool r = mbar_wait(my_turn, tc & 1, abort_flag);
+        ++tc;
+        return r;
+    };
+    auto pass_turn = [&]() { mbar_arrive(next_turn); };
 
     for (int r = 0; ok; ++r) {
         Unit U;
         if (!decode_work<SPLIT>(p, unit_of_round(r), cur, U)) break;
-        const int n0 = U.n[0], n1 = U.n[1], j0 = U.j0, jn = U.j1;
+        const int n = t ? U.n[1] : U.n[0], j0 = U.j0, jn = U.j1;
         if (j0 >= jn) continue;
-        if (n0 > j0) {
-            ok = mbar_wait(smem_u32(&bars->q_full[0]), qc0 & 1, abort_flag);
-            ++qc0;
+        if (n > j0) {
+            ok = mbar_wait(smem_u32(&bars->q_full[t]), qc & 1, abort_flag);
+            ++qc;
         }
-        if (ok && n1 > j0) {
-            ok = mbar_wait(smem_u32(&bars->q_full[1]), qc1 & 1, abort_flag);
-            ++qc1;
-        }
-        if (!ok) break;
+        int kst;
+        if (!ok || !next_kv(kst) || !take_turn()) { ok = false; break; }
         // the previous unit's epilogue read O_t from TMEM before its softmax
         // warps published this unit's first P_t, so no wait is needed here
-        int kst;
-        if (!next_kv(kst)) { ok = false; break; }
-        if (n0 > j0) {
-            issue_s(0, kst);
-            tc_commit(smem_u32(&bars->s_full[0]));
-            if (n0 == j0 + 1) tc_commit(smem_u32(&bars->q_empty[0]));
-        }
-        if (n1 > j0) {
-            issue_s(1, kst);
-            tc_commit(smem_u32(&bars->s_full[1]));
-            if (n1 == j0 + 1) tc_commit(smem_u32(&bars->q_empty[1]));
+        if (n > j0) issue_s(kst);
+        pass_turn();
+        if (n > j0) {
+            tc_commit(s_full);
+            if (n == j0 + 1) tc_commit(q_empty);
         }
         tc_commit(smem_u32(&bars->kv_empty[kst]));
-        if constexpr (C::PAIRED) {
-            for (int j = j0; j < jn; ++j) {
-                int st;                                    // stage holding V_j and K_{j+1}
-                if (!next_kv(st)) { ok = false; break; }
-                if (j < n0) {
-                    if (!wait_p(0)) { ok = false; break; }
-                    issue_pv(0, st, j > j0);
-                    if (j == n0 - 1) tc_commit(smem_u32(&bars->o_full[0]));
-                }
-                if (j + 1 < n0) {
-                    issue_s(0, st);
-                    tc_commit(smem_u32(&bars->s_full[0]));
-                    if (j + 2 == n0) tc_commit(smem_u32(&bars->q_empty[0]));
-                }
-                if (j < n1) {
-                    if (!wait_p(1)) { ok = false; break; }
-                    issue_pv(1, st, j > j0);
-                    if (j == n1 - 1) tc_commit(smem_u32(&bars->o_full[1]));
-                }
-                if (j + 1 < n1) {
-                    issue_s(1, st);
-                    tc_commit(smem_u32(&bars->s_full[1]));
-                    if (j + 2 == n1) tc_commit(smem_u32(&bars->q_empty[1]));
-                }
-                tc_commit(smem_u32(&bars->kv_empty[st]));
+        for (int j = j0; j < jn; ++j) {
+            // paired ring: one stage holds V_j and K_{j+1}; otherwise V_j,
+            // then K_{j+1} in the next stage (when a next key tile exists)
+            int v_st, k_st = 0;
+            if (!next_kv(v_st)) { ok = false; break; }
+            if constexpr (C::PAIRED) k_st = v_st;
+            else if (j + 1 < jn && !next_kv(k_st)) { ok = false; break; }
+            const bool act = j < n, more = j + 1 < n;
+            // P_t is published in two halves: PV over keys 0-63 starts once
+            // the first half is in TMEM, while the softmax computes the
+            // second; S_t,j+1 overwrites P_t after both PV halves in pipe order
+            if (act && !wait_p(p_half, hc)) { ok = false; break; }
+            if (!take_turn()) { ok = false; break; }
+            if (act) {
+                issue_pv_half(v_st, 0, j > j0);
+                if (!wait_p(p_full, pc)) { ok = false; break; }
+                issue_pv_half(v_st, 1, true);
+                if (more) issue_s(k_st);
             }
-        } else {
-            for (int j = j0; j < jn; ++j) {
-                int vst, nst = 0;
-                if (!next_kv(vst)) { ok = false; break; }
-                const bool has_next = j + 1 < jn;
-                if (j < n0) {
-                    if (!wait_p(0)) { ok = false; break; }
-                    issue_pv(0, vst, j > j0);
-                    if (j == n0 - 1) tc_commit(smem_u32(&bars->o_full[0]));
+            pass_turn();
+            if (act) {
+                if (!more) {
+                    tc_commit(o_full);
+                } else {
+                    tc_commit(s_full);
+                    if (j + 2 == n) tc_commit(q_empty);
                 }
-                if (has_next && !next_kv(nst)) { ok = false; break; }
-                if (j + 1 < n0) {
-                    issue_s(0, nst);
-                    tc_commit(smem_u32(&bars->s_full[0]));
-                    if (j + 2 == n0) tc_commit(smem_u32(&bars->q_empty[0]));
-                }
-                if (j < n1) {
-                    if (!wait_p(1)) { ok = false; break; }
-                    issue_pv(1, vst, j > j0);
-                    if (j == n1 - 1) tc_commit(smem_u32(&bars->o_full[1]));
-                }
-                tc_commit(smem_u32(&bars->kv_empty[vst]));
-                if (j + 1 < n1) {
-                    issue_s(1, nst);
-                    tc_commit(smem_u32(&bars->s_full[1]));
-                    if (j + 2 == n1) tc_commit(smem_u32(&bars->q_empty[1]));
-                }
-                if (has_next) tc_commit(smem_u32(&bars->kv_empty[nst]));
             }
+            tc_commit(smem_u32(&bars->kv_empty[v_st]));
+            if (!C::PAIRED && j + 1 < jn) tc_commit(smem_u32(&bars->kv_empty[k_st]));
         }
     }
     // no tensor-core operation may be in flight when TMEM is released
@@ -906,28 +916,6 @@ __device__ __forceinline__ float exp_half(const float *x, uint64_t c2, uint64_t 
     return a + b;
 }
 
-// P from scores held in registers, stored half a row at a time (keeps the
-// register footprint low).  Returns the fp32 sum.
-template <class C>
-__device__ __forceinline__ float exp_store_regs(uint32_t s_tm, const float (&s)[kTile], float c, float neg_m) {
-    const uint64_t c2 = pack_f2(c, c), nm2 = pack_f2(neg_m, neg_m);
-    float sum = 0.f;
-    if constexpr (!C::FP8) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t w[32];
-            sum += exp_half<C>(s + 64 * h, c2, nm2, w);
-            tmem_st32(s_tm + 32 * h, w);
-        }
-    } else {
-        uint32_t w[32];
-        sum += exp_half<C>(s, c2, nm2, w);
-        sum += exp_half<C>(s + 64, c2, nm2, w + 16);
-        tmem_st32(s_tm, w);
-    }
-    return sum;
-}
-
 template <class C>
 __device__ __forceinline__ void rescale_o(uint32_t o_tm, float alpha) {
 #pragma unroll 1
@@ -940,6 +928,42 @@ __device__ __forceinline__ void rescale_o(uint32_t o_tm, float alpha) {
         tmem_st32(o_tm + 32 * ch, r);
     }
     tmem_wait_st();
+}
+
+// P from scores held in registers, one half row (64 keys) at a time, each
+// half published on its own barrier as soon as it is in TMEM: the tensor
+// pipe starts PV over the first 64 keys while the second half is computed.
+// P words of keys 0-63 land below those of keys 64-127 (32 columns per half
+// for 16-bit P, 16 for e4m3).  Returns the fp32 sum.
+//
+// O_t holds PV_t_{j-1} (complete, since S_t_j was issued after it) and is
+// rescaled by alpha when `rescale` is set, before the first half of P_t_j is
+// published; that happens after the first half is stored, while only the
+// second half of the scores is live.
+template <class C>
+__device__ __forceinline__ float exp_store_publish(uint32_t s_tm, const float (&s)[kTile], float c, float neg_m,
+                                                   bool rescale, uint32_t o_tm, float alpha, uint32_t half_bar,
+                                                   uint32_t full_bar, int lane) {
+    const uint64_t c2 = pack_f2(c, c), nm2 = pack_f2(neg_m, neg_m);
+    float sum = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if constexpr (!C::FP8) {
+            uint32_t w[32];
+            sum += exp_half<C>(s + 64 * h, c2, nm2, w);
+            tmem_st32(s_tm + 32 * h, w);
+        } else {
+            uint32_t w[16];
+            sum += exp_half<C>(s + 64 * h, c2, nm2, w);
+            tmem_st16(s_tm + 16 * h, w);
+        }
+        if (h == 0 && rescale) rescale_o<C>(o_tm, alpha);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(h ? full_bar : half_bar);
+    }
+    return sum;
 }
 
 template <class C>
@@ -972,6 +996,7 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
     const uint32_t s_tm = lane_base + (t ? C::S_COL1 : C::S_COL0);
     const uint32_t o_tm = lane_base + (t ? C::O_COL1 : C::O_COL0);
     const uint32_t s_bar = smem_u32(&bars->s_full[t]);
+    const uint32_t ph_bar = smem_u32(&bars->p_half[t]);
     const uint32_t p_bar = smem_u32(&bars->p_full[t]);
     const uint32_t o_bar = smem_u32(&bars->o_full[t]);
     const float c = p.scale * kLog2e;          // scores in log2 units: s * scale * log2(e)
@@ -1004,14 +1029,8 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
                 l *= alpha;
                 m_ref = m_tile;
             }
-            l += exp_store_regs<C>(s_tm, s, c, m_ref == -INFINITY ? 0.f : -m_ref);
-            // O_t holds PV_t_{j-1}, complete since S_t_j was issued after it;
-            // it must be rescaled before P_t_j is published
-            if (j > j0 && __any_sync(0xffffffffu, resc)) rescale_o<C>(o_tm, alpha);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_bar);
+            l += exp_store_publish<C>(s_tm, s, c, m_ref == -INFINITY ? 0.f : -m_ref,
+                                      j > j0 && __any_sync(0xffffffffu, resc), o_tm, alpha, ph_bar, p_bar, lane);
         }
         if (!ok) break;
 
@@ -1092,16 +1111,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bars->q_full[t]), 1);
             mbar_init(smem_u32(&bars->q_empty[t]), 1);
             mbar_init(smem_u32(&bars->s_full[t]), 1);
-            mbar_init(smem_u32(&bars->p_full[t]), 4);   // one arrival per softmax warp
+            mbar_init(smem_u32(&bars->p_half[t]), 4);   // one arrival per softmax warp
+            mbar_init(smem_u32(&bars->p_full[t]), 4);
             mbar_init(smem_u32(&bars->o_full[t]), 1);
         }
-        mbar_init(smem_u32(&bars->drain), 1);
+        mbar_init(smem_u32(&bars->drain), 2);             // one commit per MMA lane
+        mbar_init(smem_u32(&bars->turn[0]), 1);
+        mbar_init(smem_u32(&bars->turn[1]), 1);
         for (int s = 0; s < C::NSTAGE; ++s) {
             mbar_init(smem_u32(&bars->kv_full[s]), 1);
-            mbar_init(smem_u32(&bars->kv_empty[s]), 1);
+            mbar_init(smem_u32(&bars->kv_empty[s]), 2);   // released by both MMA lanes
         }
         bars->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_arrive(smem_u32(&bars->turn[0]));            // tile 0's lane issues first
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
@@ -1117,7 +1140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kProducerWarp) {
         if (lane == 0) producer<C, SPLIT>(p, &tmQ, &tmK, &tmV, sQ, sKV, bars);
     } else {
-        if (lane == 0) mma_issuer<C, SPLIT>(p, sQ, sKV, bars, tmem);
+        if (lane == 0) mma_issuer<C, SPLIT>(p, sQ, sKV, bars, tmem, warp - kMmaWarp);
     }
 
     tc_fence_before();
