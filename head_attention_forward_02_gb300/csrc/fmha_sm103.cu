@@ -85,6 +85,13 @@ struct Cfg {
     // not held back by K_{j+1} (pairing measured -3% there).
     static constexpr bool PAIRED = !FP8;
     static constexpr int NSTAGE = PAIRED ? NS / 2 : NS;   // ring stages (barrier pairs)
+    // The MMA lane hands the issue turn to the other lane this many MMAs
+    // before the end of an S group, hiding the other lane's wake-up behind
+    // MMAs still to issue (16-bit: +6% at D=128).  The e4m3 key step is
+    // softmax-bound, and there letting the other tile's MMAs in ahead of the
+    // last S MMAs costs more than the hand-off (measured -2% to -5%).
+    static constexpr int TURN_EARLY = FP8 ? 0 : 2;
+    static constexpr int TURN_AT = QK_STEPS - 1 - TURN_EARLY > 0 ? QK_STEPS - 1 - TURN_EARLY : 0;
     static constexpr int S_COL0 = 0, S_COL1 = kTile;
     static constexpr int O_COL0 = 2 * kTile, O_COL1 = 2 * kTile + D;
     static constexpr int BAR_BYTES = 512;
@@ -726,8 +733,10 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
     const uint32_t p_half = smem_u32(&bars->p_half[t]), p_full = smem_u32(&bars->p_full[t]);
     const uint32_t my_turn = smem_u32(&bars->turn[t]), next_turn = smem_u32(&bars->turn[t ^ 1]);
 
+    auto pass_turn = [&]() { mbar_arrive(next_turn); };
     // S_t = Q_t K^T: both operands K-major; each k-step advances 32 bytes
     // within a 128-byte swizzled panel row, then moves to the next panel.
+    // The issue turn passes to the other lane within this group (TURN_AT).
     auto issue_s = [&](int st) {
         // K tile: whole stage, or the first half of a paired stage
         const uint32_t b = k_lo + st * (C::PAIRED ? 2 : 1) * kTileStep;
@@ -736,6 +745,7 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
             const uint32_t off =
                 ((kk * C::KSTEP_BYTES / C::SW) * C::PANEL_BYTES + (kk * C::KSTEP_BYTES) % C::SW) >> 4;
             mma_ss_w<C::FP8>(s_tm, q_lo + off, b + off, kHi, kIdS, kk > 0 ? 1u : 0u);
+            if (kk == C::TURN_AT) pass_turn();
         }
     };
     // O_t (+)= P_t V over one half of the keys (hf = 0: keys 0-63, 1: 64-127):
@@ -774,7 +784,6 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
         ++tc;
         return r;
     };
-    auto pass_turn = [&]() { mbar_arrive(next_turn); };
 
     for (int r = 0; ok; ++r) {
         Unit U;
@@ -790,7 +799,7 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
         // the previous unit's epilogue read O_t from TMEM before its softmax
         // warps published this unit's first P_t, so no wait is needed here
         if (n > j0) issue_s(kst);
-        pass_turn();
+        else pass_turn();
         if (n > j0) {
             tc_commit(s_full);
             if (n == j0 + 1) tc_commit(q_empty);
@@ -815,7 +824,7 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
                 issue_pv_half(v_st, 1, true);
                 if (more) issue_s(k_st);
             }
-            pass_turn();
+            if (!act || !more) pass_turn();
             if (act) {
                 if (!more) {
                     tc_commit(o_full);
