@@ -62,6 +62,12 @@ def _load():
             ctypes.c_double, ctypes.c_double, ctypes.c_int, ctypes.c_int,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_gen_fwd.restype = ctypes.c_int
+        lib.oracle_gen_fwd.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_double, ctypes.c_double,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -131,6 +137,35 @@ def fmha_fwd(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, dtype: 
         cq.ctypes.data if varlen else None, ck.ctypes.data if varlen else None,
         int(total_length), r.ctypes.data if r is not None else None, n,
         o.ctypes.data, lse.ctypes.data, int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return o, lse
+
+
+def gen_fwd(q_bits: np.ndarray, k_cache_bits: np.ndarray, v_cache_bits: np.ndarray,
+            k_new_bits: Optional[np.ndarray], v_new_bits: Optional[np.ndarray], dtype: int,
+            B: int, H: int, H_k: int, D: int, B_cache: int, S_max: int,
+            seqlen: np.ndarray, batch_idx: Optional[np.ndarray],
+            scale: float, out_scale: float = 1.0, threads: int = 0) -> Tuple[np.ndarray, np.ndarray]:
+    """Generation phase: O (float64 [B*H, D], row b*H + h) and LSE (float64 [B*H]).
+
+    q [B, H, D]; caches [B_cache, S_max, H_k, D]; new K/V [B, H_k, D] or None for
+    cache-only; seqlen int32 [B] cached tokens per sequence; batch_idx int32 [B]
+    (cache entry of sequence b) or None for the identity.  See ``oracle_gen_fwd``
+    in ``fmha_oracle.c`` for the definition.
+    """
+    lib = _load()
+    bd = _bits_dtype(dtype)
+    arr = [np.ascontiguousarray(x, dtype=bd) if x is not None else None
+           for x in (q_bits, k_cache_bits, v_cache_bits, k_new_bits, v_new_bits)]
+    sl = np.ascontiguousarray(seqlen, dtype=np.int32)
+    bi = np.ascontiguousarray(batch_idx, dtype=np.int32) if batch_idx is not None else None
+    o = np.empty((B * H, D), dtype=np.float64)
+    lse = np.empty((B * H,), dtype=np.float64)
+    ptr = [a.ctypes.data if a is not None else None for a in arr]
+    rc = lib.oracle_gen_fwd(*ptr, dtype, B, H, H_k, D, B_cache, S_max, sl.ctypes.data,
+                            bi.ctypes.data if bi is not None else None, float(scale),
+                            float(out_scale), o.ctypes.data, lse.ctypes.data, int(threads))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return o, lse

@@ -322,3 +322,109 @@ int oracle_fmha_fwd(const void *q, const void *k, const void *v, int dtype,
     free(table);
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Generation phase: one new query token per sequence against a K/V cache.    */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Source: "CUTLASS Blackwell FMHA 示例完全解析", §FMHA for Blackwell 生成阶段
+ * (fmha_gen): the generation-phase forward attends one new token of every
+ * sequence to that sequence's entry of a K/V cache; with batch remapping the
+ * entry of sequence b is batch_idx[b]; cache entries hold different numbers
+ * of valid tokens; in cache-only mode the kernel neither reads nor inserts a
+ * new K/V entry, otherwise the new token's K/V join the cache.  The same page
+ * fixes head dim 128 and one query-head group per thread block.
+ *
+ * Reading used here (the page gives no formula): for sequence b, query head
+ * h, kv head g = h / (H / H_k), cache entry c = batch_idx ? batch_idx[b] : b
+ * and L = seqlen[b] valid cached tokens, the keys are
+ *     K_cache[c, 0..L-1, g, :]                      (cache-only), or
+ *     K_cache[c, 0..L-1, g, :] followed by K_new[b, g, :]   (insert mode),
+ * with V alike, and the output is the plain definition of the prefill oracle
+ * above with one query row and no mask:
+ *     s_j = scale * q[b,h,:] . k_j ,  m = max s_j ,  l = sum exp(s_j - m)
+ *     O[b,h,:] = out_scale * sum_j exp(s_j - m) v_j / l ,  LSE = m + ln l
+ * (no key: O = 0, LSE = -inf).  Layouts: q, O [B, H, D]; caches
+ * [B_cache, S_max, H_k, D]; new K/V [B, H_k, D]; LSE [B, H].
+ * Returns 0, or -1 on inconsistent arguments (bad entry index, L outside
+ * [0, S_max], or L = S_max in insert mode).
+ */
+int oracle_gen_fwd(const void *q, const void *k_cache, const void *v_cache,
+                   const void *k_new, const void *v_new, int dtype,
+                   int B, int H, int H_k, int D, int B_cache, int S_max,
+                   const int *seqlen, const int *batch_idx,
+                   double scale, double out_scale,
+                   double *o_out, double *lse_out, int n_threads) {
+    if (B < 0 || H <= 0 || H_k <= 0 || H % H_k != 0 || D <= 0 || S_max < 0 || B_cache < 0) return -1;
+    if ((k_new == NULL) != (v_new == NULL)) return -1;
+    const int insert = k_new != NULL;
+    for (int b = 0; b < B; ++b) {
+        int c = batch_idx ? batch_idx[b] : b;
+        if (c < 0 || c >= B_cache) return -1;
+        if (seqlen[b] < 0 || seqlen[b] > S_max || (insert && seqlen[b] == S_max)) return -1;
+    }
+    const int group = H / H_k;
+    double dtab[256];
+    double *table = NULL;
+    if (dtype == OR_E4M3) {
+        for (int c = 0; c < 256; ++c) dtab[c] = decode_e4m3((uint32_t)c);
+    } else {
+        table = (double *)malloc(65536 * sizeof(double));
+        if (!table) return -1;
+        for (int c = 0; c < 65536; ++c) table[c] = oracle_decode(dtype, (uint32_t)c);
+    }
+    const double *lut = dtype == OR_E4M3 ? dtab : table;
+    const int64_t n_rows = (int64_t)B * H;
+
+#ifdef _OPENMP
+    if (n_threads <= 0) n_threads = omp_get_max_threads();
+#pragma omp parallel num_threads(n_threads)
+#endif
+    {
+        double *s = (double *)malloc((size_t)(S_max + 1) * sizeof(double));
+        double *qrow = (double *)malloc((size_t)D * sizeof(double));
+        double *acc = (double *)malloc((size_t)D * sizeof(double));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t r = 0; r < n_rows; ++r) {
+            const int64_t b = r / H, h = r % H, g = h / group;
+            const int64_t c = batch_idx ? batch_idx[b] : b;
+            const int64_t L = seqlen[b], n_keys = L + insert;
+            for (int d = 0; d < D; ++d) qrow[d] = lut[load_bits(q, dtype, (b * H + h) * D + d)];
+            /* key j < L lives in the cache entry; key L (insert mode) is the new token */
+            double m = -INFINITY;
+            for (int64_t j = 0; j < n_keys; ++j) {
+                const void *src = j < L ? k_cache : k_new;
+                const int64_t off = j < L ? ((c * S_max + j) * H_k + g) * D : (b * H_k + g) * D;
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d) dot += qrow[d] * lut[load_bits(src, dtype, off + d)];
+                s[j] = scale * dot;
+                if (s[j] > m) m = s[j];
+            }
+            double *orow = o_out + r * D;
+            if (n_keys == 0) {
+                for (int d = 0; d < D; ++d) orow[d] = 0.0;
+                lse_out[r] = -INFINITY;
+                continue;
+            }
+            double l = 0.0;
+            for (int d = 0; d < D; ++d) acc[d] = 0.0;
+            for (int64_t j = 0; j < n_keys; ++j) {
+                const double p = exp(s[j] - m);
+                const void *src = j < L ? v_cache : v_new;
+                const int64_t off = j < L ? ((c * S_max + j) * H_k + g) * D : (b * H_k + g) * D;
+                l += p;
+                for (int d = 0; d < D; ++d) acc[d] += p * lut[load_bits(src, dtype, off + d)];
+            }
+            for (int d = 0; d < D; ++d) orow[d] = out_scale * acc[d] / l;
+            lse_out[r] = m + log(l);
+        }
+        free(s);
+        free(qrow);
+        free(acc);
+    }
+    free(table);
+    return 0;
+}
