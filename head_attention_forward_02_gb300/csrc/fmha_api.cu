@@ -9,6 +9,10 @@
 #include "fmha_common.h"
 
 namespace fmha {
+int gen_read_status(int reset);   // fmha_gen.cu: the generation kernels' status word
+}
+
+namespace fmha {
 namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -127,7 +131,11 @@ const char *fmha_status_string(int status) {
     }
 }
 
-int fmha_device_status(int reset) { return fmha::sm103_read_status(reset); }
+int fmha_device_status(int reset) {
+    const int a = fmha::sm103_read_status(reset);
+    const int b = fmha::gen_read_status(reset);
+    return a != FMHA_OK ? a : b;
+}
 
 int fmha_kv_tile_range(int q_row0, int q_rows, int Sq, int Sk, int mask, int causal_type,
                        int tile_n, int *n_tiles, int *n_unmasked) {

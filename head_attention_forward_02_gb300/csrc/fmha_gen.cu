@@ -1,0 +1,907 @@
+// fmha_gen.cu -- generation-phase attention forward for sm_103a: one new query
+// token per sequence against that sequence's entry of a K/V cache, and the
+// merge of the per-chunk partial results.
+//
+// Operation ("CUTLASS Blackwell FMHA 示例完全解析", §FMHA for Blackwell 生成阶段):
+// for sequence b, query head h, kv head g = h / G (G = H / H_k query heads per
+// kv head), cache entry e = batch_idx ? batch_idx[b] : b and L = seqlen[b]
+// cached tokens, the keys are K_cache[e, 0..L-1, g] and, unless the call is
+// cache-only, the new token's K_new[b, g], which is also written into the
+// cache at row L (V alike); O[b, h] = softmax(scale * q[b, h] K^T) V.  The
+// page fixes head dim 128 and one query-head group per thread block.
+//
+// The work is memory bound: every cached K/V byte is read once, and a group of
+// G <= 32 query heads does 4 * G flops per cached element pair.  The design
+// therefore aims at HBM bandwidth: the key range of every (sequence, kv head)
+// is cut into chunks so that all SMs stream at once, each CTA keeps three
+// 64 KB K/V stages in flight through TMA, and the contraction runs on the
+// tensor cores with the roles swapped so that the small head group is the N
+// dimension: S^T = K Q^T (M = 128 keys, N = 32 padded heads, K = 128) and
+// O^T = V^T P^T (M = 128 = head dim, N = 32, K = 128 keys).  Thread i of the
+// softmax warps owns key i of a tile (TMEM lane i) and, in the epilogue, head
+// dimension i of O^T.  The row maximum is kept lazily per head (rescale only
+// when a score exceeds the reference by 2^8), so the common tile needs no
+// cross-thread reduction; a named-barrier vote finds the rare tile that does.
+// Each chunk writes a normalised fp32 partial O and its LSE; a merge kernel
+// combines the chunks of every (b, h) by their LSE weights.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "fmha_common.h"
+
+namespace fmha {
+
+__device__ int g_gen_status;   // FMHA_OK, or the first error a generation kernel met
+
+namespace {
+
+constexpr int kD = 128;                 // head dim
+constexpr int kKT = 128;                // keys per tile (MMA M of S^T)
+constexpr int kNP = 32;                 // query heads of a group, padded (MMA N)
+constexpr int kNS = 3;                  // K/V ring stages, a K and a V tile each
+constexpr int kSoftWarps = 4;           // warps 0-3: softmax and epilogue
+constexpr int kProdWarp = 4;            // TMA producer (lane 0), cache insert
+constexpr int kMmaWarp = 5;             // tcgen05.mma issuer (lane 0), owns TMEM
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 64;      // S^T in [0, 32), O^T in [32, 64)
+constexpr int kPanelBytes = kKT * 128;  // 128 rows of one 128-byte swizzled panel
+constexpr int kTileBytes = 2 * kPanelBytes;           // 128 keys x 128 dims x 16 bit
+constexpr int kQPanelBytes = kNP * 128;
+constexpr int kQBytes = 2 * kQPanelBytes;             // 32 heads x 128 dims x 16 bit
+constexpr int kStageBytes = 2 * kTileBytes;           // K tile, then V tile
+constexpr int kPBytes = kKT * kNP * 2;                // P^T: 128 keys x 32 heads x 16 bit
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kOffQ + kQBytes;
+constexpr int kOffP = kOffKV + kNS * kStageBytes;
+constexpr int kOffBars = kOffP + kPBytes;
+constexpr int kSmemBytes = kOffBars + 1024 + 1024;    // barriers and scratch, 1 KB alignment
+constexpr unsigned long long kTimeoutNs = 4000000000ull;
+constexpr unsigned long long kDrainNs = 200000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;    // rescale when a head's max grows by more than 2^8
+
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+struct GenParams {
+    const void *q, *k_new, *v_new;      // q [B, H, D]; new K/V [B, H_k, D] (insert mode)
+    void *k_cache, *v_cache;            // [B_cache, S_max, H_k, D]
+    const int *seqlen, *batch_idx;      // device int32 [B]; batch_idx may be NULL
+    void *o;                            // [B, H, D]
+    float *lse;                         // [B, H] or NULL
+    float *part_o, *part_lse;           // [B*H][max_chunks][D], [B*H][max_chunks]
+    int B, H, H_k, G, B_cache, S_max;
+    int chunk, max_chunks;              // keys per work item (multiple of 128)
+    int insert, dtype;
+    float c;                            // scale * log2(e)
+    float out_scale;
+};
+
+struct GenBars {
+    uint64_t q_full, q_empty, s_full, p_full, o_full, drain;
+    uint64_t kv_full[kNS], kv_empty[kNS];
+    uint32_t tmem_base;
+    int abort;
+    float red[kSoftWarps][kNP];         // per-warp partial max / sum of each head
+};
+static_assert(sizeof(GenBars) <= 1024, "barrier block");
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: the phase completes, the CTA aborts, or kTimeoutNs pass (then
+// the timeout is recorded and the abort flag raised).
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kTimeoutNs) {
+                *abort_flag = 1;
+                atomicExch(&g_gen_status, FMHA_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort_flag);
+}
+
+// Bounded wait that ignores the abort flag (only while draining).
+__device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > kDrainNs) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                            int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor: start address and leading / stride byte
+// offsets in 16-byte units, descriptor version 1, swizzle mode (128 B = 2,
+// 64 B = 4).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint64_t swz) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (swz << 61);
+}
+
+// D[tmem] (+)= A[smem] * B[smem], kind::f16 (fp16 or bf16 inputs, fp32 accumulator)
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// Instruction descriptor: fp32 accumulator, A/B format (0 = f16, 1 = bf16),
+// A and B major-ness (0 = K-major, 1 = MN-major), N, M = 128.
+__host__ __device__ constexpr uint32_t gen_idesc(uint32_t fmt, bool a_mn, bool b_mn) {
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(kNP >> 3) << 17) | ((uint32_t)(kKT >> 4) << 24);
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// 32 consecutive TMEM columns of this thread's lane (32x32b shape).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+// Wait for this thread's TMEM loads; the register operands tie the values to the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Named barrier 1 over the 128 softmax threads, with a vote.
+__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool soft_all(bool v) {
+    uint32_t r;
+    asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 1, 128, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+                 : "=r"(r)
+                 : "r"((uint32_t)v)
+                 : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ bool soft_any(bool v) {
+    uint32_t r;
+    asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, 1, 128, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+                 : "=r"(r)
+                 : "r"((uint32_t)v)
+                 : "memory");
+    return r != 0;
+}
+
+template <bool BF>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    uint32_t r;
+    if constexpr (BF) asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    else asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// Work items: (sequence b, chunk c of its keys, kv head g), g fastest
+// ---------------------------------------------------------------------------
+
+// Keys of sequence b: its cached tokens, plus the new one unless cache-only.
+// A length outside [0, S_max - insert] is clamped and reported.
+__device__ __forceinline__ int gen_tokens(const GenParams &p, int b, bool report) {
+    int L = p.seqlen[b];
+    const int hi = p.S_max - p.insert;
+    if (L < 0 || L > hi) {
+        if (report) atomicCAS(&g_gen_status, FMHA_OK, FMHA_ERR_INVALID_ARG);
+        L = L < 0 ? 0 : hi;
+    }
+    return L;
+}
+
+__device__ __forceinline__ int gen_entry(const GenParams &p, int b, bool report) {
+    int e = p.batch_idx ? p.batch_idx[b] : b;
+    if (e < 0 || e >= p.B_cache) {
+        if (report) atomicCAS(&g_gen_status, FMHA_OK, FMHA_ERR_INVALID_ARG);
+        e = -1;   // reads of a missing entry are zero-filled; no insert
+    }
+    return e;
+}
+
+struct GenItem {
+    int b, g, c, entry, L, k0, k1;      // keys [k0, k1) of sequence b
+    bool len_ok;                        // seqlen[b] was within [0, S_max - insert]
+};
+
+struct GenCursor {                      // items are decoded in increasing order
+    int b = 0, base = 0;
+};
+
+__device__ bool gen_item(const GenParams &p, int u, GenCursor &cur, GenItem &it, bool report) {
+    int b = cur.b, base = cur.base;
+    for (;;) {
+        if (b >= p.B) {
+            cur.b = b;
+            cur.base = base;
+            return false;
+        }
+        const int n_keys = gen_tokens(p, b, false) + p.insert;
+        const int cnt = (n_keys + p.chunk - 1) / p.chunk * p.H_k;
+        if (u < base + cnt) break;
+        base += cnt;
+        ++b;
+    }
+    cur.b = b;
+    cur.base = base;
+    const int rem = u - base;
+    it.b = b;
+    it.c = rem / p.H_k;
+    it.g = rem - it.c * p.H_k;
+    it.L = gen_tokens(p, b, report && rem == 0);
+    it.len_ok = p.seqlen[b] == it.L;
+    it.entry = gen_entry(p, b, report && rem == 0);
+    it.k0 = it.c * p.chunk;
+    it.k1 = imin(it.k0 + p.chunk, it.L + p.insert);
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Roles
+// ---------------------------------------------------------------------------
+
+// TMA producer: per item, the new token's row into the cache (when this chunk
+// holds it), the 32-head Q tile, then the chunk's K/V tiles into the ring.
+__device__ void gen_producer(const GenParams &p, const CUtensorMap *tmQ, const CUtensorMap *tmK,
+                             const CUtensorMap *tmV, uint8_t *smem, GenBars *bars) {
+    volatile int *abort_flag = &bars->abort;
+    prefetch_tmap(tmQ);
+    prefetch_tmap(tmK);
+    prefetch_tmap(tmV);
+    uint32_t fill = 0, qn = 0;
+    bool ok = true;
+    GenCursor cur;
+    for (int r = 0; ok; ++r) {
+        GenItem it;
+        if (!gen_item(p, r * gridDim.x + blockIdx.x, cur, it, true)) break;
+        if (p.insert && it.len_ok && it.entry >= 0 && it.L >= it.k0 && it.L < it.k1) {
+            // 256-byte K and V rows of the new token; the async proxy (TMA)
+            // reads row L below, so order these generic writes before it
+            const int64_t src = ((int64_t)it.b * p.H_k + it.g) * kD;
+            const int64_t dst = (((int64_t)it.entry * p.S_max + it.L) * p.H_k + it.g) * kD;
+            const uint4 *kn = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.k_new) + src);
+            const uint4 *vn = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.v_new) + src);
+            uint4 *kc = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.k_cache) + dst);
+            uint4 *vc = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.v_cache) + dst);
+#pragma unroll 4
+            for (int i = 0; i < kD * 2 / 16; ++i) {
+                kc[i] = kn[i];
+                vc[i] = vn[i];
+            }
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        if (qn > 0 && !mbar_wait(smem_u32(&bars->q_empty), (qn - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+        }
+        const uint32_t qb = smem_u32(&bars->q_full);
+        mbar_expect_tx(qb, kQBytes);
+        const int qrow = it.b * p.H + it.g * p.G;
+        tma_load_2d(smem_u32(smem + kOffQ), tmQ, qb, 0, qrow);
+        tma_load_2d(smem_u32(smem + kOffQ + kQPanelBytes), tmQ, qb, 64, qrow);
+        ++qn;
+        for (int k = it.k0; k < it.k1; k += kKT) {
+            const int st = fill % kNS;
+            const uint32_t rnd = fill / kNS;
+            if (rnd > 0 && !mbar_wait(smem_u32(&bars->kv_empty[st]), (rnd - 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = smem_u32(&bars->kv_full[st]);
+            mbar_expect_tx(fb, kStageBytes);
+            const uint32_t dst = smem_u32(smem + kOffKV + st * kStageBytes);
+            const int e = it.entry >= 0 ? it.entry : p.B_cache;   // out of range: zero fill
+#pragma unroll
+            for (int pn = 0; pn < 2; ++pn) {
+                tma_load_4d(dst + pn * kPanelBytes, tmK, fb, pn * 64, it.g, k, e);
+                tma_load_4d(dst + kTileBytes + pn * kPanelBytes, tmV, fb, pn * 64, it.g, k, e);
+            }
+            ++fill;
+        }
+    }
+    if (ok) {
+        // every stage's and the Q tile's last release must arrive before exit
+        for (int st = 0; st < kNS; ++st) {
+            const uint32_t nf = fill > (uint32_t)st ? (fill - st + kNS - 1) / kNS : 0;
+            if (nf && !mbar_wait(smem_u32(&bars->kv_empty[st]), (nf - 1) & 1, abort_flag)) break;
+        }
+        if (qn) mbar_wait(smem_u32(&bars->q_empty), (qn - 1) & 1, abort_flag);
+    } else {
+        // aborted: let the copies already issued land before the CTA exits
+        const uint32_t first = fill > (uint32_t)kNS ? fill - kNS : 0;
+        for (uint32_t f = first; f < fill; ++f) mbar_wait_drain(smem_u32(&bars->kv_full[f % kNS]), (f / kNS) & 1);
+        if (qn) mbar_wait_drain(smem_u32(&bars->q_full), (qn - 1) & 1);
+    }
+}
+
+// MMA issuer (one lane): per tile, S^T = K Q^T, then (after the softmax wrote
+// P^T) O^T += V^T P^T.  The single issuing thread keeps the tensor pipe in
+// order, so "S^T of tile j+1 complete" implies "PV of tile j complete": the
+// softmax may then rewrite P^T and rescale O^T without another barrier.
+template <bool BF>
+__device__ void gen_mma(const GenParams &p, uint8_t *smem, GenBars *bars, uint32_t tmem) {
+    volatile int *abort_flag = &bars->abort;
+    constexpr uint32_t kIdS = gen_idesc(BF ? 1u : 0u, false, false);
+    constexpr uint32_t kIdPV = gen_idesc(BF ? 1u : 0u, true, true);
+    const uint32_t s_tm = tmem, o_tm = tmem + kNP;
+    const uint64_t q_desc = smem_desc(smem_u32(smem + kOffQ), 16, 1024, 2);
+    const uint64_t p_desc = smem_desc(smem_u32(smem + kOffP), kPBytes, 8 * 64, 4);   // MN-major, 64-byte rows
+    uint32_t cons = 0, qn = 0, pn = 0;
+    bool ok = true;
+    GenCursor cur;
+    for (int r = 0; ok; ++r) {
+        GenItem it;
+        if (!gen_item(p, r * gridDim.x + blockIdx.x, cur, it, false)) break;
+        if (!mbar_wait(smem_u32(&bars->q_full), qn & 1, abort_flag)) break;
+        ++qn;
+        bool first = true;
+        for (int k = it.k0; k < it.k1; k += kKT) {
+            const int st = cons % kNS;
+            if (!mbar_wait(smem_u32(&bars->kv_full[st]), (cons / kNS) & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            ++cons;
+            const uint32_t kaddr = smem_u32(smem + kOffKV + st * kStageBytes);
+            // S^T: A = K tile (K-major, 128 keys), B = Q tile (K-major, 32 heads);
+            // each k-step is 16 dims = 32 bytes within a 128-byte panel row
+            const uint64_t k_desc = smem_desc(kaddr, 16, 1024, 2);
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+                const uint32_t koff = (kk * 32 / 128) * kPanelBytes + (kk * 32) % 128;
+                const uint32_t qoff = (kk * 32 / 128) * kQPanelBytes + (kk * 32) % 128;
+                mma_ss(s_tm, k_desc + (koff >> 4), q_desc + (qoff >> 4), kIdS, kk > 0 ? 1u : 0u);
+            }
+            if (k + kKT >= it.k1) tc_commit(smem_u32(&bars->q_empty));
+            tc_commit(smem_u32(&bars->s_full));
+            if (!mbar_wait(smem_u32(&bars->p_full), pn & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            ++pn;
+            tc_fence_after();
+            // O^T: A = V tile MN-major (M = head dim over two 64-wide panels,
+            // LBO = panel stride), B = P^T MN-major (32 heads in one 64-byte
+            // swizzled row per key); each k-step is 16 keys
+            const uint64_t v_desc = smem_desc(kaddr + kTileBytes, kPanelBytes, 1024, 2);
+#pragma unroll
+            for (int kk = 0; kk < kKT / 16; ++kk)
+                mma_ss(o_tm, v_desc + ((kk * 16 * 128) >> 4), p_desc + ((kk * 16 * 64) >> 4), kIdPV,
+                       (!first || kk > 0) ? 1u : 0u);
+            tc_commit(smem_u32(&bars->kv_empty[st]));
+            first = false;
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&bars->o_full));
+    }
+    // no tensor-core operation may be in flight when TMEM is released
+    tc_commit(smem_u32(&bars->drain));
+    mbar_wait_drain(smem_u32(&bars->drain), 0);
+}
+
+// Softmax and epilogue: thread t of warps 0-3 owns key t of every tile (TMEM
+// lane t of S^T) and head dimension t of O^T.
+template <bool BF>
+__device__ void gen_softmax(const GenParams &p, uint8_t *smem, GenBars *bars, uint32_t tmem, int warp, int lane) {
+    volatile int *abort_flag = &bars->abort;
+    const int t = warp * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t s_tm = lane_base, o_tm = lane_base + kNP;
+    uint8_t *prow = smem + kOffP + t * 64;      // this key's P^T row (64-byte swizzle)
+    uint32_t sph = 0, oph = 0, cons = 0;
+    GenCursor cur;
+    for (int r = 0;; ++r) {
+        GenItem it;
+        if (!gen_item(p, r * gridDim.x + blockIdx.x, cur, it, false)) break;
+        float m[kNP], l[kNP];
+#pragma unroll
+        for (int h = 0; h < kNP; ++h) {
+            m[h] = -INFINITY;   // reference max (log2 units) P and O^T are relative to
+            l[h] = 0.f;         // this thread's part of the row sum
+        }
+        bool ok = true, first = true;
+        for (int k = it.k0; k < it.k1; k += kKT) {
+            const bool got = mbar_wait(smem_u32(&bars->s_full), sph, abort_flag);
+            sph ^= 1;
+            if (!soft_all(got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int st = cons % kNS;
+            ++cons;
+            uint32_t sr[32];
+            tmem_ld32(s_tm, sr);
+            tmem_wait_ld(sr);
+            const bool valid = k + t < it.k1;
+            float s[kNP];
+            bool need = false;
+#pragma unroll
+            for (int h = 0; h < kNP; ++h) {
+                s[h] = valid ? __uint_as_float(sr[h]) * p.c : -INFINITY;
+                need |= s[h] > m[h] + kRescaleLog2;
+            }
+            bool rescaled = false;
+            if (soft_any(need)) {
+                // tile maximum of every head over the 128 keys
+#pragma unroll
+                for (int h = 0; h < kNP; ++h) {
+                    float x = s[h];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+                    if (lane == 0) bars->red[warp][h] = x;
+                }
+                soft_sync();
+                float alpha[kNP];
+#pragma unroll
+                for (int h = 0; h < kNP; ++h) {
+                    const float tmax = fmaxf(fmaxf(bars->red[0][h], bars->red[1][h]),
+                                             fmaxf(bars->red[2][h], bars->red[3][h]));
+                    alpha[h] = 1.f;
+                    if (tmax > m[h] + kRescaleLog2) {
+                        alpha[h] = m[h] == -INFINITY ? 0.f : ex2(m[h] - tmax);
+                        l[h] *= alpha[h];
+                        m[h] = tmax;
+                    }
+                }
+                soft_sync();   // the scratch row may be rewritten after this
+                if (!first) {
+                    // O^T holds the PV of the previous tile (complete: this
+                    // tile's S^T was issued after it); row t, one column per head
+                    uint32_t orr[32];
+                    tmem_ld32(o_tm, orr);
+                    tmem_wait_ld(orr);
+#pragma unroll
+                    for (int h = 0; h < kNP; ++h) orr[h] = __float_as_uint(__uint_as_float(orr[h]) * alpha[h]);
+                    tmem_st32(o_tm, orr);
+                    rescaled = true;
+                }
+            }
+            // P^T row of key t: 32 heads, 64 bytes in four 16-byte chunks
+            // placed by the 64-byte swizzle (chunk index ^= (row / 2) % 4)
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float a = m[2 * i] == -INFINITY ? 0.f : ex2(s[2 * i] - m[2 * i]);
+                const float b = m[2 * i + 1] == -INFINITY ? 0.f : ex2(s[2 * i + 1] - m[2 * i + 1]);
+                l[2 * i] += a;
+                l[2 * i + 1] += b;
+                w[i] = pack2<BF>(a, b);
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4 *>(prow + ((c ^ ((t >> 1) & 3)) << 4)) =
+                    make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+            if (!valid) {
+                // a key past the chunk's end: its V row (stale cache contents,
+                // possibly not finite) is zeroed so that P = 0 contributes 0
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                uint8_t *vrow = smem + kOffKV + st * kStageBytes + kTileBytes + t * 128;
+#pragma unroll
+                for (int pn = 0; pn < 2; ++pn)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4 *>(vrow + pn * kPanelBytes + ((c ^ (t & 7)) << 4)) =
+                            make_uint4(0u, 0u, 0u, 0u);
+            }
+            // generic-proxy writes (P^T, zeroed V rows) become visible to the
+            // tensor core; TMEM stores complete; then publish
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (rescaled) tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+            first = false;
+        }
+        if (!ok) break;
+
+        // epilogue: row sums, then the normalised partial O and its LSE
+        const bool got = mbar_wait(smem_u32(&bars->o_full), oph, abort_flag);
+        oph ^= 1;
+        if (!soft_all(got)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int h = 0; h < kNP; ++h) {
+            float x = l[h];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            if (lane == 0) bars->red[warp][h] = x;
+        }
+        soft_sync();
+        float lt[kNP];
+#pragma unroll
+        for (int h = 0; h < kNP; ++h) lt[h] = (bars->red[0][h] + bars->red[1][h]) + (bars->red[2][h] + bars->red[3][h]);
+        soft_sync();
+        uint32_t orr[32];
+        tmem_ld32(o_tm, orr);
+        tmem_wait_ld(orr);
+        const int64_t row0 = (int64_t)it.b * p.H + (int64_t)it.g * p.G;
+#pragma unroll
+        for (int h = 0; h < kNP; ++h) {
+            if (h < p.G) {
+                const int64_t slot = (row0 + h) * p.max_chunks + it.c;
+                p.part_o[slot * kD + t] = lt[h] > 0.f ? __uint_as_float(orr[h]) / lt[h] : 0.f;
+                if (t == h) p.part_lse[slot] = lt[h] > 0.f ? (m[h] + log2f(lt[h])) * kLn2 : -INFINITY;
+            }
+        }
+    }
+}
+
+template <bool BF>
+__global__ void __launch_bounds__(kThreads, 1)
+    fmha_gen_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const GenParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    GenBars *bars = reinterpret_cast<GenBars *>(smem + kOffBars);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars->q_full), 1);
+        mbar_init(smem_u32(&bars->q_empty), 1);
+        mbar_init(smem_u32(&bars->s_full), 1);
+        mbar_init(smem_u32(&bars->p_full), kSoftWarps);
+        mbar_init(smem_u32(&bars->o_full), 1);
+        mbar_init(smem_u32(&bars->drain), 1);
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(smem_u32(&bars->kv_full[s]), 1);
+            mbar_init(smem_u32(&bars->kv_empty[s]), 1);
+        }
+        bars->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    if (warp < kSoftWarps) {
+        gen_softmax<BF>(p, smem, bars, tmem, warp, lane);
+    } else if (warp == kProdWarp) {
+        if (lane == 0) gen_producer(p, &tmQ, &tmK, &tmV, smem, bars);
+    } else {
+        if (lane == 0) gen_mma<BF>(p, smem, bars, tmem);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// One warp per (sequence, query head): O = out_scale * sum_c w_c O_c / sum_c w_c
+// with w_c = exp(LSE_c - max LSE), LSE = max + ln sum_c w_c.
+template <bool BF>
+__global__ void fmha_gen_merge_kernel(const GenParams p) {
+    const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= p.B * p.H) return;
+    const int b = row / p.H;
+    const int n_keys = gen_tokens(p, b, false) + p.insert;
+    const int nch = (n_keys + p.chunk - 1) / p.chunk;
+    const float *lse_c = p.part_lse + (int64_t)row * p.max_chunks;
+    float mx = -INFINITY;
+    for (int c = 0; c < nch; ++c) mx = fmaxf(mx, lse_c[c]);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, wsum = 0.f;
+    if (mx != -INFINITY) {
+        for (int c = 0; c < nch; ++c) {
+            const float w = __expf(lse_c[c] - mx);
+            const float4 v =
+                *reinterpret_cast<const float4 *>(p.part_o + ((int64_t)row * p.max_chunks + c) * kD + lane * 4);
+            wsum += w;
+            acc[0] += w * v.x;
+            acc[1] += w * v.y;
+            acc[2] += w * v.z;
+            acc[3] += w * v.w;
+        }
+    }
+    const float inv = wsum > 0.f ? p.out_scale / wsum : 0.f;
+    uint2 out;
+    out.x = pack2<BF>(acc[0] * inv, acc[1] * inv);
+    out.y = pack2<BF>(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.o) + (int64_t)row * kD + lane * 4) = out;
+    if (lane == 0 && p.lse) p.lse[row] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 gen_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+int gen_sm_count() {
+    static std::mutex mu;
+    static int cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// Keys per work item: whole 128-key tiles, sized so that caches filled to
+// S_max give about two work items per SM.
+int gen_chunk(int B, int H_k, int S_max, int sms) {
+    const int64_t tiles = (S_max + kKT - 1) / kKT;
+    const int64_t want = 2 * (int64_t)(sms > 0 ? sms : 1);
+    int64_t per = ((int64_t)B * H_k * tiles + want - 1) / want;
+    if (per < 1) per = 1;
+    if (per > tiles) per = tiles > 0 ? tiles : 1;
+    return (int)(per * kKT);
+}
+
+}  // namespace
+
+int gen_read_status(int reset) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_gen_status, sizeof(int)) != cudaSuccess) return FMHA_ERR_CUDA;
+    if (reset && v != 0) {
+        const int z = 0;
+        if (cudaMemcpyToSymbol(g_gen_status, &z, sizeof(int)) != cudaSuccess) return FMHA_ERR_CUDA;
+    }
+    return v;
+}
+
+}  // namespace fmha
+
+using namespace fmha;
+
+namespace {
+
+struct GenLayout {
+    int chunk, max_chunks;
+    size_t o_bytes, lse_off, total;
+};
+
+bool gen_layout(int B, int H, int H_k, int S_max, GenLayout *g) {
+    const int sms = gen_sm_count();
+    if (sms <= 0) return false;
+    g->chunk = gen_chunk(B, H_k, S_max, sms);
+    g->max_chunks = (S_max + g->chunk - 1) / g->chunk;
+    if (g->max_chunks < 1) g->max_chunks = 1;
+    const size_t rows = (size_t)B * H * g->max_chunks;
+    g->o_bytes = rows * kD * sizeof(float);
+    g->lse_off = (g->o_bytes + 255) / 256 * 256;
+    g->total = g->lse_off + rows * sizeof(float);
+    return true;
+}
+
+}  // namespace
+
+extern "C" size_t fmha_gen_workspace_size(int B, int H, int H_k, int D, int S_max) {
+    if (B <= 0 || H <= 0 || H_k <= 0 || H % H_k != 0 || D != kD || S_max <= 0) return 0;
+    GenLayout g;
+    if (!gen_layout(B, H, H_k, S_max, &g)) return 0;
+    return g.total;
+}
+
+extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_cache, fmha_tensor k_new,
+                            fmha_tensor v_new, fmha_tensor o, float *lse, int B, int H, int H_k, int D, int B_cache,
+                            int S_max, const int *seqlen, const int *batch_idx, float scale, float out_scale,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    // ---- host-side validation: nothing is launched on a bad argument ----
+    if (B < 0 || H <= 0 || H_k <= 0 || H % H_k != 0 || H / H_k > kNP || D != kD) return FMHA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !(scale < INFINITY) || !(out_scale == out_scale) || out_scale == INFINITY ||
+        out_scale == -INFINITY)
+        return FMHA_ERR_INVALID_ARG;
+    if ((k_new.data == nullptr) != (v_new.data == nullptr)) return FMHA_ERR_INVALID_ARG;
+    const bool insert = k_new.data != nullptr;
+    if (B == 0) return FMHA_OK;
+    if (S_max <= 0 || B_cache <= 0 || !seqlen) return FMHA_ERR_INVALID_ARG;
+    if (!q.data || !k_cache.data || !v_cache.data || !o.data) return FMHA_ERR_INVALID_ARG;
+    const int dt = q.dtype;
+    if (dt != FMHA_F16 && dt != FMHA_BF16) return FMHA_ERR_UNSUPPORTED;
+    if (k_cache.dtype != dt || v_cache.dtype != dt || o.dtype != dt) return FMHA_ERR_UNSUPPORTED;
+    if (insert && (k_new.dtype != dt || v_new.dtype != dt)) return FMHA_ERR_UNSUPPORTED;
+    auto misaligned = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+    if (misaligned(q.data) || misaligned(k_cache.data) || misaligned(v_cache.data) || misaligned(o.data) ||
+        (insert && (misaligned(k_new.data) || misaligned(v_new.data))))
+        return FMHA_ERR_UNSUPPORTED;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FMHA_ERR_INVALID_ARG;
+    GenLayout g;
+    if (!gen_layout(B, H, H_k, S_max, &g)) return FMHA_ERR_CUDA;
+    if (!workspace || workspace_bytes < g.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return FMHA_ERR_INVALID_ARG;
+
+    GenParams p{};
+    p.q = q.data;
+    p.k_new = k_new.data;
+    p.v_new = v_new.data;
+    p.k_cache = k_cache.data;
+    p.v_cache = v_cache.data;
+    p.seqlen = seqlen;
+    p.batch_idx = batch_idx;
+    p.o = o.data;
+    p.lse = lse;
+    p.part_o = static_cast<float *>(workspace);
+    p.part_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + g.lse_off);
+    p.B = B;
+    p.H = H;
+    p.H_k = H_k;
+    p.G = H / H_k;
+    p.B_cache = B_cache;
+    p.S_max = S_max;
+    p.chunk = g.chunk;
+    p.max_chunks = g.max_chunks;
+    p.insert = insert ? 1 : 0;
+    p.dtype = dt;
+    p.c = scale * kLog2e;
+    p.out_scale = out_scale;
+
+    // ---- tensor maps ----
+    auto fn = gen_encode_fn();
+    if (!fn) return FMHA_ERR_CUDA;
+    const CUtensorMapDataType tdt = dt == FMHA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap tq, tk, tv;
+    {
+        // q as [B*H rows, 128]: a box of 32 heads x 64 dims (one swizzle panel)
+        cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)B * H};
+        cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+        cuuint32_t box[2] = {64, (cuuint32_t)kNP};
+        cuuint32_t es[2] = {1, 1};
+        if (fn(&tq, tdt, 2, const_cast<void *>(q.data), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return FMHA_ERR_CUDA;
+    }
+    for (int kv = 0; kv < 2; ++kv) {
+        // cache as [B_cache, S_max, H_k, 128]: a box of 128 tokens x 64 dims of one head
+        cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H_k, (cuuint64_t)S_max, (cuuint64_t)B_cache};
+        cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)kD * 2 * H_k, (cuuint64_t)kD * 2 * H_k * S_max};
+        cuuint32_t box[4] = {64, 1, (cuuint32_t)kKT, 1};
+        cuuint32_t es[4] = {1, 1, 1, 1};
+        if (fn(kv ? &tv : &tk, tdt, 4, kv ? v_cache.data : k_cache.data, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return FMHA_ERR_CUDA;
+    }
+
+    // ---- launch: persistent CTAs over the work items, then the merge ----
+    const int sms = gen_sm_count();
+    const int64_t items = (int64_t)B * H_k * g.max_chunks;
+    const int grid = (int)(items < sms ? items : sms);
+    auto kern = dt == FMHA_BF16 ? fmha_gen_kernel<true> : fmha_gen_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+        return FMHA_ERR_CUDA;
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
+    const int rows = B * H;
+    auto merge = dt == FMHA_BF16 ? fmha_gen_merge_kernel<true> : fmha_gen_merge_kernel<false>;
+    merge<<<(rows + 7) / 8, 256, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
+    return FMHA_OK;
+}

@@ -70,6 +70,12 @@ def lib():
         L.fmha_fwd_splitkv_noalloc.argtypes = fwd_args[:-1] + [ctypes.c_int, ctypes.c_void_p]
         L.fmha_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
         L.fmha_fwd_splitkv_workspace_size.argtypes = [ctypes.c_int] * 5 + [ctypes.c_int64]
+        L.fmha_gen_fwd.restype = ctypes.c_int
+        L.fmha_gen_fwd.argtypes = [fmha_tensor] * 6 + [ctypes.c_void_p] + [ctypes.c_int] * 6 + [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_float, ctypes.c_void_p,
+            ctypes.c_size_t, ctypes.c_void_p]
+        L.fmha_gen_workspace_size.restype = ctypes.c_size_t
+        L.fmha_gen_workspace_size.argtypes = [ctypes.c_int] * 5
         L.fmha_status_string.restype = ctypes.c_char_p
         L.fmha_status_string.argtypes = [ctypes.c_int]
         L.fmha_device_status.restype = ctypes.c_int
@@ -224,6 +230,49 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Optional[fl
     name = "fmha_fwd" if impl == "tc" else "fmha_fwd_simt"
     rc = _call(name, q, k, v, out, lse, B, H, H_k, Sq, Sk, D, sc, out_scale, _MASKS[mask],
                _CAUSAL[causal_type], cu_seqlens_q, cu_seqlens_k, max_len or 0, T, stream)
+    if rc != OK:
+        raise FmhaError(rc, status_string(rc))
+    return out, lse
+
+
+def fmha_gen_fwd(q, k_cache, v_cache, k_new, v_new, o, lse, B, H, H_k, D, B_cache, S_max, seqlen,
+                 batch_idx, scale, out_scale, workspace, workspace_bytes, stream=None) -> int:
+    """Same arguments, order and status codes as the C function fmha_gen_fwd."""
+    dt = _TORCH_DTYPE[q.dtype] if isinstance(q, torch.Tensor) else None
+    return lib().fmha_gen_fwd(
+        _tensor(q), _tensor(k_cache), _tensor(v_cache), _tensor(k_new, dt), _tensor(v_new, dt), _tensor(o),
+        _ptr(lse), int(B), int(H), int(H_k), int(D), int(B_cache), int(S_max), _ptr(seqlen),
+        _ptr(batch_idx), float(scale), float(out_scale), _ptr(workspace), int(workspace_bytes),
+        _stream(stream))
+
+
+def fmha_gen_workspace_size(B, H, H_k, D, S_max) -> int:
+    return int(lib().fmha_gen_workspace_size(int(B), int(H), int(H_k), int(D), int(S_max)))
+
+
+def gen_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seqlen: torch.Tensor, *,
+            k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None,
+            batch_idx: Optional[torch.Tensor] = None, scale: Optional[float] = None,
+            out_scale: float = 1.0, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+            return_lse: bool = True, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Generation-phase attention on device tensors (see fmha_gen_fwd).
+
+    q [B, H, 128]; k_cache / v_cache [B_cache, S_max, H_k, 128]; seqlen int32
+    [B]; k_new / v_new [B, H_k, 128] (insert mode) or None (cache-only);
+    batch_idx int32 [B] or None.  Allocates O, LSE and the workspace with torch
+    when not given.  Returns (O, LSE)."""
+    B, H, D = q.shape
+    B_cache, S_max, H_k = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    nbytes = fmha_gen_workspace_size(B, H, H_k, D, S_max) if B > 0 else 0
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    sc = 1.0 / math.sqrt(D) if scale is None else scale
+    rc = fmha_gen_fwd(q, k_cache, v_cache, k_new, v_new, out, lse, B, H, H_k, D, B_cache, S_max, seqlen,
+                      batch_idx, sc, out_scale, workspace, max(nbytes, workspace.numel()), stream)
     if rc != OK:
         raise FmhaError(rc, status_string(rc))
     return out, lse

@@ -205,13 +205,71 @@ int fmha_fwd_splitkv_noalloc(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_t
                              const int *cu_seqlens_q, const int *cu_seqlens_k, int max_len,
                              int64_t total_length, int num_splits, cudaStream_t stream);
 
+/*
+ * fmha_gen_fwd -- generation phase: one new query token per sequence attends
+ * to that sequence's entry of a key/value cache ("CUTLASS Blackwell FMHA
+ * 示例完全解析", §FMHA for Blackwell 生成阶段: KV-cache forward with batch
+ * index remapping, cache-only mode and per-entry sequence lengths; head dim
+ * 128; one query-head group per thread block).
+ *
+ * For sequence b, query head h, kv head g = h / (H / H_k), cache entry
+ * e = batch_idx ? batch_idx[b] : b and L = seqlen[b] cached tokens:
+ *   keys   = K_cache[e, 0..L-1, g, :], then (insert mode) K_new[b, g, :]
+ *   values = V_cache[e, 0..L-1, g, :], then (insert mode) V_new[b, g, :]
+ *   O[b, h, :] = out_scale * softmax(scale * q[b, h, :] . keys) values
+ *   lse[b, h]  = natural-log log-sum-exp of the scaled scores
+ * (no key at all: O = 0, lse = -inf).  In insert mode (k_new.data and
+ * v_new.data both non-NULL) the call also writes K_new[b, g, :] and
+ * V_new[b, g, :] into row L of entry e of the caches; it does not change
+ * seqlen (the caller advances it).  Cache-only mode (both NULL) neither
+ * reads nor writes new rows.
+ *
+ * Layouts (contiguous, device memory):
+ *   q, o               [B, H, 128]
+ *   k_cache, v_cache   [B_cache, S_max, H_k, 128]
+ *   k_new, v_new       [B, H_k, 128]
+ *   seqlen, batch_idx  int32 [B] (batch_idx may be NULL: entry b)
+ *   lse                float [B, H], or NULL
+ * All tensors share one dtype, FMHA_F16 or FMHA_BF16; D must be 128 and
+ * H / H_k at most 32.  Device pointers must be 16-byte aligned.
+ * Requirements the host cannot check (they live in device memory):
+ * 0 <= seqlen[b] <= S_max - (insert ? 1 : 0) and 0 <= batch_idx[b] < B_cache;
+ * a kernel that meets a violation clamps the length (and inserts nothing) or
+ * reads zeros for the missing entry, and fmha_device_status then reports
+ * FMHA_ERR_INVALID_ARG.  In insert mode two sequences must not share an entry.
+ * Cached rows at or past a sequence's length are never used, and may hold any
+ * bits, including NaN.
+ *
+ * workspace: caller-owned scratch of at least fmha_gen_workspace_size(...)
+ * bytes, 256-byte aligned; nothing in it needs initialising; it must not be
+ * shared with a call that may run concurrently.  The call allocates nothing
+ * and is asynchronous on `stream` (a kernel, then a merge kernel).
+ * Returns FMHA_OK, FMHA_ERR_INVALID_ARG (bad sizes or pointers, scale not
+ * finite and > 0, workspace too small or misaligned, only one of k_new /
+ * v_new), FMHA_ERR_UNSUPPORTED (dtype, alignment) or FMHA_ERR_CUDA.
+ * B = 0 succeeds without a launch.
+ */
+int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_cache,
+                 fmha_tensor k_new, fmha_tensor v_new, fmha_tensor o, float *lse,
+                 int B, int H, int H_k, int D, int B_cache, int S_max,
+                 const int *seqlen, const int *batch_idx, float scale, float out_scale,
+                 void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Workspace bytes fmha_gen_fwd needs for these sizes on the current device
+ * (the key-range split depends on its SM count).  0 for invalid sizes.
+ */
+size_t fmha_gen_workspace_size(int B, int H, int H_k, int D, int S_max);
+
 /* Text for a status code (static storage, never NULL). */
 const char *fmha_status_string(int status);
 
 /*
  * fmha_device_status -- read the device-side status word of the current
- * device: FMHA_OK, or FMHA_ERR_TIMEOUT if a kernel gave up a bounded wait
- * (it then skipped its remaining work and released its resources).
+ * device: FMHA_OK, FMHA_ERR_TIMEOUT if a kernel gave up a bounded wait
+ * (it then skipped its remaining work and released its resources), or
+ * FMHA_ERR_INVALID_ARG if fmha_gen_fwd met a sequence length or cache entry
+ * outside its bounds.
  * Synchronises the device.  reset != 0 clears the word.  Returns
  * FMHA_ERR_CUDA if the word cannot be read.
  */

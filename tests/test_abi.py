@@ -146,3 +146,36 @@ def test_splitkv_validation(fm):
     assert call_split(fm, ws=P + 16) == -1                     # not 256-byte aligned
     assert call_split(fm, D=48) == -1
     assert call_split(fm, B=0, splits=3) == 0                  # nothing to do
+
+
+def call_gen(fm, **kw):
+    a = dict(q=P, kc=P, vc=P, kn=None, vn=None, o=P, lse=None, B=2, H=8, H_k=2, D=128, B_cache=2, S_max=64,
+             seqlen=P, bidx=None, scale=0.1, out_scale=1.0, ws=P, ws_bytes=1 << 30, dtypes=(1, 1, 1, 1))
+    a.update(kw)
+    dq, dkc, dvc, do = a.pop("dtypes")
+    t = fm.fmha_tensor
+    return fm.lib().fmha_gen_fwd(t(a["q"], dq), t(a["kc"], dkc), t(a["vc"], dvc), t(a["kn"], dq),
+                                 t(a["vn"], dq), t(a["o"], do), a["lse"], a["B"], a["H"], a["H_k"], a["D"],
+                                 a["B_cache"], a["S_max"], a["seqlen"], a["bidx"], a["scale"],
+                                 a["out_scale"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=64), -1), (dict(H=3, H_k=2), -1), (dict(H=64, H_k=1), -1), (dict(H_k=0), -1),
+    (dict(B=-1), -1), (dict(scale=0.0), -1), (dict(scale=float("inf")), -1),
+    (dict(out_scale=float("nan")), -1), (dict(kn=P), -1), (dict(vn=P), -1),
+    (dict(S_max=0), -1), (dict(B_cache=0), -1), (dict(seqlen=None), -1), (dict(q=None), -1),
+    (dict(o=None), -1), (dict(dtypes=(2, 2, 2, 2)), -2), (dict(dtypes=(1, 0, 1, 1)), -2),
+    (dict(q=P + 8), -2), (dict(kc=P + 2), -2), (dict(lse=P + 2), -1),
+])
+def test_gen_validation_rejects_before_any_launch(fm, kw, code):
+    assert call_gen(fm, **kw) == code
+
+
+def test_gen_empty_batch_succeeds_without_a_device(fm):
+    assert call_gen(fm, B=0, q=None, kc=None, vc=None, o=None, seqlen=None, ws=None) == 0
+
+
+def test_gen_workspace_size_rejects_bad_sizes(fm):
+    for bad in [(0, 8, 2, 128, 64), (2, 8, 3, 128, 64), (2, 8, 2, 64, 64), (2, 8, 2, 128, 0)]:
+        assert fm.fmha_gen_workspace_size(*bad) == 0
