@@ -51,10 +51,11 @@ constexpr int kPanelBytes = kKT * 128;  // 128 rows of one 128-byte swizzled pan
 constexpr int kTileBytes = 2 * kPanelBytes;           // 128 keys x 128 dims x 16 bit
 constexpr int kQPanelBytes = kNP * 128;
 constexpr int kQBytes = 2 * kQPanelBytes;             // 32 heads x 128 dims x 16 bit
+constexpr int kQSlots = 2;                            // Q tiles of consecutive work items
 constexpr int kStageBytes = 2 * kTileBytes;           // K tile, then V tile
 constexpr int kPBytes = kKT * kNP * 2;                // P^T: 128 keys x 32 heads x 16 bit
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQBytes;
+constexpr int kOffKV = kOffQ + kQSlots * kQBytes;
 constexpr int kOffP = kOffKV + kNS * kStageBytes;
 constexpr int kOffBars = kOffP + kPBytes;
 constexpr int kSmemBytes = kOffBars + 1024 + 1024;    // barriers and scratch, 1 KB alignment
@@ -72,20 +73,28 @@ struct GenParams {
     const int *seqlen, *batch_idx;      // device int32 [B]; batch_idx may be NULL
     void *o;                            // [B, H, D]
     float *lse;                         // [B, H] or NULL
-    float *part_o, *part_lse;           // [B*H][max_chunks][D], [B*H][max_chunks]
+    float *part_o, *part_lse;           // [B*H][max_seg][D], [B*H][max_seg]
     int B, H, H_k, G, B_cache, S_max;
-    int chunk, max_chunks;              // keys per work item (multiple of 128)
+    int max_seg;                        // partial results per (sequence, head): tiles of S_max + 1
+    int ncta;                           // CTAs of the attention kernel (the stream-K split)
     int insert, dtype;
     float c;                            // scale * log2(e)
     float out_scale;
 };
 
+struct GenSched {
+    int64_t per, G0, G1;                // this CTA's tiles [G0, G1)
+    int64_t off0;                       // first tile of sequence b0
+    int b0;                             // first sequence with a tile at or past G0
+};
+
 struct GenBars {
-    uint64_t q_full, q_empty, s_full, p_full, o_full, drain;
+    uint64_t q_full[kQSlots], q_empty[kQSlots], s_full, p_full, o_full, drain;
     uint64_t kv_full[kNS], kv_empty[kNS];
     uint32_t tmem_base;
     int abort;
     float red[kSoftWarps][kNP];         // per-warp partial max / sum of each head
+    GenSched sched;
 };
 static_assert(sizeof(GenBars) <= 1024, "barrier block");
 
@@ -315,41 +324,95 @@ __device__ __forceinline__ int gen_entry(const GenParams &p, int b, bool report)
     return e;
 }
 
+__device__ __forceinline__ int gen_tiles(const GenParams &p, int b) {
+    return (gen_tokens(p, b, false) + p.insert + kKT - 1) / kKT;
+}
+
+// Stream-K split: the 128-key tiles of every (sequence b, kv head g) pair, in
+// (b, g) order, form one sequence of T tiles; CTA i takes tiles
+// [i * per, (i + 1) * per) with per = ceil(T / gridDim.x), so every CTA
+// streams the same amount of K/V whatever the lengths.  A CTA's range is cut
+// at pair boundaries into segments; segment s of a pair is its part in the
+// s-th CTA that covers the pair, and writes partial slot s.
+
+// One warp: T, this CTA's range, and where its first segment starts.
+__device__ void gen_schedule(const GenParams &p, GenSched *sc, int lane) {
+    int64_t T = 0;
+    for (int b = lane; b < p.B; b += 32) T += (int64_t)p.H_k * gen_tiles(p, b);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) T += __shfl_xor_sync(0xffffffffu, T, o);
+    const int64_t per = (T + gridDim.x - 1) / gridDim.x;
+    const int64_t G0 = min((int64_t)blockIdx.x * per, T), G1 = min(G0 + per, T);
+    int b0 = p.B;
+    int64_t off0 = T, base = 0;
+    for (int bb = 0; bb < p.B && G0 < G1; bb += 32) {
+        const int b = bb + lane;
+        const int64_t n = b < p.B ? (int64_t)p.H_k * gen_tiles(p, b) : 0;
+        int64_t incl = n;                 // inclusive prefix over the 32 sequences
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, n > 0 && base + incl > G0);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            b0 = bb + l;
+            off0 = __shfl_sync(0xffffffffu, base + incl - n, l);
+            break;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+        sc->per = per;
+        sc->G0 = G0;
+        sc->G1 = G1;
+        sc->b0 = b0;
+        sc->off0 = off0;
+    }
+}
+
 struct GenItem {
-    int b, g, c, entry, L, k0, k1;      // keys [k0, k1) of sequence b
+    int b, g, entry, L, k0, k1;         // keys [k0, k1) of sequence b, kv head g
+    int seg;                            // partial slot of this segment
     bool len_ok;                        // seqlen[b] was within [0, S_max - insert]
 };
 
-struct GenCursor {                      // items are decoded in increasing order
-    int b = 0, base = 0;
+struct GenCursor {                      // next pair (b, g) and its first tile
+    int b = -1, g = 0;
+    int64_t off = 0;
 };
 
-__device__ bool gen_item(const GenParams &p, int u, GenCursor &cur, GenItem &it, bool report) {
-    int b = cur.b, base = cur.base;
-    for (;;) {
-        if (b >= p.B) {
-            cur.b = b;
-            cur.base = base;
-            return false;
-        }
-        const int n_keys = gen_tokens(p, b, false) + p.insert;
-        const int cnt = (n_keys + p.chunk - 1) / p.chunk * p.H_k;
-        if (u < base + cnt) break;
-        base += cnt;
-        ++b;
+__device__ bool gen_next(const GenParams &p, const GenSched &sc, GenCursor &cur, GenItem &it, bool report) {
+    if (cur.b < 0) {
+        cur.b = sc.b0;
+        cur.g = 0;
+        cur.off = sc.off0;
     }
-    cur.b = b;
-    cur.base = base;
-    const int rem = u - base;
-    it.b = b;
-    it.c = rem / p.H_k;
-    it.g = rem - it.c * p.H_k;
-    it.L = gen_tokens(p, b, report && rem == 0);
-    it.len_ok = p.seqlen[b] == it.L;
-    it.entry = gen_entry(p, b, report && rem == 0);
-    it.k0 = it.c * p.chunk;
-    it.k1 = imin(it.k0 + p.chunk, it.L + p.insert);
-    return true;
+    for (;;) {
+        if (cur.b >= p.B || cur.off >= sc.G1) return false;
+        const int nt = gen_tiles(p, cur.b);
+        const int64_t end = cur.off + nt;
+        const bool hit = nt > 0 && end > sc.G0;
+        if (hit) {
+            const int64_t t0 = max(sc.G0, cur.off) - cur.off, t1 = min(sc.G1, end) - cur.off;
+            const bool first = t0 == 0 && cur.g == 0;      // reports once per sequence
+            it.b = cur.b;
+            it.g = cur.g;
+            it.L = gen_tokens(p, cur.b, report && first);
+            it.len_ok = p.seqlen[cur.b] == it.L;
+            it.entry = gen_entry(p, cur.b, report && first);
+            it.k0 = (int)(t0 * kKT);
+            it.k1 = imin((int)(t1 * kKT), it.L + p.insert);
+            it.seg = (int)(blockIdx.x - cur.off / sc.per);
+        }
+        cur.off = end;
+        if (++cur.g == p.H_k) {
+            cur.g = 0;
+            ++cur.b;
+        }
+        if (hit) return true;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -358,8 +421,8 @@ __device__ bool gen_item(const GenParams &p, int u, GenCursor &cur, GenItem &it,
 
 // TMA producer: per item, the new token's row into the cache (when this chunk
 // holds it), the 32-head Q tile, then the chunk's K/V tiles into the ring.
-__device__ void gen_producer(const GenParams &p, const CUtensorMap *tmQ, const CUtensorMap *tmK,
-                             const CUtensorMap *tmV, uint8_t *smem, GenBars *bars) {
+__device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUtensorMap *tmQ,
+                             const CUtensorMap *tmK, const CUtensorMap *tmV, uint8_t *smem, GenBars *bars) {
     volatile int *abort_flag = &bars->abort;
     prefetch_tmap(tmQ);
     prefetch_tmap(tmK);
@@ -367,9 +430,9 @@ __device__ void gen_producer(const GenParams &p, const CUtensorMap *tmQ, const C
     uint32_t fill = 0, qn = 0;
     bool ok = true;
     GenCursor cur;
-    for (int r = 0; ok; ++r) {
+    while (ok) {
         GenItem it;
-        if (!gen_item(p, r * gridDim.x + blockIdx.x, cur, it, true)) break;
+        if (!gen_next(p, sc, cur, it, true)) break;
         if (p.insert && it.len_ok && it.entry >= 0 && it.L >= it.k0 && it.L < it.k1) {
             // 256-byte K and V rows of the new token; the async proxy (TMA)
             // reads row L below, so order these generic writes before it
@@ -386,15 +449,19 @@ __device__ void gen_producer(const GenParams &p, const CUtensorMap *tmQ, const C
             }
             asm volatile("fence.proxy.async.global;" ::: "memory");
         }
-        if (qn > 0 && !mbar_wait(smem_u32(&bars->q_empty), (qn - 1) & 1, abort_flag)) {
+        // Q slot qn % 2: free once the S^T MMAs of the item two back are done,
+        // so the K/V ring keeps streaming across item boundaries
+        const int qs = qn % kQSlots;
+        const uint32_t qr = qn / kQSlots;
+        if (qr > 0 && !mbar_wait(smem_u32(&bars->q_empty[qs]), (qr - 1) & 1, abort_flag)) {
             ok = false;
             break;
         }
-        const uint32_t qb = smem_u32(&bars->q_full);
+        const uint32_t qb = smem_u32(&bars->q_full[qs]);
         mbar_expect_tx(qb, kQBytes);
         const int qrow = it.b * p.H + it.g * p.G;
-        tma_load_2d(smem_u32(smem + kOffQ), tmQ, qb, 0, qrow);
-        tma_load_2d(smem_u32(smem + kOffQ + kQPanelBytes), tmQ, qb, 64, qrow);
+        tma_load_2d(smem_u32(smem + kOffQ + qs * kQBytes), tmQ, qb, 0, qrow);
+        tma_load_2d(smem_u32(smem + kOffQ + qs * kQBytes + kQPanelBytes), tmQ, qb, 64, qrow);
         ++qn;
         for (int k = it.k0; k < it.k1; k += kKT) {
             const int st = fill % kNS;
@@ -421,12 +488,14 @@ __device__ void gen_producer(const GenParams &p, const CUtensorMap *tmQ, const C
             const uint32_t nf = fill > (uint32_t)st ? (fill - st + kNS - 1) / kNS : 0;
             if (nf && !mbar_wait(smem_u32(&bars->kv_empty[st]), (nf - 1) & 1, abort_flag)) break;
         }
-        if (qn) mbar_wait(smem_u32(&bars->q_empty), (qn - 1) & 1, abort_flag);
+        for (uint32_t f = qn > kQSlots ? qn - kQSlots : 0; f < qn; ++f)
+            if (!mbar_wait(smem_u32(&bars->q_empty[f % kQSlots]), (f / kQSlots) & 1, abort_flag)) break;
     } else {
         // aborted: let the copies already issued land before the CTA exits
         const uint32_t first = fill > (uint32_t)kNS ? fill - kNS : 0;
         for (uint32_t f = first; f < fill; ++f) mbar_wait_drain(smem_u32(&bars->kv_full[f % kNS]), (f / kNS) & 1);
-        if (qn) mbar_wait_drain(smem_u32(&bars->q_full), (qn - 1) & 1);
+        for (uint32_t f = qn > kQSlots ? qn - kQSlots : 0; f < qn; ++f)
+            mbar_wait_drain(smem_u32(&bars->q_full[f % kQSlots]), (f / kQSlots) & 1);
     }
 }
 
@@ -435,21 +504,23 @@ __device__ void gen_producer(const GenParams &p, const CUtensorMap *tmQ, const C
 // order, so "S^T of tile j+1 complete" implies "PV of tile j complete": the
 // softmax may then rewrite P^T and rescale O^T without another barrier.
 template <bool BF>
-__device__ void gen_mma(const GenParams &p, uint8_t *smem, GenBars *bars, uint32_t tmem) {
+__device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, GenBars *bars, uint32_t tmem) {
     volatile int *abort_flag = &bars->abort;
     constexpr uint32_t kIdS = gen_idesc(BF ? 1u : 0u, false, false);
     constexpr uint32_t kIdPV = gen_idesc(BF ? 1u : 0u, true, true);
     const uint32_t s_tm = tmem, o_tm = tmem + kNP;
-    const uint64_t q_desc = smem_desc(smem_u32(smem + kOffQ), 16, 1024, 2);
+    const uint64_t q_desc0 = smem_desc(smem_u32(smem + kOffQ), 16, 1024, 2);
     const uint64_t p_desc = smem_desc(smem_u32(smem + kOffP), kPBytes, 8 * 64, 4);   // MN-major, 64-byte rows
     uint32_t cons = 0, qn = 0, pn = 0;
     bool ok = true;
     GenCursor cur;
-    for (int r = 0; ok; ++r) {
+    while (ok) {
         GenItem it;
-        if (!gen_item(p, r * gridDim.x + blockIdx.x, cur, it, false)) break;
-        if (!mbar_wait(smem_u32(&bars->q_full), qn & 1, abort_flag)) break;
+        if (!gen_next(p, sc, cur, it, false)) break;
+        const int qs = qn % kQSlots;
+        if (!mbar_wait(smem_u32(&bars->q_full[qs]), (qn / kQSlots) & 1, abort_flag)) break;
         ++qn;
+        const uint64_t q_desc = q_desc0 + ((qs * kQBytes) >> 4);
         bool first = true;
         for (int k = it.k0; k < it.k1; k += kKT) {
             const int st = cons % kNS;
@@ -468,7 +539,7 @@ __device__ void gen_mma(const GenParams &p, uint8_t *smem, GenBars *bars, uint32
                 const uint32_t qoff = (kk * 32 / 128) * kQPanelBytes + (kk * 32) % 128;
                 mma_ss(s_tm, k_desc + (koff >> 4), q_desc + (qoff >> 4), kIdS, kk > 0 ? 1u : 0u);
             }
-            if (k + kKT >= it.k1) tc_commit(smem_u32(&bars->q_empty));
+            if (k + kKT >= it.k1) tc_commit(smem_u32(&bars->q_empty[qs]));
             tc_commit(smem_u32(&bars->s_full));
             if (!mbar_wait(smem_u32(&bars->p_full), pn & 1, abort_flag)) {
                 ok = false;
@@ -498,7 +569,8 @@ __device__ void gen_mma(const GenParams &p, uint8_t *smem, GenBars *bars, uint32
 // Softmax and epilogue: thread t of warps 0-3 owns key t of every tile (TMEM
 // lane t of S^T) and head dimension t of O^T.
 template <bool BF>
-__device__ void gen_softmax(const GenParams &p, uint8_t *smem, GenBars *bars, uint32_t tmem, int warp, int lane) {
+__device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *smem, GenBars *bars, uint32_t tmem,
+                            int warp, int lane) {
     volatile int *abort_flag = &bars->abort;
     const int t = warp * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
@@ -506,9 +578,9 @@ __device__ void gen_softmax(const GenParams &p, uint8_t *smem, GenBars *bars, ui
     uint8_t *prow = smem + kOffP + t * 64;      // this key's P^T row (64-byte swizzle)
     uint32_t sph = 0, oph = 0, cons = 0;
     GenCursor cur;
-    for (int r = 0;; ++r) {
+    for (;;) {
         GenItem it;
-        if (!gen_item(p, r * gridDim.x + blockIdx.x, cur, it, false)) break;
+        if (!gen_next(p, sc, cur, it, false)) break;
         float m[kNP], l[kNP];
 #pragma unroll
         for (int h = 0; h < kNP; ++h) {
@@ -635,7 +707,7 @@ __device__ void gen_softmax(const GenParams &p, uint8_t *smem, GenBars *bars, ui
 #pragma unroll
         for (int h = 0; h < kNP; ++h) {
             if (h < p.G) {
-                const int64_t slot = (row0 + h) * p.max_chunks + it.c;
+                const int64_t slot = (row0 + h) * p.max_seg + it.seg;
                 p.part_o[slot * kD + t] = lt[h] > 0.f ? __uint_as_float(orr[h]) / lt[h] : 0.f;
                 if (t == h) p.part_lse[slot] = lt[h] > 0.f ? (m[h] + log2f(lt[h])) * kLn2 : -INFINITY;
             }
@@ -652,8 +724,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     GenBars *bars = reinterpret_cast<GenBars *>(smem + kOffBars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&bars->q_full), 1);
-        mbar_init(smem_u32(&bars->q_empty), 1);
+        for (int i = 0; i < kQSlots; ++i) {
+            mbar_init(smem_u32(&bars->q_full[i]), 1);
+            mbar_init(smem_u32(&bars->q_empty[i]), 1);
+        }
         mbar_init(smem_u32(&bars->s_full), 1);
         mbar_init(smem_u32(&bars->p_full), kSoftWarps);
         mbar_init(smem_u32(&bars->o_full), 1);
@@ -669,16 +743,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
         tmem_relinquish();
     }
+    if (warp == kProdWarp) gen_schedule(p, &bars->sched, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    const GenSched sc = bars->sched;
     if (warp < kSoftWarps) {
-        gen_softmax<BF>(p, smem, bars, tmem, warp, lane);
+        gen_softmax<BF>(p, sc, smem, bars, tmem, warp, lane);
     } else if (warp == kProdWarp) {
-        if (lane == 0) gen_producer(p, &tmQ, &tmK, &tmV, smem, bars);
+        if (lane == 0) gen_producer(p, sc, &tmQ, &tmK, &tmV, smem, bars);
     } else {
-        if (lane == 0) gen_mma<BF>(p, smem, bars, tmem);
+        if (lane == 0) gen_mma<BF>(p, sc, smem, bars, tmem);
     }
     tc_fence_before();
     __syncthreads();
@@ -689,36 +765,95 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// One warp per (sequence, query head): O = out_scale * sum_c w_c O_c / sum_c w_c
-// with w_c = exp(LSE_c - max LSE), LSE = max + ln sum_c w_c.
+// One CTA of kMergeThreads per (sequence, query head): O = out_scale *
+// sum_c w_c O_c / sum_c w_c with w_c = exp(LSE_c - max LSE), LSE = max +
+// ln sum_c w_c.  Eight groups of 32 threads take every eighth chunk (each
+// thread four of the 128 dims), so eight 512-byte partial rows are in flight.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeGroups = kMergeThreads / 32;
+
 template <bool BF>
-__global__ void fmha_gen_merge_kernel(const GenParams p) {
-    const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= p.B * p.H) return;
-    const int b = row / p.H;
-    const int n_keys = gen_tokens(p, b, false) + p.insert;
-    const int nch = (n_keys + p.chunk - 1) / p.chunk;
-    const float *lse_c = p.part_lse + (int64_t)row * p.max_chunks;
+__global__ void __launch_bounds__(kMergeThreads) fmha_gen_merge_kernel(const GenParams p) {
+    __shared__ float red_m[kMergeGroups];
+    __shared__ float4 red_o[kMergeGroups][32];
+    __shared__ float red_w[kMergeGroups];
+    __shared__ long long red_t[kMergeGroups], red_p[kMergeGroups];
+    const int row = blockIdx.x;
+    const int grp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = row / p.H, g = (row % p.H) / p.G;
+    // the attention kernel's split: total tiles, and the tiles before sequence b
+    long long tot = 0, pre = 0;
+    for (int bb = threadIdx.x; bb < p.B; bb += kMergeThreads) {
+        const long long n = (long long)p.H_k * gen_tiles(p, bb);
+        tot += n;
+        if (bb < b) pre += n;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        pre += __shfl_xor_sync(0xffffffffu, pre, o);
+    }
+    if (lane == 0) {
+        red_t[grp] = tot;
+        red_p[grp] = pre;
+    }
+    __syncthreads();
+    tot = 0;
+    pre = 0;
+#pragma unroll
+    for (int i = 0; i < kMergeGroups; ++i) {
+        tot += red_t[i];
+        pre += red_p[i];
+    }
+    const int nt = gen_tiles(p, b);
+    int nch = 0;                       // CTAs that covered this pair = its partial slots
+    if (nt > 0) {
+        const long long per = (tot + p.ncta - 1) / p.ncta;
+        const long long off = pre + (long long)g * nt;
+        nch = (int)((off + nt - 1) / per - off / per + 1);
+    }
+    const float *lse_c = p.part_lse + (int64_t)row * p.max_seg;
     float mx = -INFINITY;
-    for (int c = 0; c < nch; ++c) mx = fmaxf(mx, lse_c[c]);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f}, wsum = 0.f;
+    for (int c = threadIdx.x; c < nch; c += kMergeThreads) mx = fmaxf(mx, lse_c[c]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red_m[grp] = mx;
+    __syncthreads();
+    mx = red_m[0];
+#pragma unroll
+    for (int i = 1; i < kMergeGroups; ++i) mx = fmaxf(mx, red_m[i]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
     if (mx != -INFINITY) {
-        for (int c = 0; c < nch; ++c) {
+        for (int c = grp; c < nch; c += kMergeGroups) {
             const float w = __expf(lse_c[c] - mx);
             const float4 v =
-                *reinterpret_cast<const float4 *>(p.part_o + ((int64_t)row * p.max_chunks + c) * kD + lane * 4);
+                *reinterpret_cast<const float4 *>(p.part_o + ((int64_t)row * p.max_seg + c) * kD + lane * 4);
             wsum += w;
-            acc[0] += w * v.x;
-            acc[1] += w * v.y;
-            acc[2] += w * v.z;
-            acc[3] += w * v.w;
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
         }
     }
+    red_o[grp][lane] = acc;
+    if (lane == 0) red_w[grp] = wsum;
+    __syncthreads();
+    if (grp != 0) return;
+    for (int i = 1; i < kMergeGroups; ++i) {
+        const float4 v = red_o[i][lane];
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+        wsum += red_w[i];
+    }
+    if (lane != 0) wsum = 0.f;   // lane 0 holds group 0's sum; share the total
+    wsum = __shfl_sync(0xffffffffu, lane == 0 ? wsum : 0.f, 0);
     const float inv = wsum > 0.f ? p.out_scale / wsum : 0.f;
     uint2 out;
-    out.x = pack2<BF>(acc[0] * inv, acc[1] * inv);
-    out.y = pack2<BF>(acc[2] * inv, acc[3] * inv);
+    out.x = pack2<BF>(acc.x * inv, acc.y * inv);
+    out.y = pack2<BF>(acc.z * inv, acc.w * inv);
     *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.o) + (int64_t)row * kD + lane * 4) = out;
     if (lane == 0 && p.lse) p.lse[row] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
 }
@@ -753,17 +888,6 @@ int gen_sm_count() {
     return cached[dev];
 }
 
-// Keys per work item: whole 128-key tiles, sized so that caches filled to
-// S_max give about two work items per SM.
-int gen_chunk(int B, int H_k, int S_max, int sms) {
-    const int64_t tiles = (S_max + kKT - 1) / kKT;
-    const int64_t want = 2 * (int64_t)(sms > 0 ? sms : 1);
-    int64_t per = ((int64_t)B * H_k * tiles + want - 1) / want;
-    if (per < 1) per = 1;
-    if (per > tiles) per = tiles > 0 ? tiles : 1;
-    return (int)(per * kKT);
-}
-
 }  // namespace
 
 int gen_read_status(int reset) {
@@ -783,30 +907,27 @@ using namespace fmha;
 namespace {
 
 struct GenLayout {
-    int chunk, max_chunks;
+    int max_seg;
     size_t o_bytes, lse_off, total;
 };
 
-bool gen_layout(int B, int H, int H_k, int S_max, GenLayout *g) {
-    const int sms = gen_sm_count();
-    if (sms <= 0) return false;
-    g->chunk = gen_chunk(B, H_k, S_max, sms);
-    g->max_chunks = (S_max + g->chunk - 1) / g->chunk;
-    if (g->max_chunks < 1) g->max_chunks = 1;
-    const size_t rows = (size_t)B * H * g->max_chunks;
-    g->o_bytes = rows * kD * sizeof(float);
-    g->lse_off = (g->o_bytes + 255) / 256 * 256;
-    g->total = g->lse_off + rows * sizeof(float);
-    return true;
+// Partial slots per (sequence, head): a pair of n tiles meets at most n + 1
+// CTAs' ranges, and n <= ceil(S_max / 128).
+GenLayout gen_layout(int B, int H, int S_max) {
+    GenLayout g;
+    g.max_seg = (S_max + kKT - 1) / kKT + 1;
+    const size_t rows = (size_t)B * H * g.max_seg;
+    g.o_bytes = rows * kD * sizeof(float);
+    g.lse_off = (g.o_bytes + 255) / 256 * 256;
+    g.total = g.lse_off + rows * sizeof(float);
+    return g;
 }
 
 }  // namespace
 
 extern "C" size_t fmha_gen_workspace_size(int B, int H, int H_k, int D, int S_max) {
     if (B <= 0 || H <= 0 || H_k <= 0 || H % H_k != 0 || D != kD || S_max <= 0) return 0;
-    GenLayout g;
-    if (!gen_layout(B, H, H_k, S_max, &g)) return 0;
-    return g.total;
+    return gen_layout(B, H, S_max).total;
 }
 
 extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_cache, fmha_tensor k_new,
@@ -832,8 +953,9 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
         (insert && (misaligned(k_new.data) || misaligned(v_new.data))))
         return FMHA_ERR_UNSUPPORTED;
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FMHA_ERR_INVALID_ARG;
-    GenLayout g;
-    if (!gen_layout(B, H, H_k, S_max, &g)) return FMHA_ERR_CUDA;
+    const GenLayout g = gen_layout(B, H, S_max);
+    const int sms = gen_sm_count();
+    if (sms <= 0) return FMHA_ERR_CUDA;
     if (!workspace || workspace_bytes < g.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return FMHA_ERR_INVALID_ARG;
 
@@ -855,8 +977,8 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
     p.G = H / H_k;
     p.B_cache = B_cache;
     p.S_max = S_max;
-    p.chunk = g.chunk;
-    p.max_chunks = g.max_chunks;
+    p.max_seg = g.max_seg;
+    p.ncta = sms;
     p.insert = insert ? 1 : 0;
     p.dtype = dt;
     p.c = scale * kLog2e;
@@ -891,9 +1013,7 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
     }
 
     // ---- launch: persistent CTAs over the work items, then the merge ----
-    const int sms = gen_sm_count();
-    const int64_t items = (int64_t)B * H_k * g.max_chunks;
-    const int grid = (int)(items < sms ? items : sms);
+    const int grid = sms;   // one persistent CTA per SM; each streams 1/grid of the tiles
     auto kern = dt == FMHA_BF16 ? fmha_gen_kernel<true> : fmha_gen_kernel<false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
         return FMHA_ERR_CUDA;
@@ -901,7 +1021,7 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
     const int rows = B * H;
     auto merge = dt == FMHA_BF16 ? fmha_gen_merge_kernel<true> : fmha_gen_merge_kernel<false>;
-    merge<<<(rows + 7) / 8, 256, 0, stream>>>(p);
+    merge<<<rows, kMergeThreads, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
     return FMHA_OK;
 }

@@ -179,3 +179,11 @@ def test_gen_empty_batch_succeeds_without_a_device(fm):
 def test_gen_workspace_size_rejects_bad_sizes(fm):
     for bad in [(0, 8, 2, 128, 64), (2, 8, 3, 128, 64), (2, 8, 2, 64, 64), (2, 8, 2, 128, 0)]:
         assert fm.fmha_gen_workspace_size(*bad) == 0
+
+
+def test_gen_workspace_size(fm):
+    # fp32 partial O then (256-byte aligned) LSE, ceil(S_max/128)+1 slots per (sequence, head)
+    B, H, S_max = 3, 8, 1000
+    slots = B * H * ((S_max + 127) // 128 + 1)
+    o_bytes = slots * 128 * 4
+    assert fm.fmha_gen_workspace_size(B, H, 2, 128, S_max) == (o_bytes + 255) // 256 * 256 + slots * 4
