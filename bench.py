@@ -31,9 +31,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from head_attention_forward_02_gb300 import workloads as wl  # noqa: E402
-from head_attention_forward_02_gb300.metrics import algorithmic_bytes, attention_flops  # noqa: E402
+from head_attention_forward_02_gb300.metrics import (algorithmic_bytes, attention_flops, gen_bytes,  # noqa: E402
+                                                     gen_flops)
 
 DEFAULT_CONFIG = "bf16_causal_gqa_b2_h32_hk8_s8192_d128"
+DEFAULT_GEN_CONFIG = "gen_bf16_b32_h32_hk8_s8192"
 L2_BYTES = 129 * 2 ** 20
 KERNEL_SOURCES = ["head_attention_forward_02_gb300/csrc/fmha_sm103.cu",
                   "head_attention_forward_02_gb300/csrc/fmha_common.h"]
@@ -44,7 +46,11 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--op", default="fwd", choices=["fwd", "gen"],
+                    help="fwd: the fused forward (fmha_fwd); gen: generation phase against a "
+                         "K/V cache (fmha_gen_fwd)")
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(wl.CONFIGS))
+    ap.add_argument("--gen-config", default=DEFAULT_GEN_CONFIG, choices=list(wl.GEN_CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--kernel", default="tc", choices=["tc", "simt"],
                     help="tc: tcgen05 kernel (fmha_fwd); simt: CUDA-core cross-check kernel")
@@ -491,6 +497,209 @@ def run_ours(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def gen_source_hash() -> str:
+    """Hash of the generation kernel's source (profiles carry it)."""
+    h = hashlib.sha256()
+    for f in ("fmha_gen.cu", "fmha_common.h"):
+        h.update(open(os.path.join(ROOT, "head_attention_forward_02_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def gen_profiled_traffic(workload: str):
+    want = gen_source_hash()
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        text = open(path).read()
+        kv = dict(re.findall(r"^- ?(workload|source_sha256|traffic_bytes_per_launch): *(\S+)",
+                             text, flags=re.M))
+        if kv.get("workload") == workload and kv.get("source_sha256") == want:
+            try:
+                return float(kv["traffic_bytes_per_launch"])
+            except (KeyError, ValueError):
+                return None
+    return None
+
+
+def time_gen_oracle(inp, target_s: float):
+    """The generation oracle on the first sequences of the workload (one more
+    each round) until about target_s of CPU work; returns (bytes, seconds,
+    sequences, threads)."""
+    import oracle
+    oracle.build()
+    w = inp.w
+    odt = oracle.BF16 if w.dtype == "bf16" else oracle.F16
+    threads = cpu_threads()
+    n, total_b, total_t = 1, 0.0, 0.0
+    while True:
+        sl = inp.seqlen[:n].numpy()
+        args = [wl.bits(inp.q[:n]), wl.bits(inp.k_cache[:n]), wl.bits(inp.v_cache[:n]),
+                wl.bits(inp.k_new[:n]) if inp.k_new is not None else None,
+                wl.bits(inp.v_new[:n]) if inp.v_new is not None else None]
+        t = time.perf_counter()
+        oracle.gen_fwd(*args, odt, n, w.H, w.H_k, 128, n, w.S_max, sl, None, 128 ** -0.5, 1.0,
+                       threads=threads)
+        dt = time.perf_counter() - t
+        total_b, total_t = gen_bytes(n, w.H, w.H_k, sl.tolist(), w.insert, 2), dt
+        if dt >= target_s or n >= w.B:
+            return total_b, total_t, n, threads
+        n = min(w.B, max(n + 1, int(n * target_s / max(dt, 1e-3))))
+
+
+def run_gen(args, rank, world, local):
+    """Generation phase (fmha_gen_fwd) on a synthetic K/V cache; one JSON line
+    on the HBM roofline."""
+    from head_attention_forward_02_gb300 import build, fmha as fm
+    build.build()
+    fm.lib()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    w = wl.GEN_CONFIGS[args.gen_config]
+    stream = torch.cuda.current_stream(dev)
+    inp = wl.generate_gen(w)
+    d = {"q": inp.q.to(dev), "kc": inp.k_cache.to(dev), "vc": inp.v_cache.to(dev),
+         "kn": inp.k_new.to(dev) if inp.k_new is not None else None,
+         "vn": inp.v_new.to(dev) if inp.v_new is not None else None,
+         "sl": inp.seqlen.to(dev)}
+    d["o"] = torch.empty_like(d["q"])
+    d["lse"] = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
+    nws = fm.fmha_gen_workspace_size(w.B, w.H, w.H_k, 128, w.S_max)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    cache_bytes = 2 * d["kc"].numel() * d["kc"].element_size()
+    nbytes = gen_bytes(w.B, w.H, w.H_k, inp.seqlen.tolist(), w.insert, d["q"].element_size())
+    flops = gen_flops(w.H, inp.seqlen.tolist(), w.insert)
+
+    def step():
+        fm.gen_fwd(d["q"], d["kc"], d["vc"], d["sl"], k_new=d["kn"], v_new=d["vn"], out=d["o"],
+                   lse=d["lse"], workspace=ws, stream=stream)
+
+    sampler = ClockSampler(gpu_uuid(dev.index or 0))
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fm.device_status(reset=True) != 0:
+        raise RuntimeError("device status reports an error")
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(K):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t_host1 = time.time()
+    if rank == 0:
+        sampler.stop()
+    if fm.device_status(reset=True) != 0:
+        raise RuntimeError("device status reports an error")
+    ms_per_step = max_over_ranks(ev0.elapsed_time(ev1) / K, world)
+    launch_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / K, world)
+    value = world * nbytes / (ms_per_step * 1e-3) / 1e9
+
+    # end to end: the cache stays resident; every step copies the new token's
+    # q (and K/V rows) and the lengths in from pinned memory, and O and LSE out
+    h = {k: inp_t.pin_memory() for k, inp_t in (("q", inp.q), ("kn", inp.k_new), ("vn", inp.v_new),
+                                                 ("sl", inp.seqlen)) if inp_t is not None}
+    ho = torch.empty(d["o"].shape, dtype=d["o"].dtype).pin_memory()
+    hl = torch.empty(d["lse"].shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        for k, t in h.items():
+            d[k].copy_(t, non_blocking=True)
+        step()
+        ho.copy_(d["o"], non_blocking=True)
+        hl.copy_(d["lse"], non_blocking=True)
+
+    e2e_steps = args.e2e_steps or max(3, min(K, 50))
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = ho.numel() * ho.element_size() + hl.numel() * 4
+    if rank != 0:
+        return
+    peaks, peak_src = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    achieved = nbytes / (launch_ms * 1e-3) / 1e9
+    line = {
+        "metric": "generation-phase attention HBM bandwidth (GB/s) and % of measured copy rate",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1) cache, query and new rows)",
+        "config": {"workload": args.gen_config, "op": "fmha_gen_fwd", "B": w.B, "H": w.H, "H_k": w.H_k,
+                   "D": 128, "S_max": w.S_max, "lengths": w.lengths, "insert": w.insert,
+                   "cached_tokens": int(inp.seqlen.sum()),
+                   "l2": f"K/V cache of {cache_bytes / 2**30:.2f} GiB (> L2) read once per step",
+                   "parallelism": f"replicas x{world} (independent problems)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "peak_source": f"hbm_gbs of {peak_src}",
+                     "traffic": gen_profiled_traffic(args.gen_config), "algorithmic_bytes": nbytes,
+                     "algorithmic_flops": flops, "launch_ms": round(launch_ms, 5)},
+        "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * K,
+        "clocks": sampler.summary(t_host0, t_host1),
+    }
+    if not args.no_cpu_baseline:
+        b, t, n, threads = time_gen_oracle(inp, target_s=10.0)
+        line["cpu_baseline"] = {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"the first {n} of {w.B} sequences, all heads "
+                                          f"({b / 1e9:.2f} GB of the workload, {t:.1f} s)"}
+    print(json.dumps(line), flush=True)
+
+
+def run_gen_reference(args, rank, world):
+    """The generation oracle as the reference arm: each step one sequence of the
+    workload (all heads), on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = wl.GEN_CONFIGS[args.gen_config]
+    inp = wl.generate_gen(w)
+    odt = oracle.BF16 if w.dtype == "bf16" else oracle.F16
+    threads = cpu_threads()
+
+    def one(b):
+        sl = inp.seqlen[b:b + 1].numpy()
+        oracle.gen_fwd(wl.bits(inp.q[b:b + 1]), wl.bits(inp.k_cache[b:b + 1]), wl.bits(inp.v_cache[b:b + 1]),
+                       wl.bits(inp.k_new[b:b + 1]) if inp.k_new is not None else None,
+                       wl.bits(inp.v_new[b:b + 1]) if inp.v_new is not None else None, odt, 1, w.H, w.H_k,
+                       128, 1, w.S_max, sl, None, 128 ** -0.5, 1.0, threads=threads)
+        return gen_bytes(1, w.H, w.H_k, sl.tolist(), w.insert, 2)
+
+    for i in range(args.warmup):
+        one(i % w.B)
+    t = time.perf_counter()
+    nb = sum(one((args.warmup + i) % w.B) for i in range(args.steps))
+    dt = time.perf_counter() - t
+    value = nb / dt / 1e9
+    print(json.dumps({
+        "metric": "generation-phase attention HBM bandwidth (GB/s) and % of measured copy rate",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": args.gen_config}, "impl": "reference",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": "one sequence (all heads) per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+        flush=True)
+
+
 def run_reference(args, rank, world):
     """The CPU oracle as the reference arm: each step is a bounded seeded sample
     of query rows of the same workload."""
@@ -540,11 +749,11 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
-        run_reference(args, rank, world)
+        (run_gen_reference if args.op == "gen" else run_reference)(args, rank, world)
         return
     rank, world, local = dist_setup(args.gpus)
     try:
-        run_ours(args, rank, world, local)
+        (run_gen if args.op == "gen" else run_ours)(args, rank, world, local)
     finally:
         if world > 1:
             import torch.distributed as dist

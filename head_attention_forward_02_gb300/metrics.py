@@ -33,3 +33,20 @@ def algorithmic_bytes(B: int, H: int, H_k: int, Sq: int, Sk: int, D: int, elem_b
     rd = tq * H * D * elem_bytes + 2 * tk * H_k * D * elem_bytes
     wr = tq * H * D * out_bytes + (tq * H * 4 if with_lse else 0)
     return float(rd + wr)
+
+
+def gen_bytes(B: int, H: int, H_k: int, seqlens: Sequence[int], insert: bool, elem_bytes: int,
+              D: int = 128, with_lse: bool = True) -> float:
+    """Algorithmic HBM bytes of one generation-phase call: every cached K and V
+    row of the attended tokens read once, the new K/V rows read and written into
+    the cache (insert mode), q read, O (and LSE) written."""
+    rows = sum(int(L) for L in seqlens)
+    kv = 2.0 * rows * H_k * D * elem_bytes
+    new = (2.0 * 2.0 * B * H_k * D * elem_bytes) if insert else 0.0
+    qo = 2.0 * B * H * D * elem_bytes
+    return kv + new + qo + (4.0 * B * H if with_lse else 0.0)
+
+
+def gen_flops(H: int, seqlens: Sequence[int], insert: bool, D: int = 128) -> float:
+    """The two products of the definition for one query row per head: 4*D per key."""
+    return sum(4.0 * H * (int(L) + (1 if insert else 0)) * D for L in seqlens)

@@ -142,3 +142,59 @@ CONFIGS = {
         "e4m3_nomask_b1_h16_s16384_d128", dtype="e4m3", B=1, H=16, H_k=16, Sq=16384,
         Sk=16384, D=128, mask="none", out_scale=1.0, seed=5),
 }
+
+
+# ----------------------------------------------------------------------------
+# Generation phase: one new query token per sequence against a K/V cache
+# ----------------------------------------------------------------------------
+
+@dataclass
+class GenWorkload:
+    name: str
+    dtype: str = "bf16"
+    B: int = 1
+    H: int = 32
+    H_k: int = 8
+    S_max: int = 8192
+    lengths: str = "full"          # "full": S_max - 1 cached tokens; "uniform": U[S_max/8, S_max-1]
+    insert: bool = True            # new K/V row written into the cache and attended
+    seed: int = 1
+
+
+@dataclass
+class GenInputs:
+    w: GenWorkload
+    q: torch.Tensor                # [B, H, 128]
+    k_cache: torch.Tensor          # [B, S_max, H_k, 128]
+    v_cache: torch.Tensor
+    k_new: Optional[torch.Tensor]  # [B, H_k, 128] or None (cache-only)
+    v_new: Optional[torch.Tensor]
+    seqlen: torch.Tensor           # int32 [B]
+
+
+def generate_gen(w: GenWorkload, seed: Optional[int] = None) -> GenInputs:
+    """Seeded N(0,1) query, caches and new rows; every cache row is finite."""
+    gen = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    D = 128
+    q = _randn((w.B, w.H, D), gen, w.dtype)
+    kc = _randn((w.B, w.S_max, w.H_k, D), gen, w.dtype)
+    vc = _randn((w.B, w.S_max, w.H_k, D), gen, w.dtype)
+    kn = _randn((w.B, w.H_k, D), gen, w.dtype) if w.insert else None
+    vn = _randn((w.B, w.H_k, D), gen, w.dtype) if w.insert else None
+    top = w.S_max - (1 if w.insert else 0)
+    if w.lengths == "full":
+        sl = torch.full((w.B,), top, dtype=torch.int32)
+    else:
+        sl = torch.randint(max(1, w.S_max // 8), top + 1, (w.B,), generator=gen, dtype=torch.int32)
+    return GenInputs(w, q, kc, vc, kn, vn, sl)
+
+
+GEN_CONFIGS = {
+    "gen_bf16_b32_h32_hk8_s8192": GenWorkload("gen_bf16_b32_h32_hk8_s8192", B=32, H=32, H_k=8, S_max=8192,
+                                              lengths="full", seed=21),
+    "gen_bf16_varlen_b64_h32_hk8_s16384": GenWorkload("gen_bf16_varlen_b64_h32_hk8_s16384", B=64, H=32, H_k=8,
+                                                      S_max=16384, lengths="uniform", seed=22),
+    "gen_f16_b8_h64_hk2_s32768_cacheonly": GenWorkload("gen_f16_b8_h64_hk2_s32768_cacheonly", dtype="f16", B=8,
+                                                       H=64, H_k=2, S_max=32768, lengths="full", insert=False,
+                                                       seed=23),
+}
