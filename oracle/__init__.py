@@ -68,6 +68,13 @@ def _load():
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_double, ctypes.c_double,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_attn_fwd_f64.restype = ctypes.c_int
+        lib.oracle_attn_fwd_f64.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [
+            ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_attn_bwd_f64.restype = ctypes.c_int
+        lib.oracle_attn_bwd_f64.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 5 + [
+            ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -169,3 +176,34 @@ def gen_fwd(q_bits: np.ndarray, k_cache_bits: np.ndarray, v_cache_bits: np.ndarr
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return o, lse
+
+
+def attn_fwd_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, mask: int = MASK_NONE,
+                 causal_type: int = QBEGIN) -> Tuple[np.ndarray, np.ndarray]:
+    """Forward on real values: q [B,Sq,H,D], k/v [B,Sk,H,D] (float64) -> O [B,Sq,H,D], LSE [B,H,Sq]."""
+    lib = _load()
+    q, k, v = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    o = np.empty_like(q)
+    lse = np.empty((B, H, Sq), dtype=np.float64)
+    if lib.oracle_attn_fwd_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, Sq, Sk, D, float(scale),
+                               mask, causal_type, o.ctypes.data, lse.ctypes.data) != 0:
+        raise ValueError("oracle rejected the arguments")
+    return o, lse
+
+
+def attn_bwd_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray, scale: float,
+                 mask: int = MASK_NONE, causal_type: int = QBEGIN, threads: int = 0):
+    """Backward on real values: (dQ, dK, dV) for upstream gradient dout [B,Sq,H,D].
+    See ``oracle_attn_bwd_f64`` in ``fmha_oracle.c`` for the definition."""
+    lib = _load()
+    q, k, v, g = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v, dout))
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    if lib.oracle_attn_bwd_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data, B, H, Sq, Sk, D,
+                               float(scale), mask, causal_type, dq.ctypes.data, dk.ctypes.data,
+                               dv.ctypes.data, int(threads)) != 0:
+        raise ValueError("oracle rejected the arguments")
+    return dq, dk, dv

@@ -428,3 +428,131 @@ int oracle_gen_fwd(const void *q, const void *k_cache, const void *v_cache,
     free(table);
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Backward pass, on real (already decoded) values.                           */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Source: "CUTLASS Blackwell FMHA 示例完全解析", §FMHA for Blackwell 反向
+ * (Backward): the backward pass produces dQ, dK and dV from dO, uses the row
+ * sums of O * dO, supports causal masking (a key past the query's position
+ * plus the q-end offset, or outside the problem, is masked to -infinity) and
+ * no GQA.  What it differentiates is the forward definition above:
+ *     P = softmax_j(scale * Q K^T + mask),  O = P V.
+ * For a loss with gradient dO the chain rule gives, per (b, h):
+ *     dV_j  = sum_i P_ij dO_i
+ *     dP_ij = dO_i . V_j
+ *     D_i   = sum_j P_ij dP_ij            (= dO_i . O_i)
+ *     dS_ij = P_ij (dP_ij - D_i)
+ *     dQ_i  = scale * sum_j dS_ij K_j ,   dK_j = scale * sum_i dS_ij Q_i
+ * Layouts as the forward (fixed length): q, dq, do [B, Sq, H, D];
+ * k, v, dk, dv [B, Sk, H, D] (H_k = H).  All arrays are double.  Rows without
+ * a visible key contribute nothing.  Returns 0, or -1 on bad arguments.
+ */
+int oracle_attn_fwd_f64(const double *q, const double *k, const double *v, int B, int H, int Sq, int Sk,
+                        int D, double scale, int mask, int causal_type, double *o, double *lse) {
+    if (B < 0 || H <= 0 || Sq < 0 || Sk < 0 || D <= 0) return -1;
+    double *s = (double *)malloc((size_t)(Sk > 0 ? Sk : 1) * sizeof(double));
+    if (!s) return -1;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t h = 0; h < H; ++h)
+            for (int64_t i = 0; i < Sq; ++i) {
+                const double *qi = q + ((b * Sq + i) * H + h) * D;
+                double m = -INFINITY;
+                for (int64_t j = 0; j < Sk; ++j) {
+                    if (!key_allowed(mask, causal_type, i, j, Sq, Sk)) { s[j] = -INFINITY; continue; }
+                    const double *kj = k + ((b * Sk + j) * H + h) * D;
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d) dot += qi[d] * kj[d];
+                    s[j] = scale * dot;
+                    if (s[j] > m) m = s[j];
+                }
+                double *oi = o + ((b * Sq + i) * H + h) * D;
+                for (int d = 0; d < D; ++d) oi[d] = 0.0;
+                if (m == -INFINITY) { lse[(b * H + h) * Sq + i] = -INFINITY; continue; }
+                double l = 0.0;
+                for (int64_t j = 0; j < Sk; ++j) {
+                    if (s[j] == -INFINITY) continue;
+                    const double p = exp(s[j] - m);
+                    const double *vj = v + ((b * Sk + j) * H + h) * D;
+                    l += p;
+                    for (int d = 0; d < D; ++d) oi[d] += p * vj[d];
+                }
+                for (int d = 0; d < D; ++d) oi[d] /= l;
+                lse[(b * H + h) * Sq + i] = m + log(l);
+            }
+    free(s);
+    return 0;
+}
+
+int oracle_attn_bwd_f64(const double *q, const double *k, const double *v, const double *dout, int B, int H,
+                        int Sq, int Sk, int D, double scale, int mask, int causal_type, double *dq, double *dk,
+                        double *dv, int n_threads) {
+    if (B < 0 || H <= 0 || Sq < 0 || Sk < 0 || D <= 0) return -1;
+    const int64_t nq = (int64_t)B * Sq * H * D, nk = (int64_t)B * Sk * H * D;
+    for (int64_t x = 0; x < nq; ++x) dq[x] = 0.0;
+    for (int64_t x = 0; x < nk; ++x) { dk[x] = 0.0; dv[x] = 0.0; }
+#ifdef _OPENMP
+    if (n_threads <= 0) n_threads = omp_get_max_threads();
+#pragma omp parallel num_threads(n_threads)
+#endif
+    {
+        double *p = (double *)malloc((size_t)(Sk > 0 ? Sk : 1) * sizeof(double));
+        double *dp = (double *)malloc((size_t)(Sk > 0 ? Sk : 1) * sizeof(double));
+        /* one (b, h) per task: dK and dV rows of (b, h) are written by that task only */
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t bh = 0; bh < (int64_t)B * H; ++bh) {
+            const int64_t b = bh / H, h = bh % H;
+            for (int64_t i = 0; i < Sq; ++i) {
+                const double *qi = q + ((b * Sq + i) * H + h) * D;
+                const double *gi = dout + ((b * Sq + i) * H + h) * D;
+                /* P row: softmax of the visible scaled scores */
+                double m = -INFINITY;
+                for (int64_t j = 0; j < Sk; ++j) {
+                    if (!key_allowed(mask, causal_type, i, j, Sq, Sk)) { p[j] = -INFINITY; continue; }
+                    const double *kj = k + ((b * Sk + j) * H + h) * D;
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d) dot += qi[d] * kj[d];
+                    p[j] = scale * dot;
+                    if (p[j] > m) m = p[j];
+                }
+                if (m == -INFINITY) continue;
+                double l = 0.0;
+                for (int64_t j = 0; j < Sk; ++j) {
+                    p[j] = p[j] == -INFINITY ? 0.0 : exp(p[j] - m);
+                    l += p[j];
+                }
+                /* dP = dO_i . V_j, and D_i = sum_j P_ij dP_ij */
+                double Di = 0.0;
+                for (int64_t j = 0; j < Sk; ++j) {
+                    p[j] /= l;
+                    if (p[j] == 0.0) { dp[j] = 0.0; continue; }
+                    const double *vj = v + ((b * Sk + j) * H + h) * D;
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d) dot += gi[d] * vj[d];
+                    dp[j] = dot;
+                    Di += p[j] * dot;
+                }
+                double *dqi = dq + ((b * Sq + i) * H + h) * D;
+                for (int64_t j = 0; j < Sk; ++j) {
+                    if (p[j] == 0.0) continue;
+                    const double ds = p[j] * (dp[j] - Di);
+                    const double *kj = k + ((b * Sk + j) * H + h) * D;
+                    double *dkj = dk + ((b * Sk + j) * H + h) * D;
+                    double *dvj = dv + ((b * Sk + j) * H + h) * D;
+                    for (int d = 0; d < D; ++d) {
+                        dqi[d] += scale * ds * kj[d];
+                        dkj[d] += scale * ds * qi[d];
+                        dvj[d] += p[j] * gi[d];
+                    }
+                }
+            }
+        }
+        free(p);
+        free(dp);
+    }
+    return 0;
+}
