@@ -12,7 +12,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfmha.so")
-SOURCES = ["fmha_api.cu", "fmha_simt.cu", "fmha_sm103.cu", "fmha_splitkv.cu", "fmha_gen.cu"]
+SOURCES = ["fmha_api.cu", "fmha_simt.cu", "fmha_sm103.cu", "fmha_splitkv.cu", "fmha_gen.cu", "fmha_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -10,6 +10,7 @@
 
 namespace fmha {
 int gen_read_status(int reset);   // fmha_gen.cu: the generation kernels' status word
+int bwd_read_status(int reset);   // fmha_bwd.cu: the backward kernels' status word
 }
 
 namespace fmha {
@@ -134,7 +135,8 @@ const char *fmha_status_string(int status) {
 int fmha_device_status(int reset) {
     const int a = fmha::sm103_read_status(reset);
     const int b = fmha::gen_read_status(reset);
-    return a != FMHA_OK ? a : b;
+    const int c = fmha::bwd_read_status(reset);
+    return a != FMHA_OK ? a : (b != FMHA_OK ? b : c);
 }
 
 int fmha_kv_tile_range(int q_row0, int q_rows, int Sq, int Sk, int mask, int causal_type,

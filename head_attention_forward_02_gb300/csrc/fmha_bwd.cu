@@ -1,0 +1,879 @@
+// fmha_bwd.cu -- backward pass of the fused attention forward on sm_103a:
+// dQ, dK and dV from dO, the forward's O and its log-sum-exp.
+//
+// Definition ("CUTLASS Blackwell FMHA 示例完全解析", §FMHA for Blackwell 反向
+// (Backward)): with P = softmax(scale Q K^T + mask) and O = P V, per (b, h)
+//     D_i   = dO_i . O_i                       (the row sums of O * dO)
+//     P_ij  = exp(scale q_i . k_j - LSE_i)     (LSE from the forward pass)
+//     dP_ij = dO_i . v_j ,   dS_ij = P_ij (dP_ij - D_i)
+//     dQ_i  = scale sum_j dS_ij k_j ,  dK_j = scale sum_i dS_ij q_i ,
+//     dV_j  = sum_i P_ij dO_i .
+// The page describes three kernels (row sums of O * dO; the main kernel,
+// itself split into a dK/dV kernel and a dQ kernel; a dQ conversion), Q and
+// K blocking of 128, TMA loads, causal masking (a key past the query's
+// position plus the q-offset, or outside the problem, is masked), head dims
+// 64 and 128, and no GQA.
+//
+// This file: a row-sum kernel, then two tcgen05 kernels that each recompute
+// S and dP for their tiles, so that every output tile has one owner and no
+// atomics are needed.  The dQ kernel owns a 128-row Q tile and loops over key
+// tiles: S = Q K^T and dP = dO V^T (both A and B K-major from shared memory)
+// land in TMEM; four warps (one query row per thread) form dS and write it
+// back over S as 16-bit values; dQ += dS K is a TMEM-A MMA with K read
+// MN-major.  The dK/dV kernel owns a 128-key tile and loops over query tiles:
+// S^T = K Q^T and dP^T = V dO^T; one key per thread; P^T and dS^T go back over
+// S^T and dP^T; dV += P^T dO and dK += dS^T Q.  Each kernel writes its output
+// in the input type directly (no fp32 dQ round trip).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "fmha_common.h"
+
+namespace fmha {
+
+__device__ int g_bwd_status;   // FMHA_OK, or FMHA_ERR_TIMEOUT after a bounded wait expired
+
+namespace {
+
+constexpr int kT = 128;                 // rows per tile, both sides
+constexpr int kCompWarps = 4;           // warps 0-3: elementwise work and epilogue
+constexpr int kProdWarp = 4;            // TMA producer (all lanes: the dK/dV kernel's row vectors)
+constexpr int kMmaWarp = 5;             // tcgen05.mma issuer (lane 0), owns TMEM
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr unsigned long long kTimeoutNs = 4000000000ull;
+constexpr unsigned long long kDrainNs = 200000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum Mode { kDQ = 0, kDKDV = 1 };
+
+template <int D_>
+struct BCfg {
+    static constexpr int D = D_;
+    static constexpr int ROW = D * 2;                       // bytes per row (16-bit types)
+    static constexpr int SW = ROW >= 128 ? 128 : ROW;       // swizzle span
+    static constexpr int PANELS = ROW / SW;
+    static constexpr int BOX_D = SW / 2;
+    static constexpr int PANEL_BYTES = kT * SW;
+    static constexpr int TILE_BYTES = kT * ROW;
+    static constexpr uint64_t SW_CODE = SW == 128 ? 2 : 4;  // 128-byte or 64-byte swizzle
+    static constexpr int SBO = 8 * SW;
+    static constexpr int OWN = 0;                           // two owned tiles
+    static constexpr int RING = 2 * TILE_BYTES;             // two stages of two tiles
+    static constexpr int VEC = RING + 2 * 2 * TILE_BYTES;   // per stage: LSE*log2e and D, 128 floats each
+    static constexpr int BARS = VEC + 2 * 2 * kT * 4;
+    // at least 120 KB so that a second CTA never shares the SM: each
+    // allocates all 512 TMEM columns; plus 1 KB to align for the swizzle
+    static constexpr int SMEM_USED = BARS + 256;
+    static constexpr int SMEM_BYTES = (SMEM_USED < 120 * 1024 ? 120 * 1024 : SMEM_USED) + 1024;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    // TMEM columns
+    static constexpr int S_COL = 0, DP_COL = 128, ACC0 = 256, ACC1 = 256 + D;
+    static_assert(ACC1 + D <= (int)kTmemCols, "TMEM budget");
+};
+
+struct BwdParams {
+    const void *q, *k, *v, *o, *dout;   // q, o, dout [B, Sq, H, D]; k, v [B, Sk, H, D]
+    const float *lse;                   // [B, H, Sq] natural-log LSE of the forward
+    float *dvec;                        // [B, H, Sq] D_i = dO_i . O_i (workspace)
+    void *dq, *dk, *dv;
+    int B, H, Sq, Sk;
+    float scale, c2;                    // c2 = scale * log2(e)
+    int mask, causal_type, off;         // off = Sk - Sq for a q-end causal mask, else 0
+};
+
+struct BwdBars {
+    uint64_t own_full, own_empty, s_full, c_full, acc_full, drain;
+    uint64_t st_full[2], st_empty[2];
+    uint32_t tmem_base;
+    int abort;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kTimeoutNs) {
+                *abort_flag = 1;
+                atomicExch(&g_bwd_status, FMHA_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait: the phase completes, the CTA aborts, or kTimeoutNs pass.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort_flag);
+}
+
+__device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > kDrainNs) return false;
+    }
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    const bool r = mbar_wait(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, r);
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                            int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint64_t swz) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (swz << 61);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__host__ __device__ constexpr uint32_t bwd_idesc(uint32_t fmt, int n, bool b_mn) {
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(kT >> 4) << 24);
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld2(uint32_t (&a)[32], uint32_t (&b)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+                   "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]),
+                   "+r"(a[15]), "+r"(a[16]), "+r"(a[17]), "+r"(a[18]), "+r"(a[19]), "+r"(a[20]), "+r"(a[21]),
+                   "+r"(a[22]), "+r"(a[23]), "+r"(a[24]), "+r"(a[25]), "+r"(a[26]), "+r"(a[27]), "+r"(a[28]),
+                   "+r"(a[29]), "+r"(a[30]), "+r"(a[31])
+                 :
+                 : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]),
+                   "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]),
+                   "+r"(b[15]), "+r"(b[16]), "+r"(b[17]), "+r"(b[18]), "+r"(b[19]), "+r"(b[20]), "+r"(b[21]),
+                   "+r"(b[22]), "+r"(b[23]), "+r"(b[24]), "+r"(b[25]), "+r"(b[26]), "+r"(b[27]), "+r"(b[28]),
+                   "+r"(b[29]), "+r"(b[30]), "+r"(b[31])
+                 :
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld1(uint32_t (&a)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+                   "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]),
+                   "+r"(a[15]), "+r"(a[16]), "+r"(a[17]), "+r"(a[18]), "+r"(a[19]), "+r"(a[20]), "+r"(a[21]),
+                   "+r"(a[22]), "+r"(a[23]), "+r"(a[24]), "+r"(a[25]), "+r"(a[26]), "+r"(a[27]), "+r"(a[28]),
+                   "+r"(a[29]), "+r"(a[30]), "+r"(a[31])
+                 :
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <bool BF>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    uint32_t r;
+    if constexpr (BF) asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    else asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+template <bool BF>
+__device__ __forceinline__ float to_f32(uint16_t x) {
+    if constexpr (BF) return __uint_as_float((uint32_t)x << 16);
+    else return __half2float(__ushort_as_half(x));
+}
+
+// Is key kk visible to query qq (both inside the problem)?
+__device__ __forceinline__ bool visible(const BwdParams &p, int qq, int kk) {
+    return qq < p.Sq && kk < p.Sk && (p.mask != FMHA_MASK_CAUSAL || kk <= qq + p.off);
+}
+
+// ---------------------------------------------------------------------------
+// Work units: (b, h, owned tile); the loop covers the tiles of the other side
+// that hold a visible pair.
+// ---------------------------------------------------------------------------
+
+struct BUnit {
+    int b, h, row0;                     // owned tile's first row (query row for dQ, key row for dK/dV)
+    int j0, j1;                         // loop tiles [j0, j1)
+};
+
+template <int MODE>
+__device__ __forceinline__ bool bwd_unit(const BwdParams &p, int u, BUnit &U) {
+    const int own_tiles = MODE == kDQ ? (p.Sq + kT - 1) / kT : (p.Sk + kT - 1) / kT;
+    const int per = p.B * p.H;
+    if (u >= per * own_tiles) return false;
+    const int r = u / per, rem = u - r * per;
+    U.b = rem / p.H;
+    U.h = rem - U.b * p.H;
+    const bool causal = p.mask == FMHA_MASK_CAUSAL;
+    if (MODE == kDQ) {
+        // heaviest first: later query tiles see more keys under a causal mask
+        const int t = causal ? own_tiles - 1 - r : r;
+        U.row0 = t * kT;
+        int nt, nu;
+        kv_tile_range(U.row0, kT, p.Sq, p.Sk, p.mask, p.causal_type, kT, &nt, &nu);
+        U.j0 = 0;
+        U.j1 = nt;
+    } else {
+        // heaviest first: earlier key tiles are seen by more queries
+        const int t = r;
+        U.row0 = t * kT;
+        const int q_tiles = (p.Sq + kT - 1) / kT;
+        int first = 0;
+        if (causal) {
+            const int q_first = U.row0 - p.off;          // first query that sees key row0
+            first = q_first <= 0 ? 0 : q_first / kT;
+        }
+        U.j0 = imin(first, q_tiles);
+        U.j1 = (p.Sk > U.row0) ? q_tiles : U.j0;
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Roles
+// ---------------------------------------------------------------------------
+
+// Producer: the owned pair of tiles, then the loop pairs through a 2-stage
+// ring; in dK/dV mode the warp also writes each loop tile's 128 values of
+// LSE * log2(e) and D_i into the stage.
+template <class C, int MODE>
+__device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const CUtensorMap *tmK,
+                             const CUtensorMap *tmV, const CUtensorMap *tmO, uint8_t *smem, BwdBars *bars,
+                             int lane) {
+    volatile int *abort_flag = &bars->abort;
+    if (lane == 0) {
+        prefetch_tmap(tmQ);
+        prefetch_tmap(tmK);
+        prefetch_tmap(tmV);
+        prefetch_tmap(tmO);
+    }
+    // the owned tiles come from (Q, dO) for dQ and (K, V) for dK/dV; the loop
+    // tiles from the other pair
+    const CUtensorMap *own0 = MODE == kDQ ? tmQ : tmK, *own1 = MODE == kDQ ? tmO : tmV;
+    const CUtensorMap *ld0 = MODE == kDQ ? tmK : tmQ, *ld1 = MODE == kDQ ? tmV : tmO;
+    uint32_t fill = 0, owned = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok; u += gridDim.x) {
+        BUnit U;
+        if (!bwd_unit<MODE>(p, u, U)) break;
+        if (U.j0 >= U.j1) continue;
+        if (owned > 0 && !warp_wait(smem_u32(&bars->own_empty), (owned - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+        }
+        if (lane == 0) {
+            const uint32_t fb = smem_u32(&bars->own_full);
+            mbar_expect_tx(fb, 2 * C::TILE_BYTES);
+#pragma unroll
+            for (int pn = 0; pn < C::PANELS; ++pn) {
+                tma_load_4d(smem_u32(smem + C::OWN + pn * C::PANEL_BYTES), own0, fb, pn * C::BOX_D, U.h, U.row0, U.b);
+                tma_load_4d(smem_u32(smem + C::OWN + C::TILE_BYTES + pn * C::PANEL_BYTES), own1, fb, pn * C::BOX_D,
+                            U.h, U.row0, U.b);
+            }
+        }
+        ++owned;
+        for (int j = U.j0; j < U.j1; ++j) {
+            const int st = fill & 1;
+            const uint32_t rnd = fill >> 1;
+            if (rnd > 0 && !warp_wait(smem_u32(&bars->st_empty[st]), (rnd - 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = smem_u32(&bars->st_full[st]);
+            if (lane == 0) {
+                mbar_expect_tx(fb, 2 * C::TILE_BYTES);
+                const uint32_t dst = smem_u32(smem + C::RING + st * 2 * C::TILE_BYTES);
+#pragma unroll
+                for (int pn = 0; pn < C::PANELS; ++pn) {
+                    tma_load_4d(dst + pn * C::PANEL_BYTES, ld0, fb, pn * C::BOX_D, U.h, j * kT, U.b);
+                    tma_load_4d(dst + C::TILE_BYTES + pn * C::PANEL_BYTES, ld1, fb, pn * C::BOX_D, U.h, j * kT, U.b);
+                }
+            }
+            if constexpr (MODE == kDKDV) {
+                float *vec = reinterpret_cast<float *>(smem + C::VEC) + st * 2 * kT;
+                const int64_t base = ((int64_t)U.b * p.H + U.h) * p.Sq;
+#pragma unroll
+                for (int i = 0; i < kT / 32; ++i) {
+                    const int q = j * kT + i * 32 + lane;
+                    const bool in = q < p.Sq;
+                    vec[i * 32 + lane] = in ? p.lse[base + q] * kLog2e : INFINITY;
+                    vec[kT + i * 32 + lane] = in ? p.dvec[base + q] : 0.f;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(fb);
+            }
+            ++fill;
+        }
+    }
+    if (ok) {
+        // the last releases of every stage and of the owned tiles
+        for (int st = 0; st < 2; ++st) {
+            const uint32_t nf = fill > (uint32_t)st ? (fill - st + 1) / 2 : 0;
+            if (nf && !warp_wait(smem_u32(&bars->st_empty[st]), (nf - 1) & 1, abort_flag)) break;
+        }
+        if (owned) warp_wait(smem_u32(&bars->own_empty), (owned - 1) & 1, abort_flag);
+    } else if (lane == 0) {
+        const uint32_t first = fill > 2 ? fill - 2 : 0;
+        for (uint32_t f = first; f < fill; ++f) mbar_wait_drain(smem_u32(&bars->st_full[f & 1]), (f >> 1) & 1);
+        if (owned) mbar_wait_drain(smem_u32(&bars->own_full), (owned - 1) & 1);
+    }
+}
+
+// MMA issuer (one lane).  Per loop tile: S and dP (both SS, K-major), then,
+// once the compute warps wrote dS (and P^T), the accumulating MMA(s) with A
+// from TMEM and B = a loop tile read MN-major.  In-order issue makes "S of
+// tile j+1 complete" imply "the accumulation of tile j complete".
+template <class C, bool BF, int MODE>
+__device__ void bwd_mma(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem) {
+    volatile int *abort_flag = &bars->abort;
+    constexpr uint32_t fmt = BF ? 1u : 0u;
+    constexpr uint32_t kIdS = bwd_idesc(fmt, kT, false);
+    constexpr uint32_t kIdAcc = bwd_idesc(fmt, C::D, true);
+    const uint32_t own = smem_u32(smem + C::OWN);
+    uint32_t cons = 0, owned = 0, cc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok; u += gridDim.x) {
+        BUnit U;
+        if (!bwd_unit<MODE>(p, u, U)) break;
+        if (U.j0 >= U.j1) continue;
+        if (!mbar_wait(smem_u32(&bars->own_full), owned & 1, abort_flag)) break;
+        ++owned;
+        const uint64_t a0 = smem_desc(own, 16, C::SBO, C::SW_CODE);                     // owned tile 0
+        const uint64_t a1 = smem_desc(own + C::TILE_BYTES, 16, C::SBO, C::SW_CODE);     // owned tile 1
+        for (int j = U.j0; j < U.j1; ++j) {
+            const int st = cons & 1;
+            if (!mbar_wait(smem_u32(&bars->st_full[st]), (cons >> 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            ++cons;
+            const uint32_t ring = smem_u32(smem + C::RING + st * 2 * C::TILE_BYTES);
+            const uint64_t b0 = smem_desc(ring, 16, C::SBO, C::SW_CODE);
+            const uint64_t b1 = smem_desc(ring + C::TILE_BYTES, 16, C::SBO, C::SW_CODE);
+            // S (or S^T) = own0 . ld0^T and dP (or dP^T) = own1 . ld1^T over the head dim
+#pragma unroll
+            for (int kk = 0; kk < C::D / 16; ++kk) {
+                const uint32_t off = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
+                mma_ss(tmem + C::S_COL, a0 + off, b0 + off, kIdS, kk > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = 0; kk < C::D / 16; ++kk) {
+                const uint32_t off = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
+                mma_ss(tmem + C::DP_COL, a1 + off, b1 + off, kIdS, kk > 0 ? 1u : 0u);
+            }
+            if (j == U.j1 - 1) tc_commit(smem_u32(&bars->own_empty));
+            tc_commit(smem_u32(&bars->s_full));
+            if (!mbar_wait(smem_u32(&bars->c_full), cc & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            ++cc;
+            tc_fence_after();
+            // accumulate over the 128 loop rows (16 per MMA): A = 16-bit values in
+            // TMEM (8 columns per step), B = loop tile rows, MN-major
+            const uint32_t acc = j > U.j0 ? 1u : 0u;
+            if constexpr (MODE == kDQ) {
+                const uint64_t bk = smem_desc(ring, C::PANEL_BYTES, C::SBO, C::SW_CODE);   // K_j
+#pragma unroll
+                for (int kk = 0; kk < kT / 16; ++kk)
+                    mma_ts(tmem + C::ACC0, tmem + C::S_COL + kk * 8, bk + ((kk * 16 * C::SW) >> 4), kIdAcc,
+                           (acc || kk > 0) ? 1u : 0u);
+            } else {
+                const uint64_t bo = smem_desc(ring + C::TILE_BYTES, C::PANEL_BYTES, C::SBO, C::SW_CODE);   // dO_i
+                const uint64_t bq = smem_desc(ring, C::PANEL_BYTES, C::SBO, C::SW_CODE);                   // Q_i
+#pragma unroll
+                for (int kk = 0; kk < kT / 16; ++kk)
+                    mma_ts(tmem + C::ACC0, tmem + C::S_COL + kk * 8, bo + ((kk * 16 * C::SW) >> 4), kIdAcc,
+                           (acc || kk > 0) ? 1u : 0u);                                                    // dV
+#pragma unroll
+                for (int kk = 0; kk < kT / 16; ++kk)
+                    mma_ts(tmem + C::ACC1, tmem + C::DP_COL + kk * 8, bq + ((kk * 16 * C::SW) >> 4), kIdAcc,
+                           (acc || kk > 0) ? 1u : 0u);                                                    // dK
+            }
+            tc_commit(smem_u32(&bars->st_empty[st]));
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&bars->acc_full));
+    }
+    tc_commit(smem_u32(&bars->drain));
+    mbar_wait_drain(smem_u32(&bars->drain), 0);
+}
+
+// Store 32 fp32 accumulator columns times mul as 16-bit values (64 bytes).
+template <bool BF>
+__device__ __forceinline__ void store32(uint8_t *dst, const uint32_t (&r)[32], float mul) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack2<BF>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+// Elementwise work and epilogue: thread t owns TMEM lane t (a query row in
+// dQ mode, a key row in dK/dV mode).
+template <class C, bool BF, int MODE>
+__device__ void bwd_compute(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem, int warp, int lane) {
+    volatile int *abort_flag = &bars->abort;
+    const int t = warp * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    uint32_t sph = 0, aph = 0, cons = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok; u += gridDim.x) {
+        BUnit U;
+        if (!bwd_unit<MODE>(p, u, U)) break;
+        const int row = U.row0 + t;
+        const bool have = U.j0 < U.j1;
+        float lse2 = 0.f, Di = 0.f;
+        if (MODE == kDQ && row < p.Sq) {
+            const int64_t li = ((int64_t)U.b * p.H + U.h) * p.Sq + row;
+            lse2 = p.lse[li] * kLog2e;
+            Di = p.dvec[li];
+        }
+        for (int j = U.j0; j < U.j1 && ok; ++j) {
+            const int st = cons & 1;
+            const uint32_t sfp = (cons >> 1) & 1;
+            ++cons;
+            bool got = warp_wait(smem_u32(&bars->s_full), sph, abort_flag);
+            sph ^= 1;
+            // dK/dV mode reads the stage's row vectors written by the producer warp
+            if (MODE == kDKDV && got) got = warp_wait(smem_u32(&bars->st_full[st]), sfp, abort_flag);
+            if (!got) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float *vec = reinterpret_cast<const float *>(smem + C::VEC) + st * 2 * kT;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t s[32], dp[32];
+                tmem_ld32(lane_base + C::S_COL + 32 * c, s);
+                tmem_ld32(lane_base + C::DP_COL + 32 * c, dp);
+                tmem_wait_ld2(s, dp);
+                uint32_t pw[16], dw[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float pr[2], dr[2];
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        const int col = j * kT + 32 * c + e + x;
+                        float pv, dv;
+                        if constexpr (MODE == kDQ) {
+                            const bool vis = visible(p, row, col);
+                            pv = vis ? ex2(__uint_as_float(s[e + x]) * p.c2 - lse2) : 0.f;
+                            dv = pv * (__uint_as_float(dp[e + x]) - Di);
+                        } else {
+                            const bool vis = visible(p, col, row);
+                            pv = vis ? ex2(__uint_as_float(s[e + x]) * p.c2 - vec[32 * c + e + x]) : 0.f;
+                            dv = pv * (__uint_as_float(dp[e + x]) - vec[kT + 32 * c + e + x]);
+                        }
+                        pr[x] = pv;
+                        dr[x] = dv;
+                    }
+                    pw[e / 2] = pack2<BF>(pr[0], pr[1]);
+                    dw[e / 2] = pack2<BF>(dr[0], dr[1]);
+                }
+                // dS (and P^T) as 16-bit pairs over the S / dP columns already read
+                if constexpr (MODE == kDQ) {
+                    tmem_st16(lane_base + C::S_COL + 16 * c, dw);
+                } else {
+                    tmem_st16(lane_base + C::S_COL + 16 * c, pw);
+                    tmem_st16(lane_base + C::DP_COL + 16 * c, dw);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->c_full));
+        }
+        if (!ok) break;
+        // epilogue
+        if (have) {
+            if (!warp_wait(smem_u32(&bars->acc_full), aph, abort_flag)) break;
+            aph ^= 1;
+            tc_fence_after();
+        }
+        // The TMEM loads are warp-wide (.sync.aligned): every lane takes part,
+        // whether or not its row exists; only the stores are per row.
+        if (MODE == kDQ) {
+            const bool keep = row < p.Sq;
+            uint8_t *dst = static_cast<uint8_t *>(p.dq) + (((int64_t)U.b * p.Sq + row) * p.H + U.h) * C::ROW;
+#pragma unroll 1
+            for (int c = 0; c < C::D / 32; ++c) {
+                uint32_t r[32];
+                if (have) {
+                    tmem_ld32(lane_base + C::ACC0 + 32 * c, r);
+                    tmem_wait_ld1(r);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = 0u;
+                }
+                if (keep) store32<BF>(dst + c * 64, r, p.scale);
+            }
+        } else {
+            const bool keep = row < p.Sk;
+            const int64_t ro = (((int64_t)U.b * p.Sk + row) * p.H + U.h) * C::ROW;
+            uint8_t *dvd = static_cast<uint8_t *>(p.dv) + ro;
+            uint8_t *dkd = static_cast<uint8_t *>(p.dk) + ro;
+#pragma unroll 1
+            for (int c = 0; c < C::D / 32; ++c) {
+                uint32_t rv[32], rk[32];
+                if (have) {
+                    tmem_ld32(lane_base + C::ACC0 + 32 * c, rv);
+                    tmem_ld32(lane_base + C::ACC1 + 32 * c, rk);
+                    tmem_wait_ld2(rv, rk);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) rv[i] = rk[i] = 0u;
+                }
+                if (keep) {
+                    store32<BF>(dvd + c * 64, rv, 1.f);
+                    store32<BF>(dkd + c * 64, rk, p.scale);
+                }
+            }
+        }
+    }
+}
+
+template <class C, bool BF, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    fmha_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    BwdBars *bars = reinterpret_cast<BwdBars *>(smem + C::BARS);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars->own_full), 1);
+        mbar_init(smem_u32(&bars->own_empty), 1);
+        mbar_init(smem_u32(&bars->s_full), 1);
+        mbar_init(smem_u32(&bars->c_full), kCompWarps);
+        mbar_init(smem_u32(&bars->acc_full), 1);
+        mbar_init(smem_u32(&bars->drain), 1);
+        for (int s = 0; s < 2; ++s) {
+            // dK/dV mode: the TMA transaction plus the producer warp's row vectors
+            mbar_init(smem_u32(&bars->st_full[s]), MODE == kDKDV ? 2 : 1);
+            mbar_init(smem_u32(&bars->st_empty[s]), 1);
+        }
+        bars->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    if (warp < kCompWarps) {
+        bwd_compute<C, BF, MODE>(p, smem, bars, tmem, warp, lane);
+    } else if (warp == kProdWarp) {
+        bwd_producer<C, MODE>(p, &tmQ, &tmK, &tmV, &tmO, smem, bars, lane);
+    } else {
+        if (lane == 0) bwd_mma<C, BF, MODE>(p, smem, bars, tmem);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// D_i = dO_i . O_i in fp32, one warp per (b, i, h) row.
+template <int D, bool BF>
+__global__ void fmha_bwd_dot_kernel(const BwdParams p) {
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = (int64_t)p.B * p.Sq * p.H;
+    if (row >= rows) return;
+    const uint16_t *o = static_cast<const uint16_t *>(p.o) + row * D;
+    const uint16_t *g = static_cast<const uint16_t *>(p.dout) + row * D;
+    float acc = 0.f;
+#pragma unroll
+    for (int d = lane; d < D; d += 32) acc += to_f32<BF>(o[d]) * to_f32<BF>(g[d]);
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) {
+        const int64_t h = row % p.H, bi = row / p.H, i = bi % p.Sq, b = bi / p.Sq;
+        p.dvec[(b * p.H + h) * p.Sq + i] = acc;
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 bwd_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+int bwd_sm_count() {
+    static std::mutex mu;
+    static int cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// [B, rows, H, D] with a box of one head, 128 rows and one swizzle panel.
+template <class C>
+bool bwd_map(CUtensorMap *m, const void *base, bool bf, int H, int rows, int B) {
+    auto fn = bwd_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)C::D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)C::ROW, (cuuint64_t)C::ROW * H, (cuuint64_t)C::ROW * H * (rows > 0 ? rows : 1)};
+    cuuint32_t box[4] = {(cuuint32_t)C::BOX_D, 1, (cuuint32_t)kT, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void *>(base),
+              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              C::SW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+int bwd_launch(const BwdParams &p, bool bf, cudaStream_t stream) {
+    using C = BCfg<D>;
+    CUtensorMap tq, tk, tv, to;
+    if (!bwd_map<C>(&tq, p.q, bf, p.H, p.Sq, p.B) || !bwd_map<C>(&tk, p.k, bf, p.H, p.Sk, p.B) ||
+        !bwd_map<C>(&tv, p.v, bf, p.H, p.Sk, p.B) || !bwd_map<C>(&to, p.dout, bf, p.H, p.Sq, p.B))
+        return FMHA_ERR_CUDA;
+    const int sms = bwd_sm_count();
+    if (sms <= 0) return FMHA_ERR_CUDA;
+    // 1) D_i = dO_i . O_i
+    const int64_t rows = (int64_t)p.B * p.Sq * p.H;
+    auto dot = bf ? fmha_bwd_dot_kernel<D, true> : fmha_bwd_dot_kernel<D, false>;
+    dot<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
+    // 2) dQ, 3) dK and dV
+    for (int mode = 0; mode < 2; ++mode) {
+        const int own = mode == kDQ ? (p.Sq + kT - 1) / kT : (p.Sk + kT - 1) / kT;
+        const int64_t units = (int64_t)p.B * p.H * own;
+        const int grid = (int)(units < sms ? units : sms);
+        if (grid <= 0) continue;
+        auto kern = mode == kDQ ? (bf ? fmha_bwd_kernel<C, true, kDQ> : fmha_bwd_kernel<C, false, kDQ>)
+                                : (bf ? fmha_bwd_kernel<C, true, kDKDV> : fmha_bwd_kernel<C, false, kDKDV>);
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+            return FMHA_ERR_CUDA;
+        kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, to, p);
+        if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
+    }
+    return FMHA_OK;
+}
+
+}  // namespace
+
+int bwd_read_status(int reset) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_bwd_status, sizeof(int)) != cudaSuccess) return FMHA_ERR_CUDA;
+    if (reset && v != 0) {
+        const int z = 0;
+        if (cudaMemcpyToSymbol(g_bwd_status, &z, sizeof(int)) != cudaSuccess) return FMHA_ERR_CUDA;
+    }
+    return v;
+}
+
+}  // namespace fmha
+
+using namespace fmha;
+
+extern "C" size_t fmha_bwd_workspace_size(int B, int H, int Sq) {
+    if (B <= 0 || H <= 0 || Sq <= 0) return 0;
+    return ((size_t)B * H * Sq * sizeof(float) + 255) / 256 * 256;
+}
+
+extern "C" int fmha_bwd(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor o, fmha_tensor dout,
+                        const float *lse, fmha_tensor dq, fmha_tensor dk, fmha_tensor dv, int B, int H, int Sq,
+                        int Sk, int D, float scale, int mask, int causal_type, void *workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+    if (B < 0 || H <= 0 || Sq < 0 || Sk < 0 || (D != 64 && D != 128)) return FMHA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !(scale < INFINITY)) return FMHA_ERR_INVALID_ARG;
+    if (mask < FMHA_MASK_NONE || mask > FMHA_MASK_CAUSAL) return FMHA_ERR_INVALID_ARG;
+    if (causal_type != FMHA_CAUSAL_QBEGIN && causal_type != FMHA_CAUSAL_QEND) return FMHA_ERR_INVALID_ARG;
+    if (B == 0 || (Sq == 0 && Sk == 0)) return FMHA_OK;
+    if (Sq == 0 || Sk == 0) {
+        // no query or no key: every gradient is zero (the side that exists is cleared)
+        const size_t n = (size_t)B * (Sq == 0 ? Sk : Sq) * H * D * 2;
+        if (Sq == 0) {
+            if (!dk.data || !dv.data) return FMHA_ERR_INVALID_ARG;
+            if (cudaMemsetAsync(dk.data, 0, n, stream) != cudaSuccess ||
+                cudaMemsetAsync(dv.data, 0, n, stream) != cudaSuccess)
+                return FMHA_ERR_CUDA;
+        } else {
+            if (!dq.data) return FMHA_ERR_INVALID_ARG;
+            if (cudaMemsetAsync(dq.data, 0, n, stream) != cudaSuccess) return FMHA_ERR_CUDA;
+        }
+        return FMHA_OK;
+    }
+    const void *ptrs[9] = {q.data, k.data, v.data, o.data, dout.data, lse, dq.data, dk.data, dv.data};
+    const bool need_q = Sq > 0, need_k = Sk > 0;
+    const bool need[9] = {need_q, need_k, need_k, need_q, need_q, need_q, need_q, need_k, need_k};
+    for (int i = 0; i < 9; ++i)
+        if (need[i] && !ptrs[i]) return FMHA_ERR_INVALID_ARG;
+    const int dt = q.dtype;
+    if (dt != FMHA_F16 && dt != FMHA_BF16) return FMHA_ERR_UNSUPPORTED;
+    const fmha_tensor all[8] = {q, k, v, o, dout, dq, dk, dv};
+    for (const fmha_tensor &t : all)
+        if (t.data && t.dtype != dt) return FMHA_ERR_UNSUPPORTED;
+    for (int i = 0; i < 9; ++i) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(ptrs[i]);
+        if (i == 5 ? (a & 3u) != 0 : (a & 15u) != 0) return i == 5 ? FMHA_ERR_INVALID_ARG : FMHA_ERR_UNSUPPORTED;
+    }
+    const size_t need_ws = fmha_bwd_workspace_size(B, H, Sq);
+    if (Sq > 0 && (!workspace || workspace_bytes < need_ws || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return FMHA_ERR_INVALID_ARG;
+
+    BwdParams p{};
+    p.q = q.data;
+    p.k = k.data;
+    p.v = v.data;
+    p.o = o.data;
+    p.dout = dout.data;
+    p.lse = lse;
+    p.dvec = static_cast<float *>(workspace);
+    p.dq = dq.data;
+    p.dk = dk.data;
+    p.dv = dv.data;
+    p.B = B;
+    p.H = H;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.scale = scale;
+    p.c2 = scale * kLog2e;
+    p.mask = mask;
+    p.causal_type = causal_type;
+    p.off = (mask == FMHA_MASK_CAUSAL && causal_type == FMHA_CAUSAL_QEND) ? Sk - Sq : 0;
+    const bool bf = dt == FMHA_BF16;
+    return D == 64 ? bwd_launch<64>(p, bf, stream) : bwd_launch<128>(p, bf, stream);
+}

@@ -76,6 +76,11 @@ def lib():
             ctypes.c_size_t, ctypes.c_void_p]
         L.fmha_gen_workspace_size.restype = ctypes.c_size_t
         L.fmha_gen_workspace_size.argtypes = [ctypes.c_int] * 5
+        L.fmha_bwd.restype = ctypes.c_int
+        L.fmha_bwd.argtypes = [fmha_tensor] * 5 + [ctypes.c_void_p] + [fmha_tensor] * 3 + [ctypes.c_int] * 5 + [
+            ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        L.fmha_bwd_workspace_size.restype = ctypes.c_size_t
+        L.fmha_bwd_workspace_size.argtypes = [ctypes.c_int] * 3
         L.fmha_status_string.restype = ctypes.c_char_p
         L.fmha_status_string.argtypes = [ctypes.c_int]
         L.fmha_device_status.restype = ctypes.c_int
@@ -276,3 +281,38 @@ def gen_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seqle
     if rc != OK:
         raise FmhaError(rc, status_string(rc))
     return out, lse
+
+
+def fmha_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, Sq, Sk, D, scale, mask, causal_type, workspace,
+             workspace_bytes, stream=None) -> int:
+    """Same arguments, order and status codes as the C function fmha_bwd."""
+    return lib().fmha_bwd(_tensor(q), _tensor(k), _tensor(v), _tensor(o), _tensor(dout), _ptr(lse), _tensor(dq),
+                          _tensor(dk), _tensor(dv), int(B), int(H), int(Sq), int(Sk), int(D), float(scale),
+                          int(mask), int(causal_type), _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def fmha_bwd_workspace_size(B, H, Sq) -> int:
+    return int(lib().fmha_bwd_workspace_size(int(B), int(H), int(Sq)))
+
+
+def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, dout: torch.Tensor,
+        lse: torch.Tensor, *, scale: Optional[float] = None, mask: str = "none", causal_type: str = "qbegin",
+        dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+        workspace: Optional[torch.Tensor] = None, stream=None):
+    """Backward of fwd (see fmha_bwd): q, o, dout [B,Sq,H,D]; k, v [B,Sk,H,D];
+    lse [B,H,Sq] from fwd.  Allocates the gradients and the workspace with torch
+    when not given.  Returns (dq, dk, dv)."""
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    nbytes = fmha_bwd_workspace_size(B, H, Sq)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    sc = 1.0 / math.sqrt(D) if scale is None else scale
+    rc = fmha_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, Sq, Sk, D, sc, _MASKS[mask], _CAUSAL[causal_type],
+                  workspace, max(nbytes, workspace.numel()), stream)
+    if rc != OK:
+        raise FmhaError(rc, status_string(rc))
+    return dq, dk, dv

@@ -261,6 +261,38 @@ int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_cache,
  */
 size_t fmha_gen_workspace_size(int B, int H, int H_k, int D, int S_max);
 
+/*
+ * fmha_bwd -- backward pass of fmha_fwd: dQ, dK, dV from dO ("CUTLASS
+ * Blackwell FMHA 示例完全解析", §FMHA for Blackwell 反向 (Backward): row sums
+ * of O * dO, a dK/dV kernel and a dQ kernel, Q and K blocking 128, causal
+ * masking, head dims 64 and 128, no GQA).
+ *
+ * With P = softmax(scale Q K^T + mask) (the forward's definition, out_scale
+ * = 1) and a loss whose gradient with respect to O is dO:
+ *   dV = P^T dO,  dS = P * (dO V^T - rowsum(dO * O)),  dQ = scale dS K,
+ *   dK = scale dS^T Q.
+ * Inputs: q, o, dout [B, Sq, H, D]; k, v [B, Sk, H, D] (H_k = H: no GQA);
+ * lse float [B, H, Sq] as written by fmha_fwd for the same q, k, v, mask.
+ * Outputs: dq [B, Sq, H, D], dk, dv [B, Sk, H, D], same dtype (FMHA_F16 or
+ * FMHA_BF16).  D is 64 or 128; mask NONE, RESIDUAL or CAUSAL (q-begin or
+ * q-end), as fmha_fwd.  Fixed length only.  Tensors 16-byte aligned, lse
+ * 4-byte aligned.
+ * workspace: caller-owned, fmha_bwd_workspace_size(B, H, Sq) bytes, 256-byte
+ * aligned (the fp32 row sums); no initialisation needed; not shared with a
+ * concurrent call.  Asynchronous on `stream` (three kernels); allocates
+ * nothing.  Returns FMHA_OK, FMHA_ERR_INVALID_ARG (sizes, scale, mask,
+ * pointers, workspace), FMHA_ERR_UNSUPPORTED (dtype, alignment) or
+ * FMHA_ERR_CUDA.  B = 0 succeeds without a launch; Sq = 0 or Sk = 0 clears
+ * the gradients that exist.
+ */
+int fmha_bwd(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor o, fmha_tensor dout,
+             const float *lse, fmha_tensor dq, fmha_tensor dk, fmha_tensor dv,
+             int B, int H, int Sq, int Sk, int D, float scale, int mask, int causal_type,
+             void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes fmha_bwd needs (0 for invalid sizes). */
+size_t fmha_bwd_workspace_size(int B, int H, int Sq);
+
 /* Text for a status code (static storage, never NULL). */
 const char *fmha_status_string(int status);
 

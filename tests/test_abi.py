@@ -187,3 +187,29 @@ def test_gen_workspace_size(fm):
     slots = B * H * ((S_max + 127) // 128 + 1)
     o_bytes = slots * 128 * 4
     assert fm.fmha_gen_workspace_size(B, H, 2, 128, S_max) == (o_bytes + 255) // 256 * 256 + slots * 4
+
+
+def call_bwd(fm, **kw):
+    a = dict(q=P, k=P, v=P, o=P, do=P, lse=P, dq=P, dk=P, dv=P, B=2, H=4, Sq=128, Sk=128, D=128, scale=0.1,
+             mask=0, ct=0, ws=P, ws_bytes=1 << 30, dt=1)
+    a.update(kw)
+    t = lambda x: fm.fmha_tensor(a[x], a["dt"])
+    return fm.lib().fmha_bwd(t("q"), t("k"), t("v"), t("o"), t("do"), a["lse"], t("dq"), t("dk"), t("dv"),
+                             a["B"], a["H"], a["Sq"], a["Sk"], a["D"], a["scale"], a["mask"], a["ct"], a["ws"],
+                             a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=32), -1), (dict(D=96), -1), (dict(H=0), -1), (dict(B=-1), -1), (dict(Sq=-1), -1),
+    (dict(scale=0.0), -1), (dict(scale=float("nan")), -1), (dict(mask=3), -1), (dict(ct=2), -1),
+    (dict(q=None), -1), (dict(lse=None), -1), (dict(dk=None), -1), (dict(ws=None), -1), (dict(ws_bytes=16), -1),
+    (dict(ws=P + 16), -1), (dict(dt=2), -2), (dict(q=P + 8), -2), (dict(lse=P + 2), -1),
+])
+def test_bwd_validation_rejects_before_any_launch(fm, kw, code):
+    assert call_bwd(fm, **kw) == code
+
+
+def test_bwd_workspace_size(fm):
+    assert fm.fmha_bwd_workspace_size(2, 4, 100) == (2 * 4 * 100 * 4 + 255) // 256 * 256
+    assert fm.fmha_bwd_workspace_size(0, 4, 100) == 0
+    assert call_bwd(fm, B=0) == 0

@@ -1,0 +1,86 @@
+"""Backward pass (fmha_bwd) against the oracle, on the GPU.
+
+The forward kernel supplies O and LSE, as in training; the oracle recomputes
+everything exactly from the stored inputs.  The kernel rounds P and dS to the
+input type for the tensor cores and each gradient to the output type, so an
+element may differ from the exact gradient by 1% of that gradient's largest
+magnitude plus half a unit in the last place of the output (relative error of a
+16-bit P or dS term: 2^-9; sums over up to a few thousand terms).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_util import half_ulp
+
+pytestmark = pytest.mark.gpu
+
+DT = {"bf16": (torch.bfloat16, oracle.BF16), "f16": (torch.float16, oracle.F16)}
+MASK = {"none": oracle.MASK_NONE, "causal": oracle.MASK_CAUSAL}
+CT = {"qbegin": oracle.QBEGIN, "qend": oracle.QEND}
+
+
+@pytest.fixture(scope="module")
+def fm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from head_attention_forward_02_gb300 import build, fmha
+    build.build()
+    fmha.lib()
+    return fmha
+
+
+def run_case(fm, dtype, B, H, Sq, Sk, D, mask, ct, seed):
+    tdt, odt = DT[dtype]
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, Sq, H, D, generator=g).to(tdt)
+    k = torch.randn(B, Sk, H, D, generator=g).to(tdt)
+    v = torch.randn(B, Sk, H, D, generator=g).to(tdt)
+    do = torch.randn(B, Sq, H, D, generator=g).to(tdt)
+    dev = "cuda"
+    qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    o, lse = fm.fwd(qd, kd, vd, mask=mask, causal_type=ct)
+    dq, dk, dv = fm.bwd(qd, kd, vd, o, dod, lse, mask=mask, causal_type=ct)
+    torch.cuda.synchronize()
+    assert fm.device_status(reset=True) == 0
+    dec = lambda t: oracle.decode(odt, t.view(torch.uint16).numpy())
+    ref = oracle.attn_bwd_f64(dec(q), dec(k), dec(v), dec(do), D ** -0.5, MASK[mask], CT[ct])
+    for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        got = got.float().cpu().numpy().astype(np.float64)
+        assert not np.isnan(got).any(), f"NaN in {name}"
+        scale = np.abs(want).max() if want.size else 0.0
+        bound = 1e-2 * scale + half_ulp(dtype, want)
+        err = np.abs(got - want)
+        assert (err <= bound).all(), (f"{name}: worst {err.max():.4g} (scale {scale:.3g}) at "
+                                      f"{np.unravel_index(err.argmax(), err.shape)}")
+        assert err.mean() <= 2e-3 * max(scale, 1e-6), (name, err.mean(), scale)
+
+
+CASES = [
+    # dtype, B, H, Sq, Sk, D, mask, causal_type
+    ("bf16", 1, 2, 128, 128, 128, "none", "qbegin"),
+    ("bf16", 2, 3, 300, 300, 128, "causal", "qbegin"),
+    ("f16", 1, 4, 200, 333, 64, "none", "qbegin"),
+    ("bf16", 2, 2, 257, 129, 128, "causal", "qend"),
+    ("f16", 1, 2, 130, 400, 128, "causal", "qend"),
+    ("bf16", 1, 2, 96, 700, 64, "causal", "qbegin"),     # keys after every query get zero gradient
+    ("bf16", 2, 4, 1024, 1024, 128, "causal", "qbegin"),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}_b{c[1]}h{c[2]}_{c[3]}x{c[4]}_d{c[5]}_{c[6]}_{c[7]}"
+                                             for c in CASES])
+def test_bwd_matches_oracle(fm, case):
+    run_case(fm, *case, seed=sum(case[1:6]))
+
+
+def test_bwd_empty_sides_give_zero(fm):
+    k = torch.randn(1, 64, 2, 64, device="cuda", dtype=torch.bfloat16)
+    q = torch.empty(1, 0, 2, 64, device="cuda", dtype=torch.bfloat16)
+    dk = torch.full_like(k, 3.0)
+    dv = torch.full_like(k, 3.0)
+    lse = torch.empty(1, 2, 0, device="cuda")
+    fm.bwd(q, k, k, q, q, lse, dk=dk, dv=dv, workspace=torch.empty(256, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert bool((dk == 0).all()) and bool((dv == 0).all())
