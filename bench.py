@@ -46,9 +46,12 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--op", default="fwd", choices=["fwd", "gen"],
+    ap.add_argument("--op", default="fwd", choices=["fwd", "gen", "bwd"],
                     help="fwd: the fused forward (fmha_fwd); gen: generation phase against a "
-                         "K/V cache (fmha_gen_fwd)")
+                         "K/V cache (fmha_gen_fwd); bwd: the backward pass (fmha_bwd)")
+    ap.add_argument("--bwd-config", default="bwd_bf16_causal_b2_h16_s8192_d128",
+                    choices=["bwd_bf16_causal_b2_h16_s8192_d128", "bwd_bf16_nomask_b2_h16_s8192_d128",
+                             "bwd_bf16_causal_b4_h16_s2048_d128"])
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(wl.CONFIGS))
     ap.add_argument("--gen-config", default=DEFAULT_GEN_CONFIG, choices=list(wl.GEN_CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -700,6 +703,133 @@ def run_gen_reference(args, rank, world):
         flush=True)
 
 
+BWD_SHAPES = {   # name -> (B, H, S, D, mask); synthetic N(0,1) q, k, v, dO
+    "bwd_bf16_causal_b2_h16_s8192_d128": (2, 16, 8192, 128, "causal"),
+    "bwd_bf16_nomask_b2_h16_s8192_d128": (2, 16, 8192, 128, "none"),
+    "bwd_bf16_causal_b4_h16_s2048_d128": (4, 16, 2048, 128, "causal"),
+}
+
+
+def bwd_flops(B, H, S, D, causal):
+    """Algorithmic FLOPs of the backward: the five products of the chain rule
+    (S, dP, dV, dQ, dK), 2*S*S*D each per head, halved for a causal mask."""
+    return 10.0 * B * H * S * S * D * (0.5 if causal else 1.0)
+
+
+def run_bwd(args, rank, world, local):
+    """Backward pass (fmha_bwd) on synthetic inputs; O and LSE come from fmha_fwd."""
+    from head_attention_forward_02_gb300 import build, fmha as fm
+    build.build()
+    fm.lib()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    B, H, S, D, mask = BWD_SHAPES[args.bwd_config]
+    stream = torch.cuda.current_stream(dev)
+    g = torch.Generator().manual_seed(31)
+    host = {n: torch.randn(B, S, H, D, generator=g).to(torch.bfloat16) for n in ("q", "k", "v", "do")}
+    d = {n: t.to(dev) for n, t in host.items()}
+    o, lse = fm.fwd(d["q"], d["k"], d["v"], mask=mask)
+    ws = torch.empty(fm.fmha_bwd_workspace_size(B, H, S), dtype=torch.uint8, device=dev)
+    grads = [torch.empty_like(d["q"]) for _ in range(3)]
+    flops = bwd_flops(B, H, S, D, mask == "causal")
+
+    def step():
+        fm.bwd(d["q"], d["k"], d["v"], o, d["do"], lse, mask=mask, dq=grads[0], dk=grads[1], dv=grads[2],
+               workspace=ws, stream=stream)
+
+    sampler = ClockSampler(gpu_uuid(dev.index or 0))
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fm.device_status(reset=True) != 0:
+        raise RuntimeError("device status reports an error")
+    K = args.steps
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(K):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t_host1 = time.time()
+    if rank == 0:
+        sampler.stop()
+    if fm.device_status(reset=True) != 0:
+        raise RuntimeError("device status reports an error")
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / K, world)
+    value = world * flops / (ms * 1e-3) / 1e12
+    # end to end: q, k, v, O, dO and LSE in from pinned memory, dQ, dK, dV out
+    pin = {n: t.pin_memory() for n, t in host.items()}
+    o_h, lse_h = o.cpu().pin_memory(), lse.cpu().pin_memory()
+    outs = [torch.empty_like(t).pin_memory() for t in (host["q"],) * 3]
+
+    def e2e_step():
+        for n, t in pin.items():
+            d[n].copy_(t, non_blocking=True)
+        o.copy_(o_h, non_blocking=True)
+        lse.copy_(lse_h, non_blocking=True)
+        step()
+        for hst, dv_ in zip(outs, grads):
+            hst.copy_(dv_, non_blocking=True)
+
+    e2e_steps = args.e2e_steps or 5
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in pin.values()) + o_h.numel() * 2 + lse_h.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    if rank != 0:
+        return
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    line = {
+        "metric": "FMHA backward TFLOP/s (5 products of the chain rule) and % of GB300 dense bf16 peak",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) q, k, v, dO; O and LSE from fmha_fwd)",
+        "config": {"workload": args.bwd_config, "op": "fmha_bwd", "B": B, "H": H, "S": S, "D": D, "mask": mask,
+                   "l2": f"inputs and outputs {7 * B * S * H * D * 2 / 2**20:.0f} MiB (> L2)",
+                   "parallelism": f"replicas x{world} (independent problems)"},
+        "roofline": {"bound": "tensor", "achieved": round(flops / (ms * 1e-3) / 1e12, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(flops / (ms * 1e-3) / 1e12 / peak, 4),
+                     "peak_source": f"bf16_tflops of {peak_src}", "traffic": None,
+                     "algorithmic_flops": flops, "executed_flops": flops * 7 / 5,
+                     "note": "two-pass design: S and dP are computed in both the dQ and the dK/dV kernel"},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * K,
+        "clocks": sampler.summary(t_host0, t_host1),
+    }
+    if not args.no_cpu_baseline:
+        import numpy as np
+        import oracle
+        oracle.build()
+        n = 384                                   # the first query rows of batch 0, every head, all keys
+        dec = lambda t: t.float().numpy().astype(np.float64)
+        q1, k1, v1, g1 = (dec(host[x][:1]) for x in ("q", "k", "v", "do"))
+        t = time.perf_counter()
+        oracle.attn_bwd_f64(q1[:, :n], k1, v1, g1[:, :n], D ** -0.5, oracle.MASK_NONE, oracle.QBEGIN,
+                            threads=cpu_threads())
+        dt = time.perf_counter() - t
+        f = 10.0 * H * n * S * D
+        line["cpu_baseline"] = {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cpu_threads(),
+                                "kind": "oracle",
+                                "sample": f"{n} query rows x {S} keys x {H} heads, no mask "
+                                          f"({f / 1e9:.1f} GFLOP, {dt:.1f} s)"}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, world):
     """The CPU oracle as the reference arm: each step is a bounded seeded sample
     of query rows of the same workload."""
@@ -753,7 +883,7 @@ def main():
         return
     rank, world, local = dist_setup(args.gpus)
     try:
-        (run_gen if args.op == "gen" else run_ours)(args, rank, world, local)
+        {"gen": run_gen, "bwd": run_bwd}.get(args.op, run_ours)(args, rank, world, local)
     finally:
         if world > 1:
             import torch.distributed as dist
