@@ -40,10 +40,10 @@ __device__ int g_bwd_status;   // FMHA_OK, or FMHA_ERR_TIMEOUT after a bounded w
 namespace {
 
 constexpr int kT = 128;                 // rows per tile, both sides
-constexpr int kCompWarps = 4;           // warps 0-3: elementwise work and epilogue
-constexpr int kProdWarp = 4;            // TMA producer (all lanes: the dK/dV kernel's row vectors)
-constexpr int kMmaWarp = 5;             // tcgen05.mma issuer (lane 0), owns TMEM
-constexpr int kThreads = 192;
+constexpr int kCompWarps = 8;           // warps 0-7: elementwise work and epilogue
+constexpr int kProdWarp = 8;            // TMA producer (all lanes: the dK/dV kernel's row vectors)
+constexpr int kMmaWarp = 9;             // tcgen05.mma issuer (lane 0), owns TMEM
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;
 constexpr unsigned long long kDrainNs = 200000000ull;
@@ -73,6 +73,7 @@ struct BCfg {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     // TMEM columns
     static constexpr int S_COL = 0, DP_COL = 128, ACC0 = 256, ACC1 = 256 + D;
+    static constexpr int DS_COL = 384;                     // dQ kernel: dS of tile j at DS_COL + 64 * (j % 2)
     static_assert(ACC1 + D <= (int)kTmemCols, "TMEM budget");
 };
 
@@ -88,7 +89,9 @@ struct BwdParams {
 
 struct BwdBars {
     uint64_t own_full, own_empty, s_full, c_full, acc_full, drain;
+    uint64_t s_read;                    // dQ kernel: S and dP of the current tile are in registers
     uint64_t st_full[2], st_empty[2];
+    uint64_t pair_ld[4];                // dK/dV: the lower-half warp of a row quadrant has read S^T, dP^T
     uint32_t tmem_base;
     int abort;
 };
@@ -281,6 +284,23 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+__device__ __forceinline__ uint64_t pack_f2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ void unpack_f2(uint64_t v, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+
+// a * b + c on two fp32 lanes at once
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 template <bool BF>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     uint32_t r;
@@ -433,6 +453,92 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
     }
 }
 
+// MMA issuer of the dQ kernel (one lane).  dS lives apart from S and dP (two
+// buffers), so S and dP of tile j+1 are issued as soon as the compute warps
+// have read S_j and dP_j (s_read), and dQ += dS_j K_j once dS_j is written
+// (c_full): the elementwise work of tile j overlaps the MMAs of tile j+1.
+// In issue order S_j+2 follows dQ_j, so "S_j+2 complete" implies "dS buffer
+// j % 2 read".
+template <class C, bool BF>
+__device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem) {
+    volatile int *abort_flag = &bars->abort;
+    constexpr uint32_t fmt = BF ? 1u : 0u;
+    constexpr uint32_t kIdS = bwd_idesc(fmt, kT, false);
+    constexpr uint32_t kIdAcc = bwd_idesc(fmt, C::D, true);
+    const uint32_t own = smem_u32(smem + C::OWN);
+    const uint64_t a0 = smem_desc(own, 16, C::SBO, C::SW_CODE);                     // Q
+    const uint64_t a1 = smem_desc(own + C::TILE_BYTES, 16, C::SBO, C::SW_CODE);     // dO
+    uint32_t cons = 0, owned = 0, cc = 0, rc = 0;
+    bool ok = true;
+    auto ring = [&](int st) { return smem_u32(smem + C::RING + st * 2 * C::TILE_BYTES); };
+    // S = Q K^T and dP = dO V^T of the tile in stage st
+    auto issue_s = [&](int st) {
+        const uint64_t bk = smem_desc(ring(st), 16, C::SBO, C::SW_CODE);
+        const uint64_t bv = smem_desc(ring(st) + C::TILE_BYTES, 16, C::SBO, C::SW_CODE);
+#pragma unroll
+        for (int kk = 0; kk < C::D / 16; ++kk) {
+            const uint32_t off = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
+            mma_ss(tmem + C::S_COL, a0 + off, bk + off, kIdS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < C::D / 16; ++kk) {
+            const uint32_t off = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
+            mma_ss(tmem + C::DP_COL, a1 + off, bv + off, kIdS, kk > 0 ? 1u : 0u);
+        }
+    };
+    auto next_stage = [&](int &st) -> bool {
+        st = cons & 1;
+        const bool r = mbar_wait(smem_u32(&bars->st_full[st]), (cons >> 1) & 1, abort_flag);
+        ++cons;
+        return r;
+    };
+    for (int u = blockIdx.x; ok; u += gridDim.x) {
+        BUnit U;
+        if (!bwd_unit<kDQ>(p, u, U)) break;
+        if (U.j0 >= U.j1) continue;
+        if (!mbar_wait(smem_u32(&bars->own_full), owned & 1, abort_flag)) break;
+        ++owned;
+        int st;
+        if (!next_stage(st)) break;
+        issue_s(st);
+        if (U.j0 + 1 == U.j1) tc_commit(smem_u32(&bars->own_empty));
+        tc_commit(smem_u32(&bars->s_full));
+        for (int j = U.j0; j < U.j1; ++j) {
+            if (j + 1 < U.j1) {
+                int st2;
+                if (!next_stage(st2)) { ok = false; break; }
+                if (!mbar_wait(smem_u32(&bars->s_read), rc & 1, abort_flag)) { ok = false; break; }
+                ++rc;
+                tc_fence_after();
+                issue_s(st2);
+                if (j + 2 == U.j1) tc_commit(smem_u32(&bars->own_empty));
+                tc_commit(smem_u32(&bars->s_full));
+            } else {
+                // the last tile's s_read keeps the phase count in step
+                if (!mbar_wait(smem_u32(&bars->s_read), rc & 1, abort_flag)) { ok = false; break; }
+                ++rc;
+            }
+            if (!mbar_wait(smem_u32(&bars->c_full), cc & 1, abort_flag)) { ok = false; break; }
+            ++cc;
+            tc_fence_after();
+            // dQ += dS_j K_j: A = dS buffer j % 2 (16-bit, 8 columns per step of
+            // 16 keys), B = K_j rows MN-major
+            const uint32_t ds = tmem + C::DS_COL + 64 * (j & 1);
+            const uint64_t bk = smem_desc(ring(st), C::PANEL_BYTES, C::SBO, C::SW_CODE);
+#pragma unroll
+            for (int kk = 0; kk < kT / 16; ++kk)
+                mma_ts(tmem + C::ACC0, ds + kk * 8, bk + ((kk * 16 * C::SW) >> 4), kIdAcc,
+                       (j > U.j0 || kk > 0) ? 1u : 0u);
+            tc_commit(smem_u32(&bars->st_empty[st]));
+            st = (st + 1) & 1;     // tile j+1's stage (issued above)
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&bars->acc_full));
+    }
+    tc_commit(smem_u32(&bars->drain));
+    mbar_wait_drain(smem_u32(&bars->drain), 0);
+}
+
 // MMA issuer (one lane).  Per loop tile: S and dP (both SS, K-major), then,
 // once the compute warps wrote dS (and P^T), the accumulating MMA(s) with A
 // from TMEM and B = a loop tile read MN-major.  In-order issue makes "S of
@@ -490,7 +596,7 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32
                 const uint64_t bk = smem_desc(ring, C::PANEL_BYTES, C::SBO, C::SW_CODE);   // K_j
 #pragma unroll
                 for (int kk = 0; kk < kT / 16; ++kk)
-                    mma_ts(tmem + C::ACC0, tmem + C::S_COL + kk * 8, bk + ((kk * 16 * C::SW) >> 4), kIdAcc,
+                    mma_ts(tmem + C::ACC0, tmem + C::DS_COL + kk * 8, bk + ((kk * 16 * C::SW) >> 4), kIdAcc,
                            (acc || kk > 0) ? 1u : 0u);
             } else {
                 const uint64_t bo = smem_desc(ring + C::TILE_BYTES, C::PANEL_BYTES, C::SBO, C::SW_CODE);   // dO_i
@@ -524,25 +630,81 @@ __device__ __forceinline__ void store32(uint8_t *dst, const uint32_t (&r)[32], f
     for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
-// Elementwise work and epilogue: thread t owns TMEM lane t (a query row in
-// dQ mode, a key row in dK/dV mode).
+// One 32-column chunk of the elementwise work for this thread's row:
+// P = exp2(S * scale * log2e - LSE * log2e) (zero where masked) and
+// dS = P (dP - D), from the chunk's S and dP values; packed to 16-bit pairs.
+// nl / nd give -LSE*log2e and -D per column pair (they are per row in the
+// dQ kernel, per column in the dK/dV kernel).
+template <bool BF, int MODE>
+__device__ __forceinline__ void bwd_chunk(const BwdParams &p, const uint32_t (&s)[32], const uint32_t (&dp)[32],
+                                          uint64_t c2x2, uint64_t nl_row, uint64_t nd_row, const float *vec_l,
+                                          const float *vec_d, bool full, int row, int col0, uint32_t (&pw)[16],
+                                          uint32_t (&dw)[16]) {
+    const uint64_t ones = pack_f2(1.f, 1.f), zero2 = pack_f2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+        uint64_t nl = nl_row, nd = nd_row;
+        if constexpr (MODE == kDKDV) {
+            const float2 lv = *reinterpret_cast<const float2 *>(vec_l + e);
+            const float2 dv = *reinterpret_cast<const float2 *>(vec_d + e);
+            nl = pack_f2(-lv.x, -lv.y);
+            nd = pack_f2(-dv.x, -dv.y);
+        }
+        float a, b;
+        unpack_f2(fma_f2(pack_f2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), c2x2, nl), a, b);
+        a = ex2(a);
+        b = ex2(b);
+        if (!full) {
+            const int col = col0 + e;
+            const bool va = MODE == kDQ ? visible(p, row, col) : visible(p, col, row);
+            const bool vb = MODE == kDQ ? visible(p, row, col + 1) : visible(p, col + 1, row);
+            a = va ? a : 0.f;
+            b = vb ? b : 0.f;
+        }
+        const uint64_t pp = pack_f2(a, b);
+        const uint64_t diff = fma_f2(pack_f2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), ones, nd);
+        float da, db;
+        unpack_f2(fma_f2(pp, diff, zero2), da, db);
+        pw[e / 2] = pack2<BF>(a, b);
+        dw[e / 2] = pack2<BF>(da, db);
+    }
+}
+
+// Elementwise work and epilogue: warps w and w+4 share TMEM lanes
+// 32*(w%4)..+31 (rows of the owned tile) and take the lower / upper 64
+// columns of every loop tile; in the epilogue, the lower / upper half of the
+// head dimension.  dS needs no exchange across columns, so the halves only
+// meet in the dK/dV kernel, where P^T and dS^T go back over S^T and dP^T: the
+// upper half's stores overwrite columns the lower half reads, so it stores
+// only after the lower half signalled (pair_ld) that its loads are done.
 template <class C, bool BF, int MODE>
 __device__ void bwd_compute(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem, int warp, int lane) {
     volatile int *abort_flag = &bars->abort;
-    const int t = warp * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    uint32_t sph = 0, aph = 0, cons = 0;
+    const int half = warp >> 2, wq = warp & 3;
+    const int t = wq * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t pair_bar = smem_u32(&bars->pair_ld[wq]);
+    const uint64_t c2x2 = pack_f2(p.c2, p.c2);
+    uint32_t sph = 0, aph = 0, cons = 0, pph = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok; u += gridDim.x) {
         BUnit U;
         if (!bwd_unit<MODE>(p, u, U)) break;
         const int row = U.row0 + t;
         const bool have = U.j0 < U.j1;
-        float lse2 = 0.f, Di = 0.f;
-        if (MODE == kDQ && row < p.Sq) {
-            const int64_t li = ((int64_t)U.b * p.H + U.h) * p.Sq + row;
-            lse2 = p.lse[li] * kLog2e;
-            Di = p.dvec[li];
+        uint64_t nl_row = 0, nd_row = 0;
+        int nu = 0;                                   // dQ: leading key tiles visible to every row
+        if (MODE == kDQ) {
+            float l2 = INFINITY, di = 0.f;            // a row past Sq: P = 0
+            if (row < p.Sq) {
+                const int64_t li = ((int64_t)U.b * p.H + U.h) * p.Sq + row;
+                l2 = p.lse[li] * kLog2e;
+                di = p.dvec[li];
+            }
+            nl_row = pack_f2(-l2, -l2);
+            nd_row = pack_f2(-di, -di);
+            int nt;
+            kv_tile_range(U.row0, kT, p.Sq, p.Sk, p.mask, p.causal_type, kT, &nt, &nu);
         }
         for (int j = U.j0; j < U.j1 && ok; ++j) {
             const int st = cons & 1;
@@ -557,43 +719,63 @@ __device__ void bwd_compute(const BwdParams &p, uint8_t *smem, BwdBars *bars, ui
                 break;
             }
             tc_fence_after();
+            // every (query, key) pair of the tile pair visible: no per-element
+            // mask (rows / columns outside the problem already give P = 0 or
+            // touch only discarded rows)
+            const bool full = MODE == kDQ ? j < nu
+                                          : (p.mask != FMHA_MASK_CAUSAL || j * kT + p.off >= U.row0 + kT - 1);
             const float *vec = reinterpret_cast<const float *>(smem + C::VEC) + st * 2 * kT;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t s[32], dp[32];
-                tmem_ld32(lane_base + C::S_COL + 32 * c, s);
-                tmem_ld32(lane_base + C::DP_COL + 32 * c, dp);
-                tmem_wait_ld2(s, dp);
-                uint32_t pw[16], dw[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float pr[2], dr[2];
-#pragma unroll
-                    for (int x = 0; x < 2; ++x) {
-                        const int col = j * kT + 32 * c + e + x;
-                        float pv, dv;
-                        if constexpr (MODE == kDQ) {
-                            const bool vis = visible(p, row, col);
-                            pv = vis ? ex2(__uint_as_float(s[e + x]) * p.c2 - lse2) : 0.f;
-                            dv = pv * (__uint_as_float(dp[e + x]) - Di);
-                        } else {
-                            const bool vis = visible(p, col, row);
-                            pv = vis ? ex2(__uint_as_float(s[e + x]) * p.c2 - vec[32 * c + e + x]) : 0.f;
-                            dv = pv * (__uint_as_float(dp[e + x]) - vec[kT + 32 * c + e + x]);
-                        }
-                        pr[x] = pv;
-                        dr[x] = dv;
+            if constexpr (MODE == kDQ) {
+                uint32_t s0[32], d0[32], s1[32], d1[32];
+                tmem_ld32(lane_base + C::S_COL + 64 * half, s0);
+                tmem_ld32(lane_base + C::DP_COL + 64 * half, d0);
+                tmem_wait_ld2(s0, d0);
+                tmem_ld32(lane_base + C::S_COL + 64 * half + 32, s1);
+                tmem_ld32(lane_base + C::DP_COL + 64 * half + 32, d1);
+                tmem_wait_ld2(s1, d1);
+                // S and dP may now be overwritten by the next tile's MMAs
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->s_read));
+                uint32_t pw[16], dw0[16], dw1[16];
+                bwd_chunk<BF, MODE>(p, s0, d0, c2x2, nl_row, nd_row, nullptr, nullptr, full, row,
+                                    j * kT + 64 * half, pw, dw0);
+                bwd_chunk<BF, MODE>(p, s1, d1, c2x2, nl_row, nd_row, nullptr, nullptr, full, row,
+                                    j * kT + 64 * half + 32, pw, dw1);
+                const uint32_t ds = lane_base + C::DS_COL + 64 * (j & 1) + 32 * half;
+                tmem_st16(ds, dw0);
+                tmem_st16(ds + 16, dw1);
+            } else {
+                uint32_t s0[32], d0[32], s1[32], d1[32];
+                tmem_ld32(lane_base + C::S_COL + 64 * half, s0);
+                tmem_ld32(lane_base + C::DP_COL + 64 * half, d0);
+                tmem_wait_ld2(s0, d0);
+                tmem_ld32(lane_base + C::S_COL + 64 * half + 32, s1);
+                tmem_ld32(lane_base + C::DP_COL + 64 * half + 32, d1);
+                tmem_wait_ld2(s1, d1);
+                if (half == 0) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(pair_bar);
+                }
+                uint32_t pw0[16], dw0[16], pw1[16], dw1[16];
+                bwd_chunk<BF, MODE>(p, s0, d0, c2x2, 0, 0, vec + 64 * half, vec + kT + 64 * half, full, row,
+                                    j * kT + 64 * half, pw0, dw0);
+                bwd_chunk<BF, MODE>(p, s1, d1, c2x2, 0, 0, vec + 64 * half + 32, vec + kT + 64 * half + 32, full,
+                                    row, j * kT + 64 * half + 32, pw1, dw1);
+                if (half == 1) {
+                    const bool peer = warp_wait(pair_bar, pph, abort_flag);
+                    if (!peer) {
+                        ok = false;
+                        break;
                     }
-                    pw[e / 2] = pack2<BF>(pr[0], pr[1]);
-                    dw[e / 2] = pack2<BF>(dr[0], dr[1]);
+                    tc_fence_after();
                 }
-                // dS (and P^T) as 16-bit pairs over the S / dP columns already read
-                if constexpr (MODE == kDQ) {
-                    tmem_st16(lane_base + C::S_COL + 16 * c, dw);
-                } else {
-                    tmem_st16(lane_base + C::S_COL + 16 * c, pw);
-                    tmem_st16(lane_base + C::DP_COL + 16 * c, dw);
-                }
+                pph ^= 1;
+                tmem_st16(lane_base + C::S_COL + 32 * half, pw0);
+                tmem_st16(lane_base + C::S_COL + 32 * half + 16, pw1);
+                tmem_st16(lane_base + C::DP_COL + 32 * half, dw0);
+                tmem_st16(lane_base + C::DP_COL + 32 * half + 16, dw1);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -601,19 +783,21 @@ __device__ void bwd_compute(const BwdParams &p, uint8_t *smem, BwdBars *bars, ui
             if (lane == 0) mbar_arrive(smem_u32(&bars->c_full));
         }
         if (!ok) break;
-        // epilogue
+        // epilogue: this warp's half of the head dimension.  The TMEM loads are
+        // warp-wide (.sync.aligned): every lane takes part, whether or not its
+        // row exists; only the stores are per row.
         if (have) {
             if (!warp_wait(smem_u32(&bars->acc_full), aph, abort_flag)) break;
             aph ^= 1;
             tc_fence_after();
         }
-        // The TMEM loads are warp-wide (.sync.aligned): every lane takes part,
-        // whether or not its row exists; only the stores are per row.
+        constexpr int HC = C::D / 64;                 // 32-column chunks per half
         if (MODE == kDQ) {
             const bool keep = row < p.Sq;
             uint8_t *dst = static_cast<uint8_t *>(p.dq) + (((int64_t)U.b * p.Sq + row) * p.H + U.h) * C::ROW;
 #pragma unroll 1
-            for (int c = 0; c < C::D / 32; ++c) {
+            for (int cc = 0; cc < HC; ++cc) {
+                const int c = half * HC + cc;
                 uint32_t r[32];
                 if (have) {
                     tmem_ld32(lane_base + C::ACC0 + 32 * c, r);
@@ -630,7 +814,8 @@ __device__ void bwd_compute(const BwdParams &p, uint8_t *smem, BwdBars *bars, ui
             uint8_t *dvd = static_cast<uint8_t *>(p.dv) + ro;
             uint8_t *dkd = static_cast<uint8_t *>(p.dk) + ro;
 #pragma unroll 1
-            for (int c = 0; c < C::D / 32; ++c) {
+            for (int cc = 0; cc < HC; ++cc) {
+                const int c = half * HC + cc;
                 uint32_t rv[32], rk[32];
                 if (have) {
                     tmem_ld32(lane_base + C::ACC0 + 32 * c, rv);
@@ -663,6 +848,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&bars->own_empty), 1);
         mbar_init(smem_u32(&bars->s_full), 1);
         mbar_init(smem_u32(&bars->c_full), kCompWarps);
+        mbar_init(smem_u32(&bars->s_read), kCompWarps);
+        for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&bars->pair_ld[w]), 1);
         mbar_init(smem_u32(&bars->acc_full), 1);
         mbar_init(smem_u32(&bars->drain), 1);
         for (int s = 0; s < 2; ++s) {
@@ -686,7 +873,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kProdWarp) {
         bwd_producer<C, MODE>(p, &tmQ, &tmK, &tmV, &tmO, smem, bars, lane);
     } else {
-        if (lane == 0) bwd_mma<C, BF, MODE>(p, smem, bars, tmem);
+        if (lane == 0) {
+            if constexpr (MODE == kDQ) bwd_mma_dq<C, BF>(p, smem, bars, tmem);
+            else bwd_mma<C, BF, MODE>(p, smem, bars, tmem);
+        }
     }
     tc_fence_before();
     __syncthreads();
