@@ -64,7 +64,7 @@ struct BCfg {
     static constexpr int SBO = 8 * SW;
     static constexpr int OWN = 0;                           // two owned tiles
     static constexpr int RING = 2 * TILE_BYTES;             // two stages of two tiles
-    static constexpr int VEC = RING + 2 * 2 * TILE_BYTES;   // per stage: LSE*log2e and D, 128 floats each
+    static constexpr int VEC = RING + 2 * 2 * TILE_BYTES;   // per stage: -LSE*log2e and -D, 128 floats each
     static constexpr int BARS = VEC + 2 * 2 * kT * 4;
     // at least 120 KB so that a second CTA never shares the SM: each
     // allocates all 512 TMEM columns; plus 1 KB to align for the swizzle
@@ -430,8 +430,8 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
                 for (int i = 0; i < kT / 32; ++i) {
                     const int q = j * kT + i * 32 + lane;
                     const bool in = q < p.Sq;
-                    vec[i * 32 + lane] = in ? p.lse[base + q] * kLog2e : INFINITY;
-                    vec[kT + i * 32 + lane] = in ? p.dvec[base + q] : 0.f;
+                    vec[i * 32 + lane] = in ? -p.lse[base + q] * kLog2e : -INFINITY;   // -LSE * log2(e)
+                    vec[kT + i * 32 + lane] = in ? -p.dvec[base + q] : 0.f;            // -D
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(fb);
@@ -633,41 +633,56 @@ __device__ __forceinline__ void store32(uint8_t *dst, const uint32_t (&r)[32], f
 // One 32-column chunk of the elementwise work for this thread's row:
 // P = exp2(S * scale * log2e - LSE * log2e) (zero where masked) and
 // dS = P (dP - D), from the chunk's S and dP values; packed to 16-bit pairs.
-// nl / nd give -LSE*log2e and -D per column pair (they are per row in the
-// dQ kernel, per column in the dK/dV kernel).
-template <bool BF, int MODE>
+// nl / nd are -LSE*log2e and -D: per row in the dQ kernel, per column (read
+// from the stage's vectors, four at a time) in the dK/dV kernel.  FULL: every
+// pair of the tile is visible, no per-element test.
+template <bool BF, int MODE, bool FULL>
 __device__ __forceinline__ void bwd_chunk(const BwdParams &p, const uint32_t (&s)[32], const uint32_t (&dp)[32],
                                           uint64_t c2x2, uint64_t nl_row, uint64_t nd_row, const float *vec_l,
-                                          const float *vec_d, bool full, int row, int col0, uint32_t (&pw)[16],
+                                          const float *vec_d, int row, int col0, uint32_t (&pw)[16],
                                           uint32_t (&dw)[16]) {
     const uint64_t ones = pack_f2(1.f, 1.f), zero2 = pack_f2(0.f, 0.f);
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-        uint64_t nl = nl_row, nd = nd_row;
+    for (int e = 0; e < 32; e += 4) {
+        uint64_t nl[2] = {nl_row, nl_row}, nd[2] = {nd_row, nd_row};
         if constexpr (MODE == kDKDV) {
-            const float2 lv = *reinterpret_cast<const float2 *>(vec_l + e);
-            const float2 dv = *reinterpret_cast<const float2 *>(vec_d + e);
-            nl = pack_f2(-lv.x, -lv.y);
-            nd = pack_f2(-dv.x, -dv.y);
+            const float4 lv = *reinterpret_cast<const float4 *>(vec_l + e);
+            const float4 dv = *reinterpret_cast<const float4 *>(vec_d + e);
+            nl[0] = pack_f2(lv.x, lv.y);
+            nl[1] = pack_f2(lv.z, lv.w);
+            nd[0] = pack_f2(dv.x, dv.y);
+            nd[1] = pack_f2(dv.z, dv.w);
         }
-        float a, b;
-        unpack_f2(fma_f2(pack_f2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), c2x2, nl), a, b);
-        a = ex2(a);
-        b = ex2(b);
-        if (!full) {
-            const int col = col0 + e;
-            const bool va = MODE == kDQ ? visible(p, row, col) : visible(p, col, row);
-            const bool vb = MODE == kDQ ? visible(p, row, col + 1) : visible(p, col + 1, row);
-            a = va ? a : 0.f;
-            b = vb ? b : 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int x = e + 2 * h;
+            float a, b;
+            unpack_f2(fma_f2(pack_f2(__uint_as_float(s[x]), __uint_as_float(s[x + 1])), c2x2, nl[h]), a, b);
+            a = ex2(a);
+            b = ex2(b);
+            if constexpr (!FULL) {
+                const int col = col0 + x;
+                const bool va = MODE == kDQ ? visible(p, row, col) : visible(p, col, row);
+                const bool vb = MODE == kDQ ? visible(p, row, col + 1) : visible(p, col + 1, row);
+                a = va ? a : 0.f;
+                b = vb ? b : 0.f;
+            }
+            const uint64_t diff = fma_f2(pack_f2(__uint_as_float(dp[x]), __uint_as_float(dp[x + 1])), ones, nd[h]);
+            float da, db;
+            unpack_f2(fma_f2(pack_f2(a, b), diff, zero2), da, db);
+            pw[x / 2] = pack2<BF>(a, b);
+            dw[x / 2] = pack2<BF>(da, db);
         }
-        const uint64_t pp = pack_f2(a, b);
-        const uint64_t diff = fma_f2(pack_f2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), ones, nd);
-        float da, db;
-        unpack_f2(fma_f2(pp, diff, zero2), da, db);
-        pw[e / 2] = pack2<BF>(a, b);
-        dw[e / 2] = pack2<BF>(da, db);
     }
+}
+
+template <bool BF, int MODE>
+__device__ __forceinline__ void bwd_chunk_sel(bool full, const BwdParams &p, const uint32_t (&s)[32],
+                                              const uint32_t (&dp)[32], uint64_t c2x2, uint64_t nl_row,
+                                              uint64_t nd_row, const float *vec_l, const float *vec_d, int row,
+                                              int col0, uint32_t (&pw)[16], uint32_t (&dw)[16]) {
+    if (full) bwd_chunk<BF, MODE, true>(p, s, dp, c2x2, nl_row, nd_row, vec_l, vec_d, row, col0, pw, dw);
+    else bwd_chunk<BF, MODE, false>(p, s, dp, c2x2, nl_row, nd_row, vec_l, vec_d, row, col0, pw, dw);
 }
 
 // Elementwise work and epilogue: warps w and w+4 share TMEM lanes
@@ -737,45 +752,64 @@ __device__ void bwd_compute(const BwdParams &p, uint8_t *smem, BwdBars *bars, ui
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars->s_read));
-                uint32_t pw[16], dw0[16], dw1[16];
-                bwd_chunk<BF, MODE>(p, s0, d0, c2x2, nl_row, nd_row, nullptr, nullptr, full, row,
-                                    j * kT + 64 * half, pw, dw0);
-                bwd_chunk<BF, MODE>(p, s1, d1, c2x2, nl_row, nd_row, nullptr, nullptr, full, row,
-                                    j * kT + 64 * half + 32, pw, dw1);
                 const uint32_t ds = lane_base + C::DS_COL + 64 * (j & 1) + 32 * half;
-                tmem_st16(ds, dw0);
-                tmem_st16(ds + 16, dw1);
-            } else {
-                uint32_t s0[32], d0[32], s1[32], d1[32];
-                tmem_ld32(lane_base + C::S_COL + 64 * half, s0);
-                tmem_ld32(lane_base + C::DP_COL + 64 * half, d0);
-                tmem_wait_ld2(s0, d0);
-                tmem_ld32(lane_base + C::S_COL + 64 * half + 32, s1);
-                tmem_ld32(lane_base + C::DP_COL + 64 * half + 32, d1);
-                tmem_wait_ld2(s1, d1);
-                if (half == 0) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(pair_bar);
+                {
+                    uint32_t pw[16], dw[16];
+                    bwd_chunk_sel<BF, MODE>(full, p, s0, d0, c2x2, nl_row, nd_row, nullptr, nullptr, row, j * kT + 64 * half, pw, dw);
+                    tmem_st16(ds, dw);
                 }
-                uint32_t pw0[16], dw0[16], pw1[16], dw1[16];
-                bwd_chunk<BF, MODE>(p, s0, d0, c2x2, 0, 0, vec + 64 * half, vec + kT + 64 * half, full, row,
-                                    j * kT + 64 * half, pw0, dw0);
-                bwd_chunk<BF, MODE>(p, s1, d1, c2x2, 0, 0, vec + 64 * half + 32, vec + kT + 64 * half + 32, full,
-                                    row, j * kT + 64 * half + 32, pw1, dw1);
-                if (half == 1) {
-                    const bool peer = warp_wait(pair_bar, pph, abort_flag);
-                    if (!peer) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                {
+                    uint32_t pw[16], dw[16];
+                    bwd_chunk_sel<BF, MODE>(full, p, s1, d1, c2x2, nl_row, nd_row, nullptr, nullptr, row, j * kT + 64 * half + 32, pw, dw);
+                    tmem_st16(ds + 16, dw);
+                }
+            } else if (half == 0) {
+                // queries 0-63: the upper half will overwrite columns 32-63 of S^T
+                // and dP^T, so read those first and signal; columns 0-31 are
+                // overwritten only by this warp
+                uint32_t s1[32], d1[32], s0[32], d0[32];
+                tmem_ld32(lane_base + C::S_COL + 32, s1);
+                tmem_ld32(lane_base + C::DP_COL + 32, d1);
+                tmem_wait_ld2(s1, d1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pair_bar);
+                tmem_ld32(lane_base + C::S_COL, s0);
+                tmem_ld32(lane_base + C::DP_COL, d0);
+                tmem_wait_ld2(s0, d0);
+                {
+                    uint32_t pw[16], dw[16];
+                    bwd_chunk_sel<BF, MODE>(full, p, s0, d0, c2x2, 0, 0, vec, vec + kT, row, j * kT, pw, dw);
+                    tmem_st16(lane_base + C::S_COL, pw);
+                    tmem_st16(lane_base + C::DP_COL, dw);
+                }
+                {
+                    uint32_t pw[16], dw[16];
+                    bwd_chunk_sel<BF, MODE>(full, p, s1, d1, c2x2, 0, 0, vec + 32, vec + kT + 32, row, j * kT + 32, pw, dw);
+                    tmem_st16(lane_base + C::S_COL + 16, pw);
+                    tmem_st16(lane_base + C::DP_COL + 16, dw);
                 }
                 pph ^= 1;
-                tmem_st16(lane_base + C::S_COL + 32 * half, pw0);
-                tmem_st16(lane_base + C::S_COL + 32 * half + 16, pw1);
-                tmem_st16(lane_base + C::DP_COL + 32 * half, dw0);
-                tmem_st16(lane_base + C::DP_COL + 32 * half + 16, dw1);
+            } else {
+                // queries 64-127: stores land on the lower half's columns 32-63,
+                // so wait until it has read them
+                const bool peer = warp_wait(pair_bar, pph, abort_flag);
+                pph ^= 1;
+                if (!peer) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t sv[32], dv[32], pw[16], dw[16];
+                    tmem_ld32(lane_base + C::S_COL + 64 + 32 * cc, sv);
+                    tmem_ld32(lane_base + C::DP_COL + 64 + 32 * cc, dv);
+                    tmem_wait_ld2(sv, dv);
+                    bwd_chunk_sel<BF, MODE>(full, p, sv, dv, c2x2, 0, 0, vec + 64 + 32 * cc, vec + kT + 64 + 32 * cc, row, j * kT + 64 + 32 * cc, pw, dw);
+                    tmem_st16(lane_base + C::S_COL + 32 + 16 * cc, pw);
+                    tmem_st16(lane_base + C::DP_COL + 32 + 16 * cc, dw);
+                }
             }
             tmem_wait_st();
             tc_fence_before();
