@@ -51,7 +51,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 enum Mode { kDQ = 0, kDKDV = 1 };
 
-template <int D_>
+template <int D_, int MODE_>
 struct BCfg {
     static constexpr int D = D_;
     static constexpr int ROW = D * 2;                       // bytes per row (16-bit types)
@@ -63,9 +63,17 @@ struct BCfg {
     static constexpr uint64_t SW_CODE = SW == 128 ? 2 : 4;  // 128-byte or 64-byte swizzle
     static constexpr int SBO = 8 * SW;
     static constexpr int OWN = 0;                           // two owned tiles
-    static constexpr int RING = 2 * TILE_BYTES;             // two stages of two tiles
-    static constexpr int VEC = RING + 2 * 2 * TILE_BYTES;   // per stage: -LSE*log2e and -D, 128 floats each
-    static constexpr int BARS = VEC + 2 * 2 * kT * 4;
+    // Loop tiles.  The dQ kernel keeps K and V in rings of their own: V_j is
+    // free once dP_j is done, K_j only after dQ += dS_j K_j, and a third K
+    // slot lets K_j+3 load while tile j+1 is worked on, so that no load waits
+    // on the MMA that frees its slot.  The dK/dV kernel has two stages, Q_i in
+    // the first ring and dO_i in the second, plus the stage's row vectors.
+    static constexpr int KSLOTS = MODE_ == kDQ ? 3 : 2;
+    static constexpr int VSLOTS = 2;
+    static constexpr int KRING = 2 * TILE_BYTES;
+    static constexpr int VRING = KRING + KSLOTS * TILE_BYTES;
+    static constexpr int VEC = VRING + VSLOTS * TILE_BYTES;  // dK/dV, per stage: -LSE*log2e and -D, 128 floats each
+    static constexpr int BARS = VEC + (MODE_ == kDKDV ? 2 * 2 * kT * 4 : 0);
     // at least 120 KB so that a second CTA never shares the SM: each
     // allocates all 512 TMEM columns; plus 1 KB to align for the swizzle
     static constexpr int SMEM_USED = BARS + 256;
@@ -90,11 +98,13 @@ struct BwdParams {
 struct BwdBars {
     uint64_t own_full, own_empty, s_full, c_full, acc_full, drain;
     uint64_t s_read;                    // dQ kernel: S and dP of the current tile are in registers
-    uint64_t st_full[2], st_empty[2];
+    uint64_t st_full[3], st_empty[3];   // K slots (dQ) or stages (dK/dV)
+    uint64_t v_full[2], v_empty[2];     // dQ kernel: V slots
     uint64_t pair_ld[4];                // dK/dV: the lower-half warp of a row quadrant has read S^T, dP^T
     uint32_t tmem_base;
     int abort;
 };
+static_assert(sizeof(BwdBars) <= 256, "barrier block");
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -367,9 +377,10 @@ __device__ __forceinline__ bool bwd_unit(const BwdParams &p, int u, BUnit &U) {
 // Roles
 // ---------------------------------------------------------------------------
 
-// Producer: the owned pair of tiles, then the loop pairs through a 2-stage
-// ring; in dK/dV mode the warp also writes each loop tile's 128 values of
-// LSE * log2(e) and D_i into the stage.
+// Producer: the owned pair of tiles, then the loop tiles: K_j and V_j into
+// their own rings for dQ, (Q_i, dO_i) pairs through a 2-stage ring for dK/dV,
+// where the warp also writes each loop tile's 128 values of -LSE * log2(e)
+// and -D_i into the stage.
 template <class C, int MODE>
 __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const CUtensorMap *tmK,
                              const CUtensorMap *tmV, const CUtensorMap *tmO, uint8_t *smem, BwdBars *bars,
@@ -385,7 +396,8 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
     // tiles from the other pair
     const CUtensorMap *own0 = MODE == kDQ ? tmQ : tmK, *own1 = MODE == kDQ ? tmO : tmV;
     const CUtensorMap *ld0 = MODE == kDQ ? tmK : tmQ, *ld1 = MODE == kDQ ? tmV : tmO;
-    uint32_t fill = 0, owned = 0;
+    constexpr int KS = C::KSLOTS;
+    uint32_t kfill = 0, vfill = 0, owned = 0;   // loads issued into each ring
     bool ok = true;
     for (int u = blockIdx.x; ok; u += gridDim.x) {
         BUnit U;
@@ -407,24 +419,47 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
         }
         ++owned;
         for (int j = U.j0; j < U.j1; ++j) {
-            const int st = fill & 1;
-            const uint32_t rnd = fill >> 1;
-            if (rnd > 0 && !warp_wait(smem_u32(&bars->st_empty[st]), (rnd - 1) & 1, abort_flag)) {
+            const int ks = kfill % KS;
+            const uint32_t kr = kfill / KS;
+            if (kr > 0 && !warp_wait(smem_u32(&bars->st_empty[ks]), (kr - 1) & 1, abort_flag)) {
                 ok = false;
                 break;
             }
-            const uint32_t fb = smem_u32(&bars->st_full[st]);
-            if (lane == 0) {
-                mbar_expect_tx(fb, 2 * C::TILE_BYTES);
-                const uint32_t dst = smem_u32(smem + C::RING + st * 2 * C::TILE_BYTES);
+            const uint32_t kb = smem_u32(&bars->st_full[ks]);
+            const uint32_t kdst = smem_u32(smem + C::KRING + ks * C::TILE_BYTES);
+            const uint32_t vdst = smem_u32(smem + C::VRING + (MODE == kDQ ? vfill & 1 : ks) * C::TILE_BYTES);
+            if constexpr (MODE == kDQ) {
+                if (lane == 0) {
+                    mbar_expect_tx(kb, C::TILE_BYTES);
 #pragma unroll
-                for (int pn = 0; pn < C::PANELS; ++pn) {
-                    tma_load_4d(dst + pn * C::PANEL_BYTES, ld0, fb, pn * C::BOX_D, U.h, j * kT, U.b);
-                    tma_load_4d(dst + C::TILE_BYTES + pn * C::PANEL_BYTES, ld1, fb, pn * C::BOX_D, U.h, j * kT, U.b);
+                    for (int pn = 0; pn < C::PANELS; ++pn)
+                        tma_load_4d(kdst + pn * C::PANEL_BYTES, ld0, kb, pn * C::BOX_D, U.h, j * kT, U.b);
                 }
-            }
-            if constexpr (MODE == kDKDV) {
-                float *vec = reinterpret_cast<float *>(smem + C::VEC) + st * 2 * kT;
+                ++kfill;
+                const int vs = vfill & 1;
+                const uint32_t vr = vfill >> 1;
+                if (vr > 0 && !warp_wait(smem_u32(&bars->v_empty[vs]), (vr - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t vb = smem_u32(&bars->v_full[vs]);
+                if (lane == 0) {
+                    mbar_expect_tx(vb, C::TILE_BYTES);
+#pragma unroll
+                    for (int pn = 0; pn < C::PANELS; ++pn)
+                        tma_load_4d(vdst + pn * C::PANEL_BYTES, ld1, vb, pn * C::BOX_D, U.h, j * kT, U.b);
+                }
+                ++vfill;
+            } else {
+                if (lane == 0) {
+                    mbar_expect_tx(kb, 2 * C::TILE_BYTES);
+#pragma unroll
+                    for (int pn = 0; pn < C::PANELS; ++pn) {
+                        tma_load_4d(kdst + pn * C::PANEL_BYTES, ld0, kb, pn * C::BOX_D, U.h, j * kT, U.b);
+                        tma_load_4d(vdst + pn * C::PANEL_BYTES, ld1, kb, pn * C::BOX_D, U.h, j * kT, U.b);
+                    }
+                }
+                float *vec = reinterpret_cast<float *>(smem + C::VEC) + ks * 2 * kT;
                 const int64_t base = ((int64_t)U.b * p.H + U.h) * p.Sq;
 #pragma unroll
                 for (int i = 0; i < kT / 32; ++i) {
@@ -434,21 +469,30 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
                     vec[kT + i * 32 + lane] = in ? -p.dvec[base + q] : 0.f;            // -D
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(fb);
+                if (lane == 0) mbar_arrive(kb);
+                ++kfill;
             }
-            ++fill;
         }
     }
     if (ok) {
-        // the last releases of every stage and of the owned tiles
-        for (int st = 0; st < 2; ++st) {
-            const uint32_t nf = fill > (uint32_t)st ? (fill - st + 1) / 2 : 0;
+        // the last releases of every slot and of the owned tiles
+        for (int st = 0; st < KS; ++st) {
+            const uint32_t nf = kfill > (uint32_t)st ? (kfill - st + KS - 1) / KS : 0;
             if (nf && !warp_wait(smem_u32(&bars->st_empty[st]), (nf - 1) & 1, abort_flag)) break;
+        }
+        if (MODE == kDQ) {
+            for (int st = 0; st < 2; ++st) {
+                const uint32_t nf = vfill > (uint32_t)st ? (vfill - st + 1) / 2 : 0;
+                if (nf && !warp_wait(smem_u32(&bars->v_empty[st]), (nf - 1) & 1, abort_flag)) break;
+            }
         }
         if (owned) warp_wait(smem_u32(&bars->own_empty), (owned - 1) & 1, abort_flag);
     } else if (lane == 0) {
-        const uint32_t first = fill > 2 ? fill - 2 : 0;
-        for (uint32_t f = first; f < fill; ++f) mbar_wait_drain(smem_u32(&bars->st_full[f & 1]), (f >> 1) & 1);
+        // let the copies in flight land before the CTA exits
+        for (uint32_t f = kfill > (uint32_t)KS ? kfill - KS : 0; f < kfill; ++f)
+            mbar_wait_drain(smem_u32(&bars->st_full[f % KS]), (f / KS) & 1);
+        for (uint32_t f = vfill > 2 ? vfill - 2 : 0; f < vfill; ++f)
+            mbar_wait_drain(smem_u32(&bars->v_full[f & 1]), (f >> 1) & 1);
         if (owned) mbar_wait_drain(smem_u32(&bars->own_full), (owned - 1) & 1);
     }
 }
@@ -458,39 +502,39 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
 // have read S_j and dP_j (s_read), and dQ += dS_j K_j once dS_j is written
 // (c_full): the elementwise work of tile j overlaps the MMAs of tile j+1.
 // In issue order S_j+2 follows dQ_j, so "S_j+2 complete" implies "dS buffer
-// j % 2 read".
+// j % 2 read".  V_j's slot is released after dP_j, K_j's after dQ_j.
 template <class C, bool BF>
 __device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem) {
     volatile int *abort_flag = &bars->abort;
     constexpr uint32_t fmt = BF ? 1u : 0u;
     constexpr uint32_t kIdS = bwd_idesc(fmt, kT, false);
     constexpr uint32_t kIdAcc = bwd_idesc(fmt, C::D, true);
+    constexpr int KS = C::KSLOTS;
     const uint32_t own = smem_u32(smem + C::OWN);
     const uint64_t a0 = smem_desc(own, 16, C::SBO, C::SW_CODE);                     // Q
     const uint64_t a1 = smem_desc(own + C::TILE_BYTES, 16, C::SBO, C::SW_CODE);     // dO
+    const uint32_t kring = smem_u32(smem + C::KRING), vring = smem_u32(smem + C::VRING);
     uint32_t cons = 0, owned = 0, cc = 0, rc = 0;
     bool ok = true;
-    auto ring = [&](int st) { return smem_u32(smem + C::RING + st * 2 * C::TILE_BYTES); };
-    // S = Q K^T and dP = dO V^T of the tile in stage st
-    auto issue_s = [&](int st) {
-        const uint64_t bk = smem_desc(ring(st), 16, C::SBO, C::SW_CODE);
-        const uint64_t bv = smem_desc(ring(st) + C::TILE_BYTES, 16, C::SBO, C::SW_CODE);
+    // S = Q K^T and dP = dO V^T of the loop tile with sequence number c
+    auto issue_s = [&](uint32_t c) -> bool {
+        const int ks = c % KS, vs = c & 1;
+        if (!mbar_wait(smem_u32(&bars->st_full[ks]), (c / KS) & 1, abort_flag)) return false;
+        const uint64_t bk = smem_desc(kring + ks * C::TILE_BYTES, 16, C::SBO, C::SW_CODE);
 #pragma unroll
         for (int kk = 0; kk < C::D / 16; ++kk) {
             const uint32_t off = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
             mma_ss(tmem + C::S_COL, a0 + off, bk + off, kIdS, kk > 0 ? 1u : 0u);
         }
+        if (!mbar_wait(smem_u32(&bars->v_full[vs]), (c >> 1) & 1, abort_flag)) return false;
+        const uint64_t bv = smem_desc(vring + vs * C::TILE_BYTES, 16, C::SBO, C::SW_CODE);
 #pragma unroll
         for (int kk = 0; kk < C::D / 16; ++kk) {
             const uint32_t off = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
             mma_ss(tmem + C::DP_COL, a1 + off, bv + off, kIdS, kk > 0 ? 1u : 0u);
         }
-    };
-    auto next_stage = [&](int &st) -> bool {
-        st = cons & 1;
-        const bool r = mbar_wait(smem_u32(&bars->st_full[st]), (cons >> 1) & 1, abort_flag);
-        ++cons;
-        return r;
+        tc_commit(smem_u32(&bars->v_empty[vs]));
+        return true;
     };
     for (int u = blockIdx.x; ok; u += gridDim.x) {
         BUnit U;
@@ -498,39 +542,33 @@ __device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uin
         if (U.j0 >= U.j1) continue;
         if (!mbar_wait(smem_u32(&bars->own_full), owned & 1, abort_flag)) break;
         ++owned;
-        int st;
-        if (!next_stage(st)) break;
-        issue_s(st);
+        uint32_t cur = cons;                 // sequence number of tile j
+        if (!issue_s(cons++)) break;
         if (U.j0 + 1 == U.j1) tc_commit(smem_u32(&bars->own_empty));
         tc_commit(smem_u32(&bars->s_full));
         for (int j = U.j0; j < U.j1; ++j) {
+            if (!mbar_wait(smem_u32(&bars->s_read), rc & 1, abort_flag)) { ok = false; break; }
+            ++rc;
             if (j + 1 < U.j1) {
-                int st2;
-                if (!next_stage(st2)) { ok = false; break; }
-                if (!mbar_wait(smem_u32(&bars->s_read), rc & 1, abort_flag)) { ok = false; break; }
-                ++rc;
                 tc_fence_after();
-                issue_s(st2);
+                if (!issue_s(cons++)) { ok = false; break; }
                 if (j + 2 == U.j1) tc_commit(smem_u32(&bars->own_empty));
                 tc_commit(smem_u32(&bars->s_full));
-            } else {
-                // the last tile's s_read keeps the phase count in step
-                if (!mbar_wait(smem_u32(&bars->s_read), rc & 1, abort_flag)) { ok = false; break; }
-                ++rc;
             }
             if (!mbar_wait(smem_u32(&bars->c_full), cc & 1, abort_flag)) { ok = false; break; }
             ++cc;
             tc_fence_after();
             // dQ += dS_j K_j: A = dS buffer j % 2 (16-bit, 8 columns per step of
             // 16 keys), B = K_j rows MN-major
+            const int ks = cur % KS;
             const uint32_t ds = tmem + C::DS_COL + 64 * (j & 1);
-            const uint64_t bk = smem_desc(ring(st), C::PANEL_BYTES, C::SBO, C::SW_CODE);
+            const uint64_t bk = smem_desc(kring + ks * C::TILE_BYTES, C::PANEL_BYTES, C::SBO, C::SW_CODE);
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
                 mma_ts(tmem + C::ACC0, ds + kk * 8, bk + ((kk * 16 * C::SW) >> 4), kIdAcc,
                        (j > U.j0 || kk > 0) ? 1u : 0u);
-            tc_commit(smem_u32(&bars->st_empty[st]));
-            st = (st + 1) & 1;     // tile j+1's stage (issued above)
+            tc_commit(smem_u32(&bars->st_empty[ks]));
+            ++cur;
         }
         if (!ok) break;
         tc_commit(smem_u32(&bars->acc_full));
@@ -539,12 +577,14 @@ __device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uin
     mbar_wait_drain(smem_u32(&bars->drain), 0);
 }
 
-// MMA issuer (one lane).  Per loop tile: S and dP (both SS, K-major), then,
-// once the compute warps wrote dS (and P^T), the accumulating MMA(s) with A
-// from TMEM and B = a loop tile read MN-major.  In-order issue makes "S of
-// tile j+1 complete" imply "the accumulation of tile j complete".
-template <class C, bool BF, int MODE>
-__device__ void bwd_mma(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem) {
+// MMA issuer of the dK/dV kernel (one lane).  Per loop tile: S^T and dP^T
+// (both SS, K-major), then, once the compute warps wrote P^T and dS^T, the two
+// accumulating MMAs with A from TMEM and B = a loop tile read MN-major.
+// In-order issue makes "S^T of tile j+1 complete" imply "the accumulation of
+// tile j complete".
+template <class C, bool BF>
+__device__ void bwd_mma_dkdv(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem) {
+    constexpr int MODE = kDKDV;
     volatile int *abort_flag = &bars->abort;
     constexpr uint32_t fmt = BF ? 1u : 0u;
     constexpr uint32_t kIdS = bwd_idesc(fmt, kT, false);
@@ -567,9 +607,10 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32
                 break;
             }
             ++cons;
-            const uint32_t ring = smem_u32(smem + C::RING + st * 2 * C::TILE_BYTES);
-            const uint64_t b0 = smem_desc(ring, 16, C::SBO, C::SW_CODE);
-            const uint64_t b1 = smem_desc(ring + C::TILE_BYTES, 16, C::SBO, C::SW_CODE);
+            const uint32_t r0 = smem_u32(smem + C::KRING + st * C::TILE_BYTES);   // Q_i
+            const uint32_t r1 = smem_u32(smem + C::VRING + st * C::TILE_BYTES);   // dO_i
+            const uint64_t b0 = smem_desc(r0, 16, C::SBO, C::SW_CODE);
+            const uint64_t b1 = smem_desc(r1, 16, C::SBO, C::SW_CODE);
             // S (or S^T) = own0 . ld0^T and dP (or dP^T) = own1 . ld1^T over the head dim
 #pragma unroll
             for (int kk = 0; kk < C::D / 16; ++kk) {
@@ -592,15 +633,9 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32
             // accumulate over the 128 loop rows (16 per MMA): A = 16-bit values in
             // TMEM (8 columns per step), B = loop tile rows, MN-major
             const uint32_t acc = j > U.j0 ? 1u : 0u;
-            if constexpr (MODE == kDQ) {
-                const uint64_t bk = smem_desc(ring, C::PANEL_BYTES, C::SBO, C::SW_CODE);   // K_j
-#pragma unroll
-                for (int kk = 0; kk < kT / 16; ++kk)
-                    mma_ts(tmem + C::ACC0, tmem + C::DS_COL + kk * 8, bk + ((kk * 16 * C::SW) >> 4), kIdAcc,
-                           (acc || kk > 0) ? 1u : 0u);
-            } else {
-                const uint64_t bo = smem_desc(ring + C::TILE_BYTES, C::PANEL_BYTES, C::SBO, C::SW_CODE);   // dO_i
-                const uint64_t bq = smem_desc(ring, C::PANEL_BYTES, C::SBO, C::SW_CODE);                   // Q_i
+            {
+                const uint64_t bo = smem_desc(r1, C::PANEL_BYTES, C::SBO, C::SW_CODE);   // dO_i
+                const uint64_t bq = smem_desc(r0, C::PANEL_BYTES, C::SBO, C::SW_CODE);   // Q_i
 #pragma unroll
                 for (int kk = 0; kk < kT / 16; ++kk)
                     mma_ts(tmem + C::ACC0, tmem + C::S_COL + kk * 8, bo + ((kk * 16 * C::SW) >> 4), kIdAcc,
@@ -886,10 +921,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&bars->pair_ld[w]), 1);
         mbar_init(smem_u32(&bars->acc_full), 1);
         mbar_init(smem_u32(&bars->drain), 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < 3; ++s) {
             // dK/dV mode: the TMA transaction plus the producer warp's row vectors
             mbar_init(smem_u32(&bars->st_full[s]), MODE == kDKDV ? 2 : 1);
             mbar_init(smem_u32(&bars->st_empty[s]), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&bars->v_full[s]), 1);
+            mbar_init(smem_u32(&bars->v_empty[s]), 1);
         }
         bars->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -909,7 +948,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         if (lane == 0) {
             if constexpr (MODE == kDQ) bwd_mma_dq<C, BF>(p, smem, bars, tmem);
-            else bwd_mma<C, BF, MODE>(p, smem, bars, tmem);
+            else bwd_mma_dkdv<C, BF>(p, smem, bars, tmem);
         }
     }
     tc_fence_before();
@@ -986,9 +1025,23 @@ bool bwd_map(CUtensorMap *m, const void *base, bool bf, int H, int rows, int B) 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <class C, int MODE>
+int bwd_launch_mode(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
+                    const BwdParams &p, bool bf, int sms, cudaStream_t stream) {
+    const int own = MODE == kDQ ? (p.Sq + kT - 1) / kT : (p.Sk + kT - 1) / kT;
+    const int64_t units = (int64_t)p.B * p.H * own;
+    const int grid = (int)(units < sms ? units : sms);
+    if (grid <= 0) return FMHA_OK;
+    auto kern = bf ? fmha_bwd_kernel<C, true, MODE> : fmha_bwd_kernel<C, false, MODE>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+        return FMHA_ERR_CUDA;
+    kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, to, p);
+    return cudaGetLastError() == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
+}
+
 template <int D>
 int bwd_launch(const BwdParams &p, bool bf, cudaStream_t stream) {
-    using C = BCfg<D>;
+    using C = BCfg<D, kDQ>;
     CUtensorMap tq, tk, tv, to;
     if (!bwd_map<C>(&tq, p.q, bf, p.H, p.Sq, p.B) || !bwd_map<C>(&tk, p.k, bf, p.H, p.Sk, p.B) ||
         !bwd_map<C>(&tv, p.v, bf, p.H, p.Sk, p.B) || !bwd_map<C>(&to, p.dout, bf, p.H, p.Sq, p.B))
@@ -1001,19 +1054,9 @@ int bwd_launch(const BwdParams &p, bool bf, cudaStream_t stream) {
     dot<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
     // 2) dQ, 3) dK and dV
-    for (int mode = 0; mode < 2; ++mode) {
-        const int own = mode == kDQ ? (p.Sq + kT - 1) / kT : (p.Sk + kT - 1) / kT;
-        const int64_t units = (int64_t)p.B * p.H * own;
-        const int grid = (int)(units < sms ? units : sms);
-        if (grid <= 0) continue;
-        auto kern = mode == kDQ ? (bf ? fmha_bwd_kernel<C, true, kDQ> : fmha_bwd_kernel<C, false, kDQ>)
-                                : (bf ? fmha_bwd_kernel<C, true, kDKDV> : fmha_bwd_kernel<C, false, kDKDV>);
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
-            return FMHA_ERR_CUDA;
-        kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, to, p);
-        if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
-    }
-    return FMHA_OK;
+    const int r = bwd_launch_mode<BCfg<D, kDQ>, kDQ>(tq, tk, tv, to, p, bf, sms, stream);
+    if (r != FMHA_OK) return r;
+    return bwd_launch_mode<BCfg<D, kDKDV>, kDKDV>(tq, tk, tv, to, p, bf, sms, stream);
 }
 
 }  // namespace
