@@ -43,7 +43,9 @@ constexpr int kT = 128;                 // rows per tile, both sides
 constexpr int kCompWarps = 8;           // warps 0-7: elementwise work and epilogue
 constexpr int kProdWarp = 8;            // TMA producer (all lanes: the dK/dV kernel's row vectors)
 constexpr int kMmaWarp = 9;             // tcgen05.mma issuer (lane 0), owns TMEM
-constexpr int kThreads = 320;
+constexpr int kMmaWarp2 = 10;           // dK/dV kernel: issuer (lane 0) of query half b
+constexpr int kThreads = 352;
+static_assert(kThreads == 32 * (kMmaWarp2 + 1), "one warp per role");
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;
 constexpr unsigned long long kDrainNs = 200000000ull;
@@ -66,14 +68,20 @@ struct BCfg {
     // Loop tiles.  The dQ kernel keeps K and V in rings of their own: V_j is
     // free once dP_j is done, K_j only after dQ += dS_j K_j, and a third K
     // slot lets K_j+3 load while tile j+1 is worked on, so that no load waits
-    // on the MMA that frees its slot.  The dK/dV kernel has two stages, Q_i in
-    // the first ring and dO_i in the second, plus the stage's row vectors.
-    static constexpr int KSLOTS = MODE_ == kDQ ? 3 : 2;
-    static constexpr int VSLOTS = 2;
+    // on the MMA that frees its slot.
+    static constexpr int KSLOTS = 3, VSLOTS = 2;
     static constexpr int KRING = 2 * TILE_BYTES;
     static constexpr int VRING = KRING + KSLOTS * TILE_BYTES;
-    static constexpr int VEC = VRING + VSLOTS * TILE_BYTES;  // dK/dV, per stage: -LSE*log2e and -D, 128 floats each
-    static constexpr int BARS = VEC + (MODE_ == kDKDV ? 2 * 2 * kT * 4 : 0);
+    // The dK/dV kernel works through each query tile in two halves of 64 rows
+    // and keeps a ring of four half slots (Q rows, then dO rows, of one half)
+    // with the half's row vectors (-LSE*log2e, then -D; 64 floats each): a
+    // half's slot is free once that half's accumulation is done, a whole tile
+    // period before the slot's next half is needed.
+    static constexpr int HSLOTS = 4, HALF_BYTES = TILE_BYTES / 2, HPANEL = PANEL_BYTES / 2;
+    static constexpr int HRING = 2 * TILE_BYTES;
+    static constexpr int HVEC = HRING + HSLOTS * TILE_BYTES;
+    static constexpr int HVEC_BYTES = 2 * (kT / 2) * 4;
+    static constexpr int BARS = MODE_ == kDQ ? VRING + VSLOTS * TILE_BYTES : HVEC + HSLOTS * HVEC_BYTES;
     // at least 120 KB so that a second CTA never shares the SM: each
     // allocates all 512 TMEM columns; plus 1 KB to align for the swizzle
     static constexpr int SMEM_USED = BARS + 256;
@@ -96,11 +104,14 @@ struct BwdParams {
 };
 
 struct BwdBars {
-    uint64_t own_full, own_empty, s_full, c_full, acc_full, drain;
+    uint64_t own_full, own_empty, acc_full, drain;
+    uint64_t acc_empty;                 // dK/dV: every compute warp has read the accumulators
+    uint64_t turn[2];                   // dK/dV: issuing turn of lane a / lane b
+    uint64_t s_full[2], c_full[2];      // dQ: index 0 only; dK/dV: one per half of the query tile
     uint64_t s_read;                    // dQ kernel: S and dP of the current tile are in registers
-    uint64_t st_full[3], st_empty[3];   // K slots (dQ) or stages (dK/dV)
+    uint64_t st_full[3], st_empty[3];   // dQ kernel: K slots
     uint64_t v_full[2], v_empty[2];     // dQ kernel: V slots
-    uint64_t pair_ld[4];                // dK/dV: the lower-half warp of a row quadrant has read S^T, dP^T
+    uint64_t h_full[4], h_empty[4];     // dK/dV kernel: half slots
     uint32_t tmem_base;
     int abort;
 };
@@ -378,9 +389,9 @@ __device__ __forceinline__ bool bwd_unit(const BwdParams &p, int u, BUnit &U) {
 // ---------------------------------------------------------------------------
 
 // Producer: the owned pair of tiles, then the loop tiles: K_j and V_j into
-// their own rings for dQ, (Q_i, dO_i) pairs through a 2-stage ring for dK/dV,
-// where the warp also writes each loop tile's 128 values of -LSE * log2(e)
-// and -D_i into the stage.
+// their own rings for dQ; for dK/dV each query half (64 rows of Q_i and of
+// dO_i) into a half slot, where the warp also writes the half's 64 values of
+// -LSE * log2(e) and -D.
 template <class C, int MODE>
 __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const CUtensorMap *tmK,
                              const CUtensorMap *tmV, const CUtensorMap *tmO, uint8_t *smem, BwdBars *bars,
@@ -397,7 +408,7 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
     const CUtensorMap *own0 = MODE == kDQ ? tmQ : tmK, *own1 = MODE == kDQ ? tmO : tmV;
     const CUtensorMap *ld0 = MODE == kDQ ? tmK : tmQ, *ld1 = MODE == kDQ ? tmV : tmO;
     constexpr int KS = C::KSLOTS;
-    uint32_t kfill = 0, vfill = 0, owned = 0;   // loads issued into each ring
+    uint32_t kfill = 0, vfill = 0, hfill = 0, owned = 0;   // loads issued into each ring
     bool ok = true;
     for (int u = blockIdx.x; ok; u += gridDim.x) {
         BUnit U;
@@ -418,17 +429,16 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
             }
         }
         ++owned;
-        for (int j = U.j0; j < U.j1; ++j) {
-            const int ks = kfill % KS;
-            const uint32_t kr = kfill / KS;
-            if (kr > 0 && !warp_wait(smem_u32(&bars->st_empty[ks]), (kr - 1) & 1, abort_flag)) {
-                ok = false;
-                break;
-            }
-            const uint32_t kb = smem_u32(&bars->st_full[ks]);
-            const uint32_t kdst = smem_u32(smem + C::KRING + ks * C::TILE_BYTES);
-            const uint32_t vdst = smem_u32(smem + C::VRING + (MODE == kDQ ? vfill & 1 : ks) * C::TILE_BYTES);
-            if constexpr (MODE == kDQ) {
+        if constexpr (MODE == kDQ) {
+            for (int j = U.j0; j < U.j1; ++j) {
+                const int ks = kfill % KS;
+                const uint32_t kr = kfill / KS;
+                if (kr > 0 && !warp_wait(smem_u32(&bars->st_empty[ks]), (kr - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t kb = smem_u32(&bars->st_full[ks]);
+                const uint32_t kdst = smem_u32(smem + C::KRING + ks * C::TILE_BYTES);
                 if (lane == 0) {
                     mbar_expect_tx(kb, C::TILE_BYTES);
 #pragma unroll
@@ -443,6 +453,7 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
                     break;
                 }
                 const uint32_t vb = smem_u32(&bars->v_full[vs]);
+                const uint32_t vdst = smem_u32(smem + C::VRING + vs * C::TILE_BYTES);
                 if (lane == 0) {
                     mbar_expect_tx(vb, C::TILE_BYTES);
 #pragma unroll
@@ -450,40 +461,62 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
                         tma_load_4d(vdst + pn * C::PANEL_BYTES, ld1, vb, pn * C::BOX_D, U.h, j * kT, U.b);
                 }
                 ++vfill;
-            } else {
-                if (lane == 0) {
-                    mbar_expect_tx(kb, 2 * C::TILE_BYTES);
-#pragma unroll
-                    for (int pn = 0; pn < C::PANELS; ++pn) {
-                        tma_load_4d(kdst + pn * C::PANEL_BYTES, ld0, kb, pn * C::BOX_D, U.h, j * kT, U.b);
-                        tma_load_4d(vdst + pn * C::PANEL_BYTES, ld1, kb, pn * C::BOX_D, U.h, j * kT, U.b);
+            }
+        } else {
+            // half x of loop tile j: 64 rows of Q and dO (64-row boxes) and the
+            // rows' vectors
+            const int64_t base = ((int64_t)U.b * p.H + U.h) * p.Sq;
+            for (int j = U.j0; j < U.j1 && ok; ++j) {
+#pragma unroll 1
+                for (int x = 0; x < 2; ++x) {
+                    const int hs = hfill & 3;
+                    const uint32_t hr = hfill >> 2;
+                    if (hr > 0 && !warp_wait(smem_u32(&bars->h_empty[hs]), (hr - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
                     }
-                }
-                float *vec = reinterpret_cast<float *>(smem + C::VEC) + ks * 2 * kT;
-                const int64_t base = ((int64_t)U.b * p.H + U.h) * p.Sq;
+                    const uint32_t hb = smem_u32(&bars->h_full[hs]);
+                    const uint32_t dst = smem_u32(smem + C::HRING + hs * C::TILE_BYTES);
+                    const int r0 = j * kT + x * (kT / 2);
+                    if (lane == 0) {
+                        mbar_expect_tx(hb, C::TILE_BYTES);
 #pragma unroll
-                for (int i = 0; i < kT / 32; ++i) {
-                    const int q = j * kT + i * 32 + lane;
-                    const bool in = q < p.Sq;
-                    vec[i * 32 + lane] = in ? -p.lse[base + q] * kLog2e : -INFINITY;   // -LSE * log2(e)
-                    vec[kT + i * 32 + lane] = in ? -p.dvec[base + q] : 0.f;            // -D
+                        for (int pn = 0; pn < C::PANELS; ++pn) {
+                            tma_load_4d(dst + pn * C::HPANEL, ld0, hb, pn * C::BOX_D, U.h, r0, U.b);
+                            tma_load_4d(dst + C::HALF_BYTES + pn * C::HPANEL, ld1, hb, pn * C::BOX_D, U.h, r0, U.b);
+                        }
+                    }
+                    float *vec = reinterpret_cast<float *>(smem + C::HVEC + hs * C::HVEC_BYTES);
+#pragma unroll
+                    for (int i = 0; i < kT / 64; ++i) {
+                        const int q = r0 + i * 32 + lane;
+                        const bool in = q < p.Sq;
+                        vec[i * 32 + lane] = in ? -p.lse[base + q] * kLog2e : -INFINITY;    // -LSE * log2(e)
+                        vec[kT / 2 + i * 32 + lane] = in ? -p.dvec[base + q] : 0.f;         // -D
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(hb);
+                    ++hfill;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(kb);
-                ++kfill;
             }
         }
+        if (!ok) break;
     }
     if (ok) {
         // the last releases of every slot and of the owned tiles
-        for (int st = 0; st < KS; ++st) {
-            const uint32_t nf = kfill > (uint32_t)st ? (kfill - st + KS - 1) / KS : 0;
-            if (nf && !warp_wait(smem_u32(&bars->st_empty[st]), (nf - 1) & 1, abort_flag)) break;
-        }
         if (MODE == kDQ) {
+            for (int st = 0; st < KS; ++st) {
+                const uint32_t nf = kfill > (uint32_t)st ? (kfill - st + KS - 1) / KS : 0;
+                if (nf && !warp_wait(smem_u32(&bars->st_empty[st]), (nf - 1) & 1, abort_flag)) break;
+            }
             for (int st = 0; st < 2; ++st) {
                 const uint32_t nf = vfill > (uint32_t)st ? (vfill - st + 1) / 2 : 0;
                 if (nf && !warp_wait(smem_u32(&bars->v_empty[st]), (nf - 1) & 1, abort_flag)) break;
+            }
+        } else {
+            for (int st = 0; st < 4; ++st) {
+                const uint32_t nf = hfill > (uint32_t)st ? (hfill - st + 3) / 4 : 0;
+                if (nf && !warp_wait(smem_u32(&bars->h_empty[st]), (nf - 1) & 1, abort_flag)) break;
             }
         }
         if (owned) warp_wait(smem_u32(&bars->own_empty), (owned - 1) & 1, abort_flag);
@@ -493,6 +526,8 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
             mbar_wait_drain(smem_u32(&bars->st_full[f % KS]), (f / KS) & 1);
         for (uint32_t f = vfill > 2 ? vfill - 2 : 0; f < vfill; ++f)
             mbar_wait_drain(smem_u32(&bars->v_full[f & 1]), (f >> 1) & 1);
+        for (uint32_t f = hfill > 4 ? hfill - 4 : 0; f < hfill; ++f)
+            mbar_wait_drain(smem_u32(&bars->h_full[f & 3]), (f >> 2) & 1);
         if (owned) mbar_wait_drain(smem_u32(&bars->own_full), (owned - 1) & 1);
     }
 }
@@ -545,7 +580,7 @@ __device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uin
         uint32_t cur = cons;                 // sequence number of tile j
         if (!issue_s(cons++)) break;
         if (U.j0 + 1 == U.j1) tc_commit(smem_u32(&bars->own_empty));
-        tc_commit(smem_u32(&bars->s_full));
+        tc_commit(smem_u32(&bars->s_full[0]));
         for (int j = U.j0; j < U.j1; ++j) {
             if (!mbar_wait(smem_u32(&bars->s_read), rc & 1, abort_flag)) { ok = false; break; }
             ++rc;
@@ -553,9 +588,9 @@ __device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uin
                 tc_fence_after();
                 if (!issue_s(cons++)) { ok = false; break; }
                 if (j + 2 == U.j1) tc_commit(smem_u32(&bars->own_empty));
-                tc_commit(smem_u32(&bars->s_full));
+                tc_commit(smem_u32(&bars->s_full[0]));
             }
-            if (!mbar_wait(smem_u32(&bars->c_full), cc & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(smem_u32(&bars->c_full[0]), cc & 1, abort_flag)) { ok = false; break; }
             ++cc;
             tc_fence_after();
             // dQ += dS_j K_j: A = dS buffer j % 2 (16-bit, 8 columns per step of
@@ -577,78 +612,116 @@ __device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uin
     mbar_wait_drain(smem_u32(&bars->drain), 0);
 }
 
-// MMA issuer of the dK/dV kernel (one lane).  Per loop tile: S^T and dP^T
-// (both SS, K-major), then, once the compute warps wrote P^T and dS^T, the two
-// accumulating MMAs with A from TMEM and B = a loop tile read MN-major.
-// In-order issue makes "S^T of tile j+1 complete" imply "the accumulation of
-// tile j complete".
+// MMA issuers of the dK/dV kernel: lane 0 of warp kMmaWarp for query half a,
+// of warp kMmaWarp2 for half b.  The loop tile's 128 queries are taken in two
+// halves of 64 with TMEM of their own: S^T and dP^T of half x (M = 128 keys,
+// N = 64 queries) land in columns S_COL + 64x and DP_COL + 64x, four compute
+// warps turn them into P^T and dS^T in place, and dV += P^T dO, dK += dS^T Q
+// then take the half's 64 queries as the reduction.  While one half is in the
+// compute warps the MMAs of the other run, so the tensor pipe and the
+// elementwise work overlap.
+//
+// The lanes take turns; turn k of lane x issues acc(x, i-1) and S/dP(x, i)
+// for loop tile i = j0 + k (the first turn of a unit has no accumulation,
+// the last no S/dP), so the pipe sees a, b, a, b, ... and "S^T of half x of
+// tile i complete" implies "the accumulation from half x of tile i-1
+// complete", which is what lets S^T overwrite P^T.  A lane does its waits
+// (c_full, the stage, the previous unit's epilogue) before taking its turn,
+// while the other lane issues, and hands the turn over two MMAs before its
+// last one, so the pipe never drains between turns: an MMA holds its issuing
+// thread for most of its pipe time, and one lane alone cannot both issue and
+// wait.  Lane a's first accumulation of a unit overwrites dV and dK; lane b's
+// comes a turn later.
 template <class C, bool BF>
-__device__ void bwd_mma_dkdv(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem) {
-    constexpr int MODE = kDKDV;
+__device__ void bwd_mma_dkdv(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem, int x) {
     volatile int *abort_flag = &bars->abort;
     constexpr uint32_t fmt = BF ? 1u : 0u;
-    constexpr uint32_t kIdS = bwd_idesc(fmt, kT, false);
+    constexpr uint32_t kIdS = bwd_idesc(fmt, kT / 2, false);
     constexpr uint32_t kIdAcc = bwd_idesc(fmt, C::D, true);
+    constexpr int kSteps = C::D / 16;                  // MMAs of one S^T (or dP^T)
+    constexpr int kPassAt = 2 * kSteps - 3;            // S/dP MMA (index) after which the turn passes
     const uint32_t own = smem_u32(smem + C::OWN);
-    uint32_t cons = 0, owned = 0, cc = 0;
+    const uint64_t a0 = smem_desc(own, 16, C::SBO, C::SW_CODE);                     // K (owned)
+    const uint64_t a1 = smem_desc(own + C::TILE_BYTES, 16, C::SBO, C::SW_CODE);     // V (owned)
+    const uint32_t my_turn = smem_u32(&bars->turn[x]), next_turn = smem_u32(&bars->turn[x ^ 1]);
+    uint32_t cons = 0, owned = 0, cc = 0, units = 0, turns = 0;
     bool ok = true;
+    // S^T and dP^T of half x from half slot hs (B = its 64 rows of Q_i, dO_i);
+    // passes the turn two MMAs before the end
+    auto issue_sdp = [&](int hs) {
+        const uint32_t q = smem_u32(smem + C::HRING + hs * C::TILE_BYTES), o = q + C::HALF_BYTES;
+        const uint64_t bq = smem_desc(q, 16, C::SBO, C::SW_CODE), bo = smem_desc(o, 16, C::SBO, C::SW_CODE);
+#pragma unroll
+        for (int kk = 0; kk < kSteps; ++kk) {
+            const uint32_t oa = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
+            const uint32_t ob = ((kk * 32 / C::SW) * C::HPANEL + (kk * 32) % C::SW) >> 4;
+            mma_ss(tmem + C::S_COL + 64 * x, a0 + oa, bq + ob, kIdS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kSteps; ++kk) {
+            const uint32_t oa = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
+            const uint32_t ob = ((kk * 32 / C::SW) * C::HPANEL + (kk * 32) % C::SW) >> 4;
+            mma_ss(tmem + C::DP_COL + 64 * x, a1 + oa, bo + ob, kIdS, kk > 0 ? 1u : 0u);
+            if (kSteps + kk == kPassAt) mbar_arrive(next_turn);
+        }
+        tc_commit(smem_u32(&bars->s_full[x]));
+    };
+    // dV += P^T_x dO_x and dK += dS^T_x Q_x over the half's 64 queries (16 per
+    // MMA): A = 16-bit values in TMEM (8 columns per step), B = the slot's
+    // rows MN-major
+    auto issue_acc = [&](int hs, bool first) {
+        const uint32_t q = smem_u32(smem + C::HRING + hs * C::TILE_BYTES), o = q + C::HALF_BYTES;
+        const uint64_t bq = smem_desc(q, C::HPANEL, C::SBO, C::SW_CODE), bo = smem_desc(o, C::HPANEL, C::SBO, C::SW_CODE);
+#pragma unroll
+        for (int kk = 0; kk < kT / 32; ++kk)
+            mma_ts(tmem + C::ACC0, tmem + C::S_COL + 64 * x + kk * 8, bo + ((kk * 16 * C::SW) >> 4), kIdAcc,
+                   (!first || kk > 0) ? 1u : 0u);                   // dV
+#pragma unroll
+        for (int kk = 0; kk < kT / 32; ++kk)
+            mma_ts(tmem + C::ACC1, tmem + C::DP_COL + 64 * x + kk * 8, bq + ((kk * 16 * C::SW) >> 4), kIdAcc,
+                   (!first || kk > 0) ? 1u : 0u);                   // dK
+    };
+    // half slot and its fill phase of half x of the loop tile with sequence number c
+    auto slot = [&](uint32_t c) { return (int)((2 * c + x) & 3); };
+    auto slot_phase = [&](uint32_t c) { return ((2 * c + x) >> 2) & 1; };
     for (int u = blockIdx.x; ok; u += gridDim.x) {
         BUnit U;
-        if (!bwd_unit<MODE>(p, u, U)) break;
+        if (!bwd_unit<kDKDV>(p, u, U)) break;
         if (U.j0 >= U.j1) continue;
-        if (!mbar_wait(smem_u32(&bars->own_full), owned & 1, abort_flag)) break;
-        ++owned;
-        const uint64_t a0 = smem_desc(own, 16, C::SBO, C::SW_CODE);                     // owned tile 0
-        const uint64_t a1 = smem_desc(own + C::TILE_BYTES, 16, C::SBO, C::SW_CODE);     // owned tile 1
-        for (int j = U.j0; j < U.j1; ++j) {
-            const int st = cons & 1;
-            if (!mbar_wait(smem_u32(&bars->st_full[st]), (cons >> 1) & 1, abort_flag)) {
+        const int n = U.j1 - U.j0;
+        for (int k = 0; k <= n; ++k) {
+            // waits first, while the other lane holds the turn
+            bool w = true;
+            if (k == 0) w = mbar_wait(smem_u32(&bars->own_full), owned & 1, abort_flag);
+            if (w && k > 0) w = mbar_wait(smem_u32(&bars->c_full[x]), cc & 1, abort_flag);
+            if (w && k == 1 && x == 0 && units > 0)
+                w = mbar_wait(smem_u32(&bars->acc_empty), (units - 1) & 1, abort_flag);
+            if (w && k < n) w = mbar_wait(smem_u32(&bars->h_full[slot(cons + k)]), slot_phase(cons + k), abort_flag);
+            if (w) w = mbar_wait(my_turn, turns & 1, abort_flag);
+            if (!w) {
                 ok = false;
                 break;
             }
-            ++cons;
-            const uint32_t r0 = smem_u32(smem + C::KRING + st * C::TILE_BYTES);   // Q_i
-            const uint32_t r1 = smem_u32(smem + C::VRING + st * C::TILE_BYTES);   // dO_i
-            const uint64_t b0 = smem_desc(r0, 16, C::SBO, C::SW_CODE);
-            const uint64_t b1 = smem_desc(r1, 16, C::SBO, C::SW_CODE);
-            // S (or S^T) = own0 . ld0^T and dP (or dP^T) = own1 . ld1^T over the head dim
-#pragma unroll
-            for (int kk = 0; kk < C::D / 16; ++kk) {
-                const uint32_t off = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
-                mma_ss(tmem + C::S_COL, a0 + off, b0 + off, kIdS, kk > 0 ? 1u : 0u);
-            }
-#pragma unroll
-            for (int kk = 0; kk < C::D / 16; ++kk) {
-                const uint32_t off = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
-                mma_ss(tmem + C::DP_COL, a1 + off, b1 + off, kIdS, kk > 0 ? 1u : 0u);
-            }
-            if (j == U.j1 - 1) tc_commit(smem_u32(&bars->own_empty));
-            tc_commit(smem_u32(&bars->s_full));
-            if (!mbar_wait(smem_u32(&bars->c_full), cc & 1, abort_flag)) {
-                ok = false;
-                break;
-            }
-            ++cc;
+            ++turns;
             tc_fence_after();
-            // accumulate over the 128 loop rows (16 per MMA): A = 16-bit values in
-            // TMEM (8 columns per step), B = loop tile rows, MN-major
-            const uint32_t acc = j > U.j0 ? 1u : 0u;
-            {
-                const uint64_t bo = smem_desc(r1, C::PANEL_BYTES, C::SBO, C::SW_CODE);   // dO_i
-                const uint64_t bq = smem_desc(r0, C::PANEL_BYTES, C::SBO, C::SW_CODE);   // Q_i
-#pragma unroll
-                for (int kk = 0; kk < kT / 16; ++kk)
-                    mma_ts(tmem + C::ACC0, tmem + C::S_COL + kk * 8, bo + ((kk * 16 * C::SW) >> 4), kIdAcc,
-                           (acc || kk > 0) ? 1u : 0u);                                                    // dV
-#pragma unroll
-                for (int kk = 0; kk < kT / 16; ++kk)
-                    mma_ts(tmem + C::ACC1, tmem + C::DP_COL + kk * 8, bq + ((kk * 16 * C::SW) >> 4), kIdAcc,
-                           (acc || kk > 0) ? 1u : 0u);                                                    // dK
+            if (k > 0) {
+                ++cc;
+                const int hs = slot(cons + k - 1);
+                issue_acc(hs, k == 1 && x == 0);
+                tc_commit(smem_u32(&bars->h_empty[hs]));    // the half slot is read
             }
-            tc_commit(smem_u32(&bars->st_empty[st]));
+            if (k < n) {
+                issue_sdp(slot(cons + k));
+                if (k == n - 1) tc_commit(smem_u32(&bars->own_empty));
+            } else {
+                mbar_arrive(next_turn);
+            }
         }
         if (!ok) break;
+        ++owned;
+        cons += n;
         tc_commit(smem_u32(&bars->acc_full));
+        ++units;
     }
     tc_commit(smem_u32(&bars->drain));
     mbar_wait_drain(smem_u32(&bars->drain), 0);
@@ -721,21 +794,21 @@ __device__ __forceinline__ void bwd_chunk_sel(bool full, const BwdParams &p, con
 }
 
 // Elementwise work and epilogue: warps w and w+4 share TMEM lanes
-// 32*(w%4)..+31 (rows of the owned tile) and take the lower / upper 64
-// columns of every loop tile; in the epilogue, the lower / upper half of the
-// head dimension.  dS needs no exchange across columns, so the halves only
-// meet in the dK/dV kernel, where P^T and dS^T go back over S^T and dP^T: the
-// upper half's stores overwrite columns the lower half reads, so it stores
-// only after the lower half signalled (pair_ld) that its loads are done.
+// 32*(w%4)..+31 (rows of the owned tile).  dQ kernel: they take the lower /
+// upper 64 columns of every loop tile.  dK/dV kernel: warps 0-3 take query
+// half a (columns 0-63) of every loop tile and warps 4-7 half b, each in the
+// half's own TMEM columns, so the two groups never touch each other's data.
+// In the epilogue, the lower / upper half of the head dimension.
 template <class C, bool BF, int MODE>
 __device__ void bwd_compute(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem, int warp, int lane) {
     volatile int *abort_flag = &bars->abort;
     const int half = warp >> 2, wq = warp & 3;
     const int t = wq * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-    const uint32_t pair_bar = smem_u32(&bars->pair_ld[wq]);
     const uint64_t c2x2 = pack_f2(p.c2, p.c2);
-    uint32_t sph = 0, aph = 0, cons = 0, pph = 0;
+    // dK/dV: this group's half of the query tile has barriers of its own
+    const int bi = MODE == kDKDV ? half : 0;
+    uint32_t sph = 0, aph = 0, cons = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok; u += gridDim.x) {
         BUnit U;
@@ -757,32 +830,34 @@ __device__ void bwd_compute(const BwdParams &p, uint8_t *smem, BwdBars *bars, ui
             kv_tile_range(U.row0, kT, p.Sq, p.Sk, p.mask, p.causal_type, kT, &nt, &nu);
         }
         for (int j = U.j0; j < U.j1 && ok; ++j) {
-            const int st = cons & 1;
-            const uint32_t sfp = (cons >> 1) & 1;
+            const int hs = (int)((2 * cons + half) & 3);          // dK/dV: this half's slot
+            const uint32_t hph = ((2 * cons + half) >> 2) & 1;
             ++cons;
-            bool got = warp_wait(smem_u32(&bars->s_full), sph, abort_flag);
+            bool got = warp_wait(smem_u32(&bars->s_full[bi]), sph, abort_flag);
             sph ^= 1;
-            // dK/dV mode reads the stage's row vectors written by the producer warp
-            if (MODE == kDKDV && got) got = warp_wait(smem_u32(&bars->st_full[st]), sfp, abort_flag);
+            // dK/dV mode reads the slot's row vectors written by the producer warp
+            if (MODE == kDKDV && got) got = warp_wait(smem_u32(&bars->h_full[hs]), hph, abort_flag);
             if (!got) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            // every (query, key) pair of the tile pair visible: no per-element
-            // mask (rows / columns outside the problem already give P = 0 or
-            // touch only discarded rows)
+            // every (query, key) pair of the columns this warp handles visible:
+            // no per-element mask (rows / columns outside the problem already
+            // give P = 0 or touch only discarded rows)
             const bool full = MODE == kDQ ? j < nu
-                                          : (p.mask != FMHA_MASK_CAUSAL || j * kT + p.off >= U.row0 + kT - 1);
-            const float *vec = reinterpret_cast<const float *>(smem + C::VEC) + st * 2 * kT;
+                                          : (p.mask != FMHA_MASK_CAUSAL || j * kT + 64 * half + p.off >= U.row0 + kT - 1);
+            // S and dP (S^T and dP^T) of this warp's 64 columns, two chunks of 32
+            const uint32_t sc = lane_base + C::S_COL + 64 * half, dc = lane_base + C::DP_COL + 64 * half;
+            uint32_t s0[32], d0[32], s1[32], d1[32];
+            tmem_ld32(sc, s0);
+            tmem_ld32(dc, d0);
+            tmem_wait_ld2(s0, d0);
+            tmem_ld32(sc + 32, s1);
+            tmem_ld32(dc + 32, d1);
+            tmem_wait_ld2(s1, d1);
+            const int col0 = j * kT + 64 * half;
             if constexpr (MODE == kDQ) {
-                uint32_t s0[32], d0[32], s1[32], d1[32];
-                tmem_ld32(lane_base + C::S_COL + 64 * half, s0);
-                tmem_ld32(lane_base + C::DP_COL + 64 * half, d0);
-                tmem_wait_ld2(s0, d0);
-                tmem_ld32(lane_base + C::S_COL + 64 * half + 32, s1);
-                tmem_ld32(lane_base + C::DP_COL + 64 * half + 32, d1);
-                tmem_wait_ld2(s1, d1);
                 // S and dP may now be overwritten by the next tile's MMAs
                 tc_fence_before();
                 __syncwarp();
@@ -790,66 +865,35 @@ __device__ void bwd_compute(const BwdParams &p, uint8_t *smem, BwdBars *bars, ui
                 const uint32_t ds = lane_base + C::DS_COL + 64 * (j & 1) + 32 * half;
                 {
                     uint32_t pw[16], dw[16];
-                    bwd_chunk_sel<BF, MODE>(full, p, s0, d0, c2x2, nl_row, nd_row, nullptr, nullptr, row, j * kT + 64 * half, pw, dw);
+                    bwd_chunk_sel<BF, MODE>(full, p, s0, d0, c2x2, nl_row, nd_row, nullptr, nullptr, row, col0, pw, dw);
                     tmem_st16(ds, dw);
                 }
                 {
                     uint32_t pw[16], dw[16];
-                    bwd_chunk_sel<BF, MODE>(full, p, s1, d1, c2x2, nl_row, nd_row, nullptr, nullptr, row, j * kT + 64 * half + 32, pw, dw);
+                    bwd_chunk_sel<BF, MODE>(full, p, s1, d1, c2x2, nl_row, nd_row, nullptr, nullptr, row, col0 + 32, pw, dw);
                     tmem_st16(ds + 16, dw);
                 }
-            } else if (half == 0) {
-                // queries 0-63: the upper half will overwrite columns 32-63 of S^T
-                // and dP^T, so read those first and signal; columns 0-31 are
-                // overwritten only by this warp
-                uint32_t s1[32], d1[32], s0[32], d0[32];
-                tmem_ld32(lane_base + C::S_COL + 32, s1);
-                tmem_ld32(lane_base + C::DP_COL + 32, d1);
-                tmem_wait_ld2(s1, d1);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(pair_bar);
-                tmem_ld32(lane_base + C::S_COL, s0);
-                tmem_ld32(lane_base + C::DP_COL, d0);
-                tmem_wait_ld2(s0, d0);
-                {
-                    uint32_t pw[16], dw[16];
-                    bwd_chunk_sel<BF, MODE>(full, p, s0, d0, c2x2, 0, 0, vec, vec + kT, row, j * kT, pw, dw);
-                    tmem_st16(lane_base + C::S_COL, pw);
-                    tmem_st16(lane_base + C::DP_COL, dw);
-                }
-                {
-                    uint32_t pw[16], dw[16];
-                    bwd_chunk_sel<BF, MODE>(full, p, s1, d1, c2x2, 0, 0, vec + 32, vec + kT + 32, row, j * kT + 32, pw, dw);
-                    tmem_st16(lane_base + C::S_COL + 16, pw);
-                    tmem_st16(lane_base + C::DP_COL + 16, dw);
-                }
-                pph ^= 1;
             } else {
-                // queries 64-127: stores land on the lower half's columns 32-63,
-                // so wait until it has read them
-                const bool peer = warp_wait(pair_bar, pph, abort_flag);
-                pph ^= 1;
-                if (!peer) {
-                    ok = false;
-                    break;
+                // P^T and dS^T go back over the first 32 columns of S^T and dP^T
+                // (16-bit pairs); both chunks are already in registers
+                const float *vec = reinterpret_cast<const float *>(smem + C::HVEC + hs * C::HVEC_BYTES);
+                {
+                    uint32_t pw[16], dw[16];
+                    bwd_chunk_sel<BF, MODE>(full, p, s0, d0, c2x2, 0, 0, vec, vec + kT / 2, row, col0, pw, dw);
+                    tmem_st16(sc, pw);
+                    tmem_st16(dc, dw);
                 }
-                tc_fence_after();
-#pragma unroll 1
-                for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t sv[32], dv[32], pw[16], dw[16];
-                    tmem_ld32(lane_base + C::S_COL + 64 + 32 * cc, sv);
-                    tmem_ld32(lane_base + C::DP_COL + 64 + 32 * cc, dv);
-                    tmem_wait_ld2(sv, dv);
-                    bwd_chunk_sel<BF, MODE>(full, p, sv, dv, c2x2, 0, 0, vec + 64 + 32 * cc, vec + kT + 64 + 32 * cc, row, j * kT + 64 + 32 * cc, pw, dw);
-                    tmem_st16(lane_base + C::S_COL + 32 + 16 * cc, pw);
-                    tmem_st16(lane_base + C::DP_COL + 32 + 16 * cc, dw);
+                {
+                    uint32_t pw[16], dw[16];
+                    bwd_chunk_sel<BF, MODE>(full, p, s1, d1, c2x2, 0, 0, vec + 32, vec + kT / 2 + 32, row, col0 + 32, pw, dw);
+                    tmem_st16(sc + 16, pw);
+                    tmem_st16(dc + 16, dw);
                 }
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars->c_full));
+            if (lane == 0) mbar_arrive(smem_u32(&bars->c_full[bi]));
         }
         if (!ok) break;
         // epilogue: this warp's half of the head dimension.  The TMEM loads are
@@ -899,6 +943,12 @@ __device__ void bwd_compute(const BwdParams &p, uint8_t *smem, BwdBars *bars, ui
                     store32<BF>(dkd + c * 64, rk, p.scale);
                 }
             }
+            if (have) {
+                // the accumulators may now be overwritten by the next unit
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty));
+            }
         }
     }
 }
@@ -913,18 +963,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     BwdBars *bars = reinterpret_cast<BwdBars *>(smem + C::BARS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
+        // dK/dV: both issuing lanes commit the owned-tile, stage, accumulator
+        // and drain barriers
+        const uint32_t lanes = MODE == kDKDV ? 2 : 1;
         mbar_init(smem_u32(&bars->own_full), 1);
-        mbar_init(smem_u32(&bars->own_empty), 1);
-        mbar_init(smem_u32(&bars->s_full), 1);
-        mbar_init(smem_u32(&bars->c_full), kCompWarps);
+        mbar_init(smem_u32(&bars->own_empty), lanes);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(smem_u32(&bars->s_full[x]), 1);
+            // dQ: all eight compute warps on index 0; dK/dV: four per half
+            mbar_init(smem_u32(&bars->c_full[x]), MODE == kDQ ? kCompWarps : kCompWarps / 2);
+        }
         mbar_init(smem_u32(&bars->s_read), kCompWarps);
-        for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&bars->pair_ld[w]), 1);
-        mbar_init(smem_u32(&bars->acc_full), 1);
-        mbar_init(smem_u32(&bars->drain), 1);
+        mbar_init(smem_u32(&bars->acc_full), lanes);
+        mbar_init(smem_u32(&bars->drain), lanes);
+        mbar_init(smem_u32(&bars->turn[0]), 1);
+        mbar_init(smem_u32(&bars->turn[1]), 1);
+        mbar_init(smem_u32(&bars->acc_empty), kCompWarps);
         for (int s = 0; s < 3; ++s) {
-            // dK/dV mode: the TMA transaction plus the producer warp's row vectors
-            mbar_init(smem_u32(&bars->st_full[s]), MODE == kDKDV ? 2 : 1);
+            mbar_init(smem_u32(&bars->st_full[s]), 1);
             mbar_init(smem_u32(&bars->st_empty[s]), 1);
+        }
+        for (int s = 0; s < 4; ++s) {
+            // the TMA transaction plus the producer warp's row vectors; freed
+            // by the lane of its half
+            mbar_init(smem_u32(&bars->h_full[s]), 2);
+            mbar_init(smem_u32(&bars->h_empty[s]), 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&bars->v_full[s]), 1);
@@ -932,6 +995,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bars->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_arrive(smem_u32(&bars->turn[0]));          // lane a issues first
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
@@ -947,8 +1011,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         bwd_producer<C, MODE>(p, &tmQ, &tmK, &tmV, &tmO, smem, bars, lane);
     } else {
         if (lane == 0) {
-            if constexpr (MODE == kDQ) bwd_mma_dq<C, BF>(p, smem, bars, tmem);
-            else bwd_mma_dkdv<C, BF>(p, smem, bars, tmem);
+            if constexpr (MODE == kDQ) {
+                if (warp == kMmaWarp) bwd_mma_dq<C, BF>(p, smem, bars, tmem);
+            } else {
+                bwd_mma_dkdv<C, BF>(p, smem, bars, tmem, warp == kMmaWarp ? 0 : 1);
+            }
         }
     }
     tc_fence_before();
@@ -1012,12 +1079,12 @@ int bwd_sm_count() {
 
 // [B, rows, H, D] with a box of one head, 128 rows and one swizzle panel.
 template <class C>
-bool bwd_map(CUtensorMap *m, const void *base, bool bf, int H, int rows, int B) {
+bool bwd_map(CUtensorMap *m, const void *base, bool bf, int H, int rows, int B, int box_rows = kT) {
     auto fn = bwd_encode_fn();
     if (!fn) return false;
     cuuint64_t dims[4] = {(cuuint64_t)C::D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)B};
     cuuint64_t strides[3] = {(cuuint64_t)C::ROW, (cuuint64_t)C::ROW * H, (cuuint64_t)C::ROW * H * (rows > 0 ? rows : 1)};
-    cuuint32_t box[4] = {(cuuint32_t)C::BOX_D, 1, (cuuint32_t)kT, 1};
+    cuuint32_t box[4] = {(cuuint32_t)C::BOX_D, 1, (cuuint32_t)box_rows, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return fn(m, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void *>(base),
               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1053,10 +1120,13 @@ int bwd_launch(const BwdParams &p, bool bf, cudaStream_t stream) {
     auto dot = bf ? fmha_bwd_dot_kernel<D, true> : fmha_bwd_dot_kernel<D, false>;
     dot<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
-    // 2) dQ, 3) dK and dV
+    // 2) dQ, 3) dK and dV; the dK/dV kernel loads Q and dO in halves of 64 rows
     const int r = bwd_launch_mode<BCfg<D, kDQ>, kDQ>(tq, tk, tv, to, p, bf, sms, stream);
     if (r != FMHA_OK) return r;
-    return bwd_launch_mode<BCfg<D, kDKDV>, kDKDV>(tq, tk, tv, to, p, bf, sms, stream);
+    CUtensorMap tq2, to2;
+    if (!bwd_map<C>(&tq2, p.q, bf, p.H, p.Sq, p.B, kT / 2) || !bwd_map<C>(&to2, p.dout, bf, p.H, p.Sq, p.B, kT / 2))
+        return FMHA_ERR_CUDA;
+    return bwd_launch_mode<BCfg<D, kDKDV>, kDKDV>(tq2, tk, tv, to2, p, bf, sms, stream);
 }
 
 }  // namespace

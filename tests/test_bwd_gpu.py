@@ -66,6 +66,10 @@ CASES = [
     ("f16", 1, 2, 130, 400, 128, "causal", "qend"),
     ("bf16", 1, 2, 96, 700, 64, "causal", "qbegin"),     # keys after every query get zero gradient
     ("bf16", 2, 4, 1024, 1024, 128, "causal", "qbegin"),
+    # more work units than SMs: each CTA runs several (b, h, tile) units in
+    # turn, reusing its accumulators, ring slots and barrier phases
+    ("bf16", 2, 16, 2048, 2048, 128, "causal", "qbegin"),
+    ("f16", 1, 20, 1536, 1536, 64, "none", "qbegin"),
 ]
 
 
