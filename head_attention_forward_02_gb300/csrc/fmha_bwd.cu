@@ -208,26 +208,39 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint64_t swz) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (swz << 61);
+// Shared-memory descriptors as two 32-bit words.  The high word (stride
+// byte offset, version, swizzle) is the same for every operand here; the low
+// word holds the start address (16-byte units, 14 bits) and the leading byte
+// offset, and adding (bytes >> 4) to it moves the start address only, since
+// shared memory stays inside the 256 KB the field spans.  Each MMA then costs
+// one 32-bit add for its k-step.
+__host__ __device__ constexpr uint32_t desc_hi(uint32_t sbo, uint32_t swz) {
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (swz << 29);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+
+// D[tmem] (+)= A[smem] * B[smem], descriptors as (low word, shared high word)
+__device__ __forceinline__ void mma_ss_w(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc,
+                                         uint32_t acc) {
     asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        "{\n.reg .pred p;\n.reg .b64 da, db;\nsetp.ne.b32 p, %4, 0;\n"
+        "mov.b64 da, {%1, %3};\nmov.b64 db, {%2, %3};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d),
+        "r"(a_lo), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
         : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// D[tmem] (+)= A[tmem] * B[smem], B's descriptor as (low word, high word)
+__device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a, uint32_t b_lo, uint32_t hi, uint32_t idesc,
+                                         uint32_t acc) {
     asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
-        "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        "{\n.reg .pred p;\n.reg .b64 db;\nsetp.ne.b32 p, %4, 0;\n"
+        "mov.b64 db, {%2, %3};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %5, p;\n}\n" ::"r"(d),
+        "r"(a), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
         : "memory");
 }
 
@@ -545,28 +558,33 @@ __device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uin
     constexpr uint32_t kIdS = bwd_idesc(fmt, kT, false);
     constexpr uint32_t kIdAcc = bwd_idesc(fmt, C::D, true);
     constexpr int KS = C::KSLOTS;
-    const uint32_t own = smem_u32(smem + C::OWN);
-    const uint64_t a0 = smem_desc(own, 16, C::SBO, C::SW_CODE);                     // Q
-    const uint64_t a1 = smem_desc(own + C::TILE_BYTES, 16, C::SBO, C::SW_CODE);     // dO
-    const uint32_t kring = smem_u32(smem + C::KRING), vring = smem_u32(smem + C::VRING);
+    // descriptor words: K-major operands (LBO unused) and K read MN-major
+    // (LBO = panel stride); each MMA adds its k-step's offset to the low word
+    constexpr uint32_t kHi = desc_hi(C::SBO, (uint32_t)C::SW_CODE);
+    constexpr uint32_t kTileStep = C::TILE_BYTES >> 4;
+    const uint32_t a0 = desc_lo(smem_u32(smem + C::OWN), 16);                        // Q
+    const uint32_t a1 = a0 + kTileStep;                                              // dO
+    const uint32_t k_lo = desc_lo(smem_u32(smem + C::KRING), 16);
+    const uint32_t kmn_lo = desc_lo(smem_u32(smem + C::KRING), C::PANEL_BYTES);
+    const uint32_t v_lo = desc_lo(smem_u32(smem + C::VRING), 16);
     uint32_t cons = 0, owned = 0, cc = 0, rc = 0;
     bool ok = true;
     // S = Q K^T and dP = dO V^T of the loop tile with sequence number c
     auto issue_s = [&](uint32_t c) -> bool {
         const int ks = c % KS, vs = c & 1;
         if (!mbar_wait(smem_u32(&bars->st_full[ks]), (c / KS) & 1, abort_flag)) return false;
-        const uint64_t bk = smem_desc(kring + ks * C::TILE_BYTES, 16, C::SBO, C::SW_CODE);
+        const uint32_t bk = k_lo + ks * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < C::D / 16; ++kk) {
             const uint32_t off = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
-            mma_ss(tmem + C::S_COL, a0 + off, bk + off, kIdS, kk > 0 ? 1u : 0u);
+            mma_ss_w(tmem + C::S_COL, a0 + off, bk + off, kHi, kIdS, kk > 0 ? 1u : 0u);
         }
         if (!mbar_wait(smem_u32(&bars->v_full[vs]), (c >> 1) & 1, abort_flag)) return false;
-        const uint64_t bv = smem_desc(vring + vs * C::TILE_BYTES, 16, C::SBO, C::SW_CODE);
+        const uint32_t bv = v_lo + vs * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < C::D / 16; ++kk) {
             const uint32_t off = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
-            mma_ss(tmem + C::DP_COL, a1 + off, bv + off, kIdS, kk > 0 ? 1u : 0u);
+            mma_ss_w(tmem + C::DP_COL, a1 + off, bv + off, kHi, kIdS, kk > 0 ? 1u : 0u);
         }
         tc_commit(smem_u32(&bars->v_empty[vs]));
         return true;
@@ -597,11 +615,11 @@ __device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uin
             // 16 keys), B = K_j rows MN-major
             const int ks = cur % KS;
             const uint32_t ds = tmem + C::DS_COL + 64 * (j & 1);
-            const uint64_t bk = smem_desc(kring + ks * C::TILE_BYTES, C::PANEL_BYTES, C::SBO, C::SW_CODE);
+            const uint32_t bk = kmn_lo + ks * kTileStep;
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
-                mma_ts(tmem + C::ACC0, ds + kk * 8, bk + ((kk * 16 * C::SW) >> 4), kIdAcc,
-                       (j > U.j0 || kk > 0) ? 1u : 0u);
+                mma_ts_w(tmem + C::ACC0, ds + kk * 8, bk + ((kk * 16 * C::SW) >> 4), kHi, kIdAcc,
+                         (j > U.j0 || kk > 0) ? 1u : 0u);
             tc_commit(smem_u32(&bars->st_empty[ks]));
             ++cur;
         }
@@ -640,28 +658,32 @@ __device__ void bwd_mma_dkdv(const BwdParams &p, uint8_t *smem, BwdBars *bars, u
     constexpr uint32_t kIdAcc = bwd_idesc(fmt, C::D, true);
     constexpr int kSteps = C::D / 16;                  // MMAs of one S^T (or dP^T)
     constexpr int kPassAt = 2 * kSteps - 3;            // S/dP MMA (index) after which the turn passes
-    const uint32_t own = smem_u32(smem + C::OWN);
-    const uint64_t a0 = smem_desc(own, 16, C::SBO, C::SW_CODE);                     // K (owned)
-    const uint64_t a1 = smem_desc(own + C::TILE_BYTES, 16, C::SBO, C::SW_CODE);     // V (owned)
+    // descriptor words (see bwd_mma_dq); half slot hs starts hs tiles into the ring
+    constexpr uint32_t kHi = desc_hi(C::SBO, (uint32_t)C::SW_CODE);
+    constexpr uint32_t kTileStep = C::TILE_BYTES >> 4, kHalfStep = C::HALF_BYTES >> 4;
+    const uint32_t a0 = desc_lo(smem_u32(smem + C::OWN), 16);                        // K (owned)
+    const uint32_t a1 = a0 + kTileStep;                                              // V (owned)
+    const uint32_t h_lo = desc_lo(smem_u32(smem + C::HRING), 16);
+    const uint32_t hmn_lo = desc_lo(smem_u32(smem + C::HRING), C::HPANEL);
     const uint32_t my_turn = smem_u32(&bars->turn[x]), next_turn = smem_u32(&bars->turn[x ^ 1]);
     uint32_t cons = 0, owned = 0, cc = 0, units = 0, turns = 0;
     bool ok = true;
     // S^T and dP^T of half x from half slot hs (B = its 64 rows of Q_i, dO_i);
     // passes the turn two MMAs before the end
     auto issue_sdp = [&](int hs) {
-        const uint32_t q = smem_u32(smem + C::HRING + hs * C::TILE_BYTES), o = q + C::HALF_BYTES;
-        const uint64_t bq = smem_desc(q, 16, C::SBO, C::SW_CODE), bo = smem_desc(o, 16, C::SBO, C::SW_CODE);
+        const uint32_t bq = h_lo + hs * kTileStep, bo = bq + kHalfStep;
+        const uint32_t ds = tmem + C::S_COL + 64 * x, dd = tmem + C::DP_COL + 64 * x;
 #pragma unroll
         for (int kk = 0; kk < kSteps; ++kk) {
             const uint32_t oa = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
             const uint32_t ob = ((kk * 32 / C::SW) * C::HPANEL + (kk * 32) % C::SW) >> 4;
-            mma_ss(tmem + C::S_COL + 64 * x, a0 + oa, bq + ob, kIdS, kk > 0 ? 1u : 0u);
+            mma_ss_w(ds, a0 + oa, bq + ob, kHi, kIdS, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < kSteps; ++kk) {
             const uint32_t oa = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
             const uint32_t ob = ((kk * 32 / C::SW) * C::HPANEL + (kk * 32) % C::SW) >> 4;
-            mma_ss(tmem + C::DP_COL + 64 * x, a1 + oa, bo + ob, kIdS, kk > 0 ? 1u : 0u);
+            mma_ss_w(dd, a1 + oa, bo + ob, kHi, kIdS, kk > 0 ? 1u : 0u);
             if (kSteps + kk == kPassAt) mbar_arrive(next_turn);
         }
         tc_commit(smem_u32(&bars->s_full[x]));
@@ -670,16 +692,16 @@ __device__ void bwd_mma_dkdv(const BwdParams &p, uint8_t *smem, BwdBars *bars, u
     // MMA): A = 16-bit values in TMEM (8 columns per step), B = the slot's
     // rows MN-major
     auto issue_acc = [&](int hs, bool first) {
-        const uint32_t q = smem_u32(smem + C::HRING + hs * C::TILE_BYTES), o = q + C::HALF_BYTES;
-        const uint64_t bq = smem_desc(q, C::HPANEL, C::SBO, C::SW_CODE), bo = smem_desc(o, C::HPANEL, C::SBO, C::SW_CODE);
+        const uint32_t bq = hmn_lo + hs * kTileStep, bo = bq + kHalfStep;
+        const uint32_t ps = tmem + C::S_COL + 64 * x, pd = tmem + C::DP_COL + 64 * x;
 #pragma unroll
         for (int kk = 0; kk < kT / 32; ++kk)
-            mma_ts(tmem + C::ACC0, tmem + C::S_COL + 64 * x + kk * 8, bo + ((kk * 16 * C::SW) >> 4), kIdAcc,
-                   (!first || kk > 0) ? 1u : 0u);                   // dV
+            mma_ts_w(tmem + C::ACC0, ps + kk * 8, bo + ((kk * 16 * C::SW) >> 4), kHi, kIdAcc,
+                     (!first || kk > 0) ? 1u : 0u);                 // dV
 #pragma unroll
         for (int kk = 0; kk < kT / 32; ++kk)
-            mma_ts(tmem + C::ACC1, tmem + C::DP_COL + 64 * x + kk * 8, bq + ((kk * 16 * C::SW) >> 4), kIdAcc,
-                   (!first || kk > 0) ? 1u : 0u);                   // dK
+            mma_ts_w(tmem + C::ACC1, pd + kk * 8, bq + ((kk * 16 * C::SW) >> 4), kHi, kIdAcc,
+                     (!first || kk > 0) ? 1u : 0u);                 // dK
     };
     // half slot and its fill phase of half x of the loop tile with sequence number c
     auto slot = [&](uint32_t c) { return (int)((2 * c + x) & 3); };
