@@ -244,6 +244,43 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a, uint32_t b_lo, 
         : "memory");
 }
 
+// Warp-collective forms: the whole (converged) warp executes them with
+// warp-uniform operands and one elected lane issues the instruction, so the
+// operands can stay in uniform registers.
+__device__ __forceinline__ void mma_ss_e(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc,
+                                         uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p, e;\n.reg .b64 da, db;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+        "mov.b64 da, {%1, %3};\nmov.b64 db, {%2, %3};\n"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d),
+        "r"(a_lo), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_e(uint32_t d, uint32_t a, uint32_t b_lo, uint32_t hi, uint32_t idesc,
+                                         uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p, e;\n.reg .b64 db;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+        "mov.b64 db, {%2, %3};\n"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %5, p;\n}\n" ::"r"(d),
+        "r"(a), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_e(uint32_t bar) {
+    asm volatile(
+        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_e(uint32_t bar) {
+    asm volatile(
+        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+        "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n}\n" ::"r"(bar)
+        : "memory");
+}
+
 __host__ __device__ constexpr uint32_t bwd_idesc(uint32_t fmt, int n, bool b_mn) {
     return (1u << 4) | (fmt << 7) | (fmt << 10) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)(kT >> 4) << 24);
@@ -630,8 +667,9 @@ __device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uin
     mbar_wait_drain(smem_u32(&bars->drain), 0);
 }
 
-// MMA issuers of the dK/dV kernel: lane 0 of warp kMmaWarp for query half a,
-// of warp kMmaWarp2 for half b.  The loop tile's 128 queries are taken in two
+// MMA issuers of the dK/dV kernel: warp kMmaWarp for query half a, warp
+// kMmaWarp2 for half b; the whole warp runs the loop with warp-uniform values
+// and one elected lane issues each MMA, commit and arrive.  The loop tile's 128 queries are taken in two
 // halves of 64 with TMEM of their own: S^T and dP^T of half x (M = 128 keys,
 // N = 64 queries) land in columns S_COL + 64x and DP_COL + 64x, four compute
 // warps turn them into P^T and dS^T in place, and dV += P^T dO, dK += dS^T Q
@@ -651,8 +689,9 @@ __device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uin
 // wait.  Lane a's first accumulation of a unit overwrites dV and dK; lane b's
 // comes a turn later.
 template <class C, bool BF>
-__device__ void bwd_mma_dkdv(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem, int x) {
+__device__ void bwd_mma_dkdv(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem_any, int x) {
     volatile int *abort_flag = &bars->abort;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_any, 0);   // the same in every lane
     constexpr uint32_t fmt = BF ? 1u : 0u;
     constexpr uint32_t kIdS = bwd_idesc(fmt, kT / 2, false);
     constexpr uint32_t kIdAcc = bwd_idesc(fmt, C::D, true);
@@ -677,16 +716,16 @@ __device__ void bwd_mma_dkdv(const BwdParams &p, uint8_t *smem, BwdBars *bars, u
         for (int kk = 0; kk < kSteps; ++kk) {
             const uint32_t oa = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
             const uint32_t ob = ((kk * 32 / C::SW) * C::HPANEL + (kk * 32) % C::SW) >> 4;
-            mma_ss_w(ds, a0 + oa, bq + ob, kHi, kIdS, kk > 0 ? 1u : 0u);
+            mma_ss_e(ds, a0 + oa, bq + ob, kHi, kIdS, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < kSteps; ++kk) {
             const uint32_t oa = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
             const uint32_t ob = ((kk * 32 / C::SW) * C::HPANEL + (kk * 32) % C::SW) >> 4;
-            mma_ss_w(dd, a1 + oa, bo + ob, kHi, kIdS, kk > 0 ? 1u : 0u);
-            if (kSteps + kk == kPassAt) mbar_arrive(next_turn);
+            mma_ss_e(dd, a1 + oa, bo + ob, kHi, kIdS, kk > 0 ? 1u : 0u);
+            if (kSteps + kk == kPassAt) mbar_arrive_e(next_turn);
         }
-        tc_commit(smem_u32(&bars->s_full[x]));
+        tc_commit_e(smem_u32(&bars->s_full[x]));
     };
     // dV += P^T_x dO_x and dK += dS^T_x Q_x over the half's 64 queries (16 per
     // MMA): A = 16-bit values in TMEM (8 columns per step), B = the slot's
@@ -696,11 +735,11 @@ __device__ void bwd_mma_dkdv(const BwdParams &p, uint8_t *smem, BwdBars *bars, u
         const uint32_t ps = tmem + C::S_COL + 64 * x, pd = tmem + C::DP_COL + 64 * x;
 #pragma unroll
         for (int kk = 0; kk < kT / 32; ++kk)
-            mma_ts_w(tmem + C::ACC0, ps + kk * 8, bo + ((kk * 16 * C::SW) >> 4), kHi, kIdAcc,
+            mma_ts_e(tmem + C::ACC0, ps + kk * 8, bo + ((kk * 16 * C::SW) >> 4), kHi, kIdAcc,
                      (!first || kk > 0) ? 1u : 0u);                 // dV
 #pragma unroll
         for (int kk = 0; kk < kT / 32; ++kk)
-            mma_ts_w(tmem + C::ACC1, pd + kk * 8, bq + ((kk * 16 * C::SW) >> 4), kHi, kIdAcc,
+            mma_ts_e(tmem + C::ACC1, pd + kk * 8, bq + ((kk * 16 * C::SW) >> 4), kHi, kIdAcc,
                      (!first || kk > 0) ? 1u : 0u);                 // dK
     };
     // half slot and its fill phase of half x of the loop tile with sequence number c
@@ -714,12 +753,12 @@ __device__ void bwd_mma_dkdv(const BwdParams &p, uint8_t *smem, BwdBars *bars, u
         for (int k = 0; k <= n; ++k) {
             // waits first, while the other lane holds the turn
             bool w = true;
-            if (k == 0) w = mbar_wait(smem_u32(&bars->own_full), owned & 1, abort_flag);
-            if (w && k > 0) w = mbar_wait(smem_u32(&bars->c_full[x]), cc & 1, abort_flag);
+            if (k == 0) w = warp_wait(smem_u32(&bars->own_full), owned & 1, abort_flag);
+            if (w && k > 0) w = warp_wait(smem_u32(&bars->c_full[x]), cc & 1, abort_flag);
             if (w && k == 1 && x == 0 && units > 0)
-                w = mbar_wait(smem_u32(&bars->acc_empty), (units - 1) & 1, abort_flag);
-            if (w && k < n) w = mbar_wait(smem_u32(&bars->h_full[slot(cons + k)]), slot_phase(cons + k), abort_flag);
-            if (w) w = mbar_wait(my_turn, turns & 1, abort_flag);
+                w = warp_wait(smem_u32(&bars->acc_empty), (units - 1) & 1, abort_flag);
+            if (w && k < n) w = warp_wait(smem_u32(&bars->h_full[slot(cons + k)]), slot_phase(cons + k), abort_flag);
+            if (w) w = warp_wait(my_turn, turns & 1, abort_flag);
             if (!w) {
                 ok = false;
                 break;
@@ -730,22 +769,22 @@ __device__ void bwd_mma_dkdv(const BwdParams &p, uint8_t *smem, BwdBars *bars, u
                 ++cc;
                 const int hs = slot(cons + k - 1);
                 issue_acc(hs, k == 1 && x == 0);
-                tc_commit(smem_u32(&bars->h_empty[hs]));    // the half slot is read
+                tc_commit_e(smem_u32(&bars->h_empty[hs]));    // the half slot is read
             }
             if (k < n) {
                 issue_sdp(slot(cons + k));
-                if (k == n - 1) tc_commit(smem_u32(&bars->own_empty));
+                if (k == n - 1) tc_commit_e(smem_u32(&bars->own_empty));
             } else {
-                mbar_arrive(next_turn);
+                mbar_arrive_e(next_turn);
             }
         }
         if (!ok) break;
         ++owned;
         cons += n;
-        tc_commit(smem_u32(&bars->acc_full));
+        tc_commit_e(smem_u32(&bars->acc_full));
         ++units;
     }
-    tc_commit(smem_u32(&bars->drain));
+    tc_commit_e(smem_u32(&bars->drain));
     mbar_wait_drain(smem_u32(&bars->drain), 0);
 }
 
@@ -1035,10 +1074,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             if constexpr (MODE == kDQ) {
                 if (warp == kMmaWarp) bwd_mma_dq<C, BF>(p, smem, bars, tmem);
-            } else {
-                bwd_mma_dkdv<C, BF>(p, smem, bars, tmem, warp == kMmaWarp ? 0 : 1);
             }
         }
+        if constexpr (MODE == kDKDV) bwd_mma_dkdv<C, BF>(p, smem, bars, tmem, warp == kMmaWarp ? 0 : 1);
     }
     tc_fence_before();
     __syncthreads();
