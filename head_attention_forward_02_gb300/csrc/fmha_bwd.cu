@@ -582,15 +582,17 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
     }
 }
 
-// MMA issuer of the dQ kernel (one lane).  dS lives apart from S and dP (two
+// MMA issuer of the dQ kernel (warp kMmaWarp, converged; one elected lane
+// issues each MMA, commit and arrive).  dS lives apart from S and dP (two
 // buffers), so S and dP of tile j+1 are issued as soon as the compute warps
 // have read S_j and dP_j (s_read), and dQ += dS_j K_j once dS_j is written
 // (c_full): the elementwise work of tile j overlaps the MMAs of tile j+1.
 // In issue order S_j+2 follows dQ_j, so "S_j+2 complete" implies "dS buffer
 // j % 2 read".  V_j's slot is released after dP_j, K_j's after dQ_j.
 template <class C, bool BF>
-__device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem) {
+__device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem_any) {
     volatile int *abort_flag = &bars->abort;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_any, 0);   // the same in every lane
     constexpr uint32_t fmt = BF ? 1u : 0u;
     constexpr uint32_t kIdS = bwd_idesc(fmt, kT, false);
     constexpr uint32_t kIdAcc = bwd_idesc(fmt, C::D, true);
@@ -609,43 +611,43 @@ __device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uin
     // S = Q K^T and dP = dO V^T of the loop tile with sequence number c
     auto issue_s = [&](uint32_t c) -> bool {
         const int ks = c % KS, vs = c & 1;
-        if (!mbar_wait(smem_u32(&bars->st_full[ks]), (c / KS) & 1, abort_flag)) return false;
+        if (!warp_wait(smem_u32(&bars->st_full[ks]), (c / KS) & 1, abort_flag)) return false;
         const uint32_t bk = k_lo + ks * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < C::D / 16; ++kk) {
             const uint32_t off = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
-            mma_ss_w(tmem + C::S_COL, a0 + off, bk + off, kHi, kIdS, kk > 0 ? 1u : 0u);
+            mma_ss_e(tmem + C::S_COL, a0 + off, bk + off, kHi, kIdS, kk > 0 ? 1u : 0u);
         }
-        if (!mbar_wait(smem_u32(&bars->v_full[vs]), (c >> 1) & 1, abort_flag)) return false;
+        if (!warp_wait(smem_u32(&bars->v_full[vs]), (c >> 1) & 1, abort_flag)) return false;
         const uint32_t bv = v_lo + vs * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < C::D / 16; ++kk) {
             const uint32_t off = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
-            mma_ss_w(tmem + C::DP_COL, a1 + off, bv + off, kHi, kIdS, kk > 0 ? 1u : 0u);
+            mma_ss_e(tmem + C::DP_COL, a1 + off, bv + off, kHi, kIdS, kk > 0 ? 1u : 0u);
         }
-        tc_commit(smem_u32(&bars->v_empty[vs]));
+        tc_commit_e(smem_u32(&bars->v_empty[vs]));
         return true;
     };
     for (int u = blockIdx.x; ok; u += gridDim.x) {
         BUnit U;
         if (!bwd_unit<kDQ>(p, u, U)) break;
         if (U.j0 >= U.j1) continue;
-        if (!mbar_wait(smem_u32(&bars->own_full), owned & 1, abort_flag)) break;
+        if (!warp_wait(smem_u32(&bars->own_full), owned & 1, abort_flag)) break;
         ++owned;
         uint32_t cur = cons;                 // sequence number of tile j
         if (!issue_s(cons++)) break;
-        if (U.j0 + 1 == U.j1) tc_commit(smem_u32(&bars->own_empty));
-        tc_commit(smem_u32(&bars->s_full[0]));
+        if (U.j0 + 1 == U.j1) tc_commit_e(smem_u32(&bars->own_empty));
+        tc_commit_e(smem_u32(&bars->s_full[0]));
         for (int j = U.j0; j < U.j1; ++j) {
-            if (!mbar_wait(smem_u32(&bars->s_read), rc & 1, abort_flag)) { ok = false; break; }
+            if (!warp_wait(smem_u32(&bars->s_read), rc & 1, abort_flag)) { ok = false; break; }
             ++rc;
             if (j + 1 < U.j1) {
                 tc_fence_after();
                 if (!issue_s(cons++)) { ok = false; break; }
-                if (j + 2 == U.j1) tc_commit(smem_u32(&bars->own_empty));
-                tc_commit(smem_u32(&bars->s_full[0]));
+                if (j + 2 == U.j1) tc_commit_e(smem_u32(&bars->own_empty));
+                tc_commit_e(smem_u32(&bars->s_full[0]));
             }
-            if (!mbar_wait(smem_u32(&bars->c_full[0]), cc & 1, abort_flag)) { ok = false; break; }
+            if (!warp_wait(smem_u32(&bars->c_full[0]), cc & 1, abort_flag)) { ok = false; break; }
             ++cc;
             tc_fence_after();
             // dQ += dS_j K_j: A = dS buffer j % 2 (16-bit, 8 columns per step of
@@ -655,15 +657,15 @@ __device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uin
             const uint32_t bk = kmn_lo + ks * kTileStep;
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
-                mma_ts_w(tmem + C::ACC0, ds + kk * 8, bk + ((kk * 16 * C::SW) >> 4), kHi, kIdAcc,
+                mma_ts_e(tmem + C::ACC0, ds + kk * 8, bk + ((kk * 16 * C::SW) >> 4), kHi, kIdAcc,
                          (j > U.j0 || kk > 0) ? 1u : 0u);
-            tc_commit(smem_u32(&bars->st_empty[ks]));
+            tc_commit_e(smem_u32(&bars->st_empty[ks]));
             ++cur;
         }
         if (!ok) break;
-        tc_commit(smem_u32(&bars->acc_full));
+        tc_commit_e(smem_u32(&bars->acc_full));
     }
-    tc_commit(smem_u32(&bars->drain));
+    tc_commit_e(smem_u32(&bars->drain));
     mbar_wait_drain(smem_u32(&bars->drain), 0);
 }
 
@@ -1071,12 +1073,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kProdWarp) {
         bwd_producer<C, MODE>(p, &tmQ, &tmK, &tmV, &tmO, smem, bars, lane);
     } else {
-        if (lane == 0) {
-            if constexpr (MODE == kDQ) {
-                if (warp == kMmaWarp) bwd_mma_dq<C, BF>(p, smem, bars, tmem);
-            }
+        if constexpr (MODE == kDQ) {
+            if (warp == kMmaWarp) bwd_mma_dq<C, BF>(p, smem, bars, tmem);
+        } else {
+            bwd_mma_dkdv<C, BF>(p, smem, bars, tmem, warp == kMmaWarp ? 0 : 1);
         }
-        if constexpr (MODE == kDKDV) bwd_mma_dkdv<C, BF>(p, smem, bars, tmem, warp == kMmaWarp ? 0 : 1);
     }
     tc_fence_before();
     __syncthreads();
