@@ -305,6 +305,69 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a, uint32_t b_lo, 
     }
 }
 
+// Warp-collective forms of the two above: the whole (converged) warp executes
+// them with warp-uniform operands and one elected lane issues the MMA, so the
+// operand words can stay in uniform registers.
+template <bool FP8>
+__device__ __forceinline__ void mma_ss_e(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc,
+                                         uint32_t acc) {
+    if constexpr (FP8) {
+        asm volatile(
+            "{\n.reg .pred p, e;\n.reg .b64 da, db;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+            "mov.b64 da, {%1, %3};\nmov.b64 db, {%2, %3};\n"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n}\n" ::"r"(d),
+            "r"(a_lo), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n.reg .pred p, e;\n.reg .b64 da, db;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+            "mov.b64 da, {%1, %3};\nmov.b64 db, {%2, %3};\n"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d),
+            "r"(a_lo), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
+            : "memory");
+    }
+}
+
+template <bool FP8>
+__device__ __forceinline__ void mma_ts_e(uint32_t d, uint32_t a, uint32_t b_lo, uint32_t hi, uint32_t idesc,
+                                         uint32_t acc) {
+    if constexpr (FP8) {
+        asm volatile(
+            "{\n.reg .pred p, e;\n.reg .b64 db;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+            "mov.b64 db, {%2, %3};\n"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %5, p;\n}\n" ::"r"(d),
+            "r"(a), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n.reg .pred p, e;\n.reg .b64 db;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+            "mov.b64 db, {%2, %3};\n"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %5, p;\n}\n" ::"r"(d),
+            "r"(a), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
+            : "memory");
+    }
+}
+
+__device__ __forceinline__ void tc_commit_e(uint32_t bar) {
+    asm volatile(
+        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_e(uint32_t bar) {
+    asm volatile(
+        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+        "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n}\n" ::"r"(bar)
+        : "memory");
+}
+
+// Bounded wait by a whole warp: true in every lane, or false in every lane.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    const bool r = mbar_wait(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, r);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]
 template <bool FP8>
 __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -703,16 +766,20 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
 // ---------------------------------------------------------------------------
 
 template <class C, bool SPLIT>
-__device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bars, uint32_t tmem, int t) {
-    // Two lanes issue the MMAs, lane t for Q tile t, and take turns so that
+__device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bars, uint32_t tmem_any, int t) {
+    // Two warps issue the MMAs, warp t for Q tile t, and take turns so that
     // the tensor pipe sees the order S0_j0, S1_j0, then per key step
     // PV0_j S0_j+1, PV1_j S1_j+1: each S_t lands right behind its PV_t and the
     // other tile's work fills the pipe while tile t's softmax runs.  A
     // tcgen05.mma holds its issuing thread for most of its 64 pipe cycles, so
-    // one lane alone cannot also do the commits and barrier waits between
-    // groups without starving the shallow tensor queue; with two lanes that
-    // bookkeeping runs while the other lane issues.
+    // one issuer alone cannot also do the commits and barrier waits between
+    // groups without starving the shallow tensor queue; with two issuers
+    // that bookkeeping runs while the other one issues.
+    // The whole warp runs this loop, converged and with warp-uniform values;
+    // one elected lane issues each MMA, commit and arrive, so the operand
+    // words stay in uniform registers.
     volatile int *abort_flag = &bars->abort;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_any, 0);   // the same in every lane
     constexpr uint32_t kIdS = C::idesc(kTile, false);
     constexpr uint32_t kIdPV = C::idesc(C::D, true);
     uint32_t cons = 0, qc = 0, pc = 0, hc = 0, tc = 0;
@@ -733,7 +800,7 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
     const uint32_t p_half = smem_u32(&bars->p_half[t]), p_full = smem_u32(&bars->p_full[t]);
     const uint32_t my_turn = smem_u32(&bars->turn[t]), next_turn = smem_u32(&bars->turn[t ^ 1]);
 
-    auto pass_turn = [&]() { mbar_arrive(next_turn); };
+    auto pass_turn = [&]() { mbar_arrive_e(next_turn); };
     // S_t = Q_t K^T: both operands K-major; each k-step advances 32 bytes
     // within a 128-byte swizzled panel row, then moves to the next panel.
     // The issue turn passes to the other lane within this group (TURN_AT).
@@ -744,7 +811,7 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
         for (int kk = 0; kk < C::QK_STEPS; ++kk) {
             const uint32_t off =
                 ((kk * C::KSTEP_BYTES / C::SW) * C::PANEL_BYTES + (kk * C::KSTEP_BYTES) % C::SW) >> 4;
-            mma_ss_w<C::FP8>(s_tm, q_lo + off, b + off, kHi, kIdS, kk > 0 ? 1u : 0u);
+            mma_ss_e<C::FP8>(s_tm, q_lo + off, b + off, kHi, kIdS, kk > 0 ? 1u : 0u);
             if (kk == C::TURN_AT) pass_turn();
         }
     };
@@ -758,7 +825,7 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
 #pragma unroll
         for (int k = 0; k < H; ++k) {
             const int kk = hf * H + k;
-            mma_ts_w<C::FP8>(o_tm, s_tm + kk * (C::MMA_K * C::E / 4), b + ((kk * C::MMA_K * C::SW) >> 4), kHi,
+            mma_ts_e<C::FP8>(o_tm, s_tm + kk * (C::MMA_K * C::E / 4), b + ((kk * C::MMA_K * C::SW) >> 4), kHi,
                              kIdPV, (acc || kk > 0) ? 1u : 0u);
         }
     };
@@ -767,20 +834,20 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
     // Both lanes consume every ring stage and each releases it once.
     auto next_kv = [&](int &st) -> bool {
         st = cons % C::NSTAGE;
-        const bool r = mbar_wait(smem_u32(&bars->kv_full[st]), (cons / C::NSTAGE) & 1, abort_flag);
+        const bool r = warp_wait(smem_u32(&bars->kv_full[st]), (cons / C::NSTAGE) & 1, abort_flag);
         ++cons;
         return r;
     };
     // P_t was written to TMEM by the softmax threads (tcgen05.st): order this
     // thread's MMAs after their fence::before_thread_sync + arrive.
     auto wait_p = [&](uint32_t bar, uint32_t &cnt) -> bool {
-        const bool r = mbar_wait(bar, cnt & 1, abort_flag);
+        const bool r = warp_wait(bar, cnt & 1, abort_flag);
         ++cnt;
         if (r) tc_fence_after();
         return r;
     };
     auto take_turn = [&]() -> bool {
-        const bool r = mbar_wait(my_turn, tc & 1, abort_flag);
+        const bool r = warp_wait(my_turn, tc & 1, abort_flag);
         ++tc;
         return r;
     };
@@ -791,7 +858,7 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
         const int n = t ? U.n[1] : U.n[0], j0 = U.j0, jn = U.j1;
         if (j0 >= jn) continue;
         if (n > j0) {
-            ok = mbar_wait(smem_u32(&bars->q_full[t]), qc & 1, abort_flag);
+            ok = warp_wait(smem_u32(&bars->q_full[t]), qc & 1, abort_flag);
             ++qc;
         }
         int kst;
@@ -801,10 +868,10 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
         if (n > j0) issue_s(kst);
         else pass_turn();
         if (n > j0) {
-            tc_commit(s_full);
-            if (n == j0 + 1) tc_commit(q_empty);
+            tc_commit_e(s_full);
+            if (n == j0 + 1) tc_commit_e(q_empty);
         }
-        tc_commit(smem_u32(&bars->kv_empty[kst]));
+        tc_commit_e(smem_u32(&bars->kv_empty[kst]));
         for (int j = j0; j < jn; ++j) {
             // paired ring: one stage holds V_j and K_{j+1}; otherwise V_j,
             // then K_{j+1} in the next stage (when a next key tile exists)
@@ -827,29 +894,24 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
             if (!act || !more) pass_turn();
             if (act) {
                 if (!more) {
-                    tc_commit(o_full);
+                    tc_commit_e(o_full);
                 } else {
-                    tc_commit(s_full);
-                    if (j + 2 == n) tc_commit(q_empty);
+                    tc_commit_e(s_full);
+                    if (j + 2 == n) tc_commit_e(q_empty);
                 }
             }
-            tc_commit(smem_u32(&bars->kv_empty[v_st]));
-            if (!C::PAIRED && j + 1 < jn) tc_commit(smem_u32(&bars->kv_empty[k_st]));
+            tc_commit_e(smem_u32(&bars->kv_empty[v_st]));
+            if (!C::PAIRED && j + 1 < jn) tc_commit_e(smem_u32(&bars->kv_empty[k_st]));
         }
     }
     // no tensor-core operation may be in flight when TMEM is released
-    tc_commit(smem_u32(&bars->drain));
+    tc_commit_e(smem_u32(&bars->drain));
     mbar_wait_drain(smem_u32(&bars->drain), 0);
 }
 
 // ---------------------------------------------------------------------------
 // Softmax warpgroups (one thread per query row) and the epilogue
 // ---------------------------------------------------------------------------
-
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
-    const bool r = mbar_wait(bar, parity, abort_flag);
-    return __all_sync(0xffffffffu, r);
-}
 
 // This thread's row of S_t (128 fp32 columns of its TMEM lane).
 __device__ __forceinline__ void load_s(uint32_t s_tm, float (&s)[kTile]) {
@@ -1149,7 +1211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kProducerWarp) {
         if (lane == 0) producer<C, SPLIT>(p, &tmQ, &tmK, &tmV, sQ, sKV, bars);
     } else {
-        if (lane == 0) mma_issuer<C, SPLIT>(p, sQ, sKV, bars, tmem, warp - kMmaWarp);
+        mma_issuer<C, SPLIT>(p, sQ, sKV, bars, tmem, warp - kMmaWarp);
     }
 
     tc_fence_before();
