@@ -203,10 +203,6 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
 
 // Shared-memory descriptors as two 32-bit words.  The high word (stride
 // byte offset, version, swizzle) is the same for every operand here; the low
@@ -735,13 +731,15 @@ __device__ void bwd_mma_dkdv(const BwdParams &p, uint8_t *smem, BwdBars *bars, u
     auto issue_acc = [&](int hs, bool first) {
         const uint32_t bq = hmn_lo + hs * kTileStep, bo = bq + kHalfStep;
         const uint32_t ps = tmem + C::S_COL + 64 * x, pd = tmem + C::DP_COL + 64 * x;
+        // queries 0-31 of the half are packed in columns 0-15, queries 32-63
+        // in columns 32-47 (each compute warp writes over its own columns)
 #pragma unroll
         for (int kk = 0; kk < kT / 32; ++kk)
-            mma_ts_e(tmem + C::ACC0, ps + kk * 8, bo + ((kk * 16 * C::SW) >> 4), kHi, kIdAcc,
+            mma_ts_e(tmem + C::ACC0, ps + (kk >> 1) * 32 + (kk & 1) * 8, bo + ((kk * 16 * C::SW) >> 4), kHi, kIdAcc,
                      (!first || kk > 0) ? 1u : 0u);                 // dV
 #pragma unroll
         for (int kk = 0; kk < kT / 32; ++kk)
-            mma_ts_e(tmem + C::ACC1, pd + kk * 8, bq + ((kk * 16 * C::SW) >> 4), kHi, kIdAcc,
+            mma_ts_e(tmem + C::ACC1, pd + (kk >> 1) * 32 + (kk & 1) * 8, bq + ((kk * 16 * C::SW) >> 4), kHi, kIdAcc,
                      (!first || kk > 0) ? 1u : 0u);                 // dK
     };
     // half slot and its fill phase of half x of the loop tile with sequence number c
@@ -858,10 +856,10 @@ __device__ __forceinline__ void bwd_chunk_sel(bool full, const BwdParams &p, con
 
 // Elementwise work and epilogue: warps w and w+4 share TMEM lanes
 // 32*(w%4)..+31 (rows of the owned tile).  dQ kernel: they take the lower /
-// upper 64 columns of every loop tile.  dK/dV kernel: warps 0-3 take query
-// half a (columns 0-63) of every loop tile and warps 4-7 half b, each in the
-// half's own TMEM columns, so the two groups never touch each other's data.
-// In the epilogue, the lower / upper half of the head dimension.
+// upper 64 columns of every loop tile.  dK/dV kernel: they take the lower /
+// upper 32 columns of each query half, half a then half b, as soon as that
+// half's S^T and dP^T are in TMEM.  In the epilogue, the lower / upper half
+// of the head dimension.
 template <class C, bool BF, int MODE>
 __device__ void bwd_compute(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem, int warp, int lane) {
     volatile int *abort_flag = &bars->abort;
@@ -869,8 +867,6 @@ __device__ void bwd_compute(const BwdParams &p, uint8_t *smem, BwdBars *bars, ui
     const int t = wq * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
     const uint64_t c2x2 = pack_f2(p.c2, p.c2);
-    // dK/dV: this group's half of the query tile has barriers of its own
-    const int bi = MODE == kDKDV ? half : 0;
     uint32_t sph = 0, aph = 0, cons = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok; u += gridDim.x) {
@@ -892,35 +888,29 @@ __device__ void bwd_compute(const BwdParams &p, uint8_t *smem, BwdBars *bars, ui
             int nt;
             kv_tile_range(U.row0, kT, p.Sq, p.Sk, p.mask, p.causal_type, kT, &nt, &nu);
         }
-        for (int j = U.j0; j < U.j1 && ok; ++j) {
-            const int hs = (int)((2 * cons + half) & 3);          // dK/dV: this half's slot
-            const uint32_t hph = ((2 * cons + half) >> 2) & 1;
-            ++cons;
-            bool got = warp_wait(smem_u32(&bars->s_full[bi]), sph, abort_flag);
-            sph ^= 1;
-            // dK/dV mode reads the slot's row vectors written by the producer warp
-            if (MODE == kDKDV && got) got = warp_wait(smem_u32(&bars->h_full[hs]), hph, abort_flag);
-            if (!got) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            // every (query, key) pair of the columns this warp handles visible:
-            // no per-element mask (rows / columns outside the problem already
-            // give P = 0 or touch only discarded rows)
-            const bool full = MODE == kDQ ? j < nu
-                                          : (p.mask != FMHA_MASK_CAUSAL || j * kT + 64 * half + p.off >= U.row0 + kT - 1);
-            // S and dP (S^T and dP^T) of this warp's 64 columns, two chunks of 32
-            const uint32_t sc = lane_base + C::S_COL + 64 * half, dc = lane_base + C::DP_COL + 64 * half;
-            uint32_t s0[32], d0[32], s1[32], d1[32];
-            tmem_ld32(sc, s0);
-            tmem_ld32(dc, d0);
-            tmem_wait_ld2(s0, d0);
-            tmem_ld32(sc + 32, s1);
-            tmem_ld32(dc + 32, d1);
-            tmem_wait_ld2(s1, d1);
-            const int col0 = j * kT + 64 * half;
-            if constexpr (MODE == kDQ) {
+        if constexpr (MODE == kDQ) {
+            for (int j = U.j0; j < U.j1 && ok; ++j) {
+                const bool got = warp_wait(smem_u32(&bars->s_full[0]), sph, abort_flag);
+                sph ^= 1;
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // every (query, key) pair of the tile visible: no per-element
+                // mask (rows and columns outside the problem already give P = 0
+                // or touch only discarded rows)
+                const bool full = j < nu;
+                // S and dP of this warp's 64 columns, two chunks of 32
+                const uint32_t sc = lane_base + C::S_COL + 64 * half, dc = lane_base + C::DP_COL + 64 * half;
+                uint32_t s0[32], d0[32], s1[32], d1[32];
+                tmem_ld32(sc, s0);
+                tmem_ld32(dc, d0);
+                tmem_wait_ld2(s0, d0);
+                tmem_ld32(sc + 32, s1);
+                tmem_ld32(dc + 32, d1);
+                tmem_wait_ld2(s1, d1);
+                const int col0 = j * kT + 64 * half;
                 // S and dP may now be overwritten by the next tile's MMAs
                 tc_fence_before();
                 __syncwarp();
@@ -936,27 +926,50 @@ __device__ void bwd_compute(const BwdParams &p, uint8_t *smem, BwdBars *bars, ui
                     bwd_chunk_sel<BF, MODE>(full, p, s1, d1, c2x2, nl_row, nd_row, nullptr, nullptr, row, col0 + 32, pw, dw);
                     tmem_st16(ds + 16, dw);
                 }
-            } else {
-                // P^T and dS^T go back over the first 32 columns of S^T and dP^T
-                // (16-bit pairs); both chunks are already in registers
-                const float *vec = reinterpret_cast<const float *>(smem + C::HVEC + hs * C::HVEC_BYTES);
-                {
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->c_full[0]));
+            }
+        } else {
+            // every warp takes both query halves of a tile in turn, 32 of the
+            // half's 64 columns each (c32); P^T and dS^T of those 32 queries go
+            // back, as 16-bit pairs, over the first 16 of this warp's own 32
+            // columns of S^T and dP^T, which no other warp reads
+            const int c32 = 32 * half;
+            for (int j = U.j0; j < U.j1 && ok; ++j) {
+#pragma unroll 1
+                for (int x = 0; x < 2; ++x) {
+                    const int hs = (int)((2 * cons + x) & 3);          // the half's slot
+                    const uint32_t hph = ((2 * cons + x) >> 2) & 1;
+                    bool got = warp_wait(smem_u32(&bars->s_full[x]), (sph >> x) & 1, abort_flag);
+                    sph ^= 1u << x;
+                    // the slot's row vectors, written by the producer warp
+                    if (got) got = warp_wait(smem_u32(&bars->h_full[hs]), hph, abort_flag);
+                    if (!got) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int col0 = j * kT + 64 * x + c32;
+                    const bool full = p.mask != FMHA_MASK_CAUSAL || col0 + p.off >= U.row0 + kT - 1;
+                    const uint32_t sc = lane_base + C::S_COL + 64 * x + c32, dc = lane_base + C::DP_COL + 64 * x + c32;
+                    uint32_t s0[32], d0[32];
+                    tmem_ld32(sc, s0);
+                    tmem_ld32(dc, d0);
+                    tmem_wait_ld2(s0, d0);
+                    const float *vec = reinterpret_cast<const float *>(smem + C::HVEC + hs * C::HVEC_BYTES) + c32;
                     uint32_t pw[16], dw[16];
                     bwd_chunk_sel<BF, MODE>(full, p, s0, d0, c2x2, 0, 0, vec, vec + kT / 2, row, col0, pw, dw);
                     tmem_st16(sc, pw);
                     tmem_st16(dc, dw);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&bars->c_full[x]));
                 }
-                {
-                    uint32_t pw[16], dw[16];
-                    bwd_chunk_sel<BF, MODE>(full, p, s1, d1, c2x2, 0, 0, vec + 32, vec + kT / 2 + 32, row, col0 + 32, pw, dw);
-                    tmem_st16(sc + 16, pw);
-                    tmem_st16(dc + 16, dw);
-                }
+                ++cons;
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars->c_full[bi]));
         }
         if (!ok) break;
         // epilogue: this warp's half of the head dimension.  The TMEM loads are
@@ -1033,8 +1046,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&bars->own_empty), lanes);
         for (int x = 0; x < 2; ++x) {
             mbar_init(smem_u32(&bars->s_full[x]), 1);
-            // dQ: all eight compute warps on index 0; dK/dV: four per half
-            mbar_init(smem_u32(&bars->c_full[x]), MODE == kDQ ? kCompWarps : kCompWarps / 2);
+            // every compute warp arrives (dQ uses index 0 only)
+            mbar_init(smem_u32(&bars->c_full[x]), kCompWarps);
         }
         mbar_init(smem_u32(&bars->s_read), kCompWarps);
         mbar_init(smem_u32(&bars->acc_full), lanes);
