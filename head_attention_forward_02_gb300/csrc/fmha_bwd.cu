@@ -96,7 +96,10 @@ struct BCfg {
 struct BwdParams {
     const void *q, *k, *v, *o, *dout;   // q, o, dout [B, Sq, H, D]; k, v [B, Sk, H, D]
     const float *lse;                   // [B, H, Sq] natural-log LSE of the forward
-    float *dvec;                        // [B, H, Sq] D_i = dO_i . O_i (workspace)
+    // workspace: per (b, h) row, sq_pad = Sq rounded up to 128 entries of
+    // -LSE_i * log2(e) and -D_i (D_i = dO_i . O_i); -inf and 0 past Sq
+    float *nl, *nd;
+    int sq_pad;
     void *dq, *dk, *dv;
     int B, H, Sq, Sk;
     float scale, c2;                    // c2 = scale * log2(e)
@@ -194,6 +197,14 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
         : "memory");
+}
+
+// Untiled bulk copy global -> shared (both 16-byte aligned, bytes a multiple
+// of 16), completing on an mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
@@ -436,8 +447,8 @@ __device__ __forceinline__ bool bwd_unit(const BwdParams &p, int u, BUnit &U) {
 
 // Producer: the owned pair of tiles, then the loop tiles: K_j and V_j into
 // their own rings for dQ; for dK/dV each query half (64 rows of Q_i and of
-// dO_i) into a half slot, where the warp also writes the half's 64 values of
-// -LSE * log2(e) and -D.
+// dO_i, and the rows' -LSE * log2(e) and -D) into a half slot.  Every load
+// is an asynchronous copy, so no thread of this warp waits on memory.
 template <class C, int MODE>
 __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const CUtensorMap *tmK,
                              const CUtensorMap *tmV, const CUtensorMap *tmO, uint8_t *smem, BwdBars *bars,
@@ -510,8 +521,8 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
             }
         } else {
             // half x of loop tile j: 64 rows of Q and dO (64-row boxes) and the
-            // rows' vectors
-            const int64_t base = ((int64_t)U.b * p.H + U.h) * p.Sq;
+            // rows' two vectors (bulk copies from the padded workspace rows)
+            const int64_t vrow = ((int64_t)U.b * p.H + U.h) * p.sq_pad;
             for (int j = U.j0; j < U.j1 && ok; ++j) {
 #pragma unroll 1
                 for (int x = 0; x < 2; ++x) {
@@ -523,25 +534,18 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
                     }
                     const uint32_t hb = smem_u32(&bars->h_full[hs]);
                     const uint32_t dst = smem_u32(smem + C::HRING + hs * C::TILE_BYTES);
+                    const uint32_t vdst = smem_u32(smem + C::HVEC + hs * C::HVEC_BYTES);
                     const int r0 = j * kT + x * (kT / 2);
                     if (lane == 0) {
-                        mbar_expect_tx(hb, C::TILE_BYTES);
+                        mbar_expect_tx(hb, C::TILE_BYTES + C::HVEC_BYTES);
 #pragma unroll
                         for (int pn = 0; pn < C::PANELS; ++pn) {
                             tma_load_4d(dst + pn * C::HPANEL, ld0, hb, pn * C::BOX_D, U.h, r0, U.b);
                             tma_load_4d(dst + C::HALF_BYTES + pn * C::HPANEL, ld1, hb, pn * C::BOX_D, U.h, r0, U.b);
                         }
+                        bulk_load(vdst, p.nl + vrow + r0, C::HVEC_BYTES / 2, hb);
+                        bulk_load(vdst + C::HVEC_BYTES / 2, p.nd + vrow + r0, C::HVEC_BYTES / 2, hb);
                     }
-                    float *vec = reinterpret_cast<float *>(smem + C::HVEC + hs * C::HVEC_BYTES);
-#pragma unroll
-                    for (int i = 0; i < kT / 64; ++i) {
-                        const int q = r0 + i * 32 + lane;
-                        const bool in = q < p.Sq;
-                        vec[i * 32 + lane] = in ? -p.lse[base + q] * kLog2e : -INFINITY;    // -LSE * log2(e)
-                        vec[kT / 2 + i * 32 + lane] = in ? -p.dvec[base + q] : 0.f;         // -D
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(hb);
                     ++hfill;
                 }
             }
@@ -877,14 +881,11 @@ __device__ void bwd_compute(const BwdParams &p, uint8_t *smem, BwdBars *bars, ui
         uint64_t nl_row = 0, nd_row = 0;
         int nu = 0;                                   // dQ: leading key tiles visible to every row
         if (MODE == kDQ) {
-            float l2 = INFINITY, di = 0.f;            // a row past Sq: P = 0
-            if (row < p.Sq) {
-                const int64_t li = ((int64_t)U.b * p.H + U.h) * p.Sq + row;
-                l2 = p.lse[li] * kLog2e;
-                di = p.dvec[li];
-            }
-            nl_row = pack_f2(-l2, -l2);
-            nd_row = pack_f2(-di, -di);
+            // a row past Sq reads the padding (-inf, 0): P = 0
+            const int64_t li = ((int64_t)U.b * p.H + U.h) * p.sq_pad + row;
+            const float nl = p.nl[li], nd = p.nd[li];
+            nl_row = pack_f2(nl, nl);
+            nd_row = pack_f2(nd, nd);
             int nt;
             kv_tile_range(U.row0, kT, p.Sq, p.Sk, p.mask, p.causal_type, kT, &nt, &nu);
         }
@@ -1060,9 +1061,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bars->st_empty[s]), 1);
         }
         for (int s = 0; s < 4; ++s) {
-            // the TMA transaction plus the producer warp's row vectors; freed
-            // by the lane of its half
-            mbar_init(smem_u32(&bars->h_full[s]), 2);
+            // the copies' transaction count; freed by the issuing warp of its half
+            mbar_init(smem_u32(&bars->h_full[s]), 1);
             mbar_init(smem_u32(&bars->h_empty[s]), 1);
         }
         for (int s = 0; s < 2; ++s) {
@@ -1101,23 +1101,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// D_i = dO_i . O_i in fp32, one warp per (b, i, h) row.
+// D_i = dO_i . O_i in fp32, one warp per (b, i, h) row with i < sq_pad; the
+// row's workspace entries -LSE_i * log2(e) and -D_i (padding: -inf and 0).
 template <int D, bool BF>
 __global__ void fmha_bwd_dot_kernel(const BwdParams p) {
     const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    const int64_t rows = (int64_t)p.B * p.Sq * p.H;
+    const int64_t rows = (int64_t)p.B * p.sq_pad * p.H;
     if (row >= rows) return;
-    const uint16_t *o = static_cast<const uint16_t *>(p.o) + row * D;
-    const uint16_t *g = static_cast<const uint16_t *>(p.dout) + row * D;
+    const int64_t h = row % p.H, bi = row / p.H, i = bi % p.sq_pad, b = bi / p.sq_pad;
+    const int64_t w = (b * p.H + h) * p.sq_pad + i;
+    if (i >= p.Sq) {
+        if (lane == 0) {
+            p.nl[w] = -INFINITY;
+            p.nd[w] = 0.f;
+        }
+        return;
+    }
+    const int64_t src = (b * p.Sq + i) * p.H + h;
+    const uint16_t *o = static_cast<const uint16_t *>(p.o) + src * D;
+    const uint16_t *g = static_cast<const uint16_t *>(p.dout) + src * D;
     float acc = 0.f;
 #pragma unroll
     for (int d = lane; d < D; d += 32) acc += to_f32<BF>(o[d]) * to_f32<BF>(g[d]);
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
     if (lane == 0) {
-        const int64_t h = row % p.H, bi = row / p.H, i = bi % p.Sq, b = bi / p.Sq;
-        p.dvec[(b * p.H + h) * p.Sq + i] = acc;
+        p.nl[w] = -p.lse[(b * p.H + h) * p.Sq + i] * kLog2e;
+        p.nd[w] = -acc;
     }
 }
 
@@ -1190,7 +1201,7 @@ int bwd_launch(const BwdParams &p, bool bf, cudaStream_t stream) {
     const int sms = bwd_sm_count();
     if (sms <= 0) return FMHA_ERR_CUDA;
     // 1) D_i = dO_i . O_i
-    const int64_t rows = (int64_t)p.B * p.Sq * p.H;
+    const int64_t rows = (int64_t)p.B * p.sq_pad * p.H;
     auto dot = bf ? fmha_bwd_dot_kernel<D, true> : fmha_bwd_dot_kernel<D, false>;
     dot<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
@@ -1219,9 +1230,11 @@ int bwd_read_status(int reset) {
 
 using namespace fmha;
 
+// Two fp32 vectors per (b, h) row of Sq rounded up to 128 entries.
 extern "C" size_t fmha_bwd_workspace_size(int B, int H, int Sq) {
     if (B <= 0 || H <= 0 || Sq <= 0) return 0;
-    return ((size_t)B * H * Sq * sizeof(float) + 255) / 256 * 256;
+    const size_t sq_pad = ((size_t)Sq + kT - 1) / kT * kT;
+    return 2 * (size_t)B * H * sq_pad * sizeof(float);
 }
 
 extern "C" int fmha_bwd(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor o, fmha_tensor dout,
@@ -1272,7 +1285,9 @@ extern "C" int fmha_bwd(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor
     p.o = o.data;
     p.dout = dout.data;
     p.lse = lse;
-    p.dvec = static_cast<float *>(workspace);
+    p.sq_pad = (Sq + kT - 1) / kT * kT;
+    p.nl = static_cast<float *>(workspace);
+    p.nd = p.nl + (size_t)B * H * p.sq_pad;
     p.dq = dq.data;
     p.dk = dk.data;
     p.dv = dv.data;

@@ -278,7 +278,8 @@ size_t fmha_gen_workspace_size(int B, int H, int H_k, int D, int S_max);
  * q-end), as fmha_fwd.  Fixed length only.  Tensors 16-byte aligned, lse
  * 4-byte aligned.
  * workspace: caller-owned, fmha_bwd_workspace_size(B, H, Sq) bytes, 256-byte
- * aligned (the fp32 row sums); no initialisation needed; not shared with a
+ * aligned (two fp32 values per query row, -LSE*log2(e) and -dO.O, each row
+ * padded to a multiple of 128); no initialisation needed; not shared with a
  * concurrent call.  Asynchronous on `stream` (three kernels); allocates
  * nothing.  Returns FMHA_OK, FMHA_ERR_INVALID_ARG (sizes, scale, mask,
  * pointers, workspace), FMHA_ERR_UNSUPPORTED (dtype, alignment) or

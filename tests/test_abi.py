@@ -210,6 +210,8 @@ def test_bwd_validation_rejects_before_any_launch(fm, kw, code):
 
 
 def test_bwd_workspace_size(fm):
-    assert fm.fmha_bwd_workspace_size(2, 4, 100) == (2 * 4 * 100 * 4 + 255) // 256 * 256
+    # two fp32 vectors per (b, h), each padded to a multiple of 128 rows
+    assert fm.fmha_bwd_workspace_size(2, 4, 100) == 2 * 2 * 4 * 128 * 4
+    assert fm.fmha_bwd_workspace_size(1, 3, 300) == 2 * 1 * 3 * 384 * 4
     assert fm.fmha_bwd_workspace_size(0, 4, 100) == 0
     assert call_bwd(fm, B=0) == 0
