@@ -283,6 +283,50 @@ def make_device_set(inp, dev):
     return s
 
 
+def e2e_pipelined(dev, steps, sets, h_in, h_out, launch):
+    """Milliseconds per step of `steps` end-to-end steps.  Step i copies the
+    pinned host inputs `h_in` (name -> tensor) into device set i % len(sets),
+    runs `launch(set, stream)` and copies the set's outputs into the pinned
+    host tensors h_out[i % len(sets)] (name -> tensor).  Host-to-device copies,
+    kernels and device-to-host copies run on three streams, so the copies of
+    one step overlap the kernels of its neighbours, as a serving loop would
+    run them; a set is refilled only after its previous step's kernel read
+    its inputs and its outputs were copied out.  Every step still moves all
+    of its own input and output bytes."""
+    s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ran = [None] * len(sets)
+    out_done = [None] * len(sets)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(s_in)
+    s_run.wait_event(start)
+    s_out.wait_event(start)
+    for i in range(steps):
+        j = i % len(sets)
+        d = sets[j]
+        if ran[j] is not None:
+            s_in.wait_event(ran[j])
+        with torch.cuda.stream(s_in):
+            for k, t in h_in.items():
+                d[k].copy_(t, non_blocking=True)
+        copied = torch.cuda.Event()
+        copied.record(s_in)
+        s_run.wait_event(copied)
+        if out_done[j] is not None:
+            s_run.wait_event(out_done[j])
+        launch(d, s_run)
+        ran[j] = torch.cuda.Event()
+        ran[j].record(s_run)
+        s_out.wait_event(ran[j])
+        with torch.cuda.stream(s_out):
+            for k, t in h_out[j].items():
+                t.copy_(d[k], non_blocking=True)
+        out_done[j] = torch.cuda.Event()
+        out_done[j].record(s_out)
+    end.record(s_out)          # after the last D2H, which follows every earlier step
+    torch.cuda.synchronize(dev)
+    return start.elapsed_time(end) / steps
+
+
 def call(fm, inp, s, kernel, stream):
     w = inp.w
     f = fm.fmha_fwd if kernel == "tc" else fm.fmha_fwd_simt
@@ -403,33 +447,22 @@ def run_ours(args, rank, world, local):
     step_ms = launch_ms if n_sets == 1 else ms_per_step
     value = world * flops / (step_ms * 1e-3) / 1e12
 
-    # end to end through the public API: pinned host inputs in, O and LSE out
+    # end to end through the public API: every step copies its inputs in from
+    # pinned host memory and its O and LSE out, pipelined over two device sets
     e2e_steps = args.e2e_steps or max(3, min(K, 20))
     h = {"q": inputs[0].q.pin_memory(), "k": inputs[0].k.pin_memory(), "v": inputs[0].v.pin_memory()}
-    ho = torch.empty(sets[0]["o"].shape, dtype=sets[0]["o"].dtype).pin_memory()
-    hl = torch.empty(sets[0]["lse"].shape, dtype=torch.float32).pin_memory()
-    s = sets[0]
+    e2e_sets = sets if len(sets) >= 2 else sets + [make_device_set(inputs[0], dev)]
+    h_out = [{"o": torch.empty(d["o"].shape, dtype=d["o"].dtype).pin_memory(),
+              "lse": torch.empty(d["lse"].shape, dtype=torch.float32).pin_memory()} for d in e2e_sets[:2]]
 
-    def e2e_step():
-        for key in ("q", "k", "v"):
-            s[key].copy_(h[key], non_blocking=True)
-        call(fm, inputs[0], s, args.kernel, stream)
-        ho.copy_(s["o"], non_blocking=True)
-        hl.copy_(s["lse"], non_blocking=True)
+    def launch(d, st):
+        call(fm, inputs[0], d, args.kernel, st)
 
-    e2e_step()
-    torch.cuda.synchronize(dev)
+    e2e_pipelined(dev, 2, e2e_sets[:2], h, h_out, launch)          # warm-up
     barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    e2e_ms = max_over_ranks(e2e_pipelined(dev, e2e_steps, e2e_sets[:2], h, h_out, launch), world)
     h2d = sum(t.numel() * t.element_size() for t in h.values())
-    d2h = ho.numel() * ho.element_size() + hl.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
 
     if rank != 0:
         return
@@ -763,32 +796,27 @@ def run_bwd(args, rank, world, local):
         raise RuntimeError("device status reports an error")
     ms = max_over_ranks(ev0.elapsed_time(ev1) / K, world)
     value = world * flops / (ms * 1e-3) / 1e12
-    # end to end: q, k, v, O, dO and LSE in from pinned memory, dQ, dK, dV out
+    # end to end: every step copies q, k, v, O, dO and LSE in from pinned
+    # memory and dQ, dK, dV out, pipelined over two device sets
     pin = {n: t.pin_memory() for n, t in host.items()}
-    o_h, lse_h = o.cpu().pin_memory(), lse.cpu().pin_memory()
-    outs = [torch.empty_like(t).pin_memory() for t in (host["q"],) * 3]
+    pin["o"], pin["lse"] = o.cpu().pin_memory(), lse.cpu().pin_memory()
+    e2e_sets = [{n: torch.empty_like(t, device=dev) for n, t in pin.items()} for _ in range(2)]
+    for es in e2e_sets:
+        es.update({"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["q"]), "dv": torch.empty_like(d["q"]),
+                   "ws": torch.empty_like(ws)})
+    outs = [{n: torch.empty(tuple(host["q"].shape), dtype=torch.bfloat16).pin_memory() for n in ("dq", "dk", "dv")}
+            for _ in range(2)]
 
-    def e2e_step():
-        for n, t in pin.items():
-            d[n].copy_(t, non_blocking=True)
-        o.copy_(o_h, non_blocking=True)
-        lse.copy_(lse_h, non_blocking=True)
-        step()
-        for hst, dv_ in zip(outs, grads):
-            hst.copy_(dv_, non_blocking=True)
+    def launch(es, st):
+        fm.bwd(es["q"], es["k"], es["v"], es["o"], es["do"], es["lse"], mask=mask, dq=es["dq"], dk=es["dk"],
+               dv=es["dv"], workspace=es["ws"], stream=st)
 
-    e2e_steps = args.e2e_steps or 5
-    e2e_step()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
-    h2d = sum(t.numel() * t.element_size() for t in pin.values()) + o_h.numel() * 2 + lse_h.numel() * 4
-    d2h = sum(t.numel() * t.element_size() for t in outs)
+    e2e_steps = args.e2e_steps or 6
+    e2e_pipelined(dev, 2, e2e_sets, pin, outs, launch)          # warm-up
+    barrier(world)
+    e2e_ms = max_over_ranks(e2e_pipelined(dev, e2e_steps, e2e_sets, pin, outs, launch), world)
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs[0].values())
     if rank != 0:
         return
     peaks, peak_src = measured_peaks()
