@@ -699,6 +699,7 @@ __device__ void bwd_mma_dkdv(const BwdParams &p, uint8_t *smem, BwdBars *bars, u
     constexpr uint32_t kIdAcc = bwd_idesc(fmt, C::D, true);
     constexpr int kSteps = C::D / 16;                  // MMAs of one S^T (or dP^T)
     constexpr int kPassAt = 2 * kSteps - 3;            // S/dP MMA (index) after which the turn passes
+    static_assert(kPassAt >= 0 && kPassAt < 2 * kSteps, "the turn passes exactly once per S/dP group");
     // descriptor words (see bwd_mma_dq); half slot hs starts hs tiles into the ring
     constexpr uint32_t kHi = desc_hi(C::SBO, (uint32_t)C::SW_CODE);
     constexpr uint32_t kTileStep = C::TILE_BYTES >> 4, kHalfStep = C::HALF_BYTES >> 4;
@@ -719,6 +720,7 @@ __device__ void bwd_mma_dkdv(const BwdParams &p, uint8_t *smem, BwdBars *bars, u
             const uint32_t oa = ((kk * 32 / C::SW) * C::PANEL_BYTES + (kk * 32) % C::SW) >> 4;
             const uint32_t ob = ((kk * 32 / C::SW) * C::HPANEL + (kk * 32) % C::SW) >> 4;
             mma_ss_e(ds, a0 + oa, bq + ob, kHi, kIdS, kk > 0 ? 1u : 0u);
+            if (kk == kPassAt) mbar_arrive_e(next_turn);
         }
 #pragma unroll
         for (int kk = 0; kk < kSteps; ++kk) {
