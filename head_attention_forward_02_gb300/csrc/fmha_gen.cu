@@ -211,6 +211,29 @@ __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint3
         : "memory");
 }
 
+// Warp-collective forms: the whole (converged) warp executes them with
+// warp-uniform operands and one elected lane issues the instruction.
+__device__ __forceinline__ void mma_ss_e(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_e(uint32_t bar) {
+    asm volatile(
+        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
+        : "memory");
+}
+
+// Bounded wait by a whole warp: true in every lane, or false in every lane.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    const bool r = mbar_wait(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, r);
+}
+
 // Instruction descriptor: fp32 accumulator, A/B format (0 = f16, 1 = bf16),
 // A and B major-ness (0 = K-major, 1 = MN-major), N, M = 128.
 __host__ __device__ constexpr uint32_t gen_idesc(uint32_t fmt, bool a_mn, bool b_mn) {
@@ -504,8 +527,11 @@ __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUten
 // order, so "S^T of tile j+1 complete" implies "PV of tile j complete": the
 // softmax may then rewrite P^T and rescale O^T without another barrier.
 template <bool BF>
-__device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, GenBars *bars, uint32_t tmem) {
+__device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, GenBars *bars, uint32_t tmem_any) {
+    // the whole warp runs this loop converged, with warp-uniform values; one
+    // elected lane issues each MMA and commit
     volatile int *abort_flag = &bars->abort;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_any, 0);   // the same in every lane
     constexpr uint32_t kIdS = gen_idesc(BF ? 1u : 0u, false, false);
     constexpr uint32_t kIdPV = gen_idesc(BF ? 1u : 0u, true, true);
     const uint32_t s_tm = tmem, o_tm = tmem + kNP;
@@ -518,13 +544,13 @@ __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, G
         GenItem it;
         if (!gen_next(p, sc, cur, it, false)) break;
         const int qs = qn % kQSlots;
-        if (!mbar_wait(smem_u32(&bars->q_full[qs]), (qn / kQSlots) & 1, abort_flag)) break;
+        if (!warp_wait(smem_u32(&bars->q_full[qs]), (qn / kQSlots) & 1, abort_flag)) break;
         ++qn;
         const uint64_t q_desc = q_desc0 + ((qs * kQBytes) >> 4);
         bool first = true;
         for (int k = it.k0; k < it.k1; k += kKT) {
             const int st = cons % kNS;
-            if (!mbar_wait(smem_u32(&bars->kv_full[st]), (cons / kNS) & 1, abort_flag)) {
+            if (!warp_wait(smem_u32(&bars->kv_full[st]), (cons / kNS) & 1, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -537,11 +563,11 @@ __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, G
             for (int kk = 0; kk < kD / 16; ++kk) {
                 const uint32_t koff = (kk * 32 / 128) * kPanelBytes + (kk * 32) % 128;
                 const uint32_t qoff = (kk * 32 / 128) * kQPanelBytes + (kk * 32) % 128;
-                mma_ss(s_tm, k_desc + (koff >> 4), q_desc + (qoff >> 4), kIdS, kk > 0 ? 1u : 0u);
+                mma_ss_e(s_tm, k_desc + (koff >> 4), q_desc + (qoff >> 4), kIdS, kk > 0 ? 1u : 0u);
             }
-            if (k + kKT >= it.k1) tc_commit(smem_u32(&bars->q_empty[qs]));
-            tc_commit(smem_u32(&bars->s_full));
-            if (!mbar_wait(smem_u32(&bars->p_full), pn & 1, abort_flag)) {
+            if (k + kKT >= it.k1) tc_commit_e(smem_u32(&bars->q_empty[qs]));
+            tc_commit_e(smem_u32(&bars->s_full));
+            if (!warp_wait(smem_u32(&bars->p_full), pn & 1, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -553,16 +579,16 @@ __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, G
             const uint64_t v_desc = smem_desc(kaddr + kTileBytes, kPanelBytes, 1024, 2);
 #pragma unroll
             for (int kk = 0; kk < kKT / 16; ++kk)
-                mma_ss(o_tm, v_desc + ((kk * 16 * 128) >> 4), p_desc + ((kk * 16 * 64) >> 4), kIdPV,
+                mma_ss_e(o_tm, v_desc + ((kk * 16 * 128) >> 4), p_desc + ((kk * 16 * 64) >> 4), kIdPV,
                        (!first || kk > 0) ? 1u : 0u);
-            tc_commit(smem_u32(&bars->kv_empty[st]));
+            tc_commit_e(smem_u32(&bars->kv_empty[st]));
             first = false;
         }
         if (!ok) break;
-        tc_commit(smem_u32(&bars->o_full));
+        tc_commit_e(smem_u32(&bars->o_full));
     }
     // no tensor-core operation may be in flight when TMEM is released
-    tc_commit(smem_u32(&bars->drain));
+    tc_commit_e(smem_u32(&bars->drain));
     mbar_wait_drain(smem_u32(&bars->drain), 0);
 }
 
@@ -754,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kProdWarp) {
         if (lane == 0) gen_producer(p, sc, &tmQ, &tmK, &tmV, smem, bars);
     } else {
-        if (lane == 0) gen_mma<BF>(p, sc, smem, bars, tmem);
+        gen_mma<BF>(p, sc, smem, bars, tmem);
     }
     tc_fence_before();
     __syncthreads();
