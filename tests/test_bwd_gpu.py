@@ -88,3 +88,30 @@ def test_bwd_empty_sides_give_zero(fm):
     fm.bwd(q, k, k, q, q, lse, dk=dk, dv=dv, workspace=torch.empty(256, dtype=torch.uint8, device="cuda"))
     torch.cuda.synchronize()
     assert bool((dk == 0).all()) and bool((dv == 0).all())
+
+
+@pytest.mark.parametrize("b,h", [(0, 0), (1, 15)])
+def test_bwd_full_size_sampled_heads(fm, b, h):
+    """The benchmark's backward workload at full size (causal B=2 H=16 S=8192
+    D=128 bf16, the launch bench.py times); heads are independent, so the
+    oracle checks every gradient element of sampled (batch, head) pairs."""
+    B, H, S, D = 2, 16, 8192, 128
+    g = torch.Generator().manual_seed(1234)
+    q, k, v, do = (torch.randn(B, S, H, D, generator=g).to(torch.bfloat16) for _ in range(4))
+    dev = "cuda"
+    qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    o, lse = fm.fwd(qd, kd, vd, mask="causal")
+    dq, dk, dv = fm.bwd(qd, kd, vd, o, dod, lse, mask="causal")
+    torch.cuda.synchronize()
+    assert fm.device_status(reset=True) == 0
+    dec = lambda t: oracle.decode(oracle.BF16, t[b:b + 1, :, h:h + 1].contiguous().view(torch.uint16).numpy())
+    ref = oracle.attn_bwd_f64(dec(q), dec(k), dec(v), dec(do), D ** -0.5, oracle.MASK_CAUSAL, oracle.QBEGIN)
+    for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        got = got[b:b + 1, :, h:h + 1].float().cpu().numpy().astype(np.float64)
+        assert not np.isnan(got).any(), f"NaN in {name}"
+        scale = np.abs(want).max()
+        bound = 1e-2 * scale + half_ulp("bf16", want)
+        err = np.abs(got - want)
+        assert (err <= bound).all(), (f"{name}: worst {err.max():.4g} (scale {scale:.3g}) at "
+                                      f"{np.unravel_index(err.argmax(), err.shape)}")
+        assert err.mean() <= 2e-3 * max(scale, 1e-6), (name, err.mean(), scale)

@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import oracle
+from head_attention_forward_02_gb300 import workloads as wl
 from tests.gpu_util import TOL_LSE, TOL_O, half_ulp
 
 pytestmark = pytest.mark.gpu
@@ -158,3 +159,23 @@ def test_gen_length_outside_the_cache_is_reported(fm):
     assert status == fm.ERR_INVALID_ARG
     assert torch.equal(kc[0].view(torch.uint16), c_ok["kc"][0].view(torch.uint16))   # entry 0 untouched
     assert fm.device_status() == 0                                                      # reset by run()
+
+
+@pytest.mark.parametrize("name", list(wl.GEN_CONFIGS))
+def test_gen_full_size_configs(fm, name):
+    """The benchmark's generation workloads at full size, through the same call
+    the benchmark times: every output row against the oracle (which reads the
+    caches as they were before the call) and the rows the call inserted."""
+    w = wl.GEN_CONFIGS[name]
+    inp = wl.generate_gen(w)
+    dev = torch.device("cuda")
+    kc, vc = inp.k_cache.to(dev), inp.v_cache.to(dev)
+    o, lse = fm.gen_fwd(inp.q.to(dev), kc, vc, inp.seqlen.to(dev),
+                        k_new=None if inp.k_new is None else inp.k_new.to(dev),
+                        v_new=None if inp.v_new is None else inp.v_new.to(dev))
+    torch.cuda.synchronize()
+    assert fm.device_status(reset=True) == 0
+    c = dict(q=inp.q, kc=inp.k_cache, vc=inp.v_cache, kn=inp.k_new, vn=inp.v_new, seqlen=inp.seqlen, bidx=None,
+             B=w.B, H=w.H, H_k=w.H_k, B_cache=w.B, S_max=w.S_max, dtype=w.dtype)
+    check(c, o.cpu(), lse.cpu())
+    check_cache(c, kc.cpu(), vc.cpu())
