@@ -49,9 +49,7 @@ def parse():
     ap.add_argument("--op", default="fwd", choices=["fwd", "gen", "bwd"],
                     help="fwd: the fused forward (fmha_fwd); gen: generation phase against a "
                          "K/V cache (fmha_gen_fwd); bwd: the backward pass (fmha_bwd)")
-    ap.add_argument("--bwd-config", default="bwd_bf16_causal_b2_h16_s8192_d128",
-                    choices=["bwd_bf16_causal_b2_h16_s8192_d128", "bwd_bf16_nomask_b2_h16_s8192_d128",
-                             "bwd_bf16_causal_b4_h16_s2048_d128"])
+    ap.add_argument("--bwd-config", default="bwd_bf16_causal_b2_h16_s8192_d128", choices=list(BWD_SHAPES))
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(wl.CONFIGS))
     ap.add_argument("--gen-config", default=DEFAULT_GEN_CONFIG, choices=list(wl.GEN_CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -740,6 +738,7 @@ BWD_SHAPES = {   # name -> (B, H, S, D, mask); synthetic N(0,1) q, k, v, dO
     "bwd_bf16_causal_b2_h16_s8192_d128": (2, 16, 8192, 128, "causal"),
     "bwd_bf16_nomask_b2_h16_s8192_d128": (2, 16, 8192, 128, "none"),
     "bwd_bf16_causal_b4_h16_s2048_d128": (4, 16, 2048, 128, "causal"),
+    "bwd_bf16_causal_b2_h16_s4096_d128": (2, 16, 4096, 128, "causal"),   # profiling size (7 x 32 MB)
 }
 
 
