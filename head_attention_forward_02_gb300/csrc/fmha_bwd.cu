@@ -91,6 +91,8 @@ struct BCfg {
     static constexpr int S_COL = 0, DP_COL = 128, ACC0 = 256, ACC1 = 256 + D;
     static constexpr int DS_COL = 384;                     // dQ kernel: dS of tile j at DS_COL + 64 * (j % 2)
     static_assert(ACC1 + D <= (int)kTmemCols, "TMEM budget");
+    static_assert(DS_COL + 128 <= (int)kTmemCols, "dQ kernel: two 64-column dS buffers");
+    static_assert(2 * HALF_BYTES == TILE_BYTES && 2 * HPANEL == PANEL_BYTES, "half slots split a tile in two");
 };
 
 struct BwdParams {
@@ -229,31 +231,12 @@ __device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
     return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
 
-// D[tmem] (+)= A[smem] * B[smem], descriptors as (low word, shared high word)
-__device__ __forceinline__ void mma_ss_w(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc,
-                                         uint32_t acc) {
-    asm volatile(
-        "{\n.reg .pred p;\n.reg .b64 da, db;\nsetp.ne.b32 p, %4, 0;\n"
-        "mov.b64 da, {%1, %3};\nmov.b64 db, {%2, %3};\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d),
-        "r"(a_lo), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
-        : "memory");
-}
 
-// D[tmem] (+)= A[tmem] * B[smem], B's descriptor as (low word, high word)
-__device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a, uint32_t b_lo, uint32_t hi, uint32_t idesc,
-                                         uint32_t acc) {
-    asm volatile(
-        "{\n.reg .pred p;\n.reg .b64 db;\nsetp.ne.b32 p, %4, 0;\n"
-        "mov.b64 db, {%2, %3};\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %5, p;\n}\n" ::"r"(d),
-        "r"(a), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
-        : "memory");
-}
 
-// Warp-collective forms: the whole (converged) warp executes them with
-// warp-uniform operands and one elected lane issues the instruction, so the
-// operands can stay in uniform registers.
+// MMA (D[tmem] (+)= A * B, A from shared memory or TMEM, B from shared memory),
+// commit and arrive in warp-collective form: the whole (converged) warp
+// executes them with warp-uniform operands and one elected lane issues the
+// instruction, so the operand words can stay in uniform registers.
 __device__ __forceinline__ void mma_ss_e(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc,
                                          uint32_t acc) {
     asm volatile(

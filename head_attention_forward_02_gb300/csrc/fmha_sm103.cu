@@ -50,6 +50,7 @@ constexpr int kUnitRows = 2 * kTile;       // query rows per work unit
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;                // issues Q tile 0's MMAs; owns the TMEM allocation
 constexpr int kMmaWarp1 = 10;              // issues Q tile 1's MMAs
+static_assert(kMmaWarp1 == kMmaWarp + 1, "issuing warp t is kMmaWarp + t");
 constexpr int kThreads = 352;              // softmax warps 0-7, producer warp 8, MMA warps 9-10
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;
@@ -237,24 +238,12 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Arrive on an mbarrier once every tcgen05 operation issued so far by this
-// thread has completed.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// Shared-memory matrix descriptor: start address, leading / stride byte
-// offsets (16-byte units), descriptor version 1, swizzle mode.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint64_t swz) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (swz << 61);
-}
-
-// The same descriptor split in two 32-bit words.  The low word holds the
-// start address (16-byte units, 14 bits) and the leading byte offset; adding
-// (bytes >> 4) to it moves the start address without touching anything else
-// as long as the address stays in the 256 KB window, which shared memory does.
+// Shared-memory matrix descriptor (start address, leading / stride byte
+// offsets in 16-byte units, descriptor version 1, swizzle mode) as two 32-bit
+// words.  The low word holds the start address (14 bits) and the leading
+// byte offset; adding (bytes >> 4) to it moves the start address without
+// touching anything else as long as the address stays in the 256 KB window,
+// which shared memory does.
 __host__ __device__ constexpr uint32_t desc_hi(uint32_t sbo, uint32_t swz) {
     return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (swz << 29);
 }
@@ -263,51 +252,12 @@ __device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
     return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
 
-// D[tmem] (+)= A[smem] * B[smem], descriptors given as (low word, shared high word)
-template <bool FP8>
-__device__ __forceinline__ void mma_ss_w(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc,
-                                         uint32_t acc) {
-    if constexpr (FP8) {
-        asm volatile(
-            "{\n.reg .pred p;\n.reg .b64 da, db;\nsetp.ne.b32 p, %4, 0;\n"
-            "mov.b64 da, {%1, %3};\nmov.b64 db, {%2, %3};\n"
-            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n}\n" ::"r"(d),
-            "r"(a_lo), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n.reg .pred p;\n.reg .b64 da, db;\nsetp.ne.b32 p, %4, 0;\n"
-            "mov.b64 da, {%1, %3};\nmov.b64 db, {%2, %3};\n"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d),
-            "r"(a_lo), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
-            : "memory");
-    }
-}
 
-// D[tmem] (+)= A[tmem] * B[smem], B's descriptor given as (low word, high word)
-template <bool FP8>
-__device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a, uint32_t b_lo, uint32_t hi, uint32_t idesc,
-                                         uint32_t acc) {
-    if constexpr (FP8) {
-        asm volatile(
-            "{\n.reg .pred p;\n.reg .b64 db;\nsetp.ne.b32 p, %4, 0;\n"
-            "mov.b64 db, {%2, %3};\n"
-            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %5, p;\n}\n" ::"r"(d),
-            "r"(a), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n.reg .pred p;\n.reg .b64 db;\nsetp.ne.b32 p, %4, 0;\n"
-            "mov.b64 db, {%2, %3};\n"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %5, p;\n}\n" ::"r"(d),
-            "r"(a), "r"(b_lo), "r"(hi), "r"(acc), "r"(idesc)
-            : "memory");
-    }
-}
 
-// Warp-collective forms of the two above: the whole (converged) warp executes
-// them with warp-uniform operands and one elected lane issues the MMA, so the
-// operand words can stay in uniform registers.
+// MMA (D[tmem] (+)= A * B, A from shared memory or TMEM, B from shared memory),
+// commit and arrive in warp-collective form: the whole (converged) warp
+// executes them with warp-uniform operands and one elected lane issues the
+// instruction, so the operand words can stay in uniform registers.
 template <bool FP8>
 __device__ __forceinline__ void mma_ss_e(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc,
                                          uint32_t acc) {
@@ -368,41 +318,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, r);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]
-template <bool FP8>
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    if constexpr (FP8) {
-        asm volatile(
-            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-            "l"(a), "l"(b), "r"(idesc), "r"(acc)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-            "l"(a), "l"(b), "r"(idesc), "r"(acc)
-            : "memory");
-    }
-}
 
-// D[tmem] (+)= A[tmem] * B[smem]
-template <bool FP8>
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    if constexpr (FP8) {
-        asm volatile(
-            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
-            "r"(a), "l"(b), "r"(idesc), "r"(acc)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
-            "r"(a), "l"(b), "r"(idesc), "r"(acc)
-            : "memory");
-    }
-}
 
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -459,20 +375,7 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
                  : "memory");
 }
 
-// Load 16 consecutive TMEM columns of this thread's lane (32x32b shape).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-                 : "r"(taddr));
-}
 
-// Wait for this thread's TMEM loads, tying the 16 loaded registers to the wait.
-__device__ __forceinline__ void tmem_wait_ld16(uint32_t *r) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
-                 :
-                 : "memory");
-}
 
 // Store 16 consecutive TMEM columns of this thread's lane (32x32b shape).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
