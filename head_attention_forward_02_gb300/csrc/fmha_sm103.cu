@@ -375,6 +375,15 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
                  : "memory");
 }
 
+// The same wait, also taking a value computed before it as an operand, so that
+// the computation stays ahead of the wait and overlaps the loads in flight.
+__device__ __forceinline__ void tmem_wait_ld_after(uint32_t (&r)[32], float &v) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]), "+f"(v)
+                 :
+                 : "memory");
+}
+
 
 
 // Store 16 consecutive TMEM columns of this thread's lane (32x32b shape).
@@ -855,6 +864,45 @@ __device__ __forceinline__ float row_max(const float (&s)[kTile]) {
     return max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
 }
 
+// This thread's row of S_t and its maximum, for a tile with no masked element:
+// the maximum of the first 64 columns is taken while the last 64 load.
+__device__ __forceinline__ float load_s_max(uint32_t s_tm, float (&s)[kTile]) {
+    uint32_t r0[32], r1[32], r2[32], r3[32];
+    tmem_ld32(s_tm, r0);
+    tmem_ld32(s_tm + 32, r1);
+    tmem_wait_ld(r0);
+    tmem_wait_ld(r1);
+    tmem_ld32(s_tm + 64, r2);
+    tmem_ld32(s_tm + 96, r3);
+    float m8[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        m8[k] = max3(__uint_as_float(r0[k]), __uint_as_float(r0[8 + k]), __uint_as_float(r0[16 + k]));
+        m8[k] = max3(m8[k], __uint_as_float(r0[24 + k]), __uint_as_float(r1[k]));
+        m8[k] = max3(m8[k], __uint_as_float(r1[8 + k]), __uint_as_float(r1[16 + k]));
+        m8[k] = fmaxf(m8[k], __uint_as_float(r1[24 + k]));
+    }
+    float m_lo = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+    tmem_wait_ld_after(r2, m_lo);
+    tmem_wait_ld(r3);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        m8[k] = max3(__uint_as_float(r2[k]), __uint_as_float(r2[8 + k]), __uint_as_float(r2[16 + k]));
+        m8[k] = max3(m8[k], __uint_as_float(r2[24 + k]), __uint_as_float(r3[k]));
+        m8[k] = max3(m8[k], __uint_as_float(r3[8 + k]), __uint_as_float(r3[16 + k]));
+        m8[k] = fmaxf(m8[k], __uint_as_float(r3[24 + k]));
+    }
+    const float m_hi = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        s[i] = __uint_as_float(r0[i]);
+        s[32 + i] = __uint_as_float(r1[i]);
+        s[64 + i] = __uint_as_float(r2[i]);
+        s[96 + i] = __uint_as_float(r3[i]);
+    }
+    return fmaxf(m_lo, m_hi);
+}
+
 // exp2 of 64 scores (one half row) into packed P words: 32 words for 16-bit
 // types, 16 for e4m3.  Returns the fp32 sum.
 template <class C>
@@ -993,9 +1041,15 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
             s_ph ^= 1;
             tc_fence_after();
             float s[kTile];
-            load_s(s_tm, s);
-            if (j >= nu) mask_s(s, key_end - j * kTile);     // boundary tile
-            const float m_tile = row_max(s) * c;             // scale > 0 keeps the argmax
+            float m_raw;
+            if (j >= nu) {                                   // boundary tile
+                load_s(s_tm, s);
+                mask_s(s, key_end - j * kTile);
+                m_raw = row_max(s);
+            } else {
+                m_raw = load_s_max(s_tm, s);
+            }
+            const float m_tile = m_raw * c;                  // scale > 0 keeps the argmax
             const bool resc = m_tile > m_ref + kRescaleLog2;
             float alpha = 1.f;
             if (resc) {
