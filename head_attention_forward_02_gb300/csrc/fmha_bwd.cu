@@ -18,12 +18,13 @@
 // S and dP for their tiles, so that every output tile has one owner and no
 // atomics are needed.  The dQ kernel owns a 128-row Q tile and loops over key
 // tiles: S = Q K^T and dP = dO V^T (both A and B K-major from shared memory)
-// land in TMEM; four warps (one query row per thread) form dS and write it
-// back over S as 16-bit values; dQ += dS K is a TMEM-A MMA with K read
-// MN-major.  The dK/dV kernel owns a 128-key tile and loops over query tiles:
-// S^T = K Q^T and dP^T = V dO^T; one key per thread; P^T and dS^T go back over
-// S^T and dP^T; dV += P^T dO and dK += dS^T Q.  Each kernel writes its output
-// in the input type directly (no fp32 dQ round trip).
+// land in TMEM; eight warps (one query row per thread, two warps per row
+// quadrant) form dS into a separate TMEM buffer as 16-bit values; dQ += dS K
+// is a TMEM-A MMA with K read MN-major.  The dK/dV kernel owns a 128-key tile
+// and loops over query tiles in halves of 64: S^T = K Q^T and dP^T = V dO^T;
+// one key per thread; P^T and dS^T go back over S^T and dP^T; dV += P^T dO and
+// dK += dS^T Q.  Each kernel writes its output in the input type directly (no
+// fp32 dQ round trip).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -41,9 +42,9 @@ namespace {
 
 constexpr int kT = 128;                 // rows per tile, both sides
 constexpr int kCompWarps = 8;           // warps 0-7: elementwise work and epilogue
-constexpr int kProdWarp = 8;            // TMA producer (all lanes: the dK/dV kernel's row vectors)
-constexpr int kMmaWarp = 9;             // tcgen05.mma issuer (lane 0), owns TMEM
-constexpr int kMmaWarp2 = 10;           // dK/dV kernel: issuer (lane 0) of query half b
+constexpr int kProdWarp = 8;            // TMA producer (the warp waits together, lane 0 issues the copies)
+constexpr int kMmaWarp = 9;             // tcgen05.mma issuer (whole warp, one elected lane), owns TMEM
+constexpr int kMmaWarp2 = 10;           // dK/dV kernel: issuer of query half b
 constexpr int kThreads = 352;
 static_assert(kThreads == 32 * (kMmaWarp2 + 1), "one warp per role");
 constexpr uint32_t kTmemCols = 512;
@@ -654,25 +655,25 @@ __device__ void bwd_mma_dq(const BwdParams &p, uint8_t *smem, BwdBars *bars, uin
 
 // MMA issuers of the dK/dV kernel: warp kMmaWarp for query half a, warp
 // kMmaWarp2 for half b; the whole warp runs the loop with warp-uniform values
-// and one elected lane issues each MMA, commit and arrive.  The loop tile's 128 queries are taken in two
-// halves of 64 with TMEM of their own: S^T and dP^T of half x (M = 128 keys,
-// N = 64 queries) land in columns S_COL + 64x and DP_COL + 64x, four compute
-// warps turn them into P^T and dS^T in place, and dV += P^T dO, dK += dS^T Q
-// then take the half's 64 queries as the reduction.  While one half is in the
-// compute warps the MMAs of the other run, so the tensor pipe and the
-// elementwise work overlap.
+// and one elected lane issues each MMA, commit and arrive.  The loop tile's
+// 128 queries are taken in two halves of 64 with TMEM of their own: S^T and
+// dP^T of half x (M = 128 keys, N = 64 queries) land in columns S_COL + 64x
+// and DP_COL + 64x, the compute warps turn them into P^T and dS^T in place,
+// and dV += P^T dO, dK += dS^T Q then take the half's 64 queries as the
+// reduction.  While one half is in the compute warps the MMAs of the other
+// run, so the tensor pipe and the elementwise work overlap.
 //
-// The lanes take turns; turn k of lane x issues acc(x, i-1) and S/dP(x, i)
-// for loop tile i = j0 + k (the first turn of a unit has no accumulation,
-// the last no S/dP), so the pipe sees a, b, a, b, ... and "S^T of half x of
-// tile i complete" implies "the accumulation from half x of tile i-1
-// complete", which is what lets S^T overwrite P^T.  A lane does its waits
-// (c_full, the stage, the previous unit's epilogue) before taking its turn,
-// while the other lane issues, and hands the turn over two MMAs before its
-// last one, so the pipe never drains between turns: an MMA holds its issuing
-// thread for most of its pipe time, and one lane alone cannot both issue and
-// wait.  Lane a's first accumulation of a unit overwrites dV and dK; lane b's
-// comes a turn later.
+// The two warps take turns; turn k of warp x issues acc(x, i-1) and
+// S/dP(x, i) for loop tile i = j0 + k (the first turn of a unit has no
+// accumulation, the last no S/dP), so the pipe sees a, b, a, b, ... and "S^T
+// of half x of tile i complete" implies "the accumulation from half x of tile
+// i-1 complete", which is what lets S^T overwrite P^T.  A warp does its waits
+// (c_full, the half slot, the previous unit's epilogue) before taking its
+// turn, while the other warp issues, and hands the turn over two MMAs before
+// its last one, so the pipe never drains between turns: an MMA holds its
+// issuing thread for most of its pipe time, and one issuer alone cannot both
+// issue and wait.  Warp a's first accumulation of a unit overwrites dV and dK;
+// warp b's comes a turn later.
 template <class C, bool BF>
 __device__ void bwd_mma_dkdv(const BwdParams &p, uint8_t *smem, BwdBars *bars, uint32_t tmem_any, int x) {
     volatile int *abort_flag = &bars->abort;
@@ -792,7 +793,7 @@ __device__ __forceinline__ void store32(uint8_t *dst, const uint32_t (&r)[32], f
 // P = exp2(S * scale * log2e - LSE * log2e) (zero where masked) and
 // dS = P (dP - D), from the chunk's S and dP values; packed to 16-bit pairs.
 // nl / nd are -LSE*log2e and -D: per row in the dQ kernel, per column (read
-// from the stage's vectors, four at a time) in the dK/dV kernel.  FULL: every
+// from the half slot's vectors, four at a time) in the dK/dV kernel.  FULL: every
 // pair of the tile is visible, no per-element test.
 template <bool BF, int MODE, bool FULL>
 __device__ __forceinline__ void bwd_chunk(const BwdParams &p, const uint32_t (&s)[32], const uint32_t (&dp)[32],
@@ -1025,19 +1026,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     BwdBars *bars = reinterpret_cast<BwdBars *>(smem + C::BARS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        // dK/dV: both issuing lanes commit the owned-tile, stage, accumulator
-        // and drain barriers
-        const uint32_t lanes = MODE == kDKDV ? 2 : 1;
+        // dK/dV: both issuing warps commit the owned-tile, accumulator and
+        // drain barriers
+        const uint32_t issuers = MODE == kDKDV ? 2 : 1;
         mbar_init(smem_u32(&bars->own_full), 1);
-        mbar_init(smem_u32(&bars->own_empty), lanes);
+        mbar_init(smem_u32(&bars->own_empty), issuers);
         for (int x = 0; x < 2; ++x) {
             mbar_init(smem_u32(&bars->s_full[x]), 1);
             // every compute warp arrives (dQ uses index 0 only)
             mbar_init(smem_u32(&bars->c_full[x]), kCompWarps);
         }
         mbar_init(smem_u32(&bars->s_read), kCompWarps);
-        mbar_init(smem_u32(&bars->acc_full), lanes);
-        mbar_init(smem_u32(&bars->drain), lanes);
+        mbar_init(smem_u32(&bars->acc_full), issuers);
+        mbar_init(smem_u32(&bars->drain), issuers);
         mbar_init(smem_u32(&bars->turn[0]), 1);
         mbar_init(smem_u32(&bars->turn[1]), 1);
         mbar_init(smem_u32(&bars->acc_empty), kCompWarps);
