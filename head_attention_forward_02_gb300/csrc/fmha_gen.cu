@@ -44,7 +44,7 @@ constexpr int kNP = 32;                 // query heads of a group, padded (MMA N
 constexpr int kNS = 3;                  // K/V ring stages, a K and a V tile each
 constexpr int kSoftWarps = 4;           // warps 0-3: softmax and epilogue
 constexpr int kProdWarp = 4;            // TMA producer (lane 0), cache insert
-constexpr int kMmaWarp = 5;             // tcgen05.mma issuer (lane 0), owns TMEM
+constexpr int kMmaWarp = 5;             // tcgen05.mma issuer (whole warp, one elected lane), owns TMEM
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 64;      // S^T in [0, 32), O^T in [32, 64)
 constexpr int kPanelBytes = kKT * 128;  // 128 rows of one 128-byte swizzled panel
@@ -510,8 +510,8 @@ __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUten
     }
 }
 
-// MMA issuer (one lane): per tile, S^T = K Q^T, then (after the softmax wrote
-// P^T) O^T += V^T P^T.  The single issuing thread keeps the tensor pipe in
+// MMA issuer (one warp, one elected lane): per tile, S^T = K Q^T, then (after
+// the softmax wrote P^T) O^T += V^T P^T.  The single issuer keeps the tensor pipe in
 // order, so "S^T of tile j+1 complete" implies "PV of tile j complete": the
 // softmax may then rewrite P^T and rescale O^T without another barrier.
 template <bool BF>

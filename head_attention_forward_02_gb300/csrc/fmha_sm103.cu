@@ -13,16 +13,18 @@
 //  * persistent CTAs, one per SM; a work unit is (batch, query head, 256
 //    query rows) = two 128-row Q tiles; units are taken heaviest first;
 //  * warp 8 (one lane) loads Q tiles and a ring of K/V tiles by TMA;
-//  * warp 9 (one lane) issues tcgen05.mma: S_t = Q_t K^T into TMEM (fp32),
-//    then O_t += P_t V with P_t read from TMEM (aliasing S_t) and V from
-//    shared memory (MN-major); it owns the TMEM allocation;
+//  * warps 9 and 10 issue the tcgen05.mma of Q tile 0 / 1 (each runs its
+//    loop as a whole warp and issues through one elected lane): S_t = Q_t K^T
+//    into TMEM (fp32), then O_t += P_t V with P_t read from TMEM (aliasing
+//    S_t) and V from shared memory (MN-major); warp 9 owns the TMEM
+//    allocation, and the two warps take turns so the pipe sees the order below;
 //  * warps 0-3 / 4-7 run the softmax of Q tile 0 / 1, one thread per query
 //    row (TMEM lane), and the epilogue of their tile;
 //  * the MMA order S0_j, S1_j, PV0_j, S0_{j+1}, PV1_j, S1_{j+1}, ... gives
 //    each softmax warpgroup the time of two GEMMs to produce P, and makes
 //    "S_t_j complete" imply "PV_t_{j-1} complete", so the softmax warps may
 //    rescale O_t in TMEM before publishing P_t_j without another barrier.
-//    (Two issuing lanes, one per tile, were measured slower: the tensor pipe
+//    (Two issuers without the turns were measured slower: the tensor pipe
 //    then interleaves the tiles and S_t completes later.)
 //
 // Every wait is bounded: after kTimeoutNs the waiting thread records
@@ -81,13 +83,13 @@ struct Cfg {
     static constexpr int PV_STEPS = kTile / MMA_K;
     static constexpr int NS = TILE_BYTES <= 8192 ? 8 : (TILE_BYTES <= 16384 ? 6 : 4);
     // 16-bit inputs pair the ring: stage i holds V_{j-1} and K_j behind one
-    // barrier, so the issuing lane waits and releases once per key step
+    // barrier, so an issuing warp waits and releases once per key step
     // (measured +2% at D=128); e4m3 keeps one tile per stage, where V_j is
     // not held back by K_{j+1} (pairing measured -3% there).
     static constexpr bool PAIRED = !FP8;
     static constexpr int NSTAGE = PAIRED ? NS / 2 : NS;   // ring stages (barrier pairs)
-    // The MMA lane hands the issue turn to the other lane this many MMAs
-    // before the end of an S group, hiding the other lane's wake-up behind
+    // An issuing warp hands the turn to the other one this many MMAs before
+    // the end of an S group, hiding the other warp's wake-up behind
     // MMAs still to issue (16-bit: +6% at D=128).  The e4m3 key step is
     // softmax-bound, and there letting the other tile's MMAs in ahead of the
     // last S MMAs costs more than the hand-off (measured -2% to -5%).
@@ -115,7 +117,7 @@ struct Cfg {
 
 struct Bars {
     uint64_t q_full[2], q_empty[2], s_full[2], p_half[2], p_full[2], o_full[2], drain;
-    uint64_t turn[2];          // issue turn of the MMA lane of Q tile t
+    uint64_t turn[2];          // issue turn of the issuing warp of Q tile t
     uint64_t kv_full[8], kv_empty[8];
     uint32_t tmem_base;
     int abort;
@@ -674,7 +676,7 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer (one lane)
+// MMA issuers (warps 9 and 10, one elected lane each)
 // ---------------------------------------------------------------------------
 
 template <class C, bool SPLIT>
@@ -1143,12 +1145,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bars->p_full[t]), 4);
             mbar_init(smem_u32(&bars->o_full[t]), 1);
         }
-        mbar_init(smem_u32(&bars->drain), 2);             // one commit per MMA lane
+        mbar_init(smem_u32(&bars->drain), 2);             // one commit per issuing warp
         mbar_init(smem_u32(&bars->turn[0]), 1);
         mbar_init(smem_u32(&bars->turn[1]), 1);
         for (int s = 0; s < C::NSTAGE; ++s) {
             mbar_init(smem_u32(&bars->kv_full[s]), 1);
-            mbar_init(smem_u32(&bars->kv_empty[s]), 2);   // released by both MMA lanes
+            mbar_init(smem_u32(&bars->kv_empty[s]), 2);   // released by both issuing warps
         }
         bars->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
