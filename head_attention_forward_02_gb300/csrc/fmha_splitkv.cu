@@ -15,7 +15,6 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <math.h>
-#include <mutex>
 
 #include "fmha_common.h"
 
@@ -193,26 +192,19 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = FMHA_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch on the current device.  In host code
+// Device address of g_noalloc_scratch in the current context.  In host code
 // the array's name stands for a host-side shadow, not for device memory, so
-// the address must come from cudaGetSymbolAddress -- once per device, with
-// that device current.
+// the address must come from cudaGetSymbolAddress, with the device current.
+// It is looked up on every call rather than cached: the array moves when the
+// device's context is destroyed and created again (cudaDeviceReset), and a
+// cached address would then point at unmapped memory.
 int noalloc_scratch(void **out) {
-    static std::mutex mu;
-    static void *addr[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return FMHA_ERR_CUDA; }
-    if (dev < 0 || dev >= 64) return FMHA_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lk(mu);
-    if (!addr[dev]) {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
-            cudaGetLastError();
-            return FMHA_ERR_CUDA;
-        }
-        addr[dev] = ptr;
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return FMHA_ERR_CUDA;
     }
-    *out = addr[dev];
+    *out = ptr;
     return FMHA_OK;
 }
 
@@ -224,14 +216,20 @@ extern "C" int fmha_fwd_splitkv_noalloc(fmha_tensor q, fmha_tensor k, fmha_tenso
                                         float scale, float out_scale, int mask, int causal_type,
                                         const int *cu_seqlens_q, const int *cu_seqlens_k, int max_len,
                                         int64_t total_length, int num_splits, cudaStream_t stream) {
-    const bool varlen = cu_seqlens_q != nullptr && cu_seqlens_k != nullptr;
-    const size_t need = fmha_fwd_splitkv_workspace_size(B, H, varlen ? 0 : Sq, D, num_splits,
-                                                        varlen ? total_length : 0);
+    // the same checks, in the same order, as fmha_fwd_splitkv: an empty problem
+    // succeeds and a bad argument gets its own status before the size test
+    if (num_splits < 1 || num_splits > fmha::kMaxSplits) return FMHA_ERR_INVALID_ARG;
+    fmha::Params p{};
+    int rc = fmha::make_params(p, q, k, v, o, lse, B, H, H_k, Sq, Sk, D, scale, out_scale, mask,
+                               causal_type, cu_seqlens_q, cu_seqlens_k, max_len, total_length);
+    if (rc == 1) return FMHA_OK;
+    if (rc != FMHA_OK) return rc;
+    const size_t need = fmha_fwd_splitkv_workspace_size(B, H, p.varlen ? 0 : Sq, D, num_splits,
+                                                        p.varlen ? total_length : 0);
     if (need == 0) return FMHA_ERR_INVALID_ARG;
     if (need > fmha::kNoAllocScratchBytes) return FMHA_ERR_UNSUPPORTED;   // too big for the array
     void *scratch = nullptr;
-    const int rc = fmha::noalloc_scratch(&scratch);
-    if (rc != FMHA_OK) return rc;
+    if ((rc = fmha::noalloc_scratch(&scratch)) != FMHA_OK) return rc;
     return fmha_fwd_splitkv(q, k, v, o, lse, B, H, H_k, Sq, Sk, D, scale, out_scale, mask, causal_type,
                             cu_seqlens_q, cu_seqlens_k, max_len, total_length, num_splits, scratch,
                             fmha::kNoAllocScratchBytes, stream);

@@ -186,10 +186,12 @@ size_t fmha_fwd_splitkv_workspace_size(int B, int H, int Sq, int D, int num_spli
  * exits.  The caller still owns q, k, v, o and lse.  No device memory is
  * allocated or freed by this call.
  *
- * - The first call on a device looks up the array's device address with the
- *   device current (a host-side step, once per device); make that first call
- *   before any stream capture.
- * - Problems whose split-KV scratch (fmha_fwd_splitkv_workspace_size) exceeds
+ * - Every call looks up the array's device address in the current context, a
+ *   host-side step (the first call on a device also loads the library's device
+ *   code there); make the first call on a device before any stream capture.
+ * - Arguments are checked first, exactly as fmha_fwd_splitkv checks them: an
+ *   empty problem returns FMHA_OK and a bad argument its own status.  Then
+ *   problems whose split-KV scratch (fmha_fwd_splitkv_workspace_size) exceeds
  *   the array return FMHA_ERR_UNSUPPORTED without launching; use
  *   fmha_fwd_splitkv with a workspace for those.
  * - Every call uses the same array.  Nothing in it needs to start at zero

@@ -148,6 +148,42 @@ def test_splitkv_validation(fm):
     assert call_split(fm, B=0, splits=3) == 0                  # nothing to do
 
 
+def call_noalloc(fm, splits=2, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=None, B=1, H=2, H_k=2, Sq=128, Sk=128, D=128, scale=0.1,
+             out_scale=1.0, mask=0, causal_type=0, cu_q=None, cu_k=None, max_len=0, total_length=0)
+    a.update(kw)
+    t = [fm.fmha_tensor(a[x], 1) for x in "qkvo"]
+    return fm.lib().fmha_fwd_splitkv_noalloc(*t, a["lse"], a["B"], a["H"], a["H_k"], a["Sq"], a["Sk"],
+                                              a["D"], a["scale"], a["out_scale"], a["mask"],
+                                              a["causal_type"], a["cu_q"], a["cu_k"], a["max_len"],
+                                              a["total_length"], splits, None)
+
+
+# Every case below returns before the device is touched: the entry point
+# checks its arguments as fmha_fwd_splitkv does, and only then its size limit.
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), 0), (dict(Sq=0), 0), (dict(B=0, q=None, k=None, v=None, o=None), 0),
+    (dict(cu_q=P, cu_k=P, total_length=0, max_len=0, B=3), 0),      # empty varlen problem
+    (dict(splits=0), -1), (dict(splits=257), -1), (dict(D=48), -1), (dict(H=3, H_k=2), -1),
+    (dict(scale=0.0), -1), (dict(mask=5), -1), (dict(cu_q=P), -1), (dict(q=None), -1),
+    (dict(q=P + 8), -2), (dict(lse=P + 2), -1),
+    (dict(B=1, H=32, H_k=32, Sq=8192, Sk=8192, splits=4), -2),      # 34 MiB of scratch > 32 MiB
+    (dict(B=1, H=33, H_k=2, Sq=8192, Sk=8192, splits=4), -1),       # too big and a bad head count
+    (dict(cu_q=P, cu_k=P, total_length=1 << 20, max_len=4096, H=16, splits=2), -2),
+])
+def test_noalloc_validation_before_any_launch(fm, kw, code):
+    assert call_noalloc(fm, **kw) == code
+
+
+def test_noalloc_limit_is_the_split_kv_scratch_size(fm):
+    # B=1, H=2, D=128, 4 splits: Sq = 8128 needs just under the 32 MiB array,
+    # Sq = 8129 just over it (and is refused before any launch)
+    limit = 32 << 20
+    assert fm.fmha_fwd_splitkv_workspace_size(1, 2, 8128, 128, 4) <= limit
+    assert fm.fmha_fwd_splitkv_workspace_size(1, 2, 8129, 128, 4) > limit
+    assert call_noalloc(fm, H=2, H_k=2, Sq=8129, Sk=300, splits=4) == -2
+
+
 def call_gen(fm, **kw):
     a = dict(q=P, kc=P, vc=P, kn=None, vn=None, o=P, lse=None, B=2, H=8, H_k=2, D=128, B_cache=2, S_max=64,
              seqlen=P, bidx=None, scale=0.1, out_scale=1.0, ws=P, ws_bytes=1 << 30, dtypes=(1, 1, 1, 1))

@@ -14,7 +14,7 @@ import zlib
 import pytest
 import torch
 
-from tests.gpu_util import Run, all_rows, compare
+from tests.gpu_util import Run, all_rows, compare, e4m3_weight_bound
 from tests.helpers import fixed_inputs, varlen_inputs
 
 pytestmark = pytest.mark.gpu
@@ -165,13 +165,15 @@ def test_growing_max_forces_rescale(fm, oracle, dtype, mask, impl):
     gain = torch.ones(420)
     gain[:128], gain[128:256], gain[256:] = 0.1, 2.0, 6.0
     inp.k[:] = (k * gain[None, :, None, None]).to(inp.k.dtype)
-    if dtype == "e4m3":
-        # Attention this peaked puts most weight on a few keys, where the e4m3
-        # rounding of P (3 mantissa bits) shows up undamped in O; smaller V
-        # keeps the comparison inside the e4m3 bound while the same rescale
-        # path runs.
-        inp.v[:] = (inp.v.float() * 0.25).to(inp.v.dtype)
     run = Run(fm, inp, impl)
     assert run.status == 0
     assert run.guards_intact()
-    compare(run, oracle, all_rows(inp))
+    rows = all_rows(inp)
+    extra = None
+    if dtype == "e4m3" and impl == "tc":
+        # Attention this peaked puts most of a row's weight on a few keys, so
+        # the e4m3 rounding of those weights is not averaged away: the bound
+        # adds its derived worst case (e4m3_weight_bound) to the e4m3 tolerance.
+        extra = e4m3_weight_bound(oracle, inp, rows)
+    stats = compare(run, oracle, rows, extra=extra)
+    print(dtype, mask, impl, stats, None if extra is None else float(extra.max()))

@@ -8,11 +8,12 @@ caller workspace on two calls in a row -- different problem sizes, so scratch
 left over from the first call would show in the second -- and that it rejects
 a problem too big for the array.  The file is named to be collected last.
 """
+import numpy as np
 import pytest
 import torch
 
-from tests.gpu_util import TOL_LSE, TOL_O
-from tests.helpers import fixed_inputs
+from tests.gpu_util import TOL_LSE, TOL_O, half_ulp
+from tests.helpers import fixed_inputs, oracle_on, varlen_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -76,6 +77,39 @@ def test_noalloc_matches_workspace_entry_on_two_calls(fm):
     free_before, free_after = _call_pair(fm, *b, splits=3)
     _check(b[0], b[2])
     assert free_after >= free_before          # the call reserved no device memory
+
+
+def test_noalloc_at_the_size_limit(fm):
+    # B=1, H=2, D=128, 4 splits: Sq = 8128 needs all but 2 KB of the 32 MiB
+    # array, so every partial result lands at the far end of it
+    a = _problem(fm, B=1, H=2, H_k=2, Sq=8128, Sk=700, mask="causal", causal_type="qend", seed=43)
+    assert fm.fmha_fwd_splitkv_workspace_size(1, 2, 8128, 128, 4) <= 32 << 20
+    _call_pair(fm, *a, splits=4)
+    _check(a[0], a[2])
+
+
+def test_noalloc_varlen_against_the_oracle(fm, oracle):
+    inp = varlen_inputs([300, 0, 517, 129], [700, 40, 517, 1000], dtype="bf16", H=4, H_k=2, D=128,
+                        mask="causal", causal_type="qend", seed=44)
+    w, T = inp.w, inp.total_length
+    q, k, v = inp.q.cuda(), inp.k.cuda(), inp.v.cuda()
+    cq, ck = inp.cu_seqlens_q.cuda(), inp.cu_seqlens_k.cuda()
+    o = torch.full(q.shape, float("nan"), dtype=q.dtype, device="cuda")
+    lse = torch.full((w.H, T), float("nan"), dtype=torch.float32, device="cuda")
+    rc = fm.fmha_fwd_splitkv_noalloc(q, k, v, o, lse, len(inp.seqlens_q), w.H, w.H_k, 0, 0, w.D,
+                                     w.softmax_scale, 1.0, 2, 1, cq, ck, inp.max_len, T, num_splits=3)
+    assert rc == 0, fm.status_string(rc)
+    torch.cuda.synchronize()
+    assert fm.device_status(reset=True) == 0
+    end = int(inp.cu_seqlens_q[-1])
+    rows = np.array([h * T + t for h in range(w.H) for t in range(end)], dtype=np.int64)
+    o_ref, lse_ref = oracle_on(oracle, inp, rows=rows)
+    got = o[:end].permute(1, 0, 2).reshape(-1, w.D).double().cpu().numpy()
+    assert (np.abs(got - o_ref) <= TOL_O["bf16"] + half_ulp("bf16", o_ref)).all()
+    got_lse = lse[:, :end].reshape(-1).double().cpu().numpy()
+    masked = np.isneginf(lse_ref)
+    assert np.isneginf(got_lse[masked]).all() and (got[masked] == 0).all()
+    assert (np.abs(got_lse[~masked] - lse_ref[~masked]) <= TOL_LSE).all()
 
 
 def test_noalloc_rejects_problems_larger_than_its_scratch(fm):
