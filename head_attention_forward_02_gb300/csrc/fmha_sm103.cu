@@ -82,11 +82,18 @@ struct Cfg {
     static constexpr int QK_STEPS = D / MMA_K;
     static constexpr int PV_STEPS = kTile / MMA_K;
     static constexpr int NS = TILE_BYTES <= 8192 ? 8 : (TILE_BYTES <= 16384 ? 6 : 4);
+    // Head dims up to 64 leave TMEM for a third 128-column score region: S
+    // tiles then rotate over three regions, so the next S of a Q tile is
+    // computed while the softmax still works on the current one (the
+    // three-region schedule, mma_issuer3 / softmax_wg3).  At D = 128 the two
+    // O accumulators take the room and each Q tile keeps one region.
+    static constexpr bool TRIPLE = D <= 64;
     // 16-bit inputs pair the ring: stage i holds V_{j-1} and K_j behind one
     // barrier, so an issuing warp waits and releases once per key step
     // (measured +2% at D=128); e4m3 keeps one tile per stage, where V_j is
-    // not held back by K_{j+1} (pairing measured -3% there).
-    static constexpr bool PAIRED = !FP8;
+    // not held back by K_{j+1} (pairing measured -3% there).  The
+    // three-region schedule takes K_j and V_j as separate fills.
+    static constexpr bool PAIRED = !FP8 && !TRIPLE;
     static constexpr int NSTAGE = PAIRED ? NS / 2 : NS;   // ring stages (barrier pairs)
     // An issuing warp hands the turn to the other one this many MMAs before
     // the end of an S group, hiding the other warp's wake-up behind
@@ -95,8 +102,8 @@ struct Cfg {
     // last S MMAs costs more than the hand-off (measured -2% to -5%).
     static constexpr int TURN_EARLY = FP8 ? 0 : 2;
     static constexpr int TURN_AT = QK_STEPS - 1 - TURN_EARLY > 0 ? QK_STEPS - 1 - TURN_EARLY : 0;
-    static constexpr int S_COL0 = 0, S_COL1 = kTile;
-    static constexpr int O_COL0 = 2 * kTile, O_COL1 = 2 * kTile + D;
+    static constexpr int S_COL0 = 0, S_COL1 = kTile;      // regions 0, 1 (and 2 at 2 * kTile)
+    static constexpr int O_COL0 = (TRIPLE ? 3 : 2) * kTile, O_COL1 = O_COL0 + D;
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_USED = 2 * TILE_BYTES + NS * TILE_BYTES + BAR_BYTES;
     // at least 120 KB so that a second CTA can never share the SM (TMEM is
@@ -116,8 +123,11 @@ struct Cfg {
 };
 
 struct Bars {
-    uint64_t q_full[2], q_empty[2], s_full[2], p_half[2], p_full[2], o_full[2], drain;
+    // s_full / p_half / p_full: per Q tile, or per slot mod 6 in the
+    // three-region schedule
+    uint64_t q_full[2], q_empty[2], s_full[6], p_half[6], p_full[6], o_full[2], drain;
     uint64_t turn[2];          // issue turn of the issuing warp of Q tile t
+    uint64_t pv_done[2];       // three-region schedule: PV of Q tile t complete
     uint64_t kv_full[8], kv_empty[8];
     uint32_t tmem_base;
     int abort;
@@ -548,7 +558,11 @@ __device__ __forceinline__ bool decode_unit(const Params &p, int u, Cursor &cur,
 // unit's key tiles [0, max(n0, n1)) are cut into num_splits near-equal
 // contiguous ranges; tile t then covers [j0, min(n_t, j1)) and is active
 // when that range is not empty.  Without split-KV, j0 = 0 and j1 = max(n0, n1).
-template <bool SPLIT>
+// BOTH (the three-region schedule): both tiles run all of [j0, j1), a tile
+// past its last visible key on fully masked tiles (their weights are 0), so
+// that every key step holds one S slot per tile and the slot sequence is the
+// same for every role.
+template <bool SPLIT, bool BOTH = false>
 __device__ __forceinline__ bool decode_work(const Params &p, int u, Cursor &cur, Unit &U) {
     const int ns = SPLIT ? p.num_splits : 1;      // a constant 1 folds the split arithmetic away
     if (!decode_unit(p, u / ns, cur, U)) return false;
@@ -556,8 +570,8 @@ __device__ __forceinline__ bool decode_work(const Params &p, int u, Cursor &cur,
     U.split = u % ns;
     U.j0 = (int)((int64_t)nmax * U.split / ns);
     U.j1 = (int)((int64_t)nmax * (U.split + 1) / ns);
-    U.n[0] = imin(U.n[0], U.j1);
-    U.n[1] = imin(U.n[1], U.j1);
+    U.n[0] = BOTH ? U.j1 : imin(U.n[0], U.j1);
+    U.n[1] = BOTH ? U.j1 : imin(U.n[1], U.j1);
     return true;
 }
 
@@ -577,7 +591,7 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
     Cursor cur;
     for (int r = 0; ok; ++r) {
         Unit U;
-        if (!decode_work<SPLIT>(p, unit_of_round(r), cur, U)) break;
+        if (!decode_work<SPLIT, C::TRIPLE>(p, unit_of_round(r), cur, U)) break;
         for (int t = 0; t < 2; ++t) {
             if (U.n[t] <= U.j0) continue;                 // tile inactive in this work item
             if (qload[t] > 0 &&
@@ -964,10 +978,18 @@ __device__ __forceinline__ void rescale_o(uint32_t o_tm, float alpha) {
 // rescaled by alpha when `rescale` is set, before the first half of P_t_j is
 // published; that happens after the first half is stored, while only the
 // second half of the scores is live.
-template <class C>
+struct NoWait {
+    __device__ bool operator()() const { return true; }
+};
+
+// `before_o` runs (warp-wide) after the first half of P is stored and before
+// O may be rescaled; if it fails (an aborted wait) *failed is set and O is
+// left alone.
+template <class C, class Pre = NoWait>
 __device__ __forceinline__ float exp_store_publish(uint32_t s_tm, const float (&s)[kTile], float c, float neg_m,
                                                    bool rescale, uint32_t o_tm, float alpha, uint32_t half_bar,
-                                                   uint32_t full_bar, int lane) {
+                                                   uint32_t full_bar, int lane, Pre before_o = Pre(),
+                                                   bool *failed = nullptr) {
     const uint64_t c2 = pack_f2(c, c), nm2 = pack_f2(neg_m, neg_m);
     float sum = 0.f;
 #pragma unroll
@@ -980,6 +1002,10 @@ __device__ __forceinline__ float exp_store_publish(uint32_t s_tm, const float (&
             uint32_t w[16];
             sum += exp_half<C>(s + 64 * h, c2, nm2, w);
             tmem_st16(s_tm + 16 * h, w);
+        }
+        if (h == 0 && !before_o()) {
+            if (failed) *failed = true;
+            rescale = false;
         }
         if (h == 0 && rescale) rescale_o<C>(o_tm, alpha);
         tmem_wait_st();
@@ -1009,6 +1035,62 @@ __device__ __forceinline__ void store_chunk(uint8_t *dst, const uint32_t (&r)[32
         uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
         for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
+}
+
+// Epilogue of one Q tile of a work item, by its softmax thread (one row):
+// O = out_scale * O_acc / l cast to the output type, LSE = ln(sum exp(scale s));
+// split-KV writes the normalised fp32 partial O and its LSE instead.  `have`
+// is false when the tile had no key tile in this item (O = 0, LSE = -inf).
+template <class C, bool SPLIT>
+__device__ __forceinline__ void epilogue(const Params &p, const Unit &U, int row, bool have, float l, float m_ref,
+                                         uint32_t o_tm) {
+    const bool valid = row < U.sq;
+    if constexpr (SPLIT) {
+        // split-KV: normalised fp32 partial O and its LSE for the combine
+        const int64_t prow = ((int64_t)U.split * p.part_rows + U.q_row + row) * p.H + U.h;
+        float *po = p.part_o + prow * C::D;
+        const float pinv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+        for (int ch = 0; ch < C::D / 32; ++ch) {
+            uint32_t r[32];
+            if (have) {
+                tmem_ld32(o_tm + 32 * ch, r);
+                tmem_wait_ld(r);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = 0u;
+            }
+            if (valid) {
+                float4 *d4 = reinterpret_cast<float4 *>(po + 32 * ch);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    d4[i] = make_float4(__uint_as_float(r[4 * i]) * pinv, __uint_as_float(r[4 * i + 1]) * pinv,
+                                        __uint_as_float(r[4 * i + 2]) * pinv, __uint_as_float(r[4 * i + 3]) * pinv);
+            }
+        }
+        if (valid) p.part_lse[prow] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        return;
+    }
+    const float inv = l > 0.f ? p.out_scale / l : 0.f;
+    uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) +
+                    (((int64_t)U.q_row + row) * p.H + U.h) * (int64_t)(C::D * C::E);
+#pragma unroll 1
+    for (int ch = 0; ch < C::D / 32; ++ch) {
+        uint32_t r[32];
+        if (have) {
+            tmem_ld32(o_tm + 32 * ch, r);
+            tmem_wait_ld(r);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
+        if (valid) store_chunk<C>(orow + ch * 32 * C::E, r, inv);
+    }
+    if (valid && p.lse) {
+        const int64_t li = p.varlen ? (int64_t)U.h * p.total_length + U.q_row + row
+                                    : ((int64_t)U.b * p.H + U.h) * p.Sq + row;
+        p.lse[li] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
     }
 }
 
@@ -1071,53 +1153,238 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
             o_ph ^= 1;
             tc_fence_after();
         }
-        const bool valid = row < U.sq;
-        if constexpr (SPLIT) {
-            // split-KV: normalised fp32 partial O and its LSE for the combine
-            const int64_t prow = ((int64_t)U.split * p.part_rows + U.q_row + row) * p.H + U.h;
-            float *po = p.part_o + prow * C::D;
-            const float pinv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll 1
-            for (int ch = 0; ch < C::D / 32; ++ch) {
-                uint32_t r[32];
-                if (have) {
-                    tmem_ld32(o_tm + 32 * ch, r);
-                    tmem_wait_ld(r);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = 0u;
-                }
-                if (valid) {
-                    float4 *d4 = reinterpret_cast<float4 *>(po + 32 * ch);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        d4[i] = make_float4(__uint_as_float(r[4 * i]) * pinv, __uint_as_float(r[4 * i + 1]) * pinv,
-                                            __uint_as_float(r[4 * i + 2]) * pinv, __uint_as_float(r[4 * i + 3]) * pinv);
-                }
+        epilogue<C, SPLIT>(p, U, row, have, l, m_ref, o_tm);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Three-region schedule (head dims 32 and 64)
+// ---------------------------------------------------------------------------
+//
+// The S tiles of a CTA form one sequence of slots: work item by work item,
+// key step by key step, tile 0 then tile 1, so slot g is (step, tile g & 1).
+// Slot g's S lives in score region g % 3 (128 TMEM columns); its P
+// overwrites the same columns.  A region's uses alternate between the two
+// tiles, so its barriers are kept per slot mod 6 (region and tile): each
+// such barrier has one waiting role, which meets its phases in order -- a
+// parity wait for phase k must never run while phase k - 1 is still open,
+// or it passes at once.  Slot g is phase g / 6 of barrier g % 6.  K_j and V_j
+// of a work item are ring fills numbered like the item's slots: K_j is the
+// fill of slot (step j, tile 0), V_j that of (step j, tile 1).
+//
+// Issuing warp w issues PV of tile w and S of tile 1 - w, in the order
+//   PV_g, S_{g+3}, PV_{g+2}, S_{g+5}, ...   (g = w, w + 2, ...)
+// after S_0, S_2 (warp 1) or S_1 (warp 0).  S_{g+3} takes the region that
+// PV_g has just read, and both come from the same thread, so the tensor pipe
+// runs them in that order and no barrier is needed between them.  Each tile
+// thus has its next S computed while its softmax works on the current one;
+// the chain softmax -> PV -> S -> softmax of the two-region schedule becomes
+// softmax -> softmax.  Because S of tile t no longer implies that the
+// previous PV of tile t is done, the softmax warps of tile t wait for
+// pv_done[t] (that PV) before they may rescale O_t -- at every step, so
+// that this barrier's phases are met in order too.
+
+// The work items that hold slots g .. g + 3 of an issuing warp, decoded in
+// order (an item has at least two slots, so four items always suffice).
+template <bool SPLIT>
+struct ItemWindow {
+    static constexpr int N = 4;
+    Unit u[N];
+    int base[N];
+    int head = 0, cnt = 0, r = 0, next_base = 0;
+    bool done = false;
+    Cursor cur;
+
+    // index of the item holding slot g, or -1 past the last slot
+    __device__ int find(const Params &p, int g) {
+        for (;;) {
+            for (int i = 0; i < cnt; ++i) {
+                const int k = (head + i) & (N - 1);
+                if (g >= base[k] && g < base[k] + 2 * (u[k].j1 - u[k].j0)) return k;
             }
-            if (valid) p.part_lse[prow] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-            continue;
+            if (done || cnt == N) return -1;
+            Unit U;
+            for (;;) {
+                if (!decode_work<SPLIT, true>(p, unit_of_round(r), cur, U)) { done = true; break; }
+                ++r;
+                if (U.j1 > U.j0) break;                    // items without a key tile hold no slot
+            }
+            if (done) return -1;
+            const int k = (head + cnt) & (N - 1);
+            u[k] = U;
+            base[k] = next_base;
+            next_base += 2 * (U.j1 - U.j0);
+            ++cnt;
         }
-        const float inv = l > 0.f ? p.out_scale / l : 0.f;
-        uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) +
-                        (((int64_t)U.q_row + row) * p.H + U.h) * (int64_t)(C::D * C::E);
-#pragma unroll 1
-        for (int ch = 0; ch < C::D / 32; ++ch) {
-            uint32_t r[32];
-            if (have) {
-                tmem_ld32(o_tm + 32 * ch, r);
-                tmem_wait_ld(r);
+    }
+    // forget the items that end at or before slot g
+    __device__ void drop_before(int g) {
+        while (cnt > 0 && base[head] + 2 * (u[head].j1 - u[head].j0) <= g) {
+            head = (head + 1) & (N - 1);
+            --cnt;
+        }
+    }
+};
+
+template <class C, bool SPLIT>
+__device__ void mma_issuer3(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bars, uint32_t tmem_any, int w) {
+    volatile int *abort_flag = &bars->abort;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_any, 0);   // the same in every lane
+    constexpr uint32_t kIdS = C::idesc(kTile, false);
+    constexpr uint32_t kIdPV = C::idesc(C::D, true);
+    constexpr uint32_t kHi = desc_hi(C::SBO, (uint32_t)C::SW_CODE);
+    constexpr uint32_t kTileStep = C::TILE_BYTES >> 4;
+    const uint32_t q_lo = desc_lo(smem_u32(sQ), 16);                 // K-major: LBO unused
+    const uint32_t k_lo = desc_lo(smem_u32(sKV), 16);
+    const uint32_t v_lo = desc_lo(smem_u32(sKV), C::PANEL_BYTES);    // MN-major: LBO = panel stride
+    const uint32_t o_tm = tmem + (w ? C::O_COL1 : C::O_COL0);
+    ItemWindow<SPLIT> win;
+    uint32_t qc = 0;                 // Q tiles of tile 1 - w waited for
+    bool ok = true;
+
+    auto kv_wait = [&](int f) -> bool {
+        return warp_wait(smem_u32(&bars->kv_full[f % C::NSTAGE]), (uint32_t)(f / C::NSTAGE) & 1, abort_flag);
+    };
+    // S of slot g (tile 1 - w) into region g % 3
+    auto issue_s = [&](int g) -> bool {
+        const int k = win.find(p, g);
+        if (k < 0) return true;                              // past the last slot
+        const Unit &U = win.u[k];
+        const int rel = g - win.base[k], j = U.j0 + (rel >> 1), t = rel & 1;
+        if (j == U.j0) {
+            if (!warp_wait(smem_u32(&bars->q_full[t]), qc & 1, abort_flag)) return false;
+            ++qc;
+        }
+        const int fk = g - t;                                // fill of K_j
+        if (!kv_wait(fk)) return false;
+        const uint32_t s_tm = tmem + (uint32_t)((g % 3) * kTile);
+        const uint32_t qa = q_lo + t * kTileStep, kb = k_lo + (fk % C::NSTAGE) * kTileStep;
+#pragma unroll
+        for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+            const uint32_t off =
+                ((kk * C::KSTEP_BYTES / C::SW) * C::PANEL_BYTES + (kk * C::KSTEP_BYTES) % C::SW) >> 4;
+            mma_ss_e<C::FP8>(s_tm, qa + off, kb + off, kHi, kIdS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit_e(smem_u32(&bars->s_full[g % 6]));
+        if (j == U.j1 - 1) tc_commit_e(smem_u32(&bars->q_empty[t]));
+        tc_commit_e(smem_u32(&bars->kv_empty[fk % C::NSTAGE]));
+        return true;
+    };
+    // O_w (+)= P_g V_j, P from region g % 3 in two halves of 64 keys
+    auto issue_pv = [&](int k, int g) -> bool {
+        const Unit &U = win.u[k];
+        const int j = U.j0 + ((g - win.base[k]) >> 1);
+        const int fv = g - w + 1;                            // fill of V_j
+        const int b6 = g % 6;
+        const uint32_t par = (uint32_t)(g / 6) & 1;
+        if (!kv_wait(fv)) return false;
+        const uint32_t s_tm = tmem + (uint32_t)((g % 3) * kTile);
+        const uint32_t vb = v_lo + (fv % C::NSTAGE) * kTileStep;
+        constexpr int HK = C::PV_STEPS / 2;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            // P was written by the softmax threads (tcgen05.st): order this
+            // thread's MMAs after their fence::before_thread_sync + arrive
+            if (!warp_wait(smem_u32(hf ? &bars->p_full[b6] : &bars->p_half[b6]), par, abort_flag)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int kx = 0; kx < HK; ++kx) {
+                const int kk = hf * HK + kx;
+                mma_ts_e<C::FP8>(o_tm, s_tm + kk * (C::MMA_K * C::E / 4), vb + ((kk * C::MMA_K * C::SW) >> 4),
+                                 kHi, kIdPV, (j > U.j0 || kk > 0) ? 1u : 0u);
+            }
+        }
+        tc_commit_e(smem_u32(&bars->pv_done[w]));
+        if (j == U.j1 - 1) tc_commit_e(smem_u32(&bars->o_full[w]));
+        tc_commit_e(smem_u32(&bars->kv_empty[fv % C::NSTAGE]));
+        return true;
+    };
+
+    if (w == 1) ok = issue_s(0) && issue_s(2);
+    else ok = issue_s(1);
+    for (int g = w; ok; g += 2) {
+        const int k = win.find(p, g);
+        if (k < 0) break;
+        if (!issue_pv(k, g) || !issue_s(g + 3)) { ok = false; break; }
+        win.drop_before(g + 2);
+    }
+    // no tensor-core operation may be in flight when TMEM is released
+    tc_commit_e(smem_u32(&bars->drain));
+    mbar_wait_drain(smem_u32(&bars->drain), 0);
+}
+
+template <class C, bool SPLIT>
+__device__ void softmax_wg3(const Params &p, Bars *bars, uint32_t tmem, int warp, int lane) {
+    volatile int *abort_flag = &bars->abort;
+    const int t = warp >> 2, wq = warp & 3;
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t o_tm = lane_base + (t ? C::O_COL1 : C::O_COL0);
+    const uint32_t o_bar = smem_u32(&bars->o_full[t]);
+    const uint32_t pv_bar = smem_u32(&bars->pv_done[t]);
+    const float c = p.scale * kLog2e;          // scores in log2 units: s * scale * log2(e)
+    const bool causal = p.mask == FMHA_MASK_CAUSAL;
+    uint32_t o_ph = 0, pvc = 0;                // pvc: PVs of tile t issued before this step
+    int gbase = 0;                             // first slot of the work item
+    bool ok = true;
+    Cursor cur;
+    for (int r = 0; ok; ++r) {
+        Unit U;
+        if (!decode_work<SPLIT, true>(p, unit_of_round(r), cur, U)) break;
+        const int nu = U.nu[t], j0 = U.j0, j1 = U.j1;
+        const int row = U.q0 + t * kTile + wq * 32 + lane;      // query row within the sequence
+        int key_end = U.sk;                                      // keys [0, key_end) are visible to this row
+        if (causal) key_end = imin(key_end, row + 1 + (p.causal_type == FMHA_CAUSAL_QEND ? U.sk - U.sq : 0));
+        float m_ref = -INFINITY;
+        float l = 0.f;
+        for (int j = j0; j < j1; ++j) {
+            const int g = gbase + 2 * (j - j0) + t;
+            const int b6 = g % 6;
+            const uint32_t s_tm = lane_base + (uint32_t)((g % 3) * kTile);
+            if (!warp_wait(smem_u32(&bars->s_full[b6]), (uint32_t)(g / 6) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            float s[kTile];
+            float m_raw;
+            if (j >= nu) {                                   // boundary tile (or past this tile's keys)
+                load_s(s_tm, s);
+                mask_s(s, key_end - j * kTile);
+                m_raw = row_max(s);
             } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = 0u;
+                m_raw = load_s_max(s_tm, s);
             }
-            if (valid) store_chunk<C>(orow + ch * 32 * C::E, r, inv);
+            const float m_tile = m_raw * c;
+            const bool resc = m_tile > m_ref + kRescaleLog2;
+            float alpha = 1.f;
+            if (resc) {
+                alpha = ex2(m_ref - m_tile);
+                l *= alpha;
+                m_ref = m_tile;
+            }
+            const bool rescale_o = j > j0 && __any_sync(0xffffffffu, resc);
+            // O_t holds the previous step's PV only once that PV is done
+            // (checked where O_t may be rescaled, late in the step)
+            bool failed = false;
+            auto pv_wait = [&]() -> bool {
+                if (pvc == 0) return true;
+                if (!warp_wait(pv_bar, (pvc - 1) & 1, abort_flag)) return false;
+                tc_fence_after();
+                return true;
+            };
+            l += exp_store_publish<C>(s_tm, s, c, m_ref == -INFINITY ? 0.f : -m_ref, rescale_o, o_tm, alpha,
+                                      smem_u32(&bars->p_half[b6]), smem_u32(&bars->p_full[b6]), lane, pv_wait,
+                                      &failed);
+            if (failed) { ok = false; break; }
+            ++pvc;
         }
-        if (valid && p.lse) {
-            const int64_t li = p.varlen ? (int64_t)U.h * p.total_length + U.q_row + row
-                                        : ((int64_t)U.b * p.H + U.h) * p.Sq + row;
-            p.lse[li] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        if (!ok) break;
+        gbase += 2 * (j1 - j0);
+
+        const bool have = j1 > j0;
+        if (have) {
+            if (!warp_wait(o_bar, o_ph, abort_flag)) { ok = false; break; }
+            o_ph ^= 1;
+            tc_fence_after();
         }
+        epilogue<C, SPLIT>(p, U, row, have, l, m_ref, o_tm);
     }
 }
 
@@ -1129,6 +1396,8 @@ template <class C, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const Params p) {
+    static_assert(C::S_COL1 == C::S_COL0 + kTile && C::TURN_AT >= 0 && C::TURN_EARLY >= 0,
+                  "score regions are 128 columns apart; the turn hand-over is inside the S group");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sQ = smem;                               // 2 Q tiles
@@ -1140,10 +1409,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_u32(&bars->q_full[t]), 1);
             mbar_init(smem_u32(&bars->q_empty[t]), 1);
-            mbar_init(smem_u32(&bars->s_full[t]), 1);
-            mbar_init(smem_u32(&bars->p_half[t]), 4);   // one arrival per softmax warp
-            mbar_init(smem_u32(&bars->p_full[t]), 4);
             mbar_init(smem_u32(&bars->o_full[t]), 1);
+            mbar_init(smem_u32(&bars->pv_done[t]), 1);
+        }
+        for (int r = 0; r < 6; ++r) {
+            mbar_init(smem_u32(&bars->s_full[r]), 1);
+            mbar_init(smem_u32(&bars->p_half[r]), 4);   // one arrival per softmax warp
+            mbar_init(smem_u32(&bars->p_full[r]), 4);
         }
         mbar_init(smem_u32(&bars->drain), 2);             // one commit per issuing warp
         mbar_init(smem_u32(&bars->turn[0]), 1);
@@ -1166,11 +1438,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = bars->tmem_base;
 
     if (warp < kProducerWarp) {
-        softmax_wg<C, SPLIT>(p, bars, tmem, warp, lane);
+        if constexpr (C::TRIPLE) softmax_wg3<C, SPLIT>(p, bars, tmem, warp, lane);
+        else softmax_wg<C, SPLIT>(p, bars, tmem, warp, lane);
     } else if (warp == kProducerWarp) {
         if (lane == 0) producer<C, SPLIT>(p, &tmQ, &tmK, &tmV, sQ, sKV, bars);
     } else {
-        mma_issuer<C, SPLIT>(p, sQ, sKV, bars, tmem, warp - kMmaWarp);
+        if constexpr (C::TRIPLE) mma_issuer3<C, SPLIT>(p, sQ, sKV, bars, tmem, warp - kMmaWarp);
+        else mma_issuer<C, SPLIT>(p, sQ, sKV, bars, tmem, warp - kMmaWarp);
     }
 
     tc_fence_before();

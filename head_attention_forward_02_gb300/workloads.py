@@ -143,6 +143,26 @@ CONFIGS = {
         Sk=16384, D=128, mask="none", out_scale=1.0, seed=5),
 }
 
+# More shapes of the same forward kernel, timed next to the five above: other
+# head dims, the unmasked and long causal cases and causal e4m3.  Each has a
+# many-unit parity test at the same sizes (tests/test_shapes_gpu.py).
+EXTRA_CONFIGS = {
+    w.name: w for w in [
+        Workload("bf16_causal_b8_h16_s4096_d64", dtype="bf16", B=8, H=16, H_k=16, Sq=4096, Sk=4096, D=64,
+                 mask="causal", seed=6),
+        Workload("bf16_causal_b4_h16_s4096_d32", dtype="bf16", B=4, H=16, H_k=16, Sq=4096, Sk=4096, D=32,
+                 mask="causal", seed=7),
+        Workload("bf16_nomask_gqa_b2_h32_hk8_s8192_d128", dtype="bf16", B=2, H=32, H_k=8, Sq=8192, Sk=8192,
+                 D=128, mask="none", seed=8),
+        Workload("bf16_causal_b1_h32_s16384_d128", dtype="bf16", B=1, H=32, H_k=32, Sq=16384, Sk=16384,
+                 D=128, mask="causal", seed=9),
+        Workload("e4m3_causal_gqa_b2_h32_hk8_s8192_d128", dtype="e4m3", B=2, H=32, H_k=8, Sq=8192, Sk=8192,
+                 D=128, mask="causal", seed=10),
+        Workload("e4m3_causal_b4_h16_s4096_d64", dtype="e4m3", B=4, H=16, H_k=16, Sq=4096, Sk=4096, D=64,
+                 mask="causal", seed=11),
+    ]
+}
+
 
 # ----------------------------------------------------------------------------
 # Generation phase: one new query token per sequence against a K/V cache

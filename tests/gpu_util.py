@@ -190,7 +190,10 @@ def compare(run: Run, oracle, rows: np.ndarray, threads: int = 0, extra=None) ->
         stats["lse_max_err"] = float(d.max()) if d.size else 0.0
         assert not np.isnan(lse).any()
         assert (d <= TOL_LSE).all(), f"LSE mismatch, worst {d.max():.4g}"
-    mean_tol = 1e-3 if w.dtype != "e4m3" else 1e-2
+    # the mean bound carries the mean of the same output-rounding term as the
+    # per-element bound: rounding O to the output type is part of every
+    # element's error (large |O| in peaked rows), it does not average out
+    mean_tol = (1e-3 if w.dtype != "e4m3" else 1e-2) + float(np.mean(half_ulp(w.dtype, o_ref)))
     if extra is not None:
         mean_tol += float(np.mean(extra))
     assert stats["mean_err"] <= mean_tol, stats
