@@ -37,6 +37,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stddef.h>
 #include <mutex>
 
 #include "fmha_common.h"
@@ -978,17 +979,14 @@ __device__ __forceinline__ void rescale_o(uint32_t o_tm, float alpha) {
 // rescaled by alpha when `rescale` is set, before the first half of P_t_j is
 // published; that happens after the first half is stored, while only the
 // second half of the scores is live.
-struct NoWait {
-    __device__ bool operator()() const { return true; }
-};
-
-// `before_o` runs (warp-wide) after the first half of P is stored and before
-// O may be rescaled; if it fails (an aborted wait) *failed is set and O is
-// left alone.
-template <class C, class Pre = NoWait>
+// pv_bar != 0: before O may be rescaled (after the first half of P is
+// stored), wait for phase parity pv_par of pv_bar, the previous PV of this
+// tile; if that wait gives up, *failed is set and O is left alone.
+template <class C>
 __device__ __forceinline__ float exp_store_publish(uint32_t s_tm, const float (&s)[kTile], float c, float neg_m,
                                                    bool rescale, uint32_t o_tm, float alpha, uint32_t half_bar,
-                                                   uint32_t full_bar, int lane, Pre before_o = Pre(),
+                                                   uint32_t full_bar, int lane, uint32_t pv_bar = 0,
+                                                   uint32_t pv_par = 0, volatile int *abort_flag = nullptr,
                                                    bool *failed = nullptr) {
     const uint64_t c2 = pack_f2(c, c), nm2 = pack_f2(neg_m, neg_m);
     float sum = 0.f;
@@ -1003,9 +1001,13 @@ __device__ __forceinline__ float exp_store_publish(uint32_t s_tm, const float (&
             sum += exp_half<C>(s + 64 * h, c2, nm2, w);
             tmem_st16(s_tm + 16 * h, w);
         }
-        if (h == 0 && !before_o()) {
-            if (failed) *failed = true;
-            rescale = false;
+        if (h == 0 && pv_bar != 0) {
+            if (warp_wait(pv_bar, pv_par, abort_flag)) {
+                tc_fence_after();
+            } else {
+                *failed = true;
+                rescale = false;
+            }
         }
         if (h == 0 && rescale) rescale_o<C>(o_tm, alpha);
         tmem_wait_st();
@@ -1185,12 +1187,12 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
 // that this barrier's phases are met in order too.
 
 // The work items that hold slots g .. g + 3 of an issuing warp, decoded in
-// order (an item has at least two slots, so four items always suffice).
+// order (an item has at least two slots, so four items always suffice); an
+// issuing warp needs only each item's key range and first slot.
 template <bool SPLIT>
 struct ItemWindow {
     static constexpr int N = 4;
-    Unit u[N];
-    int base[N];
+    int j0[N], j1[N], base[N];
     int head = 0, cnt = 0, r = 0, next_base = 0;
     bool done = false;
     Cursor cur;
@@ -1200,7 +1202,7 @@ struct ItemWindow {
         for (;;) {
             for (int i = 0; i < cnt; ++i) {
                 const int k = (head + i) & (N - 1);
-                if (g >= base[k] && g < base[k] + 2 * (u[k].j1 - u[k].j0)) return k;
+                if (g >= base[k] && g < base[k] + 2 * (j1[k] - j0[k])) return k;
             }
             if (done || cnt == N) return -1;
             Unit U;
@@ -1211,7 +1213,8 @@ struct ItemWindow {
             }
             if (done) return -1;
             const int k = (head + cnt) & (N - 1);
-            u[k] = U;
+            j0[k] = U.j0;
+            j1[k] = U.j1;
             base[k] = next_base;
             next_base += 2 * (U.j1 - U.j0);
             ++cnt;
@@ -1219,7 +1222,7 @@ struct ItemWindow {
     }
     // forget the items that end at or before slot g
     __device__ void drop_before(int g) {
-        while (cnt > 0 && base[head] + 2 * (u[head].j1 - u[head].j0) <= g) {
+        while (cnt > 0 && base[head] + 2 * (j1[head] - j0[head]) <= g) {
             head = (head + 1) & (N - 1);
             --cnt;
         }
@@ -1249,9 +1252,9 @@ __device__ void mma_issuer3(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *ba
     auto issue_s = [&](int g) -> bool {
         const int k = win.find(p, g);
         if (k < 0) return true;                              // past the last slot
-        const Unit &U = win.u[k];
-        const int rel = g - win.base[k], j = U.j0 + (rel >> 1), t = rel & 1;
-        if (j == U.j0) {
+        const int rel = g - win.base[k], j = win.j0[k] + (rel >> 1), t = rel & 1;
+        const int ij1 = win.j1[k];
+        if (j == win.j0[k]) {
             if (!warp_wait(smem_u32(&bars->q_full[t]), qc & 1, abort_flag)) return false;
             ++qc;
         }
@@ -1266,14 +1269,14 @@ __device__ void mma_issuer3(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *ba
             mma_ss_e<C::FP8>(s_tm, qa + off, kb + off, kHi, kIdS, kk > 0 ? 1u : 0u);
         }
         tc_commit_e(smem_u32(&bars->s_full[g % 6]));
-        if (j == U.j1 - 1) tc_commit_e(smem_u32(&bars->q_empty[t]));
+        if (j == ij1 - 1) tc_commit_e(smem_u32(&bars->q_empty[t]));
         tc_commit_e(smem_u32(&bars->kv_empty[fk % C::NSTAGE]));
         return true;
     };
     // O_w (+)= P_g V_j, P from region g % 3 in two halves of 64 keys
     auto issue_pv = [&](int k, int g) -> bool {
-        const Unit &U = win.u[k];
-        const int j = U.j0 + ((g - win.base[k]) >> 1);
+        const int ij0 = win.j0[k], ij1 = win.j1[k];
+        const int j = ij0 + ((g - win.base[k]) >> 1);
         const int fv = g - w + 1;                            // fill of V_j
         const int b6 = g % 6;
         const uint32_t par = (uint32_t)(g / 6) & 1;
@@ -1291,11 +1294,11 @@ __device__ void mma_issuer3(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *ba
             for (int kx = 0; kx < HK; ++kx) {
                 const int kk = hf * HK + kx;
                 mma_ts_e<C::FP8>(o_tm, s_tm + kk * (C::MMA_K * C::E / 4), vb + ((kk * C::MMA_K * C::SW) >> 4),
-                                 kHi, kIdPV, (j > U.j0 || kk > 0) ? 1u : 0u);
+                                 kHi, kIdPV, (j > ij0 || kk > 0) ? 1u : 0u);
             }
         }
         tc_commit_e(smem_u32(&bars->pv_done[w]));
-        if (j == U.j1 - 1) tc_commit_e(smem_u32(&bars->o_full[w]));
+        if (j == ij1 - 1) tc_commit_e(smem_u32(&bars->o_full[w]));
         tc_commit_e(smem_u32(&bars->kv_empty[fv % C::NSTAGE]));
         return true;
     };
@@ -1321,10 +1324,18 @@ __device__ void softmax_wg3(const Params &p, Bars *bars, uint32_t tmem, int warp
     const uint32_t o_tm = lane_base + (t ? C::O_COL1 : C::O_COL0);
     const uint32_t o_bar = smem_u32(&bars->o_full[t]);
     const uint32_t pv_bar = smem_u32(&bars->pv_done[t]);
+    const uint32_t bar0 = smem_u32(&bars->s_full[0]);
+    constexpr uint32_t kPHalf = offsetof(Bars, p_half) - offsetof(Bars, s_full);
+    constexpr uint32_t kPFull = offsetof(Bars, p_full) - offsetof(Bars, s_full);
     const float c = p.scale * kLog2e;          // scores in log2 units: s * scale * log2(e)
     const bool causal = p.mask == FMHA_MASK_CAUSAL;
-    uint32_t o_ph = 0, pvc = 0;                // pvc: PVs of tile t issued before this step
-    int gbase = 0;                             // first slot of the work item
+    // this tile's slots: g = t, t + 2, ... kept as g % 6 (barrier) and the
+    // parity of g / 6 (its phase); the region is g % 3
+    int b6 = t;
+    uint32_t par = 0;
+    uint32_t o_ph = 0;
+    uint32_t pv_par = 0;                       // phase parity of this tile's next PV
+    bool pv_any = false;                       // a PV of this tile was published before
     bool ok = true;
     Cursor cur;
     for (int r = 0; ok; ++r) {
@@ -1337,10 +1348,9 @@ __device__ void softmax_wg3(const Params &p, Bars *bars, uint32_t tmem, int warp
         float m_ref = -INFINITY;
         float l = 0.f;
         for (int j = j0; j < j1; ++j) {
-            const int g = gbase + 2 * (j - j0) + t;
-            const int b6 = g % 6;
-            const uint32_t s_tm = lane_base + (uint32_t)((g % 3) * kTile);
-            if (!warp_wait(smem_u32(&bars->s_full[b6]), (uint32_t)(g / 6) & 1, abort_flag)) { ok = false; break; }
+            const uint32_t s_tm = lane_base + (uint32_t)((b6 >= 3 ? b6 - 3 : b6) * kTile);
+            const uint32_t sb = bar0 + 8u * (uint32_t)b6;
+            if (!warp_wait(sb, par, abort_flag)) { ok = false; break; }
             tc_fence_after();
             float s[kTile];
             float m_raw;
@@ -1359,24 +1369,19 @@ __device__ void softmax_wg3(const Params &p, Bars *bars, uint32_t tmem, int warp
                 l *= alpha;
                 m_ref = m_tile;
             }
-            const bool rescale_o = j > j0 && __any_sync(0xffffffffu, resc);
-            // O_t holds the previous step's PV only once that PV is done
-            // (checked where O_t may be rescaled, late in the step)
+            // O_t holds the previous step's PV only once that PV is done; the
+            // wait sits where O_t may be rescaled, late in the step
             bool failed = false;
-            auto pv_wait = [&]() -> bool {
-                if (pvc == 0) return true;
-                if (!warp_wait(pv_bar, (pvc - 1) & 1, abort_flag)) return false;
-                tc_fence_after();
-                return true;
-            };
-            l += exp_store_publish<C>(s_tm, s, c, m_ref == -INFINITY ? 0.f : -m_ref, rescale_o, o_tm, alpha,
-                                      smem_u32(&bars->p_half[b6]), smem_u32(&bars->p_full[b6]), lane, pv_wait,
-                                      &failed);
+            l += exp_store_publish<C>(s_tm, s, c, m_ref == -INFINITY ? 0.f : -m_ref,
+                                      j > j0 && __any_sync(0xffffffffu, resc), o_tm, alpha, sb + kPHalf,
+                                      sb + kPFull, lane, pv_any ? pv_bar : 0u, pv_par ^ 1u, abort_flag, &failed);
             if (failed) { ok = false; break; }
-            ++pvc;
+            pv_par ^= 1u;
+            pv_any = true;
+            b6 += 2;
+            if (b6 >= 6) { b6 -= 6; par ^= 1u; }
         }
         if (!ok) break;
-        gbase += 2 * (j1 - j0);
 
         const bool have = j1 > j0;
         if (have) {
