@@ -1245,21 +1245,29 @@ __device__ void mma_issuer3(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *ba
     uint32_t qc = 0;                 // Q tiles of tile 1 - w waited for
     bool ok = true;
 
+    const uint32_t my_turn = smem_u32(&bars->turn[w]), next_turn = smem_u32(&bars->turn[w ^ 1]);
+    uint32_t tc = 0;
     auto kv_wait = [&](int f) -> bool {
         return warp_wait(smem_u32(&bars->kv_full[f % C::NSTAGE]), (uint32_t)(f / C::NSTAGE) & 1, abort_flag);
     };
-    // S of slot g (tile 1 - w) into region g % 3
-    auto issue_s = [&](int g) -> bool {
+    // Operands of S_g (tile 1 - w) in place: its Q tile (first step of an
+    // item) and K tile.  Returns the item index, -1 past the last slot, or
+    // -2 when a wait gave up.
+    auto prep_s = [&](int g) -> int {
         const int k = win.find(p, g);
-        if (k < 0) return true;                              // past the last slot
-        const int rel = g - win.base[k], j = win.j0[k] + (rel >> 1), t = rel & 1;
-        const int ij1 = win.j1[k];
-        if (j == win.j0[k]) {
-            if (!warp_wait(smem_u32(&bars->q_full[t]), qc & 1, abort_flag)) return false;
+        if (k < 0) return -1;
+        const int rel = g - win.base[k], t = rel & 1;
+        if ((rel >> 1) == 0) {
+            if (!warp_wait(smem_u32(&bars->q_full[t]), qc & 1, abort_flag)) return -2;
             ++qc;
         }
+        return kv_wait(g - t) ? k : -2;
+    };
+    // S_g into region g % 3; the issue turn passes to the other warp
+    // TURN_EARLY MMAs before the end of the group
+    auto issue_s = [&](int k, int g) {
+        const int rel = g - win.base[k], j = win.j0[k] + (rel >> 1), t = rel & 1;
         const int fk = g - t;                                // fill of K_j
-        if (!kv_wait(fk)) return false;
         const uint32_t s_tm = tmem + (uint32_t)((g % 3) * kTile);
         const uint32_t qa = q_lo + t * kTileStep, kb = k_lo + (fk % C::NSTAGE) * kTileStep;
 #pragma unroll
@@ -1267,11 +1275,11 @@ __device__ void mma_issuer3(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *ba
             const uint32_t off =
                 ((kk * C::KSTEP_BYTES / C::SW) * C::PANEL_BYTES + (kk * C::KSTEP_BYTES) % C::SW) >> 4;
             mma_ss_e<C::FP8>(s_tm, qa + off, kb + off, kHi, kIdS, kk > 0 ? 1u : 0u);
+            if (kk == C::TURN_AT) mbar_arrive_e(next_turn);
         }
         tc_commit_e(smem_u32(&bars->s_full[g % 6]));
-        if (j == ij1 - 1) tc_commit_e(smem_u32(&bars->q_empty[t]));
+        if (j == win.j1[k] - 1) tc_commit_e(smem_u32(&bars->q_empty[t]));
         tc_commit_e(smem_u32(&bars->kv_empty[fk % C::NSTAGE]));
-        return true;
     };
     // O_w (+)= P_g V_j, P from region g % 3 in two halves of 64 keys
     auto issue_pv = [&](int k, int g) -> bool {
@@ -1280,7 +1288,6 @@ __device__ void mma_issuer3(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *ba
         const int fv = g - w + 1;                            // fill of V_j
         const int b6 = g % 6;
         const uint32_t par = (uint32_t)(g / 6) & 1;
-        if (!kv_wait(fv)) return false;
         const uint32_t s_tm = tmem + (uint32_t)((g % 3) * kTile);
         const uint32_t vb = v_lo + (fv % C::NSTAGE) * kTileStep;
         constexpr int HK = C::PV_STEPS / 2;
@@ -1303,13 +1310,24 @@ __device__ void mma_issuer3(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *ba
         return true;
     };
 
-    if (w == 1) ok = issue_s(0) && issue_s(2);
-    else ok = issue_s(1);
-    for (int g = w; ok; g += 2) {
-        const int k = win.find(p, g);
-        if (k < 0) break;
-        if (!issue_pv(k, g) || !issue_s(g + 3)) { ok = false; break; }
-        win.drop_before(g + 2);
+    // Group q (q = 0, 1, 2, ...) is PV_{q-3} (q >= 3) then S_q; warp (q + 1) & 1
+    // issues it, so the warps take turns group by group and the tensor pipe
+    // runs S_0 S_1 S_2 | PV_0 S_3 | PV_1 S_4 | PV_2 S_5 | ...
+    for (int q = w ^ 1; ok; q += 2) {
+        int kp = -1;
+        if (q >= 3) {
+            kp = win.find(p, q - 3);
+            if (kp < 0) break;                               // no slot left for this warp
+            if (!kv_wait(q - 3 - w + 1)) { ok = false; break; }   // V of PV_{q-3}
+        }
+        const int ks = prep_s(q);
+        if (ks == -2) { ok = false; break; }
+        if (!warp_wait(my_turn, tc & 1, abort_flag)) { ok = false; break; }
+        ++tc;
+        if (q >= 3 && !issue_pv(kp, q - 3)) { ok = false; break; }
+        if (ks >= 0) issue_s(ks, q);
+        else mbar_arrive_e(next_turn);
+        win.drop_before(q - 1);
     }
     // no tensor-core operation may be in flight when TMEM is released
     tc_commit_e(smem_u32(&bars->drain));
@@ -1431,7 +1449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bars->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        mbar_arrive(smem_u32(&bars->turn[0]));            // tile 0's lane issues first
+        // the issuing warp of tile 0's first S takes the first turn
+        mbar_arrive(smem_u32(&bars->turn[C::TRIPLE ? 1 : 0]));
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
