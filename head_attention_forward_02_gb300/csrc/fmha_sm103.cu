@@ -37,7 +37,6 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <math.h>
-#include <stddef.h>
 #include <mutex>
 
 #include "fmha_common.h"
@@ -83,18 +82,19 @@ struct Cfg {
     static constexpr int QK_STEPS = D / MMA_K;
     static constexpr int PV_STEPS = kTile / MMA_K;
     static constexpr int NS = TILE_BYTES <= 8192 ? 8 : (TILE_BYTES <= 16384 ? 6 : 4);
-    // Head dims up to 64 leave TMEM for a third 128-column score region: S
-    // tiles then rotate over three regions, so the next S of a Q tile is
-    // computed while the softmax still works on the current one (the
-    // three-region schedule, mma_issuer3 / softmax_wg3).  At D = 128 the two
-    // O accumulators take the room and each Q tile keeps one region.
-    static constexpr bool TRIPLE = D <= 64;
+    // Head dims up to 64 leave TMEM for a P buffer per Q tile, apart from its
+    // S columns (PSEP): S_t,j+1 may then overwrite S_t as soon as the softmax
+    // warps hold S_t,j in registers, instead of after PV_t,j has read P_t,j
+    // from those columns, so the next S is computed while the softmax works.
+    // At D = 128 the two O accumulators take the room and P aliases S.
+    static constexpr bool PSEP = D <= 64;
     // 16-bit inputs pair the ring: stage i holds V_{j-1} and K_j behind one
     // barrier, so an issuing warp waits and releases once per key step
     // (measured +2% at D=128); e4m3 keeps one tile per stage, where V_j is
-    // not held back by K_{j+1} (pairing measured -3% there).  The
-    // three-region schedule takes K_j and V_j as separate fills.
-    static constexpr bool PAIRED = !FP8 && !TRIPLE;
+    // not held back by K_{j+1} (pairing measured -3% there).  With separate
+    // P buffers an issuing warp takes K_{j+1} before V_j, the order of a
+    // paired stage, so those pair the ring for every input type.
+    static constexpr bool PAIRED = !FP8 || PSEP;
     static constexpr int NSTAGE = PAIRED ? NS / 2 : NS;   // ring stages (barrier pairs)
     // An issuing warp hands the turn to the other one this many MMAs before
     // the end of an S group, hiding the other warp's wake-up behind
@@ -103,8 +103,10 @@ struct Cfg {
     // last S MMAs costs more than the hand-off (measured -2% to -5%).
     static constexpr int TURN_EARLY = FP8 ? 0 : 2;
     static constexpr int TURN_AT = QK_STEPS - 1 - TURN_EARLY > 0 ? QK_STEPS - 1 - TURN_EARLY : 0;
-    static constexpr int S_COL0 = 0, S_COL1 = kTile;      // regions 0, 1 (and 2 at 2 * kTile)
-    static constexpr int O_COL0 = (TRIPLE ? 3 : 2) * kTile, O_COL1 = O_COL0 + D;
+    static constexpr int S_COL0 = 0, S_COL1 = kTile;
+    static constexpr int O_COL0 = 2 * kTile, O_COL1 = 2 * kTile + D;
+    static constexpr int P_COL0 = PSEP ? O_COL1 + D : S_COL0, P_COL1 = PSEP ? P_COL0 + 64 : S_COL1;
+    static_assert(!PSEP || P_COL1 + 64 <= (int)kTmemCols, "TMEM budget of the P buffers");
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_USED = 2 * TILE_BYTES + NS * TILE_BYTES + BAR_BYTES;
     // at least 120 KB so that a second CTA can never share the SM (TMEM is
@@ -124,11 +126,10 @@ struct Cfg {
 };
 
 struct Bars {
-    // s_full / p_half / p_full: per Q tile, or per slot mod 6 in the
-    // three-region schedule
-    uint64_t q_full[2], q_empty[2], s_full[6], p_half[6], p_full[6], o_full[2], drain;
+    uint64_t q_full[2], q_empty[2], s_full[2], p_half[2], p_full[2], o_full[2], drain;
     uint64_t turn[2];          // issue turn of the issuing warp of Q tile t
-    uint64_t pv_done[2];       // three-region schedule: PV of Q tile t complete
+    uint64_t s_free[2];        // separate P buffers: the softmax warps hold S_t in registers
+    uint64_t pv_done[2];       // separate P buffers: PV_t complete (P_t and O_t free)
     uint64_t kv_full[8], kv_empty[8];
     uint32_t tmem_base;
     int abort;
@@ -328,6 +329,28 @@ __device__ __forceinline__ void mbar_arrive_e(uint32_t bar) {
 // Bounded wait by a whole warp: true in every lane, or false in every lane.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
     const bool r = mbar_wait(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, r);
+}
+
+// The same bounded wait with its polling loop inlined: for call sites where
+// many values are live (a call to the out-of-line slow path would make the
+// compiler save them all around it).
+__device__ __forceinline__ bool warp_wait_inline(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    bool r = mbar_try_wait(bar, parity);
+    if (!r) {
+        const unsigned long long t0 = globaltimer();
+        for (uint32_t it = 1;; ++it) {
+            if ((r = mbar_try_wait(bar, parity))) break;
+            if ((it & 63) == 0) {
+                if (*abort_flag) break;
+                if (globaltimer() - t0 > kTimeoutNs) {
+                    *abort_flag = 1;
+                    atomicExch(&g_status, FMHA_ERR_TIMEOUT);
+                    break;
+                }
+            }
+        }
+    }
     return __all_sync(0xffffffffu, r);
 }
 
@@ -559,11 +582,7 @@ __device__ __forceinline__ bool decode_unit(const Params &p, int u, Cursor &cur,
 // unit's key tiles [0, max(n0, n1)) are cut into num_splits near-equal
 // contiguous ranges; tile t then covers [j0, min(n_t, j1)) and is active
 // when that range is not empty.  Without split-KV, j0 = 0 and j1 = max(n0, n1).
-// BOTH (the three-region schedule): both tiles run all of [j0, j1), a tile
-// past its last visible key on fully masked tiles (their weights are 0), so
-// that every key step holds one S slot per tile and the slot sequence is the
-// same for every role.
-template <bool SPLIT, bool BOTH = false>
+template <bool SPLIT>
 __device__ __forceinline__ bool decode_work(const Params &p, int u, Cursor &cur, Unit &U) {
     const int ns = SPLIT ? p.num_splits : 1;      // a constant 1 folds the split arithmetic away
     if (!decode_unit(p, u / ns, cur, U)) return false;
@@ -571,8 +590,8 @@ __device__ __forceinline__ bool decode_work(const Params &p, int u, Cursor &cur,
     U.split = u % ns;
     U.j0 = (int)((int64_t)nmax * U.split / ns);
     U.j1 = (int)((int64_t)nmax * (U.split + 1) / ns);
-    U.n[0] = BOTH ? U.j1 : imin(U.n[0], U.j1);
-    U.n[1] = BOTH ? U.j1 : imin(U.n[1], U.j1);
+    U.n[0] = imin(U.n[0], U.j1);
+    U.n[1] = imin(U.n[1], U.j1);
     return true;
 }
 
@@ -592,7 +611,7 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
     Cursor cur;
     for (int r = 0; ok; ++r) {
         Unit U;
-        if (!decode_work<SPLIT, C::TRIPLE>(p, unit_of_round(r), cur, U)) break;
+        if (!decode_work<SPLIT>(p, unit_of_round(r), cur, U)) break;
         for (int t = 0; t < 2; ++t) {
             if (U.n[t] <= U.j0) continue;                 // tile inactive in this work item
             if (qload[t] > 0 &&
@@ -838,6 +857,119 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
     mbar_wait_drain(smem_u32(&bars->drain), 0);
 }
 
+// Issuing warp t with separate P buffers (head dims 32 and 64).  Per key step
+// j it issues S_t,j+1 as soon as the softmax warps signal that they hold
+// S_t,j in registers (s_free), then PV_t,j from the P buffer once P_t,j is
+// published; the paired ring stage j+1 holds both K_j+1 and V_j.  The two
+// warps run free: S is issued about a softmax step ahead of its use, so the
+// pipe order between the tiles matters little.  PV_t,j completes pv_done[t],
+// which the softmax warps wait for before they overwrite P_t or rescale O_t.
+template <class C, bool SPLIT>
+__device__ void mma_issuer_psep(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bars, uint32_t tmem_any,
+                                int t) {
+    volatile int *abort_flag = &bars->abort;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_any, 0);   // the same in every lane
+    constexpr uint32_t kIdS = C::idesc(kTile, false);
+    constexpr uint32_t kIdPV = C::idesc(C::D, true);
+    constexpr uint32_t kHi = desc_hi(C::SBO, (uint32_t)C::SW_CODE);
+    constexpr uint32_t kTileStep = C::TILE_BYTES >> 4;
+    static_assert(C::PAIRED, "separate P buffers consume the ring in paired order");
+    const uint32_t q_lo = desc_lo(smem_u32(sQ), 16) + t * kTileStep;  // K-major: LBO unused
+    const uint32_t k_lo = desc_lo(smem_u32(sKV), 16);
+    const uint32_t v_lo = desc_lo(smem_u32(sKV), C::PANEL_BYTES);    // MN-major: LBO = panel stride
+    const uint32_t s_tm = tmem + (t ? C::S_COL1 : C::S_COL0);
+    const uint32_t o_tm = tmem + (t ? C::O_COL1 : C::O_COL0);
+    const uint32_t p_tm = tmem + (t ? C::P_COL1 : C::P_COL0);
+    const uint32_t s_full = smem_u32(&bars->s_full[t]), q_empty = smem_u32(&bars->q_empty[t]);
+    const uint32_t s_free = smem_u32(&bars->s_free[t]), pv_done = smem_u32(&bars->pv_done[t]);
+    const uint32_t o_full = smem_u32(&bars->o_full[t]);
+    const uint32_t p_half = smem_u32(&bars->p_half[t]), p_full = smem_u32(&bars->p_full[t]);
+    uint32_t cons = 0, qc = 0, pc = 0, hc = 0, fc = 0;
+    bool any_s = false;              // an S was issued before (its S_t must be free first)
+    bool ok = true;
+    Cursor cur;
+
+    auto issue_s = [&](int st) -> bool {
+        // the softmax warps hold the previous S_t in registers
+        if (any_s) {
+            if (!warp_wait(s_free, fc & 1, abort_flag)) return false;
+            ++fc;
+            tc_fence_after();
+        }
+        any_s = true;
+        const uint32_t b = k_lo + st * 2 * kTileStep;                  // K: first half of the stage
+#pragma unroll
+        for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+            const uint32_t off =
+                ((kk * C::KSTEP_BYTES / C::SW) * C::PANEL_BYTES + (kk * C::KSTEP_BYTES) % C::SW) >> 4;
+            mma_ss_e<C::FP8>(s_tm, q_lo + off, b + off, kHi, kIdS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit_e(s_full);
+        return true;
+    };
+    auto issue_pv = [&](int st, bool acc) -> bool {
+        const uint32_t b = v_lo + (st * 2 + 1) * kTileStep;            // V: second half of the stage
+        constexpr int HK = C::PV_STEPS / 2;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            // P was written by the softmax threads (tcgen05.st): order these
+            // MMAs after their fence::before_thread_sync + arrive
+            if (!warp_wait(hf ? p_full : p_half, hf ? (pc & 1) : (hc & 1), abort_flag)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int kx = 0; kx < HK; ++kx) {
+                const int kk = hf * HK + kx;
+                mma_ts_e<C::FP8>(o_tm, p_tm + kk * (C::MMA_K * C::E / 4), b + ((kk * C::MMA_K * C::SW) >> 4), kHi,
+                                 kIdPV, (acc || kk > 0) ? 1u : 0u);
+            }
+        }
+        ++hc;
+        ++pc;
+        tc_commit_e(pv_done);
+        return true;
+    };
+    auto next_kv = [&](int &st) -> bool {
+        st = cons % C::NSTAGE;
+        const bool r = warp_wait(smem_u32(&bars->kv_full[st]), (cons / C::NSTAGE) & 1, abort_flag);
+        ++cons;
+        return r;
+    };
+
+    for (int r = 0; ok; ++r) {
+        Unit U;
+        if (!decode_work<SPLIT>(p, unit_of_round(r), cur, U)) break;
+        const int n = t ? U.n[1] : U.n[0], j0 = U.j0, jn = U.j1;
+        if (j0 >= jn) continue;
+        int st;
+        if (n > j0) {
+            ok = warp_wait(smem_u32(&bars->q_full[t]), qc & 1, abort_flag);
+            ++qc;
+        }
+        if (!ok || !next_kv(st)) { ok = false; break; }         // stage j0: K_j0
+        if (n > j0) {
+            if (!issue_s(st)) { ok = false; break; }
+            if (n == j0 + 1) tc_commit_e(q_empty);
+        }
+        tc_commit_e(smem_u32(&bars->kv_empty[st]));
+        for (int j = j0; j < jn; ++j) {
+            if (!next_kv(st)) { ok = false; break; }            // stage j+1: V_j, K_j+1
+            const bool act = j < n, more = j + 1 < n;
+            if (more) {
+                if (!issue_s(st)) { ok = false; break; }
+                if (j + 2 == n) tc_commit_e(q_empty);
+            }
+            if (act) {
+                if (!issue_pv(st, j > j0)) { ok = false; break; }
+                if (!more) tc_commit_e(o_full);
+            }
+            tc_commit_e(smem_u32(&bars->kv_empty[st]));
+        }
+    }
+    // no tensor-core operation may be in flight when TMEM is released
+    tc_commit_e(smem_u32(&bars->drain));
+    mbar_wait_drain(smem_u32(&bars->drain), 0);
+}
+
 // ---------------------------------------------------------------------------
 // Softmax warpgroups (one thread per query row) and the epilogue
 // ---------------------------------------------------------------------------
@@ -979,15 +1111,16 @@ __device__ __forceinline__ void rescale_o(uint32_t o_tm, float alpha) {
 // rescaled by alpha when `rescale` is set, before the first half of P_t_j is
 // published; that happens after the first half is stored, while only the
 // second half of the scores is live.
-// pv_bar != 0: before O may be rescaled (after the first half of P is
-// stored), wait for phase parity pv_par of pv_bar, the previous PV of this
-// tile; if that wait gives up, *failed is set and O is left alone.
+//
+// With separate P buffers (p_tm apart from S), pv_wait != 0 names the barrier
+// (bit 31: the phase parity) of the previous PV of this tile, which must be
+// done before P_t is overwritten or O_t rescaled; it is waited for after the
+// first half of P is computed, just before it is stored.
 template <class C>
-__device__ __forceinline__ float exp_store_publish(uint32_t s_tm, const float (&s)[kTile], float c, float neg_m,
+__device__ __forceinline__ float exp_store_publish(uint32_t p_tm, const float (&s)[kTile], float c, float neg_m,
                                                    bool rescale, uint32_t o_tm, float alpha, uint32_t half_bar,
-                                                   uint32_t full_bar, int lane, uint32_t pv_bar = 0,
-                                                   uint32_t pv_par = 0, volatile int *abort_flag = nullptr,
-                                                   bool *failed = nullptr) {
+                                                   uint32_t full_bar, int lane, uint32_t pv_wait = 0,
+                                                   volatile int *abort_flag = nullptr) {
     const uint64_t c2 = pack_f2(c, c), nm2 = pack_f2(neg_m, neg_m);
     float sum = 0.f;
 #pragma unroll
@@ -995,19 +1128,19 @@ __device__ __forceinline__ float exp_store_publish(uint32_t s_tm, const float (&
         if constexpr (!C::FP8) {
             uint32_t w[32];
             sum += exp_half<C>(s + 64 * h, c2, nm2, w);
-            tmem_st32(s_tm + 32 * h, w);
+            if (h == 0 && pv_wait != 0) {
+                if (warp_wait_inline(pv_wait & 0x7fffffffu, pv_wait >> 31, abort_flag)) tc_fence_after();
+                else rescale = false;            // aborted: the caller sees the abort flag
+            }
+            tmem_st32(p_tm + 32 * h, w);
         } else {
             uint32_t w[16];
             sum += exp_half<C>(s + 64 * h, c2, nm2, w);
-            tmem_st16(s_tm + 16 * h, w);
-        }
-        if (h == 0 && pv_bar != 0) {
-            if (warp_wait(pv_bar, pv_par, abort_flag)) {
-                tc_fence_after();
-            } else {
-                *failed = true;
-                rescale = false;
+            if (h == 0 && pv_wait != 0) {
+                if (warp_wait_inline(pv_wait & 0x7fffffffu, pv_wait >> 31, abort_flag)) tc_fence_after();
+                else rescale = false;
             }
+            tmem_st16(p_tm + 16 * h, w);
         }
         if (h == 0 && rescale) rescale_o<C>(o_tm, alpha);
         tmem_wait_st();
@@ -1040,62 +1173,6 @@ __device__ __forceinline__ void store_chunk(uint8_t *dst, const uint32_t (&r)[32
     }
 }
 
-// Epilogue of one Q tile of a work item, by its softmax thread (one row):
-// O = out_scale * O_acc / l cast to the output type, LSE = ln(sum exp(scale s));
-// split-KV writes the normalised fp32 partial O and its LSE instead.  `have`
-// is false when the tile had no key tile in this item (O = 0, LSE = -inf).
-template <class C, bool SPLIT>
-__device__ __forceinline__ void epilogue(const Params &p, const Unit &U, int row, bool have, float l, float m_ref,
-                                         uint32_t o_tm) {
-    const bool valid = row < U.sq;
-    if constexpr (SPLIT) {
-        // split-KV: normalised fp32 partial O and its LSE for the combine
-        const int64_t prow = ((int64_t)U.split * p.part_rows + U.q_row + row) * p.H + U.h;
-        float *po = p.part_o + prow * C::D;
-        const float pinv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll 1
-        for (int ch = 0; ch < C::D / 32; ++ch) {
-            uint32_t r[32];
-            if (have) {
-                tmem_ld32(o_tm + 32 * ch, r);
-                tmem_wait_ld(r);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = 0u;
-            }
-            if (valid) {
-                float4 *d4 = reinterpret_cast<float4 *>(po + 32 * ch);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    d4[i] = make_float4(__uint_as_float(r[4 * i]) * pinv, __uint_as_float(r[4 * i + 1]) * pinv,
-                                        __uint_as_float(r[4 * i + 2]) * pinv, __uint_as_float(r[4 * i + 3]) * pinv);
-            }
-        }
-        if (valid) p.part_lse[prow] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-        return;
-    }
-    const float inv = l > 0.f ? p.out_scale / l : 0.f;
-    uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) +
-                    (((int64_t)U.q_row + row) * p.H + U.h) * (int64_t)(C::D * C::E);
-#pragma unroll 1
-    for (int ch = 0; ch < C::D / 32; ++ch) {
-        uint32_t r[32];
-        if (have) {
-            tmem_ld32(o_tm + 32 * ch, r);
-            tmem_wait_ld(r);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = 0u;
-        }
-        if (valid) store_chunk<C>(orow + ch * 32 * C::E, r, inv);
-    }
-    if (valid && p.lse) {
-        const int64_t li = p.varlen ? (int64_t)U.h * p.total_length + U.q_row + row
-                                    : ((int64_t)U.b * p.H + U.h) * p.Sq + row;
-        p.lse[li] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-    }
-}
-
 template <class C, bool SPLIT>
 __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp, int lane) {
     volatile int *abort_flag = &bars->abort;
@@ -1103,7 +1180,10 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
     const uint32_t s_tm = lane_base + (t ? C::S_COL1 : C::S_COL0);
     const uint32_t o_tm = lane_base + (t ? C::O_COL1 : C::O_COL0);
+    const uint32_t p_tm = lane_base + (t ? C::P_COL1 : C::P_COL0);      // = s_tm unless PSEP
     const uint32_t s_bar = smem_u32(&bars->s_full[t]);
+    const uint32_t sf_bar = smem_u32(&bars->s_free[t]), pv_bar = smem_u32(&bars->pv_done[t]);
+    uint32_t pvc = 0;                          // PSEP: PVs of this tile published so far
     const uint32_t ph_bar = smem_u32(&bars->p_half[t]);
     const uint32_t p_bar = smem_u32(&bars->p_full[t]);
     const uint32_t o_bar = smem_u32(&bars->o_full[t]);
@@ -1130,10 +1210,21 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
             float m_raw;
             if (j >= nu) {                                   // boundary tile
                 load_s(s_tm, s);
+                if constexpr (C::PSEP) {
+                    // S_t is in registers: the next S may overwrite it.  Every
+                    // thread arrives on its own (a lane-0 arrive after a warp
+                    // sync made the compiler spill the live scores)
+                    tc_fence_before();
+                    mbar_arrive(sf_bar);
+                }
                 mask_s(s, key_end - j * kTile);
                 m_raw = row_max(s);
             } else {
                 m_raw = load_s_max(s_tm, s);
+                if constexpr (C::PSEP) {
+                    tc_fence_before();
+                    mbar_arrive(sf_bar);
+                }
             }
             const float m_tile = m_raw * c;                  // scale > 0 keeps the argmax
             const bool resc = m_tile > m_ref + kRescaleLog2;
@@ -1143,8 +1234,17 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
                 l *= alpha;
                 m_ref = m_tile;
             }
-            l += exp_store_publish<C>(s_tm, s, c, m_ref == -INFINITY ? 0.f : -m_ref,
-                                      j > j0 && __any_sync(0xffffffffu, resc), o_tm, alpha, ph_bar, p_bar, lane);
+            if constexpr (C::PSEP) {
+                // P_t and O_t are free once this tile's previous PV is done
+                l += exp_store_publish<C>(p_tm, s, c, m_ref == -INFINITY ? 0.f : -m_ref,
+                                          j > j0 && __any_sync(0xffffffffu, resc), o_tm, alpha, ph_bar, p_bar,
+                                          lane, pvc > 0 ? (pv_bar | (((pvc - 1) & 1u) << 31)) : 0u, abort_flag);
+                ++pvc;
+                if (*abort_flag) { ok = false; break; }
+            } else {
+                l += exp_store_publish<C>(s_tm, s, c, m_ref == -INFINITY ? 0.f : -m_ref,
+                                          j > j0 && __any_sync(0xffffffffu, resc), o_tm, alpha, ph_bar, p_bar, lane);
+            }
         }
         if (!ok) break;
 
@@ -1155,259 +1255,53 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
             o_ph ^= 1;
             tc_fence_after();
         }
-        epilogue<C, SPLIT>(p, U, row, have, l, m_ref, o_tm);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Three-region schedule (head dims 32 and 64)
-// ---------------------------------------------------------------------------
-//
-// The S tiles of a CTA form one sequence of slots: work item by work item,
-// key step by key step, tile 0 then tile 1, so slot g is (step, tile g & 1).
-// Slot g's S lives in score region g % 3 (128 TMEM columns); its P
-// overwrites the same columns.  A region's uses alternate between the two
-// tiles, so its barriers are kept per slot mod 6 (region and tile): each
-// such barrier has one waiting role, which meets its phases in order -- a
-// parity wait for phase k must never run while phase k - 1 is still open,
-// or it passes at once.  Slot g is phase g / 6 of barrier g % 6.  K_j and V_j
-// of a work item are ring fills numbered like the item's slots: K_j is the
-// fill of slot (step j, tile 0), V_j that of (step j, tile 1).
-//
-// Issuing warp w issues PV of tile w and S of tile 1 - w, in the order
-//   PV_g, S_{g+3}, PV_{g+2}, S_{g+5}, ...   (g = w, w + 2, ...)
-// after S_0, S_2 (warp 1) or S_1 (warp 0).  S_{g+3} takes the region that
-// PV_g has just read, and both come from the same thread, so the tensor pipe
-// runs them in that order and no barrier is needed between them.  Each tile
-// thus has its next S computed while its softmax works on the current one;
-// the chain softmax -> PV -> S -> softmax of the two-region schedule becomes
-// softmax -> softmax.  Because S of tile t no longer implies that the
-// previous PV of tile t is done, the softmax warps of tile t wait for
-// pv_done[t] (that PV) before they may rescale O_t -- at every step, so
-// that this barrier's phases are met in order too.
-
-// The work items that hold slots g .. g + 3 of an issuing warp, decoded in
-// order (an item has at least two slots, so four items always suffice); an
-// issuing warp needs only each item's key range and first slot.
-template <bool SPLIT>
-struct ItemWindow {
-    static constexpr int N = 4;
-    int j0[N], j1[N], base[N];
-    int head = 0, cnt = 0, r = 0, next_base = 0;
-    bool done = false;
-    Cursor cur;
-
-    // index of the item holding slot g, or -1 past the last slot
-    __device__ int find(const Params &p, int g) {
-        for (;;) {
-            for (int i = 0; i < cnt; ++i) {
-                const int k = (head + i) & (N - 1);
-                if (g >= base[k] && g < base[k] + 2 * (j1[k] - j0[k])) return k;
-            }
-            if (done || cnt == N) return -1;
-            Unit U;
-            for (;;) {
-                if (!decode_work<SPLIT, true>(p, unit_of_round(r), cur, U)) { done = true; break; }
-                ++r;
-                if (U.j1 > U.j0) break;                    // items without a key tile hold no slot
-            }
-            if (done) return -1;
-            const int k = (head + cnt) & (N - 1);
-            j0[k] = U.j0;
-            j1[k] = U.j1;
-            base[k] = next_base;
-            next_base += 2 * (U.j1 - U.j0);
-            ++cnt;
-        }
-    }
-    // forget the items that end at or before slot g
-    __device__ void drop_before(int g) {
-        while (cnt > 0 && base[head] + 2 * (j1[head] - j0[head]) <= g) {
-            head = (head + 1) & (N - 1);
-            --cnt;
-        }
-    }
-};
-
-template <class C, bool SPLIT>
-__device__ void mma_issuer3(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bars, uint32_t tmem_any, int w) {
-    volatile int *abort_flag = &bars->abort;
-    const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_any, 0);   // the same in every lane
-    constexpr uint32_t kIdS = C::idesc(kTile, false);
-    constexpr uint32_t kIdPV = C::idesc(C::D, true);
-    constexpr uint32_t kHi = desc_hi(C::SBO, (uint32_t)C::SW_CODE);
-    constexpr uint32_t kTileStep = C::TILE_BYTES >> 4;
-    const uint32_t q_lo = desc_lo(smem_u32(sQ), 16);                 // K-major: LBO unused
-    const uint32_t k_lo = desc_lo(smem_u32(sKV), 16);
-    const uint32_t v_lo = desc_lo(smem_u32(sKV), C::PANEL_BYTES);    // MN-major: LBO = panel stride
-    const uint32_t o_tm = tmem + (w ? C::O_COL1 : C::O_COL0);
-    ItemWindow<SPLIT> win;
-    uint32_t qc = 0;                 // Q tiles of tile 1 - w waited for
-    bool ok = true;
-
-    const uint32_t my_turn = smem_u32(&bars->turn[w]), next_turn = smem_u32(&bars->turn[w ^ 1]);
-    uint32_t tc = 0;
-    auto kv_wait = [&](int f) -> bool {
-        return warp_wait(smem_u32(&bars->kv_full[f % C::NSTAGE]), (uint32_t)(f / C::NSTAGE) & 1, abort_flag);
-    };
-    // Operands of S_g (tile 1 - w) in place: its Q tile (first step of an
-    // item) and K tile.  Returns the item index, -1 past the last slot, or
-    // -2 when a wait gave up.
-    auto prep_s = [&](int g) -> int {
-        const int k = win.find(p, g);
-        if (k < 0) return -1;
-        const int rel = g - win.base[k], t = rel & 1;
-        if ((rel >> 1) == 0) {
-            if (!warp_wait(smem_u32(&bars->q_full[t]), qc & 1, abort_flag)) return -2;
-            ++qc;
-        }
-        return kv_wait(g - t) ? k : -2;
-    };
-    // S_g into region g % 3; the issue turn passes to the other warp
-    // TURN_EARLY MMAs before the end of the group
-    auto issue_s = [&](int k, int g) {
-        const int rel = g - win.base[k], j = win.j0[k] + (rel >> 1), t = rel & 1;
-        const int fk = g - t;                                // fill of K_j
-        const uint32_t s_tm = tmem + (uint32_t)((g % 3) * kTile);
-        const uint32_t qa = q_lo + t * kTileStep, kb = k_lo + (fk % C::NSTAGE) * kTileStep;
+        const bool valid = row < U.sq;
+        if constexpr (SPLIT) {
+            // split-KV: normalised fp32 partial O and its LSE for the combine
+            const int64_t prow = ((int64_t)U.split * p.part_rows + U.q_row + row) * p.H + U.h;
+            float *po = p.part_o + prow * C::D;
+            const float pinv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+            for (int ch = 0; ch < C::D / 32; ++ch) {
+                uint32_t r[32];
+                if (have) {
+                    tmem_ld32(o_tm + 32 * ch, r);
+                    tmem_wait_ld(r);
+                } else {
 #pragma unroll
-        for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-            const uint32_t off =
-                ((kk * C::KSTEP_BYTES / C::SW) * C::PANEL_BYTES + (kk * C::KSTEP_BYTES) % C::SW) >> 4;
-            mma_ss_e<C::FP8>(s_tm, qa + off, kb + off, kHi, kIdS, kk > 0 ? 1u : 0u);
-            if (kk == C::TURN_AT) mbar_arrive_e(next_turn);
-        }
-        tc_commit_e(smem_u32(&bars->s_full[g % 6]));
-        if (j == win.j1[k] - 1) tc_commit_e(smem_u32(&bars->q_empty[t]));
-        tc_commit_e(smem_u32(&bars->kv_empty[fk % C::NSTAGE]));
-    };
-    // O_w (+)= P_g V_j, P from region g % 3 in two halves of 64 keys
-    auto issue_pv = [&](int k, int g) -> bool {
-        const int ij0 = win.j0[k], ij1 = win.j1[k];
-        const int j = ij0 + ((g - win.base[k]) >> 1);
-        const int fv = g - w + 1;                            // fill of V_j
-        const int b6 = g % 6;
-        const uint32_t par = (uint32_t)(g / 6) & 1;
-        const uint32_t s_tm = tmem + (uint32_t)((g % 3) * kTile);
-        const uint32_t vb = v_lo + (fv % C::NSTAGE) * kTileStep;
-        constexpr int HK = C::PV_STEPS / 2;
+                    for (int i = 0; i < 32; ++i) r[i] = 0u;
+                }
+                if (valid) {
+                    float4 *d4 = reinterpret_cast<float4 *>(po + 32 * ch);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            // P was written by the softmax threads (tcgen05.st): order this
-            // thread's MMAs after their fence::before_thread_sync + arrive
-            if (!warp_wait(smem_u32(hf ? &bars->p_full[b6] : &bars->p_half[b6]), par, abort_flag)) return false;
-            tc_fence_after();
-#pragma unroll
-            for (int kx = 0; kx < HK; ++kx) {
-                const int kk = hf * HK + kx;
-                mma_ts_e<C::FP8>(o_tm, s_tm + kk * (C::MMA_K * C::E / 4), vb + ((kk * C::MMA_K * C::SW) >> 4),
-                                 kHi, kIdPV, (j > ij0 || kk > 0) ? 1u : 0u);
+                    for (int i = 0; i < 8; ++i)
+                        d4[i] = make_float4(__uint_as_float(r[4 * i]) * pinv, __uint_as_float(r[4 * i + 1]) * pinv,
+                                            __uint_as_float(r[4 * i + 2]) * pinv, __uint_as_float(r[4 * i + 3]) * pinv);
+                }
             }
+            if (valid) p.part_lse[prow] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+            continue;
         }
-        tc_commit_e(smem_u32(&bars->pv_done[w]));
-        if (j == ij1 - 1) tc_commit_e(smem_u32(&bars->o_full[w]));
-        tc_commit_e(smem_u32(&bars->kv_empty[fv % C::NSTAGE]));
-        return true;
-    };
-
-    // Group q (q = 0, 1, 2, ...) is PV_{q-3} (q >= 3) then S_q; warp (q + 1) & 1
-    // issues it, so the warps take turns group by group and the tensor pipe
-    // runs S_0 S_1 S_2 | PV_0 S_3 | PV_1 S_4 | PV_2 S_5 | ...
-    for (int q = w ^ 1; ok; q += 2) {
-        int kp = -1;
-        if (q >= 3) {
-            kp = win.find(p, q - 3);
-            if (kp < 0) break;                               // no slot left for this warp
-            if (!kv_wait(q - 3 - w + 1)) { ok = false; break; }   // V of PV_{q-3}
-        }
-        const int ks = prep_s(q);
-        if (ks == -2) { ok = false; break; }
-        if (!warp_wait(my_turn, tc & 1, abort_flag)) { ok = false; break; }
-        ++tc;
-        if (q >= 3 && !issue_pv(kp, q - 3)) { ok = false; break; }
-        if (ks >= 0) issue_s(ks, q);
-        else mbar_arrive_e(next_turn);
-        win.drop_before(q - 1);
-    }
-    // no tensor-core operation may be in flight when TMEM is released
-    tc_commit_e(smem_u32(&bars->drain));
-    mbar_wait_drain(smem_u32(&bars->drain), 0);
-}
-
-template <class C, bool SPLIT>
-__device__ void softmax_wg3(const Params &p, Bars *bars, uint32_t tmem, int warp, int lane) {
-    volatile int *abort_flag = &bars->abort;
-    const int t = warp >> 2, wq = warp & 3;
-    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-    const uint32_t o_tm = lane_base + (t ? C::O_COL1 : C::O_COL0);
-    const uint32_t o_bar = smem_u32(&bars->o_full[t]);
-    const uint32_t pv_bar = smem_u32(&bars->pv_done[t]);
-    const uint32_t bar0 = smem_u32(&bars->s_full[0]);
-    constexpr uint32_t kPHalf = offsetof(Bars, p_half) - offsetof(Bars, s_full);
-    constexpr uint32_t kPFull = offsetof(Bars, p_full) - offsetof(Bars, s_full);
-    const float c = p.scale * kLog2e;          // scores in log2 units: s * scale * log2(e)
-    const bool causal = p.mask == FMHA_MASK_CAUSAL;
-    // this tile's slots: g = t, t + 2, ... kept as g % 6 (barrier) and the
-    // parity of g / 6 (its phase); the region is g % 3
-    int b6 = t;
-    uint32_t par = 0;
-    uint32_t o_ph = 0;
-    uint32_t pv_par = 0;                       // phase parity of this tile's next PV
-    bool pv_any = false;                       // a PV of this tile was published before
-    bool ok = true;
-    Cursor cur;
-    for (int r = 0; ok; ++r) {
-        Unit U;
-        if (!decode_work<SPLIT, true>(p, unit_of_round(r), cur, U)) break;
-        const int nu = U.nu[t], j0 = U.j0, j1 = U.j1;
-        const int row = U.q0 + t * kTile + wq * 32 + lane;      // query row within the sequence
-        int key_end = U.sk;                                      // keys [0, key_end) are visible to this row
-        if (causal) key_end = imin(key_end, row + 1 + (p.causal_type == FMHA_CAUSAL_QEND ? U.sk - U.sq : 0));
-        float m_ref = -INFINITY;
-        float l = 0.f;
-        for (int j = j0; j < j1; ++j) {
-            const uint32_t s_tm = lane_base + (uint32_t)((b6 >= 3 ? b6 - 3 : b6) * kTile);
-            const uint32_t sb = bar0 + 8u * (uint32_t)b6;
-            if (!warp_wait(sb, par, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            float s[kTile];
-            float m_raw;
-            if (j >= nu) {                                   // boundary tile (or past this tile's keys)
-                load_s(s_tm, s);
-                mask_s(s, key_end - j * kTile);
-                m_raw = row_max(s);
+        const float inv = l > 0.f ? p.out_scale / l : 0.f;
+        uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) +
+                        (((int64_t)U.q_row + row) * p.H + U.h) * (int64_t)(C::D * C::E);
+#pragma unroll 1
+        for (int ch = 0; ch < C::D / 32; ++ch) {
+            uint32_t r[32];
+            if (have) {
+                tmem_ld32(o_tm + 32 * ch, r);
+                tmem_wait_ld(r);
             } else {
-                m_raw = load_s_max(s_tm, s);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = 0u;
             }
-            const float m_tile = m_raw * c;
-            const bool resc = m_tile > m_ref + kRescaleLog2;
-            float alpha = 1.f;
-            if (resc) {
-                alpha = ex2(m_ref - m_tile);
-                l *= alpha;
-                m_ref = m_tile;
-            }
-            // O_t holds the previous step's PV only once that PV is done; the
-            // wait sits where O_t may be rescaled, late in the step
-            bool failed = false;
-            l += exp_store_publish<C>(s_tm, s, c, m_ref == -INFINITY ? 0.f : -m_ref,
-                                      j > j0 && __any_sync(0xffffffffu, resc), o_tm, alpha, sb + kPHalf,
-                                      sb + kPFull, lane, pv_any ? pv_bar : 0u, pv_par ^ 1u, abort_flag, &failed);
-            if (failed) { ok = false; break; }
-            pv_par ^= 1u;
-            pv_any = true;
-            b6 += 2;
-            if (b6 >= 6) { b6 -= 6; par ^= 1u; }
+            if (valid) store_chunk<C>(orow + ch * 32 * C::E, r, inv);
         }
-        if (!ok) break;
-
-        const bool have = j1 > j0;
-        if (have) {
-            if (!warp_wait(o_bar, o_ph, abort_flag)) { ok = false; break; }
-            o_ph ^= 1;
-            tc_fence_after();
+        if (valid && p.lse) {
+            const int64_t li = p.varlen ? (int64_t)U.h * p.total_length + U.q_row + row
+                                        : ((int64_t)U.b * p.H + U.h) * p.Sq + row;
+            p.lse[li] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
         }
-        epilogue<C, SPLIT>(p, U, row, have, l, m_ref, o_tm);
     }
 }
 
@@ -1419,8 +1313,7 @@ template <class C, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const Params p) {
-    static_assert(C::S_COL1 == C::S_COL0 + kTile && C::TURN_AT >= 0 && C::TURN_EARLY >= 0,
-                  "score regions are 128 columns apart; the turn hand-over is inside the S group");
+    static_assert(C::TURN_AT >= 0 && C::TURN_EARLY >= 0, "the turn hand-over is inside the S group");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sQ = smem;                               // 2 Q tiles
@@ -1432,15 +1325,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_u32(&bars->q_full[t]), 1);
             mbar_init(smem_u32(&bars->q_empty[t]), 1);
+            mbar_init(smem_u32(&bars->s_full[t]), 1);
+            mbar_init(smem_u32(&bars->p_half[t]), 4);   // one arrival per softmax warp
+            mbar_init(smem_u32(&bars->p_full[t]), 4);
             mbar_init(smem_u32(&bars->o_full[t]), 1);
-            mbar_init(smem_u32(&bars->pv_done[t]), 1);
-        }
-        for (int r = 0; r < 6; ++r) {
-            mbar_init(smem_u32(&bars->s_full[r]), 1);
-            mbar_init(smem_u32(&bars->p_half[r]), 4);   // one arrival per softmax warp
-            mbar_init(smem_u32(&bars->p_full[r]), 4);
         }
         mbar_init(smem_u32(&bars->drain), 2);             // one commit per issuing warp
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_u32(&bars->s_free[t]), 128);   // one arrival per softmax thread
+            mbar_init(smem_u32(&bars->pv_done[t]), 1);
+        }
         mbar_init(smem_u32(&bars->turn[0]), 1);
         mbar_init(smem_u32(&bars->turn[1]), 1);
         for (int s = 0; s < C::NSTAGE; ++s) {
@@ -1449,8 +1343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bars->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        // the issuing warp of tile 0's first S takes the first turn
-        mbar_arrive(smem_u32(&bars->turn[C::TRIPLE ? 1 : 0]));
+        mbar_arrive(smem_u32(&bars->turn[0]));            // tile 0's lane issues first
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
@@ -1462,13 +1355,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = bars->tmem_base;
 
     if (warp < kProducerWarp) {
-        if constexpr (C::TRIPLE) softmax_wg3<C, SPLIT>(p, bars, tmem, warp, lane);
-        else softmax_wg<C, SPLIT>(p, bars, tmem, warp, lane);
+        softmax_wg<C, SPLIT>(p, bars, tmem, warp, lane);
     } else if (warp == kProducerWarp) {
         if (lane == 0) producer<C, SPLIT>(p, &tmQ, &tmK, &tmV, sQ, sKV, bars);
+    } else if constexpr (C::PSEP) {
+        mma_issuer_psep<C, SPLIT>(p, sQ, sKV, bars, tmem, warp - kMmaWarp);
     } else {
-        if constexpr (C::TRIPLE) mma_issuer3<C, SPLIT>(p, sQ, sKV, bars, tmem, warp - kMmaWarp);
-        else mma_issuer<C, SPLIT>(p, sQ, sKV, bars, tmem, warp - kMmaWarp);
+        mma_issuer<C, SPLIT>(p, sQ, sKV, bars, tmem, warp - kMmaWarp);
     }
 
     tc_fence_before();
