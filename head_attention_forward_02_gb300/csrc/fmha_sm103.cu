@@ -974,17 +974,47 @@ __device__ void mma_issuer_psep(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars
 // Softmax warpgroups (one thread per query row) and the epilogue
 // ---------------------------------------------------------------------------
 
-// This thread's row of S_t (128 fp32 columns of its TMEM lane).
-__device__ __forceinline__ void load_s(uint32_t s_tm, float (&s)[kTile]) {
+// This thread's row of S_t on a tile with masked elements (keys at local
+// column >= lim get score -inf) and its maximum; the same load-and-reduce
+// order as load_s_max below, with the mask applied to the loaded words.
+__device__ __forceinline__ float load_s_mask_max(uint32_t s_tm, int lim, float (&s)[kTile]) {
+    constexpr uint32_t kNegInf = 0xff800000u;
     uint32_t r0[32], r1[32], r2[32], r3[32];
     tmem_ld32(s_tm, r0);
     tmem_ld32(s_tm + 32, r1);
-    tmem_ld32(s_tm + 64, r2);
-    tmem_ld32(s_tm + 96, r3);
     tmem_wait_ld(r0);
     tmem_wait_ld(r1);
-    tmem_wait_ld(r2);
+    tmem_ld32(s_tm + 64, r2);
+    tmem_ld32(s_tm + 96, r3);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        r0[i] = i >= lim ? kNegInf : r0[i];
+        r1[i] = 32 + i >= lim ? kNegInf : r1[i];
+    }
+    float m8[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        m8[k] = max3(__uint_as_float(r0[k]), __uint_as_float(r0[8 + k]), __uint_as_float(r0[16 + k]));
+        m8[k] = max3(m8[k], __uint_as_float(r0[24 + k]), __uint_as_float(r1[k]));
+        m8[k] = max3(m8[k], __uint_as_float(r1[8 + k]), __uint_as_float(r1[16 + k]));
+        m8[k] = fmaxf(m8[k], __uint_as_float(r1[24 + k]));
+    }
+    float m_lo = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+    tmem_wait_ld_after(r2, m_lo);
     tmem_wait_ld(r3);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        r2[i] = 64 + i >= lim ? kNegInf : r2[i];
+        r3[i] = 96 + i >= lim ? kNegInf : r3[i];
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        m8[k] = max3(__uint_as_float(r2[k]), __uint_as_float(r2[8 + k]), __uint_as_float(r2[16 + k]));
+        m8[k] = max3(m8[k], __uint_as_float(r2[24 + k]), __uint_as_float(r3[k]));
+        m8[k] = max3(m8[k], __uint_as_float(r3[8 + k]), __uint_as_float(r3[16 + k]));
+        m8[k] = fmaxf(m8[k], __uint_as_float(r3[24 + k]));
+    }
+    const float m_hi = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         s[i] = __uint_as_float(r0[i]);
@@ -992,25 +1022,7 @@ __device__ __forceinline__ void load_s(uint32_t s_tm, float (&s)[kTile]) {
         s[64 + i] = __uint_as_float(r2[i]);
         s[96 + i] = __uint_as_float(r3[i]);
     }
-}
-
-// Keys at local column >= lim are invisible to this row: score -inf.
-__device__ __forceinline__ void mask_s(float (&s)[kTile], int lim) {
-#pragma unroll
-    for (int i = 0; i < kTile; ++i)
-        if (i >= lim) s[i] = -INFINITY;
-}
-
-__device__ __forceinline__ float row_max(const float (&s)[kTile]) {
-    float m8[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m8[i] = s[i];
-#pragma unroll
-    for (int i = 8; i < kTile; i += 16) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = max3(m8[k], s[i + k], s[i + 8 + k]);
-    }
-    return max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+    return fmaxf(m_lo, m_hi);
 }
 
 // This thread's row of S_t and its maximum, for a tile with no masked element:
@@ -1209,22 +1221,16 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
             float s[kTile];
             float m_raw;
             if (j >= nu) {                                   // boundary tile
-                load_s(s_tm, s);
-                if constexpr (C::PSEP) {
-                    // S_t is in registers: the next S may overwrite it.  Every
-                    // thread arrives on its own (a lane-0 arrive after a warp
-                    // sync made the compiler spill the live scores)
-                    tc_fence_before();
-                    mbar_arrive(sf_bar);
-                }
-                mask_s(s, key_end - j * kTile);
-                m_raw = row_max(s);
+                m_raw = load_s_mask_max(s_tm, key_end - j * kTile, s);
             } else {
                 m_raw = load_s_max(s_tm, s);
-                if constexpr (C::PSEP) {
-                    tc_fence_before();
-                    mbar_arrive(sf_bar);
-                }
+            }
+            if constexpr (C::PSEP) {
+                // S_t is in registers: the next S may overwrite it.  Every
+                // thread arrives on its own (a lane-0 arrive after a warp
+                // sync made the compiler spill the live scores)
+                tc_fence_before();
+                mbar_arrive(sf_bar);
             }
             const float m_tile = m_raw * c;                  // scale > 0 keeps the argmax
             const bool resc = m_tile > m_ref + kRescaleLog2;

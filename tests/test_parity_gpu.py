@@ -177,3 +177,23 @@ def test_growing_max_forces_rescale(fm, oracle, dtype, mask, impl):
         extra = e4m3_weight_bound(oracle, inp, rows)
     stats = compare(run, oracle, rows, extra=extra)
     print(dtype, mask, impl, stats, None if extra is None else float(extra.max()))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "e4m3"])
+@pytest.mark.parametrize("D", [32, 64, 128])
+def test_single_negative_score_row_is_exact(fm, dtype, D):
+    """Causal q-begin row 0 sees only key 0, so its weight is exactly 1 and
+    O[0] must equal V[0] bit for bit.  With a negative score the row maximum
+    is that negative value; a row maximum taken over anything but the row's
+    own scores would move the reference and round the weight (visibly in
+    e4m3, by one unit in the last place of O)."""
+    inp = fixed_inputs(dtype=dtype, B=1, H=2, H_k=2, Sq=256, Sk=256, D=D, mask="causal", seed=17)
+    q, k = inp.q.float(), inp.k.float()
+    for h in range(2):
+        if float((q[0, 0, h] * k[0, 0, h]).sum()) > 0:        # make q0 . k0 negative
+            inp.q[0, 0, h] = (-q[0, 0, h]).to(inp.q.dtype)
+    run = Run(fm, inp, "tc")
+    assert run.status == 0
+    got = run.o[0, 0].float().cpu()
+    want = inp.v[0, 0].float()
+    assert torch.equal(got, want), (got - want).abs().max().item()
