@@ -504,10 +504,21 @@ __device__ __forceinline__ bool decode_unit(const Params &p, int u, Cursor &cur,
         const int nqb = (p.Sq + kUnitRows - 1) / kUnitRows;
         const int per = p.B * p.H;
         if (u >= per * nqb) return false;
-        const int r = u / per, rem = u - r * per;
-        b = rem / p.H;
-        h = rem - b * p.H;
-        qb = p.mask == FMHA_MASK_CAUSAL ? nqb - 1 - r : r;
+        if (p.mask == FMHA_MASK_CAUSAL) {
+            // causal work grows with the block index: block level by block
+            // level, deepest first, across all heads (heaviest first)
+            const int r = u / per, rem = u - r * per;
+            b = rem / p.H;
+            h = rem - b * p.H;
+            qb = nqb - 1 - r;
+        } else {
+            // every unit has the same work: all blocks of one head in a row,
+            // so the CTAs in flight share that head's K/V in L2
+            const int bh = u / nqb;
+            qb = u - bh * nqb;
+            b = bh / p.H;
+            h = bh - b * p.H;
+        }
         U.sq = p.Sq;
         U.sk = p.Sk;
         U.q_row = b * p.Sq;
