@@ -88,18 +88,6 @@ struct Cfg {
     // from those columns, so the next S is computed while the softmax works.
     // At D = 128 the two O accumulators take the room and P aliases S.
     static constexpr bool PSEP = D <= 64;
-    // One Q tile in flight (ONE_T: e4m3, and 16-bit inputs at D <= 64): the
-    // two tiles of a work item run one after the other on all eight softmax
-    // warps (two per row, 64 keys each), with S and P double-buffered in TMEM
-    // (S_a, S_b, O, P_a, P_b), so the softmax never waits for the MMAs of its
-    // own chain.  K and V tiles are loaded once per tile instead of once per
-    // item; at these tile sizes that stays well inside the L2 bandwidth,
-    // while 16-bit D = 128 would need ~16 of the ~20 TB/s measured.
-    static constexpr bool ONE_T = FP8 || D <= 64;
-    static constexpr int T1_S0 = 0, T1_S1 = kTile, T1_O = 2 * kTile;
-    static constexpr int T1_P0 = 2 * kTile + D, T1_P1 = T1_P0 + 64;
-    static_assert(T1_P1 + 64 <= (int)kTmemCols, "TMEM budget of the one-tile schedule");
-    static constexpr int T1_NKV = TILE_BYTES <= 4096 ? 8 : (TILE_BYTES <= 8192 ? 6 : 4);  // K (and V) ring slots
     // 16-bit inputs pair the ring: stage i holds V_{j-1} and K_j behind one
     // barrier, so an issuing warp waits and releases once per key step
     // (measured +2% at D=128); e4m3 keeps one tile per stage, where V_j is
@@ -120,10 +108,6 @@ struct Cfg {
     static constexpr int P_COL0 = PSEP ? O_COL1 + D : S_COL0, P_COL1 = PSEP ? P_COL0 + 64 : S_COL1;
     static_assert(!PSEP || P_COL1 + 64 <= (int)kTmemCols, "TMEM budget of the P buffers");
     static constexpr int BAR_BYTES = 512;
-    static constexpr int T1_BAR_BYTES = 5120;
-    static constexpr int T1_SMEM_USED = 2 * TILE_BYTES + 2 * T1_NKV * TILE_BYTES + T1_BAR_BYTES;
-    static constexpr int T1_SMEM_BYTES = (T1_SMEM_USED < 120 * 1024 ? 120 * 1024 : T1_SMEM_USED) + 1024;
-    static_assert(!ONE_T || T1_SMEM_BYTES <= 227 * 1024, "shared memory budget of the one-tile schedule");
     static constexpr int SMEM_USED = 2 * TILE_BYTES + NS * TILE_BYTES + BAR_BYTES;
     // at least 120 KB so that a second CTA can never share the SM (TMEM is
     // allocated whole), plus 1 KB to align the tiles for the 128-byte swizzle
@@ -147,22 +131,6 @@ struct Bars {
     uint64_t s_free[2];        // separate P buffers: the softmax warps hold S_t in registers
     uint64_t pv_done[2];       // separate P buffers: PV_t complete (P_t and O_t free)
     uint64_t kv_full[8], kv_empty[8];
-    uint32_t tmem_base;
-    int abort;
-};
-
-// Barriers of the one-tile schedule (global step k: buffer k % 2).
-struct Bars1T {
-    uint64_t q_full[2], q_empty[2];      // Q slot of tile 0 / tile 1 of a work item
-    uint64_t s_full[2], s_free[2];       // S buffer written / read into the softmax registers
-    uint64_t p_lo[2], p_hi[2];           // P buffer keys 0-63 / 64-127 written
-    uint64_t pv_done[2];                 // PV that read P buffer b complete
-    uint64_t o_full, drain;
-    uint64_t xm[2][4];                   // max exchange of the two warps of a row quadrant
-    uint64_t xl[2][4];                   // row-sum exchange at the end of a tile
-    uint64_t k_full[8], k_empty[8], v_full[8], v_empty[8];
-    float xm_val[2][2][kTile];           // [slot][half][row]
-    float xl_val[2][2][kTile];           // [slot][half][row]
     uint32_t tmem_base;
     int abort;
 };
@@ -1355,492 +1323,6 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
 }
 
 // ---------------------------------------------------------------------------
-// One-tile schedule (e4m3 inputs, and 16-bit inputs at D <= 64)
-// ---------------------------------------------------------------------------
-//
-// The two Q tiles of a work item run one after the other.  Global step k
-// (over items, tiles and key tiles) has its S in S buffer k % 2 and its P in
-// P buffer k % 2.  Warp 9 issues S_k as soon as the softmax warps hold
-// S_k-2 in registers; warp 10 issues PV_k as each half of P_k is published.
-// Softmax warp w works on TMEM lane quadrant w % 4 (32 rows) and on keys
-// 64 (w / 4) .. 64 (w / 4) + 63 of each tile; the two warps of a quadrant
-// exchange their half-row maxima through shared memory every step (an
-// mbarrier of 64 arrivals, waited with a bound) and their row sums once per
-// tile, and each rescales and stores its half of the O columns.  A softmax
-// warp overwrites P buffer k % 2 after PV_k-2 is done, and rescales O after
-// PV_k-1 is done (pv_done of each buffer, met in order).
-
-// 16 consecutive TMEM columns of this thread's lane (32x32b shape).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-                 : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
-                 :
-                 : "memory");
-}
-
-// Columns [c0, c0 + W) of this thread's lane of O (fp32 words), W = 32 or 16.
-template <int W>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[W]) {
-    if constexpr (W == 32) {
-        tmem_ld32(taddr, r);
-        tmem_wait_ld(r);
-    } else {
-        tmem_ld16(taddr, r);
-        tmem_wait_ld16(r);
-    }
-}
-
-template <int W>
-__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[W]) {
-    if constexpr (W == 32) tmem_st32(taddr, r);
-    else tmem_st16(taddr, r);
-}
-
-// W output values (W = 32 or 16) scaled by inv, cast and stored with 16-byte stores.
-template <class C, int W>
-__device__ __forceinline__ void store_cols(uint8_t *dst, const uint32_t (&r)[W], float inv) {
-    if constexpr (C::FP8) {
-        uint32_t w[W / 4];
-#pragma unroll
-        for (int i = 0; i < W / 4; ++i)
-            w[i] = pack4_e4m3(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                              __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-        for (int i = 0; i < W / 16; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-    } else {
-        uint32_t w[W / 2];
-#pragma unroll
-        for (int i = 0; i < W / 2; ++i)
-            w[i] = pack2<C::ELEM>(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-        for (int i = 0; i < W / 8; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-    }
-}
-
-template <class C, bool SPLIT>
-__device__ void producer1t(const Params &p, const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
-                           uint8_t *sQ, uint8_t *sK, uint8_t *sV, Bars1T *bars) {
-    volatile int *abort_flag = &bars->abort;
-    constexpr int NKV = C::T1_NKV;
-    prefetch_tmap(tmQ);
-    prefetch_tmap(tmK);
-    prefetch_tmap(tmV);
-    uint32_t f = 0, qload[2] = {0, 0};
-    bool ok = true;
-    Cursor cur;
-    auto load = [&](const CUtensorMap *m, uint32_t dst, uint32_t bar, int h, int row, int b, int row_v) {
-#pragma unroll
-        for (int pn = 0; pn < C::PANELS; ++pn) {
-            if (p.varlen) tma_load_3d(dst + pn * C::PANEL_BYTES, m, bar, pn * C::BOX_D, h, row_v);
-            else tma_load_4d(dst + pn * C::PANEL_BYTES, m, bar, pn * C::BOX_D, h, row, b);
-        }
-    };
-    for (int r = 0; ok; ++r) {
-        Unit U;
-        if (!decode_work<SPLIT>(p, unit_of_round(r), cur, U)) break;
-        for (int t = 0; t < 2; ++t) {
-            if (U.n[t] <= U.j0) continue;                 // tile inactive in this work item
-            if (qload[t] > 0 && !mbar_wait(smem_u32(&bars->q_empty[t]), (qload[t] - 1) & 1, abort_flag)) {
-                ok = false;
-                break;
-            }
-            const uint32_t fb = smem_u32(&bars->q_full[t]);
-            mbar_expect_tx(fb, C::TILE_BYTES);
-            const int row = U.q0 + t * kTile;
-            load(tmQ, smem_u32(sQ + t * C::TILE_BYTES), fb, U.h, row, U.b, U.q_row + row);
-            ++qload[t];
-        }
-        for (int t = 0; t < 2 && ok; ++t) {
-            for (int j = U.j0; j < U.n[t]; ++j) {
-                const int st = f % NKV;
-                const uint32_t rnd = f / NKV;
-                if (rnd > 0 && !mbar_wait(smem_u32(&bars->k_empty[st]), (rnd - 1) & 1, abort_flag)) { ok = false; break; }
-                uint32_t fb = smem_u32(&bars->k_full[st]);
-                mbar_expect_tx(fb, C::TILE_BYTES);
-                load(tmK, smem_u32(sK + st * C::TILE_BYTES), fb, U.g, j * kTile, U.b, U.k_row + j * kTile);
-                if (rnd > 0 && !mbar_wait(smem_u32(&bars->v_empty[st]), (rnd - 1) & 1, abort_flag)) { ok = false; break; }
-                fb = smem_u32(&bars->v_full[st]);
-                mbar_expect_tx(fb, C::TILE_BYTES);
-                load(tmV, smem_u32(sV + st * C::TILE_BYTES), fb, U.g, j * kTile, U.b, U.k_row + j * kTile);
-                ++f;
-            }
-        }
-    }
-    if (ok) {
-        // every slot's last release and every Q slot's last release must have
-        // arrived before the CTA may exit
-        for (int st = 0; st < NKV; ++st) {
-            const uint32_t nf = f > (uint32_t)st ? (f - st + NKV - 1) / NKV : 0;
-            if (nf && (!mbar_wait(smem_u32(&bars->k_empty[st]), (nf - 1) & 1, abort_flag) ||
-                       !mbar_wait(smem_u32(&bars->v_empty[st]), (nf - 1) & 1, abort_flag)))
-                break;
-        }
-        for (int t = 0; t < 2; ++t)
-            if (qload[t] && !mbar_wait(smem_u32(&bars->q_empty[t]), (qload[t] - 1) & 1, abort_flag)) break;
-    } else {
-        // aborted: let the copies already issued land before the CTA exits
-        const uint32_t first = f > (uint32_t)NKV ? f - NKV : 0;
-        for (uint32_t g = first; g <= f; ++g) {
-            mbar_wait_drain(smem_u32(&bars->k_full[g % NKV]), (g / NKV) & 1);
-            mbar_wait_drain(smem_u32(&bars->v_full[g % NKV]), (g / NKV) & 1);
-        }
-        for (int t = 0; t < 2; ++t)
-            if (qload[t]) mbar_wait_drain(smem_u32(&bars->q_full[t]), (qload[t] - 1) & 1);
-    }
-}
-
-// Warp 9: S_k = Q_t K_j^T into S buffer k % 2.
-template <class C, bool SPLIT>
-__device__ void s_issuer1t(const Params &p, uint8_t *sQ, uint8_t *sK, Bars1T *bars, uint32_t tmem_any) {
-    volatile int *abort_flag = &bars->abort;
-    const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_any, 0);
-    constexpr int NKV = C::T1_NKV;
-    constexpr uint32_t kIdS = C::idesc(kTile, false);
-    constexpr uint32_t kHi = desc_hi(C::SBO, (uint32_t)C::SW_CODE);
-    constexpr uint32_t kTileStep = C::TILE_BYTES >> 4;
-    const uint32_t q_lo = desc_lo(smem_u32(sQ), 16), k_lo = desc_lo(smem_u32(sK), 16);
-    uint32_t k = 0, qc[2] = {0, 0};
-    bool ok = true;
-    Cursor cur;
-    for (int r = 0; ok; ++r) {
-        Unit U;
-        if (!decode_work<SPLIT>(p, unit_of_round(r), cur, U)) break;
-        for (int t = 0; t < 2 && ok; ++t) {
-            const int n = U.n[t];
-            for (int j = U.j0; j < n; ++j, ++k) {
-                if (j == U.j0) {
-                    if (!warp_wait(smem_u32(&bars->q_full[t]), qc[t] & 1, abort_flag)) { ok = false; break; }
-                    ++qc[t];
-                }
-                const int st = k % NKV;
-                if (!warp_wait(smem_u32(&bars->k_full[st]), (k / NKV) & 1, abort_flag)) { ok = false; break; }
-                const uint32_t b = k & 1;
-                if (k >= 2) {
-                    // the softmax threads hold S_k-2 in registers
-                    if (!warp_wait(smem_u32(&bars->s_free[b]), ((k - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                }
-                const uint32_t s_tm = tmem + (b ? C::T1_S1 : C::T1_S0);
-                const uint32_t qa = q_lo + t * kTileStep, kb = k_lo + st * kTileStep;
-#pragma unroll
-                for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-                    const uint32_t off =
-                        ((kk * C::KSTEP_BYTES / C::SW) * C::PANEL_BYTES + (kk * C::KSTEP_BYTES) % C::SW) >> 4;
-                    mma_ss_e<C::FP8>(s_tm, qa + off, kb + off, kHi, kIdS, kk > 0 ? 1u : 0u);
-                }
-                tc_commit_e(smem_u32(&bars->s_full[b]));
-                if (j == n - 1) tc_commit_e(smem_u32(&bars->q_empty[t]));
-                tc_commit_e(smem_u32(&bars->k_empty[st]));
-            }
-        }
-    }
-    tc_commit_e(smem_u32(&bars->drain));
-    mbar_wait_drain(smem_u32(&bars->drain), 0);
-}
-
-// Warp 10: O += P_k V_j, each half of P_k as soon as it is published.
-template <class C, bool SPLIT>
-__device__ void pv_issuer1t(const Params &p, uint8_t *sV, Bars1T *bars, uint32_t tmem_any) {
-    volatile int *abort_flag = &bars->abort;
-    const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_any, 0);
-    constexpr int NKV = C::T1_NKV;
-    constexpr uint32_t kIdPV = C::idesc(C::D, true);
-    constexpr uint32_t kHi = desc_hi(C::SBO, (uint32_t)C::SW_CODE);
-    constexpr uint32_t kTileStep = C::TILE_BYTES >> 4;
-    constexpr int HK = C::PV_STEPS / 2;
-    const uint32_t v_lo = desc_lo(smem_u32(sV), C::PANEL_BYTES);
-    const uint32_t o_tm = tmem + C::T1_O;
-    uint32_t k = 0;
-    bool ok = true;
-    Cursor cur;
-    for (int r = 0; ok; ++r) {
-        Unit U;
-        if (!decode_work<SPLIT>(p, unit_of_round(r), cur, U)) break;
-        for (int t = 0; t < 2 && ok; ++t) {
-            const int n = U.n[t];
-            for (int j = U.j0; j < n; ++j, ++k) {
-                const int st = k % NKV;
-                if (!warp_wait(smem_u32(&bars->v_full[st]), (k / NKV) & 1, abort_flag)) { ok = false; break; }
-                const uint32_t b = k & 1, par = (k >> 1) & 1;
-                const uint32_t p_tm = tmem + (b ? C::T1_P1 : C::T1_P0);
-                const uint32_t vb = v_lo + st * kTileStep;
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    if (!warp_wait(smem_u32(hf ? &bars->p_hi[b] : &bars->p_lo[b]), par, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int kx = 0; kx < HK; ++kx) {
-                        const int kk = hf * HK + kx;
-                        mma_ts_e<C::FP8>(o_tm, p_tm + kk * (C::MMA_K * C::E / 4), vb + ((kk * C::MMA_K * C::SW) >> 4),
-                                         kHi, kIdPV, (j > U.j0 || kk > 0) ? 1u : 0u);
-                    }
-                }
-                if (!ok) break;
-                tc_commit_e(smem_u32(&bars->pv_done[b]));
-                if (j == n - 1) tc_commit_e(smem_u32(&bars->o_full));
-                tc_commit_e(smem_u32(&bars->v_empty[st]));
-            }
-        }
-    }
-    tc_commit_e(smem_u32(&bars->drain));
-    mbar_wait_drain(smem_u32(&bars->drain), 0);
-}
-
-// Scores of this thread's row in its 64 columns of S buffer s_tm (hf picks
-// the columns); keys at column >= lim (counted from this half's first
-// column) are masked when `masked`.  Returns the half-row maximum.
-__device__ __forceinline__ float load_half_max(uint32_t s_tm, bool masked, int lim, float (&s)[64]) {
-    constexpr uint32_t kNegInf = 0xff800000u;
-    uint32_t r0[32], r1[32];
-    tmem_ld32(s_tm, r0);
-    tmem_ld32(s_tm + 32, r1);
-    tmem_wait_ld(r0);
-    tmem_wait_ld(r1);
-    if (masked) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            r0[i] = i >= lim ? kNegInf : r0[i];
-            r1[i] = 32 + i >= lim ? kNegInf : r1[i];
-        }
-    }
-    float m8[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        m8[k] = max3(__uint_as_float(r0[k]), __uint_as_float(r0[8 + k]), __uint_as_float(r0[16 + k]));
-        m8[k] = max3(m8[k], __uint_as_float(r0[24 + k]), __uint_as_float(r1[k]));
-        m8[k] = max3(m8[k], __uint_as_float(r1[8 + k]), __uint_as_float(r1[16 + k]));
-        m8[k] = fmaxf(m8[k], __uint_as_float(r1[24 + k]));
-    }
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        s[i] = __uint_as_float(r0[i]);
-        s[32 + i] = __uint_as_float(r1[i]);
-    }
-    return max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-}
-
-template <class C, bool SPLIT>
-__device__ void softmax1t(const Params &p, Bars1T *bars, uint32_t tmem, int warp, int lane) {
-    volatile int *abort_flag = &bars->abort;
-    constexpr int HALF_D = C::D / 2;                   // O columns of this warp
-    constexpr int CW = HALF_D < 32 ? HALF_D : 32;      // O columns per TMEM access
-    constexpr int PW = C::FP8 ? 16 : 32;               // P words of one half row
-    const int q = warp & 3, hf = warp >> 2;
-    const int rloc = q * 32 + lane;                    // row within the tile (TMEM lane)
-    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    const uint32_t o_tm = lane_base + C::T1_O + hf * HALF_D;
-    const float c = p.scale * kLog2e;
-    const bool causal = p.mask == FMHA_MASK_CAUSAL;
-    uint32_t k = 0, o_ph = 0, tcount = 0;
-    bool ok = true;
-    Cursor cur;
-    for (int r = 0; ok; ++r) {
-        Unit U;
-        if (!decode_work<SPLIT>(p, unit_of_round(r), cur, U)) break;
-        for (int t = 0; t < 2 && ok; ++t, ++tcount) {
-            const int n = U.n[t], nu = U.nu[t], j0 = U.j0;
-            const int row = U.q0 + t * kTile + rloc;
-            int key_end = U.sk;
-            if (causal) key_end = imin(key_end, row + 1 + (p.causal_type == FMHA_CAUSAL_QEND ? U.sk - U.sq : 0));
-            float m_ref = -INFINITY, l = 0.f;
-            for (int j = j0; j < n; ++j, ++k) {
-                const uint32_t b = k & 1;
-                if (!warp_wait(smem_u32(&bars->s_full[b]), (k >> 1) & 1, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                float s[64];
-                const float m_half = load_half_max(lane_base + (b ? C::T1_S1 : C::T1_S0) + hf * 64, j >= nu,
-                                                   key_end - j * kTile - hf * 64, s);
-                // S_k is in registers: S buffer b may take S_k+2
-                tc_fence_before();
-                mbar_arrive(smem_u32(&bars->s_free[b]));
-                // the row maximum over both halves
-                bars->xm_val[b][hf][rloc] = m_half;
-                mbar_arrive(smem_u32(&bars->xm[b][q]));
-                if (!warp_wait(smem_u32(&bars->xm[b][q]), (k >> 1) & 1, abort_flag)) { ok = false; break; }
-                const float m_raw = fmaxf(m_half, bars->xm_val[b][hf ^ 1][rloc]);
-                const float m_tile = m_raw * c;
-                const bool resc = m_tile > m_ref + kRescaleLog2;
-                float alpha = 1.f;
-                if (resc) {
-                    alpha = ex2(m_ref - m_tile);
-                    l *= alpha;
-                    m_ref = m_tile;
-                }
-                const bool rescale_o = j > j0 && __any_sync(0xffffffffu, resc);
-                const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
-                uint32_t w[PW];
-                l += exp_half<C>(s, pack_f2(c, c), pack_f2(nm, nm), w);
-                // P buffer b was last read by PV_k-2
-                if (k >= 2) {
-                    if (!warp_wait_inline(smem_u32(&bars->pv_done[b]), ((k - 2) >> 1) & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                }
-                if (rescale_o) {
-                    // O holds PV_k-1 once that PV is done
-                    if (!warp_wait_inline(smem_u32(&bars->pv_done[b ^ 1]), ((k - 1) >> 1) & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int ch = 0; ch < HALF_D / CW; ++ch) {
-                        uint32_t o[CW];
-                        tmem_ld_cols<CW>(o_tm + ch * CW, o);
-#pragma unroll
-                        for (int i = 0; i < CW; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st_cols<CW>(o_tm + ch * CW, o);
-                    }
-                }
-                if constexpr (C::FP8) tmem_st16(lane_base + (b ? C::T1_P1 : C::T1_P0) + hf * 16, w);
-                else tmem_st32(lane_base + (b ? C::T1_P1 : C::T1_P0) + hf * 32, w);
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(smem_u32(hf ? &bars->p_hi[b] : &bars->p_lo[b]));
-            }
-            if (!ok) break;
-
-            // epilogue of tile t: both halves' row sums, then this warp's O columns
-            const bool have = n > j0;
-            if (have) {
-                if (!warp_wait(smem_u32(&bars->o_full), o_ph, abort_flag)) { ok = false; break; }
-                o_ph ^= 1;
-                tc_fence_after();
-            }
-            const uint32_t xs = tcount & 1;
-            bars->xl_val[xs][hf][rloc] = l;
-            mbar_arrive(smem_u32(&bars->xl[xs][q]));
-            if (!warp_wait(smem_u32(&bars->xl[xs][q]), (tcount >> 1) & 1, abort_flag)) { ok = false; break; }
-            const float lt = l + bars->xl_val[xs][hf ^ 1][rloc];
-            const bool valid = row < U.sq;
-            if constexpr (SPLIT) {
-                const int64_t prow = ((int64_t)U.split * p.part_rows + U.q_row + row) * p.H + U.h;
-                float *po = p.part_o + prow * C::D + hf * HALF_D;
-                const float pinv = lt > 0.f ? 1.f / lt : 0.f;
-#pragma unroll 1
-                for (int ch = 0; ch < HALF_D / CW; ++ch) {
-                    uint32_t o[CW];
-                    if (have) tmem_ld_cols<CW>(o_tm + ch * CW, o);
-                    else {
-#pragma unroll
-                        for (int i = 0; i < CW; ++i) o[i] = 0u;
-                    }
-                    if (valid) {
-                        float4 *d4 = reinterpret_cast<float4 *>(po + ch * CW);
-#pragma unroll
-                        for (int i = 0; i < CW / 4; ++i)
-                            d4[i] = make_float4(__uint_as_float(o[4 * i]) * pinv, __uint_as_float(o[4 * i + 1]) * pinv,
-                                                __uint_as_float(o[4 * i + 2]) * pinv, __uint_as_float(o[4 * i + 3]) * pinv);
-                    }
-                }
-                if (valid && hf == 0) p.part_lse[prow] = lt > 0.f ? (m_ref + log2f(lt)) * kLn2 : -INFINITY;
-            } else {
-                const float inv = lt > 0.f ? p.out_scale / lt : 0.f;
-                uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) +
-                                (((int64_t)U.q_row + row) * p.H + U.h) * (int64_t)(C::D * C::E) + hf * HALF_D * C::E;
-#pragma unroll 1
-                for (int ch = 0; ch < HALF_D / CW; ++ch) {
-                    uint32_t o[CW];
-                    if (have) tmem_ld_cols<CW>(o_tm + ch * CW, o);
-                    else {
-#pragma unroll
-                        for (int i = 0; i < CW; ++i) o[i] = 0u;
-                    }
-                    if (valid) store_cols<C, CW>(orow + ch * CW * C::E, o, inv);
-                }
-                if (valid && hf == 0 && p.lse) {
-                    const int64_t li = p.varlen ? (int64_t)U.h * p.total_length + U.q_row + row
-                                                : ((int64_t)U.b * p.H + U.h) * p.Sq + row;
-                    p.lse[li] = lt > 0.f ? (m_ref + log2f(lt)) * kLn2 : -INFINITY;
-                }
-            }
-        }
-    }
-}
-
-template <class C, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, 1)
-    fmha_fwd_sm103_1t_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                             const __grid_constant__ CUtensorMap tmV, const Params p) {
-    static_assert(sizeof(Bars1T) <= C::T1_BAR_BYTES, "barrier block");
-    static_assert(C::T1_NKV <= 8, "ring barriers");
-    // (the two-tile schedule's constants, unused by this one)
-    static_assert(C::TURN_AT >= 0 && C::TURN_EARLY >= 0 && C::NSTAGE > 0 && (C::PAIRED || !C::PAIRED) &&
-                      C::O_COL0 >= 0, "configuration");
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t *sQ = smem;                                          // 2 Q slots
-    uint8_t *sK = smem + 2 * C::TILE_BYTES;                      // K ring
-    uint8_t *sV = sK + C::T1_NKV * C::TILE_BYTES;                // V ring
-    Bars1T *bars = reinterpret_cast<Bars1T *>(sV + C::T1_NKV * C::TILE_BYTES);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&bars->q_full[i]), 1);
-            mbar_init(smem_u32(&bars->q_empty[i]), 1);
-            mbar_init(smem_u32(&bars->s_full[i]), 1);
-            mbar_init(smem_u32(&bars->s_free[i]), 256);         // every softmax thread
-            mbar_init(smem_u32(&bars->p_lo[i]), 128);           // the softmax threads of keys 0-63
-            mbar_init(smem_u32(&bars->p_hi[i]), 128);           // ... of keys 64-127
-            mbar_init(smem_u32(&bars->pv_done[i]), 1);
-            for (int q = 0; q < 4; ++q) {
-                mbar_init(smem_u32(&bars->xm[i][q]), 64);       // the two warps of a quadrant
-                mbar_init(smem_u32(&bars->xl[i][q]), 64);
-            }
-        }
-        mbar_init(smem_u32(&bars->o_full), 1);
-        mbar_init(smem_u32(&bars->drain), 2);                   // one commit per issuing warp
-        for (int st = 0; st < C::T1_NKV; ++st) {
-            mbar_init(smem_u32(&bars->k_full[st]), 1);
-            mbar_init(smem_u32(&bars->k_empty[st]), 1);
-            mbar_init(smem_u32(&bars->v_full[st]), 1);
-            mbar_init(smem_u32(&bars->v_empty[st]), 1);
-        }
-        bars->abort = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == kMmaWarp) {
-        tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = bars->tmem_base;
-
-    if (warp < kProducerWarp) {
-        softmax1t<C, SPLIT>(p, bars, tmem, warp, lane);
-    } else if (warp == kProducerWarp) {
-        if (lane == 0) producer1t<C, SPLIT>(p, &tmQ, &tmK, &tmV, sQ, sK, sV, bars);
-    } else if (warp == kMmaWarp) {
-        s_issuer1t<C, SPLIT>(p, sQ, sK, bars, tmem);
-    } else {
-        pv_issuer1t<C, SPLIT>(p, sV, bars, tmem);
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == kMmaWarp) {
-        __syncwarp();
-        tmem_dealloc(tmem, kTmemCols);
-    }
-}
-
-// ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
 
@@ -1849,7 +1331,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const Params p) {
     static_assert(C::TURN_AT >= 0 && C::TURN_EARLY >= 0, "the turn hand-over is inside the S group");
-    static_assert(C::T1_S0 == 0 && C::T1_S1 == kTile && C::T1_O == 2 * kTile, "one-tile TMEM layout");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sQ = smem;                               // 2 Q tiles
@@ -1986,22 +1467,12 @@ int launch_cfg(const Params &p, cudaStream_t stream) {
     const int grid = (int)(units < nsm ? units : nsm);
     if (grid <= 0) return FMHA_OK;
     // split-KV is a separate instantiation so the plain kernel keeps its code
-    if constexpr (C::ONE_T) {
-        auto kern = p.part_o ? fmha_fwd_sm103_1t_kernel<C, true> : fmha_fwd_sm103_1t_kernel<C, false>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::T1_SMEM_BYTES) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            return FMHA_ERR_CUDA;
-        }
-        kern<<<grid, kThreads, C::T1_SMEM_BYTES, stream>>>(tq, tk, tv, p);
-    } else {
-        auto kern = p.part_o ? fmha_fwd_sm103_kernel<C, true> : fmha_fwd_sm103_kernel<C, false>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess) {
-            cudaGetLastError();
-            return FMHA_ERR_CUDA;
-        }
-        kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+    auto kern = p.part_o ? fmha_fwd_sm103_kernel<C, true> : fmha_fwd_sm103_kernel<C, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess) {
+        cudaGetLastError();
+        return FMHA_ERR_CUDA;
     }
+    kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
     return FMHA_OK;
 }
