@@ -669,7 +669,8 @@ def time_gen_oracle(inp, target_s: float):
     import oracle
     oracle.build()
     w = inp.w
-    odt = oracle.BF16 if w.dtype == "bf16" else oracle.F16
+    odt = {"bf16": oracle.BF16, "f16": oracle.F16, "e4m3": oracle.E4M3}[w.dtype]
+    esz = 1 if w.dtype == "e4m3" else 2
     threads = cpu_threads()
     n, total_b, total_t = 1, 0.0, 0.0
     while True:
@@ -681,7 +682,7 @@ def time_gen_oracle(inp, target_s: float):
         oracle.gen_fwd(*args, odt, n, w.H, w.H_k, 128, n, w.S_max, sl, None, 128 ** -0.5, 1.0,
                        threads=threads)
         dt = time.perf_counter() - t
-        total_b, total_t = gen_bytes(n, w.H, w.H_k, sl.tolist(), w.insert, 2), dt
+        total_b, total_t = gen_bytes(n, w.H, w.H_k, sl.tolist(), w.insert, esz), dt
         if dt >= target_s or n >= w.B:
             return total_b, total_t, n, threads
         n = min(w.B, max(n + 1, int(n * target_s / max(dt, 1e-3))))
@@ -814,7 +815,8 @@ def run_gen_reference(args, rank, world):
     oracle.build()
     w = wl.GEN_CONFIGS[args.gen_config]
     inp = wl.generate_gen(w)
-    odt = oracle.BF16 if w.dtype == "bf16" else oracle.F16
+    odt = {"bf16": oracle.BF16, "f16": oracle.F16, "e4m3": oracle.E4M3}[w.dtype]
+    esz = 1 if w.dtype == "e4m3" else 2
     threads = cpu_threads()
 
     def one(b):
@@ -823,7 +825,7 @@ def run_gen_reference(args, rank, world):
                        wl.bits(inp.k_new[b:b + 1]) if inp.k_new is not None else None,
                        wl.bits(inp.v_new[b:b + 1]) if inp.v_new is not None else None, odt, 1, w.H, w.H_k,
                        128, 1, w.S_max, sl, None, 128 ** -0.5, 1.0, threads=threads)
-        return gen_bytes(1, w.H, w.H_k, sl.tolist(), w.insert, 2)
+        return gen_bytes(1, w.H, w.H_k, sl.tolist(), w.insert, esz)
 
     for i in range(args.warmup):
         one(i % w.B)

@@ -8,15 +8,18 @@
 // cached tokens, the keys are K_cache[e, 0..L-1, g] and, unless the call is
 // cache-only, the new token's K_new[b, g], which is also written into the
 // cache at row L (V alike); O[b, h] = softmax(scale * q[b, h] K^T) V.  The
-// page fixes head dim 128 and one query-head group per thread block.
+// page fixes head dim 128 and one query-head group per thread block.  Element
+// types: fp16, bf16 and fp8 e4m3 (kind::f8f6f4 MMAs; the weights P are
+// rounded to e4m3 before P.V, their row sum is kept in fp32).
 //
 // The work is memory bound: every cached K/V byte is read once, and a group of
 // G <= 32 query heads does 4 * G flops per cached element pair.  The design
 // therefore aims at HBM bandwidth: the key range of every (sequence, kv head)
 // is cut into chunks so that all SMs stream at once, each CTA keeps three
-// 64 KB K/V stages in flight through TMA, and the contraction runs on the
-// tensor cores with the roles swapped so that the small head group is the N
-// dimension: S^T = K Q^T (M = 128 keys, N = 32 padded heads, K = 128) and
+// K/V stages (64 KB, or 32 KB for e4m3) in flight through TMA, and the
+// contraction runs on the tensor cores with the roles swapped so that the
+// small head group is the N dimension:
+// S^T = K Q^T (M = 128 keys, N = 32 padded heads, K = 128) and
 // O^T = V^T P^T (M = 128 = head dim, N = 32, K = 128 keys).  Thread i of the
 // softmax warps owns key i of a tile (TMEM lane i) and, in the epilogue, head
 // dimension i of O^T.  The row maximum is kept lazily per head (rescale only
@@ -25,6 +28,7 @@
 // Each chunk writes a normalised fp32 partial O and its LSE; a merge kernel
 // combines the chunks of every (b, h) by their LSE weights.
 #include <cuda.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -46,26 +50,39 @@ constexpr int kSoftWarps = 4;           // warps 0-3: softmax and epilogue
 constexpr int kProdWarp = 4;            // TMA producer (lane 0), cache insert
 constexpr int kMmaWarp = 5;             // tcgen05.mma issuer (whole warp, one elected lane), owns TMEM
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 64;      // S^T in [0, 32), O^T in [32, 64)
+constexpr uint32_t kTmemCols = 128;     // S^T buffers in [0, 32) and [32, 64), O^T in [64, 96)
 constexpr int kPanelBytes = kKT * 128;  // 128 rows of one 128-byte swizzled panel
-constexpr int kTileBytes = 2 * kPanelBytes;           // 128 keys x 128 dims x 16 bit
 constexpr int kQPanelBytes = kNP * 128;
-constexpr int kQBytes = 2 * kQPanelBytes;             // 32 heads x 128 dims x 16 bit
 constexpr int kQSlots = 2;                            // Q tiles of consecutive work items
-constexpr int kStageBytes = 2 * kTileBytes;           // K tile, then V tile
-constexpr int kPBytes = kKT * kNP * 2;                // P^T: 128 keys x 32 heads x 16 bit
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQSlots * kQBytes;
-constexpr int kOffP = kOffKV + kNS * kStageBytes;
-constexpr int kOffBars = kOffP + kPBytes;
-constexpr int kSmemBytes = kOffBars + 1024 + 1024;    // barriers and scratch, 1 KB alignment
+
+// Sizes and layouts of one element type: 16-bit (f16, bf16) or e4m3.  A 128-dim
+// row is two 128-byte swizzle panels of 64 elements, or one of 128.
+template <int ELEM>
+struct GenCfg {
+    static constexpr bool FP8 = ELEM == FMHA_E4M3;
+    static constexpr int E = FP8 ? 1 : 2;                 // bytes per element
+    static constexpr int PANELS = kD * E / 128;
+    static constexpr int BOX = 128 / E;                   // elements per panel row
+    static constexpr int TILE_BYTES = PANELS * kPanelBytes;   // 128 keys x 128 dims
+    static constexpr int Q_BYTES = PANELS * kQPanelBytes;     // 32 heads x 128 dims
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;        // K tile, then V tile
+    static constexpr int P_ROW = kNP * E;                 // bytes of one key's P^T row (32 heads)
+    static constexpr int P_BYTES = kKT * P_ROW;           // one of the two P^T buffers
+    static constexpr uint64_t P_SWZ = FP8 ? 6 : 4;        // 32-byte or 64-byte swizzle of P^T
+    static constexpr int MMA_K = FP8 ? 32 : 16;           // K of one tcgen05.mma
+    static constexpr uint32_t FMT = ELEM == FMHA_BF16 ? 1u : 0u;   // kind::f16: f16 0, bf16 1; f8f6f4: e4m3 0
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_KV = OFF_Q + kQSlots * Q_BYTES;
+    static constexpr int OFF_P = OFF_KV + kNS * STAGE_BYTES;
+    static constexpr int OFF_BARS = OFF_P + 2 * P_BYTES;
+    static constexpr int SMEM_BYTES = OFF_BARS + 1024 + 1024;    // barriers and scratch, 1 KB alignment
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
 constexpr unsigned long long kTimeoutNs = 4000000000ull;
 constexpr unsigned long long kDrainNs = 200000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;    // rescale when a head's max grows by more than 2^8
-
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct GenParams {
     const void *q, *k_new, *v_new;      // q [B, H, D]; new K/V [B, H_k, D] (insert mode)
@@ -89,7 +106,8 @@ struct GenSched {
 };
 
 struct GenBars {
-    uint64_t q_full[kQSlots], q_empty[kQSlots], s_full, p_full, o_full, drain;
+    uint64_t q_full[kQSlots], q_empty[kQSlots], o_full, drain;
+    uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];   // per S^T / P^T buffer
     uint64_t kv_full[kNS], kv_empty[kNS];
     uint32_t tmem_base;
     int abort;
@@ -201,12 +219,21 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 
 // Warp-collective forms: the whole (converged) warp executes them with
 // warp-uniform operands and one elected lane issues the instruction.
+template <bool FP8>
 __device__ __forceinline__ void mma_ss_e(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
+    if constexpr (FP8) {
+        asm volatile(
+            "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(acc)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(acc)
+            : "memory");
+    }
 }
 
 __device__ __forceinline__ void tc_commit_e(uint32_t bar) {
@@ -222,7 +249,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, r);
 }
 
-// Instruction descriptor: fp32 accumulator, A/B format (0 = f16, 1 = bf16),
+// Instruction descriptor: fp32 accumulator, A/B format (kind::f16: 0 = f16,
+// 1 = bf16; kind::f8f6f4: 0 = e4m3),
 // A and B major-ness (0 = K-major, 1 = MN-major), N, M = 128.
 __host__ __device__ constexpr uint32_t gen_idesc(uint32_t fmt, bool a_mn, bool b_mn) {
     return (1u << 4) | (fmt << 7) | (fmt << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
@@ -308,6 +336,13 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     if constexpr (BF) asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     else asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// four values to e4m3 (round to nearest even, saturating), first value in the low byte
+__device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
 }
 
 // ---------------------------------------------------------------------------
@@ -432,8 +467,10 @@ __device__ bool gen_next(const GenParams &p, const GenSched &sc, GenCursor &cur,
 
 // TMA producer: per item, the new token's row into the cache (when this chunk
 // holds it), the 32-head Q tile, then the chunk's K/V tiles into the ring.
+template <int ELEM>
 __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUtensorMap *tmQ,
                              const CUtensorMap *tmK, const CUtensorMap *tmV, uint8_t *smem, GenBars *bars) {
+    using C = GenCfg<ELEM>;
     volatile int *abort_flag = &bars->abort;
     prefetch_tmap(tmQ);
     prefetch_tmap(tmK);
@@ -445,16 +482,16 @@ __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUten
         GenItem it;
         if (!gen_next(p, sc, cur, it, true)) break;
         if (p.insert && it.len_ok && it.entry >= 0 && it.L >= it.k0 && it.L < it.k1) {
-            // 256-byte K and V rows of the new token; the async proxy (TMA)
-            // reads row L below, so order these generic writes before it
-            const int64_t src = ((int64_t)it.b * p.H_k + it.g) * kD;
-            const int64_t dst = (((int64_t)it.entry * p.S_max + it.L) * p.H_k + it.g) * kD;
-            const uint4 *kn = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.k_new) + src);
-            const uint4 *vn = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.v_new) + src);
-            uint4 *kc = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.k_cache) + dst);
-            uint4 *vc = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.v_cache) + dst);
+            // K and V rows of the new token (128 elements); the async proxy
+            // (TMA) reads row L below, so order these generic writes before it
+            const int64_t src = ((int64_t)it.b * p.H_k + it.g) * kD * C::E;
+            const int64_t dst = (((int64_t)it.entry * p.S_max + it.L) * p.H_k + it.g) * kD * C::E;
+            const uint4 *kn = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(p.k_new) + src);
+            const uint4 *vn = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(p.v_new) + src);
+            uint4 *kc = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.k_cache) + dst);
+            uint4 *vc = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.v_cache) + dst);
 #pragma unroll 4
-            for (int i = 0; i < kD * 2 / 16; ++i) {
+            for (int i = 0; i < kD * C::E / 16; ++i) {
                 kc[i] = kn[i];
                 vc[i] = vn[i];
             }
@@ -469,10 +506,11 @@ __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUten
             break;
         }
         const uint32_t qb = smem_u32(&bars->q_full[qs]);
-        mbar_expect_tx(qb, kQBytes);
+        mbar_expect_tx(qb, C::Q_BYTES);
         const int qrow = it.b * p.H + it.g * p.G;
-        tma_load_2d(smem_u32(smem + kOffQ + qs * kQBytes), tmQ, qb, 0, qrow);
-        tma_load_2d(smem_u32(smem + kOffQ + qs * kQBytes + kQPanelBytes), tmQ, qb, 64, qrow);
+#pragma unroll
+        for (int pn = 0; pn < C::PANELS; ++pn)
+            tma_load_2d(smem_u32(smem + C::OFF_Q + qs * C::Q_BYTES + pn * kQPanelBytes), tmQ, qb, pn * C::BOX, qrow);
         ++qn;
         for (int k = it.k0; k < it.k1; k += kKT) {
             const int st = fill % kNS;
@@ -482,13 +520,13 @@ __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUten
                 break;
             }
             const uint32_t fb = smem_u32(&bars->kv_full[st]);
-            mbar_expect_tx(fb, kStageBytes);
-            const uint32_t dst = smem_u32(smem + kOffKV + st * kStageBytes);
+            mbar_expect_tx(fb, C::STAGE_BYTES);
+            const uint32_t dst = smem_u32(smem + C::OFF_KV + st * C::STAGE_BYTES);
             const int e = it.entry >= 0 ? it.entry : p.B_cache;   // out of range: zero fill
 #pragma unroll
-            for (int pn = 0; pn < 2; ++pn) {
-                tma_load_4d(dst + pn * kPanelBytes, tmK, fb, pn * 64, it.g, k, e);
-                tma_load_4d(dst + kTileBytes + pn * kPanelBytes, tmV, fb, pn * 64, it.g, k, e);
+            for (int pn = 0; pn < C::PANELS; ++pn) {
+                tma_load_4d(dst + pn * kPanelBytes, tmK, fb, pn * C::BOX, it.g, k, e);
+                tma_load_4d(dst + C::TILE_BYTES + pn * kPanelBytes, tmV, fb, pn * C::BOX, it.g, k, e);
             }
             ++fill;
         }
@@ -510,23 +548,49 @@ __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUten
     }
 }
 
-// MMA issuer (one warp, one elected lane): per tile, S^T = K Q^T, then (after
-// the softmax wrote P^T) O^T += V^T P^T.  The single issuer keeps the tensor pipe in
-// order, so "S^T of tile j+1 complete" implies "PV of tile j complete": the
-// softmax may then rewrite P^T and rescale O^T without another barrier.
-template <bool BF>
+// MMA issuer (one warp, one elected lane).  S^T and P^T are double-buffered
+// (buffer = tile counter mod 2), so S^T of tile j+1 is issued before P.V of
+// tile j and the softmax of tile j+1 overlaps the tensor-core work of tile j:
+// per tile, S^T_j = K_j Q^T into buffer j % 2 once the softmax has read S^T_j-2
+// out of it, then O^T += V^T_j-1 P^T_j-1 once the softmax has written P^T_j-1.
+// The last tile of a work item issues its own P.V before the next item starts,
+// so the epilogue never waits for the next item's loads.
+template <int ELEM>
 __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, GenBars *bars, uint32_t tmem_any) {
+    using C = GenCfg<ELEM>;
     // the whole warp runs this loop converged, with warp-uniform values; one
     // elected lane issues each MMA and commit
     volatile int *abort_flag = &bars->abort;
     const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_any, 0);   // the same in every lane
-    constexpr uint32_t kIdS = gen_idesc(BF ? 1u : 0u, false, false);
-    constexpr uint32_t kIdPV = gen_idesc(BF ? 1u : 0u, true, true);
-    const uint32_t s_tm = tmem, o_tm = tmem + kNP;
-    const uint64_t q_desc0 = smem_desc(smem_u32(smem + kOffQ), 16, 1024, 2);
-    const uint64_t p_desc = smem_desc(smem_u32(smem + kOffP), kPBytes, 8 * 64, 4);   // MN-major, 64-byte rows
-    uint32_t cons = 0, qn = 0, pn = 0;
+    constexpr uint32_t kIdS = gen_idesc(C::FMT, false, false);
+    constexpr uint32_t kIdPV = gen_idesc(C::FMT, true, true);
+    const uint32_t o_tm = tmem + 2 * kNP;
+    const uint64_t q_desc0 = smem_desc(smem_u32(smem + C::OFF_Q), 16, 1024, 2);
+    // P^T: MN-major, one swizzled row of 32 heads per key (64 or 32 bytes)
+    const uint64_t p_desc0 = smem_desc(smem_u32(smem + C::OFF_P), C::P_BYTES, 8 * C::P_ROW, C::P_SWZ);
+    uint32_t cons = 0, qn = 0;
     bool ok = true;
+
+    // P.V of tile counter j (stage st); `first` starts the item's O^T
+    auto issue_pv = [&](uint32_t j, int st, bool first) -> bool {
+        const uint32_t b = j & 1;
+        if (!warp_wait(smem_u32(&bars->p_full[b]), (j >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        // O^T: A = V tile MN-major (M = head dim over the panels, LBO = panel
+        // stride), B = P^T MN-major (32 heads in one swizzled row per key);
+        // each k-step is MMA_K keys
+        const uint32_t kaddr = smem_u32(smem + C::OFF_KV + st * C::STAGE_BYTES);
+        const uint64_t v_desc = smem_desc(kaddr + C::TILE_BYTES, kPanelBytes, 1024, 2);
+        const uint64_t p_desc = p_desc0 + ((b * C::P_BYTES) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kKT / C::MMA_K; ++kk)
+            mma_ss_e<C::FP8>(o_tm, v_desc + ((kk * C::MMA_K * 128) >> 4),
+                             p_desc + ((kk * C::MMA_K * C::P_ROW) >> 4), kIdPV, (!first || kk > 0) ? 1u : 0u);
+        tc_commit_e(smem_u32(&bars->pv_done[b]));
+        tc_commit_e(smem_u32(&bars->kv_empty[st]));
+        return true;
+    };
+
     GenCursor cur;
     while (ok) {
         GenItem it;
@@ -534,45 +598,43 @@ __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, G
         const int qs = qn % kQSlots;
         if (!warp_wait(smem_u32(&bars->q_full[qs]), (qn / kQSlots) & 1, abort_flag)) break;
         ++qn;
-        const uint64_t q_desc = q_desc0 + ((qs * kQBytes) >> 4);
+        const uint64_t q_desc = q_desc0 + ((qs * C::Q_BYTES) >> 4);
         bool first = true;
+        int prev_st = 0;
         for (int k = it.k0; k < it.k1; k += kKT) {
             const int st = cons % kNS;
-            if (!warp_wait(smem_u32(&bars->kv_full[st]), (cons / kNS) & 1, abort_flag)) {
+            const uint32_t b = cons & 1;
+            if (!warp_wait(smem_u32(&bars->kv_full[st]), (cons / kNS) & 1, abort_flag) ||
+                (cons >= 2 && !warp_wait(smem_u32(&bars->s_free[b]), ((cons - 2) >> 1) & 1, abort_flag))) {
                 ok = false;
                 break;
             }
-            ++cons;
-            const uint32_t kaddr = smem_u32(smem + kOffKV + st * kStageBytes);
+            tc_fence_after();
+            const uint32_t kaddr = smem_u32(smem + C::OFF_KV + st * C::STAGE_BYTES);
             // S^T: A = K tile (K-major, 128 keys), B = Q tile (K-major, 32 heads);
-            // each k-step is 16 dims = 32 bytes within a 128-byte panel row
+            // each k-step (16 dims of 16 bits or 32 of 8) is 32 bytes within a
+            // 128-byte panel row
             const uint64_t k_desc = smem_desc(kaddr, 16, 1024, 2);
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
+            for (int kk = 0; kk < kD / C::MMA_K; ++kk) {
                 const uint32_t koff = (kk * 32 / 128) * kPanelBytes + (kk * 32) % 128;
                 const uint32_t qoff = (kk * 32 / 128) * kQPanelBytes + (kk * 32) % 128;
-                mma_ss_e(s_tm, k_desc + (koff >> 4), q_desc + (qoff >> 4), kIdS, kk > 0 ? 1u : 0u);
+                mma_ss_e<C::FP8>(tmem + b * kNP, k_desc + (koff >> 4), q_desc + (qoff >> 4), kIdS,
+                                 kk > 0 ? 1u : 0u);
             }
             if (k + kKT >= it.k1) tc_commit_e(smem_u32(&bars->q_empty[qs]));
-            tc_commit_e(smem_u32(&bars->s_full));
-            if (!warp_wait(smem_u32(&bars->p_full), pn & 1, abort_flag)) {
+            tc_commit_e(smem_u32(&bars->s_full[b]));
+            if (!first && !issue_pv(cons - 1, prev_st, k - kKT == it.k0)) {
                 ok = false;
                 break;
             }
-            ++pn;
-            tc_fence_after();
-            // O^T: A = V tile MN-major (M = head dim over two 64-wide panels,
-            // LBO = panel stride), B = P^T MN-major (32 heads in one 64-byte
-            // swizzled row per key); each k-step is 16 keys
-            const uint64_t v_desc = smem_desc(kaddr + kTileBytes, kPanelBytes, 1024, 2);
-#pragma unroll
-            for (int kk = 0; kk < kKT / 16; ++kk)
-                mma_ss_e(o_tm, v_desc + ((kk * 16 * 128) >> 4), p_desc + ((kk * 16 * 64) >> 4), kIdPV,
-                       (!first || kk > 0) ? 1u : 0u);
-            tc_commit_e(smem_u32(&bars->kv_empty[st]));
+            prev_st = st;
             first = false;
+            ++cons;
         }
         if (!ok) break;
+        // the item's last P.V (none for an item without keys), then O^T is complete
+        if (!first && !issue_pv(cons - 1, prev_st, it.k1 - it.k0 <= kKT)) break;
         tc_commit_e(smem_u32(&bars->o_full));
     }
     // no tensor-core operation may be in flight when TMEM is released
@@ -582,15 +644,16 @@ __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, G
 
 // Softmax and epilogue: thread t of warps 0-3 owns key t of every tile (TMEM
 // lane t of S^T) and head dimension t of O^T.
-template <bool BF>
+template <int ELEM>
 __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *smem, GenBars *bars, uint32_t tmem,
                             int warp, int lane) {
+    using C = GenCfg<ELEM>;
     volatile int *abort_flag = &bars->abort;
     const int t = warp * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const uint32_t s_tm = lane_base, o_tm = lane_base + kNP;
-    uint8_t *prow = smem + kOffP + t * 64;      // this key's P^T row (64-byte swizzle)
-    uint32_t sph = 0, oph = 0, cons = 0;
+    const uint32_t o_tm = lane_base + 2 * kNP;
+    uint8_t *prow0 = smem + C::OFF_P + t * C::P_ROW;     // this key's P^T row in buffer 0
+    uint32_t oph = 0, cons = 0;
     GenCursor cur;
     for (;;) {
         GenItem it;
@@ -603,18 +666,23 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
         }
         bool ok = true, first = true;
         for (int k = it.k0; k < it.k1; k += kKT) {
-            const bool got = mbar_wait(smem_u32(&bars->s_full), sph, abort_flag);
-            sph ^= 1;
+            // S^T_j and P^T_j use buffer j % 2.  The commit that completes
+            // S^T_j also covers P.V_j-2, issued before it by the same thread,
+            // so P^T buffer j % 2 is free to rewrite once S^T_j is here.
+            const uint32_t b = cons & 1;
+            const bool got = mbar_wait(smem_u32(&bars->s_full[b]), (cons >> 1) & 1, abort_flag);
             if (!soft_all(got)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const int st = cons % kNS;
-            ++cons;
+            const uint32_t j = cons++;
             uint32_t sr[32];
-            tmem_ld32(s_tm, sr);
+            tmem_ld32(lane_base + b * kNP, sr);
             tmem_wait_ld(sr);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars->s_free[b]));   // S^T buffer b may take S^T_j+2
             const bool valid = k + t < it.k1;
             float s[kNP];
             bool need = false;
@@ -648,8 +716,14 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
                 }
                 soft_sync();   // the scratch row may be rewritten after this
                 if (!first) {
-                    // O^T holds the PV of the previous tile (complete: this
-                    // tile's S^T was issued after it); row t, one column per head
+                    // O^T holds the P.V of the previous tile once it is done;
+                    // row t, one column per head
+                    const bool pv = mbar_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag);
+                    if (!soft_all(pv)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     uint32_t orr[32];
                     tmem_ld32(o_tm, orr);
                     tmem_wait_ld(orr);
@@ -659,28 +733,40 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
                     rescaled = true;
                 }
             }
-            // P^T row of key t: 32 heads, 64 bytes in four 16-byte chunks
-            // placed by the 64-byte swizzle (chunk index ^= (row / 2) % 4)
-            uint32_t w[16];
+            // P^T row of key t: 32 heads in 16-byte chunks placed by the
+            // swizzle of the row (64-byte rows: chunk ^= (row / 2) % 4;
+            // 32-byte rows: chunk ^= (row / 4) % 2)
+            float pv[kNP];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float a = m[2 * i] == -INFINITY ? 0.f : ex2(s[2 * i] - m[2 * i]);
-                const float b = m[2 * i + 1] == -INFINITY ? 0.f : ex2(s[2 * i + 1] - m[2 * i + 1]);
-                l[2 * i] += a;
-                l[2 * i + 1] += b;
-                w[i] = pack2<BF>(a, b);
+            for (int h = 0; h < kNP; ++h) {
+                pv[h] = m[h] == -INFINITY ? 0.f : ex2(s[h] - m[h]);
+                l[h] += pv[h];
             }
+            uint8_t *prow = prow0 + b * C::P_BYTES;
+            if constexpr (C::FP8) {
+                uint32_t w[8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                *reinterpret_cast<uint4 *>(prow + ((c ^ ((t >> 1) & 3)) << 4)) =
-                    make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                for (int i = 0; i < 8; ++i) w[i] = pack4_e4m3(pv[4 * i], pv[4 * i + 1], pv[4 * i + 2], pv[4 * i + 3]);
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+                    *reinterpret_cast<uint4 *>(prow + ((c ^ ((t >> 2) & 1)) << 4)) =
+                        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+            } else {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w[i] = pack2<ELEM == FMHA_BF16>(pv[2 * i], pv[2 * i + 1]);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4 *>(prow + ((c ^ ((t >> 1) & 3)) << 4)) =
+                        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+            }
             if (!valid) {
                 // a key past the chunk's end: its V row (stale cache contents,
                 // possibly not finite) is zeroed so that P = 0 contributes 0
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                uint8_t *vrow = smem + kOffKV + st * kStageBytes + kTileBytes + t * 128;
+                uint8_t *vrow = smem + C::OFF_KV + st * C::STAGE_BYTES + C::TILE_BYTES + t * 128;
 #pragma unroll
-                for (int pn = 0; pn < 2; ++pn)
+                for (int pn = 0; pn < C::PANELS; ++pn)
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         *reinterpret_cast<uint4 *>(vrow + pn * kPanelBytes + ((c ^ (t & 7)) << 4)) =
@@ -692,7 +778,7 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
             if (rescaled) tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+            if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[b]));
             first = false;
         }
         if (!ok) break;
@@ -729,21 +815,25 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
     }
 }
 
-template <bool BF>
+template <int ELEM>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_gen_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const GenParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    GenBars *bars = reinterpret_cast<GenBars *>(smem + kOffBars);
+    GenBars *bars = reinterpret_cast<GenBars *>(smem + GenCfg<ELEM>::OFF_BARS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kQSlots; ++i) {
             mbar_init(smem_u32(&bars->q_full[i]), 1);
             mbar_init(smem_u32(&bars->q_empty[i]), 1);
         }
-        mbar_init(smem_u32(&bars->s_full), 1);
-        mbar_init(smem_u32(&bars->p_full), kSoftWarps);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bars->s_full[b]), 1);
+            mbar_init(smem_u32(&bars->s_free[b]), kSoftWarps * 32);
+            mbar_init(smem_u32(&bars->p_full[b]), kSoftWarps);
+            mbar_init(smem_u32(&bars->pv_done[b]), 1);
+        }
         mbar_init(smem_u32(&bars->o_full), 1);
         mbar_init(smem_u32(&bars->drain), 1);
         for (int s = 0; s < kNS; ++s) {
@@ -764,11 +854,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = bars->tmem_base;
     const GenSched sc = bars->sched;
     if (warp < kSoftWarps) {
-        gen_softmax<BF>(p, sc, smem, bars, tmem, warp, lane);
+        gen_softmax<ELEM>(p, sc, smem, bars, tmem, warp, lane);
     } else if (warp == kProdWarp) {
-        if (lane == 0) gen_producer(p, sc, &tmQ, &tmK, &tmV, smem, bars);
+        if (lane == 0) gen_producer<ELEM>(p, sc, &tmQ, &tmK, &tmV, smem, bars);
     } else {
-        gen_mma<BF>(p, sc, smem, bars, tmem);
+        gen_mma<ELEM>(p, sc, smem, bars, tmem);
     }
     tc_fence_before();
     __syncthreads();
@@ -786,7 +876,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kMergeThreads = 256;
 constexpr int kMergeGroups = kMergeThreads / 32;
 
-template <bool BF>
+template <int ELEM>
 __global__ void __launch_bounds__(kMergeThreads) fmha_gen_merge_kernel(const GenParams p) {
     __shared__ float red_m[kMergeGroups];
     __shared__ float4 red_o[kMergeGroups][32];
@@ -865,10 +955,15 @@ __global__ void __launch_bounds__(kMergeThreads) fmha_gen_merge_kernel(const Gen
     if (lane != 0) wsum = 0.f;   // lane 0 holds group 0's sum; share the total
     wsum = __shfl_sync(0xffffffffu, lane == 0 ? wsum : 0.f, 0);
     const float inv = wsum > 0.f ? p.out_scale / wsum : 0.f;
-    uint2 out;
-    out.x = pack2<BF>(acc.x * inv, acc.y * inv);
-    out.y = pack2<BF>(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.o) + (int64_t)row * kD + lane * 4) = out;
+    if constexpr (ELEM == FMHA_E4M3) {
+        *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.o) + (int64_t)row * kD + lane * 4) =
+            pack4_e4m3(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+        uint2 out;
+        out.x = pack2<ELEM == FMHA_BF16>(acc.x * inv, acc.y * inv);
+        out.y = pack2<ELEM == FMHA_BF16>(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.o) + (int64_t)row * kD + lane * 4) = out;
+    }
     if (lane == 0 && p.lse) p.lse[row] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
 }
 
@@ -959,7 +1054,7 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
     if (S_max <= 0 || B_cache <= 0 || !seqlen) return FMHA_ERR_INVALID_ARG;
     if (!q.data || !k_cache.data || !v_cache.data || !o.data) return FMHA_ERR_INVALID_ARG;
     const int dt = q.dtype;
-    if (dt != FMHA_F16 && dt != FMHA_BF16) return FMHA_ERR_UNSUPPORTED;
+    if (dt != FMHA_F16 && dt != FMHA_BF16 && dt != FMHA_E4M3) return FMHA_ERR_UNSUPPORTED;
     if (k_cache.dtype != dt || v_cache.dtype != dt || o.dtype != dt) return FMHA_ERR_UNSUPPORTED;
     if (insert && (k_new.dtype != dt || v_new.dtype != dt)) return FMHA_ERR_UNSUPPORTED;
     auto misaligned = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
@@ -1001,13 +1096,17 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
     // ---- tensor maps ----
     auto fn = gen_encode_fn();
     if (!fn) return FMHA_ERR_CUDA;
-    const CUtensorMapDataType tdt = dt == FMHA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType tdt = dt == FMHA_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                    : dt == FMHA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const int esz = dt == FMHA_E4M3 ? 1 : 2;
+    const cuuint32_t box_d = 128 / esz;                 // elements of one 128-byte swizzle panel
     CUtensorMap tq, tk, tv;
     {
-        // q as [B*H rows, 128]: a box of 32 heads x 64 dims (one swizzle panel)
+        // q as [B*H rows, 128]: a box of 32 heads x one swizzle panel of dims
         cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)B * H};
-        cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-        cuuint32_t box[2] = {64, (cuuint32_t)kNP};
+        cuuint64_t strides[1] = {(cuuint64_t)kD * esz};
+        cuuint32_t box[2] = {box_d, (cuuint32_t)kNP};
         cuuint32_t es[2] = {1, 1};
         if (fn(&tq, tdt, 2, const_cast<void *>(q.data), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1015,10 +1114,11 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
             return FMHA_ERR_CUDA;
     }
     for (int kv = 0; kv < 2; ++kv) {
-        // cache as [B_cache, S_max, H_k, 128]: a box of 128 tokens x 64 dims of one head
+        // cache as [B_cache, S_max, H_k, 128]: a box of 128 tokens x one panel of one head
         cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H_k, (cuuint64_t)S_max, (cuuint64_t)B_cache};
-        cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)kD * 2 * H_k, (cuuint64_t)kD * 2 * H_k * S_max};
-        cuuint32_t box[4] = {64, 1, (cuuint32_t)kKT, 1};
+        cuuint64_t strides[3] = {(cuuint64_t)kD * esz, (cuuint64_t)kD * esz * H_k,
+                                 (cuuint64_t)kD * esz * H_k * S_max};
+        cuuint32_t box[4] = {box_d, 1, (cuuint32_t)kKT, 1};
         cuuint32_t es[4] = {1, 1, 1, 1};
         if (fn(kv ? &tv : &tk, tdt, 4, kv ? v_cache.data : k_cache.data, dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1028,13 +1128,16 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
 
     // ---- launch: persistent CTAs over the work items, then the merge ----
     const int grid = sms;   // one persistent CTA per SM; each streams 1/grid of the tiles
-    auto kern = dt == FMHA_BF16 ? fmha_gen_kernel<true> : fmha_gen_kernel<false>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+    auto kern = dt == FMHA_BF16 ? fmha_gen_kernel<FMHA_BF16>
+                : dt == FMHA_F16 ? fmha_gen_kernel<FMHA_F16> : fmha_gen_kernel<FMHA_E4M3>;
+    const int smem_bytes = dt == FMHA_E4M3 ? GenCfg<FMHA_E4M3>::SMEM_BYTES : GenCfg<FMHA_BF16>::SMEM_BYTES;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
         return FMHA_ERR_CUDA;
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    kern<<<grid, kThreads, smem_bytes, stream>>>(tq, tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
     const int rows = B * H;
-    auto merge = dt == FMHA_BF16 ? fmha_gen_merge_kernel<true> : fmha_gen_merge_kernel<false>;
+    auto merge = dt == FMHA_BF16 ? fmha_gen_merge_kernel<FMHA_BF16>
+                 : dt == FMHA_F16 ? fmha_gen_merge_kernel<FMHA_F16> : fmha_gen_merge_kernel<FMHA_E4M3>;
     merge<<<rows, kMergeThreads, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
     return FMHA_OK;

@@ -217,4 +217,6 @@ GEN_CONFIGS = {
     "gen_f16_b8_h64_hk2_s32768_cacheonly": GenWorkload("gen_f16_b8_h64_hk2_s32768_cacheonly", dtype="f16", B=8,
                                                        H=64, H_k=2, S_max=32768, lengths="full", insert=False,
                                                        seed=23),
+    "gen_e4m3_b32_h32_hk8_s8192": GenWorkload("gen_e4m3_b32_h32_hk8_s8192", dtype="e4m3", B=32, H=32, H_k=8,
+                                              S_max=8192, lengths="full", seed=24),
 }

@@ -232,8 +232,10 @@ int fmha_fwd_splitkv_noalloc(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_t
  *   k_new, v_new       [B, H_k, 128]
  *   seqlen, batch_idx  int32 [B] (batch_idx may be NULL: entry b)
  *   lse                float [B, H], or NULL
- * All tensors share one dtype, FMHA_F16 or FMHA_BF16; D must be 128 and
- * H / H_k at most 32.  Device pointers must be 16-byte aligned.
+ * All tensors share one dtype, FMHA_F16, FMHA_BF16 or FMHA_E4M3; D must be
+ * 128 and H / H_k at most 32.  Device pointers must be 16-byte aligned.  With
+ * e4m3 the weights P are rounded to e4m3 before P.V (their row sum is not),
+ * and O is rounded to e4m3 with saturation.
  * Requirements the host cannot check (they live in device memory):
  * 0 <= seqlen[b] <= S_max - (insert ? 1 : 0) and 0 <= batch_idx[b] < B_cache;
  * a kernel that meets a violation clamps the length (and inserts nothing) or

@@ -201,7 +201,8 @@ def call_gen(fm, **kw):
     (dict(B=-1), -1), (dict(scale=0.0), -1), (dict(scale=float("inf")), -1),
     (dict(out_scale=float("nan")), -1), (dict(kn=P), -1), (dict(vn=P), -1),
     (dict(S_max=0), -1), (dict(B_cache=0), -1), (dict(seqlen=None), -1), (dict(q=None), -1),
-    (dict(o=None), -1), (dict(dtypes=(2, 2, 2, 2)), -2), (dict(dtypes=(1, 0, 1, 1)), -2),
+    (dict(o=None), -1), (dict(dtypes=(5, 5, 5, 5)), -2), (dict(dtypes=(1, 0, 1, 1)), -2),
+    (dict(dtypes=(2, 2, 2, 1)), -2), (dict(dtypes=(2, 1, 1, 1)), -2),
     (dict(q=P + 8), -2), (dict(kc=P + 2), -2), (dict(lse=P + 2), -1),
 ])
 def test_gen_validation_rejects_before_any_launch(fm, kw, code):

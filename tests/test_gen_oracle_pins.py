@@ -12,7 +12,7 @@ import pytest
 
 import oracle
 
-BF16, F16 = oracle.BF16, oracle.F16
+BF16, F16, E4M3 = oracle.BF16, oracle.F16, oracle.E4M3
 
 
 def enc(dtype, x):
@@ -45,10 +45,11 @@ def run(p, seqlen, batch_idx=None, insert=True, scale=None, out_scale=1.0, **ove
                           scale, out_scale)
 
 
-def test_single_new_key_returns_its_value_exactly():
-    p = problem(1)
+@pytest.mark.parametrize("dtype", [BF16, E4M3])
+def test_single_new_key_returns_its_value_exactly(dtype):
+    p = problem(1, dtype=dtype)
     o, lse = run(p, [0, 0, 0])
-    vn, kn, q = dec(BF16, p["vn"]), dec(BF16, p["kn"]), dec(BF16, p["q"])
+    vn, kn, q = dec(dtype, p["vn"]), dec(dtype, p["kn"]), dec(dtype, p["q"])
     for b in range(3):
         for h in range(4):
             g = h // 2
@@ -108,8 +109,9 @@ def test_batch_remap_reads_the_mapped_entry():
     assert not np.allclose(o_bad, o_ref)
 
 
-def test_gqa_equals_mha_with_repeated_kv_heads():
-    p = problem(6, H=8, H_k=2)
+@pytest.mark.parametrize("dtype", [BF16, E4M3])
+def test_gqa_equals_mha_with_repeated_kv_heads(dtype):
+    p = problem(6, H=8, H_k=2, dtype=dtype)
     seqlen = [3, 11, 25]
     o, lse = run(p, seqlen)
     rep = lambda x: np.repeat(x, 4, axis=-2)
@@ -117,15 +119,16 @@ def test_gqa_equals_mha_with_repeated_kv_heads():
     assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
 
 
-def test_matches_the_prefill_oracle_on_the_same_keys():
-    p = problem(7, dtype=F16)
+@pytest.mark.parametrize("dtype", [F16, E4M3])
+def test_matches_the_prefill_oracle_on_the_same_keys(dtype):
+    p = problem(7, dtype=dtype)
     seqlen, bidx = [6, 0, 33], [2, 3, 0]
     o, lse = run(p, seqlen, batch_idx=bidx, out_scale=0.75)
     for b, (L, c) in enumerate(zip(seqlen, bidx)):
         k = np.concatenate([p["kc"][c, :L], p["kn"][b][None]], axis=0)[None]   # [1, L+1, H_k, D]
         v = np.concatenate([p["vc"][c, :L], p["vn"][b][None]], axis=0)[None]
         q = p["q"][b][None, None]                                            # [1, 1, H, D]
-        o_p, lse_p = oracle.fmha_fwd(q, k, v, F16, 1, 4, 2, 1, L + 1, 128, 128 ** -0.5, 0.75)
+        o_p, lse_p = oracle.fmha_fwd(q, k, v, dtype, 1, 4, 2, 1, L + 1, 128, 128 ** -0.5, 0.75)
         assert np.allclose(o[b * 4:(b + 1) * 4], o_p, atol=1e-12)
         assert np.allclose(lse[b * 4:(b + 1) * 4], lse_p, atol=1e-12)
 
