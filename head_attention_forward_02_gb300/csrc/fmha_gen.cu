@@ -43,9 +43,10 @@ __device__ int g_gen_status;   // FMHA_OK, or the first error a generation kerne
 namespace {
 
 constexpr int kD = 128;                 // head dim
-constexpr int kKT = 128;                // keys per tile (MMA M of S^T)
+constexpr int kKT = 128;                // rows per tile (MMA M of S^T): keys, or keys x 2 heads
 constexpr int kNP = 32;                 // query heads of a group, padded (MMA N)
-constexpr int kNS = 3;                  // K/V ring stages, a K and a V tile each
+constexpr int kNSMax = 6;               // K/V ring stages at most (a K and a V tile each)
+constexpr int kBarBytes = 1536;         // barrier and scratch block
 constexpr int kSoftWarps = 4;           // warps 0-3: softmax and epilogue
 constexpr int kProdWarp = 4;            // TMA producer (lane 0), cache insert
 constexpr int kMmaWarp = 5;             // tcgen05.mma issuer (whole warp, one elected lane), owns TMEM
@@ -73,10 +74,11 @@ struct GenCfg {
     static constexpr uint32_t FMT = ELEM == FMHA_BF16 ? 1u : 0u;   // kind::f16: f16 0, bf16 1; f8f6f4: e4m3 0
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_KV = OFF_Q + kQSlots * Q_BYTES;
-    static constexpr int OFF_P = OFF_KV + kNS * STAGE_BYTES;
+    static constexpr int NS = FP8 ? 6 : 3;                // K/V ring stages
+    static constexpr int OFF_P = OFF_KV + NS * STAGE_BYTES;
     static constexpr int OFF_BARS = OFF_P + 2 * P_BYTES;
-    static constexpr int SMEM_BYTES = OFF_BARS + 1024 + 1024;    // barriers and scratch, 1 KB alignment
-    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static constexpr int SMEM_BYTES = OFF_BARS + kBarBytes + 1024;   // barriers and scratch, 1 KB alignment
+    static_assert(SMEM_BYTES <= 227 * 1024 && NS <= kNSMax, "shared memory budget");
 };
 constexpr unsigned long long kTimeoutNs = 4000000000ull;
 constexpr unsigned long long kDrainNs = 200000000ull;
@@ -92,6 +94,9 @@ struct GenParams {
     float *lse;                         // [B, H] or NULL
     float *part_o, *part_lse;           // [B*H][max_seg][D], [B*H][max_seg]
     int B, H, H_k, G, B_cache, S_max;
+    int GP;                             // kv heads per work unit: 2 (adjacent heads together) or 1
+    int TK;                             // keys per tile: 128 / GP (a tile is always 128 rows)
+    int NU;                             // work units per sequence: H_k / GP
     int max_seg;                        // partial results per (sequence, head): tiles of S_max + 1
     int ncta;                           // CTAs of the attention kernel (the stream-K split)
     int insert, dtype;
@@ -108,13 +113,14 @@ struct GenSched {
 struct GenBars {
     uint64_t q_full[kQSlots], q_empty[kQSlots], o_full, drain;
     uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];   // per S^T / P^T buffer
-    uint64_t kv_full[kNS], kv_empty[kNS];
+    uint64_t kv_full[kNSMax], kv_empty[kNSMax];
     uint32_t tmem_base;
     int abort;
     float red[kSoftWarps][kNP];         // per-warp partial max / sum of each head
+    float alpha[kNP], mref[kNP];        // rescale factors and reference maxima of every column
     GenSched sched;
 };
-static_assert(sizeof(GenBars) <= 1024, "barrier block");
+static_assert(sizeof(GenBars) <= kBarBytes, "barrier block");
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -280,6 +286,53 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
+// 32 lanes x N columns for N = 4, 8, 16 (32: tmem_ld32)
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[N]) {
+    if constexpr (N == 4) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                     : "r"(taddr));
+    } else if constexpr (N == 8) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                     : "r"(taddr));
+    } else if constexpr (N == 16) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+            "%14, %15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(taddr));
+    } else {
+        static_assert(N == 32, "tcgen05.ld width");
+        tmem_ld32(taddr, r);
+    }
+}
+
+// Wait for this thread's TMEM loads; the register operands tie the values to the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]);
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld_n(uint32_t (&r)[N]) {
+    if constexpr (N == 4) {
+        asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3])::"memory");
+    } else if constexpr (N == 8) {
+        asm volatile("tcgen05.wait::ld.sync.aligned;"
+                     : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+                     :
+                     : "memory");
+    } else if constexpr (N == 16) {
+        asm volatile("tcgen05.wait::ld.sync.aligned;"
+                     : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                       "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                       "+r"(r[15])
+                     :
+                     : "memory");
+    } else {
+        tmem_wait_ld(r);
+    }
+}
+
 // Wait for this thread's TMEM loads; the register operands tie the values to the wait.
 __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
@@ -346,7 +399,13 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
 }
 
 // ---------------------------------------------------------------------------
-// Work items: (sequence b, chunk c of its keys, kv head g), g fastest
+// Work items: (sequence b, chunk c of its keys, unit u), u fastest.  A unit is
+// one kv head, or two adjacent kv heads (GP = 2) whose query groups together
+// fill at most the 32 columns of S^T: their tiles are 64 keys x 2 heads, row
+// r of a tile being key r / 2 of head r % 2.  One key's rows of two adjacent
+// heads are contiguous in the cache, so every K/V row the tile reads is twice
+// as long; fetched alone, a 128-byte e4m3 row cost about 1.5x its size in
+// DRAM traffic on this part, and a pair of them exactly their size.
 // ---------------------------------------------------------------------------
 
 // Keys of sequence b: its cached tokens, plus the new one unless cache-only.
@@ -370,21 +429,30 @@ __device__ __forceinline__ int gen_entry(const GenParams &p, int b, bool report)
     return e;
 }
 
+// Shape of a work unit: kv heads and keys of a tile
+template <bool TWO>
+struct Unit {
+    static constexpr int GP = TWO ? 2 : 1;
+    static constexpr int TK = kKT / GP;
+};
+
+template <bool TWO>
 __device__ __forceinline__ int gen_tiles(const GenParams &p, int b) {
-    return (gen_tokens(p, b, false) + p.insert + kKT - 1) / kKT;
+    return (gen_tokens(p, b, false) + p.insert + Unit<TWO>::TK - 1) / Unit<TWO>::TK;
 }
 
-// Stream-K split: the 128-key tiles of every (sequence b, kv head g) pair, in
-// (b, g) order, form one sequence of T tiles; CTA i takes tiles
+// Stream-K split: the tiles of every (sequence b, unit u) pair, in (b, u)
+// order, form one sequence of T tiles; CTA i takes tiles
 // [i * per, (i + 1) * per) with per = ceil(T / gridDim.x), so every CTA
 // streams the same amount of K/V whatever the lengths.  A CTA's range is cut
 // at pair boundaries into segments; segment s of a pair is its part in the
 // s-th CTA that covers the pair, and writes partial slot s.
 
 // One warp: T, this CTA's range, and where its first segment starts.
+template <bool TWO>
 __device__ void gen_schedule(const GenParams &p, GenSched *sc, int lane) {
     int64_t T = 0;
-    for (int b = lane; b < p.B; b += 32) T += (int64_t)p.H_k * gen_tiles(p, b);
+    for (int b = lane; b < p.B; b += 32) T += (int64_t)p.NU * gen_tiles<TWO>(p, b);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) T += __shfl_xor_sync(0xffffffffu, T, o);
     const int64_t per = (T + gridDim.x - 1) / gridDim.x;
@@ -393,7 +461,7 @@ __device__ void gen_schedule(const GenParams &p, GenSched *sc, int lane) {
     int64_t off0 = T, base = 0;
     for (int bb = 0; bb < p.B && G0 < G1; bb += 32) {
         const int b = bb + lane;
-        const int64_t n = b < p.B ? (int64_t)p.H_k * gen_tiles(p, b) : 0;
+        const int64_t n = b < p.B ? (int64_t)p.NU * gen_tiles<TWO>(p, b) : 0;
         int64_t incl = n;                 // inclusive prefix over the 32 sequences
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -419,42 +487,44 @@ __device__ void gen_schedule(const GenParams &p, GenSched *sc, int lane) {
 }
 
 struct GenItem {
-    int b, g, entry, L, k0, k1;         // keys [k0, k1) of sequence b, kv head g
+    int b, g, entry, L, k0, k1;         // keys [k0, k1) of sequence b, kv heads g .. g + GP - 1
     int seg;                            // partial slot of this segment
     bool len_ok;                        // seqlen[b] was within [0, S_max - insert]
 };
 
-struct GenCursor {                      // next pair (b, g) and its first tile
-    int b = -1, g = 0;
+struct GenCursor {                      // next pair (b, unit u) and its first tile
+    int b = -1, u = 0;
     int64_t off = 0;
 };
 
+template <bool TWO>
 __device__ bool gen_next(const GenParams &p, const GenSched &sc, GenCursor &cur, GenItem &it, bool report) {
+    using U = Unit<TWO>;
     if (cur.b < 0) {
         cur.b = sc.b0;
-        cur.g = 0;
+        cur.u = 0;
         cur.off = sc.off0;
     }
     for (;;) {
         if (cur.b >= p.B || cur.off >= sc.G1) return false;
-        const int nt = gen_tiles(p, cur.b);
+        const int nt = gen_tiles<TWO>(p, cur.b);
         const int64_t end = cur.off + nt;
         const bool hit = nt > 0 && end > sc.G0;
         if (hit) {
             const int64_t t0 = max(sc.G0, cur.off) - cur.off, t1 = min(sc.G1, end) - cur.off;
-            const bool first = t0 == 0 && cur.g == 0;      // reports once per sequence
+            const bool first = t0 == 0 && cur.u == 0;      // reports once per sequence
             it.b = cur.b;
-            it.g = cur.g;
+            it.g = cur.u * U::GP;
             it.L = gen_tokens(p, cur.b, report && first);
             it.len_ok = p.seqlen[cur.b] == it.L;
             it.entry = gen_entry(p, cur.b, report && first);
-            it.k0 = (int)(t0 * kKT);
-            it.k1 = imin((int)(t1 * kKT), it.L + p.insert);
+            it.k0 = (int)(t0 * U::TK);
+            it.k1 = imin((int)(t1 * U::TK), it.L + p.insert);
             it.seg = (int)(blockIdx.x - cur.off / sc.per);
         }
         cur.off = end;
-        if (++cur.g == p.H_k) {
-            cur.g = 0;
+        if (++cur.u == p.NU) {
+            cur.u = 0;
             ++cur.b;
         }
         if (hit) return true;
@@ -467,10 +537,11 @@ __device__ bool gen_next(const GenParams &p, const GenSched &sc, GenCursor &cur,
 
 // TMA producer: per item, the new token's row into the cache (when this chunk
 // holds it), the 32-head Q tile, then the chunk's K/V tiles into the ring.
-template <int ELEM>
+template <int ELEM, bool TWO>
 __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUtensorMap *tmQ,
                              const CUtensorMap *tmK, const CUtensorMap *tmV, uint8_t *smem, GenBars *bars) {
     using C = GenCfg<ELEM>;
+    using U = Unit<TWO>;
     volatile int *abort_flag = &bars->abort;
     prefetch_tmap(tmQ);
     prefetch_tmap(tmK);
@@ -480,10 +551,11 @@ __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUten
     GenCursor cur;
     while (ok) {
         GenItem it;
-        if (!gen_next(p, sc, cur, it, true)) break;
+        if (!gen_next<TWO>(p, sc, cur, it, true)) break;
         if (p.insert && it.len_ok && it.entry >= 0 && it.L >= it.k0 && it.L < it.k1) {
-            // K and V rows of the new token (128 elements); the async proxy
-            // (TMA) reads row L below, so order these generic writes before it
+            // K and V rows of the new token (128 elements per kv head of the
+            // unit, contiguous); the async proxy (TMA) reads row L below, so
+            // order these generic writes before it
             const int64_t src = ((int64_t)it.b * p.H_k + it.g) * kD * C::E;
             const int64_t dst = (((int64_t)it.entry * p.S_max + it.L) * p.H_k + it.g) * kD * C::E;
             const uint4 *kn = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(p.k_new) + src);
@@ -491,7 +563,7 @@ __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUten
             uint4 *kc = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.k_cache) + dst);
             uint4 *vc = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.v_cache) + dst);
 #pragma unroll 4
-            for (int i = 0; i < kD * C::E / 16; ++i) {
+            for (int i = 0; i < U::GP * kD * C::E / 16; ++i) {
                 kc[i] = kn[i];
                 vc[i] = vn[i];
             }
@@ -507,14 +579,19 @@ __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUten
         }
         const uint32_t qb = smem_u32(&bars->q_full[qs]);
         mbar_expect_tx(qb, C::Q_BYTES);
+        // 32 query heads from the unit's first; a two-head unit takes two
+        // 16-row halves, the second from the second kv head's first query
         const int qrow = it.b * p.H + it.g * p.G;
+        const uint32_t qdst = smem_u32(smem + C::OFF_Q + qs * C::Q_BYTES);
 #pragma unroll
-        for (int pn = 0; pn < C::PANELS; ++pn)
-            tma_load_2d(smem_u32(smem + C::OFF_Q + qs * C::Q_BYTES + pn * kQPanelBytes), tmQ, qb, pn * C::BOX, qrow);
+        for (int pn = 0; pn < C::PANELS; ++pn) {
+            tma_load_2d(qdst + pn * kQPanelBytes, tmQ, qb, pn * C::BOX, qrow);
+            if (TWO) tma_load_2d(qdst + pn * kQPanelBytes + kQPanelBytes / 2, tmQ, qb, pn * C::BOX, qrow + p.G);
+        }
         ++qn;
-        for (int k = it.k0; k < it.k1; k += kKT) {
-            const int st = fill % kNS;
-            const uint32_t rnd = fill / kNS;
+        for (int k = it.k0; k < it.k1; k += U::TK) {
+            const int st = fill % C::NS;
+            const uint32_t rnd = fill / C::NS;
             if (rnd > 0 && !mbar_wait(smem_u32(&bars->kv_empty[st]), (rnd - 1) & 1, abort_flag)) {
                 ok = false;
                 break;
@@ -523,26 +600,33 @@ __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUten
             mbar_expect_tx(fb, C::STAGE_BYTES);
             const uint32_t dst = smem_u32(smem + C::OFF_KV + st * C::STAGE_BYTES);
             const int e = it.entry >= 0 ? it.entry : p.B_cache;   // out of range: zero fill
+            // rows [64 h2, 64 h2 + 64) of a two-head tile are head g + h2;
+            // the heads' loads go out back to back, so each key's rows of
+            // both heads (adjacent in the cache) are fetched together
 #pragma unroll
-            for (int pn = 0; pn < C::PANELS; ++pn) {
-                tma_load_4d(dst + pn * kPanelBytes, tmK, fb, pn * C::BOX, it.g, k, e);
-                tma_load_4d(dst + C::TILE_BYTES + pn * kPanelBytes, tmV, fb, pn * C::BOX, it.g, k, e);
+            for (int h2 = 0; h2 < U::GP; ++h2) {
+                const uint32_t ro = (uint32_t)(h2 * U::TK * 128);
+#pragma unroll
+                for (int pn = 0; pn < C::PANELS; ++pn) {
+                    tma_load_4d(dst + pn * kPanelBytes + ro, tmK, fb, pn * C::BOX, it.g + h2, k, e);
+                    tma_load_4d(dst + C::TILE_BYTES + pn * kPanelBytes + ro, tmV, fb, pn * C::BOX, it.g + h2, k, e);
+                }
             }
             ++fill;
         }
     }
     if (ok) {
         // every stage's and the Q tile's last release must arrive before exit
-        for (int st = 0; st < kNS; ++st) {
-            const uint32_t nf = fill > (uint32_t)st ? (fill - st + kNS - 1) / kNS : 0;
+        for (int st = 0; st < C::NS; ++st) {
+            const uint32_t nf = fill > (uint32_t)st ? (fill - st + C::NS - 1) / C::NS : 0;
             if (nf && !mbar_wait(smem_u32(&bars->kv_empty[st]), (nf - 1) & 1, abort_flag)) break;
         }
         for (uint32_t f = qn > kQSlots ? qn - kQSlots : 0; f < qn; ++f)
             if (!mbar_wait(smem_u32(&bars->q_empty[f % kQSlots]), (f / kQSlots) & 1, abort_flag)) break;
     } else {
         // aborted: let the copies already issued land before the CTA exits
-        const uint32_t first = fill > (uint32_t)kNS ? fill - kNS : 0;
-        for (uint32_t f = first; f < fill; ++f) mbar_wait_drain(smem_u32(&bars->kv_full[f % kNS]), (f / kNS) & 1);
+        const uint32_t first = fill > (uint32_t)C::NS ? fill - C::NS : 0;
+        for (uint32_t f = first; f < fill; ++f) mbar_wait_drain(smem_u32(&bars->kv_full[f % C::NS]), (f / C::NS) & 1);
         for (uint32_t f = qn > kQSlots ? qn - kQSlots : 0; f < qn; ++f)
             mbar_wait_drain(smem_u32(&bars->q_full[f % kQSlots]), (f / kQSlots) & 1);
     }
@@ -555,9 +639,10 @@ __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUten
 // out of it, then O^T += V^T_j-1 P^T_j-1 once the softmax has written P^T_j-1.
 // The last tile of a work item issues its own P.V before the next item starts,
 // so the epilogue never waits for the next item's loads.
-template <int ELEM>
+template <int ELEM, bool TWO>
 __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, GenBars *bars, uint32_t tmem_any) {
     using C = GenCfg<ELEM>;
+    using U = Unit<TWO>;
     // the whole warp runs this loop converged, with warp-uniform values; one
     // elected lane issues each MMA and commit
     volatile int *abort_flag = &bars->abort;
@@ -594,17 +679,17 @@ __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, G
     GenCursor cur;
     while (ok) {
         GenItem it;
-        if (!gen_next(p, sc, cur, it, false)) break;
+        if (!gen_next<TWO>(p, sc, cur, it, false)) break;
         const int qs = qn % kQSlots;
         if (!warp_wait(smem_u32(&bars->q_full[qs]), (qn / kQSlots) & 1, abort_flag)) break;
         ++qn;
         const uint64_t q_desc = q_desc0 + ((qs * C::Q_BYTES) >> 4);
         bool first = true;
         int prev_st = 0;
-        for (int k = it.k0; k < it.k1; k += kKT) {
-            const int st = cons % kNS;
+        for (int k = it.k0; k < it.k1; k += U::TK) {
+            const int st = cons % C::NS;
             const uint32_t b = cons & 1;
-            if (!warp_wait(smem_u32(&bars->kv_full[st]), (cons / kNS) & 1, abort_flag) ||
+            if (!warp_wait(smem_u32(&bars->kv_full[st]), (cons / C::NS) & 1, abort_flag) ||
                 (cons >= 2 && !warp_wait(smem_u32(&bars->s_free[b]), ((cons - 2) >> 1) & 1, abort_flag))) {
                 ok = false;
                 break;
@@ -622,9 +707,9 @@ __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, G
                 mma_ss_e<C::FP8>(tmem + b * kNP, k_desc + (koff >> 4), q_desc + (qoff >> 4), kIdS,
                                  kk > 0 ? 1u : 0u);
             }
-            if (k + kKT >= it.k1) tc_commit_e(smem_u32(&bars->q_empty[qs]));
+            if (k + U::TK >= it.k1) tc_commit_e(smem_u32(&bars->q_empty[qs]));
             tc_commit_e(smem_u32(&bars->s_full[b]));
-            if (!first && !issue_pv(cons - 1, prev_st, k - kKT == it.k0)) {
+            if (!first && !issue_pv(cons - 1, prev_st, k - U::TK == it.k0)) {
                 ok = false;
                 break;
             }
@@ -634,7 +719,7 @@ __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, G
         }
         if (!ok) break;
         // the item's last P.V (none for an item without keys), then O^T is complete
-        if (!first && !issue_pv(cons - 1, prev_st, it.k1 - it.k0 <= kKT)) break;
+        if (!first && !issue_pv(cons - 1, prev_st, it.k1 - it.k0 <= U::TK)) break;
         tc_commit_e(smem_u32(&bars->o_full));
     }
     // no tensor-core operation may be in flight when TMEM is released
@@ -642,9 +727,20 @@ __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, G
     mbar_wait_drain(smem_u32(&bars->drain), 0);
 }
 
-// Softmax and epilogue: thread t of warps 0-3 owns key t of every tile (TMEM
-// lane t of S^T) and head dimension t of O^T.
-template <int ELEM>
+// Softmax and epilogue: thread t of warps 0-3 owns row t of every tile (TMEM
+// lane t of S^T) and head dimension t of O^T.  Row t is key t of the unit's
+// kv head, or, in a two-head unit, key t % 64 of head t / 64 (warps 0-1: the
+// first head, warps 2-3: the second).
+//
+// Columns of S^T are query heads: [0, G) of a one-head unit, or [0, G) and
+// [16, 16 + G) of a two-head unit (its Q tile is two 16-row halves).  A
+// thread works on NC >= G columns from c0 = 16 * (its kv head in the unit),
+// shared by its column group (the warps of that kv head); columns of a group
+// past G hold other heads' queries and feed only O^T columns that are never
+// stored.  In a two-head unit a row's weights in the other head's columns
+// are written as 0, so P.V over the 128 rows adds, for each column, only the
+// rows of its own kv head.
+template <int ELEM, int NC, bool TWO>
 __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *smem, GenBars *bars, uint32_t tmem,
                             int warp, int lane) {
     using C = GenCfg<ELEM>;
@@ -652,20 +748,27 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
     const int t = warp * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     const uint32_t o_tm = lane_base + 2 * kNP;
-    uint8_t *prow0 = smem + C::OFF_P + t * C::P_ROW;     // this key's P^T row in buffer 0
+    uint8_t *prow0 = smem + C::OFF_P + t * C::P_ROW;     // this row's P^T row in buffer 0
+    constexpr bool two = TWO;
+    const int hh = two ? warp >> 1 : 0;                 // kv head of this thread's rows within the unit
+    const int key_of_row = two ? t & 63 : t;
+    const int c0 = 16 * hh;                             // first column of this thread's group
+    const int w0 = 2 * hh;                              // first warp of the group (two-head units)
+    // P^T swizzle: 16-byte chunk index ^= (row / 2) % 4 (64-byte rows) or (row / 4) % 2 (32-byte rows)
+    const uint32_t swz = C::FP8 ? (t >> 2) & 1 : (t >> 1) & 3;
     uint32_t oph = 0, cons = 0;
     GenCursor cur;
     for (;;) {
         GenItem it;
-        if (!gen_next(p, sc, cur, it, false)) break;
-        float m[kNP], l[kNP];
+        if (!gen_next<TWO>(p, sc, cur, it, false)) break;
+        float m[NC], l[NC];
 #pragma unroll
-        for (int h = 0; h < kNP; ++h) {
-            m[h] = -INFINITY;   // reference max (log2 units) P and O^T are relative to
-            l[h] = 0.f;         // this thread's part of the row sum
+        for (int c = 0; c < NC; ++c) {
+            m[c] = -INFINITY;   // reference max (log2 units) P and O^T are relative to
+            l[c] = 0.f;         // this thread's part of the row sum
         }
         bool ok = true, first = true;
-        for (int k = it.k0; k < it.k1; k += kKT) {
+        for (int k = it.k0; k < it.k1; k += Unit<TWO>::TK) {
             // S^T_j and P^T_j use buffer j % 2.  The commit that completes
             // S^T_j also covers P.V_j-2, issued before it by the same thread,
             // so P^T buffer j % 2 is free to rewrite once S^T_j is here.
@@ -676,48 +779,54 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
                 break;
             }
             tc_fence_after();
-            const int st = cons % kNS;
+            const int st = cons % C::NS;
             const uint32_t j = cons++;
-            uint32_t sr[32];
-            tmem_ld32(lane_base + b * kNP, sr);
-            tmem_wait_ld(sr);
+            uint32_t sr[NC];
+            tmem_ld_n<NC>(lane_base + b * kNP + c0, sr);
+            tmem_wait_ld_n<NC>(sr);
             tc_fence_before();
             mbar_arrive(smem_u32(&bars->s_free[b]));   // S^T buffer b may take S^T_j+2
-            const bool valid = k + t < it.k1;
-            float s[kNP];
+            const bool valid = k + key_of_row < it.k1;
+            float s[NC];
             bool need = false;
 #pragma unroll
-            for (int h = 0; h < kNP; ++h) {
-                s[h] = valid ? __uint_as_float(sr[h]) * p.c : -INFINITY;
-                need |= s[h] > m[h] + kRescaleLog2;
+            for (int c = 0; c < NC; ++c) {
+                s[c] = valid ? __uint_as_float(sr[c]) * p.c : -INFINITY;
+                need |= s[c] > m[c] + kRescaleLog2;
             }
             bool rescaled = false;
             if (soft_any(need)) {
-                // tile maximum of every head over the 128 keys
+                // tile maximum of every column over the group's rows
 #pragma unroll
-                for (int h = 0; h < kNP; ++h) {
-                    float x = s[h];
+                for (int c = 0; c < NC; ++c) {
+                    float x = s[c];
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-                    if (lane == 0) bars->red[warp][h] = x;
+                    if (lane == 0) bars->red[warp][c0 + c] = x;
                 }
                 soft_sync();
-                float alpha[kNP];
+                float alpha[NC];
 #pragma unroll
-                for (int h = 0; h < kNP; ++h) {
-                    const float tmax = fmaxf(fmaxf(bars->red[0][h], bars->red[1][h]),
-                                             fmaxf(bars->red[2][h], bars->red[3][h]));
-                    alpha[h] = 1.f;
-                    if (tmax > m[h] + kRescaleLog2) {
-                        alpha[h] = m[h] == -INFINITY ? 0.f : ex2(m[h] - tmax);
-                        l[h] *= alpha[h];
-                        m[h] = tmax;
+                for (int c = 0; c < NC; ++c) {
+                    float tmax = fmaxf(bars->red[w0][c0 + c], bars->red[w0 + 1][c0 + c]);
+                    if (!two) tmax = fmaxf(tmax, fmaxf(bars->red[2][c], bars->red[3][c]));
+                    alpha[c] = 1.f;
+                    if (tmax > m[c] + kRescaleLog2) {
+                        alpha[c] = m[c] == -INFINITY ? 0.f : ex2(m[c] - tmax);
+                        l[c] *= alpha[c];
+                        m[c] = tmax;
                     }
                 }
-                soft_sync();   // the scratch row may be rewritten after this
                 if (!first) {
-                    // O^T holds the P.V of the previous tile once it is done;
-                    // row t, one column per head
+                    // O^T row t holds every column: share the factors first
+                    if ((two ? warp == w0 : warp == 0) && lane == 0) {
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) bars->alpha[c0 + c] = alpha[c];
+                    }
+                }
+                soft_sync();   // the scratch rows may be rewritten after this
+                if (!first) {
+                    // O^T holds the P.V of the previous tile once it is done
                     const bool pv = mbar_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag);
                     if (!soft_all(pv)) {
                         ok = false;
@@ -728,41 +837,54 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
                     tmem_ld32(o_tm, orr);
                     tmem_wait_ld(orr);
 #pragma unroll
-                    for (int h = 0; h < kNP; ++h) orr[h] = __float_as_uint(__uint_as_float(orr[h]) * alpha[h]);
+                    for (int h = 0; h < kNP; ++h)
+                        orr[h] = __float_as_uint(__uint_as_float(orr[h]) * bars->alpha[h]);
                     tmem_st32(o_tm, orr);
                     rescaled = true;
+                    soft_sync();   // every thread has read the factors
                 }
             }
-            // P^T row of key t: 32 heads in 16-byte chunks placed by the
-            // swizzle of the row (64-byte rows: chunk ^= (row / 2) % 4;
-            // 32-byte rows: chunk ^= (row / 4) % 2)
-            float pv[kNP];
+            float pv[NC];
 #pragma unroll
-            for (int h = 0; h < kNP; ++h) {
-                pv[h] = m[h] == -INFINITY ? 0.f : ex2(s[h] - m[h]);
-                l[h] += pv[h];
+            for (int c = 0; c < NC; ++c) {
+                pv[c] = m[c] == -INFINITY ? 0.f : ex2(s[c] - m[c]);
+                l[c] += pv[c];
             }
+            // P^T row t: columns [c0, c0 + NC) from pv and, in a two-head
+            // unit, 0 in the other head's columns (the remaining columns feed
+            // only O^T columns that are never stored)
             uint8_t *prow = prow0 + b * C::P_BYTES;
+            constexpr int VB = NC * C::E;                    // bytes of this thread's values
+            uint32_t w[(VB + 3) / 4];
             if constexpr (C::FP8) {
-                uint32_t w[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) w[i] = pack4_e4m3(pv[4 * i], pv[4 * i + 1], pv[4 * i + 2], pv[4 * i + 3]);
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-                    *reinterpret_cast<uint4 *>(prow + ((c ^ ((t >> 2) & 1)) << 4)) =
-                        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                for (int i = 0; i < NC / 4; ++i) w[i] = pack4_e4m3(pv[4 * i], pv[4 * i + 1], pv[4 * i + 2], pv[4 * i + 3]);
             } else {
-                uint32_t w[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) w[i] = pack2<ELEM == FMHA_BF16>(pv[2 * i], pv[2 * i + 1]);
+                for (int i = 0; i < NC / 2; ++i) w[i] = pack2<ELEM == FMHA_BF16>(pv[2 * i], pv[2 * i + 1]);
+            }
+            const int vo = c0 * C::E;                    // byte offset of the values in the row
+            const int zo = (16 - c0) * C::E;             // the other head's columns
+            if constexpr (VB >= 16) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(prow + ((c ^ ((t >> 1) & 3)) << 4)) =
+                for (int c = 0; c < VB / 16; ++c) {
+                    *reinterpret_cast<uint4 *>(prow + ((((vo >> 4) + c) ^ swz) << 4)) =
                         make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                    if (two)
+                        *reinterpret_cast<uint4 *>(prow + ((((zo >> 4) + c) ^ swz) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            } else if constexpr (VB == 8) {
+                *reinterpret_cast<uint2 *>(prow + ((((vo >> 4) ^ swz) << 4) | (vo & 15))) = make_uint2(w[0], w[1]);
+                if (two) *reinterpret_cast<uint2 *>(prow + ((((zo >> 4) ^ swz) << 4) | (zo & 15))) = make_uint2(0u, 0u);
+            } else {
+                static_assert(VB == 4, "P^T values of a thread");
+                *reinterpret_cast<uint32_t *>(prow + ((((vo >> 4) ^ swz) << 4) | (vo & 15))) = w[0];
+                if (two) *reinterpret_cast<uint32_t *>(prow + ((((zo >> 4) ^ swz) << 4) | (zo & 15))) = 0u;
             }
             if (!valid) {
-                // a key past the chunk's end: its V row (stale cache contents,
-                // possibly not finite) is zeroed so that P = 0 contributes 0
+                // a row whose key is past the chunk's end: its V row (stale
+                // cache contents, possibly not finite) is zeroed so that P = 0
+                // contributes 0
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 uint8_t *vrow = smem + C::OFF_KV + st * C::STAGE_BYTES + C::TILE_BYTES + t * 128;
 #pragma unroll
@@ -783,22 +905,23 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
         }
         if (!ok) break;
 
-        // epilogue: row sums, then the normalised partial O and its LSE
+        // epilogue: row sums and reference maxima of every column, then the
+        // normalised partial O and its LSE
         const bool got = mbar_wait(smem_u32(&bars->o_full), oph, abort_flag);
         oph ^= 1;
         if (!soft_all(got)) break;
         tc_fence_after();
 #pragma unroll
-        for (int h = 0; h < kNP; ++h) {
-            float x = l[h];
+        for (int c = 0; c < NC; ++c) {
+            float x = l[c];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-            if (lane == 0) bars->red[warp][h] = x;
+            if (lane == 0) bars->red[warp][c0 + c] = x;
         }
-        soft_sync();
-        float lt[kNP];
+        if ((two ? warp == w0 : warp == 0) && lane == 0) {
 #pragma unroll
-        for (int h = 0; h < kNP; ++h) lt[h] = (bars->red[0][h] + bars->red[1][h]) + (bars->red[2][h] + bars->red[3][h]);
+            for (int c = 0; c < NC; ++c) bars->mref[c0 + c] = m[c];
+        }
         soft_sync();
         uint32_t orr[32];
         tmem_ld32(o_tm, orr);
@@ -806,16 +929,22 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
         const int64_t row0 = (int64_t)it.b * p.H + (int64_t)it.g * p.G;
 #pragma unroll
         for (int h = 0; h < kNP; ++h) {
-            if (h < p.G) {
-                const int64_t slot = (row0 + h) * p.max_seg + it.seg;
-                p.part_o[slot * kD + t] = lt[h] > 0.f ? __uint_as_float(orr[h]) / lt[h] : 0.f;
-                if (t == h) p.part_lse[slot] = lt[h] > 0.f ? (m[h] + log2f(lt[h])) * kLn2 : -INFINITY;
+            // column h: query head row0 + h (one-head unit), or row0 + G * (h / 16) + h % 16
+            if ((h & 15) < NC && (two ? (h & 15) < p.G : h < p.G)) {
+                const int g2 = two ? 2 * (h >> 4) : 0;
+                float lt = bars->red[g2][h] + bars->red[g2 + 1][h];
+                if (!two) lt += bars->red[2][h] + bars->red[3][h];
+                const int64_t qh = two ? row0 + (h >> 4) * p.G + (h & 15) : row0 + h;
+                const int64_t slot = qh * p.max_seg + it.seg;
+                p.part_o[slot * kD + t] = lt > 0.f ? __uint_as_float(orr[h]) / lt : 0.f;
+                if (t == h) p.part_lse[slot] = lt > 0.f ? (bars->mref[h] + log2f(lt)) * kLn2 : -INFINITY;
             }
         }
+        soft_sync();   // the scratch rows may be rewritten after this
     }
 }
 
-template <int ELEM>
+template <int ELEM, int NC, bool TWO>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_gen_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const GenParams p) {
@@ -836,29 +965,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(smem_u32(&bars->o_full), 1);
         mbar_init(smem_u32(&bars->drain), 1);
-        for (int s = 0; s < kNS; ++s) {
+        for (int s = 0; s < kNSMax; ++s) {
             mbar_init(smem_u32(&bars->kv_full[s]), 1);
             mbar_init(smem_u32(&bars->kv_empty[s]), 1);
         }
         bars->abort = 0;
+        for (int i = 0; i < kNP; ++i) bars->alpha[i] = 1.f;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
         tmem_relinquish();
     }
-    if (warp == kProdWarp) gen_schedule(p, &bars->sched, lane);
+    if (warp == kProdWarp) gen_schedule<TWO>(p, &bars->sched, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const GenSched sc = bars->sched;
     if (warp < kSoftWarps) {
-        gen_softmax<ELEM>(p, sc, smem, bars, tmem, warp, lane);
+        gen_softmax<ELEM, NC, TWO>(p, sc, smem, bars, tmem, warp, lane);
     } else if (warp == kProdWarp) {
-        if (lane == 0) gen_producer<ELEM>(p, sc, &tmQ, &tmK, &tmV, smem, bars);
+        if (lane == 0) gen_producer<ELEM, TWO>(p, sc, &tmQ, &tmK, &tmV, smem, bars);
     } else {
-        gen_mma<ELEM>(p, sc, smem, bars, tmem);
+        gen_mma<ELEM, TWO>(p, sc, smem, bars, tmem);
     }
     tc_fence_before();
     __syncthreads();
@@ -884,11 +1014,11 @@ __global__ void __launch_bounds__(kMergeThreads) fmha_gen_merge_kernel(const Gen
     __shared__ long long red_t[kMergeGroups], red_p[kMergeGroups];
     const int row = blockIdx.x;
     const int grp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = row / p.H, g = (row % p.H) / p.G;
+    const int b = row / p.H, u = (row % p.H) / (p.G * p.GP);   // sequence and work unit
     // the attention kernel's split: total tiles, and the tiles before sequence b
     long long tot = 0, pre = 0;
     for (int bb = threadIdx.x; bb < p.B; bb += kMergeThreads) {
-        const long long n = (long long)p.H_k * gen_tiles(p, bb);
+        const long long n = (long long)p.NU * (p.GP == 2 ? gen_tiles<true>(p, bb) : gen_tiles<false>(p, bb));
         tot += n;
         if (bb < b) pre += n;
     }
@@ -909,11 +1039,11 @@ __global__ void __launch_bounds__(kMergeThreads) fmha_gen_merge_kernel(const Gen
         tot += red_t[i];
         pre += red_p[i];
     }
-    const int nt = gen_tiles(p, b);
+    const int nt = p.GP == 2 ? gen_tiles<true>(p, b) : gen_tiles<false>(p, b);
     int nch = 0;                       // CTAs that covered this pair = its partial slots
     if (nt > 0) {
         const long long per = (tot + p.ncta - 1) / p.ncta;
-        const long long off = pre + (long long)g * nt;
+        const long long off = pre + (long long)u * nt;
         nch = (int)((off + nt - 1) / per - off / per + 1);
     }
     const float *lse_c = p.part_lse + (int64_t)row * p.max_seg;
@@ -1020,11 +1150,32 @@ struct GenLayout {
     size_t o_bytes, lse_off, total;
 };
 
-// Partial slots per (sequence, head): a pair of n tiles meets at most n + 1
-// CTAs' ranges, and n <= ceil(S_max / 128).
-GenLayout gen_layout(int B, int H, int S_max) {
+// Instantiations: two-head units with 4, 8 or 16 columns per thread (G <= 16),
+// one-head units with 8, 16 or 32 (G <= 32).
+using GenKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, GenParams);
+template <int ELEM>
+GenKernel gen_kernel_nc(int nc, bool two) {
+    if (two)
+        return nc == 4 ? fmha_gen_kernel<ELEM, 4, true>
+               : nc == 8 ? fmha_gen_kernel<ELEM, 8, true> : fmha_gen_kernel<ELEM, 16, true>;
+    return nc == 8 ? fmha_gen_kernel<ELEM, 8, false>
+           : nc == 16 ? fmha_gen_kernel<ELEM, 16, false> : fmha_gen_kernel<ELEM, 32, false>;
+}
+GenKernel gen_kernel_for(int dt, int nc, bool two) {
+    return dt == FMHA_BF16 ? gen_kernel_nc<FMHA_BF16>(nc, two)
+           : dt == FMHA_F16 ? gen_kernel_nc<FMHA_F16>(nc, two) : gen_kernel_nc<FMHA_E4M3>(nc, two);
+}
+
+// Two adjacent kv heads share a work unit when H_k is even and each query
+// group fits a 16-column half of S^T.
+bool gen_pairs(int H, int H_k) { return H_k % 2 == 0 && 2 * (H / H_k) <= kNP; }
+
+// Partial slots per (sequence, head): a unit of n tiles meets at most n + 1
+// CTAs' ranges, and n <= ceil(S_max / keys per tile).
+GenLayout gen_layout(int B, int H, int H_k, int S_max) {
     GenLayout g;
-    g.max_seg = (S_max + kKT - 1) / kKT + 1;
+    const int tk = gen_pairs(H, H_k) ? kKT / 2 : kKT;
+    g.max_seg = (S_max + tk - 1) / tk + 1;
     const size_t rows = (size_t)B * H * g.max_seg;
     g.o_bytes = rows * kD * sizeof(float);
     g.lse_off = (g.o_bytes + 255) / 256 * 256;
@@ -1036,7 +1187,7 @@ GenLayout gen_layout(int B, int H, int S_max) {
 
 extern "C" size_t fmha_gen_workspace_size(int B, int H, int H_k, int D, int S_max) {
     if (B <= 0 || H <= 0 || H_k <= 0 || H % H_k != 0 || D != kD || S_max <= 0) return 0;
-    return gen_layout(B, H, S_max).total;
+    return gen_layout(B, H, H_k, S_max).total;
 }
 
 extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_cache, fmha_tensor k_new,
@@ -1062,7 +1213,7 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
         (insert && (misaligned(k_new.data) || misaligned(v_new.data))))
         return FMHA_ERR_UNSUPPORTED;
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FMHA_ERR_INVALID_ARG;
-    const GenLayout g = gen_layout(B, H, S_max);
+    const GenLayout g = gen_layout(B, H, H_k, S_max);
     const int sms = gen_sm_count();
     if (sms <= 0) return FMHA_ERR_CUDA;
     if (!workspace || workspace_bytes < g.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -1084,6 +1235,9 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
     p.H = H;
     p.H_k = H_k;
     p.G = H / H_k;
+    p.GP = gen_pairs(H, H_k) ? 2 : 1;
+    p.TK = kKT / p.GP;
+    p.NU = H_k / p.GP;
     p.B_cache = B_cache;
     p.S_max = S_max;
     p.max_seg = g.max_seg;
@@ -1103,10 +1257,11 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
     const cuuint32_t box_d = 128 / esz;                 // elements of one 128-byte swizzle panel
     CUtensorMap tq, tk, tv;
     {
-        // q as [B*H rows, 128]: a box of 32 heads x one swizzle panel of dims
+        // q as [B*H rows, 128]: a box of 32 heads (16 for a two-head unit's
+        // halves) x one swizzle panel of dims
         cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)B * H};
         cuuint64_t strides[1] = {(cuuint64_t)kD * esz};
-        cuuint32_t box[2] = {box_d, (cuuint32_t)kNP};
+        cuuint32_t box[2] = {box_d, (cuuint32_t)(kNP / p.GP)};
         cuuint32_t es[2] = {1, 1};
         if (fn(&tq, tdt, 2, const_cast<void *>(q.data), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1114,11 +1269,12 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
             return FMHA_ERR_CUDA;
     }
     for (int kv = 0; kv < 2; ++kv) {
-        // cache as [B_cache, S_max, H_k, 128]: a box of 128 tokens x one panel of one head
+        // cache as [B_cache, S_max, H_k, 128]: a box of TK tokens of one head
+        // x one panel
         cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H_k, (cuuint64_t)S_max, (cuuint64_t)B_cache};
         cuuint64_t strides[3] = {(cuuint64_t)kD * esz, (cuuint64_t)kD * esz * H_k,
                                  (cuuint64_t)kD * esz * H_k * S_max};
-        cuuint32_t box[4] = {box_d, 1, (cuuint32_t)kKT, 1};
+        cuuint32_t box[4] = {box_d, 1, (cuuint32_t)p.TK, 1};
         cuuint32_t es[4] = {1, 1, 1, 1};
         if (fn(kv ? &tv : &tk, tdt, 4, kv ? v_cache.data : k_cache.data, dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1128,8 +1284,10 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
 
     // ---- launch: persistent CTAs over the work items, then the merge ----
     const int grid = sms;   // one persistent CTA per SM; each streams 1/grid of the tiles
-    auto kern = dt == FMHA_BF16 ? fmha_gen_kernel<FMHA_BF16>
-                : dt == FMHA_F16 ? fmha_gen_kernel<FMHA_F16> : fmha_gen_kernel<FMHA_E4M3>;
+    // columns of S^T a softmax thread works on: the query group, rounded up
+    const int G = H / H_k;
+    const int nc = G <= 4 && p.GP == 2 ? 4 : G <= 8 ? 8 : G <= 16 ? 16 : 32;
+    auto kern = gen_kernel_for(dt, nc, p.GP == 2);
     const int smem_bytes = dt == FMHA_E4M3 ? GenCfg<FMHA_E4M3>::SMEM_BYTES : GenCfg<FMHA_BF16>::SMEM_BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
         return FMHA_ERR_CUDA;

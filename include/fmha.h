@@ -260,8 +260,10 @@ int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_cache,
                  void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * Workspace bytes fmha_gen_fwd needs for these sizes on the current device
- * (the key-range split depends on its SM count).  0 for invalid sizes.
+ * Workspace bytes fmha_gen_fwd needs for these sizes: an fp32 partial O row
+ * and LSE per (sequence, query head, key chunk), at most one chunk per key
+ * tile of S_max plus one (tiles of 64 keys when H_k is even and H / H_k <= 16,
+ * else 128).  0 for invalid sizes.
  */
 size_t fmha_gen_workspace_size(int B, int H, int H_k, int D, int S_max);
 

@@ -218,12 +218,18 @@ def test_gen_workspace_size_rejects_bad_sizes(fm):
         assert fm.fmha_gen_workspace_size(*bad) == 0
 
 
-def test_gen_workspace_size(fm):
-    # fp32 partial O then (256-byte aligned) LSE, ceil(S_max/128)+1 slots per (sequence, head)
-    B, H, S_max = 3, 8, 1000
-    slots = B * H * ((S_max + 127) // 128 + 1)
+@pytest.mark.parametrize("H,H_k,keys_per_tile", [
+    (8, 2, 64),      # even H_k, query group <= 16: two kv heads per unit, 64-key tiles
+    (8, 1, 128),     # odd H_k: one kv head per unit
+    (64, 2, 128),    # query group of 32: one kv head per unit
+])
+def test_gen_workspace_size(fm, H, H_k, keys_per_tile):
+    # fp32 partial O then (256-byte aligned) LSE, ceil(S_max / keys per tile) + 1
+    # slots per (sequence, head)
+    B, S_max = 3, 1000
+    slots = B * H * ((S_max + keys_per_tile - 1) // keys_per_tile + 1)
     o_bytes = slots * 128 * 4
-    assert fm.fmha_gen_workspace_size(B, H, 2, 128, S_max) == (o_bytes + 255) // 256 * 256 + slots * 4
+    assert fm.fmha_gen_workspace_size(B, H, H_k, 128, S_max) == (o_bytes + 255) // 256 * 256 + slots * 4
 
 
 def call_bwd(fm, **kw):

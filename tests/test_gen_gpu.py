@@ -1,11 +1,12 @@
 """Generation-phase attention (fmha_gen_fwd) against the oracle, on the GPU.
 
 Cases cover fp16, bf16 and e4m3, insert and cache-only modes, batch remapping,
-head groups of 1 to 32, lengths at tile and chunk edges (the key range is cut
-into chunks of whole 128-key tiles), an empty cache, NaN-filled rows past every
-length, the cache rows the call writes, and a length outside the cache
-(reported, not a fault).  e4m3 inputs are compared with the oracle on their
-decoded values.
+head groups of 1 to 32, work units of one kv head (odd H_k, or query groups
+wider than 16) and of two adjacent kv heads (64-key tiles), lengths at tile
+and chunk edges (the key range is cut into chunks of whole tiles), an empty
+cache, NaN-filled rows past every length, the cache rows the call writes, and
+a length outside the cache (reported, not a fault).  e4m3 inputs are compared
+with the oracle on their decoded values.
 """
 import numpy as np
 import pytest
@@ -112,6 +113,9 @@ CASES = [
     ("f16", 5, 4, 4, 6, 700, [127, 0, 640, 2, 383], True, [5, 0, 2, 1, 3]),
     ("bf16", 2, 12, 4, 2, 2048, [2047, 1024], False, [1, 0]),
     ("bf16", 6, 8, 8, 6, 513, [0, 0, 0, 512, 0, 0], False, None),      # mostly empty caches
+    ("bf16", 3, 6, 3, 3, 700, [64, 63, 639], True, [2, 0, 1]),          # odd H_k: one kv head per unit
+    ("f16", 2, 40, 2, 2, 400, [65, 399], True, None),                   # G = 20: one kv head per unit
+    ("e4m3", 2, 32, 2, 2, 400, [64, 398], True, None),                  # G = 16: two heads fill S^T
     ("e4m3", 4, 8, 2, 5, 1000, [0, 1, 517, 998], True, [3, 1, 0, 4]),
     ("e4m3", 4, 32, 1, 4, 300, [128, 129, 255, 1], False, None),
     ("e4m3", 3, 16, 16, 3, 4096, [895, 1791, 4095], True, None),
