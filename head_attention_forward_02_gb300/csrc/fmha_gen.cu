@@ -46,11 +46,8 @@ constexpr int kD = 128;                 // head dim
 constexpr int kKT = 128;                // rows per tile (MMA M of S^T): keys, or keys x 2 heads
 constexpr int kNP = 32;                 // query heads of a group, padded (MMA N)
 constexpr int kNSMax = 6;               // K/V ring stages at most (a K and a V tile each)
-constexpr int kBarBytes = 1536;         // barrier and scratch block
-constexpr int kSoftWarps = 4;           // warps 0-3: softmax and epilogue
-constexpr int kProdWarp = 4;            // TMA producer (lane 0), cache insert
-constexpr int kMmaWarp = 5;             // tcgen05.mma issuer (whole warp, one elected lane), owns TMEM
-constexpr int kThreads = 192;
+constexpr int kBarBytes = 2048;         // barrier and scratch block
+constexpr int kSoftWarpsMax = 8;        // softmax warps of the widest layout
 constexpr uint32_t kTmemCols = 128;     // S^T buffers in [0, 32) and [32, 64), O^T in [64, 96)
 constexpr int kPanelBytes = kKT * 128;  // 128 rows of one 128-byte swizzled panel
 constexpr int kQPanelBytes = kNP * 128;
@@ -116,7 +113,7 @@ struct GenBars {
     uint64_t kv_full[kNSMax], kv_empty[kNSMax];
     uint32_t tmem_base;
     int abort;
-    float red[kSoftWarps][kNP];         // per-warp partial max / sum of each head
+    float red[kSoftWarpsMax][kNP];      // per-warp partial max / sum of each column
     float alpha[kNP], mref[kNP];        // rescale factors and reference maxima of every column
     GenSched sched;
 };
@@ -356,6 +353,25 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]) {
+    if constexpr (N == 8) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                     "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                     : "memory");
+    } else if constexpr (N == 16) {
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+            "%14, %15, %16};" ::"r"(taddr),
+            "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+            "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+            : "memory");
+    } else {
+        static_assert(N == 32, "tcgen05.st width");
+        tmem_st32(taddr, r);
+    }
+}
+
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -364,21 +380,26 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Named barrier 1 over the 128 softmax threads, with a vote.
-__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barrier 1 over the N softmax threads, with a vote.
+template <int N>
+__device__ __forceinline__ void soft_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
+}
+template <int N>
 __device__ __forceinline__ bool soft_all(bool v) {
     uint32_t r;
-    asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 1, 128, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+    asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 1, %2, p;\nselp.u32 %0, 1, 0, q;\n}\n"
                  : "=r"(r)
-                 : "r"((uint32_t)v)
+                 : "r"((uint32_t)v), "n"(N)
                  : "memory");
     return r != 0;
 }
+template <int N>
 __device__ __forceinline__ bool soft_any(bool v) {
     uint32_t r;
-    asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, 1, 128, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+    asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, 1, %2, p;\nselp.u32 %0, 1, 0, q;\n}\n"
                  : "=r"(r)
-                 : "r"((uint32_t)v)
+                 : "r"((uint32_t)v), "n"(N)
                  : "memory");
     return r != 0;
 }
@@ -434,6 +455,21 @@ template <bool TWO>
 struct Unit {
     static constexpr int GP = TWO ? 2 : 1;
     static constexpr int TK = kKT / GP;
+};
+
+// Warp layout of a kernel instantiation.
+//   MODE 0: one kv head per unit; 4 softmax warps, one column group
+//   MODE 1: two kv heads per unit; 4 softmax warps, a column group per head
+//   MODE 2: one kv head per unit; 8 softmax warps, two column groups of 16
+//           (query groups wider than 16: the exponentials of a tile are
+//           shared by twice the threads)
+// The producer and MMA warps follow the softmax warps.
+template <int MODE>
+struct Layout {
+    static constexpr bool TWO = MODE == 1;
+    static constexpr int SW = MODE == 2 ? 8 : 4;
+    static constexpr int PROD = SW, MMA = SW + 1;
+    static constexpr int THREADS = (SW + 2) * 32;
 };
 
 template <bool TWO>
@@ -727,40 +763,46 @@ __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, G
     mbar_wait_drain(smem_u32(&bars->drain), 0);
 }
 
-// Softmax and epilogue: thread t of warps 0-3 owns row t of every tile (TMEM
-// lane t of S^T) and head dimension t of O^T.  Row t is key t of the unit's
-// kv head, or, in a two-head unit, key t % 64 of head t / 64 (warps 0-1: the
-// first head, warps 2-3: the second).
+// Softmax and epilogue.  Softmax warp w owns rows 32 (w % 4) .. + 31 of every
+// tile (its TMEM lanes of S^T) and the same rows of O^T (head dimensions).
+// A tile row is a key of the unit's kv head, or, in a two-head unit (MODE 1),
+// key r % 64 of head r / 64 (warps 0-1: the first head, warps 2-3: the
+// second).
 //
 // Columns of S^T are query heads: [0, G) of a one-head unit, or [0, G) and
 // [16, 16 + G) of a two-head unit (its Q tile is two 16-row halves).  A
-// thread works on NC >= G columns from c0 = 16 * (its kv head in the unit),
-// shared by its column group (the warps of that kv head); columns of a group
-// past G hold other heads' queries and feed only O^T columns that are never
-// stored.  In a two-head unit a row's weights in the other head's columns
-// are written as 0, so P.V over the 128 rows adds, for each column, only the
-// rows of its own kv head.
-template <int ELEM, int NC, bool TWO>
+// thread works on NC >= G columns from c0 = 16 * (its column group): the
+// warps of a kv head in MODE 1, warps 0-3 and 4-7 in MODE 2 (columns 0-15 and
+// 16-31), all four warps in MODE 0.  Columns of a group past G hold other
+// heads' queries and feed only O^T columns that are never stored.  In a
+// two-head unit a row's weights in the other head's columns are written as
+// 0, so P.V over the 128 rows adds, for each column, only the rows of its
+// own kv head; O^T rows then hold columns of both heads, so the rescale
+// factors and reference maxima of every column go through shared memory.
+template <int ELEM, int NC, int MODE>
 __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *smem, GenBars *bars, uint32_t tmem,
                             int warp, int lane) {
     using C = GenCfg<ELEM>;
+    using L = Layout<MODE>;
+    constexpr bool two = L::TWO;
+    constexpr int ST = L::SW * 32;                      // softmax threads
+    constexpr int NW = MODE == 1 ? 2 : 4;               // warps of a column group
     volatile int *abort_flag = &bars->abort;
-    const int t = warp * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const int r = (warp & 3) * 32 + lane;               // tile row = TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t o_tm = lane_base + 2 * kNP;
-    uint8_t *prow0 = smem + C::OFF_P + t * C::P_ROW;     // this row's P^T row in buffer 0
-    constexpr bool two = TWO;
-    const int hh = two ? warp >> 1 : 0;                 // kv head of this thread's rows within the unit
-    const int key_of_row = two ? t & 63 : t;
-    const int c0 = 16 * hh;                             // first column of this thread's group
-    const int w0 = 2 * hh;                              // first warp of the group (two-head units)
+    uint8_t *prow0 = smem + C::OFF_P + r * C::P_ROW;     // this row's P^T row in buffer 0
+    const int gi = MODE == 1 ? warp >> 1 : MODE == 2 ? warp >> 2 : 0;   // column group
+    const int c0 = 16 * gi;                             // its first column
+    const int w0 = gi * NW;                             // its first warp
+    const int key_of_row = two ? r & 63 : r;
     // P^T swizzle: 16-byte chunk index ^= (row / 2) % 4 (64-byte rows) or (row / 4) % 2 (32-byte rows)
-    const uint32_t swz = C::FP8 ? (t >> 2) & 1 : (t >> 1) & 3;
+    const uint32_t swz = C::FP8 ? (r >> 2) & 1 : (r >> 1) & 3;
     uint32_t oph = 0, cons = 0;
     GenCursor cur;
     for (;;) {
         GenItem it;
-        if (!gen_next<TWO>(p, sc, cur, it, false)) break;
+        if (!gen_next<two>(p, sc, cur, it, false)) break;
         float m[NC], l[NC];
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
@@ -768,13 +810,13 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
             l[c] = 0.f;         // this thread's part of the row sum
         }
         bool ok = true, first = true;
-        for (int k = it.k0; k < it.k1; k += Unit<TWO>::TK) {
+        for (int k = it.k0; k < it.k1; k += Unit<two>::TK) {
             // S^T_j and P^T_j use buffer j % 2.  The commit that completes
             // S^T_j also covers P.V_j-2, issued before it by the same thread,
             // so P^T buffer j % 2 is free to rewrite once S^T_j is here.
             const uint32_t b = cons & 1;
             const bool got = mbar_wait(smem_u32(&bars->s_full[b]), (cons >> 1) & 1, abort_flag);
-            if (!soft_all(got)) {
+            if (!soft_all<ST>(got)) {
                 ok = false;
                 break;
             }
@@ -795,7 +837,7 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
                 need |= s[c] > m[c] + kRescaleLog2;
             }
             bool rescaled = false;
-            if (soft_any(need)) {
+            if (soft_any<ST>(need)) {
                 // tile maximum of every column over the group's rows
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
@@ -804,12 +846,12 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
                     for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
                     if (lane == 0) bars->red[warp][c0 + c] = x;
                 }
-                soft_sync();
+                soft_sync<ST>();
                 float alpha[NC];
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
                     float tmax = fmaxf(bars->red[w0][c0 + c], bars->red[w0 + 1][c0 + c]);
-                    if (!two) tmax = fmaxf(tmax, fmaxf(bars->red[2][c], bars->red[3][c]));
+                    if (NW == 4) tmax = fmaxf(tmax, fmaxf(bars->red[w0 + 2][c0 + c], bars->red[w0 + 3][c0 + c]));
                     alpha[c] = 1.f;
                     if (tmax > m[c] + kRescaleLog2) {
                         alpha[c] = m[c] == -INFINITY ? 0.f : ex2(m[c] - tmax);
@@ -817,31 +859,39 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
                         m[c] = tmax;
                     }
                 }
-                if (!first) {
-                    // O^T row t holds every column: share the factors first
-                    if ((two ? warp == w0 : warp == 0) && lane == 0) {
+                if (two && !first && warp == w0 && lane == 0) {
 #pragma unroll
-                        for (int c = 0; c < NC; ++c) bars->alpha[c0 + c] = alpha[c];
-                    }
+                    for (int c = 0; c < NC; ++c) bars->alpha[c0 + c] = alpha[c];
                 }
-                soft_sync();   // the scratch rows may be rewritten after this
+                soft_sync<ST>();   // the scratch rows may be rewritten after this
                 if (!first) {
                     // O^T holds the P.V of the previous tile once it is done
                     const bool pv = mbar_wait(smem_u32(&bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag);
-                    if (!soft_all(pv)) {
+                    if (!soft_all<ST>(pv)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    uint32_t orr[32];
-                    tmem_ld32(o_tm, orr);
-                    tmem_wait_ld(orr);
+                    if constexpr (two) {
+                        // row r of O^T holds both heads' columns
+                        uint32_t orr[32];
+                        tmem_ld32(o_tm, orr);
+                        tmem_wait_ld(orr);
 #pragma unroll
-                    for (int h = 0; h < kNP; ++h)
-                        orr[h] = __float_as_uint(__uint_as_float(orr[h]) * bars->alpha[h]);
-                    tmem_st32(o_tm, orr);
+                        for (int h = 0; h < kNP; ++h)
+                            orr[h] = __float_as_uint(__uint_as_float(orr[h]) * bars->alpha[h]);
+                        tmem_st32(o_tm, orr);
+                        soft_sync<ST>();   // every thread has read the factors
+                    } else {
+                        // this group's columns of row r of O^T
+                        uint32_t orr[NC];
+                        tmem_ld_n<NC>(o_tm + c0, orr);
+                        tmem_wait_ld_n<NC>(orr);
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha[c]);
+                        tmem_st_n<NC>(o_tm + c0, orr);
+                    }
                     rescaled = true;
-                    soft_sync();   // every thread has read the factors
                 }
             }
             float pv[NC];
@@ -850,7 +900,7 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
                 pv[c] = m[c] == -INFINITY ? 0.f : ex2(s[c] - m[c]);
                 l[c] += pv[c];
             }
-            // P^T row t: columns [c0, c0 + NC) from pv and, in a two-head
+            // P^T row r: columns [c0, c0 + NC) from pv and, in a two-head
             // unit, 0 in the other head's columns (the remaining columns feed
             // only O^T columns that are never stored)
             uint8_t *prow = prow0 + b * C::P_BYTES;
@@ -881,17 +931,17 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
                 *reinterpret_cast<uint32_t *>(prow + ((((vo >> 4) ^ swz) << 4) | (vo & 15))) = w[0];
                 if (two) *reinterpret_cast<uint32_t *>(prow + ((((zo >> 4) ^ swz) << 4) | (zo & 15))) = 0u;
             }
-            if (!valid) {
+            if (!valid && (MODE != 2 || gi == 0)) {
                 // a row whose key is past the chunk's end: its V row (stale
                 // cache contents, possibly not finite) is zeroed so that P = 0
-                // contributes 0
+                // contributes 0 (by one column group of the row)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                uint8_t *vrow = smem + C::OFF_KV + st * C::STAGE_BYTES + C::TILE_BYTES + t * 128;
+                uint8_t *vrow = smem + C::OFF_KV + st * C::STAGE_BYTES + C::TILE_BYTES + r * 128;
 #pragma unroll
                 for (int pn = 0; pn < C::PANELS; ++pn)
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4 *>(vrow + pn * kPanelBytes + ((c ^ (t & 7)) << 4)) =
+                        *reinterpret_cast<uint4 *>(vrow + pn * kPanelBytes + ((c ^ (r & 7)) << 4)) =
                             make_uint4(0u, 0u, 0u, 0u);
             }
             // generic-proxy writes (P^T, zeroed V rows) become visible to the
@@ -905,11 +955,11 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
         }
         if (!ok) break;
 
-        // epilogue: row sums and reference maxima of every column, then the
-        // normalised partial O and its LSE
+        // epilogue: row sums of every column, then the normalised partial O
+        // and its LSE
         const bool got = mbar_wait(smem_u32(&bars->o_full), oph, abort_flag);
         oph ^= 1;
-        if (!soft_all(got)) break;
+        if (!soft_all<ST>(got)) break;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
@@ -918,36 +968,52 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
             for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
             if (lane == 0) bars->red[warp][c0 + c] = x;
         }
-        if ((two ? warp == w0 : warp == 0) && lane == 0) {
+        if (two && warp == w0 && lane == 0) {
 #pragma unroll
             for (int c = 0; c < NC; ++c) bars->mref[c0 + c] = m[c];
         }
-        soft_sync();
-        uint32_t orr[32];
-        tmem_ld32(o_tm, orr);
-        tmem_wait_ld(orr);
+        soft_sync<ST>();
         const int64_t row0 = (int64_t)it.b * p.H + (int64_t)it.g * p.G;
+        if constexpr (two) {
+            // row r of O^T: column h is query head row0 + G * (h / 16) + h % 16
+            uint32_t orr[32];
+            tmem_ld32(o_tm, orr);
+            tmem_wait_ld(orr);
 #pragma unroll
-        for (int h = 0; h < kNP; ++h) {
-            // column h: query head row0 + h (one-head unit), or row0 + G * (h / 16) + h % 16
-            if ((h & 15) < NC && (two ? (h & 15) < p.G : h < p.G)) {
-                const int g2 = two ? 2 * (h >> 4) : 0;
-                float lt = bars->red[g2][h] + bars->red[g2 + 1][h];
-                if (!two) lt += bars->red[2][h] + bars->red[3][h];
-                const int64_t qh = two ? row0 + (h >> 4) * p.G + (h & 15) : row0 + h;
-                const int64_t slot = qh * p.max_seg + it.seg;
-                p.part_o[slot * kD + t] = lt > 0.f ? __uint_as_float(orr[h]) / lt : 0.f;
-                if (t == h) p.part_lse[slot] = lt > 0.f ? (bars->mref[h] + log2f(lt)) * kLn2 : -INFINITY;
+            for (int h = 0; h < kNP; ++h) {
+                if ((h & 15) < NC && (h & 15) < p.G) {
+                    const int g2 = 2 * (h >> 4);
+                    const float lt = bars->red[g2][h] + bars->red[g2 + 1][h];
+                    const int64_t slot = (row0 + (h >> 4) * p.G + (h & 15)) * p.max_seg + it.seg;
+                    p.part_o[slot * kD + r] = lt > 0.f ? __uint_as_float(orr[h]) / lt : 0.f;
+                    if (r == h) p.part_lse[slot] = lt > 0.f ? (bars->mref[h] + log2f(lt)) * kLn2 : -INFINITY;
+                }
+            }
+        } else {
+            // this group's columns of row r of O^T: query heads row0 + c0 + c
+            uint32_t orr[NC];
+            tmem_ld_n<NC>(o_tm + c0, orr);
+            tmem_wait_ld_n<NC>(orr);
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                if (c0 + c < p.G) {
+                    const float lt = (bars->red[w0][c0 + c] + bars->red[w0 + 1][c0 + c]) +
+                                     (bars->red[w0 + 2][c0 + c] + bars->red[w0 + 3][c0 + c]);
+                    const int64_t slot = (row0 + c0 + c) * p.max_seg + it.seg;
+                    p.part_o[slot * kD + r] = lt > 0.f ? __uint_as_float(orr[c]) / lt : 0.f;
+                    if (r == c) p.part_lse[slot] = lt > 0.f ? (m[c] + log2f(lt)) * kLn2 : -INFINITY;
+                }
             }
         }
-        soft_sync();   // the scratch rows may be rewritten after this
+        soft_sync<ST>();   // the scratch rows may be rewritten after this
     }
 }
 
-template <int ELEM, int NC, bool TWO>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int ELEM, int NC, int MODE>
+__global__ void __launch_bounds__(Layout<MODE>::THREADS, 1)
     fmha_gen_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const GenParams p) {
+    using L = Layout<MODE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     GenBars *bars = reinterpret_cast<GenBars *>(smem + GenCfg<ELEM>::OFF_BARS);
@@ -959,8 +1025,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bars->s_full[b]), 1);
-            mbar_init(smem_u32(&bars->s_free[b]), kSoftWarps * 32);
-            mbar_init(smem_u32(&bars->p_full[b]), kSoftWarps);
+            mbar_init(smem_u32(&bars->s_free[b]), L::SW * 32);
+            mbar_init(smem_u32(&bars->p_full[b]), L::SW);
             mbar_init(smem_u32(&bars->pv_done[b]), 1);
         }
         mbar_init(smem_u32(&bars->o_full), 1);
@@ -973,27 +1039,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kNP; ++i) bars->alpha[i] = 1.f;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == kMmaWarp) {
+    if (warp == L::MMA) {
         tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
         tmem_relinquish();
     }
-    if (warp == kProdWarp) gen_schedule<TWO>(p, &bars->sched, lane);
+    if (warp == L::PROD) gen_schedule<L::TWO>(p, &bars->sched, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const GenSched sc = bars->sched;
-    if (warp < kSoftWarps) {
-        gen_softmax<ELEM, NC, TWO>(p, sc, smem, bars, tmem, warp, lane);
-    } else if (warp == kProdWarp) {
-        if (lane == 0) gen_producer<ELEM, TWO>(p, sc, &tmQ, &tmK, &tmV, smem, bars);
+    if (warp < L::SW) {
+        gen_softmax<ELEM, NC, MODE>(p, sc, smem, bars, tmem, warp, lane);
+    } else if (warp == L::PROD) {
+        if (lane == 0) gen_producer<ELEM, L::TWO>(p, sc, &tmQ, &tmK, &tmV, smem, bars);
     } else {
-        gen_mma<ELEM, TWO>(p, sc, smem, bars, tmem);
+        gen_mma<ELEM, L::TWO>(p, sc, smem, bars, tmem);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kMmaWarp) {
+    if (warp == L::MMA) {
         __syncwarp();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -1150,20 +1216,20 @@ struct GenLayout {
     size_t o_bytes, lse_off, total;
 };
 
-// Instantiations: two-head units with 4, 8 or 16 columns per thread (G <= 16),
-// one-head units with 8, 16 or 32 (G <= 32).
+// Instantiations: two-head units with 4, 8 or 16 columns per thread (G <= 16);
+// one-head units with 8 or 16 (G <= 16), or two groups of 16 (G > 16).
 using GenKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, GenParams);
 template <int ELEM>
-GenKernel gen_kernel_nc(int nc, bool two) {
-    if (two)
-        return nc == 4 ? fmha_gen_kernel<ELEM, 4, true>
-               : nc == 8 ? fmha_gen_kernel<ELEM, 8, true> : fmha_gen_kernel<ELEM, 16, true>;
-    return nc == 8 ? fmha_gen_kernel<ELEM, 8, false>
-           : nc == 16 ? fmha_gen_kernel<ELEM, 16, false> : fmha_gen_kernel<ELEM, 32, false>;
+GenKernel gen_kernel_nc(int nc, int mode) {
+    if (mode == 1)
+        return nc == 4 ? fmha_gen_kernel<ELEM, 4, 1>
+               : nc == 8 ? fmha_gen_kernel<ELEM, 8, 1> : fmha_gen_kernel<ELEM, 16, 1>;
+    if (mode == 2) return fmha_gen_kernel<ELEM, 16, 2>;
+    return nc == 8 ? fmha_gen_kernel<ELEM, 8, 0> : fmha_gen_kernel<ELEM, 16, 0>;
 }
-GenKernel gen_kernel_for(int dt, int nc, bool two) {
-    return dt == FMHA_BF16 ? gen_kernel_nc<FMHA_BF16>(nc, two)
-           : dt == FMHA_F16 ? gen_kernel_nc<FMHA_F16>(nc, two) : gen_kernel_nc<FMHA_E4M3>(nc, two);
+GenKernel gen_kernel_for(int dt, int nc, int mode) {
+    return dt == FMHA_BF16 ? gen_kernel_nc<FMHA_BF16>(nc, mode)
+           : dt == FMHA_F16 ? gen_kernel_nc<FMHA_F16>(nc, mode) : gen_kernel_nc<FMHA_E4M3>(nc, mode);
 }
 
 // Two adjacent kv heads share a work unit when H_k is even and each query
@@ -1284,14 +1350,17 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
 
     // ---- launch: persistent CTAs over the work items, then the merge ----
     const int grid = sms;   // one persistent CTA per SM; each streams 1/grid of the tiles
-    // columns of S^T a softmax thread works on: the query group, rounded up
+    // warp layout, and the columns of S^T a softmax thread works on (the
+    // query group rounded up; 16 per column group for groups wider than 16)
     const int G = H / H_k;
-    const int nc = G <= 4 && p.GP == 2 ? 4 : G <= 8 ? 8 : G <= 16 ? 16 : 32;
-    auto kern = gen_kernel_for(dt, nc, p.GP == 2);
+    const int mode = p.GP == 2 ? 1 : G > 16 ? 2 : 0;
+    const int nc = mode == 1 && G <= 4 ? 4 : G <= 8 ? 8 : 16;
+    const int threads = mode == 2 ? Layout<2>::THREADS : Layout<0>::THREADS;
+    auto kern = gen_kernel_for(dt, nc, mode);
     const int smem_bytes = dt == FMHA_E4M3 ? GenCfg<FMHA_E4M3>::SMEM_BYTES : GenCfg<FMHA_BF16>::SMEM_BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
         return FMHA_ERR_CUDA;
-    kern<<<grid, kThreads, smem_bytes, stream>>>(tq, tk, tv, p);
+    kern<<<grid, threads, smem_bytes, stream>>>(tq, tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
     const int rows = B * H;
     auto merge = dt == FMHA_BF16 ? fmha_gen_merge_kernel<FMHA_BF16>

@@ -116,6 +116,9 @@ CASES = [
     ("bf16", 3, 6, 3, 3, 700, [64, 63, 639], True, [2, 0, 1]),          # odd H_k: one kv head per unit
     ("f16", 2, 40, 2, 2, 400, [65, 399], True, None),                   # G = 20: one kv head per unit
     ("e4m3", 2, 32, 2, 2, 400, [64, 398], True, None),                  # G = 16: two heads fill S^T
+    ("bf16", 2, 48, 2, 2, 900, [300, 899], True, None),                 # G = 24: two column groups of 16
+    ("e4m3", 3, 96, 3, 3, 500, [129, 0, 499], False, [1, 2, 0]),        # G = 32, odd H_k
+    ("f16", 2, 6, 3, 2, 300, [1, 255], True, None),                     # G = 2, odd H_k
     ("e4m3", 4, 8, 2, 5, 1000, [0, 1, 517, 998], True, [3, 1, 0, 4]),
     ("e4m3", 4, 32, 1, 4, 300, [128, 129, 255, 1], False, None),
     ("e4m3", 3, 16, 16, 3, 4096, [895, 1791, 4095], True, None),
