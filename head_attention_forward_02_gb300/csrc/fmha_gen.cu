@@ -1048,6 +1048,9 @@ __global__ void __launch_bounds__(Layout<MODE>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    // the merge kernel may be scheduled as CTAs of this grid exit; it waits
+    // for this grid's completion before it reads the partials
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const GenSched sc = bars->sched;
     if (warp < L::SW) {
         gen_softmax<ELEM, NC, MODE>(p, sc, smem, bars, tmem, warp, lane);
@@ -1112,6 +1115,9 @@ __global__ void __launch_bounds__(kMergeThreads) fmha_gen_merge_kernel(const Gen
         const long long off = pre + (long long)u * nt;
         nch = (int)((off + nt - 1) / per - off / per + 1);
     }
+    // the partials are the attention kernel's: wait for it (and its memory)
+    // here; everything above overlaps its tail
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const float *lse_c = p.part_lse + (int64_t)row * p.max_seg;
     float mx = -INFINITY;
     for (int c = threadIdx.x; c < nch; c += kMergeThreads) mx = fmaxf(mx, lse_c[c]);
@@ -1365,7 +1371,18 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
     const int rows = B * H;
     auto merge = dt == FMHA_BF16 ? fmha_gen_merge_kernel<FMHA_BF16>
                  : dt == FMHA_F16 ? fmha_gen_merge_kernel<FMHA_F16> : fmha_gen_merge_kernel<FMHA_E4M3>;
-    merge<<<rows, kMergeThreads, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
+    // launched as a programmatic dependent of the attention kernel, so its
+    // launch and prologue overlap that kernel's tail
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rows);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, merge, p) != cudaSuccess) return FMHA_ERR_CUDA;
     return FMHA_OK;
 }
