@@ -1370,6 +1370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    // a dependent kernel (the split-KV combine) may be scheduled as CTAs of
+    // this grid exit; it waits for this grid's completion before its reads
+    if constexpr (SPLIT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp < kProducerWarp) {
         softmax_wg<C, SPLIT>(p, bars, tmem, warp, lane);

@@ -72,6 +72,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Param
     const int h = (int)(item - row * p.H);
     const int ns = p.num_splits;
     const int64_t split_stride = p.part_rows * p.H;          // elements between splits of part_lse
+    // the partials are the attention kernel's: wait for it (and its memory)
+    // here; the launch and the lines above overlap its tail
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const float *plse = p.part_lse + row * p.H + h;
     float m = -INFINITY;
     for (int s = lane; s < ns; s += 32) m = fmaxf(m, plse[s * split_stride]);
@@ -120,13 +123,21 @@ int launch_combine(const Params &p, cudaStream_t stream) {
     const int64_t blocks = (items + kCombineWarps - 1) / kCombineWarps;
     if (blocks <= 0) return FMHA_OK;
     if (blocks > 0x7fffffff) return FMHA_ERR_UNSUPPORTED;
-    switch (p.D) {
-    case 32: combine_kernel<32><<<(unsigned)blocks, kCombineWarps * 32, 0, stream>>>(p); break;
-    case 64: combine_kernel<64><<<(unsigned)blocks, kCombineWarps * 32, 0, stream>>>(p); break;
-    case 128: combine_kernel<128><<<(unsigned)blocks, kCombineWarps * 32, 0, stream>>>(p); break;
-    default: return FMHA_ERR_INVALID_ARG;
-    }
-    return cudaGetLastError() == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
+    void (*kern)(Params) = p.D == 32 ? combine_kernel<32> : p.D == 64 ? combine_kernel<64>
+                         : p.D == 128 ? combine_kernel<128> : nullptr;
+    if (!kern) return FMHA_ERR_INVALID_ARG;
+    // a programmatic dependent of the attention kernel launched just before
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kCombineWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
 }
 
 }  // namespace fmha
