@@ -75,6 +75,10 @@ def _load():
         lib.oracle_attn_bwd_f64.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 5 + [
             ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_int]
+        lib.oracle_attn_bwd_o_f64.restype = ctypes.c_int
+        lib.oracle_attn_bwd_o_f64.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [
+            ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -205,5 +209,21 @@ def attn_bwd_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray, 
     if lib.oracle_attn_bwd_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data, B, H, Sq, Sk, D,
                                float(scale), mask, causal_type, dq.ctypes.data, dk.ctypes.data,
                                dv.ctypes.data, int(threads)) != 0:
+        raise ValueError("oracle rejected the arguments")
+    return dq, dk, dv
+
+
+def attn_bwd_o_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarray, dout: np.ndarray, scale: float,
+                   mask: int = MASK_NONE, causal_type: int = QBEGIN, threads: int = 0):
+    """Backward with D_i = dO_i . O_i formed from the given O [B,Sq,H,D] (the row sums of
+    O * dO).  See ``oracle_attn_bwd_o_f64`` in ``fmha_oracle.c``."""
+    lib = _load()
+    q, k, v, o, g = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v, o, dout))
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    if lib.oracle_attn_bwd_o_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data, o.ctypes.data, g.ctypes.data, B,
+                                 H, Sq, Sk, D, float(scale), mask, causal_type, dq.ctypes.data,
+                                 dk.ctypes.data, dv.ctypes.data, int(threads)) != 0:
         raise ValueError("oracle rejected the arguments")
     return dq, dk, dv

@@ -449,6 +449,11 @@ int oracle_gen_fwd(const void *q, const void *k_cache, const void *v_cache,
  * Layouts as the forward (fixed length): q, dq, do [B, Sq, H, D];
  * k, v, dk, dv [B, Sk, H, D] (H_k = H).  All arrays are double.  Rows without
  * a visible key contribute nothing.  Returns 0, or -1 on bad arguments.
+ *
+ * oracle_attn_bwd_o_f64 takes O as an input and forms D_i = dO_i . O_i from
+ * it, the page's first step (row sums of O * dO): with the exact O the two
+ * agree; with a stored O (rounded to the input type) this is what a backward
+ * pass that reads that O computes.
  */
 int oracle_attn_fwd_f64(const double *q, const double *k, const double *v, int B, int H, int Sq, int Sk,
                         int D, double scale, int mask, int causal_type, double *o, double *lse) {
@@ -486,9 +491,9 @@ int oracle_attn_fwd_f64(const double *q, const double *k, const double *v, int B
     return 0;
 }
 
-int oracle_attn_bwd_f64(const double *q, const double *k, const double *v, const double *dout, int B, int H,
-                        int Sq, int Sk, int D, double scale, int mask, int causal_type, double *dq, double *dk,
-                        double *dv, int n_threads) {
+static int attn_bwd(const double *q, const double *k, const double *v, const double *o, const double *dout,
+                    int B, int H, int Sq, int Sk, int D, double scale, int mask, int causal_type, double *dq,
+                    double *dk, double *dv, int n_threads) {
     if (B < 0 || H <= 0 || Sq < 0 || Sk < 0 || D <= 0) return -1;
     const int64_t nq = (int64_t)B * Sq * H * D, nk = (int64_t)B * Sk * H * D;
     for (int64_t x = 0; x < nq; ++x) dq[x] = 0.0;
@@ -525,7 +530,7 @@ int oracle_attn_bwd_f64(const double *q, const double *k, const double *v, const
                     p[j] = p[j] == -INFINITY ? 0.0 : exp(p[j] - m);
                     l += p[j];
                 }
-                /* dP = dO_i . V_j, and D_i = sum_j P_ij dP_ij */
+                /* dP = dO_i . V_j, and D_i = sum_j P_ij dP_ij (or dO_i . O_i from a given O) */
                 double Di = 0.0;
                 for (int64_t j = 0; j < Sk; ++j) {
                     p[j] /= l;
@@ -535,6 +540,11 @@ int oracle_attn_bwd_f64(const double *q, const double *k, const double *v, const
                     for (int d = 0; d < D; ++d) dot += gi[d] * vj[d];
                     dp[j] = dot;
                     Di += p[j] * dot;
+                }
+                if (o) {
+                    const double *oi = o + ((b * Sq + i) * H + h) * D;
+                    Di = 0.0;
+                    for (int d = 0; d < D; ++d) Di += gi[d] * oi[d];
                 }
                 double *dqi = dq + ((b * Sq + i) * H + h) * D;
                 for (int64_t j = 0; j < Sk; ++j) {
@@ -555,4 +565,17 @@ int oracle_attn_bwd_f64(const double *q, const double *k, const double *v, const
         free(dp);
     }
     return 0;
+}
+
+int oracle_attn_bwd_f64(const double *q, const double *k, const double *v, const double *dout, int B, int H,
+                        int Sq, int Sk, int D, double scale, int mask, int causal_type, double *dq, double *dk,
+                        double *dv, int n_threads) {
+    return attn_bwd(q, k, v, NULL, dout, B, H, Sq, Sk, D, scale, mask, causal_type, dq, dk, dv, n_threads);
+}
+
+int oracle_attn_bwd_o_f64(const double *q, const double *k, const double *v, const double *o, const double *dout,
+                          int B, int H, int Sq, int Sk, int D, double scale, int mask, int causal_type, double *dq,
+                          double *dk, double *dv, int n_threads) {
+    if (!o) return -1;
+    return attn_bwd(q, k, v, o, dout, B, H, Sq, Sk, D, scale, mask, causal_type, dq, dk, dv, n_threads);
 }

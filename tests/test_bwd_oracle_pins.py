@@ -87,3 +87,40 @@ def test_keys_no_query_sees_get_no_gradient():
     # q-end with more queries than keys: the first rows see no key and get no gradient
     dq, _, _ = oracle.attn_bwd_f64(*rand(7, 1, 9, 4, 2, 8), 0.5, CAUSAL, QE)
     assert np.all(dq[:, :5] == 0) and np.abs(dq[:, 5:]).max() > 0
+
+
+@pytest.mark.parametrize("mask,ct,Sq,Sk", [(NONE, QB, 5, 7), (CAUSAL, QB, 6, 6), (CAUSAL, QE, 7, 4)])
+def test_given_o_backward_equals_the_definition_with_the_exact_o(mask, ct, Sq, Sk):
+    # D_i = dO_i . O_i from the exact O is the same number as sum_j P_ij dP_ij
+    q, k, v, g = rand(Sq * 7 + Sk, 2, Sq, Sk, 2, 4)
+    o, _ = oracle.attn_fwd_f64(q, k, v, 0.6, mask, ct)
+    for a, b in zip(oracle.attn_bwd_o_f64(q, k, v, o, g, 0.6, mask, ct), oracle.attn_bwd_f64(q, k, v, g, 0.6, mask, ct)):
+        assert np.allclose(a, b, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("mask,ct,Sq,Sk", [(NONE, QB, 5, 7), (CAUSAL, QB, 6, 6), (CAUSAL, QE, 7, 4)])
+def test_given_o_backward_responds_to_a_changed_o_by_the_closed_form(mask, ct, Sq, Sk):
+    # O -> O + E changes D_i by c_i = dO_i . E_i, so dS_ij by -P_ij c_i:
+    # dQ_i by -scale c_i sum_j P_ij K_j, dK_j by -scale sum_i P_ij c_i Q_i, dV not at all.
+    # P comes from the forward oracle with unit-vector values (O = P exactly).
+    B, H, D, scale = 1, 2, 4, 0.6
+    q, k, v, g = rand(Sq * 3 + Sk, B, Sq, Sk, H, D)
+    o, _ = oracle.attn_fwd_f64(q, k, v, scale, mask, ct)
+    e = np.random.default_rng(5).standard_normal(o.shape)
+    # P [B, Sq, H, Sk], D columns at a time: V_j = the unit vector e_(j - j0) for keys
+    # j in [j0, j0 + D), 0 for the others, gives O = P[:, :, :, j0:j0 + D]
+    p = np.zeros((B, Sq, H, Sk))
+    for j0 in range(0, Sk, D):
+        unit = np.zeros((B, Sk, H, D))
+        for j in range(j0, min(j0 + D, Sk)):
+            unit[:, j, :, j - j0] = 1.0
+        pc, _ = oracle.attn_fwd_f64(q, k, unit, scale, mask, ct)
+        p[..., j0:j0 + D] = pc[..., :min(D, Sk - j0)]
+    c = np.sum(g * e, axis=-1)                                       # [B, Sq, H]
+    dq0, dk0, dv0 = oracle.attn_bwd_o_f64(q, k, v, o, g, scale, mask, ct)
+    dq1, dk1, dv1 = oracle.attn_bwd_o_f64(q, k, v, o + e, g, scale, mask, ct)
+    want_dq = -scale * c[..., None] * np.einsum("bihj,bjhd->bihd", p, k)
+    want_dk = -scale * np.einsum("bihj,bih,bihd->bjhd", p, c, q)
+    assert np.allclose(dq1 - dq0, want_dq, rtol=0, atol=1e-12)
+    assert np.allclose(dk1 - dk0, want_dk, rtol=0, atol=1e-12)
+    assert np.array_equal(dv1, dv0)
