@@ -845,8 +845,9 @@ def run_gen_reference(args, rank, world):
         flush=True)
 
 
-BWD_SHAPES = {   # name -> (B, H, S, D, mask); synthetic N(0,1) q, k, v, dO
+BWD_SHAPES = {   # name -> (B, H, S, D, mask[, dtype]); synthetic N(0,1) q, k, v, dO
     "bwd_bf16_causal_b2_h16_s8192_d128": (2, 16, 8192, 128, "causal"),
+    "bwd_e4m3_causal_b2_h16_s8192_d128": (2, 16, 8192, 128, "causal", "e4m3"),
     "bwd_bf16_nomask_b2_h16_s8192_d128": (2, 16, 8192, 128, "none"),
     "bwd_bf16_causal_b4_h16_s2048_d128": (4, 16, 2048, 128, "causal"),
     "bwd_bf16_causal_b2_h16_s4096_d128": (2, 16, 4096, 128, "causal"),   # profiling size (7 x 32 MB)
@@ -865,14 +866,18 @@ def run_bwd(args, rank, world, local):
     build.build()
     fm.lib()
     dev = torch.device("cuda", local if world > 1 else 0)
-    B, H, S, D, mask = BWD_SHAPES[args.bwd_config]
+    B, H, S, D, mask = BWD_SHAPES[args.bwd_config][:5]
+    dtype = (BWD_SHAPES[args.bwd_config][5:] or ("bf16",))[0]
+    tdt = wl.DTYPES[dtype]
     stream = torch.cuda.current_stream(dev)
     g = torch.Generator().manual_seed(31)
-    host = {n: torch.randn(B, S, H, D, generator=g).to(torch.bfloat16) for n in ("q", "k", "v", "do")}
+    host = {n: torch.randn(B, S, H, D, generator=g).clamp_(-448, 448).to(tdt) for n in ("q", "k", "v", "do")}
     d = {n: t.to(dev) for n, t in host.items()}
     o, lse = fm.fwd(d["q"], d["k"], d["v"], mask=mask)
-    ws = torch.empty(fm.fmha_bwd_workspace_size(B, H, S), dtype=torch.uint8, device=dev)
-    grads = [torch.empty_like(d["q"]) for _ in range(3)]
+    code = {"f16": fm.F16, "bf16": fm.BF16, "e4m3": fm.E4M3}[dtype]
+    ws = torch.empty(fm.fmha_bwd_workspace_size_ex(B, H, S, S, D, code), dtype=torch.uint8, device=dev)
+    grads = [torch.empty(d["q"].shape, dtype=torch.bfloat16 if dtype == "e4m3" else tdt, device=dev)
+             for _ in range(3)]
     flops = bwd_flops(B, H, S, D, mask == "causal")
 
     def step():
@@ -912,8 +917,8 @@ def run_bwd(args, rank, world, local):
     pin["o"], pin["lse"] = o.cpu().pin_memory(), lse.cpu().pin_memory()
     e2e_sets = [{n: torch.empty_like(t, device=dev) for n, t in pin.items()} for _ in range(2)]
     for es in e2e_sets:
-        es.update({"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["q"]), "dv": torch.empty_like(d["q"]),
-                   "ws": torch.empty_like(ws)})
+        es.update({"dq": torch.empty_like(grads[0]), "dk": torch.empty_like(grads[0]),
+                   "dv": torch.empty_like(grads[0]), "ws": torch.empty_like(ws)})
     outs = [{n: torch.empty(tuple(host["q"].shape), dtype=torch.bfloat16).pin_memory() for n in ("dq", "dk", "dv")}
             for _ in range(2)]
 
@@ -935,8 +940,9 @@ def run_bwd(args, rank, world, local):
         "metric": "FMHA backward TFLOP/s (5 products of the chain rule) and % of GB300 dense bf16 peak",
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded N(0,1) q, k, v, dO; O and LSE from fmha_fwd)",
+        "dtype": dtype, "data": "synthetic (seeded N(0,1) q, k, v, dO; O and LSE from fmha_fwd)",
         "config": {"workload": args.bwd_config, "op": "fmha_bwd", "B": B, "H": H, "S": S, "D": D, "mask": mask,
+                   "gradients": "bf16" if dtype == "e4m3" else dtype,
                    "l2": f"inputs and outputs {7 * B * S * H * D * 2 / 2**20:.0f} MiB (> L2)",
                    "parallelism": f"replicas x{world} (independent problems)"},
         "roofline": {"bound": "tensor", "achieved": round(flops / (ms * 1e-3) / 1e12, 2), "peak": peak,
@@ -946,7 +952,7 @@ def run_bwd(args, rank, world, local):
                      "note": "two-pass design: S and dP are computed in both the dQ and the dK/dV kernel"},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * K,
+        "gpu_launches": (4 if dtype == "e4m3" else 3) * K,
         "clocks": sampler.summary(t_host0, t_host1),
     }
     if not args.no_cpu_baseline:

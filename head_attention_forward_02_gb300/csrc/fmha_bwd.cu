@@ -28,7 +28,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <mutex>
 
@@ -1200,6 +1202,40 @@ int bwd_launch(const BwdParams &p, bool bf, cudaStream_t stream) {
     return bwd_launch_mode<BCfg<D, kDKDV>, kDKDV>(tq2, tk, tv, to2, p, bf, sms, stream);
 }
 
+// e4m3 inputs: every e4m3 value is a bf16 value, so the inputs are widened
+// exactly into the workspace and differentiated on the bf16 path.  One launch
+// for the five tensors; each thread converts 16 codes (16 bytes in, 32 out).
+struct Widen {
+    const uint8_t *src[5];
+    __nv_bfloat16 *dst[5];
+    int64_t n16[5];                     // 16-element groups of each tensor (its size is a multiple of 64)
+};
+
+__global__ void __launch_bounds__(256) widen_e4m3_kernel(const Widen w) {
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int t = 0; t < 5; ++t) {
+        for (int64_t g = i; g < w.n16[t]; g += stride) {
+            const uint4 x = reinterpret_cast<const uint4 *>(w.src[t])[g];
+            const uint32_t in[4] = {x.x, x.y, x.z, x.w};
+            uint32_t out[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const __nv_fp8x2_storage_t two = (__nv_fp8x2_storage_t)(in[k] >> (16 * h));
+                    const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3)));
+                    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+                    out[2 * k + h] = *reinterpret_cast<const uint32_t *>(&b);
+                }
+            }
+            uint4 *d = reinterpret_cast<uint4 *>(w.dst[t]) + 2 * g;
+            d[0] = make_uint4(out[0], out[1], out[2], out[3]);
+            d[1] = make_uint4(out[4], out[5], out[6], out[7]);
+        }
+    }
+}
+
 }  // namespace
 
 int bwd_read_status(int reset) {
@@ -1221,6 +1257,33 @@ extern "C" size_t fmha_bwd_workspace_size(int B, int H, int Sq) {
     if (B <= 0 || H <= 0 || Sq <= 0) return 0;
     const size_t sq_pad = ((size_t)Sq + kT - 1) / kT * kT;
     return 2 * (size_t)B * H * sq_pad * sizeof(float);
+}
+
+namespace {
+// e4m3 workspace: the row vectors, then bf16 copies of q, o, dout (B*Sq*H*D
+// each) and k, v (B*Sk*H*D each), every region 256-byte aligned.
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+struct WidenLayout {
+    size_t q, o, dout, k, v, total;
+};
+WidenLayout widen_layout(int B, int H, int Sq, int Sk, int D) {
+    WidenLayout l;
+    const size_t qb = (size_t)B * Sq * H * D * 2, kb = (size_t)B * Sk * H * D * 2;
+    l.q = align256(fmha_bwd_workspace_size(B, H, Sq));
+    l.o = l.q + align256(qb);
+    l.dout = l.o + align256(qb);
+    l.k = l.dout + align256(qb);
+    l.v = l.k + align256(kb);
+    l.total = l.v + kb;
+    return l;
+}
+}  // namespace
+
+extern "C" size_t fmha_bwd_workspace_size_ex(int B, int H, int Sq, int Sk, int D, int dtype) {
+    if (B <= 0 || H <= 0 || Sq <= 0 || Sk < 0 || (D != 64 && D != 128)) return 0;
+    if (dtype == FMHA_F16 || dtype == FMHA_BF16) return fmha_bwd_workspace_size(B, H, Sq);
+    if (dtype != FMHA_E4M3) return 0;
+    return widen_layout(B, H, Sq, Sk, D).total;
 }
 
 extern "C" int fmha_bwd(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor o, fmha_tensor dout,
@@ -1252,24 +1315,53 @@ extern "C" int fmha_bwd(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor
     for (int i = 0; i < 9; ++i)
         if (need[i] && !ptrs[i]) return FMHA_ERR_INVALID_ARG;
     const int dt = q.dtype;
-    if (dt != FMHA_F16 && dt != FMHA_BF16) return FMHA_ERR_UNSUPPORTED;
-    const fmha_tensor all[8] = {q, k, v, o, dout, dq, dk, dv};
-    for (const fmha_tensor &t : all)
+    if (dt != FMHA_F16 && dt != FMHA_BF16 && dt != FMHA_E4M3) return FMHA_ERR_UNSUPPORTED;
+    const bool fp8 = dt == FMHA_E4M3;
+    const int gdt = fp8 ? FMHA_BF16 : dt;                     // gradients: bf16 for e4m3 inputs
+    const fmha_tensor ins[5] = {q, k, v, o, dout}, grads[3] = {dq, dk, dv};
+    for (const fmha_tensor &t : ins)
         if (t.data && t.dtype != dt) return FMHA_ERR_UNSUPPORTED;
+    for (const fmha_tensor &t : grads)
+        if (t.data && t.dtype != gdt) return FMHA_ERR_UNSUPPORTED;
     for (int i = 0; i < 9; ++i) {
         const uintptr_t a = reinterpret_cast<uintptr_t>(ptrs[i]);
         if (i == 5 ? (a & 3u) != 0 : (a & 15u) != 0) return i == 5 ? FMHA_ERR_INVALID_ARG : FMHA_ERR_UNSUPPORTED;
     }
-    const size_t need_ws = fmha_bwd_workspace_size(B, H, Sq);
+    const size_t need_ws = fmha_bwd_workspace_size_ex(B, H, Sq, Sk, D, dt);
     if (Sq > 0 && (!workspace || workspace_bytes < need_ws || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return FMHA_ERR_INVALID_ARG;
+    const void *qx = q.data, *kx = k.data, *vx = v.data, *ox = o.data, *dox = dout.data;
+    if (fp8) {
+        const WidenLayout l = widen_layout(B, H, Sq, Sk, D);
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        Widen w{};
+        const void *src[5] = {q.data, o.data, dout.data, k.data, v.data};
+        const size_t off[5] = {l.q, l.o, l.dout, l.k, l.v};
+        const int64_t rows[5] = {(int64_t)B * Sq, (int64_t)B * Sq, (int64_t)B * Sq, (int64_t)B * Sk,
+                                 (int64_t)B * Sk};
+        int64_t most = 0;
+        for (int t = 0; t < 5; ++t) {
+            w.src[t] = static_cast<const uint8_t *>(src[t]);
+            w.dst[t] = reinterpret_cast<__nv_bfloat16 *>(ws + off[t]);
+            w.n16[t] = rows[t] * H * D / 16;
+            most = w.n16[t] > most ? w.n16[t] : most;
+        }
+        const int64_t blocks = (most + 255) / 256;
+        widen_e4m3_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(w);
+        if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
+        qx = w.dst[0];
+        ox = w.dst[1];
+        dox = w.dst[2];
+        kx = w.dst[3];
+        vx = w.dst[4];
+    }
 
     BwdParams p{};
-    p.q = q.data;
-    p.k = k.data;
-    p.v = v.data;
-    p.o = o.data;
-    p.dout = dout.data;
+    p.q = qx;
+    p.k = kx;
+    p.v = vx;
+    p.o = ox;
+    p.dout = dox;
     p.lse = lse;
     p.sq_pad = (Sq + kT - 1) / kT * kT;
     p.nl = static_cast<float *>(workspace);
@@ -1286,6 +1378,6 @@ extern "C" int fmha_bwd(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor
     p.mask = mask;
     p.causal_type = causal_type;
     p.off = (mask == FMHA_MASK_CAUSAL && causal_type == FMHA_CAUSAL_QEND) ? Sk - Sq : 0;
-    const bool bf = dt == FMHA_BF16;
+    const bool bf = gdt == FMHA_BF16;
     return D == 64 ? bwd_launch<64>(p, bf, stream) : bwd_launch<128>(p, bf, stream);
 }

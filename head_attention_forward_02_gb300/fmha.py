@@ -81,6 +81,8 @@ def lib():
             ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         L.fmha_bwd_workspace_size.restype = ctypes.c_size_t
         L.fmha_bwd_workspace_size.argtypes = [ctypes.c_int] * 3
+        L.fmha_bwd_workspace_size_ex.restype = ctypes.c_size_t
+        L.fmha_bwd_workspace_size_ex.argtypes = [ctypes.c_int] * 6
         L.fmha_status_string.restype = ctypes.c_char_p
         L.fmha_status_string.argtypes = [ctypes.c_int]
         L.fmha_device_status.restype = ctypes.c_int
@@ -295,19 +297,25 @@ def fmha_bwd_workspace_size(B, H, Sq) -> int:
     return int(lib().fmha_bwd_workspace_size(int(B), int(H), int(Sq)))
 
 
+def fmha_bwd_workspace_size_ex(B, H, Sq, Sk, D, dtype) -> int:
+    return int(lib().fmha_bwd_workspace_size_ex(int(B), int(H), int(Sq), int(Sk), int(D), int(dtype)))
+
+
 def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, dout: torch.Tensor,
         lse: torch.Tensor, *, scale: Optional[float] = None, mask: str = "none", causal_type: str = "qbegin",
         dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
         workspace: Optional[torch.Tensor] = None, stream=None):
     """Backward of fwd (see fmha_bwd): q, o, dout [B,Sq,H,D]; k, v [B,Sk,H,D];
-    lse [B,H,Sq] from fwd.  Allocates the gradients and the workspace with torch
-    when not given.  Returns (dq, dk, dv)."""
+    lse [B,H,Sq] from fwd.  Allocates the gradients (bf16 for e4m3 inputs, else
+    the inputs' type) and the workspace with torch when not given.  Returns
+    (dq, dk, dv)."""
     B, Sq, H, D = q.shape
     Sk = k.shape[1]
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    nbytes = fmha_bwd_workspace_size(B, H, Sq)
+    gdt = torch.bfloat16 if q.dtype == torch.float8_e4m3fn else q.dtype
+    dq = torch.empty(q.shape, dtype=gdt, device=q.device) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=gdt, device=k.device) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=gdt, device=v.device) if dv is None else dv
+    nbytes = fmha_bwd_workspace_size_ex(B, H, Sq, Sk, D, _TORCH_DTYPE[q.dtype])
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     sc = 1.0 / math.sqrt(D) if scale is None else scale

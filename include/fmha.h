@@ -279,15 +279,22 @@ size_t fmha_gen_workspace_size(int B, int H, int H_k, int D, int S_max);
  *   dK = scale dS^T Q.
  * Inputs: q, o, dout [B, Sq, H, D]; k, v [B, Sk, H, D] (H_k = H: no GQA);
  * lse float [B, H, Sq] as written by fmha_fwd for the same q, k, v, mask.
- * Outputs: dq [B, Sq, H, D], dk, dv [B, Sk, H, D], same dtype (FMHA_F16 or
- * FMHA_BF16).  D is 64 or 128; mask NONE, RESIDUAL or CAUSAL (q-begin or
- * q-end), as fmha_fwd.  Fixed length only.  Tensors 16-byte aligned, lse
- * 4-byte aligned.
- * workspace: caller-owned, fmha_bwd_workspace_size(B, H, Sq) bytes, 256-byte
- * aligned (two fp32 values per query row, -LSE*log2(e) and -dO.O, each row
- * padded to a multiple of 128); no initialisation needed; not shared with a
- * concurrent call.  Asynchronous on `stream` (three kernels); allocates
- * nothing.  Returns FMHA_OK, FMHA_ERR_INVALID_ARG (sizes, scale, mask,
+ * Outputs: dq [B, Sq, H, D], dk, dv [B, Sk, H, D].  Dtypes: all FMHA_F16 or
+ * all FMHA_BF16; or e4m3 inputs (q, k, v, o, dout FMHA_E4M3, as fmha_fwd
+ * writes o for e4m3) with FMHA_BF16 gradients.  The page lists fp8 among the
+ * backward's types but states no scaling of P, dS or the gradients; without
+ * scales, rounding dS to e4m3 would flush most of it (|dS| is often below
+ * e4m3's smallest subnormal, 2^-9), so e4m3 inputs are widened exactly to
+ * bf16 in the workspace and the products run on the bf16 path.  D is 64 or
+ * 128; mask NONE, RESIDUAL or CAUSAL (q-begin or q-end), as fmha_fwd.  Fixed
+ * length only.  Tensors 16-byte aligned, lse 4-byte aligned.
+ * workspace: caller-owned, fmha_bwd_workspace_size_ex(B, H, Sq, Sk, D,
+ * q.dtype) bytes (for 16-bit types equal to fmha_bwd_workspace_size(B, H,
+ * Sq)), 256-byte aligned (two fp32 values per query row, -LSE*log2(e) and
+ * -dO.O, each row padded to a multiple of 128; for e4m3 then the bf16 copies
+ * of q, o, dout, k and v); no initialisation needed; not shared with a
+ * concurrent call.  Asynchronous on `stream` (three kernels, four for e4m3);
+ * allocates nothing.  Returns FMHA_OK, FMHA_ERR_INVALID_ARG (sizes, scale, mask,
  * pointers, workspace), FMHA_ERR_UNSUPPORTED (dtype, alignment) or
  * FMHA_ERR_CUDA.  B = 0 succeeds without a launch; Sq = 0 or Sk = 0 clears
  * the gradients that exist.
@@ -297,8 +304,12 @@ int fmha_bwd(fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_tensor o, fmha_te
              int B, int H, int Sq, int Sk, int D, float scale, int mask, int causal_type,
              void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Workspace bytes fmha_bwd needs (0 for invalid sizes). */
+/* Workspace bytes fmha_bwd needs for 16-bit inputs (0 for invalid sizes). */
 size_t fmha_bwd_workspace_size(int B, int H, int Sq);
+
+/* Workspace bytes fmha_bwd needs for inputs of type `dtype` (FMHA_F16,
+ * FMHA_BF16 or FMHA_E4M3); 0 for invalid sizes or another dtype. */
+size_t fmha_bwd_workspace_size_ex(int B, int H, int Sq, int Sk, int D, int dtype);
 
 /* Text for a status code (static storage, never NULL). */
 const char *fmha_status_string(int status);

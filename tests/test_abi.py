@@ -234,9 +234,10 @@ def test_gen_workspace_size(fm, H, H_k, keys_per_tile):
 
 def call_bwd(fm, **kw):
     a = dict(q=P, k=P, v=P, o=P, do=P, lse=P, dq=P, dk=P, dv=P, B=2, H=4, Sq=128, Sk=128, D=128, scale=0.1,
-             mask=0, ct=0, ws=P, ws_bytes=1 << 30, dt=1)
+             mask=0, ct=0, ws=P, ws_bytes=1 << 30, dt=1, gdt=None)
     a.update(kw)
-    t = lambda x: fm.fmha_tensor(a[x], a["dt"])
+    gdt = a["dt"] if a["gdt"] is None else a["gdt"]
+    t = lambda x: fm.fmha_tensor(a[x], gdt if x in ("dq", "dk", "dv") else a["dt"])
     return fm.lib().fmha_bwd(t("q"), t("k"), t("v"), t("o"), t("do"), a["lse"], t("dq"), t("dk"), t("dv"),
                              a["B"], a["H"], a["Sq"], a["Sk"], a["D"], a["scale"], a["mask"], a["ct"], a["ws"],
                              a["ws_bytes"], None)
@@ -247,6 +248,9 @@ def call_bwd(fm, **kw):
     (dict(scale=0.0), -1), (dict(scale=float("nan")), -1), (dict(mask=3), -1), (dict(ct=2), -1),
     (dict(q=None), -1), (dict(lse=None), -1), (dict(dk=None), -1), (dict(ws=None), -1), (dict(ws_bytes=16), -1),
     (dict(ws=P + 16), -1), (dict(dt=2), -2), (dict(q=P + 8), -2), (dict(lse=P + 2), -1),
+    (dict(dt=2, gdt=0), -2),                          # e4m3 inputs take bf16 gradients
+    (dict(dt=2, gdt=1, ws_bytes=2 * 2 * 4 * 128 * 4), -1),   # the 16-bit workspace is too small for e4m3
+    (dict(dt=5), -2),
 ])
 def test_bwd_validation_rejects_before_any_launch(fm, kw, code):
     assert call_bwd(fm, **kw) == code
@@ -258,3 +262,17 @@ def test_bwd_workspace_size(fm):
     assert fm.fmha_bwd_workspace_size(1, 3, 300) == 2 * 1 * 3 * 384 * 4
     assert fm.fmha_bwd_workspace_size(0, 4, 100) == 0
     assert call_bwd(fm, B=0) == 0
+
+
+def test_bwd_workspace_size_ex(fm):
+    # 16-bit inputs: as fmha_bwd_workspace_size; e4m3: then 256-byte aligned bf16
+    # copies of q, o, dout (B*Sq*H*D each) and k, v (B*Sk*H*D each)
+    B, H, Sq, Sk, D = 2, 3, 100, 300, 64
+    base = fm.fmha_bwd_workspace_size(B, H, Sq)
+    assert fm.fmha_bwd_workspace_size_ex(B, H, Sq, Sk, D, 1) == base
+    assert fm.fmha_bwd_workspace_size_ex(B, H, Sq, Sk, D, 0) == base
+    a = lambda x: (x + 255) // 256 * 256
+    qb, kb = B * Sq * H * D * 2, B * Sk * H * D * 2
+    assert fm.fmha_bwd_workspace_size_ex(B, H, Sq, Sk, D, 2) == a(base) + 3 * a(qb) + a(kb) + kb
+    assert fm.fmha_bwd_workspace_size_ex(B, H, Sq, Sk, 32, 2) == 0
+    assert fm.fmha_bwd_workspace_size_ex(B, H, Sq, Sk, D, 7) == 0

@@ -6,6 +6,11 @@ input type for the tensor cores and each gradient to the output type, so an
 element may differ from the exact gradient by 1% of that gradient's largest
 magnitude plus half a unit in the last place of the output (relative error of a
 16-bit P or dS term: 2^-9; sums over up to a few thousand terms).
+
+e4m3 inputs (with O as the e4m3 forward writes it) are widened exactly to bf16
+and take bf16 gradients; they are compared with the oracle's backward that
+forms the row sums of O * dO from that stored O, on the decoded inputs, under
+the same bf16 bound.
 """
 import numpy as np
 import pytest
@@ -29,6 +34,47 @@ def fm():
     build.build()
     fmha.lib()
     return fmha
+
+
+def run_case_e4m3(fm, B, H, Sq, Sk, D, mask, ct, seed):
+    g = torch.Generator().manual_seed(seed)
+    e4 = lambda *s: torch.randn(*s, generator=g).clamp_(-448, 448).to(torch.float8_e4m3fn)
+    q, k, v, do = e4(B, Sq, H, D), e4(B, Sk, H, D), e4(B, Sk, H, D), e4(B, Sq, H, D)
+    dev = "cuda"
+    qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    o, lse = fm.fwd(qd, kd, vd, mask=mask, causal_type=ct)
+    assert o.dtype == torch.float8_e4m3fn
+    dq, dk, dv = fm.bwd(qd, kd, vd, o, dod, lse, mask=mask, causal_type=ct)
+    torch.cuda.synchronize()
+    assert fm.device_status(reset=True) == 0
+    assert dq.dtype == dk.dtype == dv.dtype == torch.bfloat16
+    dec = lambda t: oracle.decode(oracle.E4M3, t.cpu().view(torch.uint8).numpy())
+    ref = oracle.attn_bwd_o_f64(dec(q), dec(k), dec(v), dec(o), dec(do), D ** -0.5, MASK[mask], CT[ct])
+    for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        got = got.float().cpu().numpy().astype(np.float64)
+        assert not np.isnan(got).any(), f"NaN in {name}"
+        scale = np.abs(want).max() if want.size else 0.0
+        bound = 1e-2 * scale + half_ulp("bf16", want)
+        err = np.abs(got - want)
+        assert (err <= bound).all(), (f"{name}: worst {err.max():.4g} (scale {scale:.3g}) at "
+                                      f"{np.unravel_index(err.argmax(), err.shape)}")
+        assert err.mean() <= 2e-3 * max(scale, 1e-6), (name, err.mean(), scale)
+
+
+E4M3_CASES = [
+    # B, H, Sq, Sk, D, mask, causal_type
+    (1, 2, 128, 128, 128, "none", "qbegin"),
+    (2, 3, 300, 300, 128, "causal", "qbegin"),
+    (1, 4, 200, 333, 64, "none", "qbegin"),
+    (2, 2, 257, 129, 128, "causal", "qend"),
+    (2, 16, 2048, 2048, 128, "causal", "qbegin"),     # more work units than SMs
+]
+
+
+@pytest.mark.parametrize("case", E4M3_CASES, ids=[f"e4m3_b{c[0]}h{c[1]}_{c[2]}x{c[3]}_d{c[4]}_{c[5]}_{c[6]}"
+                                                  for c in E4M3_CASES])
+def test_bwd_e4m3_matches_oracle(fm, case):
+    run_case_e4m3(fm, *case, seed=sum(case[:5]) + 1)
 
 
 def run_case(fm, dtype, B, H, Sq, Sk, D, mask, ct, seed):
