@@ -108,7 +108,11 @@ struct Cfg {
     static constexpr int P_COL0 = PSEP ? O_COL1 + D : S_COL0, P_COL1 = PSEP ? P_COL0 + 64 : S_COL1;
     static_assert(!PSEP || P_COL1 + 64 <= (int)kTmemCols, "TMEM budget of the P buffers");
     static constexpr int BAR_BYTES = 512;
-    static constexpr int SMEM_USED = 2 * TILE_BYTES + NS * TILE_BYTES + BAR_BYTES;
+    // O staging for the TMA store of the epilogue: per softmax warp 32 rows x
+    // one swizzle panel (a row of several panels goes out panel by panel)
+    static constexpr int STG_WARP = 32 * SW;
+    static constexpr int STG_BYTES = 8 * STG_WARP;
+    static constexpr int SMEM_USED = 2 * TILE_BYTES + NS * TILE_BYTES + STG_BYTES + BAR_BYTES;
     // at least 120 KB so that a second CTA can never share the SM (TMEM is
     // allocated whole), plus 1 KB to align the tiles for the 128-byte swizzle
     static constexpr int SMEM_BYTES = (SMEM_USED < 120 * 1024 ? 120 * 1024 : SMEM_USED) + 1024;
@@ -224,6 +228,26 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
         : "memory");
 }
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's bulk stores have read their shared-memory source
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// this thread's bulk stores are complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -1196,8 +1220,40 @@ __device__ __forceinline__ void store_chunk(uint8_t *dst, const uint32_t (&r)[32
     }
 }
 
+// 32 values of O (one TMEM chunk) in the output type into row `row` of a
+// warp's staging panel (SW bytes per row, the TMA swizzle: 16-byte chunk c
+// of a row goes to c ^ (row % 8) for 128-byte rows, ^ (row / 2) % 4 for 64,
+// ^ (row / 4) % 2 for 32), starting at byte `col_bytes` of the row.
+template <class C>
+__device__ __forceinline__ void stage_chunk(uint8_t *stg_row, int row, int col_bytes, const uint32_t (&r)[32],
+                                            float inv) {
+    const int swz = C::SW == 128 ? (row & 7) : C::SW == 64 ? ((row >> 1) & 3) : ((row >> 2) & 1);
+    const int c0 = col_bytes >> 4;
+    if constexpr (C::FP8) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            w[i] = pack4_e4m3(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                              __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            *reinterpret_cast<uint4 *>(stg_row + (((c0 + i) ^ swz) << 4)) =
+                make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    } else {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            w[i] = pack2<C::ELEM>(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4 *>(stg_row + (((c0 + i) ^ swz) << 4)) =
+                make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
+}
+
 template <class C, bool SPLIT>
-__device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp, int lane) {
+__device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp, int lane, const CUtensorMap *tmO,
+                           uint8_t *stg) {
     volatile int *abort_flag = &bars->abort;
     const int t = warp >> 2, wq = warp & 3;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
@@ -1300,19 +1356,57 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
             continue;
         }
         const float inv = l > 0.f ? p.out_scale / l : 0.f;
-        uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) +
-                        (((int64_t)U.q_row + row) * p.H + U.h) * (int64_t)(C::D * C::E);
+        // this warp's 32 rows go out through shared memory and a TMA store
+        // (whole 128-byte lines) when they all belong to this sequence; rows
+        // past a fixed-length sequence's end fall outside the tensor map and
+        // are not written.  A packed (varlen) warp that crosses its
+        // sequence's end stores its rows one by one.
+        const int wrow0 = U.q0 + t * kTile + wq * 32;
+        const bool by_tma = wrow0 < U.sq && (!p.varlen || wrow0 + 32 <= U.sq);
+        if (by_tma) {
+            uint8_t *srow = stg + warp * C::STG_WARP + lane * C::SW;
+            constexpr int CH_PER_PANEL = C::BOX_D / 32;
 #pragma unroll 1
-        for (int ch = 0; ch < C::D / 32; ++ch) {
-            uint32_t r[32];
-            if (have) {
-                tmem_ld32(o_tm + 32 * ch, r);
-                tmem_wait_ld(r);
-            } else {
+            for (int pn = 0; pn < C::PANELS; ++pn) {
+                // the warp's previous store has read the staging panel
+                if (lane == 0) bulk_wait_read();
+                __syncwarp();
+#pragma unroll 1
+                for (int c2 = 0; c2 < CH_PER_PANEL; ++c2) {
+                    uint32_t r[32];
+                    if (have) {
+                        tmem_ld32(o_tm + 32 * (pn * CH_PER_PANEL + c2), r);
+                        tmem_wait_ld(r);
+                    } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = 0u;
+                        for (int i = 0; i < 32; ++i) r[i] = 0u;
+                    }
+                    stage_chunk<C>(srow, lane, c2 * 32 * C::E, r, inv);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t src = smem_u32(stg + warp * C::STG_WARP);
+                    if (p.varlen) tma_store_3d(tmO, src, pn * C::BOX_D, U.h, U.q_row + wrow0);
+                    else tma_store_4d(tmO, src, pn * C::BOX_D, U.h, wrow0, U.b);
+                    bulk_commit();
+                }
             }
-            if (valid) store_chunk<C>(orow + ch * 32 * C::E, r, inv);
+        } else {
+            uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) +
+                            (((int64_t)U.q_row + row) * p.H + U.h) * (int64_t)(C::D * C::E);
+#pragma unroll 1
+            for (int ch = 0; ch < C::D / 32; ++ch) {
+                uint32_t r[32];
+                if (have) {
+                    tmem_ld32(o_tm + 32 * ch, r);
+                    tmem_wait_ld(r);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = 0u;
+                }
+                if (valid) store_chunk<C>(orow + ch * 32 * C::E, r, inv);
+            }
         }
         if (valid && p.lse) {
             const int64_t li = p.varlen ? (int64_t)U.h * p.total_length + U.q_row + row
@@ -1320,6 +1414,8 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
             p.lse[li] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
         }
     }
+    // the CTA's shared memory must outlive the stores that read it
+    if (!SPLIT && lane == 0) bulk_wait_all();
 }
 
 // ---------------------------------------------------------------------------
@@ -1329,13 +1425,15 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
 template <class C, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                          const __grid_constant__ CUtensorMap tmV, const Params p) {
+                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                          const Params p) {
     static_assert(C::TURN_AT >= 0 && C::TURN_EARLY >= 0, "the turn hand-over is inside the S group");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sQ = smem;                               // 2 Q tiles
     uint8_t *sKV = smem + 2 * C::TILE_BYTES;          // NS K/V stages
-    Bars *bars = reinterpret_cast<Bars *>(sKV + C::NS * C::TILE_BYTES);
+    uint8_t *sStg = sKV + C::NS * C::TILE_BYTES;      // O staging of the softmax warps
+    Bars *bars = reinterpret_cast<Bars *>(sStg + C::STG_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -1375,7 +1473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (SPLIT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp < kProducerWarp) {
-        softmax_wg<C, SPLIT>(p, bars, tmem, warp, lane);
+        softmax_wg<C, SPLIT>(p, bars, tmem, warp, lane, &tmO, sStg);
     } else if (warp == kProducerWarp) {
         if (lane == 0) producer<C, SPLIT>(p, &tmQ, &tmK, &tmV, sQ, sKV, bars);
     } else if constexpr (C::PSEP) {
@@ -1430,7 +1528,8 @@ int sm_count() {
 // [rows, heads, D] (varlen, rank 3) or [batch, rows, heads, D] (rank 4) with
 // a 128-row box of one head and one swizzle panel of the head dim.
 template <class C>
-bool encode_map(CUtensorMap *m, const void *base, int heads, int rows, int batch, bool varlen) {
+bool encode_map(CUtensorMap *m, const void *base, int heads, int rows, int batch, bool varlen,
+                int box_rows = kTile) {
     auto fn = encode_fn();
     if (!fn) return false;
     const CUtensorMapDataType dt = C::ELEM == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -1442,7 +1541,7 @@ bool encode_map(CUtensorMap *m, const void *base, int heads, int rows, int batch
     const cuuint64_t row_bytes = (cuuint64_t)C::D * C::E;
     cuuint64_t dims[4] = {(cuuint64_t)C::D, (cuuint64_t)heads, (cuuint64_t)imax(rows, 1), (cuuint64_t)batch};
     cuuint64_t strides[3] = {row_bytes, row_bytes * heads, row_bytes * heads * (cuuint64_t)imax(rows, 1)};
-    cuuint32_t box[4] = {(cuuint32_t)C::BOX_D, 1, (cuuint32_t)kTile, 1};
+    cuuint32_t box[4] = {(cuuint32_t)C::BOX_D, 1, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUresult r = fn(m, dt, varlen ? 3 : 4, const_cast<void *>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1452,13 +1551,16 @@ bool encode_map(CUtensorMap *m, const void *base, int heads, int rows, int batch
 
 template <class C>
 int launch_cfg(const Params &p, cudaStream_t stream) {
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const int rq = p.varlen ? (int)p.total_length : p.Sq;
     const int rk = p.varlen ? (int)p.total_length : p.Sk;
     const int nb = p.varlen ? 1 : p.B;
     if (!encode_map<C>(&tq, p.q, p.H, rq, nb, p.varlen) || !encode_map<C>(&tk, p.k, p.H_k, rk, nb, p.varlen) ||
         !encode_map<C>(&tv, p.v, p.H_k, rk, nb, p.varlen))
         return FMHA_ERR_CUDA;
+    // O: the epilogue's TMA stores, 32 rows (one softmax warp) per box; the
+    // split-KV instantiation writes fp32 partials instead and never uses it
+    if (!encode_map<C>(&to, p.part_o ? p.q : p.o, p.H, rq, nb, p.varlen, 32)) return FMHA_ERR_CUDA;
     const int nsm = sm_count();
     if (nsm <= 0) return FMHA_ERR_CUDA;
     int64_t units;
@@ -1475,7 +1577,7 @@ int launch_cfg(const Params &p, cudaStream_t stream) {
         cudaGetLastError();
         return FMHA_ERR_CUDA;
     }
-    kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+    kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, to, p);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
     return FMHA_OK;
 }
