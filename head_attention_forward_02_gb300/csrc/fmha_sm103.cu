@@ -257,6 +257,25 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 // this thread's bulk stores are complete
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// loads with an L2 policy (Q: read by one unit only)
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                                 int c2, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                                 int c2, int c3, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(pol)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -666,12 +685,14 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
             mbar_expect_tx(fb, C::TILE_BYTES);
             const uint32_t dst = smem_u32(sQ + t * C::TILE_BYTES);
             const int row = U.q0 + t * kTile;
+            // a Q tile is read by this unit only: first to leave L2, ahead of K/V
+            const uint64_t pol = evict_first_policy();
 #pragma unroll
             for (int pn = 0; pn < C::PANELS; ++pn) {
                 if (p.varlen)
-                    tma_load_3d(dst + pn * C::PANEL_BYTES, tmQ, fb, pn * C::BOX_D, U.h, U.q_row + row);
+                    tma_load_3d_hint(dst + pn * C::PANEL_BYTES, tmQ, fb, pn * C::BOX_D, U.h, U.q_row + row, pol);
                 else
-                    tma_load_4d(dst + pn * C::PANEL_BYTES, tmQ, fb, pn * C::BOX_D, U.h, row, U.b);
+                    tma_load_4d_hint(dst + pn * C::PANEL_BYTES, tmQ, fb, pn * C::BOX_D, U.h, row, U.b, pol);
             }
             ++qload[t];
         }
