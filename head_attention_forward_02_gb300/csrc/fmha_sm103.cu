@@ -27,7 +27,8 @@
 //    (Two issuers without the turns were measured slower: the tensor pipe
 //    then interleaves the tiles and S_t completes later.)
 //
-// Every wait is bounded: after kTimeoutNs the waiting thread records
+// Every wait is bounded: after g_wait_ns (4 s unless a test sets another
+// limit through fmha_set_wait_limit_ns) the waiting thread records
 // FMHA_ERR_TIMEOUT in g_status, raises a CTA-wide abort flag, and all roles
 // stop issuing work, drain what they issued (bounded), free TMEM and return.
 #include <cuda.h>
@@ -44,6 +45,13 @@
 namespace fmha {
 
 __device__ int g_status;   // FMHA_OK, or FMHA_ERR_TIMEOUT after a bounded wait expired
+// the bounded waits' limit (ns); set from the host through fmha_set_wait_limit_ns
+__device__ unsigned long long g_wait_ns = 4000000000ull;
+// test hook (fmha_set_test_gate): when set, the producer first waits for a
+// flag that nothing sets, so that bounded wait expires and the launch takes
+// its failure path
+__device__ int g_test_gate;
+__device__ int g_test_flag;   // never written
 
 namespace {
 
@@ -181,14 +189,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Slow path of a bounded wait: poll until the phase completes, the CTA aborts,
-// or kTimeoutNs pass (then record the timeout and raise the abort flag).
+// or g_wait_ns pass (then record the timeout and raise the abort flag).
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > kTimeoutNs) {
+            if (globaltimer() - t0 > g_wait_ns) {
                 *abort_flag = 1;
                 atomicExch(&g_status, FMHA_ERR_TIMEOUT);
                 return false;
@@ -394,7 +402,7 @@ __device__ __forceinline__ bool warp_wait_inline(uint32_t bar, uint32_t parity, 
             if ((r = mbar_try_wait(bar, parity))) break;
             if ((it & 63) == 0) {
                 if (*abort_flag) break;
-                if (globaltimer() - t0 > kTimeoutNs) {
+                if (globaltimer() - t0 > g_wait_ns) {
                     *abort_flag = 1;
                     atomicExch(&g_status, FMHA_ERR_TIMEOUT);
                     break;
@@ -670,6 +678,20 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
     prefetch_tmap(tmV);
     uint32_t fill = 0, qload[2] = {0, 0};
     bool ok = true;
+    if (g_test_gate) {
+        // a flag nothing sets: the wait runs out, records the timeout and
+        // raises the abort flag; no copy has been issued yet
+        const volatile int *flag = &g_test_flag;
+        const unsigned long long t0 = globaltimer();
+        for (uint32_t it = 1; !*flag; ++it) {
+            if ((it & 63) == 0 && (*abort_flag || globaltimer() - t0 > g_wait_ns)) {
+                *abort_flag = 1;
+                atomicExch(&g_status, FMHA_ERR_TIMEOUT);
+                break;
+            }
+        }
+        ok = false;
+    }
     Cursor cur;
     for (int r = 0; ok; ++r) {
         Unit U;
@@ -1630,6 +1652,24 @@ int launch_sm103(const Params &p, cudaStream_t stream) {
     case 128: return launch_d<128>(p, stream);
     default: return FMHA_ERR_INVALID_ARG;
     }
+}
+
+int sm103_set_wait_limit(unsigned long long ns) {
+    const unsigned long long v = ns ? ns : kTimeoutNs;
+    if (cudaMemcpyToSymbol(g_wait_ns, &v, sizeof(v)) != cudaSuccess) {
+        cudaGetLastError();
+        return FMHA_ERR_CUDA;
+    }
+    return FMHA_OK;
+}
+
+int sm103_set_test_gate(int on) {
+    const int v = on ? 1 : 0;
+    if (cudaMemcpyToSymbol(g_test_gate, &v, sizeof(v)) != cudaSuccess) {
+        cudaGetLastError();
+        return FMHA_ERR_CUDA;
+    }
+    return FMHA_OK;
 }
 
 int sm103_read_status(int reset) {

@@ -87,6 +87,10 @@ def lib():
         L.fmha_status_string.argtypes = [ctypes.c_int]
         L.fmha_device_status.restype = ctypes.c_int
         L.fmha_device_status.argtypes = [ctypes.c_int]
+        L.fmha_set_wait_limit_ns.restype = ctypes.c_int
+        L.fmha_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+        L.fmha_set_test_gate.restype = ctypes.c_int
+        L.fmha_set_test_gate.argtypes = [ctypes.c_int]
         L.fmha_kv_tile_range.restype = ctypes.c_int
         L.fmha_kv_tile_range.argtypes = [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_int)] * 2
         _lib = L
@@ -99,6 +103,18 @@ def status_string(status: int) -> str:
 
 def device_status(reset: bool = False) -> int:
     return lib().fmha_device_status(1 if reset else 0)
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Test hook (see fmha_set_wait_limit_ns): the forward kernels' bounded waits
+    give up after ns nanoseconds; 0 restores the default."""
+    return lib().fmha_set_wait_limit_ns(int(ns))
+
+
+def set_test_gate(on: bool) -> int:
+    """Test hook (see fmha_set_test_gate): the forward's producer first waits for
+    a flag that nothing sets."""
+    return lib().fmha_set_test_gate(1 if on else 0)
 
 
 def kv_tile_range(q_row0: int, q_rows: int, Sq: int, Sk: int, mask: int, causal_type: int,
