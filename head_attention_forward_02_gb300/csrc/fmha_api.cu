@@ -88,6 +88,9 @@ int make_params(Params &p, fmha_tensor q, fmha_tensor k, fmha_tensor v, fmha_ten
     p.dtype = q.dtype; p.odtype = o.dtype;
     p.num_splits = 1;
     p.part_o = nullptr; p.part_lse = nullptr; p.part_rows = 0;
+    // up to 128 query rows fill only one of a unit's two Q tiles: pair two
+    // query heads of one kv head instead (they share the K/V stream)
+    p.hpair = (!varlen && Sq <= 128 && p.group % 2 == 0) ? 1 : 0;
     return FMHA_OK;
 }
 

@@ -19,6 +19,10 @@ struct Params {
     float *lse;
     int B, H, H_k, Sq, Sk, D;
     int group;              // H / H_k
+    // head pairs (fixed length, Sq <= 128, H / H_k even): a work unit's two
+    // Q tiles are query heads 2i and 2i + 1 (one kv head) over rows [0, Sq),
+    // instead of rows [0, 128) and [128, 256) of one head
+    int hpair;
     float scale, out_scale;
     int mask, causal_type;
     const int *cu_q, *cu_k; // device, varlen only

@@ -533,6 +533,13 @@ struct Unit {
     int split;            // split index (0 without split-KV)
 };
 
+// Query head and first row of Q tile t of a unit: rows q0 + 128 t of head h,
+// or, with head pairs, head h + t over rows [q0, q0 + 128)
+template <bool HP>
+__device__ __forceinline__ int tile_head(const Unit &U, int t) { return HP ? U.h + t : U.h; }
+template <bool HP>
+__device__ __forceinline__ int tile_row0(const Unit &U, int t) { return HP ? U.q0 : U.q0 + t * kTile; }
+
 // Unit taken by this CTA in round r: CTAs sweep the (heaviest-first) unit
 // list in alternating directions, which balances causal work to within a
 // fraction of a unit without a shared work counter.
@@ -557,8 +564,29 @@ __device__ __forceinline__ int seqs_with_block(const Params &p, int q) {
     return n;
 }
 
+template <bool HP>
 __device__ __forceinline__ bool decode_unit(const Params &p, int u, Cursor &cur, Unit &U) {
     int b, h, qb;
+    if constexpr (HP) {
+        // head pairs (fixed length, Sq <= 128, even query group): one unit
+        // per (batch, query heads 2i and 2i + 1); both Q tiles cover rows
+        // [0, Sq) and read the same kv head's K/V
+        if (u >= p.B * (p.H / 2)) return false;
+        b = u / (p.H / 2);
+        h = 2 * (u - b * (p.H / 2));
+        U.b = b;
+        U.h = h;
+        U.g = h / p.group;
+        U.q0 = 0;
+        U.sq = p.Sq;
+        U.sk = p.Sk;
+        U.q_row = b * p.Sq;
+        U.k_row = b * p.Sk;
+        kv_tile_range(0, kTile, U.sq, U.sk, p.mask, p.causal_type, kTile, &U.n[0], &U.nu[0]);
+        U.n[1] = U.n[0];
+        U.nu[1] = U.nu[0];
+        return true;
+    }
     if (!p.varlen) {
         const int nqb = (p.Sq + kUnitRows - 1) / kUnitRows;
         const int per = p.B * p.H;
@@ -652,10 +680,10 @@ __device__ __forceinline__ bool decode_unit(const Params &p, int u, Cursor &cur,
 // unit's key tiles [0, max(n0, n1)) are cut into num_splits near-equal
 // contiguous ranges; tile t then covers [j0, min(n_t, j1)) and is active
 // when that range is not empty.  Without split-KV, j0 = 0 and j1 = max(n0, n1).
-template <bool SPLIT>
+template <bool SPLIT, bool HP>
 __device__ __forceinline__ bool decode_work(const Params &p, int u, Cursor &cur, Unit &U) {
     const int ns = SPLIT ? p.num_splits : 1;      // a constant 1 folds the split arithmetic away
-    if (!decode_unit(p, u / ns, cur, U)) return false;
+    if (!decode_unit<HP>(p, u / ns, cur, U)) return false;
     const int nmax = imax(U.n[0], U.n[1]);
     U.split = u % ns;
     U.j0 = (int)((int64_t)nmax * U.split / ns);
@@ -669,7 +697,7 @@ __device__ __forceinline__ bool decode_work(const Params &p, int u, Cursor &cur,
 // Producer: Q tiles and the K/V ring, by TMA (one lane)
 // ---------------------------------------------------------------------------
 
-template <class C, bool SPLIT>
+template <class C, bool SPLIT, bool HP>
 __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensorMap *tmK,
                          const CUtensorMap *tmV, uint8_t *sQ, uint8_t *sKV, Bars *bars) {
     volatile int *abort_flag = &bars->abort;
@@ -695,7 +723,7 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
     Cursor cur;
     for (int r = 0; ok; ++r) {
         Unit U;
-        if (!decode_work<SPLIT>(p, unit_of_round(r), cur, U)) break;
+        if (!decode_work<SPLIT, HP>(p, unit_of_round(r), cur, U)) break;
         for (int t = 0; t < 2; ++t) {
             if (U.n[t] <= U.j0) continue;                 // tile inactive in this work item
             if (qload[t] > 0 &&
@@ -706,15 +734,15 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
             const uint32_t fb = smem_u32(&bars->q_full[t]);
             mbar_expect_tx(fb, C::TILE_BYTES);
             const uint32_t dst = smem_u32(sQ + t * C::TILE_BYTES);
-            const int row = U.q0 + t * kTile;
+            const int row = tile_row0<HP>(U, t), qh = tile_head<HP>(U, t);
             // a Q tile is read by this unit only: first to leave L2, ahead of K/V
             const uint64_t pol = evict_first_policy();
 #pragma unroll
             for (int pn = 0; pn < C::PANELS; ++pn) {
                 if (p.varlen)
-                    tma_load_3d_hint(dst + pn * C::PANEL_BYTES, tmQ, fb, pn * C::BOX_D, U.h, U.q_row + row, pol);
+                    tma_load_3d_hint(dst + pn * C::PANEL_BYTES, tmQ, fb, pn * C::BOX_D, qh, U.q_row + row, pol);
                 else
-                    tma_load_4d_hint(dst + pn * C::PANEL_BYTES, tmQ, fb, pn * C::BOX_D, U.h, row, U.b, pol);
+                    tma_load_4d_hint(dst + pn * C::PANEL_BYTES, tmQ, fb, pn * C::BOX_D, qh, row, U.b, pol);
             }
             ++qload[t];
         }
@@ -799,7 +827,7 @@ __device__ void producer(const Params &p, const CUtensorMap *tmQ, const CUtensor
 // MMA issuers (warps 9 and 10, one elected lane each)
 // ---------------------------------------------------------------------------
 
-template <class C, bool SPLIT>
+template <class C, bool SPLIT, bool HP>
 __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bars, uint32_t tmem_any, int t) {
     // Two warps issue the MMAs, warp t for Q tile t, and take turns so that
     // the tensor pipe sees the order S0_j0, S1_j0, then per key step
@@ -888,7 +916,7 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
 
     for (int r = 0; ok; ++r) {
         Unit U;
-        if (!decode_work<SPLIT>(p, unit_of_round(r), cur, U)) break;
+        if (!decode_work<SPLIT, HP>(p, unit_of_round(r), cur, U)) break;
         const int n = t ? U.n[1] : U.n[0], j0 = U.j0, jn = U.j1;
         if (j0 >= jn) continue;
         if (n > j0) {
@@ -950,7 +978,7 @@ __device__ void mma_issuer(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bar
 // warps run free: S is issued about a softmax step ahead of its use, so the
 // pipe order between the tiles matters little.  PV_t,j completes pv_done[t],
 // which the softmax warps wait for before they overwrite P_t or rescale O_t.
-template <class C, bool SPLIT>
+template <class C, bool SPLIT, bool HP>
 __device__ void mma_issuer_psep(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars *bars, uint32_t tmem_any,
                                 int t) {
     volatile int *abort_flag = &bars->abort;
@@ -1023,7 +1051,7 @@ __device__ void mma_issuer_psep(const Params &p, uint8_t *sQ, uint8_t *sKV, Bars
 
     for (int r = 0; ok; ++r) {
         Unit U;
-        if (!decode_work<SPLIT>(p, unit_of_round(r), cur, U)) break;
+        if (!decode_work<SPLIT, HP>(p, unit_of_round(r), cur, U)) break;
         const int n = t ? U.n[1] : U.n[0], j0 = U.j0, jn = U.j1;
         if (j0 >= jn) continue;
         int st;
@@ -1302,7 +1330,7 @@ __device__ __forceinline__ void stage_chunk(uint8_t *stg_row, int row, int col_b
     }
 }
 
-template <class C, bool SPLIT>
+template <class C, bool SPLIT, bool HP>
 __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp, int lane, const CUtensorMap *tmO,
                            uint8_t *stg) {
     volatile int *abort_flag = &bars->abort;
@@ -1324,9 +1352,9 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
     Cursor cur;
     for (int r = 0; ok; ++r) {
         Unit U;
-        if (!decode_work<SPLIT>(p, unit_of_round(r), cur, U)) break;
+        if (!decode_work<SPLIT, HP>(p, unit_of_round(r), cur, U)) break;
         const int n = U.n[t], nu = U.nu[t], j0 = U.j0;
-        const int row = U.q0 + t * kTile + wq * 32 + lane;      // query row within the sequence
+        const int row = tile_row0<HP>(U, t) + wq * 32 + lane;  // query row within the sequence
         // keys [0, key_end) are visible to this row
         int key_end = U.sk;
         if (causal) key_end = imin(key_end, row + 1 + (p.causal_type == FMHA_CAUSAL_QEND ? U.sk - U.sq : 0));
@@ -1380,9 +1408,10 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
             tc_fence_after();
         }
         const bool valid = row < U.sq;
+        const int qh = tile_head<HP>(U, t);                    // query head of this tile
         if constexpr (SPLIT) {
             // split-KV: normalised fp32 partial O and its LSE for the combine
-            const int64_t prow = ((int64_t)U.split * p.part_rows + U.q_row + row) * p.H + U.h;
+            const int64_t prow = ((int64_t)U.split * p.part_rows + U.q_row + row) * p.H + qh;
             float *po = p.part_o + prow * C::D;
             const float pinv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
@@ -1412,7 +1441,7 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
         // past a fixed-length sequence's end fall outside the tensor map and
         // are not written.  A packed (varlen) warp that crosses its
         // sequence's end stores its rows one by one.
-        const int wrow0 = U.q0 + t * kTile + wq * 32;
+        const int wrow0 = tile_row0<HP>(U, t) + wq * 32;
         const bool by_tma = wrow0 < U.sq && (!p.varlen || wrow0 + 32 <= U.sq);
         if (by_tma) {
             uint8_t *srow = stg + warp * C::STG_WARP + lane * C::SW;
@@ -1438,14 +1467,14 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
                 __syncwarp();
                 if (lane == 0) {
                     const uint32_t src = smem_u32(stg + warp * C::STG_WARP);
-                    if (p.varlen) tma_store_3d(tmO, src, pn * C::BOX_D, U.h, U.q_row + wrow0);
-                    else tma_store_4d(tmO, src, pn * C::BOX_D, U.h, wrow0, U.b);
+                    if (p.varlen) tma_store_3d(tmO, src, pn * C::BOX_D, qh, U.q_row + wrow0);
+                    else tma_store_4d(tmO, src, pn * C::BOX_D, qh, wrow0, U.b);
                     bulk_commit();
                 }
             }
         } else {
             uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) +
-                            (((int64_t)U.q_row + row) * p.H + U.h) * (int64_t)(C::D * C::E);
+                            (((int64_t)U.q_row + row) * p.H + qh) * (int64_t)(C::D * C::E);
 #pragma unroll 1
             for (int ch = 0; ch < C::D / 32; ++ch) {
                 uint32_t r[32];
@@ -1460,8 +1489,8 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
             }
         }
         if (valid && p.lse) {
-            const int64_t li = p.varlen ? (int64_t)U.h * p.total_length + U.q_row + row
-                                        : ((int64_t)U.b * p.H + U.h) * p.Sq + row;
+            const int64_t li = p.varlen ? (int64_t)qh * p.total_length + U.q_row + row
+                                        : ((int64_t)U.b * p.H + qh) * p.Sq + row;
             p.lse[li] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
         }
     }
@@ -1473,7 +1502,7 @@ __device__ void softmax_wg(const Params &p, Bars *bars, uint32_t tmem, int warp,
 // The kernel
 // ---------------------------------------------------------------------------
 
-template <class C, bool SPLIT>
+template <class C, bool SPLIT, bool HP>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -1524,13 +1553,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (SPLIT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp < kProducerWarp) {
-        softmax_wg<C, SPLIT>(p, bars, tmem, warp, lane, &tmO, sStg);
+        softmax_wg<C, SPLIT, HP>(p, bars, tmem, warp, lane, &tmO, sStg);
     } else if (warp == kProducerWarp) {
-        if (lane == 0) producer<C, SPLIT>(p, &tmQ, &tmK, &tmV, sQ, sKV, bars);
+        if (lane == 0) producer<C, SPLIT, HP>(p, &tmQ, &tmK, &tmV, sQ, sKV, bars);
     } else if constexpr (C::PSEP) {
-        mma_issuer_psep<C, SPLIT>(p, sQ, sKV, bars, tmem, warp - kMmaWarp);
+        mma_issuer_psep<C, SPLIT, HP>(p, sQ, sKV, bars, tmem, warp - kMmaWarp);
     } else {
-        mma_issuer<C, SPLIT>(p, sQ, sKV, bars, tmem, warp - kMmaWarp);
+        mma_issuer<C, SPLIT, HP>(p, sQ, sKV, bars, tmem, warp - kMmaWarp);
     }
 
     tc_fence_before();
@@ -1619,11 +1648,18 @@ int launch_cfg(const Params &p, cudaStream_t stream) {
         units = (int64_t)p.H * (p.B + p.total_length / kUnitRows + 1);   // upper bound
     else
         units = (int64_t)p.B * p.H * ((p.Sq + kUnitRows - 1) / kUnitRows);
+    // head pairs: instantiated for D = 128 (the head dim of the split-KV and
+    // short-query workloads); other head dims keep one head per unit
+    const bool hp = C::D == 128 && p.hpair;
+    if (hp) units = (int64_t)p.B * (p.H / 2);
     units *= p.num_splits;
     const int grid = (int)(units < nsm ? units : nsm);
     if (grid <= 0) return FMHA_OK;
     // split-KV is a separate instantiation so the plain kernel keeps its code
-    auto kern = p.part_o ? fmha_fwd_sm103_kernel<C, true> : fmha_fwd_sm103_kernel<C, false>;
+    void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, Params) =
+        p.part_o ? fmha_fwd_sm103_kernel<C, true, false> : fmha_fwd_sm103_kernel<C, false, false>;
+    if constexpr (C::D == 128)
+        if (hp) kern = p.part_o ? fmha_fwd_sm103_kernel<C, true, true> : fmha_fwd_sm103_kernel<C, false, true>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
         return FMHA_ERR_CUDA;

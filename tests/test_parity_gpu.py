@@ -57,6 +57,12 @@ FIXED = [
     ("e4m3", 1, 4, 4, 512, 512, 128, "causal", "qbegin"),
     ("e4m3", 2, 4, 2, 300, 470, 64, "causal", "qend"),
     ("e4m3", 1, 4, 4, 257, 333, 32, "none", "qbegin"),
+    # up to 128 query rows with an even query group: units pair two query heads
+    ("bf16", 2, 8, 2, 128, 700, 128, "causal", "qend"),
+    ("bf16", 3, 8, 4, 77, 300, 64, "none", "qbegin"),
+    ("e4m3", 2, 16, 4, 100, 1000, 128, "causal", "qbegin"),
+    ("f16", 1, 4, 2, 1, 513, 32, "none", "qbegin"),
+    ("bf16", 20, 32, 8, 64, 512, 128, "causal", "qend"),   # 320 pair units: several per CTA
 ]
 
 

@@ -34,6 +34,8 @@ FIXED = [
     ("bf16", 1, 2, 2, 17, 13, 64, "none", "qbegin", 3),        # more pieces than key tiles
     ("bf16", 1, 4, 4, 512, 512, 128, "causal", "qbegin", 1),
     ("e4m3", 1, 2, 2, 256, 1800, 128, "none", "qbegin", 4),
+    ("bf16", 2, 8, 2, 128, 3000, 128, "causal", "qend", 6),   # head pairs: Sq <= 128, even group
+    ("f16", 1, 4, 2, 33, 2100, 64, "none", "qbegin", 4),
 ]
 
 
