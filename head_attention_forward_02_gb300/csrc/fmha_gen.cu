@@ -1068,7 +1068,8 @@ __global__ void __launch_bounds__(Layout<MODE>::THREADS, 1)
     }
 }
 
-// One CTA of kMergeThreads per (sequence, query head): O = out_scale *
+// One CTA of kMergeThreads per (sequence, query head), for rows merged from
+// many chunks (eight warps share them): O = out_scale *
 // sum_c w_c O_c / sum_c w_c with w_c = exp(LSE_c - max LSE), LSE = max +
 // ln sum_c w_c.  Eight groups of 32 threads take every eighth chunk (each
 // thread four of the 128 dims), so eight 512-byte partial rows are in flight.
@@ -1076,7 +1077,7 @@ constexpr int kMergeThreads = 256;
 constexpr int kMergeGroups = kMergeThreads / 32;
 
 template <int ELEM>
-__global__ void __launch_bounds__(kMergeThreads) fmha_gen_merge_kernel(const GenParams p) {
+__global__ void __launch_bounds__(kMergeThreads) fmha_gen_merge_block_kernel(const GenParams p) {
     __shared__ float red_m[kMergeGroups];
     __shared__ float4 red_o[kMergeGroups][32];
     __shared__ float red_w[kMergeGroups];
@@ -1156,6 +1157,88 @@ __global__ void __launch_bounds__(kMergeThreads) fmha_gen_merge_kernel(const Gen
     }
     if (lane != 0) wsum = 0.f;   // lane 0 holds group 0's sum; share the total
     wsum = __shfl_sync(0xffffffffu, lane == 0 ? wsum : 0.f, 0);
+    const float inv = wsum > 0.f ? p.out_scale / wsum : 0.f;
+    if constexpr (ELEM == FMHA_E4M3) {
+        *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.o) + (int64_t)row * kD + lane * 4) =
+            pack4_e4m3(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+        uint2 out;
+        out.x = pack2<ELEM == FMHA_BF16>(acc.x * inv, acc.y * inv);
+        out.y = pack2<ELEM == FMHA_BF16>(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.o) + (int64_t)row * kD + lane * 4) = out;
+    }
+    if (lane == 0 && p.lse) p.lse[row] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
+}
+
+// One warp per (sequence, query head) row, blockDim / 32 rows per CTA (the host
+// keeps at least two CTAs per SM): O = out_scale *
+// sum_c w_c O_c / sum_c w_c with w_c = exp(LSE_c - max LSE), LSE = max +
+// ln sum_c w_c.  Lane l holds dims 4l .. 4l + 3; no shared memory and no
+// block barrier, so after the wait each row is two dependent loads (the
+// chunks' LSE, then their partial rows) and a store.
+constexpr int kMergeRowsMax = 8;
+
+template <int ELEM>
+__global__ void __launch_bounds__(32 * kMergeRowsMax) fmha_gen_merge_warp_kernel(const GenParams p) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= p.B * p.H) return;
+    const int b = row / p.H, u = (row % p.H) / (p.G * p.GP);   // sequence and work unit
+    // the attention kernel's split: total tiles, and the tiles before sequence b
+    long long tot = 0, pre = 0;
+    for (int bb = lane; bb < p.B; bb += 32) {
+        const long long n = (long long)p.NU * (p.GP == 2 ? gen_tiles<true>(p, bb) : gen_tiles<false>(p, bb));
+        tot += n;
+        if (bb < b) pre += n;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        pre += __shfl_xor_sync(0xffffffffu, pre, o);
+    }
+    const int nt = p.GP == 2 ? gen_tiles<true>(p, b) : gen_tiles<false>(p, b);
+    int nch = 0;                       // CTAs that covered this unit = its partial slots
+    if (nt > 0) {
+        const long long per = (tot + p.ncta - 1) / p.ncta;
+        const long long off = pre + (long long)u * nt;
+        nch = (int)((off + nt - 1) / per - off / per + 1);
+    }
+    // the partials are the attention kernel's: wait for it (and its memory)
+    // here; everything above overlaps its tail
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const float *lse_c = p.part_lse + (int64_t)row * p.max_seg;
+    const float4 *o_c = reinterpret_cast<const float4 *>(p.part_o + (int64_t)row * p.max_seg * kD) + lane;
+    float mx = -INFINITY;
+    for (int c = lane; c < nch; c += 32) mx = fmaxf(mx, lse_c[c]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    if (mx != -INFINITY) {
+        for (int c0 = 0; c0 < nch; c0 += 32) {
+            // weights of 32 chunks at a time, one per lane, then broadcast
+            const float wl = c0 + lane < nch ? __expf(lse_c[c0 + lane] - mx) : 0.f;
+            const int cn = nch - c0 < 32 ? nch - c0 : 32;
+            // eight chunks' rows in flight at a time
+            for (int c = 0; c < cn; c += 8) {
+                float4 v[8];
+#pragma unroll
+                for (int x = 0; x < 8; ++x)
+                    v[x] = c + x < cn ? o_c[(int64_t)(c0 + c + x) * (kD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const float w = __shfl_sync(0xffffffffu, wl, (c + x) & 31);
+                    if (c + x < cn) {
+                        wsum += w;
+                        acc.x += w * v[x].x;
+                        acc.y += w * v[x].y;
+                        acc.z += w * v[x].z;
+                        acc.w += w * v[x].w;
+                    }
+                }
+            }
+        }
+    }
     const float inv = wsum > 0.f ? p.out_scale / wsum : 0.f;
     if constexpr (ELEM == FMHA_E4M3) {
         *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.o) + (int64_t)row * kD + lane * 4) =
@@ -1369,13 +1452,20 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
     kern<<<grid, threads, smem_bytes, stream>>>(tq, tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
     const int rows = B * H;
-    auto merge = dt == FMHA_BF16 ? fmha_gen_merge_kernel<FMHA_BF16>
-                 : dt == FMHA_F16 ? fmha_gen_merge_kernel<FMHA_F16> : fmha_gen_merge_kernel<FMHA_E4M3>;
+    // a row meets about sms / (B * units per sequence) + 1 chunks: many chunks
+    // go to eight warps per row, few to one warp per row
+    const bool many = sms >= 4 * B * p.NU;
+    auto merge = many ? (dt == FMHA_BF16 ? fmha_gen_merge_block_kernel<FMHA_BF16>
+                         : dt == FMHA_F16 ? fmha_gen_merge_block_kernel<FMHA_F16> : fmha_gen_merge_block_kernel<FMHA_E4M3>)
+                      : (dt == FMHA_BF16 ? fmha_gen_merge_warp_kernel<FMHA_BF16>
+                         : dt == FMHA_F16 ? fmha_gen_merge_warp_kernel<FMHA_F16> : fmha_gen_merge_warp_kernel<FMHA_E4M3>);
     // launched as a programmatic dependent of the attention kernel, so its
     // launch and prologue overlap that kernel's tail
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(rows);
-    cfg.blockDim = dim3(kMergeThreads);
+    // rows per CTA (one warp each): as many as keep two CTAs per SM busy, at most eight
+    const int rpc = rows / (2 * sms) < 1 ? 1 : rows / (2 * sms) > kMergeRowsMax ? kMergeRowsMax : rows / (2 * sms);
+    cfg.gridDim = many ? dim3(rows) : dim3((rows + rpc - 1) / rpc);
+    cfg.blockDim = many ? dim3(kMergeThreads) : dim3(32 * rpc);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
