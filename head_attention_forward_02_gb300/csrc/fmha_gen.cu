@@ -15,8 +15,9 @@
 // The work is memory bound: every cached K/V byte is read once, and a group of
 // G <= 32 query heads does 4 * G flops per cached element pair.  The design
 // therefore aims at HBM bandwidth: the key range of every (sequence, kv head)
-// is cut into chunks so that all SMs stream at once, each CTA keeps three
-// K/V stages (64 KB, or 32 KB for e4m3) in flight through TMA, and the
+// is cut into chunks so that all SMs stream at once, each CTA keeps a ring of
+// K/V stages in flight through TMA (three 64 KB stages for 16-bit types, six
+// 32 KB stages for e4m3), and the
 // contraction runs on the tensor cores with the roles swapped so that the
 // small head group is the N dimension:
 // S^T = K Q^T (M = 128 keys, N = 32 padded heads, K = 128) and
