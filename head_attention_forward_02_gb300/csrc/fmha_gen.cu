@@ -16,13 +16,13 @@
 // G <= 32 query heads does 4 * G flops per cached element pair.  The design
 // therefore aims at HBM bandwidth: the key range of every (sequence, kv head)
 // is cut into chunks so that all SMs stream at once, each CTA keeps a ring of
-// K/V stages in flight through TMA (three 64 KB stages for 16-bit types, six
-// 32 KB stages for e4m3), and the
-// contraction runs on the tensor cores with the roles swapped so that the
-// small head group is the N dimension:
+// three 64 KB K/V stages in flight through TMA, and the contraction runs on
+// the tensor cores with the roles swapped so that the small head group is the
+// N dimension: per 128-row tile block,
 // S^T = K Q^T (M = 128 keys, N = 32 padded heads, K = 128) and
-// O^T = V^T P^T (M = 128 = head dim, N = 32, K = 128 keys).  Thread i of the
-// softmax warps owns key i of a tile (TMEM lane i) and, in the epilogue, head
+// O^T += V^T P^T (M = 128 = head dim, N = 32, K = 128 keys); a 16-bit tile is
+// one block, an e4m3 tile two (the same 64 KB).  Thread i of the softmax
+// warps owns row i of every block (TMEM lane i) and, in the epilogue, head
 // dimension i of O^T.  The row maximum is kept lazily per head (rescale only
 // when a score exceeds the reference by 2^8), so the common tile needs no
 // cross-thread reduction; a named-barrier vote finds the rare tile that does.
@@ -44,39 +44,58 @@ __device__ int g_gen_status;   // FMHA_OK, or the first error a generation kerne
 namespace {
 
 constexpr int kD = 128;                 // head dim
-constexpr int kKT = 128;                // rows per tile (MMA M of S^T): keys, or keys x 2 heads
+constexpr int kKT = 128;                // rows per tile block (MMA M of S^T): keys, or keys x 2 heads
 constexpr int kNP = 32;                 // query heads of a group, padded (MMA N)
 constexpr int kNSMax = 6;               // K/V ring stages at most (a K and a V tile each)
 constexpr int kBarBytes = 2048;         // barrier and scratch block
 constexpr int kSoftWarpsMax = 8;        // softmax warps of the widest layout
-constexpr uint32_t kTmemCols = 128;     // S^T buffers in [0, 32) and [32, 64), O^T in [64, 96)
 constexpr int kPanelBytes = kKT * 128;  // 128 rows of one 128-byte swizzled panel
 constexpr int kQPanelBytes = kNP * 128;
 constexpr int kQSlots = 2;                            // Q tiles of consecutive work items
 
 // Sizes and layouts of one element type: 16-bit (f16, bf16) or e4m3.  A 128-dim
-// row is two 128-byte swizzle panels of 64 elements, or one of 128.
-template <int ELEM>
+// row is two 128-byte swizzle panels of 64 elements, or one of 128.  A tile
+// is BLK blocks of 128 rows; each block has its own S^T columns and P^T
+// buffer, and every block's P.V accumulates into the one O^T.  e4m3 tiles
+// have two blocks, so that a tile carries as many bytes (64 KB of K and V)
+// as a 16-bit one and the per-tile hand-offs cost the same per byte.
+template <int ELEM, int BLK_>
 struct GenCfg {
     static constexpr bool FP8 = ELEM == FMHA_E4M3;
+    static constexpr int BLK = BLK_;                      // 128-row blocks per tile
     static constexpr int E = FP8 ? 1 : 2;                 // bytes per element
     static constexpr int PANELS = kD * E / 128;
     static constexpr int BOX = 128 / E;                   // elements per panel row
-    static constexpr int TILE_BYTES = PANELS * kPanelBytes;   // 128 keys x 128 dims
+    static constexpr int BLK_BYTES = PANELS * kPanelBytes;    // one block: 128 rows x 128 dims
+    static constexpr int TILE_BYTES = BLK * BLK_BYTES;        // the K (or V) half of a stage
     static constexpr int Q_BYTES = PANELS * kQPanelBytes;     // 32 heads x 128 dims
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;        // K tile, then V tile
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;        // K blocks, then V blocks
     static constexpr int P_ROW = kNP * E;                 // bytes of one key's P^T row (32 heads)
-    static constexpr int P_BYTES = kKT * P_ROW;           // one of the two P^T buffers
+    static constexpr int P_BYTES = kKT * P_ROW;           // P^T of one block
     static constexpr uint64_t P_SWZ = FP8 ? 6 : 4;        // 32-byte or 64-byte swizzle of P^T
     static constexpr int MMA_K = FP8 ? 32 : 16;           // K of one tcgen05.mma
     static constexpr uint32_t FMT = ELEM == FMHA_BF16 ? 1u : 0u;   // kind::f16: f16 0, bf16 1; f8f6f4: e4m3 0
+    // TMEM: S^T buffers in [0, SCOLS) and [SCOLS, 2 SCOLS) (block i of a
+    // buffer in its columns [32 i, 32 i + 32)), O^T in [2 SCOLS, 2 SCOLS + 32)
+    static constexpr int SCOLS = BLK * kNP;
+    static constexpr int O_COL = 2 * SCOLS;
+    static constexpr uint32_t TMEM_COLS = O_COL + kNP <= 128 ? 128 : 256;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_KV = OFF_Q + kQSlots * Q_BYTES;
-    static constexpr int NS = FP8 ? 6 : 3;                // K/V ring stages
+    static constexpr int NS = STAGE_BYTES >= 65536 ? 3 : 6;   // K/V ring stages: about 192 KB in flight
     static constexpr int OFF_P = OFF_KV + NS * STAGE_BYTES;
-    static constexpr int OFF_BARS = OFF_P + 2 * P_BYTES;
+    static constexpr int OFF_BARS = OFF_P + 2 * BLK * P_BYTES;
     static constexpr int SMEM_BYTES = OFF_BARS + kBarBytes + 1024;   // barriers and scratch, 1 KB alignment
     static_assert(SMEM_BYTES <= 227 * 1024 && NS <= kNSMax, "shared memory budget");
+    static_assert(O_COL + kNP <= (int)TMEM_COLS, "TMEM budget");
+};
+
+// Blocks per tile of an element type and warp layout: two for e4m3, except in
+// the eight-warp layout, whose two column groups of 16 already hold 168
+// registers a thread with one block
+template <int ELEM, int MODE>
+struct GenBlk {
+    static constexpr int value = ELEM == FMHA_E4M3 && MODE != 2 ? 2 : 1;
 };
 constexpr unsigned long long kTimeoutNs = 4000000000ull;
 constexpr unsigned long long kDrainNs = 200000000ull;
@@ -93,7 +112,7 @@ struct GenParams {
     float *part_o, *part_lse;           // [B*H][max_seg][D], [B*H][max_seg]
     int B, H, H_k, G, B_cache, S_max;
     int GP;                             // kv heads per work unit: 2 (adjacent heads together) or 1
-    int TK;                             // keys per tile: 128 / GP (a tile is always 128 rows)
+    int TK;                             // keys per tile: 128 x blocks per tile / GP
     int NU;                             // work units per sequence: H_k / GP
     int max_seg;                        // partial results per (sequence, head): tiles of S_max + 1
     int ncta;                           // CTAs of the attention kernel (the stream-K split)
@@ -356,7 +375,11 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 template <int N>
 __device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]) {
-    if constexpr (N == 8) {
+    if constexpr (N == 4) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]),
+                     "r"(r[1]), "r"(r[2]), "r"(r[3])
+                     : "memory");
+    } else if constexpr (N == 8) {
         asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
                      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                      : "memory");
@@ -423,11 +446,11 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
 // ---------------------------------------------------------------------------
 // Work items: (sequence b, chunk c of its keys, unit u), u fastest.  A unit is
 // one kv head, or two adjacent kv heads (GP = 2) whose query groups together
-// fill at most the 32 columns of S^T: their tiles are 64 keys x 2 heads, row
-// r of a tile being key r / 2 of head r % 2.  One key's rows of two adjacent
-// heads are contiguous in the cache, so every K/V row the tile reads is twice
-// as long; fetched alone, a 128-byte e4m3 row cost about 1.5x its size in
-// DRAM traffic on this part, and a pair of them exactly their size.
+// fill at most the 32 columns of S^T (tile shapes: Unit below).  One key's
+// rows of two adjacent heads are contiguous in the cache and the two heads'
+// loads of a tile go out back to back, so every K/V row the tile reads is
+// twice as long; fetched alone, a 128-byte e4m3 row cost about 1.5x its size
+// in DRAM traffic on this part, and a pair of them exactly their size.
 // ---------------------------------------------------------------------------
 
 // Keys of sequence b: its cached tokens, plus the new one unless cache-only.
@@ -451,11 +474,19 @@ __device__ __forceinline__ int gen_entry(const GenParams &p, int b, bool report)
     return e;
 }
 
-// Shape of a work unit: kv heads and keys of a tile
-template <bool TWO>
+// Shape of a work unit (kv heads) and of its tiles (keys per tile, and which
+// kv head and key row r of block i holds).  One block: a one-head tile is 128
+// keys; a two-head tile is 64 keys x 2 heads, rows 0-63 the first head and
+// 64-127 the second.  Two blocks: a one-head tile is 256 keys, block i keys
+// [128 i, 128 i + 128); a two-head tile is 128 keys, block i the head g + i.
+template <bool TWO_, int BLK_>
 struct Unit {
+    static constexpr bool TWO = TWO_;
+    static constexpr int BLK = BLK_;
     static constexpr int GP = TWO ? 2 : 1;
-    static constexpr int TK = kKT / GP;
+    static constexpr int TK = kKT * BLK / GP;
+    static __device__ __forceinline__ int row_head(int i, int r) { return BLK == 2 ? (TWO ? i : 0) : (TWO ? r >> 6 : 0); }
+    static __device__ __forceinline__ int row_key(int i, int r) { return BLK == 2 ? (TWO ? r : kKT * i + r) : (TWO ? r & 63 : r); }
 };
 
 // Warp layout of a kernel instantiation.
@@ -473,9 +504,9 @@ struct Layout {
     static constexpr int THREADS = (SW + 2) * 32;
 };
 
-template <bool TWO>
-__device__ __forceinline__ int gen_tiles(const GenParams &p, int b) {
-    return (gen_tokens(p, b, false) + p.insert + Unit<TWO>::TK - 1) / Unit<TWO>::TK;
+// Tiles of tk keys covering sequence b's keys
+__device__ __forceinline__ int gen_tiles(const GenParams &p, int b, int tk) {
+    return (gen_tokens(p, b, false) + p.insert + tk - 1) / tk;
 }
 
 // Stream-K split: the tiles of every (sequence b, unit u) pair, in (b, u)
@@ -486,10 +517,10 @@ __device__ __forceinline__ int gen_tiles(const GenParams &p, int b) {
 // s-th CTA that covers the pair, and writes partial slot s.
 
 // One warp: T, this CTA's range, and where its first segment starts.
-template <bool TWO>
+template <class U>
 __device__ void gen_schedule(const GenParams &p, GenSched *sc, int lane) {
     int64_t T = 0;
-    for (int b = lane; b < p.B; b += 32) T += (int64_t)p.NU * gen_tiles<TWO>(p, b);
+    for (int b = lane; b < p.B; b += 32) T += (int64_t)p.NU * gen_tiles(p, b, U::TK);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) T += __shfl_xor_sync(0xffffffffu, T, o);
     const int64_t per = (T + gridDim.x - 1) / gridDim.x;
@@ -498,7 +529,7 @@ __device__ void gen_schedule(const GenParams &p, GenSched *sc, int lane) {
     int64_t off0 = T, base = 0;
     for (int bb = 0; bb < p.B && G0 < G1; bb += 32) {
         const int b = bb + lane;
-        const int64_t n = b < p.B ? (int64_t)p.NU * gen_tiles<TWO>(p, b) : 0;
+        const int64_t n = b < p.B ? (int64_t)p.NU * gen_tiles(p, b, U::TK) : 0;
         int64_t incl = n;                 // inclusive prefix over the 32 sequences
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -534,9 +565,8 @@ struct GenCursor {                      // next pair (b, unit u) and its first t
     int64_t off = 0;
 };
 
-template <bool TWO>
+template <class U>
 __device__ bool gen_next(const GenParams &p, const GenSched &sc, GenCursor &cur, GenItem &it, bool report) {
-    using U = Unit<TWO>;
     if (cur.b < 0) {
         cur.b = sc.b0;
         cur.u = 0;
@@ -544,7 +574,7 @@ __device__ bool gen_next(const GenParams &p, const GenSched &sc, GenCursor &cur,
     }
     for (;;) {
         if (cur.b >= p.B || cur.off >= sc.G1) return false;
-        const int nt = gen_tiles<TWO>(p, cur.b);
+        const int nt = gen_tiles(p, cur.b, U::TK);
         const int64_t end = cur.off + nt;
         const bool hit = nt > 0 && end > sc.G0;
         if (hit) {
@@ -574,11 +604,10 @@ __device__ bool gen_next(const GenParams &p, const GenSched &sc, GenCursor &cur,
 
 // TMA producer: per item, the new token's row into the cache (when this chunk
 // holds it), the 32-head Q tile, then the chunk's K/V tiles into the ring.
-template <int ELEM, bool TWO>
+template <class C, class U>
 __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUtensorMap *tmQ,
                              const CUtensorMap *tmK, const CUtensorMap *tmV, uint8_t *smem, GenBars *bars) {
-    using C = GenCfg<ELEM>;
-    using U = Unit<TWO>;
+    constexpr bool TWO = U::TWO;
     volatile int *abort_flag = &bars->abort;
     prefetch_tmap(tmQ);
     prefetch_tmap(tmK);
@@ -588,7 +617,7 @@ __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUten
     GenCursor cur;
     while (ok) {
         GenItem it;
-        if (!gen_next<TWO>(p, sc, cur, it, true)) break;
+        if (!gen_next<U>(p, sc, cur, it, true)) break;
         if (p.insert && it.len_ok && it.entry >= 0 && it.L >= it.k0 && it.L < it.k1) {
             // K and V rows of the new token (128 elements per kv head of the
             // unit, contiguous); the async proxy (TMA) reads row L below, so
@@ -637,16 +666,22 @@ __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUten
             mbar_expect_tx(fb, C::STAGE_BYTES);
             const uint32_t dst = smem_u32(smem + C::OFF_KV + st * C::STAGE_BYTES);
             const int e = it.entry >= 0 ? it.entry : p.B_cache;   // out of range: zero fill
-            // rows [64 h2, 64 h2 + 64) of a two-head tile are head g + h2;
-            // the heads' loads go out back to back, so each key's rows of
-            // both heads (adjacent in the cache) are fetched together
+            // one box per block, or, in a one-block two-head tile, one per
+            // head (rows [64 h2, 64 h2 + 64) are head g + h2); the heads' loads
+            // go out back to back, so each key's rows of both heads (adjacent
+            // in the cache) are fetched together
+            constexpr int NBOX = C::BLK == 2 ? 2 : U::GP;
+            constexpr int BOX_ROWS = kKT * C::BLK / NBOX;
 #pragma unroll
-            for (int h2 = 0; h2 < U::GP; ++h2) {
-                const uint32_t ro = (uint32_t)(h2 * U::TK * 128);
+            for (int x = 0; x < NBOX; ++x) {
+                // block x of a two-block tile, or rows [64 x, 64 x + 64) of each panel
+                const uint32_t ro = (uint32_t)(C::BLK == 2 ? x * C::BLK_BYTES : x * BOX_ROWS * 128);
+                const int hx = C::BLK == 2 ? U::row_head(x, 0) : x;
+                const int kx = k + (C::BLK == 2 ? U::row_key(x, 0) : 0);
 #pragma unroll
                 for (int pn = 0; pn < C::PANELS; ++pn) {
-                    tma_load_4d(dst + pn * kPanelBytes + ro, tmK, fb, pn * C::BOX, it.g + h2, k, e);
-                    tma_load_4d(dst + C::TILE_BYTES + pn * kPanelBytes + ro, tmV, fb, pn * C::BOX, it.g + h2, k, e);
+                    tma_load_4d(dst + pn * kPanelBytes + ro, tmK, fb, pn * C::BOX, it.g + hx, kx, e);
+                    tma_load_4d(dst + C::TILE_BYTES + pn * kPanelBytes + ro, tmV, fb, pn * C::BOX, it.g + hx, kx, e);
                 }
             }
             ++fill;
@@ -675,18 +710,18 @@ __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUten
 // per tile, S^T_j = K_j Q^T into buffer j % 2 once the softmax has read S^T_j-2
 // out of it, then O^T += V^T_j-1 P^T_j-1 once the softmax has written P^T_j-1.
 // The last tile of a work item issues its own P.V before the next item starts,
-// so the epilogue never waits for the next item's loads.
-template <int ELEM, bool TWO>
+// so the epilogue never waits for the next item's loads.  A tile of two blocks
+// takes two S^T groups (one per block, into the block's columns of the
+// buffer) and two P.V groups (one per block, both into O^T).
+template <class C, class U>
 __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, GenBars *bars, uint32_t tmem_any) {
-    using C = GenCfg<ELEM>;
-    using U = Unit<TWO>;
     // the whole warp runs this loop converged, with warp-uniform values; one
     // elected lane issues each MMA and commit
     volatile int *abort_flag = &bars->abort;
     const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_any, 0);   // the same in every lane
     constexpr uint32_t kIdS = gen_idesc(C::FMT, false, false);
     constexpr uint32_t kIdPV = gen_idesc(C::FMT, true, true);
-    const uint32_t o_tm = tmem + 2 * kNP;
+    const uint32_t o_tm = tmem + C::O_COL;
     const uint64_t q_desc0 = smem_desc(smem_u32(smem + C::OFF_Q), 16, 1024, 2);
     // P^T: MN-major, one swizzled row of 32 heads per key (64 or 32 bytes)
     const uint64_t p_desc0 = smem_desc(smem_u32(smem + C::OFF_P), C::P_BYTES, 8 * C::P_ROW, C::P_SWZ);
@@ -702,12 +737,16 @@ __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, G
         // stride), B = P^T MN-major (32 heads in one swizzled row per key);
         // each k-step is MMA_K keys
         const uint32_t kaddr = smem_u32(smem + C::OFF_KV + st * C::STAGE_BYTES);
-        const uint64_t v_desc = smem_desc(kaddr + C::TILE_BYTES, kPanelBytes, 1024, 2);
-        const uint64_t p_desc = p_desc0 + ((b * C::P_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kKT / C::MMA_K; ++kk)
-            mma_ss_e<C::FP8>(o_tm, v_desc + ((kk * C::MMA_K * 128) >> 4),
-                             p_desc + ((kk * C::MMA_K * C::P_ROW) >> 4), kIdPV, (!first || kk > 0) ? 1u : 0u);
+        for (int x = 0; x < C::BLK; ++x) {
+            const uint64_t v_desc = smem_desc(kaddr + C::TILE_BYTES + x * C::BLK_BYTES, kPanelBytes, 1024, 2);
+            const uint64_t p_desc = p_desc0 + (((b * C::BLK + x) * C::P_BYTES) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kKT / C::MMA_K; ++kk)
+                mma_ss_e<C::FP8>(o_tm, v_desc + ((kk * C::MMA_K * 128) >> 4),
+                                 p_desc + ((kk * C::MMA_K * C::P_ROW) >> 4), kIdPV,
+                                 (!first || x > 0 || kk > 0) ? 1u : 0u);
+        }
         tc_commit_e(smem_u32(&bars->pv_done[b]));
         tc_commit_e(smem_u32(&bars->kv_empty[st]));
         return true;
@@ -716,7 +755,7 @@ __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, G
     GenCursor cur;
     while (ok) {
         GenItem it;
-        if (!gen_next<TWO>(p, sc, cur, it, false)) break;
+        if (!gen_next<U>(p, sc, cur, it, false)) break;
         const int qs = qn % kQSlots;
         if (!warp_wait(smem_u32(&bars->q_full[qs]), (qn / kQSlots) & 1, abort_flag)) break;
         ++qn;
@@ -736,13 +775,16 @@ __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, G
             // S^T: A = K tile (K-major, 128 keys), B = Q tile (K-major, 32 heads);
             // each k-step (16 dims of 16 bits or 32 of 8) is 32 bytes within a
             // 128-byte panel row
-            const uint64_t k_desc = smem_desc(kaddr, 16, 1024, 2);
 #pragma unroll
-            for (int kk = 0; kk < kD / C::MMA_K; ++kk) {
-                const uint32_t koff = (kk * 32 / 128) * kPanelBytes + (kk * 32) % 128;
-                const uint32_t qoff = (kk * 32 / 128) * kQPanelBytes + (kk * 32) % 128;
-                mma_ss_e<C::FP8>(tmem + b * kNP, k_desc + (koff >> 4), q_desc + (qoff >> 4), kIdS,
-                                 kk > 0 ? 1u : 0u);
+            for (int x = 0; x < C::BLK; ++x) {
+                const uint64_t k_desc = smem_desc(kaddr + x * C::BLK_BYTES, 16, 1024, 2);
+#pragma unroll
+                for (int kk = 0; kk < kD / C::MMA_K; ++kk) {
+                    const uint32_t koff = (kk * 32 / 128) * kPanelBytes + (kk * 32) % 128;
+                    const uint32_t qoff = (kk * 32 / 128) * kQPanelBytes + (kk * 32) % 128;
+                    mma_ss_e<C::FP8>(tmem + b * C::SCOLS + x * kNP, k_desc + (koff >> 4), q_desc + (qoff >> 4), kIdS,
+                                     kk > 0 ? 1u : 0u);
+                }
             }
             if (k + U::TK >= it.k1) tc_commit_e(smem_u32(&bars->q_empty[qs]));
             tc_commit_e(smem_u32(&bars->s_full[b]));
@@ -765,53 +807,63 @@ __device__ void gen_mma(const GenParams &p, const GenSched &sc, uint8_t *smem, G
 }
 
 // Softmax and epilogue.  Softmax warp w owns rows 32 (w % 4) .. + 31 of every
-// tile (its TMEM lanes of S^T) and the same rows of O^T (head dimensions).
-// A tile row is a key of the unit's kv head, or, in a two-head unit (MODE 1),
-// key r % 64 of head r / 64 (warps 0-1: the first head, warps 2-3: the
-// second).
+// tile block (its TMEM lanes of S^T) and the same rows of O^T (head
+// dimensions).  Row r of block i is key U::row_key(i, r) of kv head
+// g + U::row_head(i, r).
 //
 // Columns of S^T are query heads: [0, G) of a one-head unit, or [0, G) and
 // [16, 16 + G) of a two-head unit (its Q tile is two 16-row halves).  A
-// thread works on NC >= G columns from c0 = 16 * (its column group): the
-// warps of a kv head in MODE 1, warps 0-3 and 4-7 in MODE 2 (columns 0-15 and
-// 16-31), all four warps in MODE 0.  Columns of a group past G hold other
-// heads' queries and feed only O^T columns that are never stored.  In a
-// two-head unit a row's weights in the other head's columns are written as
-// 0, so P.V over the 128 rows adds, for each column, only the rows of its
-// own kv head; O^T rows then hold columns of both heads, so the rescale
-// factors and reference maxima of every column go through shared memory.
-template <int ELEM, int NC, int MODE>
+// thread works on NC >= G columns of each block, from the block's first
+// column cb: in a one-block two-head unit (MODE 1) the columns of the row's
+// kv head (warps 0-1 the first head, 2-3 the second: one column group per
+// head); in a two-block two-head unit columns [0, NC) of block 0 (the first
+// head's keys) and [16, 16 + NC) of block 1 (the second's), both in every
+// thread; in MODE 2 warps 0-3 and 4-7 take columns 0-15 and 16-31 (two column
+// groups); in MODE 0 all four warps take columns [0, NC).  Columns of a group
+// past G hold other heads' queries and feed only O^T columns that are never
+// stored.  In a two-head unit a row's weights in the other head's columns are
+// written as 0, so P.V adds, for each column, only the rows of its own kv
+// head.  In a one-block two-head unit an O^T row holds columns of both
+// heads' column groups, so the rescale factors and reference maxima of every
+// column go through shared memory; elsewhere every thread of a group holds
+// the factors of all the columns it rescales.
+template <class C, class U, int NC, int MODE>
 __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *smem, GenBars *bars, uint32_t tmem,
                             int warp, int lane) {
-    using C = GenCfg<ELEM>;
     using L = Layout<MODE>;
-    constexpr bool two = L::TWO;
+    constexpr bool two = U::TWO;
+    constexpr int BLK = C::BLK;
+    constexpr bool SPLIT_HEADS = two && BLK == 1;       // column groups per head, factors through shared memory
+    constexpr int NSET = two && BLK == 2 ? 2 : 1;       // column sets of a thread (one per head of a two-block tile)
     constexpr int ST = L::SW * 32;                      // softmax threads
-    constexpr int NW = MODE == 1 ? 2 : 4;               // warps of a column group
+    constexpr int NW = SPLIT_HEADS ? 2 : 4;             // warps of a column group
     volatile int *abort_flag = &bars->abort;
-    const int r = (warp & 3) * 32 + lane;               // tile row = TMEM lane
+    const int r = (warp & 3) * 32 + lane;               // block row = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t o_tm = lane_base + 2 * kNP;
-    uint8_t *prow0 = smem + C::OFF_P + r * C::P_ROW;     // this row's P^T row in buffer 0
-    const int gi = MODE == 1 ? warp >> 1 : MODE == 2 ? warp >> 2 : 0;   // column group
+    const uint32_t o_tm = lane_base + C::O_COL;
+    uint8_t *prow0 = smem + C::OFF_P + r * C::P_ROW;     // this row's P^T row in buffer 0, block 0
+    const int gi = SPLIT_HEADS ? warp >> 1 : MODE == 2 ? warp >> 2 : 0;   // column group
     const int c0 = 16 * gi;                             // its first column
     const int w0 = gi * NW;                             // its first warp
-    const int key_of_row = two ? r & 63 : r;
+    // first column of set q (and of block q's values) of this thread
+    auto cset = [&](int q) { return NSET == 2 ? 16 * q : c0; };
     // P^T swizzle: 16-byte chunk index ^= (row / 2) % 4 (64-byte rows) or (row / 4) % 2 (32-byte rows)
     const uint32_t swz = C::FP8 ? (r >> 2) & 1 : (r >> 1) & 3;
     uint32_t oph = 0, cons = 0;
     GenCursor cur;
     for (;;) {
         GenItem it;
-        if (!gen_next<two>(p, sc, cur, it, false)) break;
-        float m[NC], l[NC];
+        if (!gen_next<U>(p, sc, cur, it, false)) break;
+        float m[NSET][NC], l[NSET][NC];
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            m[c] = -INFINITY;   // reference max (log2 units) P and O^T are relative to
-            l[c] = 0.f;         // this thread's part of the row sum
-        }
+        for (int q = 0; q < NSET; ++q)
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                m[q][c] = -INFINITY;   // reference max (log2 units) P and O^T are relative to
+                l[q][c] = 0.f;         // this thread's part of the row sum
+            }
         bool ok = true, first = true;
-        for (int k = it.k0; k < it.k1; k += Unit<two>::TK) {
+        for (int k = it.k0; k < it.k1; k += U::TK) {
             // S^T_j and P^T_j use buffer j % 2.  The commit that completes
             // S^T_j also covers P.V_j-2, issued before it by the same thread,
             // so P^T buffer j % 2 is free to rewrite once S^T_j is here.
@@ -824,45 +876,57 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
             tc_fence_after();
             const int st = cons % C::NS;
             const uint32_t j = cons++;
-            uint32_t sr[NC];
-            tmem_ld_n<NC>(lane_base + b * kNP + c0, sr);
-            tmem_wait_ld_n<NC>(sr);
+            uint32_t sr[BLK][NC];
+#pragma unroll
+            for (int i = 0; i < BLK; ++i) tmem_ld_n<NC>(lane_base + b * C::SCOLS + i * kNP + cset(i), sr[i]);
+#pragma unroll
+            for (int i = 0; i < BLK; ++i) tmem_wait_ld_n<NC>(sr[i]);
             tc_fence_before();
             mbar_arrive(smem_u32(&bars->s_free[b]));   // S^T buffer b may take S^T_j+2
-            const bool valid = k + key_of_row < it.k1;
-            float s[NC];
+            float s[BLK][NC];
             bool need = false;
 #pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                s[c] = valid ? __uint_as_float(sr[c]) * p.c : -INFINITY;
-                need |= s[c] > m[c] + kRescaleLog2;
+            for (int i = 0; i < BLK; ++i) {
+                const int q = NSET == 2 ? i : 0;
+                const bool valid = k + U::row_key(i, r) < it.k1;
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    s[i][c] = valid ? __uint_as_float(sr[i][c]) * p.c : -INFINITY;
+                    need |= s[i][c] > m[q][c] + kRescaleLog2;
+                }
             }
             bool rescaled = false;
             if (soft_any<ST>(need)) {
                 // tile maximum of every column over the group's rows
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    float x = s[c];
+                for (int q = 0; q < NSET; ++q)
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-                    if (lane == 0) bars->red[warp][c0 + c] = x;
-                }
-                soft_sync<ST>();
-                float alpha[NC];
+                    for (int c = 0; c < NC; ++c) {
+                        float x = s[q][c];
+                        if constexpr (NSET == 1 && BLK == 2) x = fmaxf(x, s[1][c]);
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    float tmax = fmaxf(bars->red[w0][c0 + c], bars->red[w0 + 1][c0 + c]);
-                    if (NW == 4) tmax = fmaxf(tmax, fmaxf(bars->red[w0 + 2][c0 + c], bars->red[w0 + 3][c0 + c]));
-                    alpha[c] = 1.f;
-                    if (tmax > m[c] + kRescaleLog2) {
-                        alpha[c] = m[c] == -INFINITY ? 0.f : ex2(m[c] - tmax);
-                        l[c] *= alpha[c];
-                        m[c] = tmax;
+                        for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+                        if (lane == 0) bars->red[warp][cset(q) + c] = x;
                     }
-                }
-                if (two && !first && warp == w0 && lane == 0) {
+                soft_sync<ST>();
+                float alpha[NSET][NC];
 #pragma unroll
-                    for (int c = 0; c < NC; ++c) bars->alpha[c0 + c] = alpha[c];
+                for (int q = 0; q < NSET; ++q)
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        const int col = cset(q) + c;
+                        float tmax = fmaxf(bars->red[w0][col], bars->red[w0 + 1][col]);
+                        if (NW == 4) tmax = fmaxf(tmax, fmaxf(bars->red[w0 + 2][col], bars->red[w0 + 3][col]));
+                        alpha[q][c] = 1.f;
+                        if (tmax > m[q][c] + kRescaleLog2) {
+                            alpha[q][c] = m[q][c] == -INFINITY ? 0.f : ex2(m[q][c] - tmax);
+                            l[q][c] *= alpha[q][c];
+                            m[q][c] = tmax;
+                        }
+                    }
+                if (SPLIT_HEADS && !first && warp == w0 && lane == 0) {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) bars->alpha[c0 + c] = alpha[0][c];
                 }
                 soft_sync<ST>();   // the scratch rows may be rewritten after this
                 if (!first) {
@@ -873,7 +937,7 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
                         break;
                     }
                     tc_fence_after();
-                    if constexpr (two) {
+                    if constexpr (SPLIT_HEADS) {
                         // row r of O^T holds both heads' columns
                         uint32_t orr[32];
                         tmem_ld32(o_tm, orr);
@@ -884,66 +948,80 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
                         tmem_st32(o_tm, orr);
                         soft_sync<ST>();   // every thread has read the factors
                     } else {
-                        // this group's columns of row r of O^T
-                        uint32_t orr[NC];
-                        tmem_ld_n<NC>(o_tm + c0, orr);
-                        tmem_wait_ld_n<NC>(orr);
+                        // this thread's columns of row r of O^T
 #pragma unroll
-                        for (int c = 0; c < NC; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha[c]);
-                        tmem_st_n<NC>(o_tm + c0, orr);
+                        for (int q = 0; q < NSET; ++q) {
+                            uint32_t orr[NC];
+                            tmem_ld_n<NC>(o_tm + cset(q), orr);
+                            tmem_wait_ld_n<NC>(orr);
+#pragma unroll
+                            for (int c = 0; c < NC; ++c)
+                                orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha[q][c]);
+                            tmem_st_n<NC>(o_tm + cset(q), orr);
+                        }
                     }
                     rescaled = true;
                 }
             }
-            float pv[NC];
+            float pv[BLK][NC];
 #pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                pv[c] = m[c] == -INFINITY ? 0.f : ex2(s[c] - m[c]);
-                l[c] += pv[c];
-            }
-            // P^T row r: columns [c0, c0 + NC) from pv and, in a two-head
-            // unit, 0 in the other head's columns (the remaining columns feed
-            // only O^T columns that are never stored)
-            uint8_t *prow = prow0 + b * C::P_BYTES;
-            constexpr int VB = NC * C::E;                    // bytes of this thread's values
-            uint32_t w[(VB + 3) / 4];
-            if constexpr (C::FP8) {
+            for (int i = 0; i < BLK; ++i) {
+                const int q = NSET == 2 ? i : 0;
 #pragma unroll
-                for (int i = 0; i < NC / 4; ++i) w[i] = pack4_e4m3(pv[4 * i], pv[4 * i + 1], pv[4 * i + 2], pv[4 * i + 3]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < NC / 2; ++i) w[i] = pack2<ELEM == FMHA_BF16>(pv[2 * i], pv[2 * i + 1]);
-            }
-            const int vo = c0 * C::E;                    // byte offset of the values in the row
-            const int zo = (16 - c0) * C::E;             // the other head's columns
-            if constexpr (VB >= 16) {
-#pragma unroll
-                for (int c = 0; c < VB / 16; ++c) {
-                    *reinterpret_cast<uint4 *>(prow + ((((vo >> 4) + c) ^ swz) << 4)) =
-                        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-                    if (two)
-                        *reinterpret_cast<uint4 *>(prow + ((((zo >> 4) + c) ^ swz) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                for (int c = 0; c < NC; ++c) {
+                    pv[i][c] = m[q][c] == -INFINITY ? 0.f : ex2(s[i][c] - m[q][c]);
+                    l[q][c] += pv[i][c];
                 }
-            } else if constexpr (VB == 8) {
-                *reinterpret_cast<uint2 *>(prow + ((((vo >> 4) ^ swz) << 4) | (vo & 15))) = make_uint2(w[0], w[1]);
-                if (two) *reinterpret_cast<uint2 *>(prow + ((((zo >> 4) ^ swz) << 4) | (zo & 15))) = make_uint2(0u, 0u);
-            } else {
-                static_assert(VB == 4, "P^T values of a thread");
-                *reinterpret_cast<uint32_t *>(prow + ((((vo >> 4) ^ swz) << 4) | (vo & 15))) = w[0];
-                if (two) *reinterpret_cast<uint32_t *>(prow + ((((zo >> 4) ^ swz) << 4) | (zo & 15))) = 0u;
             }
-            if (!valid && (MODE != 2 || gi == 0)) {
-                // a row whose key is past the chunk's end: its V row (stale
-                // cache contents, possibly not finite) is zeroed so that P = 0
-                // contributes 0 (by one column group of the row)
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                uint8_t *vrow = smem + C::OFF_KV + st * C::STAGE_BYTES + C::TILE_BYTES + r * 128;
 #pragma unroll
-                for (int pn = 0; pn < C::PANELS; ++pn)
+            for (int i = 0; i < BLK; ++i) {
+                // P^T row r of block i: columns [cb, cb + NC) from pv and, in
+                // a two-head unit, 0 in the other head's columns (the
+                // remaining columns feed only O^T columns that are never
+                // stored)
+                uint8_t *prow = prow0 + (b * BLK + i) * C::P_BYTES;
+                constexpr int VB = NC * C::E;                    // bytes of this thread's values
+                uint32_t w[(VB + 3) / 4];
+                if constexpr (C::FP8) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4 *>(vrow + pn * kPanelBytes + ((c ^ (r & 7)) << 4)) =
-                            make_uint4(0u, 0u, 0u, 0u);
+                    for (int x = 0; x < NC / 4; ++x)
+                        w[x] = pack4_e4m3(pv[i][4 * x], pv[i][4 * x + 1], pv[i][4 * x + 2], pv[i][4 * x + 3]);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < NC / 2; ++x) w[x] = pack2<C::FMT == 1u>(pv[i][2 * x], pv[i][2 * x + 1]);
+                }
+                const int cb = cset(NSET == 2 ? i : 0);
+                const int vo = cb * C::E;                    // byte offset of the values in the row
+                const int zo = (16 - cb) * C::E;             // the other head's columns
+                if constexpr (VB >= 16) {
+#pragma unroll
+                    for (int c = 0; c < VB / 16; ++c) {
+                        *reinterpret_cast<uint4 *>(prow + ((((vo >> 4) + c) ^ swz) << 4)) =
+                            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                        if (two)
+                            *reinterpret_cast<uint4 *>(prow + ((((zo >> 4) + c) ^ swz) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                } else if constexpr (VB == 8) {
+                    *reinterpret_cast<uint2 *>(prow + ((((vo >> 4) ^ swz) << 4) | (vo & 15))) = make_uint2(w[0], w[1]);
+                    if (two) *reinterpret_cast<uint2 *>(prow + ((((zo >> 4) ^ swz) << 4) | (zo & 15))) = make_uint2(0u, 0u);
+                } else {
+                    static_assert(VB == 4, "P^T values of a thread");
+                    *reinterpret_cast<uint32_t *>(prow + ((((vo >> 4) ^ swz) << 4) | (vo & 15))) = w[0];
+                    if (two) *reinterpret_cast<uint32_t *>(prow + ((((zo >> 4) ^ swz) << 4) | (zo & 15))) = 0u;
+                }
+                if (k + U::row_key(i, r) >= it.k1 && (MODE != 2 || gi == 0)) {
+                    // a row whose key is past the chunk's end: its V row (stale
+                    // cache contents, possibly not finite) is zeroed so that P = 0
+                    // contributes 0 (by one column group of the row)
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    uint8_t *vrow = smem + C::OFF_KV + st * C::STAGE_BYTES + C::TILE_BYTES + i * C::BLK_BYTES + r * 128;
+#pragma unroll
+                    for (int pn = 0; pn < C::PANELS; ++pn)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4 *>(vrow + pn * kPanelBytes + ((c ^ (r & 7)) << 4)) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                }
             }
             // generic-proxy writes (P^T, zeroed V rows) become visible to the
             // tensor core; TMEM stores complete; then publish
@@ -963,19 +1041,21 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
         if (!soft_all<ST>(got)) break;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            float x = l[c];
+        for (int q = 0; q < NSET; ++q)
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-            if (lane == 0) bars->red[warp][c0 + c] = x;
-        }
-        if (two && warp == w0 && lane == 0) {
+            for (int c = 0; c < NC; ++c) {
+                float x = l[q][c];
 #pragma unroll
-            for (int c = 0; c < NC; ++c) bars->mref[c0 + c] = m[c];
+                for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                if (lane == 0) bars->red[warp][cset(q) + c] = x;
+            }
+        if (SPLIT_HEADS && warp == w0 && lane == 0) {
+#pragma unroll
+            for (int c = 0; c < NC; ++c) bars->mref[c0 + c] = m[0][c];
         }
         soft_sync<ST>();
         const int64_t row0 = (int64_t)it.b * p.H + (int64_t)it.g * p.G;
-        if constexpr (two) {
+        if constexpr (SPLIT_HEADS) {
             // row r of O^T: column h is query head row0 + G * (h / 16) + h % 16
             uint32_t orr[32];
             tmem_ld32(o_tm, orr);
@@ -991,18 +1071,39 @@ __device__ void gen_softmax(const GenParams &p, const GenSched &sc, uint8_t *sme
                 }
             }
         } else {
-            // this group's columns of row r of O^T: query heads row0 + c0 + c
-            uint32_t orr[NC];
-            tmem_ld_n<NC>(o_tm + c0, orr);
-            tmem_wait_ld_n<NC>(orr);
+            // this thread's columns of row r of O^T
+            if constexpr (NSET == 1) {
+                // column c0 + c is query head row0 + c0 + c
+                uint32_t orr[NC];
+                tmem_ld_n<NC>(o_tm + c0, orr);
+                tmem_wait_ld_n<NC>(orr);
 #pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                if (c0 + c < p.G) {
-                    const float lt = (bars->red[w0][c0 + c] + bars->red[w0 + 1][c0 + c]) +
-                                     (bars->red[w0 + 2][c0 + c] + bars->red[w0 + 3][c0 + c]);
-                    const int64_t slot = (row0 + c0 + c) * p.max_seg + it.seg;
-                    p.part_o[slot * kD + r] = lt > 0.f ? __uint_as_float(orr[c]) / lt : 0.f;
-                    if (r == c) p.part_lse[slot] = lt > 0.f ? (m[c] + log2f(lt)) * kLn2 : -INFINITY;
+                for (int c = 0; c < NC; ++c) {
+                    if (c0 + c < p.G) {
+                        const float lt = (bars->red[w0][c0 + c] + bars->red[w0 + 1][c0 + c]) +
+                                         (bars->red[w0 + 2][c0 + c] + bars->red[w0 + 3][c0 + c]);
+                        const int64_t slot = (row0 + c0 + c) * p.max_seg + it.seg;
+                        p.part_o[slot * kD + r] = lt > 0.f ? __uint_as_float(orr[c]) / lt : 0.f;
+                        if (r == c) p.part_lse[slot] = lt > 0.f ? (m[0][c] + log2f(lt)) * kLn2 : -INFINITY;
+                    }
+                }
+            } else {
+                // column 16 q + c is query head row0 + q * G + c (all four warps)
+#pragma unroll
+                for (int q = 0; q < NSET; ++q) {
+                    uint32_t orr[NC];
+                    tmem_ld_n<NC>(o_tm + 16 * q, orr);
+                    tmem_wait_ld_n<NC>(orr);
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        const int col = 16 * q + c;
+                        if (c < p.G) {
+                            const float lt = (bars->red[0][col] + bars->red[1][col]) + (bars->red[2][col] + bars->red[3][col]);
+                            const int64_t slot = (row0 + q * p.G + c) * p.max_seg + it.seg;
+                            p.part_o[slot * kD + r] = lt > 0.f ? __uint_as_float(orr[c]) / lt : 0.f;
+                            if (r == col) p.part_lse[slot] = lt > 0.f ? (m[q][c] + log2f(lt)) * kLn2 : -INFINITY;
+                        }
+                    }
                 }
             }
         }
@@ -1015,9 +1116,11 @@ __global__ void __launch_bounds__(Layout<MODE>::THREADS, 1)
     fmha_gen_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const GenParams p) {
     using L = Layout<MODE>;
+    using C = GenCfg<ELEM, GenBlk<ELEM, MODE>::value>;
+    using U = Unit<L::TWO, C::BLK>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    GenBars *bars = reinterpret_cast<GenBars *>(smem + GenCfg<ELEM>::OFF_BARS);
+    GenBars *bars = reinterpret_cast<GenBars *>(smem + C::OFF_BARS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kQSlots; ++i) {
@@ -1041,10 +1144,10 @@ __global__ void __launch_bounds__(Layout<MODE>::THREADS, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == L::MMA) {
-        tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+        tmem_alloc(smem_u32(&bars->tmem_base), C::TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp == L::PROD) gen_schedule<L::TWO>(p, &bars->sched, lane);
+    if (warp == L::PROD) gen_schedule<U>(p, &bars->sched, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1054,18 +1157,18 @@ __global__ void __launch_bounds__(Layout<MODE>::THREADS, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const GenSched sc = bars->sched;
     if (warp < L::SW) {
-        gen_softmax<ELEM, NC, MODE>(p, sc, smem, bars, tmem, warp, lane);
+        gen_softmax<C, U, NC, MODE>(p, sc, smem, bars, tmem, warp, lane);
     } else if (warp == L::PROD) {
-        if (lane == 0) gen_producer<ELEM, L::TWO>(p, sc, &tmQ, &tmK, &tmV, smem, bars);
+        if (lane == 0) gen_producer<C, U>(p, sc, &tmQ, &tmK, &tmV, smem, bars);
     } else {
-        gen_mma<ELEM, L::TWO>(p, sc, smem, bars, tmem);
+        gen_mma<C, U>(p, sc, smem, bars, tmem);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == L::MMA) {
         __syncwarp();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, C::TMEM_COLS);
     }
 }
 
@@ -1089,7 +1192,7 @@ __global__ void __launch_bounds__(kMergeThreads) fmha_gen_merge_block_kernel(con
     // the attention kernel's split: total tiles, and the tiles before sequence b
     long long tot = 0, pre = 0;
     for (int bb = threadIdx.x; bb < p.B; bb += kMergeThreads) {
-        const long long n = (long long)p.NU * (p.GP == 2 ? gen_tiles<true>(p, bb) : gen_tiles<false>(p, bb));
+        const long long n = (long long)p.NU * gen_tiles(p, bb, p.TK);
         tot += n;
         if (bb < b) pre += n;
     }
@@ -1110,7 +1213,7 @@ __global__ void __launch_bounds__(kMergeThreads) fmha_gen_merge_block_kernel(con
         tot += red_t[i];
         pre += red_p[i];
     }
-    const int nt = p.GP == 2 ? gen_tiles<true>(p, b) : gen_tiles<false>(p, b);
+    const int nt = gen_tiles(p, b, p.TK);
     int nch = 0;                       // CTAs that covered this pair = its partial slots
     if (nt > 0) {
         const long long per = (tot + p.ncta - 1) / p.ncta;
@@ -1175,8 +1278,8 @@ __global__ void __launch_bounds__(kMergeThreads) fmha_gen_merge_block_kernel(con
 // keeps at least two CTAs per SM): O = out_scale *
 // sum_c w_c O_c / sum_c w_c with w_c = exp(LSE_c - max LSE), LSE = max +
 // ln sum_c w_c.  Lane l holds dims 4l .. 4l + 3; no shared memory and no
-// block barrier, so after the wait each row is two dependent loads (the
-// chunks' LSE, then their partial rows) and a store.
+// block barrier, so after the wait a row of at most eight chunks is one round
+// of loads (its chunks' LSEs and partial rows together) and a store.
 constexpr int kMergeRowsMax = 8;
 
 template <int ELEM>
@@ -1188,7 +1291,7 @@ __global__ void __launch_bounds__(32 * kMergeRowsMax) fmha_gen_merge_warp_kernel
     // the attention kernel's split: total tiles, and the tiles before sequence b
     long long tot = 0, pre = 0;
     for (int bb = lane; bb < p.B; bb += 32) {
-        const long long n = (long long)p.NU * (p.GP == 2 ? gen_tiles<true>(p, bb) : gen_tiles<false>(p, bb));
+        const long long n = (long long)p.NU * gen_tiles(p, bb, p.TK);
         tot += n;
         if (bb < b) pre += n;
     }
@@ -1197,7 +1300,7 @@ __global__ void __launch_bounds__(32 * kMergeRowsMax) fmha_gen_merge_warp_kernel
         tot += __shfl_xor_sync(0xffffffffu, tot, o);
         pre += __shfl_xor_sync(0xffffffffu, pre, o);
     }
-    const int nt = p.GP == 2 ? gen_tiles<true>(p, b) : gen_tiles<false>(p, b);
+    const int nt = gen_tiles(p, b, p.TK);
     int nch = 0;                       // CTAs that covered this unit = its partial slots
     if (nt > 0) {
         const long long per = (tot + p.ncta - 1) / p.ncta;
@@ -1209,8 +1312,14 @@ __global__ void __launch_bounds__(32 * kMergeRowsMax) fmha_gen_merge_warp_kernel
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const float *lse_c = p.part_lse + (int64_t)row * p.max_seg;
     const float4 *o_c = reinterpret_cast<const float4 *>(p.part_o + (int64_t)row * p.max_seg * kD) + lane;
-    float mx = -INFINITY;
-    for (int c = lane; c < nch; c += 32) mx = fmaxf(mx, lse_c[c]);
+    // the first 32 chunks' LSEs and the first eight chunks' partial rows go
+    // out together: one memory round trip for a row of at most eight chunks
+    const float lse0 = lane < nch ? lse_c[lane] : -INFINITY;
+    float4 v0[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x) v0[x] = x < nch ? o_c[(int64_t)x * (kD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float mx = lse0;
+    for (int c = 32 + lane; c < nch; c += 32) mx = fmaxf(mx, lse_c[c]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1218,14 +1327,15 @@ __global__ void __launch_bounds__(32 * kMergeRowsMax) fmha_gen_merge_warp_kernel
     if (mx != -INFINITY) {
         for (int c0 = 0; c0 < nch; c0 += 32) {
             // weights of 32 chunks at a time, one per lane, then broadcast
-            const float wl = c0 + lane < nch ? __expf(lse_c[c0 + lane] - mx) : 0.f;
+            const float wl = c0 + lane < nch ? __expf((c0 == 0 ? lse0 : lse_c[c0 + lane]) - mx) : 0.f;
             const int cn = nch - c0 < 32 ? nch - c0 : 32;
             // eight chunks' rows in flight at a time
             for (int c = 0; c < cn; c += 8) {
                 float4 v[8];
 #pragma unroll
                 for (int x = 0; x < 8; ++x)
-                    v[x] = c + x < cn ? o_c[(int64_t)(c0 + c + x) * (kD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[x] = c0 + c == 0 ? v0[x]
+                                       : c + x < cn ? o_c[(int64_t)(c0 + c + x) * (kD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int x = 0; x < 8; ++x) {
                     const float w = __shfl_sync(0xffffffffu, wl, (c + x) & 31);
@@ -1326,6 +1436,26 @@ GenKernel gen_kernel_for(int dt, int nc, int mode) {
 // group fits a 16-column half of S^T.
 bool gen_pairs(int H, int H_k) { return H_k % 2 == 0 && 2 * (H / H_k) <= kNP; }
 
+// Tile blocks and shared memory of the kernel for an element type and warp layout
+template <int ELEM>
+int gen_blocks_t(int mode) {
+    return mode == 1 ? GenBlk<ELEM, 1>::value : mode == 2 ? GenBlk<ELEM, 2>::value : GenBlk<ELEM, 0>::value;
+}
+int gen_blocks(int dt, int mode) {
+    return dt == FMHA_BF16 ? gen_blocks_t<FMHA_BF16>(mode)
+           : dt == FMHA_F16 ? gen_blocks_t<FMHA_F16>(mode) : gen_blocks_t<FMHA_E4M3>(mode);
+}
+template <int ELEM>
+int gen_smem_t(int mode) {
+    return mode == 1   ? GenCfg<ELEM, GenBlk<ELEM, 1>::value>::SMEM_BYTES
+           : mode == 2 ? GenCfg<ELEM, GenBlk<ELEM, 2>::value>::SMEM_BYTES
+                       : GenCfg<ELEM, GenBlk<ELEM, 0>::value>::SMEM_BYTES;
+}
+int gen_smem_bytes(int dt, int mode) {
+    return dt == FMHA_BF16 ? gen_smem_t<FMHA_BF16>(mode)
+           : dt == FMHA_F16 ? gen_smem_t<FMHA_F16>(mode) : gen_smem_t<FMHA_E4M3>(mode);
+}
+
 // Partial slots per (sequence, head): a unit of n tiles meets at most n + 1
 // CTAs' ranges, and n <= ceil(S_max / keys per tile).
 GenLayout gen_layout(int B, int H, int H_k, int S_max) {
@@ -1392,7 +1522,13 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
     p.H_k = H_k;
     p.G = H / H_k;
     p.GP = gen_pairs(H, H_k) ? 2 : 1;
-    p.TK = kKT / p.GP;
+    // warp layout, and the columns of S^T a softmax thread works on (the
+    // query group rounded up; 16 per column group for groups wider than 16)
+    const int G = H / H_k;
+    const int mode = p.GP == 2 ? 1 : G > 16 ? 2 : 0;
+    const int nc = mode == 1 && G <= 4 ? 4 : G <= 8 ? 8 : 16;
+    const int blk = gen_blocks(dt, mode);
+    p.TK = kKT * blk / p.GP;
     p.NU = H_k / p.GP;
     p.B_cache = B_cache;
     p.S_max = S_max;
@@ -1425,12 +1561,13 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
             return FMHA_ERR_CUDA;
     }
     for (int kv = 0; kv < 2; ++kv) {
-        // cache as [B_cache, S_max, H_k, 128]: a box of TK tokens of one head
-        // x one panel
+        // cache as [B_cache, S_max, H_k, 128]: a box of the tokens of one
+        // head in one tile block (128; 64 in a one-block two-head tile) x
+        // one panel
         cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H_k, (cuuint64_t)S_max, (cuuint64_t)B_cache};
         cuuint64_t strides[3] = {(cuuint64_t)kD * esz, (cuuint64_t)kD * esz * H_k,
                                  (cuuint64_t)kD * esz * H_k * S_max};
-        cuuint32_t box[4] = {box_d, 1, (cuuint32_t)p.TK, 1};
+        cuuint32_t box[4] = {box_d, 1, (cuuint32_t)(blk == 2 ? kKT : p.TK), 1};
         cuuint32_t es[4] = {1, 1, 1, 1};
         if (fn(kv ? &tv : &tk, tdt, 4, kv ? v_cache.data : k_cache.data, dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1440,14 +1577,9 @@ extern "C" int fmha_gen_fwd(fmha_tensor q, fmha_tensor k_cache, fmha_tensor v_ca
 
     // ---- launch: persistent CTAs over the work items, then the merge ----
     const int grid = sms;   // one persistent CTA per SM; each streams 1/grid of the tiles
-    // warp layout, and the columns of S^T a softmax thread works on (the
-    // query group rounded up; 16 per column group for groups wider than 16)
-    const int G = H / H_k;
-    const int mode = p.GP == 2 ? 1 : G > 16 ? 2 : 0;
-    const int nc = mode == 1 && G <= 4 ? 4 : G <= 8 ? 8 : 16;
     const int threads = mode == 2 ? Layout<2>::THREADS : Layout<0>::THREADS;
     auto kern = gen_kernel_for(dt, nc, mode);
-    const int smem_bytes = dt == FMHA_E4M3 ? GenCfg<FMHA_E4M3>::SMEM_BYTES : GenCfg<FMHA_BF16>::SMEM_BYTES;
+    const int smem_bytes = gen_smem_bytes(dt, mode);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
         return FMHA_ERR_CUDA;
     kern<<<grid, threads, smem_bytes, stream>>>(tq, tk, tv, p);

@@ -123,6 +123,11 @@ CASES = [
     ("e4m3", 4, 32, 1, 4, 300, [128, 129, 255, 1], False, None),
     ("e4m3", 3, 16, 16, 3, 4096, [895, 1791, 4095], True, None),
     ("e4m3", 5, 4, 4, 6, 700, [127, 0, 640, 2, 383], True, [5, 0, 2, 1, 3]),
+    # e4m3 tiles of two 128-row blocks: 256 keys of one kv head, or 128 keys of two
+    ("e4m3", 3, 6, 3, 3, 700, [64, 63, 639], True, [2, 0, 1]),          # G = 2, odd H_k
+    ("e4m3", 2, 36, 3, 2, 1100, [257, 1023], True, None),               # G = 12, odd H_k
+    ("e4m3", 3, 16, 2, 3, 900, [255, 256, 899], False, None),           # G = 8, two heads a unit
+    ("e4m3", 2, 40, 2, 2, 400, [65, 399], True, None),                  # G = 20: one block, eight warps
 ]
 
 
