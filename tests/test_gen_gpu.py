@@ -153,6 +153,20 @@ def test_gen_long_caches_and_out_scale(fm, dtype):
     check_cache(c, kc, vc)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_gen_one_long_sequence_among_many(fm, dtype):
+    # 48 two-head units: one warp merges each row; the one long sequence's
+    # rows meet over a hundred chunks (the merge's 32-chunk rounds and its
+    # batches of eight); cache-only, four shared entries
+    B = 48
+    seqlen = [60000] + [1 + (37 * b) % 200 for b in range(1, B)]
+    c = make(dtype, B, 8, 2, 4, 60000, seqlen, False, seed=91, batch_idx=[b % 4 for b in range(B)],
+             nan_tail=False)
+    o, lse, _, _, status = run(fm, c)
+    assert status == 0
+    check(c, o, lse)
+
+
 def abs_v_bound(c):
     """2^-4 times the attention output of |V|: the most that rounding each
     weight to e4m3 (relative error 2^-4 in e4m3's normal range) can move O
