@@ -482,9 +482,12 @@ def time_config(fm, name, dev, kernel, warmup, steps, peaks, peak_src):
         del sets, inputs, flush
     if fm.device_status(reset=True) != 0:
         raise RuntimeError(f"device status reports a timeout ({name})")
+    roof = roofline_of(flops, nbytes, launch_ms, w.dtype, peaks, peak_src)
+    # DRAM bytes of one launch from the committed ncu summary of this kernel
+    # source and workload, as for the headline (None once the kernel changed)
+    roof["traffic"] = profiled_traffic(name)
     rec.update({"launch_ms": round(launch_ms, 5), "steps": steps,
-                "value": round(flops / (launch_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                "roofline": roofline_of(flops, nbytes, launch_ms, w.dtype, peaks, peak_src)})
+                "value": round(flops / (launch_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s", "roofline": roof})
     return rec
 
 
