@@ -491,7 +491,9 @@ struct Unit {
 
 // Warp layout of a kernel instantiation.
 //   MODE 0: one kv head per unit; 4 softmax warps, one column group
-//   MODE 1: two kv heads per unit; 4 softmax warps, a column group per head
+//   MODE 1: two kv heads per unit; 4 softmax warps (one-block tiles: a column
+//           group of two warps per head; two-block tiles: every warp takes
+//           both heads, one per block)
 //   MODE 2: one kv head per unit; 8 softmax warps, two column groups of 16
 //           (query groups wider than 16: the exponentials of a tile are
 //           shared by twice the threads)
