@@ -135,9 +135,17 @@ const char *fmha_status_string(int status) {
     }
 }
 
-int fmha_set_wait_limit_ns(unsigned long long ns) { return fmha::sm103_set_wait_limit(ns); }
+int fmha_set_wait_limit_ns(unsigned long long ns) {
+    const int a = fmha::sm103_set_wait_limit(ns);
+    const int b = fmha::gen_set_wait_limit(ns);
+    return a != FMHA_OK ? a : b;
+}
 
-int fmha_set_test_gate(int on) { return fmha::sm103_set_test_gate(on); }
+int fmha_set_test_gate(int on) {
+    const int a = fmha::sm103_set_test_gate(on);
+    const int b = fmha::gen_set_test_gate(on);
+    return a != FMHA_OK ? a : b;
+}
 
 int fmha_device_status(int reset) {
     const int a = fmha::sm103_read_status(reset);

@@ -40,6 +40,12 @@
 namespace fmha {
 
 __device__ int g_gen_status;   // FMHA_OK, or the first error a generation kernel met
+// the bounded waits' limit (ns); set from the host through fmha_set_wait_limit_ns
+__device__ unsigned long long g_gen_wait_ns = 4000000000ull;
+// test hook (fmha_set_test_gate): when set, the producer first waits for a
+// flag that nothing writes, so that bounded wait runs out before any copy
+__device__ int g_gen_test_gate;
+__device__ int g_gen_test_flag;   // never written
 
 namespace {
 
@@ -97,7 +103,7 @@ template <int ELEM, int MODE>
 struct GenBlk {
     static constexpr int value = ELEM == FMHA_E4M3 && MODE != 2 ? 2 : 1;
 };
-constexpr unsigned long long kTimeoutNs = 4000000000ull;
+constexpr unsigned long long kTimeoutNs = 4000000000ull;   // the default wait limit
 constexpr unsigned long long kDrainNs = 200000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -175,7 +181,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: the phase completes, the CTA aborts, or kTimeoutNs pass (then
+// Bounded wait: the phase completes, the CTA aborts, or g_gen_wait_ns pass (then
 // the timeout is recorded and the abort flag raised).
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
     const unsigned long long t0 = globaltimer();
@@ -183,7 +189,7 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volat
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > kTimeoutNs) {
+            if (globaltimer() - t0 > g_gen_wait_ns) {
                 *abort_flag = 1;
                 atomicExch(&g_gen_status, FMHA_ERR_TIMEOUT);
                 return false;
@@ -616,6 +622,20 @@ __device__ void gen_producer(const GenParams &p, const GenSched &sc, const CUten
     prefetch_tmap(tmV);
     uint32_t fill = 0, qn = 0;
     bool ok = true;
+    if (g_gen_test_gate) {
+        // a flag nothing sets: the wait runs out, records the timeout and
+        // raises the abort flag; no copy has been issued yet
+        const volatile int *flag = &g_gen_test_flag;
+        const unsigned long long t0 = globaltimer();
+        for (uint32_t it = 1; !*flag; ++it) {
+            if ((it & 63) == 0 && (*abort_flag || globaltimer() - t0 > g_gen_wait_ns)) {
+                *abort_flag = 1;
+                atomicExch(&g_gen_status, FMHA_ERR_TIMEOUT);
+                break;
+            }
+        }
+        ok = false;
+    }
     GenCursor cur;
     while (ok) {
         GenItem it;
@@ -1396,6 +1416,24 @@ int gen_sm_count() {
 }
 
 }  // namespace
+
+int gen_set_wait_limit(unsigned long long ns) {
+    const unsigned long long v = ns ? ns : kTimeoutNs;
+    if (cudaMemcpyToSymbol(g_gen_wait_ns, &v, sizeof(v)) != cudaSuccess) {
+        cudaGetLastError();
+        return FMHA_ERR_CUDA;
+    }
+    return FMHA_OK;
+}
+
+int gen_set_test_gate(int on) {
+    const int v = on ? 1 : 0;
+    if (cudaMemcpyToSymbol(g_gen_test_gate, &v, sizeof(v)) != cudaSuccess) {
+        cudaGetLastError();
+        return FMHA_ERR_CUDA;
+    }
+    return FMHA_OK;
+}
 
 int gen_read_status(int reset) {
     int v = 0;

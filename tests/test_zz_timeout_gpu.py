@@ -1,9 +1,10 @@
-"""The forward kernel's failure path on the GPU, without a fault: with the
-bounded waits limited to 1 ms, the producer of every CTA first waits for a
-flag that nothing sets (fmha_set_test_gate), so that wait runs out.  The call
-must report FMHA_ERR_TIMEOUT through fmha_device_status, stop every role, free
-its tensor memory and leave the context usable: with the gate off and the
-default limit back, the same call then matches the oracle."""
+"""The failure path of the forward and generation kernels on the GPU, without
+a fault: with the bounded waits limited to 1 ms, the producer of every CTA
+first waits for a flag that nothing sets (fmha_set_test_gate), so that wait
+runs out.  The call must report FMHA_ERR_TIMEOUT through fmha_device_status,
+stop every role, free its tensor memory and leave the context usable: with
+the gate off and the default limit back, the same call then matches the
+oracle."""
 import numpy as np
 import pytest
 import torch
@@ -44,3 +45,25 @@ def test_expired_wait_is_reported_and_the_context_stays_usable(fm, oracle, dtype
     # rows of every (b, h), spread over the sequence
     rows = np.concatenate([bh * w.Sq + np.arange(0, w.Sq, 61) for bh in range(w.B * w.H)])
     compare(again, oracle, rows)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_generation_expired_wait_is_reported_and_the_context_stays_usable(fm, dtype):
+    """The same for fmha_gen_fwd: its attention CTAs stop, the merge runs on
+    undefined partials, the status reads FMHA_ERR_TIMEOUT, and the next call
+    (gate off, default limit) matches the oracle."""
+    from tests import test_gen_gpu as tg
+    c = tg.make(dtype, 8, 32, 8, 8, 2048, [2047, 1000, 1, 0, 517, 1999, 64, 1500], False, seed=13,
+                nan_tail=False)
+    assert fm.device_status(reset=True) == 0
+    assert fm.set_wait_limit_ns(1_000_000) == 0
+    assert fm.set_test_gate(True) == 0
+    try:
+        _, _, _, _, status = tg.run(fm, c)
+    finally:
+        assert fm.set_test_gate(False) == 0
+        assert fm.set_wait_limit_ns(0) == 0
+    assert status == fm.ERR_TIMEOUT
+    o, lse, _, _, status = tg.run(fm, c)
+    assert status == 0
+    tg.check(c, o, lse)
