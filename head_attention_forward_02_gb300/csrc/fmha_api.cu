@@ -10,6 +10,8 @@
 
 namespace fmha {
 int gen_read_status(int reset);   // fmha_gen.cu: the generation kernels' status word
+int gen_set_wait_limit(unsigned long long ns);   // fmha_gen.cu: its wait limit (0: 4 s)
+int gen_set_test_gate(int on);                   // fmha_gen.cu: its producer test gate
 int bwd_read_status(int reset);   // fmha_bwd.cu: the backward kernels' status word
 }
 

@@ -83,7 +83,5 @@ int launch_combine(const Params &p, cudaStream_t stream);
 int sm103_read_status(int reset);
 int sm103_set_wait_limit(unsigned long long ns);   // 0: the default (4 s)
 int sm103_set_test_gate(int on);
-int gen_set_wait_limit(unsigned long long ns);     // the same hooks for fmha_gen_fwd
-int gen_set_test_gate(int on);
 
 }  // namespace fmha
