@@ -13,6 +13,8 @@ int gen_read_status(int reset);   // fmha_gen.cu: the generation kernels' status
 int gen_set_wait_limit(unsigned long long ns);   // fmha_gen.cu: its wait limit (0: 4 s)
 int gen_set_test_gate(int on);                   // fmha_gen.cu: its producer test gate
 int bwd_read_status(int reset);   // fmha_bwd.cu: the backward kernels' status word
+int bwd_set_wait_limit(unsigned long long ns);   // fmha_bwd.cu: its wait limit (0: 4 s)
+int bwd_set_test_gate(int on);                   // fmha_bwd.cu: its producer test gate
 }
 
 namespace fmha {
@@ -140,13 +142,15 @@ const char *fmha_status_string(int status) {
 int fmha_set_wait_limit_ns(unsigned long long ns) {
     const int a = fmha::sm103_set_wait_limit(ns);
     const int b = fmha::gen_set_wait_limit(ns);
-    return a != FMHA_OK ? a : b;
+    const int c = fmha::bwd_set_wait_limit(ns);
+    return a != FMHA_OK ? a : b != FMHA_OK ? b : c;
 }
 
 int fmha_set_test_gate(int on) {
     const int a = fmha::sm103_set_test_gate(on);
     const int b = fmha::gen_set_test_gate(on);
-    return a != FMHA_OK ? a : b;
+    const int c = fmha::bwd_set_test_gate(on);
+    return a != FMHA_OK ? a : b != FMHA_OK ? b : c;
 }
 
 int fmha_device_status(int reset) {

@@ -39,6 +39,12 @@
 namespace fmha {
 
 __device__ int g_bwd_status;   // FMHA_OK, or FMHA_ERR_TIMEOUT after a bounded wait expired
+// the bounded waits' limit (ns); set from the host through fmha_set_wait_limit_ns
+__device__ unsigned long long g_bwd_wait_ns = 4000000000ull;
+// test hook (fmha_set_test_gate): when set, the producer warp first waits for
+// a flag that nothing writes, so that bounded wait runs out before any copy
+__device__ int g_bwd_test_gate;
+__device__ int g_bwd_test_flag;   // never written
 
 namespace {
 
@@ -50,7 +56,7 @@ constexpr int kMmaWarp2 = 10;           // dK/dV kernel: issuer of query half b
 constexpr int kThreads = 352;
 static_assert(kThreads == 32 * (kMmaWarp2 + 1), "one warp per role");
 constexpr uint32_t kTmemCols = 512;
-constexpr unsigned long long kTimeoutNs = 4000000000ull;
+constexpr unsigned long long kTimeoutNs = 4000000000ull;   // the default wait limit
 constexpr unsigned long long kDrainNs = 200000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -167,7 +173,7 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volat
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > kTimeoutNs) {
+            if (globaltimer() - t0 > g_bwd_wait_ns) {
                 *abort_flag = 1;
                 atomicExch(&g_bwd_status, FMHA_ERR_TIMEOUT);
                 return false;
@@ -176,7 +182,7 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volat
     }
 }
 
-// Bounded wait: the phase completes, the CTA aborts, or kTimeoutNs pass.
+// Bounded wait: the phase completes, the CTA aborts, or g_bwd_wait_ns pass.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     return mbar_wait_slow(bar, parity, abort_flag);
@@ -453,6 +459,20 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
     constexpr int KS = C::KSLOTS;
     uint32_t kfill = 0, vfill = 0, hfill = 0, owned = 0;   // loads issued into each ring
     bool ok = true;
+    if (g_bwd_test_gate) {
+        // a flag nothing sets: the wait runs out, records the timeout and
+        // raises the abort flag; no copy has been issued yet
+        const volatile int *flag = &g_bwd_test_flag;
+        const unsigned long long t0 = globaltimer();
+        for (uint32_t it = 1; !*flag; ++it) {
+            if ((it & 63) == 0 && (*abort_flag || globaltimer() - t0 > g_bwd_wait_ns)) {
+                *abort_flag = 1;
+                atomicExch(&g_bwd_status, FMHA_ERR_TIMEOUT);
+                break;
+            }
+        }
+        ok = false;
+    }
     for (int u = blockIdx.x; ok; u += gridDim.x) {
         BUnit U;
         if (!bwd_unit<MODE>(p, u, U)) break;
@@ -1237,6 +1257,24 @@ __global__ void __launch_bounds__(256) widen_e4m3_kernel(const Widen w) {
 }
 
 }  // namespace
+
+int bwd_set_wait_limit(unsigned long long ns) {
+    const unsigned long long v = ns ? ns : kTimeoutNs;
+    if (cudaMemcpyToSymbol(g_bwd_wait_ns, &v, sizeof(v)) != cudaSuccess) {
+        cudaGetLastError();
+        return FMHA_ERR_CUDA;
+    }
+    return FMHA_OK;
+}
+
+int bwd_set_test_gate(int on) {
+    const int v = on ? 1 : 0;
+    if (cudaMemcpyToSymbol(g_bwd_test_gate, &v, sizeof(v)) != cudaSuccess) {
+        cudaGetLastError();
+        return FMHA_ERR_CUDA;
+    }
+    return FMHA_OK;
+}
 
 int bwd_read_status(int reset) {
     int v = 0;

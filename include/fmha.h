@@ -327,21 +327,21 @@ int fmha_device_status(int reset);
 
 /*
  * fmha_set_wait_limit_ns -- test hook for the failure path of fmha_fwd,
- * fmha_fwd_splitkv and fmha_gen_fwd: their bounded on-device waits give up
- * after ns nanoseconds instead of 4 s (ns = 0 restores 4 s).  A wait that expires
- * records FMHA_ERR_TIMEOUT for fmha_device_status and makes the call's CTAs
- * stop issuing work, wait (bounded) for the copies and MMAs they have in
- * flight, free their tensor memory and exit; the outputs of that call are
- * then undefined and the context stays usable.  Applies to launches that
+ * fmha_fwd_splitkv, fmha_gen_fwd and fmha_bwd: their bounded on-device waits
+ * give up after ns nanoseconds instead of 4 s (ns = 0 restores 4 s).  A wait
+ * that expires records FMHA_ERR_TIMEOUT for fmha_device_status and makes the
+ * call's CTAs stop issuing work, wait (bounded) for the copies and MMAs they
+ * have in flight, free their tensor memory and exit; the outputs of that call
+ * are then undefined and the context stays usable.  Applies to launches that
  * start after the call returns.  Returns FMHA_OK or FMHA_ERR_CUDA.
  */
 int fmha_set_wait_limit_ns(unsigned long long ns);
 
 /*
  * fmha_set_test_gate -- test hook: while on (on != 0), the producer warp of
- * every fmha_fwd / fmha_fwd_splitkv CTA and of every fmha_gen_fwd attention
- * CTA first waits for a device flag that nothing sets, so that bounded wait
- * expires after the limit of
+ * every fmha_fwd / fmha_fwd_splitkv CTA, of every fmha_gen_fwd attention CTA
+ * and of every fmha_bwd dQ and dK/dV CTA first waits for a device flag that
+ * nothing sets, so that bounded wait expires after the limit of
  * fmha_set_wait_limit_ns and the launch takes the failure path above before
  * any copy is issued.  Off by default.  Returns FMHA_OK or FMHA_ERR_CUDA.
  */

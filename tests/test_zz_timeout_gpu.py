@@ -1,7 +1,7 @@
-"""The failure path of the forward and generation kernels on the GPU, without
-a fault: with the bounded waits limited to 1 ms, the producer of every CTA
-first waits for a flag that nothing sets (fmha_set_test_gate), so that wait
-runs out.  The call must report FMHA_ERR_TIMEOUT through fmha_device_status,
+"""The failure path of the forward, generation and backward kernels on the
+GPU, without a fault: with the bounded waits limited to 1 ms, the producer of
+every CTA first waits for a flag that nothing sets (fmha_set_test_gate), so
+that wait runs out.  The call must report FMHA_ERR_TIMEOUT through fmha_device_status,
 stop every role, free its tensor memory and leave the context usable: with
 the gate off and the default limit back, the same call then matches the
 oracle."""
@@ -67,3 +67,27 @@ def test_generation_expired_wait_is_reported_and_the_context_stays_usable(fm, dt
     o, lse, _, _, status = tg.run(fm, c)
     assert status == 0
     tg.check(c, o, lse)
+
+
+def test_backward_expired_wait_is_reported_and_the_context_stays_usable(fm):
+    """The same for fmha_bwd: with the gate on, its dQ and dK/dV CTAs stop
+    before any copy and the status reads FMHA_ERR_TIMEOUT; with the gate off
+    the next call's gradients match the oracle."""
+    from tests import test_bwd_gpu as tb
+    g = torch.Generator().manual_seed(17)
+    q, k, v, do = (torch.randn(1, 512, 4, 128, generator=g).to(torch.bfloat16) for _ in range(4))
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fm.fwd(qd, kd, vd, mask="causal")
+    torch.cuda.synchronize()
+    assert fm.device_status(reset=True) == 0
+    assert fm.set_wait_limit_ns(1_000_000) == 0
+    assert fm.set_test_gate(True) == 0
+    try:
+        fm.bwd(qd, kd, vd, o, dod, lse, mask="causal")
+        torch.cuda.synchronize()
+        status = fm.device_status(reset=True)
+    finally:
+        assert fm.set_test_gate(False) == 0
+        assert fm.set_wait_limit_ns(0) == 0
+    assert status == fm.ERR_TIMEOUT
+    tb.run_case(fm, "bf16", 1, 4, 512, 512, 128, "causal", "qbegin", seed=17)
